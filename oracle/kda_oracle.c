@@ -1,0 +1,363 @@
+/*
+ * kda_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, fp64 CPU oracle for Kimi Delta Attention (KDA).  Only the
+ * test suite, the smoke check and the benchmark's CPU-baseline leg may load
+ * it; the CUDA library never calls it and shares no code with it.
+ *
+ * What it computes is the explicit token-by-token recurrence that
+ * "[kimi k3] add eager reference model with FSDP2" (torchtitan PR #4025,
+ * Summary and the "Addresses the review feedback" note) keeps as the
+ * numerical reference for the fused chunk_kda kernel:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * with the three in-kernel prologues that the same note and the
+ * hyper-parallel "KDA context-parallel executors" page (`_run_local_kda`,
+ * flags use_qk_l2norm_in_kernel / use_gate_in_kernel /
+ * use_beta_sigmoid_in_kernel) switch on:
+ *
+ *   - q, k L2-normalised per head:   x / sqrt(|x|^2 + eps), eps = 1e-6
+ *   - beta = sigmoid(beta_raw)
+ *   - the lower-bounded ("safe") gate built from a_log [H], dt_bias [H*K]
+ *     and a negative lower_bound (`_run_local_kda`, `_validate_projected_inputs`):
+ *         g     = lower_bound * sigmoid(exp(a_log_h) * (g_raw + dt_bias_{h,c}))
+ *         alpha = exp(g)
+ *     The pages name these ingredients but never print the formula; this is
+ *     the plainest reading that uses all three and keeps g in (lower_bound, 0).
+ *
+ * Packed documents: nemo_automodel `kimi_k3.cp` ("segment_cu_seqlens",
+ * "doc_ids_from_cu_seqlens"): every [cu[n], cu[n+1]) segment is its own
+ * recurrence, started from initial_state[n] (or zero).
+ *
+ * Backward is reverse mode of the same loop, with the state checkpointed
+ * every 64 tokens and recomputed inside each 64-token block.
+ *
+ * Layouts (token-first, as in `_validate_projected_inputs`):
+ *   q, k, g_raw [TT, H, K]; v, out, dout [TT, H, V]; beta_raw [TT, H];
+ *   a_log [H]; dt_bias [H*K]; states [N, H, K, V].   TT = B*T.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_EPS 1e-6
+#define ORACLE_CKPT 64
+
+static double sigm(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* Segment boundaries: the caller's cu_seqlens, else B rows of T tokens. */
+static int64_t seg_begin(const int32_t* cu, int T, int n) { return cu ? (int64_t)cu[n] : (int64_t)n * T; }
+static int64_t seg_end(const int32_t* cu, int T, int n) { return cu ? (int64_t)cu[n + 1] : (int64_t)(n + 1) * T; }
+
+/* ---- prologue --------------------------------------------------------- */
+
+/* Lower-bounded gate, one element (the reading stated in the header). */
+double oracle_gate_value(double g_raw, double a_log, double dt_bias, double lower_bound)
+{
+    double z = exp(a_log) * (g_raw + dt_bias);
+    return lower_bound * sigm(z);
+}
+
+/* Prologue for one (segment, head): writes q_hat, k_hat [L,K], g [L,K], beta [L]
+ * and the per-token inverse norms rq, rk [L]. */
+static void prologue(int64_t t0, int64_t L, int h, int H, int K,
+                     const double* q, const double* k, const double* g_raw, const double* beta_raw,
+                     const double* a_log, const double* dt_bias, double lb,
+                     double* qh, double* kh, double* g, double* beta, double* rq, double* rk)
+{
+    for (int64_t i = 0; i < L; ++i) {
+        const int64_t row = (t0 + i) * H + h;
+        const double* qi = q + row * K;
+        const double* ki = k + row * K;
+        double sq = 0.0, sk = 0.0;
+        for (int c = 0; c < K; ++c) { sq += qi[c] * qi[c]; sk += ki[c] * ki[c]; }
+        rq[i] = 1.0 / sqrt(sq + ORACLE_EPS);
+        rk[i] = 1.0 / sqrt(sk + ORACLE_EPS);
+        for (int c = 0; c < K; ++c) {
+            qh[i * K + c] = qi[c] * rq[i];
+            kh[i * K + c] = ki[c] * rk[i];
+            g[i * K + c] = oracle_gate_value(g_raw[row * K + c], a_log[h], dt_bias[h * K + c], lb);
+        }
+        beta[i] = sigm(beta_raw[row]);
+    }
+}
+
+/* ---- the recurrence ---------------------------------------------------- */
+
+/* One token of the recurrence, in place on S [K,V]:
+ *   P = Diag(exp(g)) S;  w = P^T k;  S = P + beta k (v - w)^T;  o = scale S^T q. */
+static void step_fwd(int K, int V, double* S, const double* qh, const double* kh, const double* v,
+                     const double* g, double beta, double scale, double* o, double* w)
+{
+    for (int c = 0; c < K; ++c) {
+        const double a = exp(g[c]);
+        for (int j = 0; j < V; ++j) S[c * V + j] *= a;
+    }
+    for (int j = 0; j < V; ++j) w[j] = 0.0;
+    for (int c = 0; c < K; ++c)
+        for (int j = 0; j < V; ++j) w[j] += S[c * V + j] * kh[c];
+    for (int c = 0; c < K; ++c)
+        for (int j = 0; j < V; ++j) S[c * V + j] += beta * kh[c] * (v[j] - w[j]);
+    if (o) {
+        for (int j = 0; j < V; ++j) {
+            double acc = 0.0;
+            for (int c = 0; c < K; ++c) acc += S[c * V + j] * qh[c];
+            o[j] = scale * acc;
+        }
+    }
+}
+
+/* Recurrence with the prologue bypassed (tests inject log-decay g and beta).
+ * Single segment, single head.  qh, kh, g: [L,K]; v, out: [L,V]; beta: [L];
+ * S0, ST: [K,V] (S0 may be NULL = zero state; ST may be NULL). */
+int oracle_recurrence(int64_t L, int K, int V, const double* qh, const double* kh, const double* v,
+                      const double* g, const double* beta, const double* S0, double scale,
+                      double* out, double* ST)
+{
+    double* S = (double*)calloc((size_t)K * V, sizeof(double));
+    double* w = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!S || !w) { free(S); free(w); return 1; }
+    if (S0) memcpy(S, S0, sizeof(double) * (size_t)K * V);
+    for (int64_t t = 0; t < L; ++t)
+        step_fwd(K, V, S, qh + t * K, kh + t * K, v + t * V, g + t * K, beta[t], scale,
+                 out ? out + t * V : NULL, w);
+    if (ST) memcpy(ST, S, sizeof(double) * (size_t)K * V);
+    free(S); free(w);
+    return 0;
+}
+
+/* ---- forward ------------------------------------------------------------ */
+
+int oracle_kda_fwd(int B, int T, int H, int K, int V, int num_seqs, const int32_t* cu_seqlens,
+                   const double* q, const double* k, const double* v, const double* g_raw,
+                   const double* beta_raw, const double* a_log, const double* dt_bias,
+                   double scale, double lower_bound, const double* initial_state,
+                   double* out, double* final_state, int nthreads)
+{
+    const int N = cu_seqlens ? num_seqs : B;
+    const int pairs = N * H;
+    int err = 0;
+    (void)nthreads;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+#endif
+    for (int p = 0; p < pairs; ++p) {
+        const int n = p / H, h = p % H;
+        const int64_t t0 = seg_begin(cu_seqlens, T, n), L = seg_end(cu_seqlens, T, n) - t0;
+        double* qh = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * K);
+        double* kh = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * K);
+        double* g = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * K);
+        double* beta = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        double* rq = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        double* rk = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        double* S = (double*)calloc((size_t)K * V, sizeof(double));
+        double* w = (double*)malloc(sizeof(double) * (size_t)V);
+        double* vv = (double*)malloc(sizeof(double) * (size_t)V);
+        double* o = (double*)malloc(sizeof(double) * (size_t)V);
+        if (!qh || !kh || !g || !beta || !rq || !rk || !S || !w || !vv || !o) {
+            err |= 1;
+        } else {
+            prologue(t0, L, h, H, K, q, k, g_raw, beta_raw, a_log, dt_bias, lower_bound,
+                     qh, kh, g, beta, rq, rk);
+            if (initial_state)
+                memcpy(S, initial_state + ((size_t)n * H + h) * K * V, sizeof(double) * (size_t)K * V);
+            for (int64_t i = 0; i < L; ++i) {
+                const int64_t row = (t0 + i) * H + h;
+                for (int j = 0; j < V; ++j) vv[j] = v[row * V + j];
+                step_fwd(K, V, S, qh + i * K, kh + i * K, vv, g + i * K, beta[i], scale, o, w);
+                for (int j = 0; j < V; ++j) out[row * V + j] = o[j];
+            }
+            if (final_state)
+                memcpy(final_state + ((size_t)n * H + h) * K * V, S, sizeof(double) * (size_t)K * V);
+        }
+        free(qh); free(kh); free(g); free(beta); free(rq); free(rk); free(S); free(w); free(vv); free(o);
+    }
+    return err;
+}
+
+/* ---- backward (reverse mode of the loop above) --------------------------- */
+
+int oracle_kda_bwd(int B, int T, int H, int K, int V, int num_seqs, const int32_t* cu_seqlens,
+                   const double* q, const double* k, const double* v, const double* g_raw,
+                   const double* beta_raw, const double* a_log, const double* dt_bias,
+                   double scale, double lower_bound, const double* initial_state,
+                   const double* dout, const double* dfinal_state,
+                   double* dq, double* dk, double* dv, double* dg_raw, double* dbeta_raw,
+                   double* da_log, double* ddt_bias, double* dinitial_state, int nthreads)
+{
+    const int N = cu_seqlens ? num_seqs : B;
+    const int pairs = N * H;
+    const size_t KV = (size_t)K * V;
+    /* per-pair partial sums of the parameter gradients, reduced in a fixed order */
+    double* pa = (double*)calloc((size_t)pairs, sizeof(double));
+    double* pd = (double*)calloc((size_t)pairs * K, sizeof(double));
+    int err = 0;
+    if (!pa || !pd) { free(pa); free(pd); return 1; }
+    (void)nthreads;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+#endif
+    for (int p = 0; p < pairs; ++p) {
+        const int n = p / H, h = p % H;
+        const int64_t t0 = seg_begin(cu_seqlens, T, n), L = seg_end(cu_seqlens, T, n) - t0;
+        const int64_t Lm = L > 0 ? L : 1;
+        const int64_t ncp = (L + ORACLE_CKPT - 1) / ORACLE_CKPT;
+        double* qh = (double*)malloc(sizeof(double) * (size_t)Lm * K);
+        double* kh = (double*)malloc(sizeof(double) * (size_t)Lm * K);
+        double* g = (double*)malloc(sizeof(double) * (size_t)Lm * K);
+        double* beta = (double*)malloc(sizeof(double) * (size_t)Lm);
+        double* rq = (double*)malloc(sizeof(double) * (size_t)Lm);
+        double* rk = (double*)malloc(sizeof(double) * (size_t)Lm);
+        double* dqh = (double*)calloc((size_t)Lm * K, sizeof(double));
+        double* dkh = (double*)calloc((size_t)Lm * K, sizeof(double));
+        double* dg = (double*)calloc((size_t)Lm * K, sizeof(double));
+        double* dbeta = (double*)calloc((size_t)Lm, sizeof(double));
+        double* ckpt = (double*)malloc(sizeof(double) * (size_t)(ncp > 0 ? ncp : 1) * KV);
+        double* Sb = (double*)malloc(sizeof(double) * (size_t)(ORACLE_CKPT + 1) * KV);
+        double* S = (double*)calloc(KV, sizeof(double));
+        double* dS = (double*)calloc(KV, sizeof(double));
+        double* P = (double*)malloc(sizeof(double) * KV);
+        double* w = (double*)malloc(sizeof(double) * (size_t)V);
+        double* e = (double*)malloc(sizeof(double) * (size_t)V);
+        double* de = (double*)malloc(sizeof(double) * (size_t)V);
+        double* vv = (double*)malloc(sizeof(double) * (size_t)V);
+        if (!qh || !kh || !g || !beta || !rq || !rk || !dqh || !dkh || !dg || !dbeta || !ckpt || !Sb ||
+            !S || !dS || !P || !w || !e || !de || !vv) {
+            err |= 1;
+            goto done;
+        }
+        prologue(t0, L, h, H, K, q, k, g_raw, beta_raw, a_log, dt_bias, lower_bound,
+                 qh, kh, g, beta, rq, rk);
+        if (initial_state) memcpy(S, initial_state + ((size_t)n * H + h) * KV, sizeof(double) * KV);
+        /* forward sweep: remember the state entering every 64-token block */
+        for (int64_t i = 0; i < L; ++i) {
+            if (i % ORACLE_CKPT == 0) memcpy(ckpt + (i / ORACLE_CKPT) * KV, S, sizeof(double) * KV);
+            const int64_t row = (t0 + i) * H + h;
+            for (int j = 0; j < V; ++j) vv[j] = v[row * V + j];
+            step_fwd(K, V, S, qh + i * K, kh + i * K, vv, g + i * K, beta[i], scale, NULL, w);
+        }
+        if (dfinal_state) memcpy(dS, dfinal_state + ((size_t)n * H + h) * KV, sizeof(double) * KV);
+        for (int64_t blk = ncp - 1; blk >= 0; --blk) {
+            const int64_t b0 = blk * ORACLE_CKPT;
+            const int64_t b1 = (b0 + ORACLE_CKPT < L) ? b0 + ORACLE_CKPT : L;
+            /* Sb[i] = state before token b0+i; Sb[b1-b0] = state after the block */
+            memcpy(Sb, ckpt + blk * KV, sizeof(double) * KV);
+            for (int64_t i = b0; i < b1; ++i) {
+                double* cur = Sb + (size_t)(i - b0 + 1) * KV;
+                memcpy(cur, Sb + (size_t)(i - b0) * KV, sizeof(double) * KV);
+                const int64_t row = (t0 + i) * H + h;
+                for (int j = 0; j < V; ++j) vv[j] = v[row * V + j];
+                step_fwd(K, V, cur, qh + i * K, kh + i * K, vv, g + i * K, beta[i], scale, NULL, w);
+            }
+            for (int64_t i = b1 - 1; i >= b0; --i) {
+                const int64_t row = (t0 + i) * H + h;
+                const double* Sprev = Sb + (size_t)(i - b0) * KV;
+                const double* St = Sb + (size_t)(i - b0 + 1) * KV;
+                const double* qi = qh + i * K;
+                const double* ki = kh + i * K;
+                const double* doi = dout + row * V;
+                const double bt = beta[i];
+                /* o = scale S_t^T q */
+                for (int c = 0; c < K; ++c) {
+                    double acc = 0.0;
+                    for (int j = 0; j < V; ++j) {
+                        acc += St[c * V + j] * doi[j];
+                        dS[c * V + j] += scale * qi[c] * doi[j];
+                    }
+                    dqh[i * K + c] += scale * acc;
+                }
+                /* P = Diag(alpha) S_prev, w = P^T k, e = v - w */
+                for (int c = 0; c < K; ++c) {
+                    const double a = exp(g[i * K + c]);
+                    for (int j = 0; j < V; ++j) P[c * V + j] = a * Sprev[c * V + j];
+                }
+                for (int j = 0; j < V; ++j) {
+                    double acc = 0.0;
+                    for (int c = 0; c < K; ++c) acc += P[c * V + j] * ki[c];
+                    e[j] = v[row * V + j] - acc;
+                }
+                /* S_t = P + beta k e^T */
+                double db = 0.0;
+                for (int c = 0; c < K; ++c) {
+                    double acc = 0.0;
+                    for (int j = 0; j < V; ++j) acc += dS[c * V + j] * e[j];
+                    db += ki[c] * acc;
+                    dkh[i * K + c] += bt * acc;
+                }
+                dbeta[i] += db;
+                for (int j = 0; j < V; ++j) {
+                    double acc = 0.0;
+                    for (int c = 0; c < K; ++c) acc += dS[c * V + j] * ki[c];
+                    de[j] = bt * acc;
+                    dv[row * V + j] = de[j];
+                }
+                /* e = v - w, w = P^T k: dP = dS - k de^T, dk -= P de */
+                for (int c = 0; c < K; ++c) {
+                    double acc = 0.0;
+                    for (int j = 0; j < V; ++j) {
+                        acc += P[c * V + j] * de[j];
+                        dS[c * V + j] -= ki[c] * de[j]; /* dS now holds dP */
+                    }
+                    dkh[i * K + c] -= acc;
+                }
+                /* P = Diag(exp(g)) S_prev */
+                for (int c = 0; c < K; ++c) {
+                    const double a = exp(g[i * K + c]);
+                    double acc = 0.0;
+                    for (int j = 0; j < V; ++j) {
+                        acc += dS[c * V + j] * Sprev[c * V + j];
+                        dS[c * V + j] *= a;
+                    }
+                    dg[i * K + c] += a * acc;
+                }
+            }
+        }
+        if (dinitial_state) memcpy(dinitial_state + ((size_t)n * H + h) * KV, dS, sizeof(double) * KV);
+        /* prologue backward */
+        for (int64_t i = 0; i < L; ++i) {
+            const int64_t row = (t0 + i) * H + h;
+            /* x_hat = x r, r = (|x|^2 + eps)^-1/2  ->  dx = r (dy - y (y . dy)) */
+            double sq = 0.0, sk = 0.0;
+            for (int c = 0; c < K; ++c) {
+                sq += qh[i * K + c] * dqh[i * K + c];
+                sk += kh[i * K + c] * dkh[i * K + c];
+            }
+            for (int c = 0; c < K; ++c) {
+                dq[row * K + c] = rq[i] * (dqh[i * K + c] - qh[i * K + c] * sq);
+                dk[row * K + c] = rk[i] * (dkh[i * K + c] - kh[i * K + c] * sk);
+            }
+            dbeta_raw[row] = dbeta[i] * beta[i] * (1.0 - beta[i]);
+            const double ea = exp(a_log[h]);
+            for (int c = 0; c < K; ++c) {
+                const double z = ea * (g_raw[row * K + c] + dt_bias[h * K + c]);
+                const double s = sigm(z);
+                const double dz = dg[i * K + c] * lower_bound * s * (1.0 - s);
+                dg_raw[row * K + c] = dz * ea;
+                pd[(size_t)p * K + c] += dz * ea;
+                pa[p] += dz * z;
+            }
+        }
+    done:
+        free(qh); free(kh); free(g); free(beta); free(rq); free(rk); free(dqh); free(dkh); free(dg);
+        free(dbeta); free(ckpt); free(Sb); free(S); free(dS); free(P); free(w); free(e); free(de); free(vv);
+    }
+    for (int h = 0; h < H; ++h) {
+        double a = 0.0;
+        for (int c = 0; c < K; ++c) ddt_bias[h * K + c] = 0.0;
+        for (int n = 0; n < N; ++n) {
+            a += pa[n * H + h];
+            for (int c = 0; c < K; ++c) ddt_bias[h * K + c] += pd[((size_t)n * H + h) * K + c];
+        }
+        da_log[h] = a;
+    }
+    free(pa); free(pd);
+    return err;
+}

@@ -1,0 +1,297 @@
+"""Pins for the fp64 CPU oracle (no GPU).
+
+The oracle is checked against things other than itself: a hand-derived
+worked example, brute-force products of per-token transfer matrices, closed
+forms (beta = 0, the small-beta limit, causal linear attention), the
+projection identity of the delta rule, invariances of the prologue,
+affinity in the initial state, document isolation, and central finite
+differences for the backward pass.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy.special import expit
+
+import brute
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng0 = np.random.default_rng(1234)
+
+
+def _unit_rows(x):
+    return x / np.linalg.norm(x, axis=-1, keepdims=True)
+
+
+def _tiny(L=5, K=3, V=4, seed=0, beta_scale=1.0):
+    r = np.random.default_rng(seed)
+    qh = _unit_rows(r.standard_normal((L, K)))
+    kh = _unit_rows(r.standard_normal((L, K)))
+    v = r.standard_normal((L, V))
+    g = -r.uniform(0.0, 2.0, (L, K))
+    beta = beta_scale * r.uniform(0.1, 1.0, L)
+    S0 = r.standard_normal((K, V))
+    return qh, kh, v, g, beta, S0
+
+
+# ---------------------------------------------------------------- worked example
+
+def test_worked_example_by_hand():
+    with open(os.path.join(GOLDEN, "recurrence_2x2_by_hand.json")) as f:
+        ex = json.load(f)
+    out, ST = oracle.recurrence(ex["q_hat"], ex["k_hat"], ex["v"], np.log(ex["alpha"]), ex["beta"],
+                                ex["scale"], np.array(ex["S0"]))
+    np.testing.assert_allclose(out, ex["out"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(ST, ex["S_T"], rtol=0, atol=1e-14)
+
+
+# ---------------------------------------------------------------- brute force
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("with_state", [False, True])
+def test_recurrence_matches_unrolled_products(seed, with_state):
+    qh, kh, v, g, beta, S0 = _tiny(L=6, K=4, V=3, seed=seed)
+    S0 = S0 if with_state else None
+    out, ST = oracle.recurrence(qh, kh, v, g, beta, 0.7, S0)
+    ob, Sb = brute.unrolled(qh, kh, v, g, beta, 0.7, S0)
+    np.testing.assert_allclose(out, ob, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(ST, Sb, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(out, brute.attention_form(qh, kh, v, g, beta, 0.7, S0), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- closed forms
+
+def test_beta_zero_is_pure_decay():
+    qh, kh, v, g, beta, S0 = _tiny(L=7, K=4, V=5, seed=3)
+    out, ST = oracle.recurrence(qh, kh, v, g, np.zeros(7), 0.5, S0)
+    G = np.cumsum(g, axis=0)
+    np.testing.assert_allclose(ST, np.exp(G[-1])[:, None] * S0, rtol=1e-13, atol=1e-15)
+    exp_out = 0.5 * (qh * np.exp(G)) @ S0
+    np.testing.assert_allclose(out, exp_out, rtol=1e-13, atol=1e-15)
+    out0, ST0 = oracle.recurrence(qh, kh, v, g, np.zeros(7), 0.5, None)
+    assert np.all(out0 == 0) and np.all(ST0 == 0)
+
+
+def test_small_beta_limit_is_decayed_sum():
+    """beta = eps: S_t / eps -> sum_{s<=t} Diag(exp(Gamma_t - Gamma_s)) k_s v_s^T, error O(eps)."""
+    qh, kh, v, g, _, _ = _tiny(L=6, K=3, V=2, seed=4)
+    G = np.cumsum(g, axis=0)
+    for eps in (1e-4, 1e-6):
+        out, ST = oracle.recurrence(qh, kh, v, g, np.full(6, eps), 1.0, None)
+        Sref = sum(np.exp(G[-1] - G[s])[:, None] * np.outer(kh[s], v[s]) for s in range(6))
+        err = np.abs(ST / eps - Sref).max()
+        assert err < 50 * eps, err
+        for t in range(6):
+            St = sum(np.exp(G[t] - G[s])[:, None] * np.outer(kh[s], v[s]) for s in range(t + 1))
+            assert np.abs(out[t] / eps - St.T @ qh[t]).max() < 50 * eps
+
+
+def test_alpha_one_small_beta_is_causal_linear_attention():
+    qh, kh, v, _, _, _ = _tiny(L=8, K=4, V=3, seed=5)
+    eps = 1e-7
+    out, _ = oracle.recurrence(qh, kh, v, np.zeros((8, 4)), np.full(8, eps), 0.25, None)
+    ref = 0.25 * np.tril(qh @ kh.T) @ v
+    np.testing.assert_allclose(out / eps, ref, rtol=0, atol=1e-5)
+
+
+def test_single_token_textbook_case():
+    r = np.random.default_rng(6)
+    q, k = _unit_rows(r.standard_normal((1, 5))), _unit_rows(r.standard_normal((1, 5)))
+    v = r.standard_normal((1, 3))
+    out, ST = oracle.recurrence(q, k, v, np.zeros((1, 5)), np.ones(1), 0.3, None)
+    np.testing.assert_allclose(out[0], 0.3 * float(q[0] @ k[0]) * v[0], rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(ST, np.outer(k[0], v[0]), rtol=1e-14, atol=1e-15)
+
+
+def test_projection_identity_repeated_token():
+    """alpha = 1, beta = 1, |k| = 1: I - k k^T is a projection, so a repeated token changes nothing."""
+    r = np.random.default_rng(7)
+    k = _unit_rows(r.standard_normal((1, 4)))
+    v = r.standard_normal((1, 3))
+    S0 = r.standard_normal((4, 3))
+    kk, vv = np.repeat(k, 2, 0), np.repeat(v, 2, 0)
+    _, S1 = oracle.recurrence(k, k, v, np.zeros((1, 4)), np.ones(1), 1.0, S0)
+    _, S2 = oracle.recurrence(kk, kk, vv, np.zeros((2, 4)), np.ones(2), 1.0, S0)
+    np.testing.assert_allclose(S2, S1, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(S1.T @ k[0], v[0], rtol=0, atol=1e-13)   # the delta rule writes v exactly
+
+
+# ---------------------------------------------------------------- prologue
+
+def test_gate_limits_and_special_values():
+    lb = -5.0
+    for a, d in [(0.0, 0.0), (math.log(16), 0.1), (1.3, -0.2)]:
+        assert oracle.gate(-d, a, d, lb) == pytest.approx(lb / 2, abs=1e-15)   # sigmoid(0) = 1/2
+        assert oracle.gate(-1e30, a, d, lb) == 0.0                           # alpha = 1 exactly
+        assert oracle.gate(1e30, a, d, lb) == lb
+        for x in rng0.standard_normal(20) * 3:
+            gv = oracle.gate(x, a, d, lb)
+            assert lb <= gv <= 0          # closed in floating point: sigmoid saturates
+            if abs(math.exp(a) * (x + d)) < 30:
+                assert lb < gv < 0
+    # a_log = 0, dt_bias = 0 reduces to lb * logistic(g_raw): scipy's logistic
+    for x in np.linspace(-8, 8, 33):
+        assert oracle.gate(x, 0.0, 0.0, -3.0) == pytest.approx(-3.0 * expit(x), rel=1e-14, abs=1e-300)
+    # monotone decreasing in g_raw, steeper with larger a_log
+    xs = np.linspace(-3, 3, 50)
+    vals = [oracle.gate(x, 1.0, 0.0, lb) for x in xs]
+    assert np.all(np.diff(vals) < 0)
+    assert abs(oracle.gate(0.5, 2.0, 0.0, lb) - lb / 2) > abs(oracle.gate(0.5, 0.0, 0.0, lb) - lb / 2)
+
+
+def _full_inputs(B=1, T=20, H=2, K=4, V=3, seed=0, state=True):
+    r = np.random.default_rng(seed)
+    d = dict(q=r.standard_normal((B, T, H, K)), k=r.standard_normal((B, T, H, K)),
+             v=r.standard_normal((B, T, H, V)), g_raw=r.standard_normal((B, T, H, K)),
+             beta_raw=r.standard_normal((B, T, H)), a_log=r.uniform(0, math.log(16), H),
+             dt_bias=0.1 * r.standard_normal(H * K))
+    S0 = 0.3 * r.standard_normal((B, H, K, V)) if state else None
+    return d, S0
+
+
+def test_prologue_invariances():
+    """q and k are L2-normalised and beta = sigmoid(beta_raw): positive rescaling of q or k leaves
+    the result unchanged; the result is linear in (v, S0); a huge beta logit means beta = 1."""
+    d, S0 = _full_inputs()
+    kw = dict(scale=0.5, lower_bound=-5.0)
+    out, fs = oracle.kda_fwd(**d, initial_state=S0, **kw)
+    d2 = dict(d, q=d["q"] * 3.7, k=d["k"] * 2.5)   # eps / |x|^2 stays ~1e-7
+    out2, fs2 = oracle.kda_fwd(**d2, initial_state=S0, **kw)
+    np.testing.assert_allclose(out2, out, rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(fs2, fs, rtol=1e-5, atol=1e-6)
+    out3, fs3 = oracle.kda_fwd(**dict(d, v=2 * d["v"]), initial_state=2 * S0, **kw)
+    np.testing.assert_allclose(out3, 2 * out, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(fs3, 2 * fs, rtol=1e-12, atol=1e-12)
+    # the full path equals the bare recurrence on normalised inputs with sigmoid(beta) and the gate
+    B, T, H, K = d["q"].shape
+    for h in range(H):
+        qh = d["q"][0, :, h] / np.sqrt((d["q"][0, :, h] ** 2).sum(-1, keepdims=True) + 1e-6)
+        kh = d["k"][0, :, h] / np.sqrt((d["k"][0, :, h] ** 2).sum(-1, keepdims=True) + 1e-6)
+        g = np.array([[oracle.gate(d["g_raw"][0, t, h, c], d["a_log"][h], d["dt_bias"][h * K + c], -5.0)
+                       for c in range(K)] for t in range(T)])
+        o, S = oracle.recurrence(qh, kh, d["v"][0, :, h], g, expit(d["beta_raw"][0, :, h]), 0.5, S0[0, h])
+        np.testing.assert_allclose(out[0, :, h], o, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(fs[0, h], S, rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- state and documents
+
+def test_affine_in_initial_state():
+    d, Sa = _full_inputs(seed=2)
+    _, Sb = _full_inputs(seed=3)
+    kw = dict(scale=0.3, lower_bound=-5.0)
+    f = lambda S: oracle.kda_fwd(**d, initial_state=S, **kw)
+    oab, sab = f(Sa + Sb)
+    ob, sb = f(Sb)
+    oa, sa = f(Sa)
+    o0, s0 = f(None)
+    np.testing.assert_allclose(sab - sb, sa - s0, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(oab - ob, oa - o0, rtol=0, atol=1e-12)
+
+
+def test_document_isolation():
+    lens = [5, 1, 9, 3, 6]
+    T = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    d, _ = _full_inputs(B=1, T=T, H=2, seed=8, state=False)
+    r = np.random.default_rng(9)
+    S0 = r.standard_normal((len(lens), 2, 4, 3))
+    kw = dict(scale=0.4, lower_bound=-5.0)
+    out, fs = oracle.kda_fwd(**d, cu_seqlens=cu, initial_state=S0, **kw)
+    for n in range(len(lens)):
+        sl = slice(cu[n], cu[n + 1])
+        dn = {key: (val[:, sl] if val.ndim >= 3 else val) for key, val in d.items()}
+        on, fn = oracle.kda_fwd(**dn, initial_state=S0[n:n + 1], **kw)
+        np.testing.assert_allclose(out[:, sl], on, rtol=0, atol=1e-14)
+        np.testing.assert_allclose(fs[n], fn[0], rtol=0, atol=1e-14)
+    # perturbing document 2 moves only document 2
+    d2 = {key: val.copy() for key, val in d.items()}
+    d2["v"][:, cu[2]:cu[3]] += 1.0
+    out2, fs2 = oracle.kda_fwd(**d2, cu_seqlens=cu, initial_state=S0, **kw)
+    changed = np.abs(out2 - out).max(axis=(0, 2, 3)) > 0
+    assert np.array_equal(np.nonzero(changed)[0], np.arange(cu[2], cu[3]))
+    assert np.array_equal(np.nonzero(np.abs(fs2 - fs).max(axis=(1, 2, 3)) > 0)[0], [2])
+
+
+def test_empty_segment_passes_state_through():
+    cu = np.array([0, 4, 4, 10])
+    d, _ = _full_inputs(B=1, T=10, H=1, seed=10, state=False)
+    S0 = np.random.default_rng(11).standard_normal((3, 1, 4, 3))
+    out, fs = oracle.kda_fwd(**d, cu_seqlens=cu, initial_state=S0, scale=0.5, lower_bound=-5.0)
+    np.testing.assert_array_equal(fs[1], S0[1])
+
+
+# ---------------------------------------------------------------- backward
+
+def _loss(res_out, res_fs, dout, dfs):
+    return float(np.sum(res_out * dout) + np.sum(res_fs * dfs))
+
+
+@pytest.mark.parametrize("varlen", [False, True])
+def test_backward_matches_central_differences(varlen):
+    if varlen:
+        lens = [3, 5, 2]
+        cu = np.concatenate([[0], np.cumsum(lens)])
+        d, _ = _full_inputs(B=1, T=10, H=2, K=3, V=2, seed=12, state=False)
+        S0 = 0.5 * np.random.default_rng(13).standard_normal((3, 2, 3, 2))
+    else:
+        cu = None
+        d, S0 = _full_inputs(B=2, T=7, H=2, K=3, V=2, seed=14)
+    r = np.random.default_rng(15)
+    dout = r.standard_normal(d["v"].shape)
+    dfs = r.standard_normal(S0.shape)
+    kw = dict(scale=0.6, lower_bound=-4.0, cu_seqlens=cu)
+    grads = oracle.kda_bwd(**d, dout=dout, initial_state=S0, dfinal_state=dfs, **kw)
+
+    def L(dd, S):
+        o, f = oracle.kda_fwd(**dd, initial_state=S, **kw)
+        return _loss(o, f, dout, dfs)
+
+    h = 1e-6
+    names = [("q", "dq"), ("k", "dk"), ("v", "dv"), ("g_raw", "dg_raw"), ("beta_raw", "dbeta_raw"),
+             ("a_log", "da_log"), ("dt_bias", "ddt_bias")]
+    for name, gname in names:
+        x = d[name]
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            num[idx] = (L(dict(d, **{name: xp}), S0) - L(dict(d, **{name: xm}), S0)) / (2 * h)
+        err = np.abs(num - grads[gname]).max() / max(1e-12, np.abs(num).max())
+        assert err < 1e-6, (name, err)
+    num = np.zeros_like(S0)
+    for idx in np.ndindex(*S0.shape):
+        Sp, Sm = S0.copy(), S0.copy()
+        Sp[idx] += h
+        Sm[idx] -= h
+        num[idx] = (L(d, Sp) - L(d, Sm)) / (2 * h)
+    err = np.abs(num - grads["dinitial_state"]).max() / np.abs(num).max()
+    assert err < 1e-6, ("S0", err)
+
+
+def test_backward_long_segment_crosses_checkpoints():
+    """150 tokens cross two 64-token checkpoint blocks of the oracle's reverse sweep."""
+    d, S0 = _full_inputs(B=1, T=150, H=1, K=3, V=2, seed=16)
+    d["g_raw"] -= 4.0            # mild decay so early tokens still matter at the end
+    r = np.random.default_rng(17)
+    dout = r.standard_normal(d["v"].shape)
+    kw = dict(scale=0.6, lower_bound=-5.0)
+    grads = oracle.kda_bwd(**d, dout=dout, initial_state=S0, **kw)
+    h = 1e-6
+    for name, gname in [("k", "dk"), ("g_raw", "dg_raw"), ("v", "dv")]:
+        x = d[name]
+        for idx in [(0, 0, 0, 0), (0, 63, 0, 1), (0, 64, 0, 1), (0, 100, 0, 0)]:
+            if x.ndim == 4 and idx[3] >= x.shape[3]:
+                continue
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            fp = np.sum(oracle.kda_fwd(**dict(d, **{name: xp}), initial_state=S0, **kw)[0] * dout)
+            fm = np.sum(oracle.kda_fwd(**dict(d, **{name: xm}), initial_state=S0, **kw)[0] * dout)
+            assert abs((fp - fm) / (2 * h) - grads[gname][idx]) < 1e-6 * max(1.0, abs(grads[gname][idx]))
