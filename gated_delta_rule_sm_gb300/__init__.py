@@ -1,0 +1,11 @@
+"""GB300 (sm_103a) Kimi Delta Attention: chunkwise gated delta rule, forward and backward.
+
+The computation lives in the CUDA library ``libkda_gb300.so`` behind the C
+ABI in ``include/kda.h``; this package only marshals torch tensors to it
+(``forward`` / ``backward``) and draws seeded synthetic inputs
+(``inputs``).  Importing the package does not load the library; the first
+call does, and raises if it has not been built.
+"""
+from ._lib import KdaError, backward, device_status, forward, load  # noqa: F401
+
+__all__ = ["forward", "backward", "load", "device_status", "KdaError"]

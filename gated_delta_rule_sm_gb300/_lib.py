@@ -1,0 +1,218 @@
+"""Thin Python binding of the KDA C ABI (``include/kda.h``).
+
+Argument marshalling only: torch provides device memory and the current CUDA
+stream, every step of the computation runs in the library's CUDA kernels.
+There is no fallback: if ``libkda_gb300.so`` is missing or CUDA is not
+available the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda_gb300.so")
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_WORKSPACE = range(6)
+KDA_BF16, KDA_FP32 = 0, 1
+
+# Every symbol include/kda.h declares.
+EXPORTS = ("kda_fwd_workspace_size", "kda_bwd_workspace_size", "kda_fwd", "kda_fwd_simt", "kda_bwd",
+           "kda_status_string", "kda_device_status", "kda_version", "kda_timing_begin", "kda_timing_end",
+           "kda_kernel_name")
+
+
+class KdaDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int), ("K", ctypes.c_int),
+                ("V", ctypes.c_int), ("dtype", ctypes.c_int), ("num_seqs", ctypes.c_int)]
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} (status {code})")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+_vp = ctypes.c_void_p
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library (build it first with ``gated_delta_rule_sm_gb300.build.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise ImportError(f"KDA CUDA library not built: {path} is missing "
+                              "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+        lib = ctypes.CDLL(path)
+        dims_p = ctypes.POINTER(KdaDims)
+        lib.kda_fwd_workspace_size.restype = ctypes.c_size_t
+        lib.kda_fwd_workspace_size.argtypes = [dims_p, ctypes.c_int]
+        lib.kda_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.kda_bwd_workspace_size.argtypes = [dims_p, ctypes.c_int]
+        fwd_args = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int] + [_vp] * 4 + \
+            [_vp, ctypes.c_size_t, _vp]
+        for name in ("kda_fwd", "kda_fwd_simt"):
+            f = getattr(lib, name)
+            f.restype = ctypes.c_int
+            f.argtypes = fwd_args
+        lib.kda_bwd.restype = ctypes.c_int
+        lib.kda_bwd.argtypes = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int] + \
+            [_vp] * 2 + [_vp] * 2 + [_vp] * 8 + [_vp, ctypes.c_size_t, _vp]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_status_string.argtypes = [ctypes.c_int]
+        lib.kda_device_status.restype = ctypes.c_int
+        lib.kda_device_status.argtypes = [ctypes.c_int]
+        lib.kda_version.restype = ctypes.c_int
+        lib.kda_version.argtypes = []
+        lib.kda_timing_begin.restype = ctypes.c_int
+        lib.kda_timing_begin.argtypes = [ctypes.c_int]
+        lib.kda_timing_end.restype = ctypes.c_int
+        lib.kda_timing_end.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), ctypes.c_int]
+        lib.kda_kernel_name.restype = ctypes.c_char_p
+        lib.kda_kernel_name.argtypes = [ctypes.c_int]
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load().kda_status_string(int(code)).decode()
+
+
+def device_status(reset: bool = True) -> int:
+    """The device status word (synchronises the device)."""
+    return load().kda_device_status(1 if reset else 0)
+
+
+def timing_begin(max_launches: int) -> None:
+    """Start recording per-kernel CUDA events inside the library (see kda_timing_begin)."""
+    _check(load().kda_timing_begin(int(max_launches)), "kda_timing_begin")
+
+
+def timing_end(cap: int = 1 << 16) -> list[tuple[str, float]]:
+    """Stop recording; returns [(kernel name, milliseconds)] in launch order."""
+    lib = load()
+    ms = (ctypes.c_float * cap)()
+    ids = (ctypes.c_int * cap)()
+    n = lib.kda_timing_end(ms, ids, cap)
+    if n < 0:
+        raise KdaError(KDA_ERR_CUDA, "kda_timing_end")
+    return [(lib.kda_kernel_name(ids[i]).decode(), float(ms[i])) for i in range(n)]
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_FP32
+    raise TypeError(f"unsupported activation dtype {t.dtype} (bf16 or fp32)")
+
+
+def make_dims(q: torch.Tensor, v: torch.Tensor, cu_seqlens: Optional[torch.Tensor]) -> KdaDims:
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    n = int(cu_seqlens.numel() - 1) if cu_seqlens is not None else 0
+    return KdaDims(B, T, H, K, V, _dtype_code(q), n)
+
+
+class _Workspace:
+    """Caches one device workspace per (device, kind); grows on demand."""
+
+    def __init__(self):
+        self.buf: dict = {}
+
+    def get(self, device: torch.device, kind: str, nbytes: int) -> torch.Tensor:
+        key = (device.index, kind)
+        b = self.buf.get(key)
+        if b is None or b.numel() < nbytes:
+            b = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+            self.buf[key] = b
+        return b
+
+    def clear(self):
+        self.buf.clear()
+
+
+workspace_cache = _Workspace()
+
+
+def _check(code: int, what: str):
+    if code != KDA_OK:
+        raise KdaError(code, what)
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("KDA inputs must be contiguous CUDA tensors")
+
+
+def forward(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale: float, lower_bound: float = -5.0,
+            chunk_size: int = 64, cu_seqlens=None, initial_state=None, output_final_state: bool = False,
+            out=None, final_state=None, simt: bool = False, stream: Optional[torch.cuda.Stream] = None):
+    """KDA forward through ``kda_fwd`` (or ``kda_fwd_simt``).  Returns (out, final_state or None)."""
+    lib = load()
+    _contig(q, k, v, g_raw, beta_raw, a_log, dt_bias, cu_seqlens, initial_state)
+    dims = make_dims(q, v, cu_seqlens)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    N = dims.num_seqs if cu_seqlens is not None else B
+    if out is None:
+        out = torch.empty((B, T, H, V), dtype=q.dtype, device=q.device)
+    if output_final_state and final_state is None:
+        final_state = torch.empty((N, H, K, V), dtype=torch.float32, device=q.device)
+    if not output_final_state:
+        final_state = None
+    ws_bytes = lib.kda_fwd_workspace_size(ctypes.byref(dims), chunk_size)
+    ws = workspace_cache.get(q.device, "fwd", ws_bytes)
+    st = stream if stream is not None else torch.cuda.current_stream(q.device)
+    fn = lib.kda_fwd_simt if simt else lib.kda_fwd
+    code = fn(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw), _ptr(a_log),
+              _ptr(dt_bias), float(scale), float(lower_bound), int(chunk_size), _ptr(cu_seqlens),
+              _ptr(initial_state), _ptr(out), _ptr(final_state), _ptr(ws), ctypes.c_size_t(ws.numel()),
+              ctypes.c_void_p(st.cuda_stream))
+    _check(code, "kda_fwd_simt" if simt else "kda_fwd")
+    return out, final_state
+
+
+def backward(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale: float, lower_bound: float = -5.0,
+             chunk_size: int = 64, cu_seqlens=None, initial_state=None, dfinal_state=None,
+             want_dinitial_state: bool = True, grads: Optional[dict] = None,
+             stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """KDA backward through ``kda_bwd``.  Returns a dict of fp32 gradients."""
+    lib = load()
+    _contig(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, cu_seqlens, initial_state, dfinal_state)
+    dims = make_dims(q, v, cu_seqlens)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    N = dims.num_seqs if cu_seqlens is not None else B
+    dev = q.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    if grads is None:
+        grads = dict(dq=torch.empty((B, T, H, K), **f32), dk=torch.empty((B, T, H, K), **f32),
+                     dv=torch.empty((B, T, H, V), **f32), dg_raw=torch.empty((B, T, H, K), **f32),
+                     dbeta_raw=torch.empty((B, T, H), **f32), da_log=torch.empty((H,), **f32),
+                     ddt_bias=torch.empty((H * K,), **f32),
+                     dinitial_state=torch.empty((N, H, K, V), **f32) if want_dinitial_state else None)
+    ws_bytes = lib.kda_bwd_workspace_size(ctypes.byref(dims), chunk_size)
+    ws = workspace_cache.get(dev, "bwd", ws_bytes)
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    code = lib.kda_bwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw), _ptr(a_log),
+                       _ptr(dt_bias), float(scale), float(lower_bound), int(chunk_size), _ptr(cu_seqlens),
+                       _ptr(initial_state), _ptr(dout), _ptr(dfinal_state), _ptr(grads["dq"]), _ptr(grads["dk"]),
+                       _ptr(grads["dv"]), _ptr(grads["dg_raw"]), _ptr(grads["dbeta_raw"]), _ptr(grads["da_log"]),
+                       _ptr(grads["ddt_bias"]), _ptr(grads.get("dinitial_state")), _ptr(ws),
+                       ctypes.c_size_t(ws.numel()), ctypes.c_void_p(st.cuda_stream))
+    _check(code, "kda_bwd")
+    return grads

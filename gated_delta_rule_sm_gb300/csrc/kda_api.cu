@@ -1,0 +1,332 @@
+// kda_api.cu -- the extern "C" boundary: validation, workspace carving and launches.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "kda.h"
+#include "kda_common.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+
+__device__ int g_status_word = 0;
+
+static constexpr size_t kAlign = 256;
+static constexpr int kGradCtas = 304;  // 2 CTAs per SM on a 152-SM GB300
+
+static size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Shape {
+    int B, T, H, K, V, N, TT, NCmax, dtype;
+    bool varlen;
+};
+
+static kda_status check_dims(const kda_dims* d, int chunk_size, bool varlen, Shape* s) {
+    if (!d) return KDA_ERR_INVALID_ARG;
+    if (d->B < 1 || d->T < 1 || d->H < 1 || d->K < 1 || d->V < 1) return KDA_ERR_INVALID_ARG;
+    if (d->dtype != KDA_BF16 && d->dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
+    if (chunk_size <= 0) return KDA_ERR_INVALID_ARG;
+    if (d->K < 16 || d->V < 16) return KDA_ERR_INVALID_ARG;           // head dims below 16 are rejected
+    if (chunk_size != kChunk) return KDA_ERR_UNSUPPORTED;
+    if (d->K > 128 || d->V > 128 || d->K % 16 || d->V % 16) return KDA_ERR_UNSUPPORTED;
+    const long long TT = (long long)d->B * d->T;
+    if (TT > (1LL << 30) || TT * d->H * (d->K > d->V ? d->K : d->V) > (1LL << 40)) return KDA_ERR_UNSUPPORTED;
+    if (varlen) {
+        if (d->B != 1 || d->num_seqs < 1) return KDA_ERR_INVALID_ARG;
+        if (d->num_seqs > (1 << 24)) return KDA_ERR_UNSUPPORTED;
+    }
+    s->B = d->B; s->T = d->T; s->H = d->H; s->K = d->K; s->V = d->V;
+    s->dtype = d->dtype;
+    s->varlen = varlen;
+    s->N = varlen ? d->num_seqs : d->B;
+    s->TT = (int)TT;
+    s->NCmax = varlen ? (int)((TT + kChunk - 1) / kChunk + s->N) : d->B * ((d->T + kChunk - 1) / kChunk);
+    return KDA_OK;
+}
+
+struct WsPlan {
+    size_t off_chunk, off_rec, off_states, off_dstates, off_pdtb, off_palog, off_scratch, total;
+    size_t rec_stride, scratch_stride;
+};
+
+static WsPlan plan_simt(const Shape& s, bool bwd) {
+    WsPlan w;
+    memset(&w, 0, sizeof(w));
+    const RecLayout L = RecLayout::make(s.K, s.V);
+    w.rec_stride = bwd ? L.bwd_size : L.fwd_size;
+    size_t o = 0;
+    w.off_chunk = o; o = align_up(o + sizeof(int32_t) * (size_t)(s.N + 1));
+    w.off_rec = o; o = align_up(o + sizeof(float) * (size_t)s.NCmax * s.H * w.rec_stride);
+    if (bwd) {
+        const size_t kv = (size_t)s.K * s.V;
+        w.off_states = o; o = align_up(o + sizeof(float) * (size_t)s.NCmax * s.H * kv);
+        w.off_dstates = o; o = align_up(o + sizeof(float) * (size_t)s.NCmax * s.H * kv);
+        w.off_pdtb = o; o = align_up(o + sizeof(float) * (size_t)s.NCmax * s.H * s.K);
+        w.off_palog = o; o = align_up(o + sizeof(float) * (size_t)s.NCmax * s.H);
+        w.scratch_stride = GradScratch::make(s.K, s.V).size;
+        w.off_scratch = o; o = align_up(o + sizeof(float) * (size_t)kGradCtas * w.scratch_stride);
+    }
+    w.total = o;
+    return w;
+}
+
+static kda_status status_ptr(int** out) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return KDA_ERR_CUDA;
+    *out = static_cast<int*>(p);
+    return KDA_OK;
+}
+
+static Params base_params(const Shape& s, const void* q, const void* k, const void* v, const void* g_raw,
+                          const void* beta_raw, const float* a_log, const float* dt_bias, float scale,
+                          float lb, const int32_t* cu, const float* S0) {
+    Params p;
+    memset(&p, 0, sizeof(p));
+    p.B = s.B; p.T = s.T; p.H = s.H; p.K = s.K; p.V = s.V; p.N = s.N; p.TT = s.TT;
+    p.dtype = s.dtype; p.NCmax = s.NCmax;
+    p.q = q; p.k = k; p.v = v; p.g_raw = g_raw; p.beta_raw = beta_raw;
+    p.a_log = a_log; p.dt_bias = dt_bias; p.scale = scale; p.lb = lb;
+    p.cu = cu; p.S0 = S0;
+    return p;
+}
+
+static void carve(Params& p, const WsPlan& w, void* ws) {
+    char* b = static_cast<char*>(ws);
+    p.chunk_off = reinterpret_cast<int32_t*>(b + w.off_chunk);
+    p.rec = reinterpret_cast<float*>(b + w.off_rec);
+    p.rec_stride = w.rec_stride;
+    if (w.off_states) {
+        p.states = reinterpret_cast<float*>(b + w.off_states);
+        p.dstates = reinterpret_cast<float*>(b + w.off_dstates);
+        p.part_dtb = reinterpret_cast<float*>(b + w.off_pdtb);
+        p.part_alog = reinterpret_cast<float*>(b + w.off_palog);
+        p.scratch = reinterpret_cast<float*>(b + w.off_scratch);
+        p.scratch_stride = w.scratch_stride;
+        p.grad_ctas = kGradCtas;
+    }
+}
+
+static kda_status common_checks(const kda_dims* dims, int chunk_size, const int32_t* cu, const void* q,
+                                const void* k, const void* v, const void* g_raw, const void* beta_raw,
+                                const float* a_log, const float* dt_bias, float scale, float lb, Shape* s) {
+    kda_status st = check_dims(dims, chunk_size, cu != nullptr, s);
+    if (st != KDA_OK) return st;
+    if (!q || !k || !v || !g_raw || !beta_raw || !a_log || !dt_bias) return KDA_ERR_INVALID_ARG;
+    if (!(lb < 0.0f) || !isfinite(lb)) return KDA_ERR_INVALID_ARG;   // the gate must be lower-bounded below 0
+    if (!isfinite(scale)) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
+static kda_status check_ws(void* ws, size_t bytes, size_t need) {
+    if (bytes < need) return KDA_ERR_WORKSPACE;
+    if (need > 0 && (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign))) return KDA_ERR_WORKSPACE;
+    return KDA_OK;
+}
+
+#define KDA_TRY_CUDA(expr)                              \
+    do {                                                \
+        if ((expr) != cudaSuccess) return KDA_ERR_CUDA; \
+    } while (0)
+
+static kda_status fwd_simt(const Shape& s, Params p, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    const WsPlan w = plan_simt(s, false);
+    kda_status st = check_ws(ws, ws_bytes, w.total);
+    if (st != KDA_OK) return st;
+    st = status_ptr(&p.status);
+    if (st != KDA_OK) return st;
+    carve(p, w, ws);
+    KDA_TRY_CUDA(launch_plan(p, stream));
+    KDA_TRY_CUDA(launch_intra_simt(p, false, stream));
+    KDA_TRY_CUDA(launch_chain_fwd_simt(p, false, stream));
+    return KDA_OK;
+}
+
+// ---- kernel timing (kda_timing_*) ----
+struct TimingState {
+    bool active = false;
+    int cap = 0, used = 0;
+    bool open = false;           // a pre event is recorded, post pending
+    cudaEvent_t* ev = nullptr;   // 2 * cap events
+    int* ids = nullptr;
+};
+static TimingState g_timing;
+
+void timing_pre(cudaStream_t st, int kernel_id) {
+    TimingState& t = g_timing;
+    if (!t.active || t.used >= t.cap) return;
+    cudaEventRecord(t.ev[2 * t.used], st);
+    t.ids[t.used] = kernel_id;
+    t.open = true;
+}
+
+void timing_post(cudaStream_t st) {
+    TimingState& t = g_timing;
+    if (!t.active || !t.open) return;
+    cudaEventRecord(t.ev[2 * t.used + 1], st);
+    t.open = false;
+    ++t.used;
+}
+
+static void timing_release() {
+    TimingState& t = g_timing;
+    if (t.ev) {
+        for (int i = 0; i < 2 * t.cap; ++i) cudaEventDestroy(t.ev[i]);
+        delete[] t.ev;
+    }
+    delete[] t.ids;
+    t = TimingState();
+}
+
+static const char* kKernelNames[] = {"kda_plan", "kda_intra_simt", "kda_chain_fwd_simt", "kda_chain_bwd_simt",
+                                     "kda_grad_simt", "kda_param_reduce", "kda_empty_segment"};
+
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" {
+
+size_t kda_fwd_workspace_size(const kda_dims* dims, int chunk_size) {
+    Shape s;
+    if (!dims) return 0;
+    if (check_dims(dims, chunk_size, dims->num_seqs > 0 && dims->B == 1, &s) != KDA_OK &&
+        check_dims(dims, chunk_size, false, &s) != KDA_OK)
+        return 0;
+    // size for the varlen bound when num_seqs is given, which also covers the fixed-length layout
+    return plan_simt(s, false).total;
+}
+
+size_t kda_bwd_workspace_size(const kda_dims* dims, int chunk_size) {
+    Shape s;
+    if (!dims) return 0;
+    if (check_dims(dims, chunk_size, dims->num_seqs > 0 && dims->B == 1, &s) != KDA_OK &&
+        check_dims(dims, chunk_size, false, &s) != KDA_OK)
+        return 0;
+    return plan_simt(s, true).total;
+}
+
+kda_status kda_fwd_simt(const kda_dims* dims, const void* q, const void* k, const void* v, const void* g_raw,
+                        const void* beta_raw, const float* a_log, const float* dt_bias, float scale,
+                        float lower_bound, int chunk_size, const int32_t* cu_seqlens, const float* initial_state,
+                        void* out, float* final_state, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
+    Shape s;
+    kda_status st = common_checks(dims, chunk_size, cu_seqlens, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale,
+                                  lower_bound, &s);
+    if (st != KDA_OK) return st;
+    if (!out) return KDA_ERR_INVALID_ARG;
+    Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
+                           initial_state);
+    p.out = out;
+    p.ST = final_state;
+    return fwd_simt(s, p, workspace, workspace_bytes, stream);
+}
+
+kda_status kda_fwd(const kda_dims* dims, const void* q, const void* k, const void* v, const void* g_raw,
+                   const void* beta_raw, const float* a_log, const float* dt_bias, float scale, float lower_bound,
+                   int chunk_size, const int32_t* cu_seqlens, const float* initial_state, void* out,
+                   float* final_state, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return kda_fwd_simt(dims, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, chunk_size,
+                        cu_seqlens, initial_state, out, final_state, workspace, workspace_bytes, stream);
+}
+
+kda_status kda_bwd(const kda_dims* dims, const void* q, const void* k, const void* v, const void* g_raw,
+                   const void* beta_raw, const float* a_log, const float* dt_bias, float scale, float lower_bound,
+                   int chunk_size, const int32_t* cu_seqlens, const float* initial_state, const void* dout,
+                   const float* dfinal_state, float* dq, float* dk, float* dv, float* dg_raw, float* dbeta_raw,
+                   float* da_log, float* ddt_bias, float* dinitial_state, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream) {
+    Shape s;
+    kda_status st = common_checks(dims, chunk_size, cu_seqlens, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale,
+                                  lower_bound, &s);
+    if (st != KDA_OK) return st;
+    if (!dout || !dq || !dk || !dv || !dg_raw || !dbeta_raw || !da_log || !ddt_bias) return KDA_ERR_INVALID_ARG;
+    Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
+                           initial_state);
+    p.dout = dout; p.dST = dfinal_state;
+    p.dq = dq; p.dk = dk; p.dv = dv; p.dg_raw = dg_raw; p.dbeta_raw = dbeta_raw;
+    p.da_log = da_log; p.ddt_bias = ddt_bias; p.dS0 = dinitial_state;
+    const WsPlan w = plan_simt(s, true);
+    st = check_ws(workspace, workspace_bytes, w.total);
+    if (st != KDA_OK) return st;
+    st = status_ptr(&p.status);
+    if (st != KDA_OK) return st;
+    carve(p, w, workspace);
+    KDA_TRY_CUDA(launch_plan(p, stream));
+    KDA_TRY_CUDA(launch_intra_simt(p, true, stream));
+    KDA_TRY_CUDA(launch_chain_fwd_simt(p, true, stream));
+    KDA_TRY_CUDA(launch_chain_bwd_simt(p, stream));
+    KDA_TRY_CUDA(launch_grad_simt(p, stream));
+    return KDA_OK;
+}
+
+const char* kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARG: return "invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "unsupported shape or parameter";
+        case KDA_ERR_CUDA: return "CUDA error";
+        case KDA_ERR_TIMEOUT: return "device wait timed out";
+        case KDA_ERR_WORKSPACE: return "workspace too small or misaligned";
+    }
+    return "unknown status";
+}
+
+kda_status kda_device_status(int reset) {
+    int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    if (reset) {
+        const int z = 0;
+        if (cudaMemcpyToSymbol(g_status_word, &z, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    return static_cast<kda_status>(v);
+}
+
+int kda_version(void) { return 100; }
+
+kda_status kda_timing_begin(int max_launches) {
+    timing_release();
+    if (max_launches <= 0) return KDA_ERR_INVALID_ARG;
+    TimingState& t = g_timing;
+    t.cap = max_launches;
+    t.ev = new cudaEvent_t[2 * (size_t)max_launches];
+    t.ids = new int[max_launches];
+    for (int i = 0; i < 2 * max_launches; ++i) {
+        if (cudaEventCreate(&t.ev[i]) != cudaSuccess) {
+            t.cap = i / 2;
+            for (int j = 0; j < i; ++j) cudaEventDestroy(t.ev[j]);
+            delete[] t.ev;
+            delete[] t.ids;
+            t = TimingState();
+            return KDA_ERR_CUDA;
+        }
+    }
+    t.active = true;
+    return KDA_OK;
+}
+
+int kda_timing_end(float* ms, int* kernel_ids, int cap) {
+    TimingState& t = g_timing;
+    if (!t.active) return 0;
+    t.active = false;
+    int n = t.used < cap ? t.used : cap;
+    int ok = 1;
+    for (int i = 0; i < n; ++i) {
+        float x = 0.f;
+        if (cudaEventSynchronize(t.ev[2 * i + 1]) != cudaSuccess ||
+            cudaEventElapsedTime(&x, t.ev[2 * i], t.ev[2 * i + 1]) != cudaSuccess)
+            ok = 0;
+        if (ms) ms[i] = x;
+        if (kernel_ids) kernel_ids[i] = t.ids[i];
+    }
+    timing_release();
+    return ok ? n : -1;
+}
+
+const char* kda_kernel_name(int kernel_id) {
+    if (kernel_id < 0 || kernel_id >= (int)(sizeof(kKernelNames) / sizeof(kKernelNames[0]))) return "unknown";
+    return kKernelNames[kernel_id];
+}
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// kda_common.cuh -- shared definitions of the KDA CUDA library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+constexpr int kChunk = 64;      // tokens per chunk
+constexpr int kSub = 16;        // tokens per decay sub-block (tensor-core path)
+constexpr float kNormEps = 1e-6f;
+
+// Everything a kernel of either path needs, passed by value.
+struct Params {
+    int B, T, H, K, V, N;       // N = number of segments
+    int TT;                     // total tokens B*T
+    int dtype;                  // KDA_BF16 / KDA_FP32
+    int NCmax;                  // upper bound on the number of chunks
+    const void *q, *k, *v, *g_raw, *beta_raw, *dout;
+    const float *a_log, *dt_bias, *S0, *dST;
+    const int32_t* cu;          // device cu_seqlens or nullptr
+    float scale, lb;
+    void* out;
+    float* ST;
+    float *dq, *dk, *dv, *dg_raw, *dbeta_raw, *da_log, *ddt_bias, *dS0;
+    // workspace views
+    int32_t* chunk_off;         // [N+1] first chunk of each segment; chunk_off[N] = total chunks
+    float* rec;                 // per (chunk, head) intra-chunk records (SIMT path)
+    size_t rec_stride;          // floats per record
+    float* states;              // [NCmax, H, K, V] chunk-entering states (backward)
+    float* dstates;             // [NCmax, H, K, V] gradient w.r.t. chunk-leaving states (backward)
+    float* part_dtb;            // [NCmax, H, K] per-chunk partial d dt_bias
+    float* part_alog;           // [NCmax, H]    per-chunk partial d a_log
+    float* scratch;             // per-CTA scratch of the SIMT gradient kernel
+    size_t scratch_stride;      // floats per CTA
+    int grad_ctas;              // CTAs of the SIMT gradient kernel
+    void* tc;                   // tensor-core path buffers (its own layout)
+    int* status;                // device status word
+};
+
+// Device status word (first error wins); `status` points at the library's word on this device.
+__device__ __forceinline__ void record_error(int* status, int code) { atomicCAS(status, 0, code); }
+
+__device__ __forceinline__ float load_act(const void* p, size_t i, int dtype) {
+    if (dtype == KDA_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
+    return reinterpret_cast<const float*>(p)[i];
+}
+
+__device__ __forceinline__ void store_act(void* p, size_t i, float x, int dtype) {
+    if (dtype == KDA_BF16) reinterpret_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(x);
+    else reinterpret_cast<float*>(p)[i] = x;
+}
+
+__device__ __forceinline__ float sigmoidf_acc(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Segment n spans tokens [seg_begin, seg_end) of the flattened B*T axis.
+__device__ __forceinline__ int seg_begin(const Params& p, int n) { return p.cu ? p.cu[n] : n * p.T; }
+__device__ __forceinline__ int seg_end(const Params& p, int n) { return p.cu ? p.cu[n + 1] : (n + 1) * p.T; }
+
+// Segment owning global chunk c (binary search over chunk_off).
+__device__ __forceinline__ int chunk_segment(const Params& p, int c) {
+    int lo = 0, hi = p.N - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (p.chunk_off[mid] <= c) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+}  // namespace kda

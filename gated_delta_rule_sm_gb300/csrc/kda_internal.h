@@ -1,0 +1,77 @@
+// kda_internal.h -- host/device layouts and launchers shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "kda_common.cuh"
+
+namespace kda {
+
+// Per (chunk, head) record of the SIMT path, in floats.
+struct RecLayout {
+    size_t W, Qg, Kd, U0, A, gC;           // forward fields
+    size_t Kg, N, G, qh, kh, B, beta;      // backward extras
+    size_t fwd_size, bwd_size;
+    __host__ __device__ static RecLayout make(int K, int V) {
+        RecLayout r;
+        size_t o = 0;
+        r.W = o; o += 64 * (size_t)K;
+        r.Qg = o; o += 64 * (size_t)K;
+        r.Kd = o; o += 64 * (size_t)K;
+        r.U0 = o; o += 64 * (size_t)V;
+        r.A = o; o += 64 * 64;
+        r.gC = o; o += (size_t)K;
+        r.fwd_size = (o + 63) / 64 * 64;
+        r.Kg = o; o += 64 * (size_t)K;
+        r.N = o; o += 64 * 64;
+        r.G = o; o += 64 * (size_t)K;
+        r.qh = o; o += 64 * (size_t)K;
+        r.kh = o; o += 64 * (size_t)K;
+        r.B = o; o += 64 * 64;
+        r.beta = o; o += 64;
+        r.bwd_size = (o + 63) / 64 * 64;
+        return r;
+    }
+};
+
+// Per-CTA scratch of the SIMT gradient kernel, in floats.
+struct GradScratch {
+    size_t dO, Vin, Vt, U, dU, dY, tmp;    // [64][V] (tmp: [64][max(V,64)])
+    size_t dT, dA, dN, dL;                 // [64][64]
+    size_t dQg, dKd, dKg, dq, dk, dG;      // [64][K]
+    size_t dbeta;                          // [64]
+    size_t size;
+    __host__ __device__ static GradScratch make(int K, int V) {
+        GradScratch z;
+        size_t o = 0;
+        const size_t cv = 64 * (size_t)V, ck = 64 * (size_t)K, cc = 64 * 64;
+        z.dO = o; o += cv; z.Vin = o; o += cv; z.Vt = o; o += cv; z.U = o; o += cv;
+        z.dU = o; o += cv; z.dY = o; o += cv;
+        z.tmp = o; o += 64 * (size_t)(V > 64 ? V : 64);
+        z.dT = o; o += cc; z.dA = o; o += cc; z.dN = o; o += cc; z.dL = o; o += cc;
+        z.dQg = o; o += ck; z.dKd = o; o += ck; z.dKg = o; o += ck; z.dq = o; o += ck; z.dk = o; o += ck;
+        z.dG = o; o += ck;
+        z.dbeta = o; o += 64;
+        z.size = (o + 63) / 64 * 64;
+        return z;
+    }
+};
+
+// Kernel ids for kda_kernel_name / kda_timing_end.
+enum KernelId {
+    K_PLAN = 0, K_INTRA_SIMT, K_CHAIN_FWD_SIMT, K_CHAIN_BWD_SIMT, K_GRAD_SIMT, K_PARAM_REDUCE, K_EMPTY_SEG,
+    K_NUM_KERNELS
+};
+
+// Launch bracketing for kda_timing_*: no-ops unless timing is active.
+void timing_pre(cudaStream_t st, int kernel_id);
+void timing_post(cudaStream_t st);
+
+cudaError_t launch_plan(const Params& p, cudaStream_t st);
+cudaError_t launch_intra_simt(const Params& p, bool bwd, cudaStream_t st);
+cudaError_t launch_chain_fwd_simt(const Params& p, bool store_states, cudaStream_t st);
+cudaError_t launch_chain_bwd_simt(const Params& p, cudaStream_t st);
+cudaError_t launch_grad_simt(const Params& p, cudaStream_t st);
+
+}  // namespace kda

@@ -1,0 +1,157 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention library.
+ *
+ * The operation is the chunkwise KDA gated delta rule: per head and token
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * ("[kimi k3] add eager reference model with FSDP2", torchtitan PR #4025:
+ * chunk_kda with the gate activation, beta sigmoid and q/k L2 norm fused into
+ * the kernel, checked against the explicit recurrence forward and backward).
+ * The prologue is computed inside the kernels:
+ *     q_hat = q / sqrt(|q|^2 + 1e-6), k_hat likewise (per head, over K)
+ *     beta  = sigmoid(beta_raw)
+ *     g     = lower_bound * sigmoid(exp(a_log_h) * (g_raw + dt_bias_{h,c})),  alpha = exp(g)
+ * (hyper-parallel "KDA context-parallel executors", `_run_local_kda`: the
+ * fused backend requires this lower-bounded gate; the exact formula is not
+ * printed on the pages and is this library's reading).
+ *
+ * Layouts follow `_validate_projected_inputs` on the same page (token-first,
+ * contiguous, row-major):
+ *     q, k, g_raw     [B, T, H, K]        dtype (bf16 or fp32)
+ *     v, out, dout    [B, T, H, V]        dtype
+ *     beta_raw        [B, T, H]           dtype
+ *     a_log           [H]                 fp32
+ *     dt_bias         [H * K]             fp32
+ *     states          [N, H, K, V]        fp32  (initial, final and their gradients)
+ *     gradients       same shape as their input, always fp32
+ * Packed documents (nemo_automodel `kimi_k3.cp`, `segment_cu_seqlens`): with
+ * cu_seqlens != NULL, B must be 1 and segment n is tokens
+ * [cu_seqlens[n], cu_seqlens[n+1]) of the T tokens; each segment is its own
+ * recurrence starting from initial_state[n] (or zero).  Without cu_seqlens
+ * the N = B rows are the segments.
+ *
+ * Ownership: every pointer is a DEVICE pointer owned by the caller (cu_seqlens
+ * too).  The library allocates no memory, keeps no pointer after a call
+ * returns, and enqueues all work on `stream` asynchronously; outputs are
+ * fully overwritten.  Scratch memory comes from the caller's `workspace`
+ * (device, 256-byte aligned, at least the size the *_workspace_size query
+ * returns).
+ *
+ * Errors: arguments are validated on the host before anything is enqueued;
+ * a failed check returns KDA_ERR_INVALID_ARG (bad shape, pointer or value),
+ * KDA_ERR_UNSUPPORTED (valid but not implemented) or KDA_ERR_WORKSPACE (too
+ * small / misaligned).  A CUDA launch failure returns KDA_ERR_CUDA.  Nothing
+ * aborts and no C++ exception crosses this boundary.  Device-side waits are
+ * bounded; one that gives up records KDA_ERR_TIMEOUT in a device status word
+ * read by kda_device_status().
+ */
+#ifndef KDA_GB300_H
+#define KDA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,
+    KDA_ERR_UNSUPPORTED = 2,
+    KDA_ERR_CUDA = 3,
+    KDA_ERR_TIMEOUT = 4,
+    KDA_ERR_WORKSPACE = 5
+} kda_status;
+
+typedef enum { KDA_BF16 = 0, KDA_FP32 = 1 } kda_dtype;
+
+/* Problem shape.  num_seqs is the number of packed segments N when
+ * cu_seqlens is given (then B == 1) and is ignored otherwise (N = B). */
+typedef struct {
+    int B, T, H, K, V;
+    kda_dtype dtype;
+    int num_seqs;
+} kda_dims;
+
+/* Bytes of workspace kda_fwd / kda_bwd need for this shape (0 on invalid input). */
+size_t kda_fwd_workspace_size(const kda_dims* dims, int chunk_size);
+size_t kda_bwd_workspace_size(const kda_dims* dims, int chunk_size);
+
+/*
+ * Forward.  Writes out [B,T,H,V] (input dtype) and, if final_state != NULL,
+ * final_state [N,H,K,V] fp32.  initial_state may be NULL (zero state).
+ * scale is applied to the output; lower_bound must be in [-5, 0) (the
+ * 16-token sub-block factorisation of the decay stays inside fp32 range
+ * only for |lower_bound| <= 5); chunk_size must be 64.
+ * Requirements: B,T,H >= 1; 16 <= K,V <= 128 and multiples of 16 (the pages
+ * reject head dims below 16); N >= 1.  bf16 with K == V == 128 runs on the
+ * tcgen05 tensor-core path; every other supported shape (and fp32 inputs)
+ * runs on the fp32 SIMT path.
+ */
+kda_status kda_fwd(const kda_dims* dims,
+                   const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
+                   const float* a_log, const float* dt_bias, float scale, float lower_bound, int chunk_size,
+                   const int32_t* cu_seqlens, const float* initial_state,
+                   void* out, float* final_state,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Same as kda_fwd but always on the fp32 SIMT kernels (any supported shape). */
+kda_status kda_fwd_simt(const kda_dims* dims,
+                        const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
+                        const float* a_log, const float* dt_bias, float scale, float lower_bound, int chunk_size,
+                        const int32_t* cu_seqlens, const float* initial_state,
+                        void* out, float* final_state,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Backward (recomputes the forward internally; nothing is saved between
+ * calls).  Inputs as for kda_fwd plus dout [B,T,H,V] (input dtype) and
+ * dfinal_state [N,H,K,V] fp32 (may be NULL = zero).  Writes fp32 gradients
+ * dq, dk, dg_raw [B,T,H,K], dv [B,T,H,V], dbeta_raw [B,T,H], da_log [H],
+ * ddt_bias [H*K] and, if dinitial_state != NULL, dinitial_state [N,H,K,V].
+ * The parameter gradients are reduced in a fixed order (deterministic).
+ */
+kda_status kda_bwd(const kda_dims* dims,
+                   const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
+                   const float* a_log, const float* dt_bias, float scale, float lower_bound, int chunk_size,
+                   const int32_t* cu_seqlens, const float* initial_state,
+                   const void* dout, const float* dfinal_state,
+                   float* dq, float* dk, float* dv, float* dg_raw, float* dbeta_raw,
+                   float* da_log, float* ddt_bias, float* dinitial_state,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* kda_status_string(kda_status s);
+
+/* Device status word of the current device: KDA_OK, or the first error a
+ * kernel recorded (e.g. KDA_ERR_TIMEOUT from a bounded wait).  Synchronises
+ * the device.  reset != 0 clears the word afterwards. */
+kda_status kda_device_status(int reset);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int kda_version(void);
+
+/*
+ * Kernel timing for benchmarks.  After kda_timing_begin(max_launches), the
+ * library records one CUDA event before and one after each kernel it
+ * launches (on that launch's stream), for at most max_launches launches.
+ * kda_timing_end() waits for those events, writes each launch's duration in
+ * milliseconds and its kernel id (name: kda_kernel_name) into the caller's
+ * host arrays (capacity `cap`), releases the events and returns how many
+ * launches were recorded, or -1 on a CUDA error.  Process-wide; not meant
+ * for concurrent use from several host threads.  Returns KDA_ERR_CUDA if the
+ * events cannot be created.
+ */
+kda_status kda_timing_begin(int max_launches);
+int kda_timing_end(float* ms, int* kernel_ids, int cap);
+const char* kda_kernel_name(int kernel_id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_H */

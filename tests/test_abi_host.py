@@ -1,0 +1,104 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports what include/kda.h
+declares, and rejects bad arguments before it touches the device."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from gated_delta_rule_sm_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return _lib.load()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert declared, "no declarations found"
+    assert declared == set(_lib.EXPORTS), declared ^ set(_lib.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert _lib.status_string(code)
+    assert lib.kda_version() >= 100
+
+
+def _dims(**kw):
+    d = dict(B=1, T=256, H=2, K=64, V=64, dtype=_lib.KDA_BF16, num_seqs=0)
+    d.update(kw)
+    return _lib.KdaDims(**d)
+
+
+def _fwd(lib, dims, chunk=64, lb=-5.0, scale=0.125, ptr=1, ws=None, ws_bytes=0, cu=None):
+    p = ctypes.c_void_p(ptr) if ptr else None
+    return lib.kda_fwd(ctypes.byref(dims), p, p, p, p, p, p, p, scale, lb, chunk, cu, None, p, None, ws,
+                       ctypes.c_size_t(ws_bytes), None)
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(B=0), _lib.KDA_ERR_INVALID_ARG),
+    (dict(T=0), _lib.KDA_ERR_INVALID_ARG),
+    (dict(K=8), _lib.KDA_ERR_INVALID_ARG),          # head dims below 16 are rejected
+    (dict(V=12), _lib.KDA_ERR_INVALID_ARG),
+    (dict(K=256), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(V=72), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(dtype=7), _lib.KDA_ERR_INVALID_ARG),
+])
+def test_shape_validation(lib, bad, code):
+    assert _fwd(lib, _dims(**bad)) == code
+
+
+def test_scalar_validation(lib):
+    assert _fwd(lib, _dims(), chunk=0) == _lib.KDA_ERR_INVALID_ARG
+    assert _fwd(lib, _dims(), chunk=32) == _lib.KDA_ERR_UNSUPPORTED
+    assert _fwd(lib, _dims(), lb=0.0) == _lib.KDA_ERR_INVALID_ARG      # the gate needs a negative bound
+    assert _fwd(lib, _dims(), lb=1.0) == _lib.KDA_ERR_INVALID_ARG
+    assert _fwd(lib, _dims(), lb=float("nan")) == _lib.KDA_ERR_INVALID_ARG
+    assert _fwd(lib, _dims(), scale=float("inf")) == _lib.KDA_ERR_INVALID_ARG
+    assert _fwd(lib, _dims(), ptr=0) == _lib.KDA_ERR_INVALID_ARG
+
+
+def test_varlen_validation(lib):
+    cu = ctypes.c_void_p(16)
+    assert _fwd(lib, _dims(B=2, num_seqs=3), cu=cu) == _lib.KDA_ERR_INVALID_ARG   # packed needs B == 1
+    assert _fwd(lib, _dims(num_seqs=0), cu=cu) == _lib.KDA_ERR_INVALID_ARG
+
+
+def test_workspace_validation(lib):
+    d = _dims()
+    need = lib.kda_fwd_workspace_size(ctypes.byref(d), 64)
+    assert need > 0
+    assert _fwd(lib, d, ws=None, ws_bytes=0) == _lib.KDA_ERR_WORKSPACE
+    assert _fwd(lib, d, ws=ctypes.c_void_p(4096 + 8), ws_bytes=need) == _lib.KDA_ERR_WORKSPACE  # misaligned
+
+
+def test_workspace_sizes_grow_with_problem(lib):
+    s = lambda **kw: lib.kda_fwd_workspace_size(ctypes.byref(_dims(**kw)), 64)
+    b = lambda **kw: lib.kda_bwd_workspace_size(ctypes.byref(_dims(**kw)), 64)
+    assert s(T=512) > s(T=256) > 0
+    assert s(H=4) > s(H=2)
+    assert b(T=256) > s(T=256)
+    assert s(num_seqs=5) >= s()            # packed sizing covers the fixed-length layout
+    assert lib.kda_fwd_workspace_size(ctypes.byref(_dims(K=8)), 64) == 0
+    assert lib.kda_fwd_workspace_size(None, 64) == 0

@@ -1,0 +1,185 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle, element by element."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from kda_cases import f64, gpu_bwd, gpu_fwd, head_slice, oracle_bwd, oracle_fwd, rel_err, tol
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from gated_delta_rule_sm_gb300 import device_status  # noqa: E402
+from gated_delta_rule_sm_gb300.inputs import WORKLOADS, Workload, make_inputs  # noqa: E402
+
+DEV = "cuda:0"
+
+
+def _check_fwd(x, dtype, simt=False, final=True):
+    out, fs = gpu_fwd(x, simt=simt, final=final)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    r_out, r_fs = oracle_fwd(x)
+    e = rel_err(out, r_out, dtype)
+    assert e <= tol(dtype), ("out", e)
+    if final:
+        e2 = rel_err(fs, r_fs, dtype)
+        assert e2 <= tol(dtype), ("final_state", e2)
+    return out, fs
+
+
+GRADS = ("dq", "dk", "dv", "dg_raw", "dbeta_raw", "da_log", "ddt_bias", "dinitial_state")
+
+
+def _check_bwd(x, dtype, dfinal=None):
+    g = gpu_bwd(x, dfinal=dfinal)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    r = oracle_bwd(x, dfinal=f64(dfinal) if dfinal is not None else None)
+    errs = {n: rel_err(g[n], r[n], dtype) for n in GRADS}
+    bad = {n: e for n, e in errs.items() if not e <= tol(dtype)}
+    assert not bad, bad
+
+
+# ------------------------------------------------------------------ the fp32 workload, exact config
+
+@pytest.mark.parametrize("simt", [False, True])
+def test_fwd_fp32_T256_H2_D64(simt):
+    x = make_inputs(WORKLOADS["fwd_fp32_T256_H2_D64"], device=DEV)
+    _check_fwd(x, "fp32", simt=simt)
+
+
+# ------------------------------------------------------------------ small bf16 / fp32 cases
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200])
+@pytest.mark.parametrize("D", [64, 128])
+def test_fwd_bf16_ragged(T, D):
+    w = Workload("t", B=2, T=T, H=2, K=D, V=D, initial_state=True, seed=T)
+    _check_fwd(make_inputs(w, device=DEV), "bf16")
+
+
+@pytest.mark.parametrize("K,V", [(64, 128), (128, 48), (16, 16), (32, 96)])
+def test_fwd_uneven_heads(K, V):
+    w = Workload("t", B=1, T=130, H=3, K=K, V=V, initial_state=True, seed=K + V)
+    _check_fwd(make_inputs(w, device=DEV), "bf16")
+
+
+def test_fwd_mild_gate_long_memory():
+    """g_raw ~ N(-4, 1) gives alpha close to 1, so early tokens and S0 still matter at the end."""
+    w = Workload("t", B=1, T=700, H=2, K=128, V=128, initial_state=True, g_mean=-4.0, seed=5)
+    _check_fwd(make_inputs(w, device=DEV), "bf16")
+
+
+def test_fwd_fp32_mild_gate():
+    w = Workload("t", B=2, T=300, H=2, K=64, V=64, dtype="fp32", initial_state=True, g_mean=-4.0, seed=6)
+    _check_fwd(make_inputs(w, device=DEV), "fp32")
+
+
+def test_fwd_varlen_with_empty_and_tiny_documents():
+    lens = [5, 0, 64, 130, 1, 63, 65]
+    w = Workload("t", B=1, T=sum(lens), H=2, K=128, V=128, varlen=True, initial_state=True, seed=7)
+    x = make_inputs(w, device=DEV, lengths=lens)
+    _check_fwd(x, "bf16")
+
+
+def test_fwd_no_final_state_and_simt_agree():
+    w = Workload("t", B=1, T=257, H=2, K=128, V=128, seed=8)
+    x = make_inputs(w, device=DEV)
+    o1, _ = gpu_fwd(x, final=False)
+    o2, _ = gpu_fwd(x, simt=True, final=False)
+    r, _ = oracle_fwd(x)
+    assert rel_err(o1, r, "bf16") <= 2e-2 and rel_err(o2, r, "bf16") <= 2e-2
+
+
+def test_fwd_is_deterministic():
+    w = Workload("t", B=2, T=300, H=4, K=128, V=128, initial_state=True, seed=9)
+    x = make_inputs(w, device=DEV)
+    a, fa = gpu_fwd(x)
+    b, fb = gpu_fwd(x)
+    assert torch.equal(a, b) and torch.equal(fa, fb)
+
+
+# ------------------------------------------------------------------ backward
+
+@pytest.mark.parametrize("T", [1, 64, 150])
+def test_bwd_bf16_small(T):
+    w = Workload("t", B=2, T=T, H=2, K=64, V=64, initial_state=True, backward=True, seed=10 + T)
+    x = make_inputs(w, device=DEV)
+    dfinal = 0.1 * torch.randn((2, 2, 64, 64), generator=torch.Generator().manual_seed(T)).to(DEV)
+    _check_bwd(x, "bf16", dfinal=dfinal)
+
+
+def test_bwd_fp32():
+    w = Workload("t", B=1, T=256, H=2, K=64, V=64, dtype="fp32", initial_state=True, backward=True,
+                 g_mean=-2.0, seed=11)
+    _check_bwd(make_inputs(w, device=DEV), "fp32")
+
+
+def test_bwd_bf16_d128_varlen():
+    lens = [70, 0, 1, 129]
+    w = Workload("t", B=1, T=sum(lens), H=2, K=128, V=128, varlen=True, initial_state=True, backward=True,
+                 seed=12)
+    _check_bwd(make_inputs(w, device=DEV, lengths=lens), "bf16")
+
+
+def test_bwd_is_deterministic():
+    w = Workload("t", B=1, T=200, H=2, K=128, V=128, backward=True, seed=13)
+    x = make_inputs(w, device=DEV)
+    a = gpu_bwd(x)
+    b = gpu_bwd(x)
+    for n in ("dq", "da_log", "ddt_bias"):
+        assert torch.equal(a[n], b[n])
+
+
+# ------------------------------------------------------------------ the quoted workloads at full size
+
+def test_full_fwd_bf16_B2_T2048_H16_D128():
+    x = make_inputs(WORKLOADS["fwd_bf16_B2_T2048_H16_D128"], device=DEV)
+    _check_fwd(x, "bf16", final=False)
+
+
+def test_full_varlen_fwd_bf16_T16384_H32_sampled_heads():
+    x = make_inputs(WORKLOADS["varlen_fwd_bf16_T16384_H32_D128"], device=DEV)
+    out, fs = gpu_fwd(x, final=True)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    heads = [0, 13, 31]
+    xs = head_slice(x, heads)
+    r_out, r_fs = oracle_fwd(xs)
+    assert rel_err(out[:, :, heads], r_out, "bf16") <= 2e-2
+    assert rel_err(fs[:, heads], r_fs, "bf16") <= 2e-2
+
+
+def test_full_long_fwd_bf16_T65536_H32_sampled_heads():
+    x = make_inputs(WORKLOADS["long_fwd_bf16_T65536_H32_D128"], device=DEV)
+    out, fs = gpu_fwd(x, final=True)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    heads = [3, 30]
+    xs = head_slice(x, heads)
+    r_out, r_fs = oracle_fwd(xs)
+    assert rel_err(out[:, :, heads], r_out, "bf16") <= 2e-2
+    assert rel_err(fs[:, heads], r_fs, "bf16") <= 2e-2
+
+
+def test_full_fwdbwd_bf16_B4_T4096_H32_sampled():
+    x = make_inputs(WORKLOADS["fwdbwd_bf16_B4_T4096_H32_D128"], device=DEV)
+    out, _ = gpu_fwd(x, final=False)
+    g = gpu_bwd(x)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    heads = [1, 17]
+    xs = head_slice(x, heads)
+    r_out, _ = oracle_fwd(xs, rows=[0])
+    assert rel_err(out[0:1][:, :, heads], r_out, "bf16") <= 2e-2
+    r = oracle_bwd(xs, rows=[0])
+    for n in ("dq", "dk", "dv", "dg_raw", "dbeta_raw"):
+        assert rel_err(g[n][0:1][:, :, heads], r[n], "bf16") <= 2e-2, n
+    # parameter gradients sum over all rows: check the per-row split is consistent via rows 0..3 sampled
+    r_all = oracle_bwd(head_slice(x, heads))
+    assert rel_err(g["da_log"][heads], r_all["da_log"], "bf16") <= 2e-2
+    K = x["q"].shape[-1]
+    assert rel_err(g["ddt_bias"].view(-1, K)[heads], r_all["ddt_bias"].reshape(len(heads), K), "bf16") <= 2e-2
