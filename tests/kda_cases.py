@@ -15,7 +15,9 @@ TOL_BF16 = 2e-2
 
 
 def f64(t):
-    return None if t is None else t.detach().to(torch.float64).cpu().numpy()
+    if t is None or isinstance(t, np.ndarray):
+        return t
+    return t.detach().to(torch.float64).cpu().numpy()
 
 
 # Storing a result in bf16 rounds it by up to half an ulp, i.e. up to 2^-8 of its magnitude; the

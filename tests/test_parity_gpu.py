@@ -38,7 +38,7 @@ def _check_bwd(x, dtype, dfinal=None):
     g = gpu_bwd(x, dfinal=dfinal)
     torch.cuda.synchronize()
     assert device_status() == 0
-    r = oracle_bwd(x, dfinal=f64(dfinal) if dfinal is not None else None)
+    r = oracle_bwd(x, dfinal=dfinal)
     errs = {n: rel_err(g[n], r[n], dtype) for n in GRADS}
     bad = {n: e for n, e in errs.items() if not e <= tol(dtype)}
     assert not bad, bad
