@@ -70,6 +70,22 @@ static WsPlan plan_simt(const Shape& s, bool bwd) {
     return w;
 }
 
+// Tensor-core path: bf16 activations with K = V = 128.
+static bool tc_eligible(const Shape& s) { return s.dtype == KDA_BF16 && s.K == 128 && s.V == 128; }
+
+struct TcPlan {
+    size_t off_chunk, off_rec, total;
+};
+
+static TcPlan plan_tc_fwd(const Shape& s) {
+    TcPlan w;
+    size_t o = 0;
+    w.off_chunk = o; o = align_up(o + sizeof(int32_t) * (size_t)(s.N + 1));
+    w.off_rec = o; o = align_up(o + tc_record_bytes(s.NCmax, s.H));
+    w.total = o;
+    return w;
+}
+
 static kda_status status_ptr(int** out) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return KDA_ERR_CUDA;
@@ -177,8 +193,24 @@ static void timing_release() {
     t = TimingState();
 }
 
-static const char* kKernelNames[] = {"kda_plan", "kda_intra_simt", "kda_chain_fwd_simt", "kda_chain_bwd_simt",
-                                     "kda_grad_simt", "kda_param_reduce", "kda_empty_segment"};
+static const char* kKernelNames[] = {"kda_plan",          "kda_intra_simt",   "kda_chain_fwd_simt",
+                                     "kda_chain_bwd_simt", "kda_grad_simt",    "kda_param_reduce",
+                                     "kda_empty_segment", "kda_intra_tc",     "kda_chain_fwd_tc"};
+
+static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    const TcPlan w = plan_tc_fwd(s);
+    kda_status st = check_ws(ws, ws_bytes, w.total);
+    if (st != KDA_OK) return st;
+    st = status_ptr(&p.status);
+    if (st != KDA_OK) return st;
+    char* b = static_cast<char*>(ws);
+    p.chunk_off = reinterpret_cast<int32_t*>(b + w.off_chunk);
+    uint8_t* recs = reinterpret_cast<uint8_t*>(b + w.off_rec);
+    KDA_TRY_CUDA(launch_plan(p, stream));
+    KDA_TRY_CUDA(launch_intra_tc(p, recs, stream));
+    KDA_TRY_CUDA(launch_chain_fwd_tc(p, recs, false, stream));
+    return KDA_OK;
+}
 
 }  // namespace kda
 
@@ -192,8 +224,11 @@ size_t kda_fwd_workspace_size(const kda_dims* dims, int chunk_size) {
     if (check_dims(dims, chunk_size, dims->num_seqs > 0 && dims->B == 1, &s) != KDA_OK &&
         check_dims(dims, chunk_size, false, &s) != KDA_OK)
         return 0;
-    // size for the varlen bound when num_seqs is given, which also covers the fixed-length layout
-    return plan_simt(s, false).total;
+    // size for the varlen bound when num_seqs is given, which also covers the fixed-length layout;
+    // the larger of the two paths, so either entry point can use it
+    const size_t a = plan_simt(s, false).total;
+    const size_t b = tc_eligible(s) ? plan_tc_fwd(s).total : 0;
+    return a > b ? a : b;
 }
 
 size_t kda_bwd_workspace_size(const kda_dims* dims, int chunk_size) {
@@ -226,8 +261,19 @@ kda_status kda_fwd(const kda_dims* dims, const void* q, const void* k, const voi
                    const void* beta_raw, const float* a_log, const float* dt_bias, float scale, float lower_bound,
                    int chunk_size, const int32_t* cu_seqlens, const float* initial_state, void* out,
                    float* final_state, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    return kda_fwd_simt(dims, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, chunk_size,
-                        cu_seqlens, initial_state, out, final_state, workspace, workspace_bytes, stream);
+    Shape s;
+    kda_status st = common_checks(dims, chunk_size, cu_seqlens, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale,
+                                  lower_bound, &s);
+    if (st != KDA_OK) return st;
+    if (!out) return KDA_ERR_INVALID_ARG;
+    if (!tc_eligible(s))
+        return kda_fwd_simt(dims, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, chunk_size,
+                            cu_seqlens, initial_state, out, final_state, workspace, workspace_bytes, stream);
+    Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
+                           initial_state);
+    p.out = out;
+    p.ST = final_state;
+    return fwd_tc(s, p, workspace, workspace_bytes, stream);
 }
 
 kda_status kda_bwd(const kda_dims* dims, const void* q, const void* k, const void* v, const void* g_raw,
