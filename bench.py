@@ -59,7 +59,8 @@ def kernel_work(name: str, w, units: float) -> tuple[float, float]:
     table = {
         "kda_intra_simt": (a["fwd_read"], a["intra_flops"]),
         "kda_chain_fwd_simt": (a["fwd_write"], a["chain_flops"]),
-        "kda_fwd_tc": (a["fwd_bytes"], a["fwd_flops"]),
+        "kda_intra_tc": (a["fwd_read"], a["intra_flops"]),
+        "kda_chain_fwd_tc": (a["fwd_write"], a["chain_flops"]),
         "kda_chain_bwd_simt": (2 * w.V, a["chain_flops"]),
         "kda_grad_simt": (a["bwd_bytes"] - 2 * w.V, a["bwd_flops"] - a["chain_flops"]),
     }

@@ -266,11 +266,12 @@ kda_status kda_fwd(const kda_dims* dims, const void* q, const void* k, const voi
                                   lower_bound, &s);
     if (st != KDA_OK) return st;
     if (!out) return KDA_ERR_INVALID_ARG;
-    if (!tc_eligible(s))
-        return kda_fwd_simt(dims, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, chunk_size,
-                            cu_seqlens, initial_state, out, final_state, workspace, workspace_bytes, stream);
     Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
                            initial_state);
+    // the tensor-core path needs 16-byte aligned activations and |lower_bound| <= 5
+    if (!tc_eligible(s) || lower_bound < -5.0f || !tc_inputs_aligned(p))
+        return kda_fwd_simt(dims, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, chunk_size,
+                            cu_seqlens, initial_state, out, final_state, workspace, workspace_bytes, stream);
     p.out = out;
     p.ST = final_state;
     return fwd_tc(s, p, workspace, workspace_bytes, stream);

@@ -76,6 +76,7 @@ cudaError_t launch_grad_simt(const Params& p, cudaStream_t st);
 
 // tensor-core path (bf16, K = V = 128)
 size_t tc_record_bytes(int NCmax, int H);
+bool tc_inputs_aligned(const Params& p);
 cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, cudaStream_t st);
 cudaError_t launch_chain_fwd_tc(const Params& p, const uint8_t* recs, bool store_states, cudaStream_t st);
 

@@ -14,28 +14,36 @@
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
 
+#include <cudaTypedefs.h>
+
 namespace kda {
 
 using namespace sm100;
 
 // ------------------------------------------------------------------ record layout (bytes)
 namespace tcrec {
-constexpr uint32_t WQ = 0;            // [W; Qg]  bf16  128 rows x 128 K, K-major, SBO 2048
-constexpr uint32_t U0 = 32768;        // U0       fp32  4 slices x (64 rows x 32 cols), K-major core, SBO 1024
-constexpr uint32_t KD = 65536;        // Kd^T     tf32  128 rows (c) x 64 K (t), K-major, SBO 2048
-constexpr uint32_t AQ = 98304;        // Aqk      tf32  64 rows (t) x 64 K (s), K-major, SBO 2048
+// One record per (chunk, head), stored in the shared-memory layouts the chain kernel's MMAs read.
+constexpr uint32_t WQ = 0;            // [W; Qg]  bf16, 128 rows x 128 K (c), MN-major: mn_bf16(r, c, 128, 2048)
+constexpr uint32_t U0 = 32768;        // U0       fp32, column-major [128 j][64 t]; slice z = j in [32z, 32z+32)
+constexpr uint32_t KD = 65536;        // Kd^T     tf32, 128 rows (c) x 64 K (t), K-major: km_f32(c, t, 2048, 128)
+constexpr uint32_t AQ = 98304;        // Aqk      tf32, 64 rows (t) x 64 K (s), K-major: km_f32(t, s, 2048, 128)
 constexpr uint32_t GC = 114688;       // exp(Gamma_last) fp32 [128]
 constexpr uint32_t BYTES = 115712;    // record stride (1 KB aligned)
 constexpr uint32_t U0_SLICE = 8192;   // one 32-column slice of U0
 constexpr uint32_t TAIL = BYTES - KD; // KD + AQ + GC, contiguous
 }  // namespace tcrec
 
-// K-major core-matrix offsets: bf16 (8 elements per 16 B row) and 32-bit (4 per row).
-__host__ __device__ __forceinline__ uint32_t off_bf16(int r, int k, uint32_t sbo) {
-    return static_cast<uint32_t>((r >> 3) * sbo + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
+// Core-matrix offsets.  MN-major bf16: 16 B rows hold 8 consecutive M/N elements of one K index.
+// K-major: 16 B rows hold 8 (bf16) or 4 (32-bit) consecutive K elements of one M/N index.
+// mstride / kstride are the byte distances between neighbouring core matrices along M/N and K.
+__host__ __device__ __forceinline__ uint32_t mn_bf16(int r, int k, uint32_t mstride, uint32_t kstride) {
+    return static_cast<uint32_t>((r >> 3) * mstride + (k >> 3) * kstride + (k & 7) * 16 + (r & 7) * 2);
 }
-__host__ __device__ __forceinline__ uint32_t off_f32(int r, int k, uint32_t sbo) {
-    return static_cast<uint32_t>((r >> 3) * sbo + (k >> 2) * 128 + (r & 7) * 16 + (k & 3) * 4);
+__host__ __device__ __forceinline__ uint32_t km_bf16(int r, int k, uint32_t mstride, uint32_t kstride) {
+    return static_cast<uint32_t>((r >> 3) * mstride + (k >> 3) * kstride + (r & 7) * 16 + (k & 7) * 2);
+}
+__host__ __device__ __forceinline__ uint32_t km_f32(int r, int k, uint32_t mstride, uint32_t kstride) {
+    return static_cast<uint32_t>((r >> 3) * mstride + (k >> 2) * kstride + (r & 7) * 16 + (k & 3) * 4);
 }
 
 __device__ __forceinline__ float tf32_rn(float x) {
@@ -44,12 +52,67 @@ __device__ __forceinline__ float tf32_rn(float x) {
     return __uint_as_float(y);
 }
 
-// ------------------------------------------------------------------ intra-chunk record (SIMT math)
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
 
-// One CTA per (chunk, head): the intra-chunk quantities in fp32 (direct exponentials), written as a
-// tensor-core record.  Requires K = V = 128.
-__global__ void __launch_bounds__(256) intra_tcrec_simt_kernel(Params p, uint8_t* recs) {
-    constexpr int K = 128, V = 128, KP = K + 1;
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+    return make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+}
+
+__device__ __forceinline__ float bf16_at(const uint8_t* base, uint32_t byte_off) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(base + byte_off));
+}
+
+// kind::tf32 MMA (A/B format 2 = TF32, f32 accumulate).
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ intra-chunk kernel (tcgen05)
+//
+// One CTA (256 threads) per (chunk, head).  Decay factorisation: inside a chunk, with Gamma_t the
+// cumulative log-decay and 16-token sub-blocks b (Gamma at the end of sub-block b-1 is G_b),
+//   exp(Gamma_t - Gamma_s) = exp(Gamma_t - G_{j+1}) * exp(G_{j+1} - Gamma_s)   for s in sub-block j.
+// The right factor is <= 1; the left is <= 1 for t past sub-block j and <= exp(16 |lower_bound|)
+// inside it, so every factor stays inside fp32/bf16 range for lower_bound >= -5.  Each column
+// sub-block j is one MMA (M = 128: 64 k-rows and 64 q-rows, N = 16, K = 128) with its own left
+// operand L^(j).  The per-token factors are running products of alpha = exp(g) inside each
+// sub-block, so the exponentials per element are exp for the gate sigmoid and exp for alpha.
+namespace intralay {
+constexpr uint32_t RAW_Q = 0, RAW_K = 16384, RAW_G = 32768, RAW_V = 49152;  // TMA tiles [64 t][128 c] bf16
+// Left operands of the A-matrix MMAs, [k rows; q rows] 128 x 128, MN-major mn_bf16(r, c, 128, 2048),
+// as a bf16 hi tile and a bf16 lo tile (v = hi + lo to ~2^-16).  Two pairs ping-pong: pair A lives
+// in its own space, pair B reuses the raw tiles once the element phase has read them.
+constexpr uint32_t LA_HI = 65536, LA_LO = 98304;
+constexpr uint32_t LB_HI = 0, LB_LO = 32768;
+constexpr uint32_t TB_HI = 0, TB_LO = 8192;  // after the A MMAs: T split in bf16, B operand (N = t, K = s), km_bf16(t, s, 1024, 128)
+constexpr uint32_t SL = LA_HI;               // after the A MMAs: fp32 [64][65] Diag(beta) Bkk
+constexpr uint32_t SN = LA_HI + 16640;       // fp32 [64][65] N = (I + L)^-1
+constexpr uint32_t SP = LA_HI + 34816;       // fp32 [3][16][17] scratch of the blocked solve
+constexpr uint32_t RB_HI = 131072, RB_LO = 147456;  // B operand (N = s, K = c) 64 x 128, mn_bf16(s, c, 128, 1024), hi / lo
+constexpr uint32_t KVB = 163840;             // A operand [Kg^T; V^T] 256 x 64 (K = s), km_bf16(r, s, 1024, 128)
+constexpr uint32_t SMALL = 196608;           // rq[64] rk[64] beta[64] dtb[128] blk[4][128] (fp32)
+constexpr uint32_t BAR = SMALL + (64 * 3 + 128 + 512) * 4;
+constexpr uint32_t BYTES = BAR + 64;
+}  // namespace intralay
+
+__global__ void __launch_bounds__(256, 1)
+    intra_tc_kernel(Params p, uint8_t* recs, const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_g,
+                    const __grid_constant__ CUtensorMap tm_v) {
+    using namespace intralay;
+    extern __shared__ __align__(1024) uint8_t smem[];
     const int c = blockIdx.x, h = blockIdx.y;
     if (c >= p.chunk_off[p.N]) return;
     const int n = chunk_segment(p, c);
@@ -57,108 +120,381 @@ __global__ void __launch_bounds__(256) intra_tcrec_simt_kernel(Params p, uint8_t
     const int len = min(kChunk, seg_end(p, n) - tok0);
     const int H = p.H;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    extern __shared__ float sm[];
-    float* sQ = sm;                  // [64][KP] q_hat
-    float* sK = sQ + 64 * KP;        // [64][KP] k_hat
-    float* sG = sK + 64 * KP;        // [64][KP] Gamma
-    float* sE = sG + 64 * KP;        // [64][KP] exp(Gamma)
-    float* sA = sE + 64 * KP;        // [64][65] Aqk
-    float* sB = sA + 64 * 65;        // [64][65] Bkk
-    float* sN = sB + 64 * 65;        // [64][65] N
-    float* sb = sN + 64 * 65;        // [64] beta
-    if (tid < kChunk) {
-        float b = 0.f;
-        if (tid < len) b = sigmoidf_acc(load_act(p.beta_raw, (size_t)(tok0 + tid) * H + h, p.dtype));
-        sb[tid] = b;
+    float* rq = reinterpret_cast<float*>(smem + SMALL);
+    float* rk = rq + 64;
+    float* sbeta = rk + 64;
+    float* sdtb = sbeta + 64;
+    float* sblk = sdtb + 128;
+    // Each MMA barrier has at most one pending phase at any time, so parity waits are unambiguous.
+    uint64_t* bar_load = reinterpret_cast<uint64_t*>(smem + BAR);
+    uint64_t* bar_a = bar_load + 1;   // MMAs reading tile pair A (and the final W / U0 MMAs)
+    uint64_t* bar_b = bar_load + 2;   // MMAs reading tile pair B
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_load + 3);
+    uint8_t* rec = recs + ((size_t)c * H + h) * tcrec::BYTES;
+
+    if (tid == 0) {
+        mbar_init(bar_load, 1);
+        mbar_init(bar_a, 1);
+        mbar_init(bar_b, 1);
+        mbar_fence_init();
+        mbar_expect_tx(bar_load, 4 * 16384);
+        tma_load_3d(smem + RAW_Q, &tm_q, 0, h, tok0, bar_load);
+        tma_load_3d(smem + RAW_K, &tm_k, 0, h, tok0, bar_load);
+        tma_load_3d(smem + RAW_G, &tm_g, 0, h, tok0, bar_load);
+        tma_load_3d(smem + RAW_V, &tm_v, 0, h, tok0, bar_load);
     }
-    for (int t = warp; t < kChunk; t += 8) {
-        const size_t base = ((size_t)(tok0 + t) * H + h) * K;
-        float qv[4], kv[4], sq = 0.f, sk = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int cc = lane + 32 * i;
-            qv[i] = t < len ? load_act(p.q, base + cc, p.dtype) : 0.f;
-            kv[i] = t < len ? load_act(p.k, base + cc, p.dtype) : 0.f;
-            sq += qv[i] * qv[i];
-            sk += kv[i] * kv[i];
-        }
+    if (warp == 0) tmem_alloc(tslot, 256);
+    if (tid < 128) sdtb[tid] = p.dt_bias[h * 128 + tid];
+    if (tid < 64) sbeta[tid] = tid < len ? sigmoidf_acc(load_act(p.beta_raw, (size_t)(tok0 + tid) * H + h, KDA_BF16)) : 0.f;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    uint32_t par_a = 0, par_b = 0;
+    bool ok = __syncthreads_and(mbar_wait(bar_load, 0) ? 1 : 0) != 0;
+    if (!ok) goto fail;
+
+    // ---- per-token inverse norms (warp w: tokens 8w .. 8w+7)
+    for (int u = 0; u < 8; ++u) {
+        const int t = warp * 8 + u;
+        const uint2 qv = *reinterpret_cast<const uint2*>(smem + RAW_Q + t * 256 + lane * 8);
+        const uint2 kv = *reinterpret_cast<const uint2*>(smem + RAW_K + t * 256 + lane * 8);
+        const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv.x));
+        const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv.y));
+        const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.x));
+        const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.y));
+        float sq = q0.x * q0.x + q0.y * q0.y + q1.x * q1.x + q1.y * q1.y;
+        float sk = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
         sq = warp_sum(sq);
         sk = warp_sum(sk);
-        const float rq = 1.0f / sqrtf(sq + kNormEps), rk = 1.0f / sqrtf(sk + kNormEps);
+        if (lane == 0) {
+            rq[t] = t < len ? 1.0f / sqrtf(sq + kNormEps) : 0.f;
+            rk[t] = t < len ? 1.0f / sqrtf(sk + kNormEps) : 0.f;
+        }
+    }
+    __syncthreads();
+
+    {
+        // ---- element phase: thread owns channels cp and cp + 64 of sub-block bi (16 tokens)
+        const int cp = tid & 63, bi = tid >> 6, t0 = 16 * bi;
+        const float ea = __expf(p.a_log[h]);
+        float kx[2][16], qx[2][16], y[2][16], fj[2][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            sQ[t * KP + lane + 32 * i] = qv[i] * rq;
-            sK[t * KP + lane + 32 * i] = kv[i] * rk;
-        }
-    }
-    const float ea = expf(p.a_log[h]);
-    for (int i = tid; i < kChunk * K; i += blockDim.x) {
-        const int t = i / K, cc = i % K;
-        float g = 0.f;
-        if (t < len) {
-            const float x = load_act(p.g_raw, ((size_t)(tok0 + t) * H + h) * K + cc, p.dtype);
-            g = p.lb * sigmoidf_acc(ea * (x + p.dt_bias[h * K + cc]));
-        }
-        sG[t * KP + cc] = g;
-    }
-    __syncthreads();
-    for (int cc = tid; cc < K; cc += blockDim.x) {
-        float acc = 0.f;
-        for (int t = 0; t < kChunk; ++t) {
-            acc += sG[t * KP + cc];
-            sG[t * KP + cc] = acc;
-            sE[t * KP + cc] = expf(acc);
-        }
-    }
-    __syncthreads();
-    for (int i = tid; i < kChunk * kChunk; i += blockDim.x) {
-        const int t = i >> 6, s = i & 63;
-        float aq = 0.f, ak = 0.f;
-        if (s <= t) {
-            for (int cc = 0; cc < K; ++cc) {
-                const float e = expf(sG[t * KP + cc] - sG[s * KP + cc]);
-                const float ks = sK[s * KP + cc] * e;
-                aq += sQ[t * KP + cc] * ks;
-                ak += sK[t * KP + cc] * ks;
+        for (int ci = 0; ci < 2; ++ci) {
+            const int cc = cp + 64 * ci;
+            const float dtb = sdtb[cc];
+            float a[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int t = t0 + u;
+                const uint32_t o = t * 256 + cc * 2;
+                kx[ci][u] = bf16_at(smem + RAW_K, o) * rk[t];
+                qx[ci][u] = bf16_at(smem + RAW_Q, o) * rq[t];
+                float g = 0.f;
+                if (t < len) g = p.lb * __fdividef(1.f, 1.f + __expf(-ea * (bf16_at(smem + RAW_G, o) + dtb)));
+                a[u] = __expf(g);
+            }
+            float run = 1.f;
+#pragma unroll
+            for (int u = 15; u >= 0; --u) {     // y_t = prod_{v > t} alpha_v  (= exp(G_{b+1} - Gamma_t))
+                y[ci][u] = run;
+                run *= a[u];
+            }
+            sblk[bi * 128 + cc] = run;           // sub-block total exp(G_{b+1} - G_b)
+            // R_b = k * y, split into bf16 hi + lo
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float hi[8], lo[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float r = kx[ci][8 * hh + e] * y[ci][8 * hh + e];
+                    hi[e] = __bfloat162float(__float2bfloat16_rn(r));
+                    lo[e] = r - hi[e];
+                }
+                *reinterpret_cast<uint4*>(smem + RB_HI + mn_bf16(t0 + 8 * hh, cc, 128, 1024)) = pack8_bf16(hi);
+                *reinterpret_cast<uint4*>(smem + RB_LO + mn_bf16(t0 + 8 * hh, cc, 128, 1024)) = pack8_bf16(lo);
+            }
+            run = 1.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {      // x_t = prod_{v <= t} alpha_v  (= exp(Gamma_t - G_b))
+                run *= a[u];
+                kx[ci][u] *= run;
+                qx[ci][u] *= run;
+            }
+            // V^T rows 128 + cc of the [Kg^T; V^T] operand: an exact copy of v (zero past the segment)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float vv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int t = t0 + 8 * hh + e;
+                    vv[e] = t < len ? bf16_at(smem + RAW_V, t * 256 + cc * 2) : 0.f;
+                }
+                *reinterpret_cast<uint4*>(smem + KVB + km_bf16(128 + cc, t0 + 8 * hh, 1024, 128)) = pack8_bf16(vv);
             }
         }
-        sA[t * 65 + s] = aq;
-        sB[t * 65 + s] = (s < t) ? ak : 0.f;
-        sN[t * 65 + s] = (s == t) ? 1.f : 0.f;
+        __syncthreads();
+        // cross-sub-block factors per channel
+#pragma unroll
+        for (int ci = 0; ci < 2; ++ci) {
+            const int cc = cp + 64 * ci;
+            const float B0 = sblk[cc], B1 = sblk[128 + cc], B2 = sblk[256 + cc], B3 = sblk[384 + cc];
+            const float eG = bi == 0 ? 1.f : bi == 1 ? B0 : bi == 2 ? B0 * B1 : B0 * B1 * B2;      // exp(G_b)
+            const float tail = bi == 0 ? B1 * B2 * B3 : bi == 1 ? B2 * B3 : bi == 2 ? B3 : 1.f;   // exp(Gamma_C - G_{b+1})
+            const float Bi = bi == 0 ? B0 : bi == 1 ? B1 : bi == 2 ? B2 : B3;
+            const float fd = 1.f / Bi;                                   // j == b
+            const float fm2 = bi >= 2 ? (bi == 2 ? B1 : B2) : 0.f;       // j == b - 2
+            const float fm3 = bi == 3 ? B1 * B2 : 0.f;                   // j == b - 3
+            // factor of L^(j) = exp(Gamma_t - G_{j+1}) / x_t for j = 0..3 (zero for j > b)
+            fj[ci][0] = bi == 0 ? fd : bi == 1 ? 1.f : bi == 2 ? fm2 : fm3;
+            fj[ci][1] = bi == 1 ? fd : bi == 2 ? 1.f : bi == 3 ? fm2 : 0.f;
+            fj[ci][2] = bi == 2 ? fd : bi == 3 ? 1.f : 0.f;
+            fj[ci][3] = bi == 3 ? fd : 0.f;
+            if (bi == 0) reinterpret_cast<float*>(rec + tcrec::GC)[cc] = B0 * B1 * B2 * B3;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int tb = t0 + 8 * hh;
+                float vk[8], vq[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { vk[e] = kx[ci][8 * hh + e] * eG; vq[e] = qx[ci][8 * hh + e] * eG; }
+                *reinterpret_cast<uint4*>(smem + KVB + km_bf16(cc, tb, 1024, 128)) = pack8_bf16(vk);
+                *reinterpret_cast<uint4*>(rec + tcrec::WQ + mn_bf16(64 + tb, cc, 128, 2048)) = pack8_bf16(vq);
+            }
+            // Kd^T (tf32): k * exp(Gamma_C - Gamma_t), four tokens per 16 B
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd) {
+                const int u = 4 * qd;
+                float kb[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) kb[e] = bf16_at(smem + RAW_K, (t0 + u + e) * 256 + cc * 2) * rk[t0 + u + e];
+                const float4 v4 = make_float4(tf32_rn(kb[0] * y[ci][u] * tail), tf32_rn(kb[1] * y[ci][u + 1] * tail),
+                                              tf32_rn(kb[2] * y[ci][u + 2] * tail), tf32_rn(kb[3] * y[ci][u + 3] * tail));
+                *reinterpret_cast<float4*>(rec + tcrec::KD + km_f32(cc, t0 + u, 2048, 128)) = v4;
+            }
+        }
+        // L^(j) rows of this thread's sub-block (k rows t, q rows 64 + t), split into bf16 hi + lo
+        auto write_L = [&](int j, uint32_t hi_off, uint32_t lo_off) {
+            if (bi < j) return;
+#pragma unroll
+            for (int ci = 0; ci < 2; ++ci) {
+                const int cc = cp + 64 * ci;
+                const float f = fj[ci][0] * (j == 0) + fj[ci][1] * (j == 1) + fj[ci][2] * (j == 2) + fj[ci][3] * (j == 3);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int tb = t0 + 8 * hh;
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+                        float hi[8], lo[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float v = (part == 0 ? kx[ci][8 * hh + e] : qx[ci][8 * hh + e]) * f;
+                            hi[e] = __bfloat162float(__float2bfloat16_rn(v));
+                            lo[e] = v - hi[e];
+                        }
+                        const uint32_t o = mn_bf16(64 * part + tb, cc, 128, 2048);
+                        *reinterpret_cast<uint4*>(smem + hi_off + o) = pack8_bf16(hi);
+                        *reinterpret_cast<uint4*>(smem + lo_off + o) = pack8_bf16(lo);
+                    }
+                }
+            }
+        };
+        // A-matrix MMAs of column sub-block j: D_j = L_hi R_hi + L_hi R_lo + L_lo R_hi
+        constexpr uint32_t idA = idesc_bf16(128, 16, 1, 1);
+        auto issue_A = [&](int j, uint32_t hi_off, uint32_t lo_off, uint64_t* bar) {
+            const uint32_t lh = smem_u32(smem + hi_off), ll = smem_u32(smem + lo_off);
+            const uint32_t rh = smem_u32(smem + RB_HI) + j * 256, rl = smem_u32(smem + RB_LO) + j * 256;
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16(tmem + 16 * j, smem_desc(lh + kk * 4096, 2048, 128), smem_desc(rh + kk * 2048, 1024, 128), idA, kk > 0);
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16(tmem + 16 * j, smem_desc(lh + kk * 4096, 2048, 128), smem_desc(rl + kk * 2048, 1024, 128), idA, 1);
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16(tmem + 16 * j, smem_desc(ll + kk * 4096, 2048, 128), smem_desc(rh + kk * 2048, 1024, 128), idA, 1);
+            mma_commit(bar);
+        };
+        auto wait_on = [&](uint64_t* bar, uint32_t& par) -> bool {
+            const bool r = __syncthreads_and(mbar_wait(bar, par) ? 1 : 0) != 0;
+            par ^= 1;
+            return r;
+        };
+        write_L(0, LA_HI, LA_LO);
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();                 // raw tiles are no longer read past this point
+        tc_fence_after();
+        if (tid == 0) issue_A(0, LA_HI, LA_LO, bar_a);
+        write_L(1, LB_HI, LB_LO);
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) issue_A(1, LB_HI, LB_LO, bar_b);
+        if (!wait_on(bar_a, par_a)) goto fail;      // pair A free again
+        tc_fence_after();
+        write_L(2, LA_HI, LA_LO);
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) issue_A(2, LA_HI, LA_LO, bar_a);
+        if (!wait_on(bar_b, par_b)) goto fail;      // pair B free again
+        tc_fence_after();
+        write_L(3, LB_HI, LB_LO);
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) issue_A(3, LB_HI, LB_LO, bar_b);
+        if (!wait_on(bar_a, par_a)) goto fail;
+        if (!wait_on(bar_b, par_b)) goto fail;
+        tc_fence_after();
     }
-    __syncthreads();
-    for (int t = 1; t < kChunk; ++t) {
-        if (tid < t) {
-            float acc = 0.f;
-            for (int r = tid; r < t; ++r) acc += sB[t * 65 + r] * sN[r * 65 + tid];
-            sN[t * 65 + tid] = -sb[t] * acc;
+
+    {
+        // ---- read the A-matrices: lanes 0-63 hold Bkk rows, lanes 64-127 hold Aqk rows
+        float* SLf = reinterpret_cast<float*>(smem + SL);
+        float* SNf = reinterpret_cast<float*>(smem + SN);
+        float* SPf = reinterpret_cast<float*>(smem + SP);
+        if (warp < 4) {
+            float d[64];
+            const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+            tmem_ld16(tmem + lb, d);
+            tmem_ld16(tmem + lb + 16, d + 16);
+            tmem_ld16(tmem + lb + 32, d + 32);
+            tmem_ld16(tmem + lb + 48, d + 48);
+            tmem_ld_wait();
+            if (warp < 2) {
+                const int t = tid;
+                const float bt = sbeta[t];
+#pragma unroll
+                for (int s2 = 0; s2 < 64; ++s2) SLf[t * 65 + s2] = s2 < t ? bt * d[s2] : 0.f;
+            } else {
+                const int t = tid - 64;
+#pragma unroll
+                for (int s4 = 0; s4 < 64; s4 += 4) {
+                    float4 v4;
+                    v4.x = tf32_rn(s4 <= t ? d[s4] : 0.f);
+                    v4.y = tf32_rn(s4 + 1 <= t ? d[s4 + 1] : 0.f);
+                    v4.z = tf32_rn(s4 + 2 <= t ? d[s4 + 2] : 0.f);
+                    v4.w = tf32_rn(s4 + 3 <= t ? d[s4 + 3] : 0.f);
+                    *reinterpret_cast<float4*>(rec + tcrec::AQ + km_f32(t, s4, 2048, 128)) = v4;
+                }
+            }
         }
         __syncthreads();
+        // ---- N = (I + L)^-1, blocked: 16x16 diagonal blocks by forward substitution, then the
+        // off-diagonal blocks N_ij = -N_ii sum_{m=j}^{i-1} L_im N_mj by increasing i - j.
+        if (warp < 4 && lane < 16) {
+            const int b = warp, s2 = lane;
+            float col[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m < r; ++m) acc += SLf[(16 * b + r) * 65 + 16 * b + m] * col[m];
+                col[r] = r == s2 ? 1.f : (r > s2 ? -acc : 0.f);
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) SNf[(16 * b + r) * 65 + 16 * b + s2] = col[r];
+        }
+        __syncthreads();
+        for (int d = 1; d < 4; ++d) {
+            const int r = tid >> 4, s2 = tid & 15;
+            for (int b = 0; b + d < 4; ++b) {
+                const int i = b + d, j = b;
+                float acc = 0.f;
+                for (int m = j; m < i; ++m)
+#pragma unroll
+                    for (int qq = 0; qq < 16; ++qq)
+                        acc += SLf[(16 * i + r) * 65 + 16 * m + qq] * SNf[(16 * m + qq) * 65 + 16 * j + s2];
+                SPf[(b * 16 + r) * 17 + s2] = acc;
+            }
+            __syncthreads();
+            for (int b = 0; b + d < 4; ++b) {
+                const int i = b + d, j = b;
+                float acc = 0.f;
+#pragma unroll
+                for (int qq = 0; qq < 16; ++qq) acc += SNf[(16 * i + r) * 65 + 16 * i + qq] * SPf[(b * 16 + qq) * 17 + s2];
+                SNf[(16 * i + r) * 65 + 16 * j + s2] = -acc;
+            }
+            __syncthreads();
+        }
+        // ---- T = N Diag(beta), split into bf16 hi + lo, as the B operand (N = t, K = s)
+        {
+            const int t = tid >> 2, sq = (tid & 3) * 16;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float hi[8], lo[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int s2 = sq + 8 * hh + e;
+                    const float tv = s2 <= t ? SNf[t * 65 + s2] * sbeta[s2] : 0.f;
+                    hi[e] = __bfloat162float(__float2bfloat16_rn(tv));
+                    lo[e] = tv - hi[e];
+                }
+                *reinterpret_cast<uint4*>(smem + TB_HI + km_bf16(t, sq + 8 * hh, 1024, 128)) = pack8_bf16(hi);
+                *reinterpret_cast<uint4*>(smem + TB_LO + km_bf16(t, sq + 8 * hh, 1024, 128)) = pack8_bf16(lo);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // ---- W^T = Kg^T T^T and U0^T = V^T (T_hi + T_lo)^T   (M = 128, N = 64, K = 64)
+        constexpr uint32_t idW = idesc_bf16(128, 64, 0, 0);
+        if (tid == 0) {
+            const uint32_t kvb = smem_u32(smem + KVB), thi = smem_u32(smem + TB_HI), tlo = smem_u32(smem + TB_LO);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tmem + 64, smem_desc(kvb + kk * 256, 128, 1024), smem_desc(thi + kk * 256, 128, 1024), idW, kk > 0);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tmem + 128, smem_desc(kvb + 16384 + kk * 256, 128, 1024), smem_desc(thi + kk * 256, 128, 1024),
+                         idW, kk > 0);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tmem + 128, smem_desc(kvb + 16384 + kk * 256, 128, 1024), smem_desc(tlo + kk * 256, 128, 1024),
+                         idW, 1);
+            mma_commit(bar_a);
+        }
+        ok = __syncthreads_and(mbar_wait(bar_a, par_a) ? 1 : 0) != 0;
+        par_a ^= 1;
+        if (!ok) goto fail;
+        tc_fence_after();
+        // ---- record W (MN-major, thread = channel) and U0 (column-major, thread = value column)
+        {
+            const uint32_t lb = static_cast<uint32_t>((warp & 3) * 32) << 16;
+            float d[64];
+            const uint32_t col = warp < 4 ? 64u : 128u;
+            tmem_ld16(tmem + lb + col, d);
+            tmem_ld16(tmem + lb + col + 16, d + 16);
+            tmem_ld16(tmem + lb + col + 32, d + 32);
+            tmem_ld16(tmem + lb + col + 48, d + 48);
+            tmem_ld_wait();
+            if (warp < 4) {
+                const int cc = tid;
+#pragma unroll
+                for (int tb = 0; tb < 64; tb += 8)
+                    *reinterpret_cast<uint4*>(rec + tcrec::WQ + mn_bf16(tb, cc, 128, 2048)) = pack8_bf16(d + tb);
+            } else {
+                const int j = tid - 128;
+                float4* dst = reinterpret_cast<float4*>(rec + tcrec::U0 + j * 256);
+#pragma unroll
+                for (int t4 = 0; t4 < 16; ++t4) dst[t4] = make_float4(d[4 * t4], d[4 * t4 + 1], d[4 * t4 + 2], d[4 * t4 + 3]);
+            }
+        }
     }
-    uint8_t* rec = recs + ((size_t)c * H + h) * tcrec::BYTES;
-    for (int i = tid; i < kChunk * K; i += blockDim.x) {
-        const int t = i / K, cc = i % K;
-        float w = 0.f;
-        for (int s = 0; s <= t; ++s) w += sN[t * 65 + s] * sb[s] * sK[s * KP + cc] * sE[s * KP + cc];
-        *reinterpret_cast<__nv_bfloat16*>(rec + tcrec::WQ + off_bf16(t, cc, 2048)) = __float2bfloat16_rn(w);
-        *reinterpret_cast<__nv_bfloat16*>(rec + tcrec::WQ + off_bf16(64 + t, cc, 2048)) =
-            __float2bfloat16_rn(sQ[t * KP + cc] * sE[t * KP + cc]);
-        const float kd = sK[t * KP + cc] * expf(sG[63 * KP + cc] - sG[t * KP + cc]);
-        *reinterpret_cast<float*>(rec + tcrec::KD + off_f32(cc, t, 2048)) = tf32_rn(kd);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+    return;
+fail:
+    // A wait gave up: record it, give outstanding copies / MMAs a bounded chance to land, release TMEM.
+    if (tid == 0) {
+        record_error(p.status, KDA_ERR_TIMEOUT);
+        mbar_wait(bar_load, 0, 1u << 16);
+        mbar_wait(bar_a, par_a, 1u << 16);
+        mbar_wait(bar_b, par_b, 1u << 16);
     }
-    for (int i = tid; i < kChunk * V; i += blockDim.x) {
-        const int t = i / V, j = i % V;
-        float acc = 0.f;
-        for (int s = 0; s <= t && s < len; ++s)
-            acc += sN[t * 65 + s] * sb[s] * load_act(p.v, ((size_t)(tok0 + s) * H + h) * V + j, p.dtype);
-        *reinterpret_cast<float*>(rec + tcrec::U0 + (j >> 5) * tcrec::U0_SLICE + off_f32(t, j & 31, 1024)) = acc;
-    }
-    for (int i = tid; i < kChunk * kChunk; i += blockDim.x) {
-        const int t = i >> 6, s = i & 63;
-        *reinterpret_cast<float*>(rec + tcrec::AQ + off_f32(t, s, 2048)) = tf32_rn(sA[t * 65 + s]);
-    }
-    for (int cc = tid; cc < K; cc += blockDim.x)
-        reinterpret_cast<float*>(rec + tcrec::GC)[cc] = sE[63 * KP + cc];
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // ------------------------------------------------------------------ state chain (tcgen05)
@@ -170,24 +506,16 @@ constexpr uint32_t SLOT_KD = 40960;       // KD, AQ, GC follow contiguously (tcr
 constexpr uint32_t SLOT_AQ = SLOT_KD + (tcrec::AQ - tcrec::KD);
 constexpr uint32_t SLOT_GC = SLOT_KD + (tcrec::GC - tcrec::KD);
 constexpr uint32_t SLOT_BYTES = (SLOT_KD + tcrec::TAIL + 1023) / 1024 * 1024;
-constexpr uint32_t SB = 2 * SLOT_BYTES;   // S as bf16 B operand: 32 rows (j) x 128 K (c), SBO 2048
-constexpr uint32_t UB = SB + 8192;        // U as tf32 B operand: 32 rows (j) x 64 K (t), SBO 2048
-constexpr uint32_t BAR = UB + 8192;       // mbarriers: full[2], mma
+constexpr uint32_t SB = 2 * SLOT_BYTES;   // S as bf16 B operand (N = j, K = c), MN-major: mn_bf16(j, c, 128, 512)
+constexpr uint32_t UB = SB + 8192;        // U as tf32 B operand (N = j, K = t), K-major, padded: km_f32(j, t, 2304, 144)
+constexpr uint32_t UB_LBO = 144, UB_SBO = 2304;
+constexpr uint32_t BAR = UB + 4 * UB_SBO; // mbarriers: full[2], mma
 constexpr uint32_t TSLOT = BAR + 64;
 constexpr uint32_t BYTES = TSLOT + 64;
 }  // namespace chainlay
 
-constexpr uint32_t kIdescWS = idesc_bf16(128, 32, 0, 0);
-// kind::tf32: A/B format 2 (TF32), f32 accumulate.
-constexpr uint32_t kIdescTF32 = (1u << 4) | (2u << 7) | (2u << 10) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
-
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
-}
+constexpr uint32_t kIdescWS = idesc_bf16(128, 32, 1, 1);   // [W; Qg] and S both MN-major
+constexpr uint32_t kIdescTF32 = idesc_tf32(128, 32);
 
 // Issue the bulk loads of chunk record `c` (head h, slice z) into slot smem.
 __device__ __forceinline__ void chain_load(uint8_t* slot, const uint8_t* rec, int z, uint64_t* bar) {
@@ -238,8 +566,7 @@ __global__ void __launch_bounds__(128, 1) chain_fwd_tc_kernel(Params p, const ui
             chain_load(smem + i * chainlay::SLOT_BYTES, recs + ((size_t)(cb + i) * H + h) * tcrec::BYTES, z, &full[i]);
     }
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-        *reinterpret_cast<__nv_bfloat16*>(SB + off_bf16(j, tid, 2048)) = __float2bfloat16_rn(S[j]);
+    for (int jg = 0; jg < 4; ++jg) *reinterpret_cast<uint4*>(SB + mn_bf16(8 * jg, tid, 128, 512)) = pack8_bf16(S + 8 * jg);
     fence_async_smem();
     __syncthreads();
 
@@ -265,8 +592,8 @@ __global__ void __launch_bounds__(128, 1) chain_fwd_tc_kernel(Params p, const ui
         if (tid == 0) {
             tc_fence_after();
             for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t a = smem_desc(smem_u32(sl + chainlay::SLOT_WQ) + kk * 256, 128, 2048);
-                const uint64_t b = smem_desc(smem_u32(SB) + kk * 256, 128, 2048);
+                const uint64_t a = smem_desc(smem_u32(sl + chainlay::SLOT_WQ) + kk * 4096, 2048, 128);
+                const uint64_t b = smem_desc(smem_u32(SB) + kk * 1024, 512, 128);
                 mma_bf16(tD1, a, b, kIdescWS, kk > 0);
             }
             mma_commit(mbar_mma);
@@ -280,14 +607,25 @@ __global__ void __launch_bounds__(128, 1) chain_fwd_tc_kernel(Params p, const ui
             tmem_ld16(tD1 + lane_base, d);
             tmem_ld16(tD1 + lane_base + 16, d + 16);
             tmem_ld_wait();
-            const uint8_t* u0 = sl + chainlay::SLOT_U0;
+            // U0 slice is column-major [32 j][64 t]; U rounded to tf32, then 4x4 transposes inside each
+            // lane quad give 16-byte rows of the K-major (t-contiguous) B operand.
+            const float* u0 = reinterpret_cast<const float*>(sl + chainlay::SLOT_U0);
+            float u[32];
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                const float4 u = *reinterpret_cast<const float4*>(u0 + off_f32(tid, j, 1024));
-                const float uu[4] = {u.x - d[j], u.y - d[j + 1], u.z - d[j + 2], u.w - d[j + 3]};
+            for (int j = 0; j < 32; ++j) u[j] = tf32_rn(u0[j * 64 + tid] - d[j]);
+            const int r = tid & 3;
+            const bool top = (r & 2) == 0, even = (r & 1) == 0;
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    *reinterpret_cast<float*>(UB + off_f32(j + e, tid, 2048)) = tf32_rn(uu[e]);
+            for (int b = 0; b < 8; ++b) {
+                float v0 = u[4 * b], v1 = u[4 * b + 1], v2 = u[4 * b + 2], v3 = u[4 * b + 3];
+                const float s0 = top ? v2 : v0, s1 = top ? v3 : v1;
+                const float g0 = __shfl_xor_sync(0xffffffffu, s0, 2), g1 = __shfl_xor_sync(0xffffffffu, s1, 2);
+                if (top) { v2 = g0; v3 = g1; } else { v0 = g0; v1 = g1; }
+                const float e0 = even ? v1 : v0, e1 = even ? v3 : v2;
+                const float h0 = __shfl_xor_sync(0xffffffffu, e0, 1), h1 = __shfl_xor_sync(0xffffffffu, e1, 1);
+                if (even) { v1 = h0; v3 = h1; } else { v0 = h0; v2 = h1; }
+                *reinterpret_cast<float4*>(UB + km_f32(4 * b + r, tid - r, chainlay::UB_SBO, chainlay::UB_LBO)) =
+                    make_float4(v0, v1, v2, v3);
             }
         }
         fence_async_smem();
@@ -297,7 +635,7 @@ __global__ void __launch_bounds__(128, 1) chain_fwd_tc_kernel(Params p, const ui
         if (tid == 0) {
             tc_fence_after();
             for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t b = smem_desc(smem_u32(UB) + kk * 256, 128, 2048);
+                const uint64_t b = smem_desc(smem_u32(UB) + kk * 2 * chainlay::UB_LBO, chainlay::UB_LBO, chainlay::UB_SBO);
                 const uint64_t a1 = smem_desc(smem_u32(sl + chainlay::SLOT_AQ) - 16384 + kk * 256, 128, 2048);
                 mma_tf32(tD1, a1, b, kIdescTF32, 1);
                 const uint64_t a2 = smem_desc(smem_u32(sl + chainlay::SLOT_KD) + kk * 256, 128, 2048);
@@ -338,10 +676,10 @@ __global__ void __launch_bounds__(128, 1) chain_fwd_tc_kernel(Params p, const ui
             tmem_ld16(tD3 + lane_base + 16, d + 16);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                S[j] = gc * S[j] + d[j];
-                *reinterpret_cast<__nv_bfloat16*>(SB + off_bf16(j, tid, 2048)) = __float2bfloat16_rn(S[j]);
-            }
+            for (int j = 0; j < 32; ++j) S[j] = gc * S[j] + d[j];
+#pragma unroll
+            for (int jg = 0; jg < 4; ++jg)
+                *reinterpret_cast<uint4*>(SB + mn_bf16(8 * jg, tid, 128, 512)) = pack8_bf16(S + 8 * jg);
         }
         fence_async_smem();
         tc_fence_before();
@@ -372,12 +710,48 @@ __global__ void __launch_bounds__(128, 1) chain_fwd_tc_kernel(Params p, const ui
 
 size_t tc_record_bytes(int NCmax, int H) { return (size_t)NCmax * H * tcrec::BYTES; }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time libcuda dependency).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// [TT tokens][H heads][128 channels] bf16 -> boxes of 64 tokens x 1 head x 128 channels (row-major in smem).
+static bool head_tile_map(CUtensorMap* m, const void* base, int H, int TT) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)TT};
+    cuuint64_t strides[2] = {128 * 2, (cuuint64_t)H * 128 * 2};
+    cuuint32_t box[3] = {128, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tc_inputs_aligned(const Params& p) {
+    auto al = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
+    return al(p.q) && al(p.k) && al(p.g_raw) && al(p.v);
+}
+
 cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, cudaStream_t st) {
-    const size_t smem = (size_t)(4 * 64 * 129 + 3 * 64 * 65 + 64) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(intra_tcrec_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    CUtensorMap mq, mk, mg, mv;
+    if (!head_tile_map(&mq, p.q, p.H, p.TT) || !head_tile_map(&mk, p.k, p.H, p.TT) ||
+        !head_tile_map(&mg, p.g_raw, p.H, p.TT) || !head_tile_map(&mv, p.v, p.H, p.TT))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)intralay::BYTES);
     if (e != cudaSuccess) return e;
     timing_pre(st, K_INTRA_TC);
-    intra_tcrec_simt_kernel<<<dim3(p.NCmax, p.H), 256, smem, st>>>(p, recs);
+    intra_tc_kernel<<<dim3(p.NCmax, p.H), 256, intralay::BYTES, st>>>(p, recs, mq, mk, mg, mv);
     timing_post(st);
     return cudaGetLastError();
 }
