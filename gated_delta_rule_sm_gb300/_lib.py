@@ -23,7 +23,8 @@ KDA_BF16, KDA_FP32 = 0, 1
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_fwd_workspace_size", "kda_bwd_workspace_size", "kda_fwd", "kda_fwd_simt", "kda_bwd",
            "kda_status_string", "kda_device_status", "kda_version", "kda_timing_begin", "kda_timing_end",
-           "kda_kernel_name")
+           "kda_kernel_name", "kda_fwd_noalloc")
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class KdaDims(ctypes.Structure):
@@ -63,6 +64,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             f = getattr(lib, name)
             f.restype = ctypes.c_int
             f.argtypes = fwd_args
+        lib.kda_fwd_noalloc.restype = ctypes.c_int
+        lib.kda_fwd_noalloc.argtypes = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int] + \
+            [_vp] * 4 + [_vp]
         lib.kda_bwd.restype = ctypes.c_int
         lib.kda_bwd.argtypes = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int] + \
             [_vp] * 2 + [_vp] * 2 + [_vp] * 8 + [_vp, ctypes.c_size_t, _vp]

@@ -132,6 +132,31 @@ const char* kda_status_string(kda_status s);
  * the device.  reset != 0 clears the word afterwards. */
 kda_status kda_device_status(int reset);
 
+/*
+ * Forward without a caller-provided workspace (no counterpart in the paper: an
+ * integration aid).  Some callers cannot allocate device memory: plugin
+ * hosts that own every device allocation and give their plugins no
+ * allocator, and latency-critical loops that must not call cudaMalloc
+ * because it can synchronise the device.  kda_fwd_noalloc takes the same
+ * arguments as kda_fwd minus the workspace and uses a scratch array built
+ * into this library instead: KDA_NOALLOC_SCRATCH_BYTES (32 MiB) of device
+ * memory, held by every GPU that loads the library until the process exits.
+ * It allocates nothing (no cudaMalloc / cudaFree, no allocating library
+ * call).  Shapes whose workspace (kda_fwd_workspace_size) exceeds that size
+ * return KDA_ERR_WORKSPACE.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  All calls share the one
+ * array: calls that overlap on the GPU (different streams, or several host
+ * threads) race and must be serialised by the caller.  No scratch content
+ * needs to start at zero (every call rewrites what it reads).
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (32u << 20)
+kda_status kda_fwd_noalloc(const kda_dims* dims,
+                           const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
+                           const float* a_log, const float* dt_bias, float scale, float lower_bound, int chunk_size,
+                           const int32_t* cu_seqlens, const float* initial_state,
+                           void* out, float* final_state, cudaStream_t stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int kda_version(void);
 
