@@ -86,6 +86,21 @@ static TcPlan plan_tc_fwd(const Shape& s) {
     return w;
 }
 
+struct TcBwdPlan {
+    WsPlan simt;        // chunk table, fp32 backward records, states, partials, scratch
+    size_t off_tcrec;   // tensor-core forward records (recompute chain)
+    size_t total;
+};
+
+static TcBwdPlan plan_tc_bwd(const Shape& s) {
+    TcBwdPlan w;
+    w.simt = plan_simt(s, true);
+    size_t o = w.simt.total;
+    w.off_tcrec = o; o = align_up(o + tc_record_bytes(s.NCmax, s.H));
+    w.total = o;
+    return w;
+}
+
 static kda_status status_ptr(int** out) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return KDA_ERR_CUDA;
@@ -195,7 +210,8 @@ static void timing_release() {
 
 static const char* kKernelNames[] = {"kda_plan",          "kda_intra_simt",   "kda_chain_fwd_simt",
                                      "kda_chain_bwd_simt", "kda_grad_simt",    "kda_param_reduce",
-                                     "kda_empty_segment", "kda_intra_tc",     "kda_chain_fwd_tc"};
+                                     "kda_empty_segment", "kda_intra_tc",     "kda_chain_fwd_tc",
+                                     "kda_grad_tc"};
 
 static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cudaStream_t stream) {
     const TcPlan w = plan_tc_fwd(s);
@@ -207,7 +223,7 @@ static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cu
     p.chunk_off = reinterpret_cast<int32_t*>(b + w.off_chunk);
     uint8_t* recs = reinterpret_cast<uint8_t*>(b + w.off_rec);
     KDA_TRY_CUDA(launch_plan(p, stream));
-    KDA_TRY_CUDA(launch_intra_tc(p, recs, stream));
+    KDA_TRY_CUDA(launch_intra_tc(p, recs, false, stream));
     KDA_TRY_CUDA(launch_chain_fwd_tc(p, recs, false, stream));
     return KDA_OK;
 }
@@ -237,7 +253,9 @@ size_t kda_bwd_workspace_size(const kda_dims* dims, int chunk_size) {
     if (check_dims(dims, chunk_size, dims->num_seqs > 0 && dims->B == 1, &s) != KDA_OK &&
         check_dims(dims, chunk_size, false, &s) != KDA_OK)
         return 0;
-    return plan_simt(s, true).total;
+    const size_t a = plan_simt(s, true).total;
+    const size_t b = tc_eligible(s) ? plan_tc_bwd(s).total : 0;
+    return a > b ? a : b;
 }
 
 kda_status kda_fwd_simt(const kda_dims* dims, const void* q, const void* k, const void* v, const void* g_raw,
@@ -293,6 +311,26 @@ kda_status kda_bwd(const kda_dims* dims, const void* q, const void* k, const voi
     p.dout = dout; p.dST = dfinal_state;
     p.dq = dq; p.dk = dk; p.dv = dv; p.dg_raw = dg_raw; p.dbeta_raw = dbeta_raw;
     p.da_log = da_log; p.ddt_bias = ddt_bias; p.dS0 = dinitial_state;
+    if (tc_eligible(s) && lower_bound >= -5.0f && tc_inputs_aligned(p)) {
+        // tensor-core intra kernel (forward records + fp32 backward records), tensor-core state
+        // recompute, then the reverse chain and per-chunk gradients
+        const TcBwdPlan w = plan_tc_bwd(s);
+        st = check_ws(workspace, workspace_bytes, w.total);
+        if (st != KDA_OK) return st;
+        st = status_ptr(&p.status);
+        if (st != KDA_OK) return st;
+        carve(p, w.simt, workspace);
+        uint8_t* recs = static_cast<uint8_t*>(workspace) + w.off_tcrec;
+        Params pf = p;
+        pf.out = nullptr;
+        pf.ST = nullptr;
+        KDA_TRY_CUDA(launch_plan(p, stream));
+        KDA_TRY_CUDA(launch_intra_tc(p, recs, true, stream));
+        KDA_TRY_CUDA(launch_chain_fwd_tc(pf, recs, true, stream));
+        KDA_TRY_CUDA(launch_chain_bwd_simt(p, stream));
+        KDA_TRY_CUDA(launch_grad_tc(p, stream));
+        return KDA_OK;
+    }
     const WsPlan w = plan_simt(s, true);
     st = check_ws(workspace, workspace_bytes, w.total);
     if (st != KDA_OK) return st;

@@ -1,0 +1,549 @@
+// kda_grad.cu -- per-chunk gradients of the chunkwise KDA recurrence for K = V = 128.
+//
+// Inputs per (chunk, head): the fp32 chunk record (W, Kg, Kd, Qg, U0, Aqk, N, Bkk, Gamma, q_hat,
+// k_hat, beta, exp(Gamma_last)), the chunk-entering state S0 and the gradient dS_end w.r.t. the
+// chunk-leaving state (both from the state chains), dO, v and the raw q, k, g_raw.  The gradient
+// of the chunk equations
+//     U = U0 - W S0,   O = scale (Qg S0 + Aqk U),   S_end = Diag(exp(Gamma_last)) S0 + Kd^T U,
+//     T = N Diag(beta), N = (I + Diag(beta) Bkk)^-1, W = T Kg, U0 = T v
+// is formed here and pushed through the decayed bilinear forms, the cumulative log-decay and the
+// prologue (L2 norm, sigmoid beta, lower-bounded gate).
+//
+// The per-chunk contractions are small (64 x 128 x {32, 64, 128}) and interleaved with
+// elementwise work, so they run as warp-level tf32 MMAs (m16n8k8, operands rounded to nearest;
+// the decayed bilinear forms use a hi/lo split because their pair terms cancel in the
+// log-decay gradient)
+// straight from padded shared-memory tiles: no descriptor or accumulator round trips between the
+// many dependent steps.  Row strides = 4 (mod 32) words make every fragment load conflict-free in
+// either orientation.
+#include "kda_common.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+
+namespace {
+
+struct Tile {
+    const float* p;
+    int rs, cs;   // element (r, c) at p[r * rs + c * cs]
+    __device__ __forceinline__ float at(int r, int c) const { return p[r * rs + c * cs]; }
+};
+
+__device__ __forceinline__ uint32_t tf32(float x) {
+    uint32_t y;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void mma1688(float* d, const uint32_t* a, const uint32_t* b) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// d (one 16 x 8 block at rows m0, cols n0) += sum_{k in [k_lo, k_hi)} A(m, k) B(k, n), k range a
+// multiple of 8.  Fragment ownership: d[0] (m0+g, n0+2q), d[1] (m0+g, n0+2q+1), d[2] (m0+g+8, n0+2q),
+// d[3] (m0+g+8, n0+2q+1) with g = lane / 4, q = lane % 4.
+__device__ __forceinline__ void mma_block(float* d, const Tile& A, const Tile& B, int m0, int n0, int k_lo, int k_hi,
+                                          int lane) {
+    const int g = lane >> 2, q = lane & 3;
+    for (int k0 = k_lo; k0 < k_hi; k0 += 8) {
+        uint32_t a[4], b[2];
+        a[0] = tf32(A.at(m0 + g, k0 + q));
+        a[1] = tf32(A.at(m0 + g + 8, k0 + q));
+        a[2] = tf32(A.at(m0 + g, k0 + q + 4));
+        a[3] = tf32(A.at(m0 + g + 8, k0 + q + 4));
+        b[0] = tf32(B.at(k0 + q, n0 + g));
+        b[1] = tf32(B.at(k0 + q + 4, n0 + g));
+        mma1688(d, a, b);
+    }
+}
+
+// Split-precision variant: x = hi + lo with hi = tf32(x), lo = tf32(x - hi); the product keeps
+// hi*hi + hi*lo + lo*hi (relative error ~2^-21).  Used where the result enters sums that cancel
+// (the decayed bilinear forms feeding the log-decay gradient).
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+    hi = tf32(x);
+    lo = tf32(x - __uint_as_float(hi));
+}
+
+__device__ __forceinline__ void mma_block3(float* d, const Tile& A, const Tile& B, int m0, int n0, int k_lo, int k_hi,
+                                           int lane) {
+    const int g = lane >> 2, q = lane & 3;
+    for (int k0 = k_lo; k0 < k_hi; k0 += 8) {
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        split_tf32(A.at(m0 + g, k0 + q), ah[0], al[0]);
+        split_tf32(A.at(m0 + g + 8, k0 + q), ah[1], al[1]);
+        split_tf32(A.at(m0 + g, k0 + q + 4), ah[2], al[2]);
+        split_tf32(A.at(m0 + g + 8, k0 + q + 4), ah[3], al[3]);
+        split_tf32(B.at(k0 + q, n0 + g), bh[0], bl[0]);
+        split_tf32(B.at(k0 + q + 4, n0 + g), bh[1], bl[1]);
+        mma1688(d, al, bh);
+        mma1688(d, ah, bl);
+        mma1688(d, ah, bh);
+    }
+}
+
+__device__ __forceinline__ void frag_rc(int lane, int e, int m0, int n0, int& r, int& c) {
+    const int g = lane >> 2, q = lane & 3;
+    r = m0 + g + ((e & 2) ? 8 : 0);
+    c = n0 + 2 * q + (e & 1);
+}
+
+constexpr int P128 = 132, P64 = 68, P32 = 36;   // padded row strides (4 mod 32)
+
+// shared-memory plan, in floats
+constexpr int O_W = 0;                      // [64][P128]  phase 1: W;     phase 2: dk accumulation
+constexpr int O_KG = O_W + 64 * P128;       // [64][P128]  phase 1: Kg;    phase 2: dq accumulation
+constexpr int O_KD = O_KG + 64 * P128;      // [64][P128]  phase 1: Kd;    phase 2: dGamma accumulation
+constexpr int O_AQ = O_KD + 64 * P128;      // [64][P64]   Aqk (phase 2: dA)
+constexpr int O_N = O_AQ + 64 * P64;        // [64][P64]   N
+constexpr int O_S0 = O_N + 64 * P64;        // [128][P32]  S0 slice       (phase 2: dT / dN / dL / dB)
+constexpr int O_DS = O_S0 + 128 * P32;      // [128][P32]  dS_end slice   (phase 2: k_hat * r)
+constexpr int O_DO = O_DS + 128 * P32;      // [64][P32]   dO slice       (phase 2 scratch from here)
+constexpr int O_U = O_DO + 64 * P32;        // [64][P32]   U slice (starts as U0)
+constexpr int O_VT = O_U + 64 * P32;        // [64][P32]   v - Kg S0 slice (starts as v)
+constexpr int O_DU = O_VT + 64 * P32;       // [64][P32]   dU slice
+constexpr int O_DY = O_DU + 64 * P32;       // [64][P32]   dY slice
+constexpr int O_BETA = O_DY + 64 * P32;     // [64]
+constexpr int O_RED = O_BETA + 64;          // [64] dbeta, [128] Gamma_last gradient, [8] block sums
+constexpr int SMEM_FLOATS = O_RED + 64 + 128 + 8;
+
+}  // namespace
+
+__global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
+    extern __shared__ float sm[];
+    const int c = blockIdx.x, h = blockIdx.y;
+    if (c >= p.chunk_off[p.N]) return;
+    constexpr int K = 128, V = 128;
+    const int H = p.H;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = chunk_segment(p, c);
+    const int tok0 = seg_begin(p, n) + (c - p.chunk_off[n]) * kChunk;
+    const int len = min(kChunk, seg_end(p, n) - tok0);
+    const RecLayout L = RecLayout::make(K, V);
+    const float* rec = p.rec + ((size_t)c * H + h) * p.rec_stride;
+    const float* S0g = p.states + ((size_t)c * H + h) * K * V;
+    const float* dSg = p.dstates + ((size_t)c * H + h) * K * V;
+    float* sW = sm + O_W;
+    float* sKg = sm + O_KG;
+    float* sKd = sm + O_KD;
+    float* sAq = sm + O_AQ;
+    float* sN = sm + O_N;
+    float* sS0 = sm + O_S0;
+    float* sdS = sm + O_DS;
+    float* sdO = sm + O_DO;
+    float* sU = sm + O_U;
+    float* sVt = sm + O_VT;
+    float* sdU = sm + O_DU;
+    float* sdY = sm + O_DY;
+    float* sbeta = sm + O_BETA;
+    float* sred = sm + O_RED;
+    const float scale = p.scale;
+
+    // chunk-wide operands
+    for (int i = tid; i < 64 * K; i += 256) {
+        const int t = i >> 7, cc = i & 127;
+        sW[t * P128 + cc] = rec[L.W + i];
+        sKg[t * P128 + cc] = rec[L.Kg + i];
+        sKd[t * P128 + cc] = rec[L.Kd + i];
+    }
+    for (int i = tid; i < 64 * 64; i += 256) {
+        const int t = i >> 6, s = i & 63;
+        sAq[t * P64 + s] = rec[L.A + i];
+        sN[t * P64 + s] = rec[L.N + i];
+    }
+    if (tid < 64) sbeta[tid] = rec[L.beta + tid];
+
+    // accumulators over the four 32-column slices of V (register fragments)
+    //   dKg, dQg, dKd [64 x 128]: warp w owns rows 16 (w / 2) .. +16, cols 64 (w % 2) .. +64 (8 blocks)
+    //   dT, dA [64 x 64]: warp w owns rows 16 (w / 2), cols 32 (w % 2) .. +32 (4 blocks)
+    float aKg[8][4], aQg[8][4], aKd[8][4], aT[4][4], aA[4][4];
+#pragma unroll
+    for (int b = 0; b < 8; ++b)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) aKg[b][e] = aQg[b][e] = aKd[b][e] = 0.f;
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) aT[b][e] = aA[b][e] = 0.f;
+    float dgc = 0.f;   // thread tid < 128: sum_j dS_end[c][j] S0[c][j] for channel c = tid
+    const int wm0 = 16 * (warp >> 1);
+
+    for (int z = 0; z < 4; ++z) {
+        const int j0 = 32 * z;
+        __syncthreads();   // previous slice's readers are done
+        for (int i = tid; i < K * 32; i += 256) {
+            const int cc = i >> 5, j = i & 31;
+            sS0[cc * P32 + j] = S0g[cc * V + j0 + j];
+            sdS[cc * P32 + j] = dSg[cc * V + j0 + j];
+        }
+        for (int i = tid; i < 64 * 32; i += 256) {
+            const int t = i >> 5, j = i & 31;
+            const size_t gi = ((size_t)(tok0 + t) * H + h) * V + j0 + j;
+            sdO[t * P32 + j] = t < len ? load_act(p.dout, gi, p.dtype) : 0.f;
+            sVt[t * P32 + j] = t < len ? load_act(p.v, gi, p.dtype) : 0.f;
+            sU[t * P32 + j] = rec[L.U0 + t * V + j0 + j];
+        }
+        __syncthreads();
+        // U = U0 - W S0 and Vt = v - Kg S0 (64 x 32 each): 32 blocks, 4 per warp
+        {
+            float d[4][4];
+            int mm[4], nn[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int blk = warp * 4 + b;            // 0..31
+                const int which = blk >> 4, bb = blk & 15;
+                mm[b] = 16 * (bb >> 2);
+                nn[b] = 8 * (bb & 3);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) d[b][e] = 0.f;
+                mma_block(d[b], Tile{which ? sKg : sW, P128, 1}, Tile{sS0, P32, 1}, mm[b], nn[b], 0, K, lane);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int which = (warp * 4 + b) >> 4;
+                float* dst = which ? sVt : sU;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int r, cc;
+                    frag_rc(lane, e, mm[b], nn[b], r, cc);
+                    dst[r * P32 + cc] -= d[b][e];
+                }
+            }
+        }
+        __syncthreads();
+        // dU = Kd dS_end + scale Aqk^T dO (64 x 32): 16 blocks, 2 per warp
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            const int blk = warp * 2 + b;
+            const int m0 = 16 * (blk >> 2), n0 = 8 * (blk & 3);
+            float d1[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_block(d1, Tile{sKd, P128, 1}, Tile{sdS, P32, 1}, m0, n0, 0, K, lane);
+            mma_block(d2, Tile{sAq, 1, P64}, Tile{sdO, P32, 1}, m0, n0, 0, 64, lane);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int r, cc;
+                frag_rc(lane, e, m0, n0, r, cc);
+                sdU[r * P32 + cc] = d1[e] + scale * d2[e];
+            }
+        }
+        __syncthreads();
+        // dY = Diag(beta) N^T dU  (-> dv)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            const int blk = warp * 2 + b;
+            const int m0 = 16 * (blk >> 2), n0 = 8 * (blk & 3);
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_block(d, Tile{sN, 1, P64}, Tile{sdU, P32, 1}, m0, n0, 0, 64, lane);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int r, cc;
+                frag_rc(lane, e, m0, n0, r, cc);
+                const float y = sbeta[r] * d[e];
+                sdY[r * P32 + cc] = y;
+                if (r < len) p.dv[((size_t)(tok0 + r) * H + h) * V + j0 + cc] = y;
+            }
+        }
+        __syncthreads();
+        // slice contributions to dKg (-dY S0^T), dQg (dO S0^T), dKd (U dS^T), dT (dU Vt^T), dA (dO U^T)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int n0 = 64 * (warp & 1) + 8 * b;
+            mma_block(aKg[b], Tile{sdY, P32, 1}, Tile{sS0, 1, P32}, wm0, n0, 0, 32, lane);
+            mma_block(aQg[b], Tile{sdO, P32, 1}, Tile{sS0, 1, P32}, wm0, n0, 0, 32, lane);
+            mma_block(aKd[b], Tile{sU, P32, 1}, Tile{sdS, 1, P32}, wm0, n0, 0, 32, lane);
+        }
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int n0 = 32 * (warp & 1) + 8 * b;
+            mma_block(aT[b], Tile{sdU, P32, 1}, Tile{sVt, 1, P32}, wm0, n0, 0, 32, lane);
+            mma_block(aA[b], Tile{sdO, P32, 1}, Tile{sU, 1, P32}, wm0, n0, 0, 32, lane);
+        }
+        if (tid < K) {
+            float acc = 0.f;
+#pragma unroll 8
+            for (int j = 0; j < 32; ++j) acc += sdS[tid * P32 + j] * sS0[tid * P32 + j];
+            dgc += acc;
+        }
+    }
+    __syncthreads();
+
+    // ---- phase 2: write the accumulators out (dKg -> sW, dQg -> sKg, dKd -> sKd, dT -> sS0, dA -> sAq)
+    float* dKg = sW;
+    float* dQg = sKg;
+    float* dKdm = sKd;
+    float* dT = sS0;     // [64][P64]
+    float* dA = sAq;     // [64][P64]
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const int n0 = 64 * (warp & 1) + 8 * b;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            int r, cc;
+            frag_rc(lane, e, wm0, n0, r, cc);
+            dKg[r * P128 + cc] = -aKg[b][e];
+            dQg[r * P128 + cc] = scale * aQg[b][e];
+            dKdm[r * P128 + cc] = aKd[b][e];
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const int n0 = 32 * (warp & 1) + 8 * b;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            int r, cc;
+            frag_rc(lane, e, wm0, n0, r, cc);
+            dT[r * P64 + cc] = aT[b][e];
+            dA[r * P64 + cc] = cc <= r ? scale * aA[b][e] : 0.f;
+        }
+    }
+    __syncthreads();
+    // Gamma_last gathers exp(Gamma_last) rowsum(dS_end * S0) and sum_t dKd Kd
+    float* sgl = sred + 64;
+    if (tid < K) {
+        float acc = rec[L.gC + tid] * dgc;
+        for (int t = 0; t < 64; ++t) acc += dKdm[t * P128 + tid] * rec[L.Kd + t * K + tid];
+        sgl[tid] = acc;
+    }
+    // dbeta_s = sum_t N[t][s] dT[t][s];  dN = dT Diag(beta)
+    float* sdbeta = sred;
+    if (tid < 64) {
+        float acc = 0.f;
+        for (int t = 0; t < 64; ++t) acc += sN[t * P64 + tid] * dT[t * P64 + tid];
+        sdbeta[tid] = acc;
+    }
+    __syncthreads();
+    for (int i = tid; i < 64 * 64; i += 256) {
+        const int t = i >> 6, s = i & 63;
+        dT[t * P64 + s] *= sbeta[s];   // dN
+    }
+    __syncthreads();
+    // tmp = N^T dN ; dL = -(tmp N^T), strict lower ; dB = Diag(beta) dL
+    float* tmp = sdO;   // [64][P64] scratch (phase-1 slice buffers are free)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const int n0 = 32 * (warp & 1) + 8 * b;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_block(d, Tile{sN, 1, P64}, Tile{dT, P64, 1}, wm0, n0, 0, 64, lane);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            int r, cc;
+            frag_rc(lane, e, wm0, n0, r, cc);
+            tmp[r * P64 + cc] = d[e];
+        }
+    }
+    __syncthreads();
+    float* dB = dT;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const int n0 = 32 * (warp & 1) + 8 * b;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_block(d, Tile{tmp, P64, 1}, Tile{sN, 1, P64}, wm0, n0, 0, 64, lane);
+        __syncwarp();
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            int r, cc;
+            frag_rc(lane, e, wm0, n0, r, cc);
+            dB[r * P64 + cc] = cc < r ? -d[e] : 0.f;   // dL (beta applied below)
+        }
+    }
+    __syncthreads();
+    if (tid < 64) {
+        float acc = 0.f;
+        for (int s = 0; s < tid; ++s) acc += dB[tid * P64 + s] * rec[L.B + tid * 64 + s];
+        sdbeta[tid] += acc;
+    }
+    __syncthreads();
+    for (int i = tid; i < 64 * 64; i += 256) {
+        const int t = i >> 6, s = i & 63;
+        dB[t * P64 + s] *= sbeta[t];
+    }
+    // R[s][c] = k_hat[s][c] exp(G_{b(s)+1,c} - Gamma[s][c]) (<= 1), with G_{b+1} = Gamma at the end of
+    // sub-block b.  Stored in the phase-1 dS_end area: [64][P128].
+    float* R = sdS;
+    const float* Gm = rec + L.G;
+    const float* qh = rec + L.qh;
+    const float* kh = rec + L.kh;
+    for (int i = tid; i < 64 * K; i += 256) {
+        const int s = i >> 7, cc = i & 127;
+        const float gref = Gm[(16 * (s >> 4) + 15) * K + cc];
+        R[s * P128 + cc] = kh[i] * __expf(gref - Gm[i]);
+    }
+    __syncthreads();
+
+    // ---- decayed bilinear forms.  For s in sub-block j: exp(Gamma_t - Gamma_s) = l_j(t) r(s) with
+    // l_j(t) = exp(Gamma_t - G_{j+1}) (only t >= 16 j contribute: dA, dB are lower triangular).
+    //   dq_A[t]  = sum_j l_j(t) (dA[:, J] R[J, :])[t]
+    //   dk_L[t]  = sum_j l_j(t) (dB[:, J] R[J, :])[t]
+    //   dk_R[s]  = r(s) sum_t (dA[t][s] q[t] + dB[t][s] k[t]) l_j(t),   s in J
+    // Each warp owns the same 8 blocks (rows wm0, cols 64 (w % 2) + 8 b) of all three results.
+    float fq[8][4], fkl[8][4], fkr[8][4];
+#pragma unroll
+    for (int b = 0; b < 8; ++b)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) fq[b][e] = fkl[b][e] = fkr[b][e] = 0.f;
+    const int bt = warp >> 1;   // sub-block of this warp's rows
+    for (int j = 0; j <= bt; ++j) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int n0 = 64 * (warp & 1) + 8 * b;
+            float dq[4] = {0.f, 0.f, 0.f, 0.f}, dk[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_block3(dq, Tile{dA, P64, 1}, Tile{R, P128, 1}, wm0, n0, 16 * j, 16 * j + 16, lane);
+            mma_block3(dk, Tile{dB, P64, 1}, Tile{R, P128, 1}, wm0, n0, 16 * j, 16 * j + 16, lane);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int r, cc;
+                frag_rc(lane, e, wm0, n0, r, cc);
+                const float l = __expf(Gm[r * K + cc] - Gm[(16 * j + 15) * K + cc]);
+                fq[b][e] += l * dq[e];
+                fkl[b][e] += l * dk[e];
+            }
+        }
+    }
+    // dk_R: rows s of this warp's sub-block bt; sum over t >= 16 bt
+    {
+        const int j = bt;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int n0 = 64 * (warp & 1) + 8 * b;
+            const int g = lane >> 2, qd = lane & 3;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k0 = 16 * j; k0 < 64; k0 += 8) {
+                uint32_t aAh[4], aAl[4], aBh[4], aBl[4], bqh[2], bql[2], bkh[2], bkl[2];
+                // A(m = s, k = t) = dA[t][s] (transposed access), rows s = wm0 + ...
+                split_tf32(dA[(k0 + qd) * P64 + wm0 + g], aAh[0], aAl[0]);
+                split_tf32(dA[(k0 + qd) * P64 + wm0 + g + 8], aAh[1], aAl[1]);
+                split_tf32(dA[(k0 + qd + 4) * P64 + wm0 + g], aAh[2], aAl[2]);
+                split_tf32(dA[(k0 + qd + 4) * P64 + wm0 + g + 8], aAh[3], aAl[3]);
+                split_tf32(dB[(k0 + qd) * P64 + wm0 + g], aBh[0], aBl[0]);
+                split_tf32(dB[(k0 + qd) * P64 + wm0 + g + 8], aBh[1], aBl[1]);
+                split_tf32(dB[(k0 + qd + 4) * P64 + wm0 + g], aBh[2], aBl[2]);
+                split_tf32(dB[(k0 + qd + 4) * P64 + wm0 + g + 8], aBh[3], aBl[3]);
+                const int cn = n0 + g;
+                const float gref = Gm[(16 * j + 15) * K + cn];
+                const int t1 = k0 + qd, t2 = k0 + qd + 4;
+                const float l1 = __expf(Gm[t1 * K + cn] - gref), l2 = __expf(Gm[t2 * K + cn] - gref);
+                split_tf32(qh[t1 * K + cn] * l1, bqh[0], bql[0]);
+                split_tf32(qh[t2 * K + cn] * l2, bqh[1], bql[1]);
+                split_tf32(kh[t1 * K + cn] * l1, bkh[0], bkl[0]);
+                split_tf32(kh[t2 * K + cn] * l2, bkh[1], bkl[1]);
+                mma1688(acc, aAl, bqh);
+                mma1688(acc, aAh, bql);
+                mma1688(acc, aAh, bqh);
+                mma1688(acc, aBl, bkh);
+                mma1688(acc, aBh, bkl);
+                mma1688(acc, aBh, bkh);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int r, cc;
+                frag_rc(lane, e, wm0, n0, r, cc);
+                const float gref = Gm[(16 * j + 15) * K + cc];
+                fkr[b][e] = acc[e] * __expf(gref - Gm[r * K + cc]);
+            }
+        }
+    }
+    __syncthreads();   // dKg / dQg / dKd are read below by their owning threads only, R and dA/dB are done
+    // combine: dq = dq_A + dQg e^G ; dk = dk_L + dk_R + dKg e^G + dKd e^{Gc - G} ;
+    //          dGamma = q dq_A + k dk_L - k dk_R + dQg Qg + dKg Kg - dKd Kd
+    float* sdq = dQg;     // in place: the owning thread reads then overwrites
+    float* sdk = dKg;
+    float* sdG = dKdm;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const int n0 = 64 * (warp & 1) + 8 * b;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            int r, cc;
+            frag_rc(lane, e, wm0, n0, r, cc);
+            const int gi = r * K + cc;
+            const float G = Gm[gi], Gc = Gm[63 * K + cc];
+            const float eG = __expf(G), eD = __expf(Gc - G);
+            const float vQg = dQg[r * P128 + cc], vKg = dKg[r * P128 + cc], vKd = dKdm[r * P128 + cc];
+            const float q = qh[gi], k = kh[gi];
+            const float dq = fq[b][e] + vQg * eG;
+            const float dk = fkl[b][e] + fkr[b][e] + vKg * eG + vKd * eD;
+            const float dG = q * fq[b][e] + k * fkl[b][e] - k * fkr[b][e] + vQg * rec[L.Qg + gi] +
+                             vKg * rec[L.Kg + gi] - vKd * rec[L.Kd + gi];
+            sdq[r * P128 + cc] = dq;
+            sdk[r * P128 + cc] = dk;
+            sdG[r * P128 + cc] = dG;
+        }
+    }
+    __syncthreads();
+    // reverse cumulative sum over t (plus the Gamma_last term) gives dg
+    if (tid < K) {
+        float run = sgl[tid];
+        for (int t = 63; t >= 0; --t) {
+            run += sdG[t * P128 + tid];
+            sdG[t * P128 + tid] = run;
+        }
+    }
+    __syncthreads();
+    // ---- prologue backward: L2 norms, sigmoid(beta), lower-bounded gate
+    for (int t = warp; t < len; t += 8) {
+        const size_t row = (size_t)(tok0 + t) * H + h;
+        float nq = 0.f, nk = 0.f, sq = 0.f, sk = 0.f;
+        for (int cc = lane; cc < K; cc += 32) {
+            const float qr = load_act(p.q, row * K + cc, p.dtype), kr = load_act(p.k, row * K + cc, p.dtype);
+            nq += qr * qr;
+            nk += kr * kr;
+            sq += qh[t * K + cc] * sdq[t * P128 + cc];
+            sk += kh[t * K + cc] * sdk[t * P128 + cc];
+        }
+        nq = warp_sum(nq); nk = warp_sum(nk); sq = warp_sum(sq); sk = warp_sum(sk);
+        const float rq = 1.0f / sqrtf(nq + kNormEps), rk = 1.0f / sqrtf(nk + kNormEps);
+        for (int cc = lane; cc < K; cc += 32) {
+            p.dq[row * K + cc] = rq * (sdq[t * P128 + cc] - qh[t * K + cc] * sq);
+            p.dk[row * K + cc] = rk * (sdk[t * P128 + cc] - kh[t * K + cc] * sk);
+        }
+        if (lane == 0) {
+            const float b = sbeta[t];
+            p.dbeta_raw[row] = sdbeta[t] * b * (1.f - b);
+        }
+    }
+    float alog_part = 0.f;
+    if (tid < K) {
+        const int cc = tid;
+        const float ea = expf(p.a_log[h]);
+        const float dtbv = p.dt_bias[h * K + cc];
+        float dtb = 0.f;
+        for (int t = 0; t < len; ++t) {
+            const size_t gi = ((size_t)(tok0 + t) * H + h) * K + cc;
+            const float z = ea * (load_act(p.g_raw, gi, p.dtype) + dtbv);
+            const float sg = sigmoidf_acc(z);
+            const float dz = sdG[t * P128 + cc] * p.lb * sg * (1.f - sg);
+            p.dg_raw[gi] = dz * ea;
+            dtb += dz * ea;
+            alog_part += dz * z;
+        }
+        p.part_dtb[((size_t)c * H + h) * K + cc] = dtb;
+    }
+    alog_part = warp_sum(alog_part);
+    float* sblk = sred + 64 + 128;
+    if (lane == 0) sblk[warp] = alog_part;
+    __syncthreads();
+    if (tid == 0) {
+        float acc = 0.f;
+        for (int w = 0; w < 8; ++w) acc += sblk[w];
+        p.part_alog[(size_t)c * H + h] = acc;
+    }
+}
+
+cudaError_t launch_grad_tc(const Params& p, cudaStream_t st) {
+    const size_t smem = (size_t)SMEM_FLOATS * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    timing_pre(st, K_GRAD_TC);
+    grad_tc_kernel<<<dim3(p.NCmax, p.H), 256, smem, st>>>(p);
+    timing_post(st);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_param_reduce(p, st);
+}
+
+}  // namespace kda

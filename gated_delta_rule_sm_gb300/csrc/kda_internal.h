@@ -61,7 +61,7 @@ struct GradScratch {
 // Kernel ids for kda_kernel_name / kda_timing_end.
 enum KernelId {
     K_PLAN = 0, K_INTRA_SIMT, K_CHAIN_FWD_SIMT, K_CHAIN_BWD_SIMT, K_GRAD_SIMT, K_PARAM_REDUCE, K_EMPTY_SEG,
-    K_INTRA_TC, K_CHAIN_FWD_TC, K_NUM_KERNELS
+    K_INTRA_TC, K_CHAIN_FWD_TC, K_GRAD_TC, K_NUM_KERNELS
 };
 
 // Launch bracketing for kda_timing_*: no-ops unless timing is active.
@@ -73,11 +73,13 @@ cudaError_t launch_intra_simt(const Params& p, bool bwd, cudaStream_t st);
 cudaError_t launch_chain_fwd_simt(const Params& p, bool store_states, cudaStream_t st);
 cudaError_t launch_chain_bwd_simt(const Params& p, cudaStream_t st);
 cudaError_t launch_grad_simt(const Params& p, cudaStream_t st);
+cudaError_t launch_param_reduce(const Params& p, cudaStream_t st);
+cudaError_t launch_grad_tc(const Params& p, cudaStream_t st);
 
 // tensor-core path (bf16, K = V = 128)
 size_t tc_record_bytes(int NCmax, int H);
 bool tc_inputs_aligned(const Params& p);
-cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, cudaStream_t st);
+cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, bool bwd, cudaStream_t st);
 cudaError_t launch_chain_fwd_tc(const Params& p, const uint8_t* recs, bool store_states, cudaStream_t st);
 
 }  // namespace kda

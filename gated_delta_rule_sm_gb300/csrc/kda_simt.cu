@@ -602,6 +602,10 @@ cudaError_t launch_grad_simt(const Params& p, cudaStream_t st) {
     timing_post(st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    return launch_param_reduce(p, st);
+}
+
+cudaError_t launch_param_reduce(const Params& p, cudaStream_t st) {
     const int total = p.H * p.K + p.H;
     timing_pre(st, K_PARAM_REDUCE);
     param_reduce_kernel<<<(total + 255) / 256, 256, 0, st>>>(p);

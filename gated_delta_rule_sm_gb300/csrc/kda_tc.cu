@@ -102,11 +102,15 @@ constexpr uint32_t SN = LA_HI + 16640;       // fp32 [64][65] N = (I + L)^-1
 constexpr uint32_t SP = LA_HI + 34816;       // fp32 [3][16][17] scratch of the blocked solve
 constexpr uint32_t RB_HI = 131072, RB_LO = 147456;  // B operand (N = s, K = c) 64 x 128, mn_bf16(s, c, 128, 1024), hi / lo
 constexpr uint32_t KVB = 163840;             // A operand [Kg^T; V^T] 256 x 64 (K = s), km_bf16(r, s, 1024, 128)
-constexpr uint32_t SMALL = 196608;           // rq[64] rk[64] beta[64] dtb[128] blk[4][128] (fp32)
-constexpr uint32_t BAR = SMALL + (64 * 3 + 128 + 512) * 4;
+constexpr uint32_t KGLO = 196608;            // bf16 lo half of Kg^T (128 x 64), same layout
+constexpr uint32_t SMALL = 212992;           // rq[64] rk[64] beta[64] dtb[128] blk[4][128] gsum[4][128] (fp32)
+constexpr uint32_t BAR = SMALL + (64 * 3 + 128 + 1024) * 4;
 constexpr uint32_t BYTES = BAR + 64;
 }  // namespace intralay
 
+// BWD = true additionally writes the fp32 per-chunk record (RecLayout, backward fields) that the
+// backward's reverse chain and gradient kernels read.
+template <bool BWD>
 __global__ void __launch_bounds__(256, 1)
     intra_tc_kernel(Params p, uint8_t* recs, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_g,
@@ -125,6 +129,9 @@ __global__ void __launch_bounds__(256, 1)
     float* sbeta = rk + 64;
     float* sdtb = sbeta + 64;
     float* sblk = sdtb + 128;
+    float* sgsum = sblk + 512;        // per sub-block sums of g (backward record only)
+    float* frec = BWD ? p.rec + ((size_t)c * H + h) * p.rec_stride : nullptr;
+    const RecLayout RL = RecLayout::make(128, 128);
     // Each MMA barrier has at most one pending phase at any time, so parity waits are unambiguous.
     uint64_t* bar_load = reinterpret_cast<uint64_t*>(smem + BAR);
     uint64_t* bar_a = bar_load + 1;   // MMAs reading tile pair A (and the final W / U0 MMAs)
@@ -179,11 +186,13 @@ __global__ void __launch_bounds__(256, 1)
         const int cp = tid & 63, bi = tid >> 6, t0 = 16 * bi;
         const float ea = __expf(p.a_log[h]);
         float kx[2][16], qx[2][16], y[2][16], fj[2][4];
+        float lg[BWD ? 2 : 1][16];          // running sum of g inside the sub-block (backward record)
 #pragma unroll
         for (int ci = 0; ci < 2; ++ci) {
             const int cc = cp + 64 * ci;
             const float dtb = sdtb[cc];
             float a[16];
+            float gs = 0.f;
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
                 const int t = t0 + u;
@@ -193,7 +202,12 @@ __global__ void __launch_bounds__(256, 1)
                 float g = 0.f;
                 if (t < len) g = p.lb * __fdividef(1.f, 1.f + __expf(-ea * (bf16_at(smem + RAW_G, o) + dtb)));
                 a[u] = __expf(g);
+                if (BWD) {
+                    gs += g;
+                    lg[BWD ? ci : 0][u] = gs;
+                }
             }
+            if (BWD) sgsum[bi * 128 + cc] = gs;
             float run = 1.f;
 #pragma unroll
             for (int u = 15; u >= 0; --u) {     // y_t = prod_{v > t} alpha_v  (= exp(G_{b+1} - Gamma_t))
@@ -251,13 +265,35 @@ __global__ void __launch_bounds__(256, 1)
             fj[ci][2] = bi == 2 ? fd : bi == 3 ? 1.f : 0.f;
             fj[ci][3] = bi == 3 ? fd : 0.f;
             if (bi == 0) reinterpret_cast<float*>(rec + tcrec::GC)[cc] = B0 * B1 * B2 * B3;
+            if (BWD) {
+                float gpre = 0.f;
+                for (int m = 0; m < bi; ++m) gpre += sgsum[m * 128 + cc];
+                if (bi == 0) frec[RL.gC + cc] = B0 * B1 * B2 * B3;
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int t = t0 + u;
+                    const float kh = bf16_at(smem + RAW_K, t * 256 + cc * 2) * rk[t];
+                    const float qh = bf16_at(smem + RAW_Q, t * 256 + cc * 2) * rq[t];
+                    frec[RL.Kg + t * 128 + cc] = kx[ci][u] * eG;
+                    frec[RL.Qg + t * 128 + cc] = qx[ci][u] * eG;
+                    frec[RL.Kd + t * 128 + cc] = kh * y[ci][u] * tail;
+                    frec[RL.G + t * 128 + cc] = gpre + lg[BWD ? ci : 0][u];
+                    frec[RL.qh + t * 128 + cc] = qh;
+                    frec[RL.kh + t * 128 + cc] = kh;
+                }
+            }
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int tb = t0 + 8 * hh;
-                float vk[8], vq[8];
+                float vk[8], vq[8], vkl[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) { vk[e] = kx[ci][8 * hh + e] * eG; vq[e] = qx[ci][8 * hh + e] * eG; }
+                for (int e = 0; e < 8; ++e) {
+                    vk[e] = kx[ci][8 * hh + e] * eG;
+                    vq[e] = qx[ci][8 * hh + e] * eG;
+                    vkl[e] = vk[e] - __bfloat162float(__float2bfloat16_rn(vk[e]));
+                }
                 *reinterpret_cast<uint4*>(smem + KVB + km_bf16(cc, tb, 1024, 128)) = pack8_bf16(vk);
+                *reinterpret_cast<uint4*>(smem + KGLO + km_bf16(cc, tb, 1024, 128)) = pack8_bf16(vkl);
                 *reinterpret_cast<uint4*>(rec + tcrec::WQ + mn_bf16(64 + tb, cc, 128, 2048)) = pack8_bf16(vq);
             }
             // Kd^T (tf32): k * exp(Gamma_C - Gamma_t), four tokens per 16 B
@@ -367,7 +403,17 @@ __global__ void __launch_bounds__(256, 1)
                 const float bt = sbeta[t];
 #pragma unroll
                 for (int s2 = 0; s2 < 64; ++s2) SLf[t * 65 + s2] = s2 < t ? bt * d[s2] : 0.f;
+                if (BWD) {
+                    frec[RL.beta + t] = bt;
+#pragma unroll
+                    for (int s2 = 0; s2 < 64; ++s2) frec[RL.B + t * 64 + s2] = s2 < t ? d[s2] : 0.f;
+                }
             } else {
+                if (BWD) {
+                    const int t = tid - 64;
+#pragma unroll
+                    for (int s2 = 0; s2 < 64; ++s2) frec[RL.A + t * 64 + s2] = s2 <= t ? d[s2] : 0.f;
+                }
                 const int t = tid - 64;
 #pragma unroll
                 for (int s4 = 0; s4 < 64; s4 += 4) {
@@ -418,6 +464,11 @@ __global__ void __launch_bounds__(256, 1)
             }
             __syncthreads();
         }
+        if (BWD)
+            for (int i2 = tid; i2 < 64 * 64; i2 += 256) {
+                const int t = i2 >> 6, s2 = i2 & 63;
+                frec[RL.N + i2] = s2 <= t ? SNf[t * 65 + s2] : 0.f;
+            }
         // ---- T = N Diag(beta), split into bf16 hi + lo, as the B operand (N = t, K = s)
         {
             const int t = tid >> 2, sq = (tid & 3) * 16;
@@ -443,8 +494,14 @@ __global__ void __launch_bounds__(256, 1)
         constexpr uint32_t idW = idesc_bf16(128, 64, 0, 0);
         if (tid == 0) {
             const uint32_t kvb = smem_u32(smem + KVB), thi = smem_u32(smem + TB_HI), tlo = smem_u32(smem + TB_LO);
+            const uint32_t kgl = smem_u32(smem + KGLO);
+            // W^T = (Kg_hi + Kg_lo)^T (T_hi + T_lo)^T without the lo * lo term
             for (int kk = 0; kk < 4; ++kk)
                 mma_bf16(tmem + 64, smem_desc(kvb + kk * 256, 128, 1024), smem_desc(thi + kk * 256, 128, 1024), idW, kk > 0);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tmem + 64, smem_desc(kvb + kk * 256, 128, 1024), smem_desc(tlo + kk * 256, 128, 1024), idW, 1);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tmem + 64, smem_desc(kgl + kk * 256, 128, 1024), smem_desc(thi + kk * 256, 128, 1024), idW, 1);
             for (int kk = 0; kk < 4; ++kk)
                 mma_bf16(tmem + 128, smem_desc(kvb + 16384 + kk * 256, 128, 1024), smem_desc(thi + kk * 256, 128, 1024),
                          idW, kk > 0);
@@ -472,11 +529,17 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                 for (int tb = 0; tb < 64; tb += 8)
                     *reinterpret_cast<uint4*>(rec + tcrec::WQ + mn_bf16(tb, cc, 128, 2048)) = pack8_bf16(d + tb);
+                if (BWD)
+#pragma unroll
+                    for (int t = 0; t < 64; ++t) frec[RL.W + t * 128 + cc] = d[t];
             } else {
                 const int j = tid - 128;
                 float4* dst = reinterpret_cast<float4*>(rec + tcrec::U0 + j * 256);
 #pragma unroll
                 for (int t4 = 0; t4 < 16; ++t4) dst[t4] = make_float4(d[4 * t4], d[4 * t4 + 1], d[4 * t4 + 2], d[4 * t4 + 3]);
+                if (BWD)
+#pragma unroll
+                    for (int t = 0; t < 64; ++t) frec[RL.U0 + t * 128 + j] = d[t];
             }
         }
     }
@@ -509,7 +572,7 @@ constexpr uint32_t SLOT_BYTES = (SLOT_KD + tcrec::TAIL + 1023) / 1024 * 1024;
 constexpr uint32_t SB = 2 * SLOT_BYTES;   // S as bf16 B operand (N = j, K = c), MN-major: mn_bf16(j, c, 128, 512)
 constexpr uint32_t UB = SB + 8192;        // U as tf32 B operand (N = j, K = t), K-major, padded: km_f32(j, t, 2304, 144)
 constexpr uint32_t UB_LBO = 144, UB_SBO = 2304;
-constexpr uint32_t BAR = UB + 4 * UB_SBO; // mbarriers: full[2], mma
+constexpr uint32_t BAR = UB + 4 * UB_SBO; // mbarriers: full[2], ws, s, o; failure flag
 constexpr uint32_t TSLOT = BAR + 64;
 constexpr uint32_t BYTES = TSLOT + 64;
 }  // namespace chainlay
@@ -526,14 +589,20 @@ __device__ __forceinline__ void chain_load(uint8_t* slot, const uint8_t* rec, in
 }
 
 // One CTA per (segment, head, 32-column slice of V); 128 threads.  Thread c keeps row c of the
-// state slice (32 fp32) in registers.
+// state slice (32 fp32) in registers.  Per chunk the critical path is
+//   MMA1 (W S) -> U = U0 - W S -> MMA2b (Kd^T U) -> S <- Diag(gC) S + Kd^T U -> next MMA1;
+// the output product (Qg S + Aqk U) goes to a double-buffered TMEM accumulator and is written out by
+// warps 2-3 while the next chunk's MMA1 runs.
 __global__ void __launch_bounds__(128, 1) chain_fwd_tc_kernel(Params p, const uint8_t* recs, int store_states) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int n = blockIdx.x, h = blockIdx.y, z = blockIdx.z, j0 = z * 32;
     const int H = p.H, K = 128, V = 128;
     const int tid = threadIdx.x, warp = tid >> 5;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + chainlay::BAR);
-    uint64_t* mbar_mma = full + 2;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + chainlay::BAR);   // [2] record slots
+    uint64_t* bar_ws = full + 2;    // MMA1
+    uint64_t* bar_s = full + 3;     // MMA2b (state update)
+    uint64_t* bar_o = full + 4;     // MMA2a (output)
+    int* sh_fail = reinterpret_cast<int*>(full + 5);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + chainlay::TSLOT);
     uint8_t* SB = smem + chainlay::SB;
     uint8_t* UB = smem + chainlay::UB;
@@ -542,13 +611,11 @@ __global__ void __launch_bounds__(128, 1) chain_fwd_tc_kernel(Params p, const ui
     const int nch = ce - cb;
 
     if (tid == 0) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
-        mbar_init(mbar_mma, 1);
+        for (int i = 0; i < 5; ++i) mbar_init(&full[i], 1);
+        *sh_fail = 0;
         mbar_fence_init();
     }
-    if (warp == 0) tmem_alloc(tslot, 64);
-    // entering state, row c = tid
+    if (warp == 0) tmem_alloc(tslot, 128);
     float S[32];
     {
         const float* src = p.S0 ? p.S0 + (((size_t)n * H + h) * K + tid) * V + j0 : nullptr;
@@ -559,56 +626,52 @@ __global__ void __launch_bounds__(128, 1) chain_fwd_tc_kernel(Params p, const ui
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tD1 = tmem, tD3 = tmem + 32;
+    const uint32_t tD3 = tmem + 64;                       // D1[b] = tmem + 32 b
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    if (tid == 0) {
-        for (int i = 0; i < 2 && i < nch; ++i)
-            chain_load(smem + i * chainlay::SLOT_BYTES, recs + ((size_t)(cb + i) * H + h) * tcrec::BYTES, z, &full[i]);
-    }
+    auto slot_ptr = [&](int i) { return smem + (i & 1) * chainlay::SLOT_BYTES; };
+    auto rec_ptr = [&](int i) { return recs + ((size_t)(cb + i) * H + h) * tcrec::BYTES; };
+    auto fail_wait = [&](uint64_t* bar, uint32_t parity) {
+        if (!mbar_wait(bar, parity)) atomicExch(sh_fail, 1);
+    };
+    auto issue_mma1 = [&](int i) {
+        const uint32_t wq = smem_u32(slot_ptr(i) + chainlay::SLOT_WQ), sb = smem_u32(SB);
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16(tmem + 32 * (i & 1), smem_desc(wq + kk * 4096, 2048, 128), smem_desc(sb + kk * 1024, 512, 128),
+                     kIdescWS, kk > 0);
+        mma_commit(bar_ws);
+    };
 #pragma unroll
     for (int jg = 0; jg < 4; ++jg) *reinterpret_cast<uint4*>(SB + mn_bf16(8 * jg, tid, 128, 512)) = pack8_bf16(S + 8 * jg);
     fence_async_smem();
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && nch > 0) {
+        for (int i = 0; i < 2 && i < nch; ++i) chain_load(slot_ptr(i), rec_ptr(i), z, &full[i]);
+        fail_wait(&full[0], 0);
+        tc_fence_after();
+        issue_mma1(0);
+    }
 
-    // Every wait is bounded and block-uniform: a timeout makes all threads leave the loop together.
-    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
-        const bool mine = mbar_wait(bar, parity);
-        return __syncthreads_and(mine ? 1 : 0) != 0;
-    };
-    uint32_t mma_phase = 0;
     bool ok = true;
-    for (int i = 0; i < nch && ok; ++i) {
+    for (int i = 0; i < nch; ++i) {
         const int c = cb + i;
-        const int slot = i & 1;
-        uint8_t* sl = smem + slot * chainlay::SLOT_BYTES;
-        const int tok0 = tb + i * kChunk, len = min(kChunk, te - tok0);
+        uint8_t* sl = slot_ptr(i);
+        const uint32_t par = i & 1;
         if (store_states) {
             float* dst = p.states + (((size_t)c * H + h) * K + tid) * V + j0;
 #pragma unroll
             for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
         }
-        if (!wait_all(&full[slot], (i >> 1) & 1)) { ok = false; break; }
-        // MMA1: D1 = [W; Qg] S   (bf16, M=128, N=32, K=128)
-        if (tid == 0) {
-            tc_fence_after();
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t a = smem_desc(smem_u32(sl + chainlay::SLOT_WQ) + kk * 4096, 2048, 128);
-                const uint64_t b = smem_desc(smem_u32(SB) + kk * 1024, 512, 128);
-                mma_bf16(tD1, a, b, kIdescWS, kk > 0);
-            }
-            mma_commit(mbar_mma);
-        }
-        if (!wait_all(mbar_mma, mma_phase)) { ok = false; break; }
-        mma_phase ^= 1;
+        fail_wait(&full[i & 1], (i >> 1) & 1);   // record visible to this thread
+        fail_wait(bar_ws, par);
         tc_fence_after();
         if (warp < 2) {
-            // U[t][j] = U0[t][j] - (W S)[t][j], t = tid
+            // U[t][j] = U0[t][j] - (W S)[t][j], t = tid; rounded to tf32 and transposed in lane quads
             float d[32];
-            tmem_ld16(tD1 + lane_base, d);
-            tmem_ld16(tD1 + lane_base + 16, d + 16);
+            tmem_ld16(tmem + 32 * (i & 1) + lane_base, d);
+            tmem_ld16(tmem + 32 * (i & 1) + lane_base + 16, d + 16);
             tmem_ld_wait();
-            // U0 slice is column-major [32 j][64 t]; U rounded to tf32, then 4x4 transposes inside each
-            // lane quad give 16-byte rows of the K-major (t-contiguous) B operand.
             const float* u0 = reinterpret_cast<const float*>(sl + chainlay::SLOT_U0);
             float u[32];
 #pragma unroll
@@ -631,46 +694,25 @@ __global__ void __launch_bounds__(128, 1) chain_fwd_tc_kernel(Params p, const ui
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // MMA2: D1 += [. ; Aqk] U  and  D3 = Kd^T U   (tf32, M=128, N=32, K=64)
-        if (tid == 0) {
-            tc_fence_after();
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t b = smem_desc(smem_u32(UB) + kk * 2 * chainlay::UB_LBO, chainlay::UB_LBO, chainlay::UB_SBO);
-                const uint64_t a1 = smem_desc(smem_u32(sl + chainlay::SLOT_AQ) - 16384 + kk * 256, 128, 2048);
-                mma_tf32(tD1, a1, b, kIdescTF32, 1);
-                const uint64_t a2 = smem_desc(smem_u32(sl + chainlay::SLOT_KD) + kk * 256, 128, 2048);
-                mma_tf32(tD3, a2, b, kIdescTF32, kk > 0);
-            }
-            mma_commit(mbar_mma);
-        }
-        if (!wait_all(mbar_mma, mma_phase)) { ok = false; break; }
-        mma_phase ^= 1;
         tc_fence_after();
-        const float gc = reinterpret_cast<const float*>(sl + chainlay::SLOT_GC)[tid];
-        if (warp >= 2 && p.out) {
-            const int t = tid - 64;
-            float d[32];
-            tmem_ld16(tD1 + lane_base, d);
-            tmem_ld16(tD1 + lane_base + 16, d + 16);
-            tmem_ld_wait();
-            if (t < len) {
-                __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)(tok0 + t) * H + h) * V + j0;
-#pragma unroll
-                for (int j = 0; j < 32; j += 8) {
-                    uint4 pk;
-                    __nv_bfloat162 b0 = __floats2bfloat162_rn(p.scale * d[j], p.scale * d[j + 1]);
-                    __nv_bfloat162 b1 = __floats2bfloat162_rn(p.scale * d[j + 2], p.scale * d[j + 3]);
-                    __nv_bfloat162 b2 = __floats2bfloat162_rn(p.scale * d[j + 4], p.scale * d[j + 5]);
-                    __nv_bfloat162 b3 = __floats2bfloat162_rn(p.scale * d[j + 6], p.scale * d[j + 7]);
-                    pk.x = *reinterpret_cast<uint32_t*>(&b0);
-                    pk.y = *reinterpret_cast<uint32_t*>(&b1);
-                    pk.z = *reinterpret_cast<uint32_t*>(&b2);
-                    pk.w = *reinterpret_cast<uint32_t*>(&b3);
-                    *reinterpret_cast<uint4*>(o + j) = pk;
-                }
-            }
+        if (*sh_fail) { ok = false; break; }
+        // MMA2b: D3 = Kd^T U (state update) first, then MMA2a: D1 += [. ; Aqk] U (output)
+        if (tid == 0) {
+            const uint32_t ub = smem_u32(UB), kd = smem_u32(sl + chainlay::SLOT_KD);
+            const uint32_t aq = smem_u32(sl + chainlay::SLOT_AQ) - 16384;
+            for (int kk = 0; kk < 8; ++kk)
+                mma_tf32(tD3, smem_desc(kd + kk * 256, 128, 2048),
+                         smem_desc(ub + kk * 2 * chainlay::UB_LBO, chainlay::UB_LBO, chainlay::UB_SBO), kIdescTF32, kk > 0);
+            mma_commit(bar_s);
+            for (int kk = 0; kk < 8; ++kk)
+                mma_tf32(tmem + 32 * (i & 1), smem_desc(aq + kk * 256, 128, 2048),
+                         smem_desc(ub + kk * 2 * chainlay::UB_LBO, chainlay::UB_LBO, chainlay::UB_SBO), kIdescTF32, 1);
+            mma_commit(bar_o);
         }
+        fail_wait(bar_s, par);
+        tc_fence_after();
         {
+            const float gc = reinterpret_cast<const float*>(sl + chainlay::SLOT_GC)[tid];
             float d[32];
             tmem_ld16(tD3 + lane_base, d);
             tmem_ld16(tD3 + lane_base + 16, d + 16);
@@ -684,17 +726,46 @@ __global__ void __launch_bounds__(128, 1) chain_fwd_tc_kernel(Params p, const ui
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // the slot is free again: prefetch chunk i + 2 into it
-        if (tid == 0 && i + 2 < nch)
-            chain_load(sl, recs + ((size_t)(c + 2) * H + h) * tcrec::BYTES, z, &full[slot]);
+        tc_fence_after();
+        if (*sh_fail) { ok = false; break; }
+        if (tid == 0 && i + 1 < nch) {
+            fail_wait(&full[(i + 1) & 1], ((i + 1) >> 1) & 1);
+            tc_fence_after();
+            issue_mma1(i + 1);
+        }
+        if (warp >= 2) {
+            // output of chunk i, overlapping the next chunk's MMA1
+            fail_wait(bar_o, par);
+            tc_fence_after();
+            float d[32];
+            tmem_ld16(tmem + 32 * (i & 1) + lane_base, d);
+            tmem_ld16(tmem + 32 * (i & 1) + lane_base + 16, d + 16);
+            tmem_ld_wait();
+            const int t = tid - 64;
+            const int tok0 = tb + i * kChunk, len = min(kChunk, te - tok0);
+            if (p.out && t < len) {
+                __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)(tok0 + t) * H + h) * V + j0;
+                float sd[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sd[j] = p.scale * d[j];
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) *reinterpret_cast<uint4*>(o + j) = pack8_bf16(sd + j);
+            }
+            // the slot is free once this chunk's MMAs are done: prefetch chunk i + 2 into it
+            if (tid == 64 && i + 2 < nch) chain_load(sl, rec_ptr(i + 2), z, &full[i & 1]);
+        }
     }
+    __syncthreads();
+    if (*sh_fail) ok = false;
     if (!ok) {
-        // Record the timeout, then give in-flight copies and MMAs a bounded chance to land before
-        // this CTA's shared memory and tensor memory are released.
+        // Record the timeout; give in-flight copies and MMAs a bounded chance to land before this CTA's
+        // shared and tensor memory are released.
         if (tid == 0) {
             record_error(p.status, KDA_ERR_TIMEOUT);
-            mbar_wait(mbar_mma, mma_phase, 1u << 16);
-            for (int s2 = 0; s2 < 2; ++s2) mbar_wait(&full[s2], 0, 1u << 16);
+            for (int b = 0; b < 5; ++b) {
+                mbar_wait(&full[b], 0, 1u << 12);
+                mbar_wait(&full[b], 1, 1u << 12);
+            }
         }
     } else if (p.ST) {
         float* dst = p.ST + (((size_t)n * H + h) * K + tid) * V + j0;
@@ -703,7 +774,7 @@ __global__ void __launch_bounds__(128, 1) chain_fwd_tc_kernel(Params p, const ui
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 64);
+    if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 // ------------------------------------------------------------------ launchers
@@ -742,16 +813,16 @@ bool tc_inputs_aligned(const Params& p) {
     return al(p.q) && al(p.k) && al(p.g_raw) && al(p.v);
 }
 
-cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, cudaStream_t st) {
+cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, bool bwd, cudaStream_t st) {
     CUtensorMap mq, mk, mg, mv;
     if (!head_tile_map(&mq, p.q, p.H, p.TT) || !head_tile_map(&mk, p.k, p.H, p.TT) ||
         !head_tile_map(&mg, p.g_raw, p.H, p.TT) || !head_tile_map(&mv, p.v, p.H, p.TT))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)intralay::BYTES);
+    auto kern = bwd ? intra_tc_kernel<true> : intra_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)intralay::BYTES);
     if (e != cudaSuccess) return e;
     timing_pre(st, K_INTRA_TC);
-    intra_tc_kernel<<<dim3(p.NCmax, p.H), 256, intralay::BYTES, st>>>(p, recs, mq, mk, mg, mv);
+    kern<<<dim3(p.NCmax, p.H), 256, intralay::BYTES, st>>>(p, recs, mq, mk, mg, mv);
     timing_post(st);
     return cudaGetLastError();
 }
