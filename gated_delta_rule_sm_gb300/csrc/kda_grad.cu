@@ -86,6 +86,22 @@ __device__ __forceinline__ void mma_block3(float* d, const Tile& A, const Tile& 
     }
 }
 
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory"); }
+
+// Eight bf16 values (16 bytes) to fp32.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
 __device__ __forceinline__ void frag_rc(int lane, int e, int m0, int n0, int& r, int& c) {
     const int g = lane >> 2, q = lane & 3;
     r = m0 + g + ((e & 2) ? 8 : 0);
@@ -108,8 +124,8 @@ constexpr int O_VT = O_U + 64 * P32;        // [64][P32]   v - Kg S0 slice (star
 constexpr int O_DU = O_VT + 64 * P32;       // [64][P32]   dU slice
 constexpr int O_DY = O_DU + 64 * P32;       // [64][P32]   dY slice
 constexpr int O_BETA = O_DY + 64 * P32;     // [64]
-constexpr int O_RED = O_BETA + 64;          // [64] dbeta, [128] Gamma_last gradient, [8] block sums
-constexpr int SMEM_FLOATS = O_RED + 64 + 128 + 8;
+constexpr int O_RED = O_BETA + 64;          // [64] dbeta, [128] Gamma_last gradient, [8] block sums, [256] dt_bias parts
+constexpr int SMEM_FLOATS = O_RED + 64 + 128 + 8 + 256;
 
 }  // namespace
 
@@ -143,19 +159,19 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     float* sred = sm + O_RED;
     const float scale = p.scale;
 
-    // chunk-wide operands
-    for (int i = tid; i < 64 * K; i += 256) {
-        const int t = i >> 7, cc = i & 127;
-        sW[t * P128 + cc] = rec[L.W + i];
-        sKg[t * P128 + cc] = rec[L.Kg + i];
-        sKd[t * P128 + cc] = rec[L.Kd + i];
+    // chunk-wide operands (16-byte asynchronous copies; completed by the first slice's wait)
+    for (int i = tid; i < 64 * K / 4; i += 256) {
+        const int t = i >> 5, c4 = (i & 31) * 4;
+        cp_async16(sW + t * P128 + c4, rec + L.W + t * K + c4);
+        cp_async16(sKg + t * P128 + c4, rec + L.Kg + t * K + c4);
+        cp_async16(sKd + t * P128 + c4, rec + L.Kd + t * K + c4);
     }
-    for (int i = tid; i < 64 * 64; i += 256) {
-        const int t = i >> 6, s = i & 63;
-        sAq[t * P64 + s] = rec[L.A + i];
-        sN[t * P64 + s] = rec[L.N + i];
+    for (int i = tid; i < 64 * 64 / 4; i += 256) {
+        const int t = i >> 4, s4 = (i & 15) * 4;
+        cp_async16(sAq + t * P64 + s4, rec + L.A + t * 64 + s4);
+        cp_async16(sN + t * P64 + s4, rec + L.N + t * 64 + s4);
     }
-    if (tid < 64) sbeta[tid] = rec[L.beta + tid];
+    if (tid < 16) cp_async16(sbeta + 4 * tid, rec + L.beta + 4 * tid);
 
     // accumulators over the four 32-column slices of V (register fragments)
     //   dKg, dQg, dKd [64 x 128]: warp w owns rows 16 (w / 2) .. +16, cols 64 (w % 2) .. +64 (8 blocks)
@@ -175,18 +191,33 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     for (int z = 0; z < 4; ++z) {
         const int j0 = 32 * z;
         __syncthreads();   // previous slice's readers are done
-        for (int i = tid; i < K * 32; i += 256) {
-            const int cc = i >> 5, j = i & 31;
-            sS0[cc * P32 + j] = S0g[cc * V + j0 + j];
-            sdS[cc * P32 + j] = dSg[cc * V + j0 + j];
+        for (int i = tid; i < K * 8; i += 256) {
+            const int cc = i >> 3, j4 = (i & 7) * 4;
+            cp_async16(sS0 + cc * P32 + j4, S0g + cc * V + j0 + j4);
+            cp_async16(sdS + cc * P32 + j4, dSg + cc * V + j0 + j4);
         }
-        for (int i = tid; i < 64 * 32; i += 256) {
-            const int t = i >> 5, j = i & 31;
-            const size_t gi = ((size_t)(tok0 + t) * H + h) * V + j0 + j;
-            sdO[t * P32 + j] = t < len ? load_act(p.dout, gi, p.dtype) : 0.f;
-            sVt[t * P32 + j] = t < len ? load_act(p.v, gi, p.dtype) : 0.f;
-            sU[t * P32 + j] = rec[L.U0 + t * V + j0 + j];
+        for (int i = tid; i < 64 * 8; i += 256) {
+            const int t = i >> 3, j4 = (i & 7) * 4;
+            cp_async16(sU + t * P32 + j4, rec + L.U0 + t * V + j0 + j4);
         }
+        {   // dO and v slices (bf16, 8 per 16-byte load): one row-quarter per thread
+            const int t = tid >> 2, j8 = (tid & 3) * 8;
+            float fo[8], fv[8];
+            if (t < len) {
+                const size_t gi = ((size_t)(tok0 + t) * H + h) * V + j0 + j8;
+                bf16x8_to_f32(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + gi), fo);
+                bf16x8_to_f32(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.v) + gi), fv);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) fo[e] = fv[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                sdO[t * P32 + j8 + e] = fo[e];
+                sVt[t * P32 + j8 + e] = fv[e];
+            }
+        }
+        cp_async_wait_all();
         __syncthreads();
         // U = U0 - W S0 and Vt = v - Kg S0 (64 x 32 each): 32 blocks, 4 per warp
         {
@@ -352,10 +383,11 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         }
     }
     __syncthreads();
-    if (tid < 64) {
-        float acc = 0.f;
-        for (int s = 0; s < tid; ++s) acc += dB[tid * P64 + s] * rec[L.B + tid * 64 + s];
-        sdbeta[tid] += acc;
+    for (int t = warp; t < 64; t += 8) {   // dbeta_t += sum_{s<t} dL[t][s] Bkk[t][s]
+        const float* brow = rec + L.B + t * 64;
+        float acc = dB[t * P64 + lane] * brow[lane] + dB[t * P64 + lane + 32] * brow[lane + 32];
+        acc = warp_sum(acc);
+        if (lane == 0) sdbeta[t] += acc;
     }
     __syncthreads();
     for (int i = tid; i < 64 * 64; i += 256) {
@@ -487,41 +519,59 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     // ---- prologue backward: L2 norms, sigmoid(beta), lower-bounded gate
     for (int t = warp; t < len; t += 8) {
         const size_t row = (size_t)(tok0 + t) * H + h;
-        float nq = 0.f, nk = 0.f, sq = 0.f, sk = 0.f;
-        for (int cc = lane; cc < K; cc += 32) {
-            const float qr = load_act(p.q, row * K + cc, p.dtype), kr = load_act(p.k, row * K + cc, p.dtype);
-            nq += qr * qr;
-            nk += kr * kr;
-            sq += qh[t * K + cc] * sdq[t * P128 + cc];
-            sk += kh[t * K + cc] * sdk[t * P128 + cc];
+        float qv[4], kv[4], sq = 0.f, sk = 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int cc = lane + 32 * u;
+            qv[u] = qh[t * K + cc];
+            kv[u] = kh[t * K + cc];
+            sq += qv[u] * sdq[t * P128 + cc];
+            sk += kv[u] * sdk[t * P128 + cc];
         }
-        nq = warp_sum(nq); nk = warp_sum(nk); sq = warp_sum(sq); sk = warp_sum(sk);
-        const float rq = 1.0f / sqrtf(nq + kNormEps), rk = 1.0f / sqrtf(nk + kNormEps);
-        for (int cc = lane; cc < K; cc += 32) {
-            p.dq[row * K + cc] = rq * (sdq[t * P128 + cc] - qh[t * K + cc] * sq);
-            p.dk[row * K + cc] = rk * (sdk[t * P128 + cc] - kh[t * K + cc] * sk);
+        sq = warp_sum(sq); sk = warp_sum(sk);
+        const float rq = rec[L.rn + t], rk = rec[L.rn + 64 + t];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int cc = lane + 32 * u;
+            p.dq[row * K + cc] = rq * (sdq[t * P128 + cc] - qv[u] * sq);
+            p.dk[row * K + cc] = rk * (sdk[t * P128 + cc] - kv[u] * sk);
         }
         if (lane == 0) {
             const float b = sbeta[t];
             p.dbeta_raw[row] = sdbeta[t] * b * (1.f - b);
         }
     }
+    // gate backward: thread (channel cc, parity hf) takes tokens hf, hf + 2, ...
     float alog_part = 0.f;
-    if (tid < K) {
-        const int cc = tid;
+    {
+        const int cc = tid & 127, hf = tid >> 7;
         const float ea = expf(p.a_log[h]);
         const float dtbv = p.dt_bias[h * K + cc];
-        float dtb = 0.f;
-        for (int t = 0; t < len; ++t) {
-            const size_t gi = ((size_t)(tok0 + t) * H + h) * K + cc;
-            const float z = ea * (load_act(p.g_raw, gi, p.dtype) + dtbv);
-            const float sg = sigmoidf_acc(z);
-            const float dz = sdG[t * P128 + cc] * p.lb * sg * (1.f - sg);
-            p.dg_raw[gi] = dz * ea;
-            dtb += dz * ea;
-            alog_part += dz * z;
+        const __nv_bfloat16* __restrict__ graw = static_cast<const __nv_bfloat16*>(p.g_raw);
+        float* __restrict__ dgr = p.dg_raw;
+        float gv[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            const int t = hf + 2 * u;
+            gv[u] = t < len ? __bfloat162float(graw[((size_t)(tok0 + t) * H + h) * K + cc]) : 0.f;
         }
-        p.part_dtb[((size_t)c * H + h) * K + cc] = dtb;
+        float dtb = 0.f;
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+            const int t = hf + 2 * u;
+            if (t < len) {
+                const float z = ea * (gv[u] + dtbv);
+                const float sg = sigmoidf_acc(z);
+                const float dz = sdG[t * P128 + cc] * p.lb * sg * (1.f - sg);
+                dgr[((size_t)(tok0 + t) * H + h) * K + cc] = dz * ea;
+                dtb += dz * ea;
+                alog_part += dz * z;
+            }
+        }
+        float* sdtb = sred + 64 + 128 + 8;   // [256]
+        sdtb[tid] = dtb;
+        __syncthreads();
+        if (tid < K) p.part_dtb[((size_t)c * H + h) * K + tid] = sdtb[tid] + sdtb[tid + 128];
     }
     alog_part = warp_sum(alog_part);
     float* sblk = sred + 64 + 128;

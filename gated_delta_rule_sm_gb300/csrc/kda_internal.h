@@ -11,7 +11,7 @@ namespace kda {
 // Per (chunk, head) record of the SIMT path, in floats.
 struct RecLayout {
     size_t W, Qg, Kd, U0, A, gC;           // forward fields
-    size_t Kg, N, G, qh, kh, B, beta;      // backward extras
+    size_t Kg, N, G, qh, kh, B, beta, rn;  // backward extras (rn: 1/|q_t|, then 1/|k_t|)
     size_t fwd_size, bwd_size;
     __host__ __device__ static RecLayout make(int K, int V) {
         RecLayout r;
@@ -30,6 +30,7 @@ struct RecLayout {
         r.kh = o; o += 64 * (size_t)K;
         r.B = o; o += 64 * 64;
         r.beta = o; o += 64;
+        r.rn = o; o += 128;
         r.bwd_size = (o + 63) / 64 * 64;
         return r;
     }

@@ -405,6 +405,8 @@ __global__ void __launch_bounds__(256, 1)
                 for (int s2 = 0; s2 < 64; ++s2) SLf[t * 65 + s2] = s2 < t ? bt * d[s2] : 0.f;
                 if (BWD) {
                     frec[RL.beta + t] = bt;
+                    frec[RL.rn + t] = rq[t];
+                    frec[RL.rn + 64 + t] = rk[t];
 #pragma unroll
                     for (int s2 = 0; s2 < 64; ++s2) frec[RL.B + t * 64 + s2] = s2 < t ? d[s2] : 0.f;
                 }
@@ -810,7 +812,7 @@ static bool head_tile_map(CUtensorMap* m, const void* base, int H, int TT) {
 
 bool tc_inputs_aligned(const Params& p) {
     auto al = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
-    return al(p.q) && al(p.k) && al(p.g_raw) && al(p.v);
+    return al(p.q) && al(p.k) && al(p.g_raw) && al(p.v) && (p.dout == nullptr || al(p.dout));
 }
 
 cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, bool bwd, cudaStream_t st) {

@@ -84,13 +84,14 @@ size_t kda_bwd_workspace_size(const kda_dims* dims, int chunk_size);
 /*
  * Forward.  Writes out [B,T,H,V] (input dtype) and, if final_state != NULL,
  * final_state [N,H,K,V] fp32.  initial_state may be NULL (zero state).
- * scale is applied to the output; lower_bound must be in [-5, 0) (the
- * 16-token sub-block factorisation of the decay stays inside fp32 range
- * only for |lower_bound| <= 5); chunk_size must be 64.
+ * scale is applied to the output; lower_bound must be finite and < 0;
+ * chunk_size must be 64.
  * Requirements: B,T,H >= 1; 16 <= K,V <= 128 and multiples of 16 (the pages
- * reject head dims below 16); N >= 1.  bf16 with K == V == 128 runs on the
- * tcgen05 tensor-core path; every other supported shape (and fp32 inputs)
- * runs on the fp32 SIMT path.
+ * reject head dims below 16); N >= 1.  bf16 with K == V == 128, 16-byte
+ * aligned q, k, v, g_raw (and dout for kda_bwd) and lower_bound >= -5 runs
+ * on the tcgen05 tensor-core path (its 16-token sub-block factorisation of
+ * the decay stays inside fp32 range only for |lower_bound| <= 5); every other
+ * supported shape (and fp32 inputs) runs on the fp32 SIMT path.
  */
 kda_status kda_fwd(const kda_dims* dims,
                    const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
