@@ -63,6 +63,7 @@ def kernel_work(name: str, w, units: float) -> tuple[float, float]:
         "kda_chain_fwd_tc": (a["fwd_write"], a["chain_flops"]),
         "kda_chain_bwd_simt": (0.0, a["chain_flops"]),
         "kda_chain_bwd_tc": (0.0, a["chain_flops"]),
+        "kda_bwd_pre": (0.0, 0.0),
         # the per-chunk gradient kernels read dout and write every fp32 gradient
         "kda_grad_simt": (a["bwd_bytes"] - a["fwd_read"], a["bwd_flops"] - a["chain_flops"] - a["intra_flops"]),
         "kda_grad_tc": (a["bwd_bytes"] - a["fwd_read"], a["bwd_flops"] - a["chain_flops"] - a["intra_flops"]),

@@ -89,6 +89,7 @@ static TcPlan plan_tc_fwd(const Shape& s) {
 struct TcBwdPlan {
     WsPlan simt;        // chunk table, fp32 backward records, states, partials, scratch
     size_t off_tcrec;   // tensor-core forward records (recompute chain)
+    size_t off_bwrec;   // reverse-chain records
     size_t total;
 };
 
@@ -97,6 +98,7 @@ static TcBwdPlan plan_tc_bwd(const Shape& s) {
     w.simt = plan_simt(s, true);
     size_t o = w.simt.total;
     w.off_tcrec = o; o = align_up(o + tc_record_bytes(s.NCmax, s.H));
+    w.off_bwrec = o; o = align_up(o + (size_t)s.NCmax * s.H * bwrec::BYTES);
     w.total = o;
     return w;
 }
@@ -211,7 +213,7 @@ static void timing_release() {
 static const char* kKernelNames[] = {"kda_plan",          "kda_intra_simt",   "kda_chain_fwd_simt",
                                      "kda_chain_bwd_simt", "kda_grad_simt",    "kda_param_reduce",
                                      "kda_empty_segment", "kda_intra_tc",     "kda_chain_fwd_tc",
-                                     "kda_grad_tc"};
+                                     "kda_grad_tc",       "kda_bwd_pre",      "kda_chain_bwd_tc"};
 
 static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cudaStream_t stream) {
     const TcPlan w = plan_tc_fwd(s);
@@ -313,7 +315,7 @@ kda_status kda_bwd(const kda_dims* dims, const void* q, const void* k, const voi
     p.da_log = da_log; p.ddt_bias = ddt_bias; p.dS0 = dinitial_state;
     if (tc_eligible(s) && lower_bound >= -5.0f && tc_inputs_aligned(p)) {
         // tensor-core intra kernel (forward records + fp32 backward records), tensor-core state
-        // recompute, then the reverse chain and per-chunk gradients
+        // recompute, reverse-chain operands, tensor-core reverse chain, per-chunk gradients
         const TcBwdPlan w = plan_tc_bwd(s);
         st = check_ws(workspace, workspace_bytes, w.total);
         if (st != KDA_OK) return st;
@@ -327,7 +329,9 @@ kda_status kda_bwd(const kda_dims* dims, const void* q, const void* k, const voi
         KDA_TRY_CUDA(launch_plan(p, stream));
         KDA_TRY_CUDA(launch_intra_tc(p, recs, true, stream));
         KDA_TRY_CUDA(launch_chain_fwd_tc(pf, recs, true, stream));
-        KDA_TRY_CUDA(launch_chain_bwd_simt(p, stream));
+        uint8_t* bw = static_cast<uint8_t*>(workspace) + w.off_bwrec;
+        KDA_TRY_CUDA(launch_bwd_pre(p, bw, stream));
+        KDA_TRY_CUDA(launch_chain_bwd_tc(p, bw, stream));
         KDA_TRY_CUDA(launch_grad_tc(p, stream));
         return KDA_OK;
     }

@@ -18,8 +18,11 @@
 // either orientation.
 #include "kda_common.cuh"
 #include "kda_internal.h"
+#include "kda_sm100.cuh"
 
 namespace kda {
+
+using sm100::km_f32;
 
 namespace {
 
@@ -582,6 +585,124 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         for (int w = 0; w < 8; ++w) acc += sblk[w];
         p.part_alog[(size_t)c * H + h] = acc;
     }
+}
+
+// ------------------------------------------------------------------ reverse-chain operands
+//
+// Per (chunk, head): the dS-independent terms of the reverse recursion, Y = scale Aqk^T dO and
+// P = scale Qg^T dO (warp tf32 MMAs, fp32 results), plus Kd and -W^T rounded to tf32 in the
+// K-major layouts the reverse chain's tcgen05 MMAs read (record layout: bwrec).
+namespace {
+constexpr int PB_A = 0;                  // [64][P64]   Aqk
+constexpr int PB_Q = PB_A + 64 * P64;    // [64][P128]  Qg
+constexpr int PB_D = PB_Q + 64 * P128;   // [64][P128]  dO
+constexpr int PB_FLOATS = PB_D + 64 * P128;
+}  // namespace
+
+__global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) {
+    extern __shared__ float sm[];
+    const int c = blockIdx.x, h = blockIdx.y;
+    if (c >= p.chunk_off[p.N]) return;
+    constexpr int K = 128, V = 128;
+    const int H = p.H;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = chunk_segment(p, c);
+    const int tok0 = seg_begin(p, n) + (c - p.chunk_off[n]) * kChunk;
+    const int len = min(kChunk, seg_end(p, n) - tok0);
+    const RecLayout L = RecLayout::make(K, V);
+    const float* rec = p.rec + ((size_t)c * H + h) * p.rec_stride;
+    uint8_t* out = bw + ((size_t)c * H + h) * bwrec::BYTES;
+    float* sA = sm + PB_A;
+    float* sQ = sm + PB_Q;
+    float* sD = sm + PB_D;
+    const float scale = p.scale;
+
+    for (int i = tid; i < 64 * K / 4; i += 256) {
+        const int t = i >> 5, c4 = (i & 31) * 4;
+        cp_async16(sQ + t * P128 + c4, rec + L.Qg + t * K + c4);
+    }
+    for (int i = tid; i < 64 * 64 / 4; i += 256) {
+        const int t = i >> 4, s4 = (i & 15) * 4;
+        cp_async16(sA + t * P64 + s4, rec + L.A + t * 64 + s4);
+    }
+    for (int i = tid; i < 64 * V / 8; i += 256) {
+        const int t = i >> 4, j8 = (i & 15) * 8;
+        float f[8];
+        if (t < len) {
+            const size_t gi = ((size_t)(tok0 + t) * H + h) * V + j8;
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + gi), f);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sD[t * P128 + j8 + e] = f[e];
+    }
+    // Kd -> tf32 K-major (rows t, K = c); -W^T -> tf32 K-major (rows c, K = t); exp(Gamma_last)
+    for (int i = tid; i < 64 * K / 4; i += 256) {
+        const int t = i >> 5, c4 = (i & 31) * 4;
+        const float4 v = *reinterpret_cast<const float4*>(rec + L.Kd + t * K + c4);
+        *reinterpret_cast<float4*>(out + bwrec::KDA + km_f32(t, c4, 4096, 128)) =
+            make_float4(__uint_as_float(tf32(v.x)), __uint_as_float(tf32(v.y)), __uint_as_float(tf32(v.z)),
+                        __uint_as_float(tf32(v.w)));
+    }
+    for (int i = tid; i < K * 16; i += 256) {
+        const int cc = i & 127, t4 = (i >> 7) * 4;
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = -__uint_as_float(tf32(rec[L.W + (t4 + u) * K + cc]));
+        *reinterpret_cast<float4*>(out + bwrec::WTN + km_f32(cc, t4, 2048, 128)) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    if (tid < K) reinterpret_cast<float*>(out + bwrec::GC)[tid] = rec[L.gC + tid];
+    cp_async_wait_all();
+    __syncthreads();
+    // Y = scale Aqk^T dO (64 x 128): warp w owns rows 16 (w / 2) and columns 64 (w % 2) .. + 64.
+    // Aqk is lower triangular, so rows s only see t >= s.
+    {
+        const int m0 = 16 * (warp >> 1);
+        float* Yg = reinterpret_cast<float*>(out + bwrec::Y);
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int n0 = 64 * (warp & 1) + 8 * b;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_block(d, Tile{sA, 1, P64}, Tile{sD, P128, 1}, m0, n0, m0, 64, lane);
+            int r, cc;
+            frag_rc(lane, 0, m0, n0, r, cc);
+            *reinterpret_cast<float2*>(Yg + r * V + cc) = make_float2(scale * d[0], scale * d[1]);
+            *reinterpret_cast<float2*>(Yg + (r + 8) * V + cc) = make_float2(scale * d[2], scale * d[3]);
+        }
+    }
+    // P = scale Qg^T dO (128 x 128): warp w owns rows 16 w, all columns in four groups
+    {
+        float* Pg = reinterpret_cast<float*>(out + bwrec::P);
+        const int m0 = 16 * warp;
+        for (int grp = 0; grp < 4; ++grp) {
+            float a1[4][4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) a1[b][e] = 0.f;
+                mma_block(a1[b], Tile{sQ, 1, P128}, Tile{sD, P128, 1}, m0, 32 * grp + 8 * b, 0, 64, lane);
+            }
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                int r, cc;
+                frag_rc(lane, 0, m0, 32 * grp + 8 * b, r, cc);
+                *reinterpret_cast<float2*>(Pg + r * V + cc) = make_float2(scale * a1[b][0], scale * a1[b][1]);
+                *reinterpret_cast<float2*>(Pg + (r + 8) * V + cc) = make_float2(scale * a1[b][2], scale * a1[b][3]);
+            }
+        }
+    }
+}
+
+cudaError_t launch_bwd_pre(const Params& p, uint8_t* bw, cudaStream_t st) {
+    const size_t smem = (size_t)PB_FLOATS * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(bwd_pre_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    timing_pre(st, K_BWD_PRE);
+    bwd_pre_kernel<<<dim3(p.NCmax, p.H), 256, smem, st>>>(p, bw);
+    timing_post(st);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_grad_tc(const Params& p, cudaStream_t st) {

@@ -33,52 +33,6 @@ constexpr uint32_t U0_SLICE = 8192;   // one 32-column slice of U0
 constexpr uint32_t TAIL = BYTES - KD; // KD + AQ + GC, contiguous
 }  // namespace tcrec
 
-// Core-matrix offsets.  MN-major bf16: 16 B rows hold 8 consecutive M/N elements of one K index.
-// K-major: 16 B rows hold 8 (bf16) or 4 (32-bit) consecutive K elements of one M/N index.
-// mstride / kstride are the byte distances between neighbouring core matrices along M/N and K.
-__host__ __device__ __forceinline__ uint32_t mn_bf16(int r, int k, uint32_t mstride, uint32_t kstride) {
-    return static_cast<uint32_t>((r >> 3) * mstride + (k >> 3) * kstride + (k & 7) * 16 + (r & 7) * 2);
-}
-__host__ __device__ __forceinline__ uint32_t km_bf16(int r, int k, uint32_t mstride, uint32_t kstride) {
-    return static_cast<uint32_t>((r >> 3) * mstride + (k >> 3) * kstride + (r & 7) * 16 + (k & 7) * 2);
-}
-__host__ __device__ __forceinline__ uint32_t km_f32(int r, int k, uint32_t mstride, uint32_t kstride) {
-    return static_cast<uint32_t>((r >> 3) * mstride + (k >> 2) * kstride + (r & 7) * 16 + (k & 3) * 4);
-}
-
-__device__ __forceinline__ float tf32_rn(float x) {
-    uint32_t y;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
-    return __uint_as_float(y);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
-    return make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
-}
-
-__device__ __forceinline__ float bf16_at(const uint8_t* base, uint32_t byte_off) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(base + byte_off));
-}
-
-// kind::tf32 MMA (A/B format 2 = TF32, f32 accumulate).
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
-}
-
-__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
-    return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-           (static_cast<uint32_t>(M >> 4) << 24);
-}
-
 // ------------------------------------------------------------------ intra-chunk kernel (tcgen05)
 //
 // One CTA (256 threads) per (chunk, head).  Decay factorisation: inside a chunk, with Gamma_t the
