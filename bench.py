@@ -72,6 +72,18 @@ def kernel_work(name: str, w, units: float) -> tuple[float, float]:
     return b * units, f * units
 
 
+# DRAM bytes (read + write) per token-head per launch, from ncu captures of the current kernels on
+# the B=1 T=4096 H=32 K=V=128 case (profiles/grad_tc_B1_T4096_H32_D128.md,
+# profiles/intra_tc_B1_T4096_H32_D128.md).  Per-chunk kernels move the same bytes per chunk-head at
+# any size, so the figure scales with the token-heads of a launch.  An entry is removed when its
+# kernel changes and has not been captured again.
+PROFILED_TRAFFIC = {
+    ("kda_grad_tc", True): 9756.0,
+    ("kda_intra_tc", False): 2401.0,             # forward mode (forward-only workloads)
+    ("kda_intra_tc", True): (2401.0 + 7289.0) / 2,   # forward + backward mode, one launch each per step
+}
+
+
 def read_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -349,7 +361,8 @@ def run_ours(args, w):
         else:
             roofline = {"bound": "hbm", "achieved": bytes_l / avg_s / 1e9, "peak": hbm, "unit": "GB/s"}
         roofline["frac"] = roofline["achieved"] / roofline["peak"]
-        roofline["traffic"] = None
+        tpu = PROFILED_TRAFFIC.get((dom, bool(w.backward)))
+        roofline["traffic"] = tpu * units / max(1.0, launches_per_step) if tpu is not None and w.K == 128 else None
         roofline["kernel"] = dom
         roofline["peak_source"] = peaks["source"]
         roofline["avg_launch_ms"] = tot_ms / n_launch
