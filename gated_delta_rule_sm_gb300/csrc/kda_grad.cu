@@ -46,24 +46,6 @@ __device__ __forceinline__ void mma1688(float* d, const uint32_t* a, const uint3
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// d (one 16 x 8 block at rows m0, cols n0) += sum_{k in [k_lo, k_hi)} A(m, k) B(k, n), k range a
-// multiple of 8.  Fragment ownership: d[0] (m0+g, n0+2q), d[1] (m0+g, n0+2q+1), d[2] (m0+g+8, n0+2q),
-// d[3] (m0+g+8, n0+2q+1) with g = lane / 4, q = lane % 4.
-__device__ __forceinline__ void mma_block(float* d, const Tile& A, const Tile& B, int m0, int n0, int k_lo, int k_hi,
-                                          int lane) {
-    const int g = lane >> 2, q = lane & 3;
-    for (int k0 = k_lo; k0 < k_hi; k0 += 8) {
-        uint32_t a[4], b[2];
-        a[0] = tf32(A.at(m0 + g, k0 + q));
-        a[1] = tf32(A.at(m0 + g + 8, k0 + q));
-        a[2] = tf32(A.at(m0 + g, k0 + q + 4));
-        a[3] = tf32(A.at(m0 + g + 8, k0 + q + 4));
-        b[0] = tf32(B.at(k0 + q, n0 + g));
-        b[1] = tf32(B.at(k0 + q + 4, n0 + g));
-        mma1688(d, a, b);
-    }
-}
-
 // Split-precision variant: x = hi + lo with hi = tf32(x), lo = tf32(x - hi); the product keeps
 // hi*hi + hi*lo + lo*hi (relative error ~2^-21).  Used where the result enters sums that cancel
 // (the decayed bilinear forms feeding the log-decay gradient).
@@ -72,20 +54,57 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) 
     lo = tf32(x - __uint_as_float(hi));
 }
 
-__device__ __forceinline__ void mma_block3(float* d, const Tile& A, const Tile& B, int m0, int n0, int k_lo, int k_hi,
-                                           int lane) {
+// d[b] (16 x 8 blocks at rows m0, cols n0 + 8 b, b < NB) += sum_k A(m, k) B(k, n): one A fragment per
+// k-step serves the whole strip; the k-loop stays rolled to keep the kernel's code small.
+template <int NB>
+__device__ __forceinline__ void mma_strip(float (&d)[NB][4], const Tile& A, const Tile& B, int m0, int n0, int k_lo,
+                                          int k_hi, int lane) {
     const int g = lane >> 2, q = lane & 3;
+#pragma unroll 1
     for (int k0 = k_lo; k0 < k_hi; k0 += 8) {
-        uint32_t ah[4], al[4], bh[2], bl[2];
-        split_tf32(A.at(m0 + g, k0 + q), ah[0], al[0]);
-        split_tf32(A.at(m0 + g + 8, k0 + q), ah[1], al[1]);
-        split_tf32(A.at(m0 + g, k0 + q + 4), ah[2], al[2]);
-        split_tf32(A.at(m0 + g + 8, k0 + q + 4), ah[3], al[3]);
-        split_tf32(B.at(k0 + q, n0 + g), bh[0], bl[0]);
-        split_tf32(B.at(k0 + q + 4, n0 + g), bh[1], bl[1]);
-        mma1688(d, al, bh);
-        mma1688(d, ah, bl);
-        mma1688(d, ah, bh);
+        uint32_t a[4];
+        a[0] = tf32(A.at(m0 + g, k0 + q));
+        a[1] = tf32(A.at(m0 + g + 8, k0 + q));
+        a[2] = tf32(A.at(m0 + g, k0 + q + 4));
+        a[3] = tf32(A.at(m0 + g + 8, k0 + q + 4));
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            uint32_t bb[2];
+            bb[0] = tf32(B.at(k0 + q, n0 + 8 * b + g));
+            bb[1] = tf32(B.at(k0 + q + 4, n0 + 8 * b + g));
+            mma1688(d[b], a, bb);
+        }
+    }
+}
+
+// Split-precision strip for two left operands sharing the right one: d1 += A1 B, d2 += A2 B with
+// hi*hi + hi*lo + lo*hi products.
+template <int NB>
+__device__ __forceinline__ void mma_strip3_pair(float (&d1)[NB][4], float (&d2)[NB][4], const Tile& A1, const Tile& A2,
+                                                const Tile& B, int m0, int n0, int k_lo, int k_hi, int lane) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll 1
+    for (int k0 = k_lo; k0 < k_hi; k0 += 8) {
+        uint32_t h1[4], l1[4], h2[4], l2[4];
+        const int rr[4] = {m0 + g, m0 + g + 8, m0 + g, m0 + g + 8};
+        const int kk[4] = {k0 + q, k0 + q, k0 + q + 4, k0 + q + 4};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            split_tf32(A1.at(rr[i], kk[i]), h1[i], l1[i]);
+            split_tf32(A2.at(rr[i], kk[i]), h2[i], l2[i]);
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            uint32_t bh[2], bl[2];
+            split_tf32(B.at(k0 + q, n0 + 8 * b + g), bh[0], bl[0]);
+            split_tf32(B.at(k0 + q + 4, n0 + 8 * b + g), bh[1], bl[1]);
+            mma1688(d1[b], l1, bh);
+            mma1688(d1[b], h1, bl);
+            mma1688(d1[b], h1, bh);
+            mma1688(d2[b], l2, bh);
+            mma1688(d2[b], h2, bl);
+            mma1688(d2[b], h2, bh);
+        }
     }
 }
 
@@ -222,81 +241,75 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         }
         cp_async_wait_all();
         __syncthreads();
-        // U = U0 - W S0 and Vt = v - Kg S0 (64 x 32 each): 32 blocks, 4 per warp
+        // U = U0 - W S0 and Vt = v - Kg S0 (64 x 32 each): warp w takes rows 16 (w % 4) of U (w < 4) or Vt
         {
+            const int which = warp >> 2, m0 = 16 * (warp & 3);
             float d[4][4];
-            int mm[4], nn[4];
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int blk = warp * 4 + b;            // 0..31
-                const int which = blk >> 4, bb = blk & 15;
-                mm[b] = 16 * (bb >> 2);
-                nn[b] = 8 * (bb & 3);
+            for (int b = 0; b < 4; ++b)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) d[b][e] = 0.f;
-                mma_block(d[b], Tile{which ? sKg : sW, P128, 1}, Tile{sS0, P32, 1}, mm[b], nn[b], 0, K, lane);
-            }
+            mma_strip<4>(d, Tile{which ? sKg : sW, P128, 1}, Tile{sS0, P32, 1}, m0, 0, 0, K, lane);
             __syncwarp();
+            float* dst = which ? sVt : sU;
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int which = (warp * 4 + b) >> 4;
-                float* dst = which ? sVt : sU;
+            for (int b = 0; b < 4; ++b)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     int r, cc;
-                    frag_rc(lane, e, mm[b], nn[b], r, cc);
+                    frag_rc(lane, e, m0, 8 * b, r, cc);
                     dst[r * P32 + cc] -= d[b][e];
                 }
-            }
         }
         __syncthreads();
-        // dU = Kd dS_end + scale Aqk^T dO (64 x 32): 16 blocks, 2 per warp
+        // dU = Kd dS_end + scale Aqk^T dO (64 x 32): warp w takes rows 16 (w / 2), columns 16 (w % 2) .. + 16.
+        // Aqk is lower triangular: rows s see t >= s only.
+        {
+            const int m0 = 16 * (warp >> 1), n0 = 16 * (warp & 1);
+            float d1[2][4], d2[2][4];
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            const int blk = warp * 2 + b;
-            const int m0 = 16 * (blk >> 2), n0 = 8 * (blk & 3);
-            float d1[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_block(d1, Tile{sKd, P128, 1}, Tile{sdS, P32, 1}, m0, n0, 0, K, lane);
-            mma_block(d2, Tile{sAq, 1, P64}, Tile{sdO, P32, 1}, m0, n0, 0, 64, lane);
+            for (int b = 0; b < 2; ++b)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                int r, cc;
-                frag_rc(lane, e, m0, n0, r, cc);
-                sdU[r * P32 + cc] = d1[e] + scale * d2[e];
-            }
+                for (int e = 0; e < 4; ++e) d1[b][e] = d2[b][e] = 0.f;
+            mma_strip<2>(d1, Tile{sKd, P128, 1}, Tile{sdS, P32, 1}, m0, n0, 0, K, lane);
+            mma_strip<2>(d2, Tile{sAq, 1, P64}, Tile{sdO, P32, 1}, m0, n0, m0, 64, lane);
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int r, cc;
+                    frag_rc(lane, e, m0, n0 + 8 * b, r, cc);
+                    sdU[r * P32 + cc] = d1[b][e] + scale * d2[b][e];
+                }
         }
         __syncthreads();
-        // dY = Diag(beta) N^T dU  (-> dv)
+        // dY = Diag(beta) N^T dU  (-> dv); N is lower triangular: rows s see t >= s only
+        {
+            const int m0 = 16 * (warp >> 1), n0 = 16 * (warp & 1);
+            float d[2][4];
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            const int blk = warp * 2 + b;
-            const int m0 = 16 * (blk >> 2), n0 = 8 * (blk & 3);
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_block(d, Tile{sN, 1, P64}, Tile{sdU, P32, 1}, m0, n0, 0, 64, lane);
+            for (int b = 0; b < 2; ++b)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                int r, cc;
-                frag_rc(lane, e, m0, n0, r, cc);
-                const float y = sbeta[r] * d[e];
-                sdY[r * P32 + cc] = y;
-                if (r < len) p.dv[((size_t)(tok0 + r) * H + h) * V + j0 + cc] = y;
-            }
+                for (int e = 0; e < 4; ++e) d[b][e] = 0.f;
+            mma_strip<2>(d, Tile{sN, 1, P64}, Tile{sdU, P32, 1}, m0, n0, m0, 64, lane);
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int r, cc;
+                    frag_rc(lane, e, m0, n0 + 8 * b, r, cc);
+                    const float y = sbeta[r] * d[b][e];
+                    sdY[r * P32 + cc] = y;
+                    if (r < len) p.dv[((size_t)(tok0 + r) * H + h) * V + j0 + cc] = y;
+                }
         }
         __syncthreads();
         // slice contributions to dKg (-dY S0^T), dQg (dO S0^T), dKd (U dS^T), dT (dU Vt^T), dA (dO U^T)
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const int n0 = 64 * (warp & 1) + 8 * b;
-            mma_block(aKg[b], Tile{sdY, P32, 1}, Tile{sS0, 1, P32}, wm0, n0, 0, 32, lane);
-            mma_block(aQg[b], Tile{sdO, P32, 1}, Tile{sS0, 1, P32}, wm0, n0, 0, 32, lane);
-            mma_block(aKd[b], Tile{sU, P32, 1}, Tile{sdS, 1, P32}, wm0, n0, 0, 32, lane);
-        }
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int n0 = 32 * (warp & 1) + 8 * b;
-            mma_block(aT[b], Tile{sdU, P32, 1}, Tile{sVt, 1, P32}, wm0, n0, 0, 32, lane);
-            mma_block(aA[b], Tile{sdO, P32, 1}, Tile{sU, 1, P32}, wm0, n0, 0, 32, lane);
-        }
+        mma_strip<8>(aKg, Tile{sdY, P32, 1}, Tile{sS0, 1, P32}, wm0, 64 * (warp & 1), 0, 32, lane);
+        mma_strip<8>(aQg, Tile{sdO, P32, 1}, Tile{sS0, 1, P32}, wm0, 64 * (warp & 1), 0, 32, lane);
+        mma_strip<8>(aKd, Tile{sU, P32, 1}, Tile{sdS, 1, P32}, wm0, 64 * (warp & 1), 0, 32, lane);
+        mma_strip<4>(aT, Tile{sdU, P32, 1}, Tile{sVt, 1, P32}, wm0, 32 * (warp & 1), 0, 32, lane);
+        mma_strip<4>(aA, Tile{sdO, P32, 1}, Tile{sU, 1, P32}, wm0, 32 * (warp & 1), 0, 32, lane);
         if (tid < K) {
             float acc = 0.f;
 #pragma unroll 8
@@ -358,32 +371,40 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     __syncthreads();
     // tmp = N^T dN ; dL = -(tmp N^T), strict lower ; dB = Diag(beta) dL
     float* tmp = sdO;   // [64][P64] scratch (phase-1 slice buffers are free)
+    {
+        float d[4][4];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        const int n0 = 32 * (warp & 1) + 8 * b;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_block(d, Tile{sN, 1, P64}, Tile{dT, P64, 1}, wm0, n0, 0, 64, lane);
+        for (int b = 0; b < 4; ++b)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            int r, cc;
-            frag_rc(lane, e, wm0, n0, r, cc);
-            tmp[r * P64 + cc] = d[e];
-        }
+            for (int e = 0; e < 4; ++e) d[b][e] = 0.f;
+        mma_strip<4>(d, Tile{sN, 1, P64}, Tile{dT, P64, 1}, wm0, 32 * (warp & 1), wm0, 64, lane);   // N[t][s], t >= s
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int r, cc;
+                frag_rc(lane, e, wm0, 32 * (warp & 1) + 8 * b, r, cc);
+                tmp[r * P64 + cc] = d[b][e];
+            }
     }
     __syncthreads();
     float* dB = dT;
+    {
+        float d[4][4];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        const int n0 = 32 * (warp & 1) + 8 * b;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_block(d, Tile{tmp, P64, 1}, Tile{sN, 1, P64}, wm0, n0, 0, 64, lane);
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[b][e] = 0.f;
+        mma_strip<4>(d, Tile{tmp, P64, 1}, Tile{sN, 1, P64}, wm0, 32 * (warp & 1), 0, 64, lane);
         __syncwarp();
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            int r, cc;
-            frag_rc(lane, e, wm0, n0, r, cc);
-            dB[r * P64 + cc] = cc < r ? -d[e] : 0.f;   // dL (beta applied below)
-        }
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int r, cc;
+                frag_rc(lane, e, wm0, 32 * (warp & 1) + 8 * b, r, cc);
+                dB[r * P64 + cc] = cc < r ? -d[b][e] : 0.f;   // dL (beta applied below)
+            }
     }
     __syncthreads();
     for (int t = warp; t < 64; t += 8) {   // dbeta_t += sum_{s<t} dL[t][s] Bkk[t][s]
@@ -424,19 +445,25 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     const int bt = warp >> 1;   // sub-block of this warp's rows
     for (int j = 0; j <= bt; ++j) {
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const int n0 = 64 * (warp & 1) + 8 * b;
-            float dq[4] = {0.f, 0.f, 0.f, 0.f}, dk[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_block3(dq, Tile{dA, P64, 1}, Tile{R, P128, 1}, wm0, n0, 16 * j, 16 * j + 16, lane);
-            mma_block3(dk, Tile{dB, P64, 1}, Tile{R, P128, 1}, wm0, n0, 16 * j, 16 * j + 16, lane);
+        for (int hb = 0; hb < 2; ++hb) {
+            const int n0 = 64 * (warp & 1) + 32 * hb;
+            float dq[4][4], dk[4][4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                int r, cc;
-                frag_rc(lane, e, wm0, n0, r, cc);
-                const float l = __expf(Gm[r * K + cc] - Gm[(16 * j + 15) * K + cc]);
-                fq[b][e] += l * dq[e];
-                fkl[b][e] += l * dk[e];
-            }
+            for (int b = 0; b < 4; ++b)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dq[b][e] = dk[b][e] = 0.f;
+            mma_strip3_pair<4>(dq, dk, Tile{dA, P64, 1}, Tile{dB, P64, 1}, Tile{R, P128, 1}, wm0, n0, 16 * j,
+                               16 * j + 16, lane);
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int r, cc;
+                    frag_rc(lane, e, wm0, n0 + 8 * b, r, cc);
+                    const float l = __expf(Gm[r * K + cc] - Gm[(16 * j + 15) * K + cc]);
+                    fq[4 * hb + b][e] += l * dq[b][e];
+                    fkl[4 * hb + b][e] += l * dk[b][e];
+                }
         }
     }
     // dk_R: rows s of this warp's sub-block bt; sum over t >= 16 bt
@@ -659,35 +686,38 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) 
     // Y = scale Aqk^T dO (64 x 128): warp w owns rows 16 (w / 2) and columns 64 (w % 2) .. + 64.
     // Aqk is lower triangular, so rows s only see t >= s.
     {
-        const int m0 = 16 * (warp >> 1);
+        const int m0 = 16 * (warp >> 1), n0 = 64 * (warp & 1);
         float* Yg = reinterpret_cast<float*>(out + bwrec::Y);
+        float d[8][4];
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[b][e] = 0.f;
+        mma_strip<8>(d, Tile{sA, 1, P64}, Tile{sD, P128, 1}, m0, n0, m0, 64, lane);
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
-            const int n0 = 64 * (warp & 1) + 8 * b;
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_block(d, Tile{sA, 1, P64}, Tile{sD, P128, 1}, m0, n0, m0, 64, lane);
             int r, cc;
-            frag_rc(lane, 0, m0, n0, r, cc);
-            *reinterpret_cast<float2*>(Yg + r * V + cc) = make_float2(scale * d[0], scale * d[1]);
-            *reinterpret_cast<float2*>(Yg + (r + 8) * V + cc) = make_float2(scale * d[2], scale * d[3]);
+            frag_rc(lane, 0, m0, n0 + 8 * b, r, cc);
+            *reinterpret_cast<float2*>(Yg + r * V + cc) = make_float2(scale * d[b][0], scale * d[b][1]);
+            *reinterpret_cast<float2*>(Yg + (r + 8) * V + cc) = make_float2(scale * d[b][2], scale * d[b][3]);
         }
     }
-    // P = scale Qg^T dO (128 x 128): warp w owns rows 16 w, all columns in four groups
+    // P = scale Qg^T dO (128 x 128): warp w owns rows 16 w, all columns in two strips of 64
     {
         float* Pg = reinterpret_cast<float*>(out + bwrec::P);
         const int m0 = 16 * warp;
-        for (int grp = 0; grp < 4; ++grp) {
-            float a1[4][4];
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+            float a1[8][4];
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
+            for (int b = 0; b < 8; ++b)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) a1[b][e] = 0.f;
-                mma_block(a1[b], Tile{sQ, 1, P128}, Tile{sD, P128, 1}, m0, 32 * grp + 8 * b, 0, 64, lane);
-            }
+            mma_strip<8>(a1, Tile{sQ, 1, P128}, Tile{sD, P128, 1}, m0, 64 * half, 0, 64, lane);
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
+            for (int b = 0; b < 8; ++b) {
                 int r, cc;
-                frag_rc(lane, 0, m0, 32 * grp + 8 * b, r, cc);
+                frag_rc(lane, 0, m0, 64 * half + 8 * b, r, cc);
                 *reinterpret_cast<float2*>(Pg + r * V + cc) = make_float2(scale * a1[b][0], scale * a1[b][1]);
                 *reinterpret_cast<float2*>(Pg + (r + 8) * V + cc) = make_float2(scale * a1[b][2], scale * a1[b][3]);
             }
