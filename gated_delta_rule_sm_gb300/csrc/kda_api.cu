@@ -90,6 +90,7 @@ struct TcBwdPlan {
     WsPlan simt;        // chunk table, fp32 backward records, states, partials, scratch
     size_t off_tcrec;   // tensor-core forward records (recompute chain)
     size_t off_bwrec;   // reverse-chain records
+    size_t off_fwrec;   // forward-recompute chain records
     size_t total;
 };
 
@@ -99,6 +100,7 @@ static TcBwdPlan plan_tc_bwd(const Shape& s) {
     size_t o = w.simt.total;
     w.off_tcrec = o; o = align_up(o + tc_record_bytes(s.NCmax, s.H));
     w.off_bwrec = o; o = align_up(o + (size_t)s.NCmax * s.H * bwrec::BYTES);
+    w.off_fwrec = o; o = align_up(o + (size_t)s.NCmax * s.H * fwrec::BYTES);
     w.total = o;
     return w;
 }
@@ -213,7 +215,8 @@ static void timing_release() {
 static const char* kKernelNames[] = {"kda_plan",          "kda_intra_simt",   "kda_chain_fwd_simt",
                                      "kda_chain_bwd_simt", "kda_grad_simt",    "kda_param_reduce",
                                      "kda_empty_segment", "kda_intra_tc",     "kda_chain_fwd_tc",
-                                     "kda_grad_tc",       "kda_bwd_pre",      "kda_chain_bwd_tc"};
+                                     "kda_grad_tc",       "kda_bwd_pre",      "kda_chain_bwd_tc",
+                                     "kda_chain_rec_tc"};
 
 static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cudaStream_t stream) {
     const TcPlan w = plan_tc_fwd(s);
@@ -314,8 +317,8 @@ kda_status kda_bwd(const kda_dims* dims, const void* q, const void* k, const voi
     p.dq = dq; p.dk = dk; p.dv = dv; p.dg_raw = dg_raw; p.dbeta_raw = dbeta_raw;
     p.da_log = da_log; p.ddt_bias = ddt_bias; p.dS0 = dinitial_state;
     if (tc_eligible(s) && lower_bound >= -5.0f && tc_inputs_aligned(p)) {
-        // tensor-core intra kernel (forward records + fp32 backward records), tensor-core state
-        // recompute, reverse-chain operands, tensor-core reverse chain, per-chunk gradients
+        // tensor-core intra kernel (fp32 backward records), chain operands, tf32 tensor-core state
+        // recompute and reverse chain, per-chunk gradients
         const TcBwdPlan w = plan_tc_bwd(s);
         st = check_ws(workspace, workspace_bytes, w.total);
         if (st != KDA_OK) return st;
@@ -328,9 +331,10 @@ kda_status kda_bwd(const kda_dims* dims, const void* q, const void* k, const voi
         pf.ST = nullptr;
         KDA_TRY_CUDA(launch_plan(p, stream));
         KDA_TRY_CUDA(launch_intra_tc(p, recs, true, stream));
-        KDA_TRY_CUDA(launch_chain_fwd_tc(pf, recs, true, stream));
         uint8_t* bw = static_cast<uint8_t*>(workspace) + w.off_bwrec;
-        KDA_TRY_CUDA(launch_bwd_pre(p, bw, stream));
+        uint8_t* fw = static_cast<uint8_t*>(workspace) + w.off_fwrec;
+        KDA_TRY_CUDA(launch_bwd_pre(p, bw, fw, stream));
+        KDA_TRY_CUDA(launch_chain_rec_tc(pf, fw, stream));
         KDA_TRY_CUDA(launch_chain_bwd_tc(p, bw, stream));
         KDA_TRY_CUDA(launch_grad_tc(p, stream));
         return KDA_OK;

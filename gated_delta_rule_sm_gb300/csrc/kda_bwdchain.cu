@@ -1,18 +1,24 @@
-// kda_bwdchain.cu -- reverse state chain on tcgen05 tensor cores (bf16 inputs, K = V = 128).
+// kda_bwdchain.cu -- the two state chains of the backward on tcgen05 tensor cores (bf16 inputs,
+// K = V = 128), both with tf32 operands rounded to nearest and the state in fp32 registers.
 //
-// Reverse mode of the chunk recursion of the gated delta rule ("[kimi k3] add eager reference model
-// with FSDP2", chunk_kda backward).  With dS the gradient w.r.t. the state leaving chunk c,
-//     dU  = Y_c + Kd_c dS                                   (64 x V)
-//     dS' = Diag(exp(Gamma_last,c)) dS - W_c^T dU + P_c      (K x V), the gradient entering chunk c,
-// where Y_c = scale Aqk^T dO and P_c = scale Qg^T dO do not depend on dS and come
-// precomputed in the reverse-chain record (bwrec).  Both products run as kind::tf32 MMAs with
-// operands rounded to nearest: the dS chain feeds every gradient, and bf16 operands for Kd dS
-// lose about 0.6% of dS under slowly decaying gates.  dS stays in fp32 registers.
+// Both are the affine recursion  X = Y_c + A1_c Z,  Z' = Diag(exp(Gamma_last,c)) Z + A2_c X (+ P_c)
+// of the chunkwise gated delta rule ("[kimi k3] add eager reference model with FSDP2", chunk_kda):
+//   * forward state recompute (REV = false): Z = S entering chunk c, A1 = -W, Y = U0, A2 = Kd^T,
+//     so X = U and Z' is the state leaving the chunk;
+//   * reverse chain (REV = true): Z = dS, the gradient w.r.t. the state leaving chunk c, A1 = Kd,
+//     Y = scale Aqk^T dO, A2 = -W^T, P = scale Qg^T dO, so X = dU and Z' is the gradient entering
+//     the chunk.
+// The operand copies (records chainrec / bwrec / fwrec) and Y, P come from bwd_pre.  Every product
+// runs in split precision, operand = hi + lo (both tf32), hi*hi + hi*lo + lo*hi: the gradient of
+// the log-decay at the end of a chunk carries dS_end * S_end-sized terms far larger than its
+// typical value, and plain tf32 chains (~2e-4 relative error in S and dS, NumPy emulation and GPU
+// measurement agree) put it outside the bf16 tolerance under slowly decaying gates.
 //
-// One CTA of 128 threads per (segment, head, column slice of JW value columns); the columns of dS
-// are independent.  Thread r owns row r of dS.  Per chunk: MMA1 (M = 64, N = JW, K = 128) into
-// TMEM, dU = D1 + Y rounded to tf32 into shared memory, MMA2 (M = 128, N = JW, K = 64), then
-// dS' = gC dS + D3 + P.  Record slots (Kd, -W^T, gC) are double buffered by bulk copies.
+// One CTA of 128 threads per (segment, head, column slice of JW value columns); the columns of Z
+// are independent.  Thread r owns row r of Z.  Per chunk: MMA1 (M = 64, N = JW, K = 128, three
+// products) into TMEM, X = D1 + Y split into tf32 hi + lo in shared memory, MMA2 (M = 128, N = JW,
+// K = 64, three products), then Z' = gC Z + D3 (+ P).  One record slot per CTA (the split operands
+// fill shared memory); the next chunk's slot is copied in as soon as both MMAs are done.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
@@ -24,10 +30,12 @@ using namespace sm100;
 namespace bwchain {
 template <int JW>
 struct Lay {
-    static constexpr uint32_t SLOT = bwrec::SLOT;          // two record slots at 0 and SLOT
-    static constexpr uint32_t DSB = 2 * SLOT;              // dS^T tf32, JW rows (j) x 128 K (c): km_f32(j, c, 4096, 128)
-    static constexpr uint32_t DUB = DSB + JW * 512;        // dU^T tf32, JW rows (j) x 64 K (t): km_f32(j, t, 2048, 128)
-    static constexpr uint32_t BAR = DUB + JW * 256;        // mbarriers: full[2], mma1, mma2; fail flag; TMEM slot
+    static constexpr uint32_t SLOT = chainrec::SLOT;       // record slot at 0 (A1, A2, gC, A1 lo, A2 lo)
+    static constexpr uint32_t ZB = SLOT;                   // Z^T tf32 hi, JW rows (j) x 128 K (c): km_f32(j, c, 4096, 128)
+    static constexpr uint32_t ZL = ZB + JW * 512;          // Z^T lo
+    static constexpr uint32_t XB = ZL + JW * 512;          // X^T tf32 hi, JW rows (j) x 64 K (t): km_f32(j, t, 2048, 128)
+    static constexpr uint32_t XL = XB + JW * 256;          // X^T lo
+    static constexpr uint32_t BAR = XL + JW * 256;         // mbarriers: full, mma1, mma2; fail flag; TMEM slot
     static constexpr uint32_t BYTES = BAR + 64;
     static constexpr uint32_t TCOLS = 2 * JW;              // D1 at column 0, D3 at column JW
 };
@@ -45,8 +53,19 @@ __device__ __forceinline__ void quad_transpose(float& v0, float& v1, float& v2, 
     if (even) { v1 = h0; v3 = h1; } else { v0 = h0; v2 = h1; }
 }
 
-template <int JW>
-__global__ void __launch_bounds__(128, 1) chain_bwd_tc_kernel(Params p, const uint8_t* bw) {
+// Where a chain finds its per-chunk inputs: slot (A1, A2, gC) of chunk c at slots + (c H + h) *
+// slot_stride bytes; Y rows at ybase + (c H + h) * ystride floats (row t, 128 columns); P likewise.
+struct ChainSrc {
+    const uint8_t* slots;
+    size_t slot_stride;
+    const float* ybase;
+    size_t ystride;
+    const float* pbase;   // reverse chain only
+    size_t pstride;
+};
+
+template <int JW, bool REV>
+__global__ void __launch_bounds__(128, 1) chain_tf32_kernel(Params p, ChainSrc src) {
     using L = bwchain::Lay<JW>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int n = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * JW;
@@ -54,27 +73,31 @@ __global__ void __launch_bounds__(128, 1) chain_bwd_tc_kernel(Params p, const ui
     constexpr int K = 128, V = 128;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r4 = lane & 3;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR);
-    uint64_t* bar1 = full + 2;
-    uint64_t* bar2 = full + 3;
-    int* sh_fail = reinterpret_cast<int*>(full + 4);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(full + 5);
-    uint8_t* DSB = smem + L::DSB;
-    uint8_t* DUB = smem + L::DUB;
+    uint64_t* bar1 = full + 1;
+    uint64_t* bar2 = full + 2;
+    int* sh_fail = reinterpret_cast<int*>(full + 3);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(full + 4);
+    uint8_t* ZB = smem + L::ZB;
+    uint8_t* ZL = smem + L::ZL;
+    uint8_t* XB = smem + L::XB;
+    uint8_t* XL = smem + L::XL;
+    uint8_t* sl = smem;
     const int cb = p.chunk_off[n], ce = p.chunk_off[n + 1];
     const int nch = ce - cb;
 
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(&full[i], 1);
+        for (int i = 0; i < 3; ++i) mbar_init(&full[i], 1);
         *sh_fail = 0;
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(tslot, L::TCOLS);
-    float dS[JW];
+    float dS[JW];   // row tid of Z (dS for the reverse chain, S for the recompute)
     {
-        const float* src = p.dST ? p.dST + (((size_t)n * H + h) * K + tid) * V + j0 : nullptr;
+        const float* z0 = REV ? p.dST : p.S0;
+        const float* zs = z0 ? z0 + (((size_t)n * H + h) * K + tid) * V + j0 : nullptr;
 #pragma unroll
         for (int j = 0; j < JW; j += 4) {
-            const float4 v = src ? *reinterpret_cast<const float4*>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 v = zs ? *reinterpret_cast<const float4*>(zs + j) : make_float4(0.f, 0.f, 0.f, 0.f);
             dS[j] = v.x; dS[j + 1] = v.y; dS[j + 2] = v.z; dS[j + 3] = v.w;
         }
     }
@@ -83,8 +106,13 @@ __global__ void __launch_bounds__(128, 1) chain_bwd_tc_kernel(Params p, const ui
         for (int b = 0; b < JW / 4; ++b) {
             float v0 = tf32_rn(dS[4 * b]), v1 = tf32_rn(dS[4 * b + 1]), v2 = tf32_rn(dS[4 * b + 2]),
                   v3 = tf32_rn(dS[4 * b + 3]);
+            float l0 = tf32_rn(dS[4 * b] - v0), l1 = tf32_rn(dS[4 * b + 1] - v1), l2 = tf32_rn(dS[4 * b + 2] - v2),
+                  l3 = tf32_rn(dS[4 * b + 3] - v3);
             quad_transpose(v0, v1, v2, v3, r4);
-            *reinterpret_cast<float4*>(DSB + km_f32(4 * b + r4, tid - r4, 4096, 128)) = make_float4(v0, v1, v2, v3);
+            quad_transpose(l0, l1, l2, l3, r4);
+            const uint32_t o = km_f32(4 * b + r4, tid - r4, 4096, 128);
+            *reinterpret_cast<float4*>(ZB + o) = make_float4(v0, v1, v2, v3);
+            *reinterpret_cast<float4*>(ZL + o) = make_float4(l0, l1, l2, l3);
         }
     };
     write_dS_operand();
@@ -95,43 +123,54 @@ __global__ void __launch_bounds__(128, 1) chain_bwd_tc_kernel(Params p, const ui
     const uint32_t tmem = *tslot;
     const uint32_t tD1 = tmem, tD3 = tmem + JW;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    auto slot_ptr = [&](int s) { return smem + (s & 1) * L::SLOT; };
-    // step s handles chunk cb + nch - 1 - s
-    auto rec_ptr = [&](int s) { return bw + ((size_t)(cb + nch - 1 - s) * H + h) * bwrec::BYTES; };
+    // step s handles chunk cb + nch - 1 - s (reverse) or cb + s (forward)
+    auto chunk_of = [&](int s) { return REV ? cb + nch - 1 - s : cb + s; };
+    auto rec_ptr = [&](int s) { return src.slots + ((size_t)chunk_of(s) * H + h) * src.slot_stride; };
+    auto y_ptr = [&](int s) { return src.ybase + ((size_t)chunk_of(s) * H + h) * src.ystride; };
+    auto p_ptr = [&](int s) { return src.pbase + ((size_t)chunk_of(s) * H + h) * src.pstride; };
     auto fail_wait = [&](uint64_t* bar, uint32_t parity) {
         if (!mbar_wait(bar, parity)) atomicExch(sh_fail, 1);
     };
-    if (tid == 0)
-        for (int s = 0; s < 2 && s < nch; ++s) {
-            mbar_expect_tx(&full[s], bwrec::SLOT);
-            bulk_g2s(slot_ptr(s), rec_ptr(s), bwrec::SLOT, &full[s]);
-        }
+    if (tid == 0 && nch > 0) {
+        mbar_expect_tx(full, L::SLOT);
+        bulk_g2s(sl, rec_ptr(0), L::SLOT, full);
+    }
 
     bool ok = true;
     for (int s = 0; s < nch; ++s) {
-        const int c = cb + nch - 1 - s;
-        uint8_t* sl = slot_ptr(s);
+        const int c = chunk_of(s);
         const uint32_t par = s & 1;
-        {   // gradient w.r.t. the state leaving chunk c
-            float* dst = p.dstates + (((size_t)c * H + h) * K + tid) * V + j0;
+        {   // reverse: gradient w.r.t. the state leaving chunk c; forward: the state entering chunk c
+            float* dst = (REV ? p.dstates : p.states) + (((size_t)c * H + h) * K + tid) * V + j0;
 #pragma unroll
             for (int j = 0; j < JW; j += 4)
                 *reinterpret_cast<float4*>(dst + j) = make_float4(dS[j], dS[j + 1], dS[j + 2], dS[j + 3]);
         }
-        fail_wait(&full[s & 1], (s >> 1) & 1);
+        fail_wait(full, par);
         tc_fence_after();
-        if (tid == 0) {
-            const uint32_t a = smem_u32(sl + bwrec::KDA), b = smem_u32(DSB);
-#pragma unroll
+        if (tid == 0) {   // D1 = A1_lo Z_hi + A1_hi Z_lo + A1_hi Z_hi
+            const uint32_t a = smem_u32(sl + chainrec::A1), al = smem_u32(sl + chainrec::A1_LO);
+            const uint32_t b = smem_u32(ZB), bl = smem_u32(ZL);
+            constexpr uint32_t id1 = idesc_tf32(64, JW);
+#pragma unroll 1
             for (int kk = 0; kk < 16; ++kk)
-                mma_tf32(tD1, smem_desc(a + kk * 256, 128, 4096), smem_desc(b + kk * 256, 128, 4096),
-                         idesc_tf32(64, JW), kk > 0);
+                mma_tf32(tD1, smem_desc(al + kk * 256, 128, 4096), smem_desc(b + kk * 256, 128, 4096), id1, kk > 0);
+#pragma unroll 1
+            for (int kk = 0; kk < 16; ++kk)
+                mma_tf32(tD1, smem_desc(a + kk * 256, 128, 4096), smem_desc(bl + kk * 256, 128, 4096), id1, 1);
+#pragma unroll 1
+            for (int kk = 0; kk < 16; ++kk)
+                mma_tf32(tD1, smem_desc(a + kk * 256, 128, 4096), smem_desc(b + kk * 256, 128, 4096), id1, 1);
             mma_commit(bar1);
-            if (s + 1 < nch) {   // warm L2 with the next chunk's Y and P
-                const uint8_t* nx = rec_ptr(s + 1) + bwrec::Y;
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(nx)),
-                             "r"(bwrec::BYTES - bwrec::Y)
+            if (s + 1 < nch) {   // warm L2 with the next chunk's Y (and P)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(y_ptr(s + 1))),
+                             "r"(64u * V * 4u)
                              : "memory");
+                if (REV)
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                                     reinterpret_cast<uint64_t>(p_ptr(s + 1))),
+                                 "r"(128u * V * 4u)
+                                 : "memory");
             }
         }
         fail_wait(bar1, par);
@@ -139,7 +178,7 @@ __global__ void __launch_bounds__(128, 1) chain_bwd_tc_kernel(Params p, const ui
         {
             // dU rows t = 16 warp + lane (lanes 0..15 of each warp carry the M = 64 result)
             const int t = 16 * warp + (lane & 15);
-            const float* yrow = reinterpret_cast<const float*>(rec_ptr(s) + bwrec::Y) + t * V + j0;
+            const float* yrow = y_ptr(s) + t * V + j0;
 #pragma unroll
             for (int jb = 0; jb < JW; jb += 32) {
                 float d[32];
@@ -154,12 +193,17 @@ __global__ void __launch_bounds__(128, 1) chain_bwd_tc_kernel(Params p, const ui
                 tmem_ld_wait();
 #pragma unroll
                 for (int b = 0; b < 8; ++b) {
-                    float v0 = tf32_rn(d[4 * b] + y[4 * b]), v1 = tf32_rn(d[4 * b + 1] + y[4 * b + 1]),
-                          v2 = tf32_rn(d[4 * b + 2] + y[4 * b + 2]), v3 = tf32_rn(d[4 * b + 3] + y[4 * b + 3]);
+                    const float x0 = d[4 * b] + y[4 * b], x1 = d[4 * b + 1] + y[4 * b + 1],
+                                x2 = d[4 * b + 2] + y[4 * b + 2], x3 = d[4 * b + 3] + y[4 * b + 3];
+                    float v0 = tf32_rn(x0), v1 = tf32_rn(x1), v2 = tf32_rn(x2), v3 = tf32_rn(x3);
+                    const uint32_t o = km_f32(jb + 4 * b + r4, t - r4, 2048, 128);
+                    float l0 = tf32_rn(x0 - v0), l1 = tf32_rn(x1 - v1), l2 = tf32_rn(x2 - v2), l3 = tf32_rn(x3 - v3);
+                    quad_transpose(l0, l1, l2, l3, r4);
                     quad_transpose(v0, v1, v2, v3, r4);
-                    if (lane < 16)
-                        *reinterpret_cast<float4*>(DUB + km_f32(jb + 4 * b + r4, t - r4, 2048, 128)) =
-                            make_float4(v0, v1, v2, v3);
+                    if (lane < 16) {
+                        *reinterpret_cast<float4*>(XL + o) = make_float4(l0, l1, l2, l3);
+                        *reinterpret_cast<float4*>(XB + o) = make_float4(v0, v1, v2, v3);
+                    }
                 }
             }
         }
@@ -168,19 +212,26 @@ __global__ void __launch_bounds__(128, 1) chain_bwd_tc_kernel(Params p, const ui
         __syncthreads();
         tc_fence_after();
         if (*sh_fail) { ok = false; break; }
-        if (tid == 0) {
-            const uint32_t a = smem_u32(sl + bwrec::WTN), b = smem_u32(DUB);
-#pragma unroll
+        if (tid == 0) {   // D3 = A2_lo X_hi + A2_hi X_lo + A2_hi X_hi
+            const uint32_t a = smem_u32(sl + chainrec::A2), al = smem_u32(sl + chainrec::A2_LO);
+            const uint32_t b = smem_u32(XB), bl = smem_u32(XL);
+            constexpr uint32_t id2 = idesc_tf32(128, JW);
+#pragma unroll 1
             for (int kk = 0; kk < 8; ++kk)
-                mma_tf32(tD3, smem_desc(a + kk * 256, 128, 2048), smem_desc(b + kk * 256, 128, 2048),
-                         idesc_tf32(128, JW), kk > 0);
+                mma_tf32(tD3, smem_desc(al + kk * 256, 128, 2048), smem_desc(b + kk * 256, 128, 2048), id2, kk > 0);
+#pragma unroll 1
+            for (int kk = 0; kk < 8; ++kk)
+                mma_tf32(tD3, smem_desc(a + kk * 256, 128, 2048), smem_desc(bl + kk * 256, 128, 2048), id2, 1);
+#pragma unroll 1
+            for (int kk = 0; kk < 8; ++kk)
+                mma_tf32(tD3, smem_desc(a + kk * 256, 128, 2048), smem_desc(b + kk * 256, 128, 2048), id2, 1);
             mma_commit(bar2);
         }
         fail_wait(bar2, par);
         tc_fence_after();
         {
-            const float gc = reinterpret_cast<const float*>(sl + bwrec::GC)[tid];
-            const float* prow = reinterpret_cast<const float*>(rec_ptr(s) + bwrec::P) + tid * V + j0;
+            const float gc = reinterpret_cast<const float*>(sl + chainrec::GC)[tid];
+            const float* prow = REV ? p_ptr(s) + tid * V + j0 : nullptr;
 #pragma unroll
             for (int jb = 0; jb < JW; jb += 32) {
                 float d[32];
@@ -189,7 +240,7 @@ __global__ void __launch_bounds__(128, 1) chain_bwd_tc_kernel(Params p, const ui
                 float pv[32];
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
-                    const float4 v = *reinterpret_cast<const float4*>(prow + jb + j);
+                    const float4 v = REV ? *reinterpret_cast<const float4*>(prow + jb + j) : make_float4(0.f, 0.f, 0.f, 0.f);
                     pv[j] = v.x; pv[j + 1] = v.y; pv[j + 2] = v.z; pv[j + 3] = v.w;
                 }
                 tmem_ld_wait();
@@ -203,10 +254,10 @@ __global__ void __launch_bounds__(128, 1) chain_bwd_tc_kernel(Params p, const ui
         __syncthreads();
         tc_fence_after();
         if (*sh_fail) { ok = false; break; }
-        // both MMAs of this chunk are complete: the slot takes the chunk two steps ahead
-        if (tid == 0 && s + 2 < nch) {
-            mbar_expect_tx(&full[s & 1], bwrec::SLOT);
-            bulk_g2s(sl, rec_ptr(s + 2), bwrec::SLOT, &full[s & 1]);
+        // both MMAs of this chunk are complete: the slot takes the next chunk
+        if (tid == 0 && s + 1 < nch) {
+            mbar_expect_tx(full, L::SLOT);
+            bulk_g2s(sl, rec_ptr(s + 1), L::SLOT, full);
         }
     }
     __syncthreads();
@@ -216,13 +267,13 @@ __global__ void __launch_bounds__(128, 1) chain_bwd_tc_kernel(Params p, const ui
         // shared and tensor memory are released.
         if (tid == 0) {
             record_error(p.status, KDA_ERR_TIMEOUT);
-            for (int b = 0; b < 4; ++b) {
+            for (int b = 0; b < 3; ++b) {
                 mbar_wait(&full[b], 0, 1u << 12);
                 mbar_wait(&full[b], 1, 1u << 12);
             }
         }
-    } else if (p.dS0) {
-        float* dst = p.dS0 + (((size_t)n * H + h) * K + tid) * V + j0;
+    } else if (REV ? p.dS0 != nullptr : p.ST != nullptr) {
+        float* dst = (REV ? p.dS0 : p.ST) + (((size_t)n * H + h) * K + tid) * V + j0;
 #pragma unroll
         for (int j = 0; j < JW; j += 4)
             *reinterpret_cast<float4*>(dst + j) = make_float4(dS[j], dS[j + 1], dS[j + 2], dS[j + 3]);
@@ -232,28 +283,42 @@ __global__ void __launch_bounds__(128, 1) chain_bwd_tc_kernel(Params p, const ui
     if (warp == 0) tmem_dealloc(tmem, L::TCOLS);
 }
 
-template <int JW>
-static cudaError_t launch_chain_bwd_jw(const Params& p, const uint8_t* bw, cudaStream_t st) {
+template <int JW, bool REV>
+static cudaError_t launch_chain_jw(const Params& p, const ChainSrc& src, cudaStream_t st) {
     using L = bwchain::Lay<JW>;
-    cudaError_t e = cudaFuncSetAttribute(chain_bwd_tc_kernel<JW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    static_assert(L::BYTES <= 232448, "shared memory per CTA");
+    cudaError_t e = cudaFuncSetAttribute(chain_tf32_kernel<JW, REV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)L::BYTES);
     if (e != cudaSuccess) return e;
-    timing_pre(st, K_CHAIN_BWD_TC);
-    chain_bwd_tc_kernel<JW><<<dim3(p.N, p.H, 128 / JW), 128, L::BYTES, st>>>(p, bw);
+    timing_pre(st, REV ? K_CHAIN_BWD_TC : K_CHAIN_REC_TC);
+    chain_tf32_kernel<JW, REV><<<dim3(p.N, p.H, 128 / JW), 128, L::BYTES, st>>>(p, src);
     timing_post(st);
     return cudaGetLastError();
 }
 
-// Column slices per (segment, head) chain: one CTA per chain when the chains alone nearly fill the
-// GPU's SMs, otherwise 2 or 4 narrower CTAs (shorter per-step latency, more parallel chains).
-cudaError_t launch_chain_bwd_tc(const Params& p, const uint8_t* bw, cudaStream_t st) {
+// Column slices per (segment, head) chain: 64 value columns per CTA when the chains fill a third of
+// the SMs, otherwise 32 (more parallel, shorter chains steps).
+template <bool REV>
+static cudaError_t launch_chain(const Params& p, const ChainSrc& src, cudaStream_t st) {
     int sms = 0, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long chains = (long)p.N * p.H;
-    if (chains * 3 >= (long)sms * 2) return launch_chain_bwd_jw<128>(p, bw, st);
-    if (chains * 3 >= (long)sms) return launch_chain_bwd_jw<64>(p, bw, st);
-    return launch_chain_bwd_jw<32>(p, bw, st);
+    if (chains * 3 >= (long)sms) return launch_chain_jw<64, REV>(p, src, st);
+    return launch_chain_jw<32, REV>(p, src, st);
+}
+
+cudaError_t launch_chain_bwd_tc(const Params& p, const uint8_t* bw, cudaStream_t st) {
+    ChainSrc src{bw, bwrec::BYTES, reinterpret_cast<const float*>(bw + bwrec::Y), bwrec::BYTES / 4,
+                 reinterpret_cast<const float*>(bw + bwrec::P), bwrec::BYTES / 4};
+    static_assert(bwrec::BYTES % 256 == 0 && fwrec::BYTES % 256 == 0, "record strides");
+    return launch_chain<true>(p, src, st);
+}
+
+cudaError_t launch_chain_rec_tc(const Params& p, const uint8_t* fw, cudaStream_t st) {
+    const RecLayout L = RecLayout::make(128, 128);
+    ChainSrc src{fw, fwrec::BYTES, p.rec + L.U0, p.rec_stride, nullptr, 0};
+    return launch_chain<false>(p, src, st);
 }
 
 }  // namespace kda

@@ -77,6 +77,53 @@ __device__ __forceinline__ void mma_strip(float (&d)[NB][4], const Tile& A, cons
     }
 }
 
+// Split-precision strip: d += A B with hi*hi + hi*lo + lo*hi products.
+template <int NB>
+__device__ __forceinline__ void mma_strip3(float (&d)[NB][4], const Tile& A, const Tile& B, int m0, int n0, int k_lo,
+                                           int k_hi, int lane) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll 1
+    for (int k0 = k_lo; k0 < k_hi; k0 += 8) {
+        uint32_t ah[4], al[4];
+        split_tf32(A.at(m0 + g, k0 + q), ah[0], al[0]);
+        split_tf32(A.at(m0 + g + 8, k0 + q), ah[1], al[1]);
+        split_tf32(A.at(m0 + g, k0 + q + 4), ah[2], al[2]);
+        split_tf32(A.at(m0 + g + 8, k0 + q + 4), ah[3], al[3]);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            uint32_t bh[2], bl[2];
+            split_tf32(B.at(k0 + q, n0 + 8 * b + g), bh[0], bl[0]);
+            split_tf32(B.at(k0 + q + 4, n0 + 8 * b + g), bh[1], bl[1]);
+            mma1688(d[b], al, bh);
+            mma1688(d[b], ah, bl);
+            mma1688(d[b], ah, bh);
+        }
+    }
+}
+
+// Strip with the left operand split (d += A_lo B + A_hi B): for a right operand that is exact in tf32.
+template <int NB>
+__device__ __forceinline__ void mma_strip_splitA(float (&d)[NB][4], const Tile& A, const Tile& B, int m0, int n0,
+                                                 int k_lo, int k_hi, int lane) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll 1
+    for (int k0 = k_lo; k0 < k_hi; k0 += 8) {
+        uint32_t ah[4], al[4];
+        split_tf32(A.at(m0 + g, k0 + q), ah[0], al[0]);
+        split_tf32(A.at(m0 + g + 8, k0 + q), ah[1], al[1]);
+        split_tf32(A.at(m0 + g, k0 + q + 4), ah[2], al[2]);
+        split_tf32(A.at(m0 + g + 8, k0 + q + 4), ah[3], al[3]);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            uint32_t bb[2];
+            bb[0] = tf32(B.at(k0 + q, n0 + 8 * b + g));
+            bb[1] = tf32(B.at(k0 + q + 4, n0 + 8 * b + g));
+            mma1688(d[b], al, bb);
+            mma1688(d[b], ah, bb);
+        }
+    }
+}
+
 // Split-precision strip for two left operands sharing the right one: d1 += A1 B, d2 += A2 B with
 // hi*hi + hi*lo + lo*hi products.
 template <int NB>
@@ -307,7 +354,9 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         // slice contributions to dKg (-dY S0^T), dQg (dO S0^T), dKd (U dS^T), dT (dU Vt^T), dA (dO U^T)
         mma_strip<8>(aKg, Tile{sdY, P32, 1}, Tile{sS0, 1, P32}, wm0, 64 * (warp & 1), 0, 32, lane);
         mma_strip<8>(aQg, Tile{sdO, P32, 1}, Tile{sS0, 1, P32}, wm0, 64 * (warp & 1), 0, 32, lane);
-        mma_strip<8>(aKd, Tile{sU, P32, 1}, Tile{sdS, 1, P32}, wm0, 64 * (warp & 1), 0, 32, lane);
+        // dKd enters dGamma twice (-dKd Kd per token, +sum_t dKd Kd at Gamma_last) and the two cancel in
+        // the reverse cumulative sum: split precision
+        mma_strip3<8>(aKd, Tile{sU, P32, 1}, Tile{sdS, 1, P32}, wm0, 64 * (warp & 1), 0, 32, lane);
         mma_strip<4>(aT, Tile{sdU, P32, 1}, Tile{sVt, 1, P32}, wm0, 32 * (warp & 1), 0, 32, lane);
         mma_strip<4>(aA, Tile{sdO, P32, 1}, Tile{sU, 1, P32}, wm0, 32 * (warp & 1), 0, 32, lane);
         if (tid < K) {
@@ -617,8 +666,9 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
 // ------------------------------------------------------------------ reverse-chain operands
 //
 // Per (chunk, head): the dS-independent terms of the reverse recursion, Y = scale Aqk^T dO and
-// P = scale Qg^T dO (warp tf32 MMAs, fp32 results), plus Kd and -W^T rounded to tf32 in the
-// K-major layouts the reverse chain's tcgen05 MMAs read (record layout: bwrec).
+// P = scale Qg^T dO (warp tf32 MMAs with the left operand split into hi + lo; dO is bf16 and exact
+// in tf32), plus the split tf32 K-major operands of the two tcgen05 chains of the backward: Kd and
+// -W^T for the reverse chain (record bwrec), -W and Kd^T for the forward state recompute (fwrec).
 namespace {
 constexpr int PB_A = 0;                  // [64][P64]   Aqk
 constexpr int PB_Q = PB_A + 64 * P64;    // [64][P128]  Qg
@@ -626,7 +676,7 @@ constexpr int PB_D = PB_Q + 64 * P128;   // [64][P128]  dO
 constexpr int PB_FLOATS = PB_D + 64 * P128;
 }  // namespace
 
-__global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) {
+__global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw, uint8_t* fw) {
     extern __shared__ float sm[];
     const int c = blockIdx.x, h = blockIdx.y;
     if (c >= p.chunk_off[p.N]) return;
@@ -639,6 +689,7 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) 
     const RecLayout L = RecLayout::make(K, V);
     const float* rec = p.rec + ((size_t)c * H + h) * p.rec_stride;
     uint8_t* out = bw + ((size_t)c * H + h) * bwrec::BYTES;
+    uint8_t* fout = fw + ((size_t)c * H + h) * fwrec::BYTES;
     float* sA = sm + PB_A;
     float* sQ = sm + PB_Q;
     float* sD = sm + PB_D;
@@ -665,22 +716,41 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) 
 #pragma unroll
         for (int e = 0; e < 8; ++e) sD[t * P128 + j8 + e] = f[e];
     }
-    // Kd -> tf32 K-major (rows t, K = c); -W^T -> tf32 K-major (rows c, K = t); exp(Gamma_last)
+    // Chain operands as tf32 hi + lo in the K-major layouts of chainrec.  Reverse chain: A1 = Kd
+    // (rows t, K = c), A2 = -W^T (rows c, K = t).  Forward recompute: A1 = -W, A2 = Kd^T.
+    auto put_split = [](uint8_t* base, uint32_t hi_off, uint32_t lo_off, uint32_t o, float4 v, float sg) {
+        const float x[4] = {sg * v.x, sg * v.y, sg * v.z, sg * v.w};
+        float hv[4], lv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            hv[e] = __uint_as_float(tf32(x[e]));
+            lv[e] = __uint_as_float(tf32(x[e] - hv[e]));
+        }
+        *reinterpret_cast<float4*>(base + hi_off + o) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+        *reinterpret_cast<float4*>(base + lo_off + o) = make_float4(lv[0], lv[1], lv[2], lv[3]);
+    };
     for (int i = tid; i < 64 * K / 4; i += 256) {
         const int t = i >> 5, c4 = (i & 31) * 4;
-        const float4 v = *reinterpret_cast<const float4*>(rec + L.Kd + t * K + c4);
-        *reinterpret_cast<float4*>(out + bwrec::KDA + km_f32(t, c4, 4096, 128)) =
-            make_float4(__uint_as_float(tf32(v.x)), __uint_as_float(tf32(v.y)), __uint_as_float(tf32(v.z)),
-                        __uint_as_float(tf32(v.w)));
+        const uint32_t o = km_f32(t, c4, 4096, 128);
+        put_split(out, chainrec::A1, chainrec::A1_LO, o, *reinterpret_cast<const float4*>(rec + L.Kd + t * K + c4), 1.f);
+        put_split(fout, chainrec::A1, chainrec::A1_LO, o, *reinterpret_cast<const float4*>(rec + L.W + t * K + c4), -1.f);
     }
     for (int i = tid; i < K * 16; i += 256) {
         const int cc = i & 127, t4 = (i >> 7) * 4;
-        float v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = -__uint_as_float(tf32(rec[L.W + (t4 + u) * K + cc]));
-        *reinterpret_cast<float4*>(out + bwrec::WTN + km_f32(cc, t4, 2048, 128)) = make_float4(v[0], v[1], v[2], v[3]);
+        float4 w, kd;
+        w.x = rec[L.W + t4 * K + cc]; w.y = rec[L.W + (t4 + 1) * K + cc];
+        w.z = rec[L.W + (t4 + 2) * K + cc]; w.w = rec[L.W + (t4 + 3) * K + cc];
+        kd.x = rec[L.Kd + t4 * K + cc]; kd.y = rec[L.Kd + (t4 + 1) * K + cc];
+        kd.z = rec[L.Kd + (t4 + 2) * K + cc]; kd.w = rec[L.Kd + (t4 + 3) * K + cc];
+        const uint32_t o = km_f32(cc, t4, 2048, 128);
+        put_split(out, chainrec::A2, chainrec::A2_LO, o, w, -1.f);
+        put_split(fout, chainrec::A2, chainrec::A2_LO, o, kd, 1.f);
     }
-    if (tid < K) reinterpret_cast<float*>(out + bwrec::GC)[tid] = rec[L.gC + tid];
+    if (tid < K) {
+        const float gc = rec[L.gC + tid];
+        reinterpret_cast<float*>(out + chainrec::GC)[tid] = gc;
+        reinterpret_cast<float*>(fout + chainrec::GC)[tid] = gc;
+    }
     cp_async_wait_all();
     __syncthreads();
     // Y = scale Aqk^T dO (64 x 128): warp w owns rows 16 (w / 2) and columns 64 (w % 2) .. + 64.
@@ -693,7 +763,7 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) 
         for (int b = 0; b < 8; ++b)
 #pragma unroll
             for (int e = 0; e < 4; ++e) d[b][e] = 0.f;
-        mma_strip<8>(d, Tile{sA, 1, P64}, Tile{sD, P128, 1}, m0, n0, m0, 64, lane);
+        mma_strip_splitA<8>(d, Tile{sA, 1, P64}, Tile{sD, P128, 1}, m0, n0, m0, 64, lane);
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
             int r, cc;
@@ -713,7 +783,7 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) 
             for (int b = 0; b < 8; ++b)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) a1[b][e] = 0.f;
-            mma_strip<8>(a1, Tile{sQ, 1, P128}, Tile{sD, P128, 1}, m0, 64 * half, 0, 64, lane);
+            mma_strip_splitA<8>(a1, Tile{sQ, 1, P128}, Tile{sD, P128, 1}, m0, 64 * half, 0, 64, lane);
 #pragma unroll
             for (int b = 0; b < 8; ++b) {
                 int r, cc;
@@ -725,12 +795,12 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) 
     }
 }
 
-cudaError_t launch_bwd_pre(const Params& p, uint8_t* bw, cudaStream_t st) {
+cudaError_t launch_bwd_pre(const Params& p, uint8_t* bw, uint8_t* fw, cudaStream_t st) {
     const size_t smem = (size_t)PB_FLOATS * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(bwd_pre_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     timing_pre(st, K_BWD_PRE);
-    bwd_pre_kernel<<<dim3(p.NCmax, p.H), 256, smem, st>>>(p, bw);
+    bwd_pre_kernel<<<dim3(p.NCmax, p.H), 256, smem, st>>>(p, bw, fw);
     timing_post(st);
     return cudaGetLastError();
 }

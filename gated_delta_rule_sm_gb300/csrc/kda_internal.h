@@ -62,23 +62,38 @@ struct GradScratch {
 // Kernel ids for kda_kernel_name / kda_timing_end.
 enum KernelId {
     K_PLAN = 0, K_INTRA_SIMT, K_CHAIN_FWD_SIMT, K_CHAIN_BWD_SIMT, K_GRAD_SIMT, K_PARAM_REDUCE, K_EMPTY_SEG,
-    K_INTRA_TC, K_CHAIN_FWD_TC, K_GRAD_TC, K_BWD_PRE, K_CHAIN_BWD_TC, K_NUM_KERNELS
+    K_INTRA_TC, K_CHAIN_FWD_TC, K_GRAD_TC, K_BWD_PRE, K_CHAIN_BWD_TC, K_CHAIN_REC_TC, K_NUM_KERNELS
 };
 
-// Reverse-chain record per (chunk, head), K = V = 128 (bytes).  The first SLOT bytes are the
-// operands of the chain's two tcgen05 MMAs in their shared-memory layouts (moved by one bulk
-// copy); Y and P are the terms of the reverse recursion that do not depend on dS:
-//     dU = Y + Kd dS,   dS' = Diag(exp(Gamma_last)) dS - W^T dU + P,
-//     Y = scale Aqk^T dO,   P = scale Qg^T dO.
-namespace bwrec {
-constexpr uint32_t KDA = 0;          // Kd    tf32, 64 rows (t) x 128 K (c), K-major km_f32(t, c, 4096, 128)
-constexpr uint32_t WTN = 32768;      // -W^T  tf32, 128 rows (c) x 64 K (t), K-major km_f32(c, t, 2048, 128)
+// Records of the two tcgen05 state chains of the backward, per (chunk, head), K = V = 128 (bytes).
+// Both chains run  X = Y + A1 Z,  Z' = Diag(exp(Gamma_last)) Z + A2 X (+ P)  with every product in
+// split precision (operand = hi + lo, both tf32; hi*hi + hi*lo + lo*hi): the gradient of the
+// log-decay at the end of a chunk carries sum dS_end * S_end-sized terms that are far larger than
+// its typical value, so the states and state gradients need ~2^-16 relative accuracy.
+// The first SLOT bytes are the operands in their shared-memory layouts (one bulk copy per chunk):
+namespace chainrec {
+constexpr uint32_t A1 = 0;           // 64 rows (t) x 128 K (c), tf32 K-major km_f32(t, c, 4096, 128), hi
+constexpr uint32_t A2 = 32768;       // 128 rows (c) x 64 K (t), tf32 K-major km_f32(c, t, 2048, 128), hi
 constexpr uint32_t GC = 65536;       // exp(Gamma_last) fp32 [128]
-constexpr uint32_t SLOT = 66048;     // bytes moved into shared memory per chunk
-constexpr uint32_t Y = 66048;        // fp32 [64 t][128 j]
-constexpr uint32_t P = 98816;        // fp32 [128 c][128 j]
-constexpr uint32_t BYTES = 164352;   // record stride (256-byte multiple)
+constexpr uint32_t A1_LO = 66048;    // lo halves, same layouts
+constexpr uint32_t A2_LO = 98816;
+constexpr uint32_t SLOT = 131584;
+}  // namespace chainrec
+
+// Reverse chain (Z = dS, the gradient w.r.t. the state leaving chunk c): A1 = Kd, A2 = -W^T,
+// Y = scale Aqk^T dO, P = scale Qg^T dO, so X = dU:
+//     dU = Y + Kd dS,   dS' = Diag(exp(Gamma_last)) dS - W^T dU + P.
+namespace bwrec {
+constexpr uint32_t Y = chainrec::SLOT;          // fp32 [64 t][128 j]
+constexpr uint32_t P = Y + 32768;               // fp32 [128 c][128 j]
+constexpr uint32_t BYTES = P + 65536;           // record stride (256-byte multiple)
 }  // namespace bwrec
+
+// Forward state recompute (Z = S entering chunk c): A1 = -W, A2 = Kd^T, Y = U0 (read from the fp32
+// backward record), no P:   U = U0 - W S,   S' = Diag(exp(Gamma_last)) S + Kd^T U.
+namespace fwrec {
+constexpr uint32_t BYTES = chainrec::SLOT;
+}  // namespace fwrec
 
 // Launch bracketing for kda_timing_*: no-ops unless timing is active.
 void timing_pre(cudaStream_t st, int kernel_id);
@@ -91,8 +106,9 @@ cudaError_t launch_chain_bwd_simt(const Params& p, cudaStream_t st);
 cudaError_t launch_grad_simt(const Params& p, cudaStream_t st);
 cudaError_t launch_param_reduce(const Params& p, cudaStream_t st);
 cudaError_t launch_grad_tc(const Params& p, cudaStream_t st);
-cudaError_t launch_bwd_pre(const Params& p, uint8_t* bw, cudaStream_t st);
+cudaError_t launch_bwd_pre(const Params& p, uint8_t* bw, uint8_t* fw, cudaStream_t st);
 cudaError_t launch_chain_bwd_tc(const Params& p, const uint8_t* bw, cudaStream_t st);
+cudaError_t launch_chain_rec_tc(const Params& p, const uint8_t* fw, cudaStream_t st);
 
 // tensor-core path (bf16, K = V = 128)
 size_t tc_record_bytes(int NCmax, int H);
