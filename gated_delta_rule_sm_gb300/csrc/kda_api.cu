@@ -88,7 +88,6 @@ static TcPlan plan_tc_fwd(const Shape& s) {
 
 struct TcBwdPlan {
     WsPlan simt;        // chunk table, fp32 backward records, states, partials, scratch
-    size_t off_tcrec;   // tensor-core forward records (recompute chain)
     size_t off_bwrec;   // reverse-chain records
     size_t off_fwrec;   // forward-recompute chain records
     size_t total;
@@ -98,7 +97,6 @@ static TcBwdPlan plan_tc_bwd(const Shape& s) {
     TcBwdPlan w;
     w.simt = plan_simt(s, true);
     size_t o = w.simt.total;
-    w.off_tcrec = o; o = align_up(o + tc_record_bytes(s.NCmax, s.H));
     w.off_bwrec = o; o = align_up(o + (size_t)s.NCmax * s.H * bwrec::BYTES);
     w.off_fwrec = o; o = align_up(o + (size_t)s.NCmax * s.H * fwrec::BYTES);
     w.total = o;
@@ -325,12 +323,11 @@ kda_status kda_bwd(const kda_dims* dims, const void* q, const void* k, const voi
         st = status_ptr(&p.status);
         if (st != KDA_OK) return st;
         carve(p, w.simt, workspace);
-        uint8_t* recs = static_cast<uint8_t*>(workspace) + w.off_tcrec;
         Params pf = p;
         pf.out = nullptr;
         pf.ST = nullptr;
         KDA_TRY_CUDA(launch_plan(p, stream));
-        KDA_TRY_CUDA(launch_intra_tc(p, recs, true, stream));
+        KDA_TRY_CUDA(launch_intra_tc(p, nullptr, true, stream));
         uint8_t* bw = static_cast<uint8_t*>(workspace) + w.off_bwrec;
         uint8_t* fw = static_cast<uint8_t*>(workspace) + w.off_fwrec;
         KDA_TRY_CUDA(launch_bwd_pre(p, bw, fw, stream));

@@ -22,7 +22,8 @@
 
 namespace kda {
 
-using sm100::km_f32;
+using sm100::km_bf16;
+using sm100::pack8_bf16;
 
 namespace {
 
@@ -667,7 +668,7 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
 //
 // Per (chunk, head): the dS-independent terms of the reverse recursion, Y = scale Aqk^T dO and
 // P = scale Qg^T dO (warp tf32 MMAs with the left operand split into hi + lo; dO is bf16 and exact
-// in tf32), plus the split tf32 K-major operands of the two tcgen05 chains of the backward: Kd and
+// in tf32), plus the split bf16 K-major operands of the two tcgen05 chains of the backward: Kd and
 // -W^T for the reverse chain (record bwrec), -W and Kd^T for the forward state recompute (fwrec).
 namespace {
 constexpr int PB_A = 0;                  // [64][P64]   Aqk
@@ -716,35 +717,42 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw, 
 #pragma unroll
         for (int e = 0; e < 8; ++e) sD[t * P128 + j8 + e] = f[e];
     }
-    // Chain operands as tf32 hi + lo in the K-major layouts of chainrec.  Reverse chain: A1 = Kd
+    // Chain operands as bf16 hi + lo in the K-major layouts of chainrec.  Reverse chain: A1 = Kd
     // (rows t, K = c), A2 = -W^T (rows c, K = t).  Forward recompute: A1 = -W, A2 = Kd^T.
-    auto put_split = [](uint8_t* base, uint32_t hi_off, uint32_t lo_off, uint32_t o, float4 v, float sg) {
-        const float x[4] = {sg * v.x, sg * v.y, sg * v.z, sg * v.w};
-        float hv[4], lv[4];
+    auto put_split8 = [](uint8_t* base, uint32_t o, const float* v, float sg) {
+        float hv[8], lv[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            hv[e] = __uint_as_float(tf32(x[e]));
-            lv[e] = __uint_as_float(tf32(x[e] - hv[e]));
+        for (int e = 0; e < 8; ++e) {
+            const float x = sg * v[e];
+            hv[e] = __bfloat162float(__float2bfloat16_rn(x));
+            lv[e] = x - hv[e];
         }
-        *reinterpret_cast<float4*>(base + hi_off + o) = make_float4(hv[0], hv[1], hv[2], hv[3]);
-        *reinterpret_cast<float4*>(base + lo_off + o) = make_float4(lv[0], lv[1], lv[2], lv[3]);
+        *reinterpret_cast<uint4*>(base + o) = pack8_bf16(hv);
+        *reinterpret_cast<uint4*>(base + o + (chainrec::A1_LO - chainrec::A1)) = pack8_bf16(lv);
     };
-    for (int i = tid; i < 64 * K / 4; i += 256) {
-        const int t = i >> 5, c4 = (i & 31) * 4;
-        const uint32_t o = km_f32(t, c4, 4096, 128);
-        put_split(out, chainrec::A1, chainrec::A1_LO, o, *reinterpret_cast<const float4*>(rec + L.Kd + t * K + c4), 1.f);
-        put_split(fout, chainrec::A1, chainrec::A1_LO, o, *reinterpret_cast<const float4*>(rec + L.W + t * K + c4), -1.f);
+    for (int i = tid; i < 64 * K / 8; i += 256) {
+        const int t = i >> 4, c8 = (i & 15) * 8;
+        float kd[8], w[8];
+        *reinterpret_cast<float4*>(kd) = *reinterpret_cast<const float4*>(rec + L.Kd + t * K + c8);
+        *reinterpret_cast<float4*>(kd + 4) = *reinterpret_cast<const float4*>(rec + L.Kd + t * K + c8 + 4);
+        *reinterpret_cast<float4*>(w) = *reinterpret_cast<const float4*>(rec + L.W + t * K + c8);
+        *reinterpret_cast<float4*>(w + 4) = *reinterpret_cast<const float4*>(rec + L.W + t * K + c8 + 4);
+        const uint32_t o = chainrec::A1 + km_bf16(t, c8, 2048, 128);
+        put_split8(out, o, kd, 1.f);
+        put_split8(fout, o, w, -1.f);
     }
-    for (int i = tid; i < K * 16; i += 256) {
-        const int cc = i & 127, t4 = (i >> 7) * 4;
-        float4 w, kd;
-        w.x = rec[L.W + t4 * K + cc]; w.y = rec[L.W + (t4 + 1) * K + cc];
-        w.z = rec[L.W + (t4 + 2) * K + cc]; w.w = rec[L.W + (t4 + 3) * K + cc];
-        kd.x = rec[L.Kd + t4 * K + cc]; kd.y = rec[L.Kd + (t4 + 1) * K + cc];
-        kd.z = rec[L.Kd + (t4 + 2) * K + cc]; kd.w = rec[L.Kd + (t4 + 3) * K + cc];
-        const uint32_t o = km_f32(cc, t4, 2048, 128);
-        put_split(out, chainrec::A2, chainrec::A2_LO, o, w, -1.f);
-        put_split(fout, chainrec::A2, chainrec::A2_LO, o, kd, 1.f);
+    for (int i = tid; i < K * 8; i += 256) {
+        const int cc = i & 127, t8 = (i >> 7) * 8;
+        float w[8], kd[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            w[u] = rec[L.W + (t8 + u) * K + cc];
+            kd[u] = rec[L.Kd + (t8 + u) * K + cc];
+        }
+        const uint32_t o = chainrec::A2 + km_bf16(cc, t8, 1024, 128);
+        static_assert(chainrec::A2_LO - chainrec::A2 == chainrec::A1_LO - chainrec::A1, "lo halves at one offset");
+        put_split8(out, o, w, -1.f);
+        put_split8(fout, o, kd, 1.f);
     }
     if (tid < K) {
         const float gc = rec[L.gC + tid];

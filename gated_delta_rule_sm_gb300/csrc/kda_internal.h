@@ -67,17 +67,18 @@ enum KernelId {
 
 // Records of the two tcgen05 state chains of the backward, per (chunk, head), K = V = 128 (bytes).
 // Both chains run  X = Y + A1 Z,  Z' = Diag(exp(Gamma_last)) Z + A2 X (+ P)  with every product in
-// split precision (operand = hi + lo, both tf32; hi*hi + hi*lo + lo*hi): the gradient of the
-// log-decay at the end of a chunk carries sum dS_end * S_end-sized terms that are far larger than
-// its typical value, so the states and state gradients need ~2^-16 relative accuracy.
-// The first SLOT bytes are the operands in their shared-memory layouts (one bulk copy per chunk):
+// split precision: operand = hi + lo, both bf16 (hi = bf16(x), lo = bf16(x - hi)), and the products
+// hi*hi + hi*lo + lo*hi (relative error ~1e-5).  The gradient of the log-decay at the end of a chunk
+// carries dS_end * S_end-sized terms far larger than its typical value, so the states and state
+// gradients need far better than tf32's 2^-11.  The first SLOT bytes are the two left operands in
+// their shared-memory layouts (one bulk copy per chunk):
 namespace chainrec {
-constexpr uint32_t A1 = 0;           // 64 rows (t) x 128 K (c), tf32 K-major km_f32(t, c, 4096, 128), hi
-constexpr uint32_t A2 = 32768;       // 128 rows (c) x 64 K (t), tf32 K-major km_f32(c, t, 2048, 128), hi
+constexpr uint32_t A1 = 0;           // 64 rows (t) x 128 K (c), bf16 K-major km_bf16(t, c, 2048, 128), hi
+constexpr uint32_t A1_LO = 16384;    // lo
+constexpr uint32_t A2 = 32768;       // 128 rows (c) x 64 K (t), bf16 K-major km_bf16(c, t, 1024, 128), hi
+constexpr uint32_t A2_LO = 49152;    // lo
 constexpr uint32_t GC = 65536;       // exp(Gamma_last) fp32 [128]
-constexpr uint32_t A1_LO = 66048;    // lo halves, same layouts
-constexpr uint32_t A2_LO = 98816;
-constexpr uint32_t SLOT = 131584;
+constexpr uint32_t SLOT = 66048;
 }  // namespace chainrec
 
 // Reverse chain (Z = dS, the gradient w.r.t. the state leaving chunk c): A1 = Kd, A2 = -W^T,

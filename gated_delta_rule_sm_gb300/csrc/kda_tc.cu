@@ -62,8 +62,8 @@ constexpr uint32_t BAR = SMALL + (64 * 3 + 128 + 1024) * 4;
 constexpr uint32_t BYTES = BAR + 64;
 }  // namespace intralay
 
-// BWD = true additionally writes the fp32 per-chunk record (RecLayout, backward fields) that the
-// backward's reverse chain and gradient kernels read.
+// BWD = false writes the chain record (tcrec) of the forward; BWD = true writes the fp32 per-chunk
+// record (RecLayout) that the backward's operand, chain and gradient kernels read instead.
 template <bool BWD>
 __global__ void __launch_bounds__(256, 1)
     intra_tc_kernel(Params p, uint8_t* recs, const __grid_constant__ CUtensorMap tm_q,
@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(256, 1)
     uint64_t* bar_a = bar_load + 1;   // MMAs reading tile pair A (and the final W / U0 MMAs)
     uint64_t* bar_b = bar_load + 2;   // MMAs reading tile pair B
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_load + 3);
-    uint8_t* rec = recs + ((size_t)c * H + h) * tcrec::BYTES;
+    uint8_t* rec = BWD ? nullptr : recs + ((size_t)c * H + h) * tcrec::BYTES;
 
     if (tid == 0) {
         mbar_init(bar_load, 1);
@@ -115,20 +115,31 @@ __global__ void __launch_bounds__(256, 1)
     bool ok = __syncthreads_and(mbar_wait(bar_load, 0) ? 1 : 0) != 0;
     if (!ok) goto fail;
 
-    // ---- per-token inverse norms (warp w: tokens 8w .. 8w+7)
-    for (int u = 0; u < 8; ++u) {
-        const int t = warp * 8 + u;
-        const uint2 qv = *reinterpret_cast<const uint2*>(smem + RAW_Q + t * 256 + lane * 8);
-        const uint2 kv = *reinterpret_cast<const uint2*>(smem + RAW_K + t * 256 + lane * 8);
-        const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv.x));
-        const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv.y));
-        const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.x));
-        const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.y));
-        float sq = q0.x * q0.x + q0.y * q0.y + q1.x * q1.x + q1.y * q1.y;
-        float sk = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
-        sq = warp_sum(sq);
-        sk = warp_sum(sk);
-        if (lane == 0) {
+    // ---- per-token inverse norms (warp w: tokens 8w .. 8w+7; the 16 reductions interleave)
+    {
+        float ss[16];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int t = warp * 8 + u;
+            const uint2 qv = *reinterpret_cast<const uint2*>(smem + RAW_Q + t * 256 + lane * 8);
+            const uint2 kv = *reinterpret_cast<const uint2*>(smem + RAW_K + t * 256 + lane * 8);
+            const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv.x));
+            const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv.y));
+            const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.x));
+            const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.y));
+            ss[u] = q0.x * q0.x + q0.y * q0.y + q1.x * q1.x + q1.y * q1.y;
+            ss[8 + u] = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], o);
+        if (lane < 8) {
+            const int t = warp * 8 + lane;
+            float sq = ss[0], sk = ss[8];
+#pragma unroll
+            for (int u = 1; u < 8; ++u)
+                if (lane == u) { sq = ss[u]; sk = ss[8 + u]; }
             rq[t] = t < len ? 1.0f / sqrtf(sq + kNormEps) : 0.f;
             rk[t] = t < len ? 1.0f / sqrtf(sk + kNormEps) : 0.f;
         }
@@ -218,7 +229,7 @@ __global__ void __launch_bounds__(256, 1)
             fj[ci][1] = bi == 1 ? fd : bi == 2 ? 1.f : bi == 3 ? fm2 : 0.f;
             fj[ci][2] = bi == 2 ? fd : bi == 3 ? 1.f : 0.f;
             fj[ci][3] = bi == 3 ? fd : 0.f;
-            if (bi == 0) reinterpret_cast<float*>(rec + tcrec::GC)[cc] = B0 * B1 * B2 * B3;
+            if (!BWD && bi == 0) reinterpret_cast<float*>(rec + tcrec::GC)[cc] = B0 * B1 * B2 * B3;
             if (BWD) {
                 float gpre = 0.f;
                 for (int m = 0; m < bi; ++m) gpre += sgsum[m * 128 + cc];
@@ -248,11 +259,11 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 *reinterpret_cast<uint4*>(smem + KVB + km_bf16(cc, tb, 1024, 128)) = pack8_bf16(vk);
                 *reinterpret_cast<uint4*>(smem + KGLO + km_bf16(cc, tb, 1024, 128)) = pack8_bf16(vkl);
-                *reinterpret_cast<uint4*>(rec + tcrec::WQ + mn_bf16(64 + tb, cc, 128, 2048)) = pack8_bf16(vq);
+                if (!BWD) *reinterpret_cast<uint4*>(rec + tcrec::WQ + mn_bf16(64 + tb, cc, 128, 2048)) = pack8_bf16(vq);
             }
-            // Kd^T (tf32): k * exp(Gamma_C - Gamma_t), four tokens per 16 B
+            // Kd^T (tf32): k * exp(Gamma_C - Gamma_t), four tokens per 16 B (forward record only)
 #pragma unroll
-            for (int qd = 0; qd < 4; ++qd) {
+            for (int qd = 0; qd < (BWD ? 0 : 4); ++qd) {
                 const int u = 4 * qd;
                 float kb[4];
 #pragma unroll
@@ -372,7 +383,7 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 const int t = tid - 64;
 #pragma unroll
-                for (int s4 = 0; s4 < 64; s4 += 4) {
+                for (int s4 = 0; s4 < (BWD ? 0 : 64); s4 += 4) {
                     float4 v4;
                     v4.x = tf32_rn(s4 <= t ? d[s4] : 0.f);
                     v4.y = tf32_rn(s4 + 1 <= t ? d[s4 + 1] : 0.f);
@@ -482,17 +493,20 @@ __global__ void __launch_bounds__(256, 1)
             tmem_ld_wait();
             if (warp < 4) {
                 const int cc = tid;
+                if (!BWD)
 #pragma unroll
-                for (int tb = 0; tb < 64; tb += 8)
-                    *reinterpret_cast<uint4*>(rec + tcrec::WQ + mn_bf16(tb, cc, 128, 2048)) = pack8_bf16(d + tb);
+                    for (int tb = 0; tb < 64; tb += 8)
+                        *reinterpret_cast<uint4*>(rec + tcrec::WQ + mn_bf16(tb, cc, 128, 2048)) = pack8_bf16(d + tb);
                 if (BWD)
 #pragma unroll
                     for (int t = 0; t < 64; ++t) frec[RL.W + t * 128 + cc] = d[t];
             } else {
                 const int j = tid - 128;
                 float4* dst = reinterpret_cast<float4*>(rec + tcrec::U0 + j * 256);
+                if (!BWD)
 #pragma unroll
-                for (int t4 = 0; t4 < 16; ++t4) dst[t4] = make_float4(d[4 * t4], d[4 * t4 + 1], d[4 * t4 + 2], d[4 * t4 + 3]);
+                    for (int t4 = 0; t4 < 16; ++t4)
+                        dst[t4] = make_float4(d[4 * t4], d[4 * t4 + 1], d[4 * t4 + 2], d[4 * t4 + 3]);
                 if (BWD)
 #pragma unroll
                     for (int t = 0; t < 64; ++t) frec[RL.U0 + t * 128 + j] = d[t];
