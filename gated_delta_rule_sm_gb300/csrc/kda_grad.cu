@@ -194,6 +194,8 @@ constexpr int O_VT = O_U + 64 * P32;        // [64][P32]   v - Kg S0 slice (star
 constexpr int O_DU = O_VT + 64 * P32;       // [64][P32]   dU slice
 constexpr int O_DY = O_DU + 64 * P32;       // [64][P32]   dY slice
 constexpr int O_BETA = O_DY + 64 * P32;     // [64]
+constexpr int O_GRAW = O_DO + 64 * P64;    // bf16 [64][128] g_raw tile, phase 2 (after dB: tmp is dead)
+static_assert(O_GRAW >= O_DS + 64 * P128 && O_GRAW + 64 * 128 / 2 <= O_BETA, "g_raw tile inside the free tail");
 constexpr int O_RED = O_BETA + 64;          // [64] dbeta, [128] Gamma_last gradient, [8] block sums, [256] dt_bias parts
 constexpr int SMEM_FLOATS = O_RED + 64 + 128 + 8 + 256;
 
@@ -242,6 +244,24 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         cp_async16(sN + t * P64 + s4, rec + L.N + t * 64 + s4);
     }
     if (tid < 16) cp_async16(sbeta + 4 * tid, rec + L.beta + 4 * tid);
+    // warm L2 with the state slices, U0, dout and v that the four V-slice loads read
+    if (tid == 0) {
+        const uint32_t kv = K * V * 4u;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(S0g)), "r"(kv) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(dSg)), "r"(kv) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(rec + L.U0)),
+                     "r"(64u * V * 4u)
+                     : "memory");
+    }
+    if (tid >= 64 && tid < 64 + len) {   // one 256-byte row of dout and of v per token
+        const size_t row = ((size_t)(tok0 + tid - 64) * H + h) * V;
+        const char* po = reinterpret_cast<const char*>(static_cast<const __nv_bfloat16*>(p.dout) + row);
+        const char* pv = reinterpret_cast<const char*>(static_cast<const __nv_bfloat16*>(p.v) + row);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(po));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(po + 128));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(pv));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(pv + 128));
+    }
 
     // accumulators over the four 32-column slices of V (register fragments)
     //   dKg, dQg, dKd [64 x 128]: warp w owns rows 16 (w / 2) .. +16, cols 64 (w % 2) .. +64 (8 blocks)
@@ -468,6 +488,16 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         const int t = i >> 6, s = i & 63;
         dB[t * P64 + s] *= sbeta[t];
     }
+    // the g_raw tile of the gate backward, staged now so its latency hides behind the bilinear forms
+    __nv_bfloat16* sgraw = reinterpret_cast<__nv_bfloat16*>(sm + O_GRAW);
+    for (int i = tid; i < 64 * 16; i += 256) {
+        const int t = i >> 4, c8 = (i & 15) * 8;
+        if (t < len)
+            cp_async16(reinterpret_cast<float*>(sgraw + t * 128 + c8),
+                       reinterpret_cast<const float*>(static_cast<const __nv_bfloat16*>(p.g_raw) +
+                                                      ((size_t)(tok0 + t) * H + h) * K + c8));
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
     // R[s][c] = k_hat[s][c] exp(G_{b(s)+1,c} - Gamma[s][c]) (<= 1), with G_{b+1} = Gamma at the end of
     // sub-block b.  Stored in the phase-1 dS_end area: [64][P128].
     float* R = sdS;
@@ -516,48 +546,56 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
                 }
         }
     }
-    // dk_R: rows s of this warp's sub-block bt; sum over t >= 16 bt
+    // dk_R: rows s of this warp's sub-block bt; sum over t >= 16 bt.  One k-step loads and splits the
+    // dA / dB fragments once and feeds the eight column blocks' independent accumulators.
     {
         const int j = bt;
+        const int g = lane >> 2, qd = lane & 3;
+        float gref[8];
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
-            const int n0 = 64 * (warp & 1) + 8 * b;
-            const int g = lane >> 2, qd = lane & 3;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int k0 = 16 * j; k0 < 64; k0 += 8) {
-                uint32_t aAh[4], aAl[4], aBh[4], aBl[4], bqh[2], bql[2], bkh[2], bkl[2];
-                // A(m = s, k = t) = dA[t][s] (transposed access), rows s = wm0 + ...
-                split_tf32(dA[(k0 + qd) * P64 + wm0 + g], aAh[0], aAl[0]);
-                split_tf32(dA[(k0 + qd) * P64 + wm0 + g + 8], aAh[1], aAl[1]);
-                split_tf32(dA[(k0 + qd + 4) * P64 + wm0 + g], aAh[2], aAl[2]);
-                split_tf32(dA[(k0 + qd + 4) * P64 + wm0 + g + 8], aAh[3], aAl[3]);
-                split_tf32(dB[(k0 + qd) * P64 + wm0 + g], aBh[0], aBl[0]);
-                split_tf32(dB[(k0 + qd) * P64 + wm0 + g + 8], aBh[1], aBl[1]);
-                split_tf32(dB[(k0 + qd + 4) * P64 + wm0 + g], aBh[2], aBl[2]);
-                split_tf32(dB[(k0 + qd + 4) * P64 + wm0 + g + 8], aBh[3], aBl[3]);
-                const int cn = n0 + g;
-                const float gref = Gm[(16 * j + 15) * K + cn];
-                const int t1 = k0 + qd, t2 = k0 + qd + 4;
-                const float l1 = __expf(Gm[t1 * K + cn] - gref), l2 = __expf(Gm[t2 * K + cn] - gref);
+            gref[b] = Gm[(16 * j + 15) * K + 64 * (warp & 1) + 8 * b + g];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) fkr[b][e] = 0.f;
+        }
+#pragma unroll 1
+        for (int k0 = 16 * j; k0 < 64; k0 += 8) {
+            uint32_t aAh[4], aAl[4], aBh[4], aBl[4];
+            // A(m = s, k = t) = dA[t][s] (transposed access), rows s = wm0 + ...
+            split_tf32(dA[(k0 + qd) * P64 + wm0 + g], aAh[0], aAl[0]);
+            split_tf32(dA[(k0 + qd) * P64 + wm0 + g + 8], aAh[1], aAl[1]);
+            split_tf32(dA[(k0 + qd + 4) * P64 + wm0 + g], aAh[2], aAl[2]);
+            split_tf32(dA[(k0 + qd + 4) * P64 + wm0 + g + 8], aAh[3], aAl[3]);
+            split_tf32(dB[(k0 + qd) * P64 + wm0 + g], aBh[0], aBl[0]);
+            split_tf32(dB[(k0 + qd) * P64 + wm0 + g + 8], aBh[1], aBl[1]);
+            split_tf32(dB[(k0 + qd + 4) * P64 + wm0 + g], aBh[2], aBl[2]);
+            split_tf32(dB[(k0 + qd + 4) * P64 + wm0 + g + 8], aBh[3], aBl[3]);
+            const int t1 = k0 + qd, t2 = k0 + qd + 4;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                const int cn = 64 * (warp & 1) + 8 * b + g;
+                uint32_t bqh[2], bql[2], bkh[2], bkl[2];
+                const float l1 = __expf(Gm[t1 * K + cn] - gref[b]), l2 = __expf(Gm[t2 * K + cn] - gref[b]);
                 split_tf32(qh[t1 * K + cn] * l1, bqh[0], bql[0]);
                 split_tf32(qh[t2 * K + cn] * l2, bqh[1], bql[1]);
                 split_tf32(kh[t1 * K + cn] * l1, bkh[0], bkl[0]);
                 split_tf32(kh[t2 * K + cn] * l2, bkh[1], bkl[1]);
-                mma1688(acc, aAl, bqh);
-                mma1688(acc, aAh, bql);
-                mma1688(acc, aAh, bqh);
-                mma1688(acc, aBl, bkh);
-                mma1688(acc, aBh, bkl);
-                mma1688(acc, aBh, bkh);
+                mma1688(fkr[b], aAl, bqh);
+                mma1688(fkr[b], aAh, bql);
+                mma1688(fkr[b], aAh, bqh);
+                mma1688(fkr[b], aBl, bkh);
+                mma1688(fkr[b], aBh, bkl);
+                mma1688(fkr[b], aBh, bkh);
             }
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 int r, cc;
-                frag_rc(lane, e, wm0, n0, r, cc);
-                const float gref = Gm[(16 * j + 15) * K + cc];
-                fkr[b][e] = acc[e] * __expf(gref - Gm[r * K + cc]);
+                frag_rc(lane, e, wm0, 64 * (warp & 1) + 8 * b, r, cc);
+                fkr[b][e] *= __expf(Gm[(16 * j + 15) * K + cc] - Gm[r * K + cc]);
             }
-        }
     }
     __syncthreads();   // dKg / dQg / dKd are read below by their owning threads only, R and dA/dB are done
     // combine: dq = dq_A + dQg e^G ; dk = dk_L + dk_R + dKg e^G + dKd e^{Gc - G} ;
@@ -627,13 +665,14 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         const int cc = tid & 127, hf = tid >> 7;
         const float ea = expf(p.a_log[h]);
         const float dtbv = p.dt_bias[h * K + cc];
-        const __nv_bfloat16* __restrict__ graw = static_cast<const __nv_bfloat16*>(p.g_raw);
         float* __restrict__ dgr = p.dg_raw;
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
         float gv[32];
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
             const int t = hf + 2 * u;
-            gv[u] = t < len ? __bfloat162float(graw[((size_t)(tok0 + t) * H + h) * K + cc]) : 0.f;
+            gv[u] = t < len ? __bfloat162float(sgraw[t * 128 + cc]) : 0.f;
         }
         float dtb = 0.f;
 #pragma unroll
@@ -641,7 +680,7 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
             const int t = hf + 2 * u;
             if (t < len) {
                 const float z = ea * (gv[u] + dtbv);
-                const float sg = sigmoidf_acc(z);
+                const float sg = __fdividef(1.f, 1.f + __expf(-z));   // ~2^-21 relative: ample for dg_raw
                 const float dz = sdG[t * P128 + cc] * p.lb * sg * (1.f - sg);
                 dgr[((size_t)(tok0 + t) * H + h) * K + cc] = dz * ea;
                 dtb += dz * ea;
