@@ -477,11 +477,26 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
             }
     }
     __syncthreads();
-    for (int t = warp; t < 64; t += 8) {   // dbeta_t += sum_{s<t} dL[t][s] Bkk[t][s]
-        const float* brow = rec + L.B + t * 64;
-        float acc = dB[t * P64 + lane] * brow[lane] + dB[t * P64 + lane + 32] * brow[lane + 32];
-        acc = warp_sum(acc);
-        if (lane == 0) sdbeta[t] += acc;
+    {   // dbeta_t += sum_{s<t} dL[t][s] Bkk[t][s]; warp w takes rows w, w + 8, ... (loads first)
+        float bv[8][2], acc[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float* brow = rec + L.B + (warp + 8 * u) * 64;
+            bv[u][0] = brow[lane];
+            bv[u][1] = brow[lane + 32];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int t = warp + 8 * u;
+            acc[u] = dB[t * P64 + lane] * bv[u][0] + dB[t * P64 + lane + 32] * bv[u][1];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
+        if (lane == 0)
+#pragma unroll
+            for (int u = 0; u < 8; ++u) sdbeta[warp + 8 * u] += acc[u];
     }
     __syncthreads();
     for (int i = tid; i < 64 * 64; i += 256) {
@@ -504,10 +519,15 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     const float* Gm = rec + L.G;
     const float* qh = rec + L.qh;
     const float* kh = rec + L.kh;
-    for (int i = tid; i < 64 * K; i += 256) {
-        const int s = i >> 7, cc = i & 127;
-        const float gref = Gm[(16 * (s >> 4) + 15) * K + cc];
-        R[s * P128 + cc] = kh[i] * __expf(gref - Gm[i]);
+#pragma unroll
+    for (int it = 0; it < 64 * K / 4 / 256; ++it) {   // float4 per thread per trip, all loads independent
+        const int i4 = tid + 256 * it, s = i4 >> 5, c4 = (i4 & 31) * 4;
+        const float4 gr = *reinterpret_cast<const float4*>(Gm + (16 * (s >> 4) + 15) * K + c4);
+        const float4 gs = *reinterpret_cast<const float4*>(Gm + s * K + c4);
+        const float4 kv = *reinterpret_cast<const float4*>(kh + s * K + c4);
+        *reinterpret_cast<float4*>(R + s * P128 + c4) =
+            make_float4(kv.x * __expf(gr.x - gs.x), kv.y * __expf(gr.y - gs.y), kv.z * __expf(gr.z - gs.z),
+                        kv.w * __expf(gr.w - gs.w));
     }
     __syncthreads();
 
@@ -606,19 +626,32 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
         const int n0 = 64 * (warp & 1) + 8 * b;
+        int r0, c0;
+        frag_rc(lane, 0, wm0, n0, r0, c0);   // elements (r0, c0 + e), (r0 + 8, c0 + e), e = 0, 1
+        const float2 Gc = *reinterpret_cast<const float2*>(Gm + 63 * K + c0);
+        float2 G[2], Q[2], Kk[2], QG[2], KG[2], KD[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {   // every load of the block first
+            const int gi = (r0 + 8 * hh) * K + c0;
+            G[hh] = *reinterpret_cast<const float2*>(Gm + gi);
+            Q[hh] = *reinterpret_cast<const float2*>(qh + gi);
+            Kk[hh] = *reinterpret_cast<const float2*>(kh + gi);
+            QG[hh] = *reinterpret_cast<const float2*>(rec + L.Qg + gi);
+            KG[hh] = *reinterpret_cast<const float2*>(rec + L.Kg + gi);
+            KD[hh] = *reinterpret_cast<const float2*>(rec + L.Kd + gi);
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            int r, cc;
-            frag_rc(lane, e, wm0, n0, r, cc);
-            const int gi = r * K + cc;
-            const float G = Gm[gi], Gc = Gm[63 * K + cc];
-            const float eG = __expf(G), eD = __expf(Gc - G);
+            const int hh = e >> 1, lo = e & 1;
+            const int r = r0 + 8 * hh, cc = c0 + lo;
+            const float g = lo ? G[hh].y : G[hh].x, gc = lo ? Gc.y : Gc.x;
+            const float q = lo ? Q[hh].y : Q[hh].x, k = lo ? Kk[hh].y : Kk[hh].x;
+            const float qg = lo ? QG[hh].y : QG[hh].x, kg = lo ? KG[hh].y : KG[hh].x, kd = lo ? KD[hh].y : KD[hh].x;
+            const float eG = __expf(g), eD = __expf(gc - g);
             const float vQg = dQg[r * P128 + cc], vKg = dKg[r * P128 + cc], vKd = dKdm[r * P128 + cc];
-            const float q = qh[gi], k = kh[gi];
             const float dq = fq[b][e] + vQg * eG;
             const float dk = fkl[b][e] + fkr[b][e] + vKg * eG + vKd * eD;
-            const float dG = q * fq[b][e] + k * fkl[b][e] - k * fkr[b][e] + vQg * rec[L.Qg + gi] +
-                             vKg * rec[L.Kg + gi] - vKd * rec[L.Kd + gi];
+            const float dG = q * fq[b][e] + k * fkl[b][e] - k * fkr[b][e] + vQg * qg + vKg * kg - vKd * kd;
             sdq[r * P128 + cc] = dq;
             sdk[r * P128 + cc] = dk;
             sdG[r * P128 + cc] = dG;
@@ -635,28 +668,51 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     }
     __syncthreads();
     // ---- prologue backward: L2 norms, sigmoid(beta), lower-bounded gate
-    for (int t = warp; t < len; t += 8) {
-        const size_t row = (size_t)(tok0 + t) * H + h;
-        float qv[4], kv[4], sq = 0.f, sk = 0.f;
+    for (int t0 = warp; t0 < len; t0 += 16) {   // rows t0 and t0 + 8 of this warp, interleaved
+        float qv[2][4], kv[2][4], sq[2] = {0.f, 0.f}, sk[2] = {0.f, 0.f};
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int cc = lane + 32 * u;
-            qv[u] = qh[t * K + cc];
-            kv[u] = kh[t * K + cc];
-            sq += qv[u] * sdq[t * P128 + cc];
-            sk += kv[u] * sdk[t * P128 + cc];
-        }
-        sq = warp_sum(sq); sk = warp_sum(sk);
-        const float rq = rec[L.rn + t], rk = rec[L.rn + 64 + t];
+        for (int w2 = 0; w2 < 2; ++w2) {
+            const int t = min(t0 + 8 * w2, 63);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int cc = lane + 32 * u;
-            p.dq[row * K + cc] = rq * (sdq[t * P128 + cc] - qv[u] * sq);
-            p.dk[row * K + cc] = rk * (sdk[t * P128 + cc] - kv[u] * sk);
+            for (int u = 0; u < 4; ++u) {
+                const int cc = lane + 32 * u;
+                qv[w2][u] = qh[t * K + cc];
+                kv[w2][u] = kh[t * K + cc];
+            }
         }
-        if (lane == 0) {
-            const float b = sbeta[t];
-            p.dbeta_raw[row] = sdbeta[t] * b * (1.f - b);
+#pragma unroll
+        for (int w2 = 0; w2 < 2; ++w2) {
+            const int t = min(t0 + 8 * w2, 63);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int cc = lane + 32 * u;
+                sq[w2] += qv[w2][u] * sdq[t * P128 + cc];
+                sk[w2] += kv[w2][u] * sdk[t * P128 + cc];
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int w2 = 0; w2 < 2; ++w2) {
+                sq[w2] += __shfl_xor_sync(0xffffffffu, sq[w2], o);
+                sk[w2] += __shfl_xor_sync(0xffffffffu, sk[w2], o);
+            }
+#pragma unroll
+        for (int w2 = 0; w2 < 2; ++w2) {
+            const int t = t0 + 8 * w2;
+            if (t >= len) continue;
+            const size_t row = (size_t)(tok0 + t) * H + h;
+            const float rq = rec[L.rn + t], rk = rec[L.rn + 64 + t];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int cc = lane + 32 * u;
+                p.dq[row * K + cc] = rq * (sdq[t * P128 + cc] - qv[w2][u] * sq[w2]);
+                p.dk[row * K + cc] = rk * (sdk[t * P128 + cc] - kv[w2][u] * sk[w2]);
+            }
+            if (lane == 0) {
+                const float b = sbeta[t];
+                p.dbeta_raw[row] = sdbeta[t] * b * (1.f - b);
+            }
         }
     }
     // gate backward: thread (channel cc, parity hf) takes tokens hf, hf + 2, ...
