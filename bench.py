@@ -78,9 +78,9 @@ def kernel_work(name: str, w, units: float) -> tuple[float, float]:
 # any size, so the figure scales with the token-heads of a launch.  An entry is removed when its
 # kernel changes and has not been captured again.
 PROFILED_TRAFFIC = {
-    ("kda_grad_tc", True): 9756.0,
-    ("kda_intra_tc", False): 2401.0,             # forward mode (forward-only workloads)
-    ("kda_intra_tc", True): (2401.0 + 7289.0) / 2,   # forward + backward mode, one launch each per step
+    ("kda_grad_tc", True): 9784.0,
+    ("kda_intra_tc", False): 2408.0,             # forward mode (forward-only workloads)
+    ("kda_intra_tc", True): (2408.0 + 5459.0) / 2,   # forward + backward mode, one launch each per step
 }
 
 
