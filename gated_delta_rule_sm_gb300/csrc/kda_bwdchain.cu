@@ -19,7 +19,7 @@
 // are independent.  Thread r owns row r of Z.  Per chunk: MMA1 (M = 64, N = JW, K = 128) into TMEM,
 // X = D1 + Y split into bf16 hi + lo (MN-major, one 16-byte store per 8 columns), MMA2 (M = 128,
 // N = JW, K = 64), then Z' = gC Z + D3 (+ P).  Record slots (A1, A2 hi/lo, gC) are double buffered
-// by bulk copies.
+// by bulk copies.  X (U, or dU) is also written out per chunk for the gradient kernel.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
@@ -194,6 +194,11 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) d[j] += y[j];
+                if (lane < 16) {   // X row t (U or dU) for the gradient kernel
+                    float* xo = (REV ? p.chunk_du : p.chunk_u) + (((size_t)c * H + h) * 64 + t) * V + j0 + jb;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(xo + j) = make_float4(d[j], d[j + 1], d[j + 2], d[j + 3]);
+                }
                 if (lane < 16)
 #pragma unroll
                     for (int g8 = 0; g8 < 4; ++g8) {

@@ -38,6 +38,8 @@ struct Params {
     size_t scratch_stride;      // floats per CTA
     int grad_ctas;              // CTAs of the SIMT gradient kernel
     void* tc;                   // tensor-core path buffers (its own layout)
+    float* chunk_u;             // tensor-core backward: U per (chunk, head) [64][V] fp32, from the recompute chain
+    float* chunk_du;            // tensor-core backward: dU per (chunk, head) [64][V] fp32, from the reverse chain
     int* status;                // device status word
 };
 

@@ -215,6 +215,8 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     const float* rec = p.rec + ((size_t)c * H + h) * p.rec_stride;
     const float* S0g = p.states + ((size_t)c * H + h) * K * V;
     const float* dSg = p.dstates + ((size_t)c * H + h) * K * V;
+    const float* Ug = p.chunk_u + ((size_t)c * H + h) * 64 * V;     // U = U0 - W S0 (recompute chain)
+    const float* dUg = p.chunk_du + ((size_t)c * H + h) * 64 * V;   // dU = scale Aqk^T dO + Kd dS_end (reverse chain)
     float* sW = sm + O_W;
     float* sKg = sm + O_KG;
     float* sKd = sm + O_KD;
@@ -232,15 +234,13 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     const float scale = p.scale;
 
     // chunk-wide operands (16-byte asynchronous copies; completed by the first slice's wait)
+    // (U and dU come per slice from the two state chains, so W, Kd and A_qk are not needed here)
     for (int i = tid; i < 64 * K / 4; i += 256) {
         const int t = i >> 5, c4 = (i & 31) * 4;
-        cp_async16(sW + t * P128 + c4, rec + L.W + t * K + c4);
         cp_async16(sKg + t * P128 + c4, rec + L.Kg + t * K + c4);
-        cp_async16(sKd + t * P128 + c4, rec + L.Kd + t * K + c4);
     }
     for (int i = tid; i < 64 * 64 / 4; i += 256) {
         const int t = i >> 4, s4 = (i & 15) * 4;
-        cp_async16(sAq + t * P64 + s4, rec + L.A + t * 64 + s4);
         cp_async16(sN + t * P64 + s4, rec + L.N + t * 64 + s4);
     }
     if (tid < 16) cp_async16(sbeta + 4 * tid, rec + L.beta + 4 * tid);
@@ -249,8 +249,9 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         const uint32_t kv = K * V * 4u;
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(S0g)), "r"(kv) : "memory");
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(dSg)), "r"(kv) : "memory");
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(rec + L.U0)),
-                     "r"(64u * V * 4u)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(Ug)), "r"(64u * V * 4u)
+                     : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(dUg)), "r"(64u * V * 4u)
                      : "memory");
     }
     if (tid >= 64 && tid < 64 + len) {   // one 256-byte row of dout and of v per token
@@ -288,7 +289,8 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         }
         for (int i = tid; i < 64 * 8; i += 256) {
             const int t = i >> 3, j4 = (i & 7) * 4;
-            cp_async16(sU + t * P32 + j4, rec + L.U0 + t * V + j0 + j4);
+            cp_async16(sU + t * P32 + j4, Ug + t * V + j0 + j4);
+            cp_async16(sdU + t * P32 + j4, dUg + t * V + j0 + j4);
         }
         {   // dO and v slices (bf16, 8 per 16-byte load): one row-quarter per thread
             const int t = tid >> 2, j8 = (tid & 3) * 8;
@@ -309,45 +311,22 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         }
         cp_async_wait_all();
         __syncthreads();
-        // U = U0 - W S0 and Vt = v - Kg S0 (64 x 32 each): warp w takes rows 16 (w % 4) of U (w < 4) or Vt
+        // Vt = v - Kg S0 (64 x 32): warp w takes rows 16 (w % 4), columns 16 (w / 4) .. + 16
         {
-            const int which = warp >> 2, m0 = 16 * (warp & 3);
-            float d[4][4];
-#pragma unroll
-            for (int b = 0; b < 4; ++b)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) d[b][e] = 0.f;
-            mma_strip<4>(d, Tile{which ? sKg : sW, P128, 1}, Tile{sS0, P32, 1}, m0, 0, 0, K, lane);
-            __syncwarp();
-            float* dst = which ? sVt : sU;
-#pragma unroll
-            for (int b = 0; b < 4; ++b)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    int r, cc;
-                    frag_rc(lane, e, m0, 8 * b, r, cc);
-                    dst[r * P32 + cc] -= d[b][e];
-                }
-        }
-        __syncthreads();
-        // dU = Kd dS_end + scale Aqk^T dO (64 x 32): warp w takes rows 16 (w / 2), columns 16 (w % 2) .. + 16.
-        // Aqk is lower triangular: rows s see t >= s only.
-        {
-            const int m0 = 16 * (warp >> 1), n0 = 16 * (warp & 1);
-            float d1[2][4], d2[2][4];
+            const int m0 = 16 * (warp & 3), n0 = 16 * (warp >> 2);
+            float d[2][4];
 #pragma unroll
             for (int b = 0; b < 2; ++b)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) d1[b][e] = d2[b][e] = 0.f;
-            mma_strip<2>(d1, Tile{sKd, P128, 1}, Tile{sdS, P32, 1}, m0, n0, 0, K, lane);
-            mma_strip<2>(d2, Tile{sAq, 1, P64}, Tile{sdO, P32, 1}, m0, n0, m0, 64, lane);
+                for (int e = 0; e < 4; ++e) d[b][e] = 0.f;
+            mma_strip<2>(d, Tile{sKg, P128, 1}, Tile{sS0, P32, 1}, m0, n0, 0, K, lane);
 #pragma unroll
             for (int b = 0; b < 2; ++b)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     int r, cc;
                     frag_rc(lane, e, m0, n0 + 8 * b, r, cc);
-                    sdU[r * P32 + cc] = d1[b][e] + scale * d2[b][e];
+                    sVt[r * P32 + cc] -= d[b][e];
                 }
         }
         __syncthreads();
