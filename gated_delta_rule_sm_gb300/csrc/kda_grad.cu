@@ -22,8 +22,7 @@
 
 namespace kda {
 
-using sm100::km_bf16;
-using sm100::pack8_bf16;
+using namespace sm100;
 
 namespace {
 
@@ -197,7 +196,20 @@ constexpr int O_BETA = O_DY + 64 * P32;     // [64]
 constexpr int O_GRAW = O_DO + 64 * P64;    // bf16 [64][128] g_raw tile, phase 2 (after dB: tmp is dead)
 static_assert(O_GRAW >= O_DS + 64 * P128 && O_GRAW + 64 * 128 / 2 <= O_BETA, "g_raw tile inside the free tail");
 constexpr int O_RED = O_BETA + 64;          // [64] dbeta, [128] Gamma_last gradient, [8] block sums, [256] dt_bias parts
-constexpr int SMEM_FLOATS = O_RED + 64 + 128 + 8 + 256;
+constexpr int O_MBAR = O_RED + 64 + 128 + 8 + 256;   // 8-byte mbarrier + TMEM slot (4 floats)
+constexpr int SMEM_FLOATS = O_MBAR + 4;
+// Phase-1 tensor-core operands (bf16, K-major over the 32 value columns of a slice: km_bf16(row, j,
+// 512, 128)), in the areas that phase 2 later fills with the accumulators: W area and Kd..N area.
+constexpr uint32_t B_S0 = O_W * 4;                  // S0^T slice hi / lo   [128 c][32 j]  2 x 8 KB
+constexpr uint32_t B_DS = B_S0 + 16384;             // dS_end^T slice hi / lo            2 x 8 KB
+constexpr uint32_t B_U = O_KD * 4;                  // U slice hi / lo      [64 t][32 j]  2 x 4 KB
+constexpr uint32_t B_DU = B_U + 8192;               // dU slice hi / lo
+constexpr uint32_t B_VT = B_DU + 8192;              // (v - Kg S0) slice hi / lo
+constexpr uint32_t B_MDY = B_VT + 8192;             // -dY slice hi / lo
+constexpr uint32_t B_DO = B_MDY + 8192;             // dO slice (bf16, exact)
+static_assert(B_DS + 16384 <= (uint32_t)O_KG * 4 && B_DO + 4096 <= (uint32_t)O_N * 4, "phase-1 operand areas");
+// TMEM columns of the five M = 64 accumulators (rows t in lanes (t / 16) * 32 + t % 16)
+constexpr uint32_t T_KG = 0, T_QG = 128, T_KD = 256, T_T = 384, T_A = 448;
 
 }  // namespace
 
@@ -267,15 +279,24 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     // accumulators over the four 32-column slices of V (register fragments)
     //   dKg, dQg, dKd [64 x 128]: warp w owns rows 16 (w / 2) .. +16, cols 64 (w % 2) .. +64 (8 blocks)
     //   dT, dA [64 x 64]: warp w owns rows 16 (w / 2), cols 32 (w % 2) .. +32 (4 blocks)
-    float aKg[8][4], aQg[8][4], aKd[8][4], aT[4][4], aA[4][4];
-#pragma unroll
-    for (int b = 0; b < 8; ++b)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) aKg[b][e] = aQg[b][e] = aKd[b][e] = 0.f;
-#pragma unroll
-    for (int b = 0; b < 4; ++b)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) aT[b][e] = aA[b][e] = 0.f;
+    // The slice contributions to dKg (-dY S0^T), dQg (dO S0^T), dKd (U dS^T), dT (dU Vt^T) and dA (dO U^T)
+    // accumulate over the four slices in tensor memory: tcgen05 MMAs on bf16 hi / lo operands
+    // (hi*hi + hi*lo + lo*hi; dO is bf16 and exact), ~1e-5 relative.  dKd enters dGamma twice (-dKd Kd
+    // per token, +sum_t dKd Kd at Gamma_last) and the two cancel in the reverse cumulative sum, so it
+    // needs that precision; the others get it for free.
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + O_MBAR);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + O_MBAR + 2);
+    uint8_t* smb = reinterpret_cast<uint8_t*>(sm);
+    if (tid == 0) {
+        mbar_init(mbar, 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(tslot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    bool mma_ok = true;
     float dgc = 0.f;   // thread tid < 128: sum_j dS_end[c][j] S0[c][j] for channel c = tid
     const int wm0 = 16 * (warp >> 1);
 
@@ -351,14 +372,70 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
                 }
         }
         __syncthreads();
-        // slice contributions to dKg (-dY S0^T), dQg (dO S0^T), dKd (U dS^T), dT (dU Vt^T), dA (dO U^T)
-        mma_strip<8>(aKg, Tile{sdY, P32, 1}, Tile{sS0, 1, P32}, wm0, 64 * (warp & 1), 0, 32, lane);
-        mma_strip<8>(aQg, Tile{sdO, P32, 1}, Tile{sS0, 1, P32}, wm0, 64 * (warp & 1), 0, 32, lane);
-        // dKd enters dGamma twice (-dKd Kd per token, +sum_t dKd Kd at Gamma_last) and the two cancel in
-        // the reverse cumulative sum: split precision
-        mma_strip3<8>(aKd, Tile{sU, P32, 1}, Tile{sdS, 1, P32}, wm0, 64 * (warp & 1), 0, 32, lane);
-        mma_strip<4>(aT, Tile{sdU, P32, 1}, Tile{sVt, 1, P32}, wm0, 32 * (warp & 1), 0, 32, lane);
-        mma_strip<4>(aA, Tile{sdO, P32, 1}, Tile{sU, 1, P32}, wm0, 32 * (warp & 1), 0, 32, lane);
+        // slice contributions on the tensor cores: the previous slice's MMAs must be done with the
+        // operand tiles before they are rewritten
+        if (z > 0 && !mbar_wait(mbar, (z - 1) & 1)) mma_ok = false;
+        tc_fence_after();
+        {
+            // groups of 8 consecutive j of one row; 8 consecutive groups share j and take rows r..r+7
+            auto put = [&](uint32_t off, const float* src, int row, int j8, float sg) {
+                float x[8];
+                *reinterpret_cast<float4*>(x) = *reinterpret_cast<const float4*>(src + row * P32 + j8);
+                *reinterpret_cast<float4*>(x + 4) = *reinterpret_cast<const float4*>(src + row * P32 + j8 + 4);
+                float hv[8], lv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float v = sg * x[e];
+                    hv[e] = __bfloat162float(__float2bfloat16_rn(v));
+                    lv[e] = v - hv[e];
+                }
+                const uint32_t o = off + km_bf16(row, j8, 512, 128);
+                *reinterpret_cast<uint4*>(smb + o) = pack8_bf16(hv);
+                if (off != B_DO) *reinterpret_cast<uint4*>(smb + o + (off >= B_U ? 4096u : 8192u)) = pack8_bf16(lv);
+            };
+            for (int g = tid; g < 128 * 4; g += 256) {
+                const int row = (g & 7) | ((g >> 5) << 3), j8 = ((g >> 3) & 3) * 8;
+                put(B_S0, sS0, row, j8, 1.f);
+                put(B_DS, sdS, row, j8, 1.f);
+            }
+            {
+                const int g = tid, row = (g & 7) | ((g >> 5) << 3), j8 = ((g >> 3) & 3) * 8;   // 64 rows x 4
+                put(B_U, sU, row, j8, 1.f);
+                put(B_DU, sdU, row, j8, 1.f);
+                put(B_VT, sVt, row, j8, 1.f);
+                put(B_MDY, sdY, row, j8, -1.f);
+                put(B_DO, sdO, row, j8, 1.f);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            const uint32_t base = smem_u32(sm);
+            constexpr uint32_t i128 = idesc_bf16(64, 128, 0, 0), i64 = idesc_bf16(64, 64, 0, 0);
+            // D (+)= A B^T over K = 32 (two K = 16 steps); A / B K-major with 8-row groups 512 B apart
+            auto mm = [&](uint32_t d, uint32_t a, uint32_t b, uint32_t id, bool first) {
+                for (int kk = 0; kk < 2; ++kk)
+                    mma_bf16(d, smem_desc(base + a + kk * 256, 128, 512), smem_desc(base + b + kk * 256, 128, 512), id,
+                             (first && kk == 0) ? 0u : 1u);
+            };
+            const bool f = z == 0;
+            mm(tmem + T_KG, B_MDY + 4096, B_S0, i128, f);          // -dY S0^T: lo * hi, hi * lo, hi * hi
+            mm(tmem + T_KG, B_MDY, B_S0 + 8192, i128, false);
+            mm(tmem + T_KG, B_MDY, B_S0, i128, false);
+            mm(tmem + T_QG, B_DO, B_S0 + 8192, i128, f);           // dO S0^T (dO exact)
+            mm(tmem + T_QG, B_DO, B_S0, i128, false);
+            mm(tmem + T_KD, B_U + 4096, B_DS, i128, f);            // U dS^T
+            mm(tmem + T_KD, B_U, B_DS + 8192, i128, false);
+            mm(tmem + T_KD, B_U, B_DS, i128, false);
+            mm(tmem + T_T, B_DU + 4096, B_VT, i64, f);             // dU Vt^T
+            mm(tmem + T_T, B_DU, B_VT + 4096, i64, false);
+            mm(tmem + T_T, B_DU, B_VT, i64, false);
+            mm(tmem + T_A, B_DO, B_U + 4096, i64, f);              // dO U^T
+            mm(tmem + T_A, B_DO, B_U, i64, false);
+            mma_commit(mbar);
+        }
         if (tid < K) {
             float acc = 0.f;
 #pragma unroll 8
@@ -369,35 +446,51 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     __syncthreads();
 
     // ---- phase 2: write the accumulators out (dKg -> sW, dQg -> sKg, dKd -> sKd, dT -> sS0, dA -> sAq)
+    if (!mbar_wait(mbar, 3 & 1)) mma_ok = false;
+    tc_fence_after();
+    if (!__syncthreads_and(mma_ok ? 1 : 0)) {
+        // a tensor-core wait ran out: record it and leave (results of this chunk are void)
+        if (tid == 0) record_error(p.status, KDA_ERR_TIMEOUT);
+        if (tid == 0) mbar_wait(mbar, 1, 1u << 16);
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, 512);
+        return;
+    }
     float* dKg = sW;
     float* dQg = sKg;
     float* dKdm = sKd;
     float* dT = sS0;     // [64][P64]
     float* dA = sAq;     // [64][P64]
+    {
+        // M = 64 accumulators: warp w reads lane quarter w % 4 (rows 16 (w % 4) + lane, lane < 16);
+        // warps w and w + 4 split the columns
+        const int r = 16 * (warp & 3) + (lane & 15), half = warp >> 2;
+        const uint32_t lb = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        auto drain = [&](uint32_t col0, int ncols, float* dst, int stride, float mul, bool lower) {
+            for (int cb = 0; cb < ncols; cb += 32) {
+                float d[32];
+                const uint32_t c0 = col0 + half * ncols + cb;
+                tmem_ld16(tmem + lb + c0, d);
+                tmem_ld16(tmem + lb + c0 + 16, d + 16);
+                tmem_ld_wait();
+                if (lane < 16)
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
-        const int n0 = 64 * (warp & 1) + 8 * b;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            int r, cc;
-            frag_rc(lane, e, wm0, n0, r, cc);
-            dKg[r * P128 + cc] = -aKg[b][e];
-            dQg[r * P128 + cc] = scale * aQg[b][e];
-            dKdm[r * P128 + cc] = aKd[b][e];
-        }
+                    for (int j = 0; j < 32; ++j) {
+                        const int cc = half * ncols + cb + j;
+                        dst[r * stride + cc] = (lower && cc > r) ? 0.f : mul * d[j];
+                    }
+            }
+        };
+        drain(T_KG, 64, dKg, P128, 1.f, false);
+        drain(T_QG, 64, dQg, P128, scale, false);
+        drain(T_KD, 64, dKdm, P128, 1.f, false);
+        drain(T_T, 32, dT, P64, 1.f, false);
+        drain(T_A, 32, dA, P64, scale, true);
     }
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        const int n0 = 32 * (warp & 1) + 8 * b;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            int r, cc;
-            frag_rc(lane, e, wm0, n0, r, cc);
-            dT[r * P64 + cc] = aT[b][e];
-            dA[r * P64 + cc] = cc <= r ? scale * aA[b][e] : 0.f;
-        }
-    }
+    tc_fence_before();
     __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
     // Gamma_last gathers exp(Gamma_last) rowsum(dS_end * S0) and sum_t dKd Kd
     float* sgl = sred + 64;
     if (tid < K) {
