@@ -50,7 +50,9 @@ constexpr uint32_t RAW_Q = 0, RAW_K = 16384, RAW_G = 32768, RAW_V = 49152;  // T
 // in its own space, pair B reuses the raw tiles once the element phase has read them.
 constexpr uint32_t LA_HI = 65536, LA_LO = 98304;
 constexpr uint32_t LB_HI = 0, LB_LO = 32768;
-constexpr uint32_t TB_HI = 0, TB_LO = 8192;  // after the A MMAs: T split in bf16, B operand (N = t, K = s), km_bf16(t, s, 1024, 128)
+constexpr uint32_t TB_HI = 131072, TB_LO = 139264;  // after the A MMAs (in the dead RB area): T split in bf16, B operand
+                                                     // (N = t, K = s), km_bf16(t, s, 1024, 128); the raw area is then free
+                                                     // for the next item's tiles
 constexpr uint32_t SL = LA_HI;               // after the A MMAs: fp32 [64][65] Diag(beta) Bkk
 constexpr uint32_t SN = LA_HI + 16640;       // fp32 [64][65] N = (I + L)^-1
 constexpr uint32_t SP = LA_HI + 34816;       // fp32 [3][16][17] scratch of the blocked solve
@@ -71,48 +73,64 @@ __global__ void __launch_bounds__(256, 1)
                     const __grid_constant__ CUtensorMap tm_v) {
     using namespace intralay;
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int c = blockIdx.x, h = blockIdx.y;
-    if (c >= p.chunk_off[p.N]) return;
-    const int n = chunk_segment(p, c);
-    const int tok0 = seg_begin(p, n) + (c - p.chunk_off[n]) * kChunk;
-    const int len = min(kChunk, seg_end(p, n) - tok0);
     const int H = p.H;
+    const int nitems = p.chunk_off[p.N] * H;   // (chunk, head) items, head fastest
+    if ((int)blockIdx.x >= nitems) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    auto item_tok0 = [&](int it, int& h, int& c, int& tok0) {
+        c = it / H;
+        h = it - c * H;
+        const int n = chunk_segment(p, c);
+        tok0 = seg_begin(p, n) + (c - p.chunk_off[n]) * kChunk;
+        return min(kChunk, seg_end(p, n) - tok0);
+    };
     float* rq = reinterpret_cast<float*>(smem + SMALL);
     float* rk = rq + 64;
     float* sbeta = rk + 64;
     float* sdtb = sbeta + 64;
     float* sblk = sdtb + 128;
     float* sgsum = sblk + 512;        // per sub-block sums of g (backward record only)
-    float* frec = BWD ? p.rec + ((size_t)c * H + h) * p.rec_stride : nullptr;
     const RecLayout RL = RecLayout::make(128, 128);
     // Each MMA barrier has at most one pending phase at any time, so parity waits are unambiguous.
     uint64_t* bar_load = reinterpret_cast<uint64_t*>(smem + BAR);
     uint64_t* bar_a = bar_load + 1;   // MMAs reading tile pair A (and the final W / U0 MMAs)
     uint64_t* bar_b = bar_load + 2;   // MMAs reading tile pair B
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_load + 3);
-    uint8_t* rec = BWD ? nullptr : recs + ((size_t)c * H + h) * tcrec::BYTES;
+    // the raw q, k, g, v tiles of one item (64 tokens x 128 channels each, out-of-range rows zero)
+    auto load_raw = [&](int it) {
+        int h2, c2, t02;
+        item_tok0(it, h2, c2, t02);
+        mbar_expect_tx(bar_load, 4 * 16384);
+        tma_load_3d(smem + RAW_Q, &tm_q, 0, h2, t02, bar_load);
+        tma_load_3d(smem + RAW_K, &tm_k, 0, h2, t02, bar_load);
+        tma_load_3d(smem + RAW_G, &tm_g, 0, h2, t02, bar_load);
+        tma_load_3d(smem + RAW_V, &tm_v, 0, h2, t02, bar_load);
+    };
 
     if (tid == 0) {
         mbar_init(bar_load, 1);
         mbar_init(bar_a, 1);
         mbar_init(bar_b, 1);
         mbar_fence_init();
-        mbar_expect_tx(bar_load, 4 * 16384);
-        tma_load_3d(smem + RAW_Q, &tm_q, 0, h, tok0, bar_load);
-        tma_load_3d(smem + RAW_K, &tm_k, 0, h, tok0, bar_load);
-        tma_load_3d(smem + RAW_G, &tm_g, 0, h, tok0, bar_load);
-        tma_load_3d(smem + RAW_V, &tm_v, 0, h, tok0, bar_load);
+        load_raw(blockIdx.x);
     }
     if (warp == 0) tmem_alloc(tslot, 256);
-    if (tid < 128) sdtb[tid] = p.dt_bias[h * 128 + tid];
-    if (tid < 64) sbeta[tid] = tid < len ? sigmoidf_acc(load_act(p.beta_raw, (size_t)(tok0 + tid) * H + h, KDA_BF16)) : 0.f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    uint32_t par_a = 0, par_b = 0;
-    bool ok = __syncthreads_and(mbar_wait(bar_load, 0) ? 1 : 0) != 0;
+    uint32_t par_a = 0, par_b = 0, par_load = 0;
+    bool ok = true;
+    // Persistent over items: each item's raw tiles were requested by the previous item (or above).
+    for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+    int h, c, tok0;
+    const int len = item_tok0(item, h, c, tok0);
+    float* frec = BWD ? p.rec + ((size_t)c * H + h) * p.rec_stride : nullptr;
+    uint8_t* rec = BWD ? nullptr : recs + ((size_t)c * H + h) * tcrec::BYTES;
+    if (tid < 128) sdtb[tid] = p.dt_bias[h * 128 + tid];
+    if (tid < 64) sbeta[tid] = tid < len ? sigmoidf_acc(load_act(p.beta_raw, (size_t)(tok0 + tid) * H + h, KDA_BF16)) : 0.f;
+    ok = __syncthreads_and(mbar_wait(bar_load, par_load) ? 1 : 0) != 0;
+    par_load ^= 1;
     if (!ok) goto fail;
 
     // ---- per-token inverse norms (warp w: tokens 8w .. 8w+7; the 16 reductions interleave)
@@ -348,6 +366,11 @@ __global__ void __launch_bounds__(256, 1)
         if (!wait_on(bar_a, par_a)) goto fail;
         if (!wait_on(bar_b, par_b)) goto fail;
         tc_fence_after();
+        // the raw / pair-B area is free for the rest of this item: fetch the next item's tiles now
+        if (tid == 0 && item + (int)gridDim.x < nitems) {
+            fence_async_smem();
+            load_raw(item + gridDim.x);
+        }
     }
 
     {
@@ -514,6 +537,10 @@ __global__ void __launch_bounds__(256, 1)
         }
     }
     tc_fence_before();
+    __syncthreads();   // this item's shared-memory readers are done before the next item writes
+    tc_fence_after();
+    }
+    tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
     return;
@@ -521,7 +548,7 @@ fail:
     // A wait gave up: record it, give outstanding copies / MMAs a bounded chance to land, release TMEM.
     if (tid == 0) {
         record_error(p.status, KDA_ERR_TIMEOUT);
-        mbar_wait(bar_load, 0, 1u << 16);
+        mbar_wait(bar_load, par_load, 1u << 16);
         mbar_wait(bar_a, par_a, 1u << 16);
         mbar_wait(bar_b, par_b, 1u << 16);
     }
@@ -792,7 +819,13 @@ cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, bool bwd, cudaStream
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)intralay::BYTES);
     if (e != cudaSuccess) return e;
     timing_pre(st, K_INTRA_TC);
-    kern<<<dim3(p.NCmax, p.H), 256, intralay::BYTES, st>>>(p, recs, mq, mk, mg, mv);
+    // persistent: one CTA per SM (shared memory allows one), each looping over (chunk, head) items
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long items = (long)p.NCmax * p.H;
+    const int grid = (int)(items < sms ? items : sms);
+    kern<<<grid, 256, intralay::BYTES, st>>>(p, recs, mq, mk, mg, mv);
     timing_post(st);
     return cudaGetLastError();
 }
