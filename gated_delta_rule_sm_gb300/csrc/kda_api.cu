@@ -89,7 +89,6 @@ static TcPlan plan_tc_fwd(const Shape& s) {
 struct TcBwdPlan {
     WsPlan simt;        // chunk table, fp32 backward records, states, partials, scratch
     size_t off_bwrec;   // reverse-chain records
-    size_t off_fwrec;   // forward-recompute chain records
     size_t off_u, off_du;   // U and dU per (chunk, head), written by the two chains
     size_t total;
 };
@@ -99,7 +98,6 @@ static TcBwdPlan plan_tc_bwd(const Shape& s) {
     w.simt = plan_simt(s, true);
     size_t o = w.simt.total;
     w.off_bwrec = o; o = align_up(o + (size_t)s.NCmax * s.H * bwrec::BYTES);
-    w.off_fwrec = o; o = align_up(o + (size_t)s.NCmax * s.H * fwrec::BYTES);
     w.off_u = o; o = align_up(o + sizeof(float) * (size_t)s.NCmax * s.H * 64 * s.V);
     w.off_du = o; o = align_up(o + sizeof(float) * (size_t)s.NCmax * s.H * 64 * s.V);
     w.total = o;
@@ -332,13 +330,12 @@ kda_status kda_bwd(const kda_dims* dims, const void* q, const void* k, const voi
         KDA_TRY_CUDA(launch_plan(p, stream));
         KDA_TRY_CUDA(launch_intra_tc(p, nullptr, true, stream));
         uint8_t* bw = static_cast<uint8_t*>(workspace) + w.off_bwrec;
-        uint8_t* fw = static_cast<uint8_t*>(workspace) + w.off_fwrec;
         p.chunk_u = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.off_u);
         p.chunk_du = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.off_du);
         pf.chunk_u = p.chunk_u;
         pf.chunk_du = p.chunk_du;
-        KDA_TRY_CUDA(launch_bwd_pre(p, bw, fw, stream));
-        KDA_TRY_CUDA(launch_chain_rec_tc(pf, fw, stream));
+        KDA_TRY_CUDA(launch_bwd_pre(p, bw, stream));
+        KDA_TRY_CUDA(launch_chain_rec_tc(pf, bw, stream));
         KDA_TRY_CUDA(launch_chain_bwd_tc(p, bw, stream));
         KDA_TRY_CUDA(launch_grad_tc(p, stream));
         return KDA_OK;

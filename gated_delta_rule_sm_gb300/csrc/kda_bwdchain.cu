@@ -8,7 +8,7 @@
 //   * reverse chain (REV = true): Z = dS, the gradient w.r.t. the state leaving chunk c, A1 = Kd,
 //     Y = scale Aqk^T dO, A2 = -W^T, P = scale Qg^T dO, so X = dU and Z' is the gradient entering
 //     the chunk.
-// The operands (records chainrec / bwrec / fwrec) and Y, P come from bwd_pre.  Every product runs
+// The operand slot (chainrec, shared by both directions) and Y, P come from bwd_pre.  Every product runs
 // in split precision with bf16 halves, operand = hi + lo, hi*hi + hi*lo + lo*hi (kind::f16, relative
 // error ~1e-5): the gradient of the log-decay at the end of a chunk carries dS_end * S_end-sized
 // terms far larger than its typical value, and plain tf32 chains (~2e-4 relative error in S and
@@ -135,16 +135,21 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
             mbar_expect_tx(&full[s], L::SLOT);
             bulk_g2s(slot_ptr(s), rec_ptr(s), L::SLOT, &full[s]);
         }
-    // D += hi*hi + hi*lo + lo*hi, the small products first
-    auto mma3 = [](uint32_t d, uint32_t ah, uint32_t al, uint32_t bh, uint32_t bl, int nk, uint32_t a_sbo,
-                   uint32_t b_lbo, uint32_t idesc) {
+    // D += hi*hi + hi*lo + lo*hi, the small products first.  A: start advance per K = 16 step, LBO, SBO
+    // (K-major: 256, 128, 2048; the same tile as MN-major transpose: 4096, 2048, 128); B: MN-major.
+    auto mma3 = [](uint32_t d, uint32_t ah, uint32_t al, uint32_t bh, uint32_t bl, int nk, uint32_t a_step,
+                   uint32_t a_lbo, uint32_t a_sbo, uint32_t b_lbo, uint32_t idesc) {
         for (int kk = 0; kk < nk; ++kk)
-            mma_bf16(d, smem_desc(al + kk * 256, 128, a_sbo), smem_desc(bh + kk * 2 * b_lbo, b_lbo, 128), idesc, kk > 0);
+            mma_bf16(d, smem_desc(al + kk * a_step, a_lbo, a_sbo), smem_desc(bh + kk * 2 * b_lbo, b_lbo, 128), idesc,
+                     kk > 0);
         for (int kk = 0; kk < nk; ++kk)
-            mma_bf16(d, smem_desc(ah + kk * 256, 128, a_sbo), smem_desc(bl + kk * 2 * b_lbo, b_lbo, 128), idesc, 1);
+            mma_bf16(d, smem_desc(ah + kk * a_step, a_lbo, a_sbo), smem_desc(bl + kk * 2 * b_lbo, b_lbo, 128), idesc, 1);
         for (int kk = 0; kk < nk; ++kk)
-            mma_bf16(d, smem_desc(ah + kk * 256, 128, a_sbo), smem_desc(bh + kk * 2 * b_lbo, b_lbo, 128), idesc, 1);
+            mma_bf16(d, smem_desc(ah + kk * a_step, a_lbo, a_sbo), smem_desc(bh + kk * 2 * b_lbo, b_lbo, 128), idesc, 1);
     };
+    // this direction's operands in the shared slot
+    constexpr uint32_t A1 = REV ? chainrec::KD : chainrec::WN, A1L = REV ? chainrec::KD_LO : chainrec::WN_LO;
+    constexpr uint32_t A2 = REV ? chainrec::WN : chainrec::KD, A2L = REV ? chainrec::WN_LO : chainrec::KD_LO;
 
     bool ok = true;
     for (int s = 0; s < nch; ++s) {
@@ -160,8 +165,8 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
         fail_wait(&full[s & 1], (s >> 1) & 1);
         tc_fence_after();
         if (tid == 0) {   // D1 = A1 Z  (M = 64, N = JW, K = 128)
-            mma3(tD1, smem_u32(sl + chainrec::A1), smem_u32(sl + chainrec::A1_LO), smem_u32(ZB), smem_u32(ZL), 8,
-                 2048, L::ZK, idesc_bf16(64, JW, 0, 1));
+            mma3(tD1, smem_u32(sl + A1), smem_u32(sl + A1L), smem_u32(ZB), smem_u32(ZL), 8, 256, 128, 2048, L::ZK,
+                 idesc_bf16(64, JW, 0, 1));
             mma_commit(bar1);
             if (s + 1 < nch) {   // warm L2 with the next chunk's Y (and P)
                 asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(y_ptr(s + 1))),
@@ -216,8 +221,8 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
         tc_fence_after();
         if (*sh_fail) { ok = false; break; }
         if (tid == 0) {   // D3 = A2 X  (M = 128, N = JW, K = 64)
-            mma3(tD3, smem_u32(sl + chainrec::A2), smem_u32(sl + chainrec::A2_LO), smem_u32(XB), smem_u32(XL), 4,
-                 1024, L::XK, idesc_bf16(128, JW, 0, 1));
+            mma3(tD3, smem_u32(sl + A2), smem_u32(sl + A2L), smem_u32(XB), smem_u32(XL), 4, 4096, 2048, 128, L::XK,
+                 idesc_bf16(128, JW, 1, 1));
             mma_commit(bar2);
         }
         fail_wait(bar2, par);
@@ -305,13 +310,13 @@ static cudaError_t launch_chain(const Params& p, const ChainSrc& src, cudaStream
 cudaError_t launch_chain_bwd_tc(const Params& p, const uint8_t* bw, cudaStream_t st) {
     ChainSrc src{bw, bwrec::BYTES, reinterpret_cast<const float*>(bw + bwrec::Y), bwrec::BYTES / 4,
                  reinterpret_cast<const float*>(bw + bwrec::P), bwrec::BYTES / 4};
-    static_assert(bwrec::BYTES % 256 == 0 && fwrec::BYTES % 256 == 0, "record strides");
+    static_assert(bwrec::BYTES % 256 == 0, "record stride");
     return launch_chain<true>(p, src, st);
 }
 
-cudaError_t launch_chain_rec_tc(const Params& p, const uint8_t* fw, cudaStream_t st) {
+cudaError_t launch_chain_rec_tc(const Params& p, const uint8_t* bw, cudaStream_t st) {
     const RecLayout L = RecLayout::make(128, 128);
-    ChainSrc src{fw, fwrec::BYTES, p.rec + L.U0, p.rec_stride, nullptr, 0};
+    ChainSrc src{bw, bwrec::BYTES, p.rec + L.U0, p.rec_stride, nullptr, 0};
     return launch_chain<false>(p, src, st);
 }
 

@@ -835,8 +835,8 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
 //
 // Per (chunk, head): the dS-independent terms of the reverse recursion, Y = scale Aqk^T dO and
 // P = scale Qg^T dO (warp tf32 MMAs with the left operand split into hi + lo; dO is bf16 and exact
-// in tf32), plus the split bf16 K-major operands of the two tcgen05 chains of the backward: Kd and
-// -W^T for the reverse chain (record bwrec), -W and Kd^T for the forward state recompute (fwrec).
+// in tf32), plus the split bf16 operand slot of the two tcgen05 chains of the backward (Kd and -W,
+// record layout chainrec / bwrec).
 namespace {
 constexpr int PB_A = 0;                  // [64][P64]   Aqk
 constexpr int PB_Q = PB_A + 64 * P64;    // [64][P128]  Qg
@@ -844,7 +844,7 @@ constexpr int PB_D = PB_Q + 64 * P128;   // [64][P128]  dO
 constexpr int PB_FLOATS = PB_D + 64 * P128;
 }  // namespace
 
-__global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw, uint8_t* fw) {
+__global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) {
     extern __shared__ float sm[];
     const int c = blockIdx.x, h = blockIdx.y;
     if (c >= p.chunk_off[p.N]) return;
@@ -857,7 +857,6 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw, 
     const RecLayout L = RecLayout::make(K, V);
     const float* rec = p.rec + ((size_t)c * H + h) * p.rec_stride;
     uint8_t* out = bw + ((size_t)c * H + h) * bwrec::BYTES;
-    uint8_t* fout = fw + ((size_t)c * H + h) * fwrec::BYTES;
     float* sA = sm + PB_A;
     float* sQ = sm + PB_Q;
     float* sD = sm + PB_D;
@@ -884,9 +883,8 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw, 
 #pragma unroll
         for (int e = 0; e < 8; ++e) sD[t * P128 + j8 + e] = f[e];
     }
-    // Chain operands as bf16 hi + lo in the K-major layouts of chainrec.  Reverse chain: A1 = Kd
-    // (rows t, K = c), A2 = -W^T (rows c, K = t).  Forward recompute: A1 = -W, A2 = Kd^T.
-    auto put_split8 = [](uint8_t* base, uint32_t o, const float* v, float sg) {
+    // Chain operands: Kd and -W as bf16 hi + lo [64 t][128 c] K-major tiles (one slot for both chains)
+    auto put_split8 = [](uint8_t* base, uint32_t o, uint32_t lo_off, const float* v, float sg) {
         float hv[8], lv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -895,7 +893,7 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw, 
             lv[e] = x - hv[e];
         }
         *reinterpret_cast<uint4*>(base + o) = pack8_bf16(hv);
-        *reinterpret_cast<uint4*>(base + o + (chainrec::A1_LO - chainrec::A1)) = pack8_bf16(lv);
+        *reinterpret_cast<uint4*>(base + o + lo_off) = pack8_bf16(lv);
     };
     for (int i = tid; i < 64 * K / 8; i += 256) {
         const int t = i >> 4, c8 = (i & 15) * 8;
@@ -904,28 +902,11 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw, 
         *reinterpret_cast<float4*>(kd + 4) = *reinterpret_cast<const float4*>(rec + L.Kd + t * K + c8 + 4);
         *reinterpret_cast<float4*>(w) = *reinterpret_cast<const float4*>(rec + L.W + t * K + c8);
         *reinterpret_cast<float4*>(w + 4) = *reinterpret_cast<const float4*>(rec + L.W + t * K + c8 + 4);
-        const uint32_t o = chainrec::A1 + km_bf16(t, c8, 2048, 128);
-        put_split8(out, o, kd, 1.f);
-        put_split8(fout, o, w, -1.f);
+        const uint32_t o = km_bf16(t, c8, 2048, 128);
+        put_split8(out, chainrec::KD + o, chainrec::KD_LO - chainrec::KD, kd, 1.f);
+        put_split8(out, chainrec::WN + o, chainrec::WN_LO - chainrec::WN, w, -1.f);
     }
-    for (int i = tid; i < K * 8; i += 256) {
-        const int cc = i & 127, t8 = (i >> 7) * 8;
-        float w[8], kd[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            w[u] = rec[L.W + (t8 + u) * K + cc];
-            kd[u] = rec[L.Kd + (t8 + u) * K + cc];
-        }
-        const uint32_t o = chainrec::A2 + km_bf16(cc, t8, 1024, 128);
-        static_assert(chainrec::A2_LO - chainrec::A2 == chainrec::A1_LO - chainrec::A1, "lo halves at one offset");
-        put_split8(out, o, w, -1.f);
-        put_split8(fout, o, kd, 1.f);
-    }
-    if (tid < K) {
-        const float gc = rec[L.gC + tid];
-        reinterpret_cast<float*>(out + chainrec::GC)[tid] = gc;
-        reinterpret_cast<float*>(fout + chainrec::GC)[tid] = gc;
-    }
+    if (tid < K) reinterpret_cast<float*>(out + chainrec::GC)[tid] = rec[L.gC + tid];
     cp_async_wait_all();
     __syncthreads();
     // Y = scale Aqk^T dO (64 x 128): warp w owns rows 16 (w / 2) and columns 64 (w % 2) .. + 64.
@@ -970,12 +951,12 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw, 
     }
 }
 
-cudaError_t launch_bwd_pre(const Params& p, uint8_t* bw, uint8_t* fw, cudaStream_t st) {
+cudaError_t launch_bwd_pre(const Params& p, uint8_t* bw, cudaStream_t st) {
     const size_t smem = (size_t)PB_FLOATS * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(bwd_pre_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     timing_pre(st, K_BWD_PRE);
-    bwd_pre_kernel<<<dim3(p.NCmax, p.H), 256, smem, st>>>(p, bw, fw);
+    bwd_pre_kernel<<<dim3(p.NCmax, p.H), 256, smem, st>>>(p, bw);
     timing_post(st);
     return cudaGetLastError();
 }

@@ -65,36 +65,32 @@ enum KernelId {
     K_INTRA_TC, K_CHAIN_FWD_TC, K_GRAD_TC, K_BWD_PRE, K_CHAIN_BWD_TC, K_CHAIN_REC_TC, K_NUM_KERNELS
 };
 
-// Records of the two tcgen05 state chains of the backward, per (chunk, head), K = V = 128 (bytes).
+// Record of the two tcgen05 state chains of the backward, per (chunk, head), K = V = 128 (bytes).
 // Both chains run  X = Y + A1 Z,  Z' = Diag(exp(Gamma_last)) Z + A2 X (+ P)  with every product in
 // split precision: operand = hi + lo, both bf16 (hi = bf16(x), lo = bf16(x - hi)), and the products
 // hi*hi + hi*lo + lo*hi (relative error ~1e-5).  The gradient of the log-decay at the end of a chunk
 // carries dS_end * S_end-sized terms far larger than its typical value, so the states and state
-// gradients need far better than tf32's 2^-11.  The first SLOT bytes are the two left operands in
-// their shared-memory layouts (one bulk copy per chunk):
+// gradients need far better than tf32's 2^-11.
+//   forward state recompute (Z = S entering chunk c):  A1 = -W,  A2 = Kd^T,  Y = U0, no P;
+//   reverse chain (Z = dS leaving chunk c):            A1 = Kd,  A2 = -W^T,  Y = scale Aqk^T dO,
+//                                                      P = scale Qg^T dO.
+// One slot serves both: Kd and -W are stored once as [64 t][128 c] bf16 K-major tiles
+// (km_bf16(t, c, 2048, 128)); read with swapped strides the same bytes are the MN-major layout of
+// Kd^T and -W^T (M = c, K = t).  The first SLOT bytes move into shared memory by one bulk copy:
 namespace chainrec {
-constexpr uint32_t A1 = 0;           // 64 rows (t) x 128 K (c), bf16 K-major km_bf16(t, c, 2048, 128), hi
-constexpr uint32_t A1_LO = 16384;    // lo
-constexpr uint32_t A2 = 32768;       // 128 rows (c) x 64 K (t), bf16 K-major km_bf16(c, t, 1024, 128), hi
-constexpr uint32_t A2_LO = 49152;    // lo
+constexpr uint32_t KD = 0;           // Kd  hi
+constexpr uint32_t KD_LO = 16384;    // Kd  lo
+constexpr uint32_t WN = 32768;       // -W  hi
+constexpr uint32_t WN_LO = 49152;    // -W  lo
 constexpr uint32_t GC = 65536;       // exp(Gamma_last) fp32 [128]
 constexpr uint32_t SLOT = 66048;
 }  // namespace chainrec
 
-// Reverse chain (Z = dS, the gradient w.r.t. the state leaving chunk c): A1 = Kd, A2 = -W^T,
-// Y = scale Aqk^T dO, P = scale Qg^T dO, so X = dU:
-//     dU = Y + Kd dS,   dS' = Diag(exp(Gamma_last)) dS - W^T dU + P.
 namespace bwrec {
-constexpr uint32_t Y = chainrec::SLOT;          // fp32 [64 t][128 j]
-constexpr uint32_t P = Y + 32768;               // fp32 [128 c][128 j]
+constexpr uint32_t Y = chainrec::SLOT;          // fp32 [64 t][128 j]: scale Aqk^T dO
+constexpr uint32_t P = Y + 32768;               // fp32 [128 c][128 j]: scale Qg^T dO
 constexpr uint32_t BYTES = P + 65536;           // record stride (256-byte multiple)
 }  // namespace bwrec
-
-// Forward state recompute (Z = S entering chunk c): A1 = -W, A2 = Kd^T, Y = U0 (read from the fp32
-// backward record), no P:   U = U0 - W S,   S' = Diag(exp(Gamma_last)) S + Kd^T U.
-namespace fwrec {
-constexpr uint32_t BYTES = chainrec::SLOT;
-}  // namespace fwrec
 
 // Launch bracketing for kda_timing_*: no-ops unless timing is active.
 void timing_pre(cudaStream_t st, int kernel_id);
@@ -107,9 +103,9 @@ cudaError_t launch_chain_bwd_simt(const Params& p, cudaStream_t st);
 cudaError_t launch_grad_simt(const Params& p, cudaStream_t st);
 cudaError_t launch_param_reduce(const Params& p, cudaStream_t st);
 cudaError_t launch_grad_tc(const Params& p, cudaStream_t st);
-cudaError_t launch_bwd_pre(const Params& p, uint8_t* bw, uint8_t* fw, cudaStream_t st);
+cudaError_t launch_bwd_pre(const Params& p, uint8_t* bw, cudaStream_t st);
 cudaError_t launch_chain_bwd_tc(const Params& p, const uint8_t* bw, cudaStream_t st);
-cudaError_t launch_chain_rec_tc(const Params& p, const uint8_t* fw, cudaStream_t st);
+cudaError_t launch_chain_rec_tc(const Params& p, const uint8_t* bw, cudaStream_t st);
 
 // tensor-core path (bf16, K = V = 128)
 size_t tc_record_bytes(int NCmax, int H);
