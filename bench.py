@@ -255,13 +255,17 @@ def run_ours(args, w):
               cu_seqlens=x["cu_seqlens"], initial_state=x["initial_state"])
 
     outs = {}
+    # a training step: the forward keeps the per-chunk quantities the backward would rebuild
+    nsaved = kda.saved_size(x["q"], x["v"], x["cu_seqlens"]) if w.backward else 0
+    saved = torch.empty(nsaved, dtype=torch.uint8, device=dev) if nsaved > 0 else None
 
     def step(inp):
         o, fs = kda.forward(*[inp[n] for n in names], output_final_state=w.final_state,
-                            out=outs.get("out"), final_state=outs.get("fs"), **kw)
+                            out=outs.get("out"), final_state=outs.get("fs"), saved=saved, **kw)
         outs["out"], outs["fs"] = o, fs
         if w.backward:
-            outs["grads"] = kda.backward(*[inp[n] for n in names], inp["dout"], grads=outs.get("grads"), **kw)
+            outs["grads"] = kda.backward(*[inp[n] for n in names], inp["dout"], grads=outs.get("grads"),
+                                         saved=saved, **kw)
 
     for _ in range(args.warmup):
         step(x)
@@ -316,11 +320,11 @@ def run_ours(args, w):
         o, fs = kda.forward(*[inp[n] for n in names], output_final_state=w.final_state, out=outs["out"],
                             final_state=outs.get("fs"), scale=x["scale"], lower_bound=x["lower_bound"],
                             chunk_size=x["chunk_size"], cu_seqlens=inp.get("cu_seqlens"),
-                            initial_state=inp.get("initial_state"))
+                            initial_state=inp.get("initial_state"), saved=saved)
         if w.backward:
             kda.backward(*[inp[n] for n in names], inp["dout"], grads=outs["grads"], scale=x["scale"],
                          lower_bound=x["lower_bound"], chunk_size=x["chunk_size"], cu_seqlens=inp.get("cu_seqlens"),
-                         initial_state=inp.get("initial_state"))
+                         initial_state=inp.get("initial_state"), saved=saved)
         for h, t in zip(host_out, result_tensors()):
             h.copy_(t, non_blocking=True)
 

@@ -6,6 +6,6 @@ ABI in ``include/kda.h``; this package only marshals torch tensors to it
 (``inputs``).  Importing the package does not load the library; the first
 call does, and raises if it has not been built.
 """
-from ._lib import KdaError, backward, device_status, forward, load  # noqa: F401
+from ._lib import KdaError, backward, device_status, forward, load, saved_size  # noqa: F401
 
-__all__ = ["forward", "backward", "load", "device_status", "KdaError"]
+__all__ = ["forward", "backward", "saved_size", "load", "device_status", "KdaError"]

@@ -23,7 +23,7 @@ KDA_BF16, KDA_FP32 = 0, 1
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_fwd_workspace_size", "kda_bwd_workspace_size", "kda_fwd", "kda_fwd_simt", "kda_bwd",
            "kda_status_string", "kda_device_status", "kda_version", "kda_timing_begin", "kda_timing_end",
-           "kda_kernel_name", "kda_fwd_noalloc")
+           "kda_kernel_name", "kda_fwd_noalloc", "kda_saved_size", "kda_fwd_save", "kda_bwd_saved")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -70,6 +70,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.kda_bwd.restype = ctypes.c_int
         lib.kda_bwd.argtypes = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int] + \
             [_vp] * 2 + [_vp] * 2 + [_vp] * 8 + [_vp, ctypes.c_size_t, _vp]
+        lib.kda_saved_size.restype = ctypes.c_size_t
+        lib.kda_saved_size.argtypes = [dims_p, ctypes.c_int]
+        lib.kda_fwd_save.restype = ctypes.c_int
+        lib.kda_fwd_save.argtypes = fwd_args[:-3] + [_vp, ctypes.c_size_t] + fwd_args[-3:]
+        lib.kda_bwd_saved.restype = ctypes.c_int
+        lib.kda_bwd_saved.argtypes = lib.kda_bwd.argtypes[:-3] + [_vp, ctypes.c_size_t] + lib.kda_bwd.argtypes[-3:]
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_device_status.restype = ctypes.c_int
@@ -164,8 +170,13 @@ def _contig(*ts):
 
 def forward(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale: float, lower_bound: float = -5.0,
             chunk_size: int = 64, cu_seqlens=None, initial_state=None, output_final_state: bool = False,
-            out=None, final_state=None, simt: bool = False, stream: Optional[torch.cuda.Stream] = None):
-    """KDA forward through ``kda_fwd`` (or ``kda_fwd_simt``).  Returns (out, final_state or None)."""
+            out=None, final_state=None, simt: bool = False, saved: Optional[torch.Tensor] = None,
+            stream: Optional[torch.cuda.Stream] = None):
+    """KDA forward through ``kda_fwd`` (or ``kda_fwd_simt``).  Returns (out, final_state or None).
+
+    ``saved``: a device byte buffer of ``saved_size(...)`` bytes; the forward then runs
+    ``kda_fwd_save`` and keeps the per-chunk quantities there for ``backward(..., saved=...)``.
+    """
     lib = load()
     _contig(q, k, v, g_raw, beta_raw, a_log, dt_bias, cu_seqlens, initial_state)
     dims = make_dims(q, v, cu_seqlens)
@@ -181,20 +192,38 @@ def forward(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale: float, lower_bou
     ws_bytes = lib.kda_fwd_workspace_size(ctypes.byref(dims), chunk_size)
     ws = workspace_cache.get(q.device, "fwd", ws_bytes)
     st = stream if stream is not None else torch.cuda.current_stream(q.device)
+    head = (ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw), _ptr(a_log),
+            _ptr(dt_bias), float(scale), float(lower_bound), int(chunk_size), _ptr(cu_seqlens),
+            _ptr(initial_state), _ptr(out), _ptr(final_state))
+    tail = (_ptr(ws), ctypes.c_size_t(ws.numel()), ctypes.c_void_p(st.cuda_stream))
+    if saved is not None:
+        if simt:
+            raise ValueError("saved= needs the tensor-core forward")
+        code = lib.kda_fwd_save(*head, _ptr(saved), ctypes.c_size_t(saved.numel() * saved.element_size()), *tail)
+        _check(code, "kda_fwd_save")
+        return out, final_state
     fn = lib.kda_fwd_simt if simt else lib.kda_fwd
-    code = fn(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw), _ptr(a_log),
-              _ptr(dt_bias), float(scale), float(lower_bound), int(chunk_size), _ptr(cu_seqlens),
-              _ptr(initial_state), _ptr(out), _ptr(final_state), _ptr(ws), ctypes.c_size_t(ws.numel()),
-              ctypes.c_void_p(st.cuda_stream))
+    code = fn(*head, *tail)
     _check(code, "kda_fwd_simt" if simt else "kda_fwd")
     return out, final_state
+
+
+def saved_size(q, v, cu_seqlens=None, chunk_size: int = 64) -> int:
+    """Bytes of the buffer ``forward(..., saved=...)`` fills (0: the shape has no saved path)."""
+    lib = load()
+    dims = make_dims(q, v, cu_seqlens)
+    return int(lib.kda_saved_size(ctypes.byref(dims), int(chunk_size)))
 
 
 def backward(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale: float, lower_bound: float = -5.0,
              chunk_size: int = 64, cu_seqlens=None, initial_state=None, dfinal_state=None,
              want_dinitial_state: bool = True, grads: Optional[dict] = None,
-             stream: Optional[torch.cuda.Stream] = None) -> dict:
-    """KDA backward through ``kda_bwd``.  Returns a dict of fp32 gradients."""
+             saved: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """KDA backward through ``kda_bwd``.  Returns a dict of fp32 gradients.
+
+    ``saved``: the buffer a ``forward(..., saved=...)`` on the same inputs filled; the backward then
+    runs ``kda_bwd_saved`` and skips rebuilding the per-chunk quantities.
+    """
     lib = load()
     _contig(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, cu_seqlens, initial_state, dfinal_state)
     dims = make_dims(q, v, cu_seqlens)
@@ -212,11 +241,16 @@ def backward(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale: float, lo
     ws_bytes = lib.kda_bwd_workspace_size(ctypes.byref(dims), chunk_size)
     ws = workspace_cache.get(dev, "bwd", ws_bytes)
     st = stream if stream is not None else torch.cuda.current_stream(dev)
-    code = lib.kda_bwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw), _ptr(a_log),
-                       _ptr(dt_bias), float(scale), float(lower_bound), int(chunk_size), _ptr(cu_seqlens),
-                       _ptr(initial_state), _ptr(dout), _ptr(dfinal_state), _ptr(grads["dq"]), _ptr(grads["dk"]),
-                       _ptr(grads["dv"]), _ptr(grads["dg_raw"]), _ptr(grads["dbeta_raw"]), _ptr(grads["da_log"]),
-                       _ptr(grads["ddt_bias"]), _ptr(grads.get("dinitial_state")), _ptr(ws),
-                       ctypes.c_size_t(ws.numel()), ctypes.c_void_p(st.cuda_stream))
+    head = (ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw), _ptr(a_log),
+            _ptr(dt_bias), float(scale), float(lower_bound), int(chunk_size), _ptr(cu_seqlens),
+            _ptr(initial_state), _ptr(dout), _ptr(dfinal_state), _ptr(grads["dq"]), _ptr(grads["dk"]),
+            _ptr(grads["dv"]), _ptr(grads["dg_raw"]), _ptr(grads["dbeta_raw"]), _ptr(grads["da_log"]),
+            _ptr(grads["ddt_bias"]), _ptr(grads.get("dinitial_state")))
+    tail = (_ptr(ws), ctypes.c_size_t(ws.numel()), ctypes.c_void_p(st.cuda_stream))
+    if saved is not None:
+        code = lib.kda_bwd_saved(*head, _ptr(saved), ctypes.c_size_t(saved.numel() * saved.element_size()), *tail)
+        _check(code, "kda_bwd_saved")
+        return grads
+    code = lib.kda_bwd(*head, *tail)
     _check(code, "kda_bwd")
     return grads

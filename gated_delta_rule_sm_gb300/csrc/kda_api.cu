@@ -217,7 +217,9 @@ static const char* kKernelNames[] = {"kda_plan",          "kda_intra_simt",   "k
                                      "kda_grad_tc",       "kda_bwd_pre",      "kda_chain_bwd_tc",
                                      "kda_chain_rec_tc"};
 
-static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cudaStream_t stream) {
+// saved != NULL: also keep the fp32 backward record there (kda_fwd_save)
+static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cudaStream_t stream,
+                         float* saved = nullptr) {
     const TcPlan w = plan_tc_fwd(s);
     kda_status st = check_ws(ws, ws_bytes, w.total);
     if (st != KDA_OK) return st;
@@ -226,10 +228,46 @@ static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cu
     char* b = static_cast<char*>(ws);
     p.chunk_off = reinterpret_cast<int32_t*>(b + w.off_chunk);
     uint8_t* recs = reinterpret_cast<uint8_t*>(b + w.off_rec);
+    if (saved) {
+        p.rec = saved;
+        p.rec_stride = RecLayout::make(s.K, s.V).bwd_size;
+    }
     KDA_TRY_CUDA(launch_plan(p, stream));
-    KDA_TRY_CUDA(launch_intra_tc(p, recs, false, stream));
+    KDA_TRY_CUDA(launch_intra_tc(p, recs, saved ? 2 : 0, stream));
     KDA_TRY_CUDA(launch_chain_fwd_tc(p, recs, false, stream));
     return KDA_OK;
+}
+
+// Tensor-core backward.  saved == NULL: the intra kernel rebuilds the fp32 backward record in the
+// workspace; otherwise the record kda_fwd_save kept is used and that pass is skipped.
+static kda_status bwd_tc(const Shape& s, Params p, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                         const float* saved) {
+    const TcBwdPlan w = plan_tc_bwd(s);
+    kda_status st = check_ws(workspace, workspace_bytes, w.total);
+    if (st != KDA_OK) return st;
+    st = status_ptr(&p.status);
+    if (st != KDA_OK) return st;
+    carve(p, w.simt, workspace);
+    if (saved) p.rec = const_cast<float*>(saved);   // same layout and stride as the workspace record area
+    uint8_t* bw = static_cast<uint8_t*>(workspace) + w.off_bwrec;
+    p.chunk_u = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.off_u);
+    p.chunk_du = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.off_du);
+    Params pf = p;   // the forward state recompute writes no output and no final state
+    pf.out = nullptr;
+    pf.ST = nullptr;
+    KDA_TRY_CUDA(launch_plan(p, stream));
+    if (!saved) KDA_TRY_CUDA(launch_intra_tc(p, nullptr, 1, stream));
+    KDA_TRY_CUDA(launch_bwd_pre(p, bw, stream));
+    KDA_TRY_CUDA(launch_chain_rec_tc(pf, bw, stream));
+    KDA_TRY_CUDA(launch_chain_bwd_tc(p, bw, stream));
+    KDA_TRY_CUDA(launch_grad_tc(p, stream));
+    return KDA_OK;
+}
+
+// Bytes of the record kda_fwd_save keeps (0 when the shape does not take the tensor-core path).
+static size_t saved_bytes_for(const Shape& s) {
+    if (!tc_eligible(s)) return 0;
+    return sizeof(float) * (size_t)s.NCmax * s.H * RecLayout::make(s.K, s.V).bwd_size;
 }
 
 }  // namespace kda
@@ -315,31 +353,8 @@ kda_status kda_bwd(const kda_dims* dims, const void* q, const void* k, const voi
     p.dout = dout; p.dST = dfinal_state;
     p.dq = dq; p.dk = dk; p.dv = dv; p.dg_raw = dg_raw; p.dbeta_raw = dbeta_raw;
     p.da_log = da_log; p.ddt_bias = ddt_bias; p.dS0 = dinitial_state;
-    if (tc_eligible(s) && lower_bound >= -5.0f && tc_inputs_aligned(p)) {
-        // tensor-core intra kernel (fp32 backward records), chain operands, tf32 tensor-core state
-        // recompute and reverse chain, per-chunk gradients
-        const TcBwdPlan w = plan_tc_bwd(s);
-        st = check_ws(workspace, workspace_bytes, w.total);
-        if (st != KDA_OK) return st;
-        st = status_ptr(&p.status);
-        if (st != KDA_OK) return st;
-        carve(p, w.simt, workspace);
-        Params pf = p;
-        pf.out = nullptr;
-        pf.ST = nullptr;
-        KDA_TRY_CUDA(launch_plan(p, stream));
-        KDA_TRY_CUDA(launch_intra_tc(p, nullptr, true, stream));
-        uint8_t* bw = static_cast<uint8_t*>(workspace) + w.off_bwrec;
-        p.chunk_u = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.off_u);
-        p.chunk_du = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.off_du);
-        pf.chunk_u = p.chunk_u;
-        pf.chunk_du = p.chunk_du;
-        KDA_TRY_CUDA(launch_bwd_pre(p, bw, stream));
-        KDA_TRY_CUDA(launch_chain_rec_tc(pf, bw, stream));
-        KDA_TRY_CUDA(launch_chain_bwd_tc(p, bw, stream));
-        KDA_TRY_CUDA(launch_grad_tc(p, stream));
-        return KDA_OK;
-    }
+    if (tc_eligible(s) && lower_bound >= -5.0f && tc_inputs_aligned(p))
+        return bwd_tc(s, p, workspace, workspace_bytes, stream, nullptr);
     const WsPlan w = plan_simt(s, true);
     st = check_ws(workspace, workspace_bytes, w.total);
     if (st != KDA_OK) return st;
@@ -352,6 +367,58 @@ kda_status kda_bwd(const kda_dims* dims, const void* q, const void* k, const voi
     KDA_TRY_CUDA(launch_chain_bwd_simt(p, stream));
     KDA_TRY_CUDA(launch_grad_simt(p, stream));
     return KDA_OK;
+}
+
+size_t kda_saved_size(const kda_dims* dims, int chunk_size) {
+    Shape s;
+    if (!dims) return 0;
+    if (check_dims(dims, chunk_size, dims->num_seqs > 0 && dims->B == 1, &s) != KDA_OK &&
+        check_dims(dims, chunk_size, false, &s) != KDA_OK)
+        return 0;
+    return saved_bytes_for(s);
+}
+
+kda_status kda_fwd_save(const kda_dims* dims, const void* q, const void* k, const void* v, const void* g_raw,
+                        const void* beta_raw, const float* a_log, const float* dt_bias, float scale,
+                        float lower_bound, int chunk_size, const int32_t* cu_seqlens, const float* initial_state,
+                        void* out, float* final_state, void* saved, size_t saved_bytes, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+    Shape s;
+    kda_status st = common_checks(dims, chunk_size, cu_seqlens, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale,
+                                  lower_bound, &s);
+    if (st != KDA_OK) return st;
+    if (!out) return KDA_ERR_INVALID_ARG;
+    Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
+                           initial_state);
+    if (!tc_eligible(s) || lower_bound < -5.0f || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
+    const size_t need = saved_bytes_for(s);
+    if (!saved || saved_bytes < need || (reinterpret_cast<uintptr_t>(saved) % kAlign)) return KDA_ERR_WORKSPACE;
+    p.out = out;
+    p.ST = final_state;
+    return fwd_tc(s, p, workspace, workspace_bytes, stream, static_cast<float*>(saved));
+}
+
+kda_status kda_bwd_saved(const kda_dims* dims, const void* q, const void* k, const void* v, const void* g_raw,
+                         const void* beta_raw, const float* a_log, const float* dt_bias, float scale,
+                         float lower_bound, int chunk_size, const int32_t* cu_seqlens, const float* initial_state,
+                         const void* dout, const float* dfinal_state, float* dq, float* dk, float* dv,
+                         float* dg_raw, float* dbeta_raw, float* da_log, float* ddt_bias, float* dinitial_state,
+                         const void* saved, size_t saved_bytes, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+    Shape s;
+    kda_status st = common_checks(dims, chunk_size, cu_seqlens, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale,
+                                  lower_bound, &s);
+    if (st != KDA_OK) return st;
+    if (!dout || !dq || !dk || !dv || !dg_raw || !dbeta_raw || !da_log || !ddt_bias) return KDA_ERR_INVALID_ARG;
+    Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
+                           initial_state);
+    p.dout = dout; p.dST = dfinal_state;
+    p.dq = dq; p.dk = dk; p.dv = dv; p.dg_raw = dg_raw; p.dbeta_raw = dbeta_raw;
+    p.da_log = da_log; p.ddt_bias = ddt_bias; p.dS0 = dinitial_state;
+    if (!tc_eligible(s) || lower_bound < -5.0f || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
+    const size_t need = saved_bytes_for(s);
+    if (!saved || saved_bytes < need || (reinterpret_cast<uintptr_t>(saved) % kAlign)) return KDA_ERR_WORKSPACE;
+    return bwd_tc(s, p, workspace, workspace_bytes, stream, static_cast<const float*>(saved));
 }
 
 const char* kda_status_string(kda_status s) {

@@ -110,7 +110,8 @@ cudaError_t launch_chain_rec_tc(const Params& p, const uint8_t* bw, cudaStream_t
 // tensor-core path (bf16, K = V = 128)
 size_t tc_record_bytes(int NCmax, int H);
 bool tc_inputs_aligned(const Params& p);
-cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, bool bwd, cudaStream_t st);
+// mode 0: forward chain record; 1: fp32 backward record; 2: both
+cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, int mode, cudaStream_t st);
 cudaError_t launch_chain_fwd_tc(const Params& p, const uint8_t* recs, bool store_states, cudaStream_t st);
 
 }  // namespace kda

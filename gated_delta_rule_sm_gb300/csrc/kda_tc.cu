@@ -64,14 +64,17 @@ constexpr uint32_t BAR = SMALL + (64 * 3 + 128 + 1024) * 4;
 constexpr uint32_t BYTES = BAR + 64;
 }  // namespace intralay
 
-// BWD = false writes the chain record (tcrec) of the forward; BWD = true writes the fp32 per-chunk
-// record (RecLayout) that the backward's operand, chain and gradient kernels read instead.
-template <bool BWD>
+// MODE 0 writes the chain record (tcrec) of the forward; MODE 1 writes the fp32 per-chunk record
+// (RecLayout) that the backward's operand, chain and gradient kernels read; MODE 2 writes both (a
+// forward that keeps the backward record, so the backward skips this pass).
+template <int MODE>
 __global__ void __launch_bounds__(256, 1)
     intra_tc_kernel(Params p, uint8_t* recs, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_g,
                     const __grid_constant__ CUtensorMap tm_v) {
     using namespace intralay;
+    constexpr bool BWD = MODE != 0;      // writes the fp32 backward record
+    constexpr bool FWDREC = MODE != 1;   // writes the forward chain record
     extern __shared__ __align__(1024) uint8_t smem[];
     const int H = p.H;
     const int nitems = p.chunk_off[p.N] * H;   // (chunk, head) items, head fastest
@@ -126,7 +129,7 @@ __global__ void __launch_bounds__(256, 1)
     int h, c, tok0;
     const int len = item_tok0(item, h, c, tok0);
     float* frec = BWD ? p.rec + ((size_t)c * H + h) * p.rec_stride : nullptr;
-    uint8_t* rec = BWD ? nullptr : recs + ((size_t)c * H + h) * tcrec::BYTES;
+    uint8_t* rec = FWDREC ? recs + ((size_t)c * H + h) * tcrec::BYTES : nullptr;
     if (tid < 128) sdtb[tid] = p.dt_bias[h * 128 + tid];
     if (tid < 64) sbeta[tid] = tid < len ? sigmoidf_acc(load_act(p.beta_raw, (size_t)(tok0 + tid) * H + h, KDA_BF16)) : 0.f;
     ok = __syncthreads_and(mbar_wait(bar_load, par_load) ? 1 : 0) != 0;
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(256, 1)
             fj[ci][1] = bi == 1 ? fd : bi == 2 ? 1.f : bi == 3 ? fm2 : 0.f;
             fj[ci][2] = bi == 2 ? fd : bi == 3 ? 1.f : 0.f;
             fj[ci][3] = bi == 3 ? fd : 0.f;
-            if (!BWD && bi == 0) reinterpret_cast<float*>(rec + tcrec::GC)[cc] = B0 * B1 * B2 * B3;
+            if (FWDREC && bi == 0) reinterpret_cast<float*>(rec + tcrec::GC)[cc] = B0 * B1 * B2 * B3;
             if (BWD) {
                 float gpre = 0.f;
                 for (int m = 0; m < bi; ++m) gpre += sgsum[m * 128 + cc];
@@ -277,11 +280,11 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 *reinterpret_cast<uint4*>(smem + KVB + km_bf16(cc, tb, 1024, 128)) = pack8_bf16(vk);
                 *reinterpret_cast<uint4*>(smem + KGLO + km_bf16(cc, tb, 1024, 128)) = pack8_bf16(vkl);
-                if (!BWD) *reinterpret_cast<uint4*>(rec + tcrec::WQ + mn_bf16(64 + tb, cc, 128, 2048)) = pack8_bf16(vq);
+                if (FWDREC) *reinterpret_cast<uint4*>(rec + tcrec::WQ + mn_bf16(64 + tb, cc, 128, 2048)) = pack8_bf16(vq);
             }
             // Kd^T (tf32): k * exp(Gamma_C - Gamma_t), four tokens per 16 B (forward record only)
 #pragma unroll
-            for (int qd = 0; qd < (BWD ? 0 : 4); ++qd) {
+            for (int qd = 0; qd < (FWDREC ? 4 : 0); ++qd) {
                 const int u = 4 * qd;
                 float kb[4];
 #pragma unroll
@@ -406,7 +409,7 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 const int t = tid - 64;
 #pragma unroll
-                for (int s4 = 0; s4 < (BWD ? 0 : 64); s4 += 4) {
+                for (int s4 = 0; s4 < (FWDREC ? 64 : 0); s4 += 4) {
                     float4 v4;
                     v4.x = tf32_rn(s4 <= t ? d[s4] : 0.f);
                     v4.y = tf32_rn(s4 + 1 <= t ? d[s4 + 1] : 0.f);
@@ -516,7 +519,7 @@ __global__ void __launch_bounds__(256, 1)
             tmem_ld_wait();
             if (warp < 4) {
                 const int cc = tid;
-                if (!BWD)
+                if (FWDREC)
 #pragma unroll
                     for (int tb = 0; tb < 64; tb += 8)
                         *reinterpret_cast<uint4*>(rec + tcrec::WQ + mn_bf16(tb, cc, 128, 2048)) = pack8_bf16(d + tb);
@@ -526,7 +529,7 @@ __global__ void __launch_bounds__(256, 1)
             } else {
                 const int j = tid - 128;
                 float4* dst = reinterpret_cast<float4*>(rec + tcrec::U0 + j * 256);
-                if (!BWD)
+                if (FWDREC)
 #pragma unroll
                     for (int t4 = 0; t4 < 16; ++t4)
                         dst[t4] = make_float4(d[4 * t4], d[4 * t4 + 1], d[4 * t4 + 2], d[4 * t4 + 3]);
@@ -810,12 +813,12 @@ bool tc_inputs_aligned(const Params& p) {
     return al(p.q) && al(p.k) && al(p.g_raw) && al(p.v) && (p.dout == nullptr || al(p.dout));
 }
 
-cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, bool bwd, cudaStream_t st) {
+cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, int mode, cudaStream_t st) {
     CUtensorMap mq, mk, mg, mv;
     if (!head_tile_map(&mq, p.q, p.H, p.TT) || !head_tile_map(&mk, p.k, p.H, p.TT) ||
         !head_tile_map(&mg, p.g_raw, p.H, p.TT) || !head_tile_map(&mv, p.v, p.H, p.TT))
         return cudaErrorInvalidValue;
-    auto kern = bwd ? intra_tc_kernel<true> : intra_tc_kernel<false>;
+    auto kern = mode == 0 ? intra_tc_kernel<0> : mode == 1 ? intra_tc_kernel<1> : intra_tc_kernel<2>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)intralay::BYTES);
     if (e != cudaSuccess) return e;
     timing_pre(st, K_INTRA_TC);

@@ -110,7 +110,7 @@ kda_status kda_fwd_simt(const kda_dims* dims,
 
 /*
  * Backward (recomputes the forward internally; nothing is saved between
- * calls).  Inputs as for kda_fwd plus dout [B,T,H,V] (input dtype) and
+ * calls; see kda_fwd_save / kda_bwd_saved for the pair that keeps it).  Inputs as for kda_fwd plus dout [B,T,H,V] (input dtype) and
  * dfinal_state [N,H,K,V] fp32 (may be NULL = zero).  Writes fp32 gradients
  * dq, dk, dg_raw [B,T,H,K], dv [B,T,H,V], dbeta_raw [B,T,H], da_log [H],
  * ddt_bias [H*K] and, if dinitial_state != NULL, dinitial_state [N,H,K,V].
@@ -126,6 +126,44 @@ kda_status kda_bwd(const kda_dims* dims,
                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Human-readable name of a status code (static string). */
+/*
+ * Training pair: a forward that keeps what the backward would otherwise
+ * recompute.  A training step runs the forward and then the backward on the
+ * same inputs; kda_bwd rebuilds the per-chunk intra quantities (the WY/UT
+ * transform, gates, norms) that the forward already formed.  kda_fwd_save
+ * runs the forward and also writes those quantities (fp32, per chunk and
+ * head, an internal layout) to the caller's `saved` buffer; kda_bwd_saved
+ * takes the same arguments as kda_bwd plus that buffer and skips the
+ * rebuild.  Results are identical to kda_fwd / kda_bwd.
+ *
+ * kda_saved_size returns the bytes `saved` must hold for these dims (0 when
+ * the shape does not take the tensor-core path; then use kda_fwd / kda_bwd).
+ * `saved` is a device buffer owned by the caller, 256-byte aligned; its
+ * contents are only valid for the inputs of the kda_fwd_save call that wrote
+ * them (same q, k, v, g_raw, beta_raw, a_log, dt_bias, lower_bound,
+ * cu_seqlens), until the caller reuses the buffer.  Both calls return
+ * KDA_ERR_UNSUPPORTED when the tensor-core path does not apply (dtype, K, V,
+ * lower_bound < -5 or unaligned activations) and KDA_ERR_WORKSPACE for a
+ * missing, small or misaligned `saved`.  The workspace of kda_fwd_save is
+ * kda_fwd_workspace_size's, of kda_bwd_saved kda_bwd_workspace_size's.
+ */
+size_t kda_saved_size(const kda_dims* dims, int chunk_size);
+kda_status kda_fwd_save(const kda_dims* dims,
+                        const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
+                        const float* a_log, const float* dt_bias, float scale, float lower_bound, int chunk_size,
+                        const int32_t* cu_seqlens, const float* initial_state,
+                        void* out, float* final_state, void* saved, size_t saved_bytes,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+kda_status kda_bwd_saved(const kda_dims* dims,
+                         const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
+                         const float* a_log, const float* dt_bias, float scale, float lower_bound, int chunk_size,
+                         const int32_t* cu_seqlens, const float* initial_state,
+                         const void* dout, const float* dfinal_state,
+                         float* dq, float* dk, float* dv, float* dg_raw, float* dbeta_raw,
+                         float* da_log, float* ddt_bias, float* dinitial_state,
+                         const void* saved, size_t saved_bytes,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 const char* kda_status_string(kda_status s);
 
 /* Device status word of the current device: KDA_OK, or the first error a

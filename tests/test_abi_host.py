@@ -102,3 +102,43 @@ def test_workspace_sizes_grow_with_problem(lib):
     assert s(num_seqs=5) >= s()            # packed sizing covers the fixed-length layout
     assert lib.kda_fwd_workspace_size(ctypes.byref(_dims(K=8)), 64) == 0
     assert lib.kda_fwd_workspace_size(None, 64) == 0
+
+
+def _fwd_save(lib, dims, saved=None, saved_bytes=0, ptr=16, lb=-5.0):
+    p = ctypes.c_void_p(ptr)
+    return lib.kda_fwd_save(ctypes.byref(dims), p, p, p, p, p, p, p, 0.125, lb, 64, None, None, p, None,
+                            saved, ctypes.c_size_t(saved_bytes), None, ctypes.c_size_t(0), None)
+
+
+def _bwd_saved(lib, dims, saved=None, saved_bytes=0, ptr=16):
+    p = ctypes.c_void_p(ptr)
+    return lib.kda_bwd_saved(ctypes.byref(dims), p, p, p, p, p, p, p, 0.125, -5.0, 64, None, None, p, None,
+                             p, p, p, p, p, p, p, None, saved, ctypes.c_size_t(saved_bytes), None,
+                             ctypes.c_size_t(0), None)
+
+
+def test_saved_context_sizes(lib):
+    sz = lambda **kw: lib.kda_saved_size(ctypes.byref(_dims(**kw)), 64)
+    assert sz() == 0                                        # K = V = 64: no tensor-core path, nothing to keep
+    assert sz(K=128, V=128, dtype=_lib.KDA_FP32) == 0
+    one = sz(K=128, V=128)
+    assert one > 0 and one % 256 == 0
+    assert sz(K=128, V=128, T=512) == 2 * one               # one record per (chunk, head)
+    assert sz(K=128, V=128, H=4) == 2 * one
+    assert lib.kda_saved_size(None, 64) == 0
+
+
+def test_saved_context_validation(lib):
+    d64, d128 = _dims(), _dims(K=128, V=128)
+    need = lib.kda_saved_size(ctypes.byref(d128), 64)
+    # shapes off the tensor-core path are refused, not silently recomputed
+    assert _fwd_save(lib, d64) == _lib.KDA_ERR_UNSUPPORTED
+    assert _bwd_saved(lib, d64) == _lib.KDA_ERR_UNSUPPORTED
+    assert _fwd_save(lib, d128, lb=-6.0) == _lib.KDA_ERR_UNSUPPORTED
+    assert _fwd_save(lib, d128, ptr=24) == _lib.KDA_ERR_UNSUPPORTED          # unaligned activations
+    # the saved buffer: missing, too small, misaligned
+    assert _fwd_save(lib, d128) == _lib.KDA_ERR_WORKSPACE
+    assert _fwd_save(lib, d128, saved=ctypes.c_void_p(4096), saved_bytes=need - 256) == _lib.KDA_ERR_WORKSPACE
+    assert _fwd_save(lib, d128, saved=ctypes.c_void_p(4096 + 16), saved_bytes=need) == _lib.KDA_ERR_WORKSPACE
+    assert _bwd_saved(lib, d128) == _lib.KDA_ERR_WORKSPACE
+    assert _bwd_saved(lib, d128, saved=ctypes.c_void_p(4096), saved_bytes=need - 256) == _lib.KDA_ERR_WORKSPACE

@@ -201,3 +201,28 @@ def test_full_fwdbwd_bf16_B4_T4096_H32_sampled():
     assert rel_err(g["da_log"][heads], r_all["da_log"], "bf16") <= 2e-2
     K = x["q"].shape[-1]
     assert rel_err(g["ddt_bias"].view(-1, K)[heads], r_all["ddt_bias"].reshape(len(heads), K), "bf16") <= 2e-2
+
+
+# ------------------------------------------------------------------ training pair (forward keeps, backward reuses)
+
+def test_saved_pair_matches_plain_calls():
+    import gated_delta_rule_sm_gb300 as kda
+    lens = [70, 0, 129, 1, 64]
+    w = Workload("t", B=1, T=sum(lens), H=3, K=128, V=128, varlen=True, initial_state=True, backward=True, seed=31)
+    x = make_inputs(w, device=DEV, lengths=lens)
+    names = ("q", "k", "v", "g_raw", "beta_raw", "a_log", "dt_bias")
+    kw = dict(scale=x["scale"], lower_bound=x["lower_bound"], chunk_size=64, cu_seqlens=x["cu_seqlens"],
+              initial_state=x["initial_state"])
+    nbytes = kda.saved_size(x["q"], x["v"], x["cu_seqlens"])
+    assert nbytes > 0
+    saved = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    o1, f1 = kda.forward(*[x[n] for n in names], output_final_state=True, **kw)
+    o2, f2 = kda.forward(*[x[n] for n in names], output_final_state=True, saved=saved, **kw)
+    dfinal = 0.05 * torch.randn((len(lens), 3, 128, 128), generator=torch.Generator().manual_seed(3)).to(DEV)
+    g1 = kda.backward(*[x[n] for n in names], x["dout"], dfinal_state=dfinal, **kw)
+    g2 = kda.backward(*[x[n] for n in names], x["dout"], dfinal_state=dfinal, saved=saved, **kw)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+    for n in GRADS:
+        assert torch.equal(g1[n], g2[n]), n
