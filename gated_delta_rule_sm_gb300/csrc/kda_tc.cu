@@ -96,9 +96,14 @@ __global__ void __launch_bounds__(256, 1)
     const RecLayout RL = RecLayout::make(128, 128);
     // Each MMA barrier has at most one pending phase at any time, so parity waits are unambiguous.
     uint64_t* bar_load = reinterpret_cast<uint64_t*>(smem + BAR);
-    uint64_t* bar_a = bar_load + 1;   // MMAs reading tile pair A (and the final W / U0 MMAs)
-    uint64_t* bar_b = bar_load + 2;   // MMAs reading tile pair B
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_load + 3);
+    uint64_t* bar_a = bar_load + 1;   // A-matrix MMAs reading tile pair A (three issuing warps)
+    uint64_t* bar_b = bar_load + 2;   // A-matrix MMAs reading tile pair B (three issuing warps)
+    uint64_t* bar_w = bar_load + 3;   // the final W / U0 MMAs (two issuing warps)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_load + 4);
+    // TMEM columns: A-matrix partial products p = 0, 1, 2 at 64 p + 16 j (sub-block j), W^T at 192,
+    // U0^T at 256.  One thread issues a tcgen05.mma every ~100 cycles, so the three split products
+    // of each sub-block and the two final products go out from different warps in parallel.
+    constexpr uint32_t T_W = 192, T_U0 = 256, TCOLS = 512;
     // the raw q, k, g, v tiles of one item (64 tokens x 128 channels each, out-of-range rows zero)
     auto load_raw = [&](int it) {
         int h2, c2, t02;
@@ -112,17 +117,18 @@ __global__ void __launch_bounds__(256, 1)
 
     if (tid == 0) {
         mbar_init(bar_load, 1);
-        mbar_init(bar_a, 1);
-        mbar_init(bar_b, 1);
+        mbar_init(bar_a, 3);
+        mbar_init(bar_b, 3);
+        mbar_init(bar_w, 2);
         mbar_fence_init();
         load_raw(blockIdx.x);
     }
-    if (warp == 0) tmem_alloc(tslot, 256);
+    if (warp == 0) tmem_alloc(tslot, TCOLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    uint32_t par_a = 0, par_b = 0, par_load = 0;
+    uint32_t par_a = 0, par_b = 0, par_w = 0, par_load = 0;
     bool ok = true;
     // Persistent over items: each item's raw tiles were requested by the previous item (or above).
     for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
@@ -320,17 +326,17 @@ __global__ void __launch_bounds__(256, 1)
                 }
             }
         };
-        // A-matrix MMAs of column sub-block j: D_j = L_hi R_hi + L_hi R_lo + L_lo R_hi
+        // A-matrix MMAs of column sub-block j: D_j = L_hi R_hi + L_hi R_lo + L_lo R_hi, one partial
+        // product per issuing warp (warps 0, 1, 2), summed when the accumulators are read
         constexpr uint32_t idA = idesc_bf16(128, 16, 1, 1);
         auto issue_A = [&](int j, uint32_t hi_off, uint32_t lo_off, uint64_t* bar) {
+            if (lane != 0 || warp > 2) return;
             const uint32_t lh = smem_u32(smem + hi_off), ll = smem_u32(smem + lo_off);
             const uint32_t rh = smem_u32(smem + RB_HI) + j * 256, rl = smem_u32(smem + RB_LO) + j * 256;
+            const uint32_t la = warp == 2 ? ll : lh, rb = warp == 1 ? rl : rh;
             for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tmem + 16 * j, smem_desc(lh + kk * 4096, 2048, 128), smem_desc(rh + kk * 2048, 1024, 128), idA, kk > 0);
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tmem + 16 * j, smem_desc(lh + kk * 4096, 2048, 128), smem_desc(rl + kk * 2048, 1024, 128), idA, 1);
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tmem + 16 * j, smem_desc(ll + kk * 4096, 2048, 128), smem_desc(rh + kk * 2048, 1024, 128), idA, 1);
+                mma_bf16(tmem + 64 * warp + 16 * j, smem_desc(la + kk * 4096, 2048, 128),
+                         smem_desc(rb + kk * 2048, 1024, 128), idA, kk > 0);
             mma_commit(bar);
         };
         auto wait_on = [&](uint64_t* bar, uint32_t& par) -> bool {
@@ -343,13 +349,13 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_before();
         __syncthreads();                 // raw tiles are no longer read past this point
         tc_fence_after();
-        if (tid == 0) issue_A(0, LA_HI, LA_LO, bar_a);
+        issue_A(0, LA_HI, LA_LO, bar_a);
         write_L(1, LB_HI, LB_LO);
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (tid == 0) issue_A(1, LB_HI, LB_LO, bar_b);
+        issue_A(1, LB_HI, LB_LO, bar_b);
         if (!wait_on(bar_a, par_a)) goto fail;      // pair A free again
         tc_fence_after();
         write_L(2, LA_HI, LA_LO);
@@ -357,7 +363,7 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (tid == 0) issue_A(2, LA_HI, LA_LO, bar_a);
+        issue_A(2, LA_HI, LA_LO, bar_a);
         if (!wait_on(bar_b, par_b)) goto fail;      // pair B free again
         tc_fence_after();
         write_L(3, LB_HI, LB_LO);
@@ -365,7 +371,7 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (tid == 0) issue_A(3, LB_HI, LB_LO, bar_b);
+        issue_A(3, LB_HI, LB_LO, bar_b);
         if (!wait_on(bar_a, par_a)) goto fail;
         if (!wait_on(bar_b, par_b)) goto fail;
         tc_fence_after();
@@ -389,6 +395,17 @@ __global__ void __launch_bounds__(256, 1)
             tmem_ld16(tmem + lb + 32, d + 32);
             tmem_ld16(tmem + lb + 48, d + 48);
             tmem_ld_wait();
+#pragma unroll
+            for (int pp = 1; pp < 3; ++pp) {   // add the other two partial products
+                float e[16];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    tmem_ld16(tmem + lb + 64 * pp + 16 * q4, e);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) d[16 * q4 + u] += e[u];
+                }
+            }
             if (warp < 2) {
                 const int t = tid;
                 const float bt = sbeta[t];
@@ -485,33 +502,37 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         // ---- W^T = Kg^T T^T and U0^T = V^T (T_hi + T_lo)^T   (M = 128, N = 64, K = 64)
         constexpr uint32_t idW = idesc_bf16(128, 64, 0, 0);
-        if (tid == 0) {
+        if (lane == 0 && warp < 2) {   // warp 0: W^T, warp 1: U0^T
             const uint32_t kvb = smem_u32(smem + KVB), thi = smem_u32(smem + TB_HI), tlo = smem_u32(smem + TB_LO);
             const uint32_t kgl = smem_u32(smem + KGLO);
-            // W^T = (Kg_hi + Kg_lo)^T (T_hi + T_lo)^T without the lo * lo term
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + 64, smem_desc(kvb + kk * 256, 128, 1024), smem_desc(thi + kk * 256, 128, 1024), idW, kk > 0);
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + 64, smem_desc(kvb + kk * 256, 128, 1024), smem_desc(tlo + kk * 256, 128, 1024), idW, 1);
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + 64, smem_desc(kgl + kk * 256, 128, 1024), smem_desc(thi + kk * 256, 128, 1024), idW, 1);
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + 128, smem_desc(kvb + 16384 + kk * 256, 128, 1024), smem_desc(thi + kk * 256, 128, 1024),
-                         idW, kk > 0);
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + 128, smem_desc(kvb + 16384 + kk * 256, 128, 1024), smem_desc(tlo + kk * 256, 128, 1024),
-                         idW, 1);
-            mma_commit(bar_a);
+            if (warp == 0) {
+                // W^T = (Kg_hi + Kg_lo)^T (T_hi + T_lo)^T without the lo * lo term
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + T_W, smem_desc(kvb + kk * 256, 128, 1024), smem_desc(thi + kk * 256, 128, 1024), idW,
+                             kk > 0);
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + T_W, smem_desc(kvb + kk * 256, 128, 1024), smem_desc(tlo + kk * 256, 128, 1024), idW, 1);
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + T_W, smem_desc(kgl + kk * 256, 128, 1024), smem_desc(thi + kk * 256, 128, 1024), idW, 1);
+            } else {
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + T_U0, smem_desc(kvb + 16384 + kk * 256, 128, 1024),
+                             smem_desc(thi + kk * 256, 128, 1024), idW, kk > 0);
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + T_U0, smem_desc(kvb + 16384 + kk * 256, 128, 1024),
+                             smem_desc(tlo + kk * 256, 128, 1024), idW, 1);
+            }
+            mma_commit(bar_w);
         }
-        ok = __syncthreads_and(mbar_wait(bar_a, par_a) ? 1 : 0) != 0;
-        par_a ^= 1;
+        ok = __syncthreads_and(mbar_wait(bar_w, par_w) ? 1 : 0) != 0;
+        par_w ^= 1;
         if (!ok) goto fail;
         tc_fence_after();
         // ---- record W (MN-major, thread = channel) and U0 (column-major, thread = value column)
         {
             const uint32_t lb = static_cast<uint32_t>((warp & 3) * 32) << 16;
             float d[64];
-            const uint32_t col = warp < 4 ? 64u : 128u;
+            const uint32_t col = warp < 4 ? T_W : T_U0;
             tmem_ld16(tmem + lb + col, d);
             tmem_ld16(tmem + lb + col + 16, d + 16);
             tmem_ld16(tmem + lb + col + 32, d + 32);
@@ -545,7 +566,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, TCOLS);
     return;
 fail:
     // A wait gave up: record it, give outstanding copies / MMAs a bounded chance to land, release TMEM.
@@ -554,10 +575,11 @@ fail:
         mbar_wait(bar_load, par_load, 1u << 16);
         mbar_wait(bar_a, par_a, 1u << 16);
         mbar_wait(bar_b, par_b, 1u << 16);
+        mbar_wait(bar_w, par_w, 1u << 16);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, TCOLS);
 }
 
 // ------------------------------------------------------------------ state chain (tcgen05)
