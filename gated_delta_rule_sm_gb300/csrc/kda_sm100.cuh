@@ -119,6 +119,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, uint3
     return false;
 }
 
+// ---------------------------------------------------------------- named barriers
+
+// Named barrier over the first `nthreads` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA / bulk copies
 
 // 3-D tiled TMA load into shared memory, completing `bytes` on mbar.

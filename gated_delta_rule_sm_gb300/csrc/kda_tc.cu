@@ -593,8 +593,9 @@ constexpr uint32_t SLOT_GC = SLOT_KD + (tcrec::GC - tcrec::KD);
 constexpr uint32_t SLOT_BYTES = (SLOT_KD + tcrec::TAIL + 1023) / 1024 * 1024;
 constexpr uint32_t SB = 2 * SLOT_BYTES;   // S as bf16 B operand (N = j, K = c), MN-major: mn_bf16(j, c, 128, 512)
 constexpr uint32_t UB = SB + 8192;        // U as tf32 B operand (N = j, K = t), K-major, padded: km_f32(j, t, 2304, 144)
-constexpr uint32_t UB_LBO = 144, UB_SBO = 2304;
-constexpr uint32_t BAR = UB + 4 * UB_SBO; // mbarriers: full[2], ws, s, o; failure flag
+constexpr uint32_t UB_LBO = 144, UB_SBO = 2304;   // two buffers (chunk parity), UB_BYTES apart
+constexpr uint32_t UB_BYTES = 4 * UB_SBO;
+constexpr uint32_t BAR = UB + 2 * UB_BYTES; // mbarriers: full[2], empty[2], ws, s, o, u
 constexpr uint32_t TSLOT = BAR + 64;
 constexpr uint32_t BYTES = TSLOT + 64;
 }  // namespace chainlay
@@ -602,104 +603,166 @@ constexpr uint32_t BYTES = TSLOT + 64;
 constexpr uint32_t kIdescWS = idesc_bf16(128, 32, 1, 1);   // [W; Qg] and S both MN-major
 constexpr uint32_t kIdescTF32 = idesc_tf32(128, 32);
 
-// Issue the bulk loads of chunk record `c` (head h, slice z) into slot smem.
-__device__ __forceinline__ void chain_load(uint8_t* slot, const uint8_t* rec, int z, uint64_t* bar) {
-    mbar_expect_tx(bar, 32768 + tcrec::U0_SLICE + tcrec::TAIL);
-    bulk_g2s(slot + chainlay::SLOT_WQ, rec + tcrec::WQ, 32768, bar);
-    bulk_g2s(slot + chainlay::SLOT_U0, rec + tcrec::U0 + z * tcrec::U0_SLICE, tcrec::U0_SLICE, bar);
-    bulk_g2s(slot + chainlay::SLOT_KD, rec + tcrec::KD, tcrec::TAIL, bar);
-}
-
-// One CTA per (segment, head, 32-column slice of V); 128 threads.  Thread c keeps row c of the
-// state slice (32 fp32) in registers.  Per chunk the critical path is
-//   MMA1 (W S) -> U = U0 - W S -> MMA2b (Kd^T U) -> S <- Diag(gC) S + Kd^T U -> next MMA1;
-// the output product (Qg S + Aqk U) goes to a double-buffered TMEM accumulator and is written out by
-// warps 2-3 while the next chunk's MMA1 runs.
-__global__ void __launch_bounds__(128, 1) chain_fwd_tc_kernel(Params p, const uint8_t* recs, int store_states) {
+// One CTA per (segment, head, 32-column slice of V): four compute warps, an MMA warp and a load warp.
+// Compute thread c keeps row c of the state slice (32 fp32) in registers.  Per chunk the critical path
+// is
+//   MMA1 (W S) -> U = U0 - W S -> MMA2b (Kd^T U) -> S <- Diag(gC) S + Kd^T U -> next MMA1.
+// MMA1 and MMA2b are split over K into four partial accumulators, one per compute warp (lane 0
+// issues), and the epilogues add the partials.  The output is Qg S (rows 64..127 of the MMA1 partials)
+// plus Aqk U, which the MMA warp issues into its own accumulator as soon as U is staged, off the
+// critical path.  Records stream through two slots; the load warp refills a slot with the chunk two
+// ahead once every reader of its chunk is done (an `empty` mbarrier per slot).
+__global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const uint8_t* recs, int store_states) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int n = blockIdx.x, h = blockIdx.y, z = blockIdx.z, j0 = z * 32;
     const int H = p.H, K = 128, V = 128;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + chainlay::BAR);   // [2] record slots
-    uint64_t* bar_ws = full + 2;    // MMA1
-    uint64_t* bar_s = full + 3;     // MMA2b (state update)
-    uint64_t* bar_o = full + 4;     // MMA2a (output)
-    int* sh_fail = reinterpret_cast<int*>(full + 5);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + chainlay::BAR);   // [2] record slots landed
+    uint64_t* empty = full + 2;     // [2] record slots released
+    uint64_t* bar_ws = full + 4;    // MMA1 (4 issuers)
+    uint64_t* bar_s = full + 5;     // MMA2b, state update (4 issuers)
+    uint64_t* bar_o = full + 6;     // MMA2a, output (MMA warp)
+    uint64_t* bar_u = full + 7;     // U of this chunk is in shared memory
+    volatile int* sh_fail = reinterpret_cast<volatile int*>(smem + chainlay::TSLOT + 4);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + chainlay::TSLOT);
     uint8_t* SB = smem + chainlay::SB;
-    uint8_t* UB = smem + chainlay::UB;
     const int cb = p.chunk_off[n], ce = p.chunk_off[n + 1];
     const int tb = seg_begin(p, n), te = seg_end(p, n);
     const int nch = ce - cb;
+    constexpr uint32_t TCOLS = 512;
 
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) mbar_init(&full[i], 1);
+        for (int b = 0; b < 4; ++b) mbar_init(&full[b], 1);   // full[2], empty[2]
+        mbar_init(bar_ws, 4);
+        mbar_init(bar_s, 4);
+        mbar_init(bar_o, 1);
+        mbar_init(bar_u, 1);
         *sh_fail = 0;
         mbar_fence_init();
     }
-    if (warp == 0) tmem_alloc(tslot, 128);
+    if (warp == 0) tmem_alloc(tslot, TCOLS);
+    auto slot_ptr = [&](int i) { return smem + (i & 1) * chainlay::SLOT_BYTES; };
+    auto rec_ptr = [&](int i) { return recs + ((size_t)(cb + i) * H + h) * tcrec::BYTES; };
+    auto ub_addr = [&](int i) { return smem_u32(smem + chainlay::UB + (i & 1) * chainlay::UB_BYTES); };
+    auto fail_wait = [&](uint64_t* bar, uint32_t parity) {
+        if (!mbar_wait(bar, parity)) atomicExch((int*)sh_fail, 1);
+    };
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    // D1[b] partial w at tmem + 128 b + 32 w; D3 partial w at tmem + 256 + 32 w; Aqk U of D1[b] at 384 + 32 b
+    const uint32_t tD3 = tmem + 256, tDO = tmem + 384;
+
+    bool ok = true;
+    if (warp == 5) {
+        // load warp: chunk k into slot k & 1 once chunk k - 2 has released it
+        if (lane == 0) {
+            for (int k = 0; k < nch; ++k) {
+                const int sl = k & 1;
+                if (k >= 2) {
+                    bool got = false;
+                    for (int tries = 0; tries < 64 && !got && *sh_fail == 0; ++tries)
+                        got = mbar_wait(&empty[sl], ((k >> 1) - 1) & 1, 1u << 16);
+                    if (!got) { atomicExch((int*)sh_fail, 1); break; }
+                }
+                uint8_t* slot = slot_ptr(k);
+                const uint8_t* rec = rec_ptr(k);
+                mbar_expect_tx(&full[sl], 32768 + tcrec::U0_SLICE + tcrec::TAIL);
+                bulk_g2s(slot + chainlay::SLOT_WQ, rec + tcrec::WQ, 32768, &full[sl]);
+                bulk_g2s(slot + chainlay::SLOT_U0, rec + tcrec::U0 + z * tcrec::U0_SLICE, tcrec::U0_SLICE, &full[sl]);
+                bulk_g2s(slot + chainlay::SLOT_KD, rec + tcrec::KD, tcrec::TAIL, &full[sl]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 4) {
+        // MMA warp: Aqk U of chunk i once its U is staged (rows 0..63 of this accumulator are unused)
+        if (lane == 0) {
+            for (int i = 0; i < nch; ++i) {
+                bool got = false;
+                for (int tries = 0; tries < 64 && !got && *sh_fail == 0; ++tries) got = mbar_wait(bar_u, i & 1, 1u << 16);
+                if (!got) { atomicExch((int*)sh_fail, 1); break; }
+                tc_fence_after();
+                const uint32_t ub = ub_addr(i);
+                const uint32_t aq = smem_u32(slot_ptr(i) + chainlay::SLOT_AQ) - 16384;
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_tf32(tDO + 32 * (i & 1), smem_desc(aq + kk * 256, 128, 2048),
+                             smem_desc(ub + kk * 2 * chainlay::UB_LBO, chainlay::UB_LBO, chainlay::UB_SBO), kIdescTF32,
+                             kk > 0);
+                mma_commit(bar_o);
+            }
+        }
+        __syncwarp();
+    } else {
     float S[32];
     {
         const float* src = p.S0 ? p.S0 + (((size_t)n * H + h) * K + tid) * V + j0 : nullptr;
 #pragma unroll
         for (int j = 0; j < 32; ++j) S[j] = src ? src[j] : 0.f;
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tslot;
-    const uint32_t tD3 = tmem + 64;                       // D1[b] = tmem + 32 b
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    auto slot_ptr = [&](int i) { return smem + (i & 1) * chainlay::SLOT_BYTES; };
-    auto rec_ptr = [&](int i) { return recs + ((size_t)(cb + i) * H + h) * tcrec::BYTES; };
-    auto fail_wait = [&](uint64_t* bar, uint32_t parity) {
-        if (!mbar_wait(bar, parity)) atomicExch(sh_fail, 1);
+    const bool issuer = lane == 0;
+    auto sync128 = [&]() {
+        tc_fence_before();
+        named_sync(1, 128);
+        tc_fence_after();
     };
+    // sum of the four partials 32 columns apart from base, this warp's lane quarter (one wait for all loads)
+    auto ld_sum4 = [&](uint32_t base, float* d) {
+        float e[3][32];
+        tmem_ld16(base + lane_base, d);
+        tmem_ld16(base + lane_base + 16, d + 16);
+#pragma unroll
+        for (int w = 0; w < 3; ++w) {
+            tmem_ld16(base + 32 * (w + 1) + lane_base, e[w]);
+            tmem_ld16(base + 32 * (w + 1) + lane_base + 16, e[w] + 16);
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) d[j] += (e[0][j] + e[1][j]) + e[2][j];
+    };
+    // MMA1 partial `warp`: K rows 32 warp .. 32 warp + 31 of [W; Qg] S
     auto issue_mma1 = [&](int i) {
+        fail_wait(&full[i & 1], (i >> 1) & 1);
+        tc_fence_after();
         const uint32_t wq = smem_u32(slot_ptr(i) + chainlay::SLOT_WQ), sb = smem_u32(SB);
-        for (int kk = 0; kk < 8; ++kk)
-            mma_bf16(tmem + 32 * (i & 1), smem_desc(wq + kk * 4096, 2048, 128), smem_desc(sb + kk * 1024, 512, 128),
-                     kIdescWS, kk > 0);
+        for (int q = 0; q < 2; ++q) {
+            const int kk = 2 * warp + q;
+            mma_bf16(tmem + 128 * (i & 1) + 32 * warp, smem_desc(wq + kk * 4096, 2048, 128),
+                     smem_desc(sb + kk * 1024, 512, 128), kIdescWS, q > 0);
+        }
         mma_commit(bar_ws);
     };
 #pragma unroll
     for (int jg = 0; jg < 4; ++jg) *reinterpret_cast<uint4*>(SB + mn_bf16(8 * jg, tid, 128, 512)) = pack8_bf16(S + 8 * jg);
     fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0 && nch > 0) {
-        for (int i = 0; i < 2 && i < nch; ++i) chain_load(slot_ptr(i), rec_ptr(i), z, &full[i]);
-        fail_wait(&full[0], 0);
-        tc_fence_after();
-        issue_mma1(0);
-    }
+    sync128();
+    if (issuer && nch > 0) issue_mma1(0);
 
-    bool ok = true;
     for (int i = 0; i < nch; ++i) {
         const int c = cb + i;
         uint8_t* sl = slot_ptr(i);
         const uint32_t par = i & 1;
+        const uint32_t tD1 = tmem + 128 * (i & 1);
         if (store_states) {
             float* dst = p.states + (((size_t)c * H + h) * K + tid) * V + j0;
 #pragma unroll
             for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
         }
         fail_wait(&full[i & 1], (i >> 1) & 1);   // record visible to this thread
-        fail_wait(bar_ws, par);
-        tc_fence_after();
         if (warp < 2) {
             // U[t][j] = U0[t][j] - (W S)[t][j], t = tid; rounded to tf32 and transposed in lane quads
+            fail_wait(bar_ws, par);
+            tc_fence_after();
             float d[32];
-            tmem_ld16(tmem + 32 * (i & 1) + lane_base, d);
-            tmem_ld16(tmem + 32 * (i & 1) + lane_base + 16, d + 16);
-            tmem_ld_wait();
+            ld_sum4(tD1, d);
             const float* u0 = reinterpret_cast<const float*>(sl + chainlay::SLOT_U0);
             float u[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) u[j] = tf32_rn(u0[j * 64 + tid] - d[j]);
             const int r = tid & 3;
             const bool top = (r & 2) == 0, even = (r & 1) == 0;
+            uint8_t* UB = smem + chainlay::UB + (i & 1) * chainlay::UB_BYTES;
 #pragma unroll
             for (int b = 0; b < 8; ++b) {
                 float v0 = u[4 * b], v1 = u[4 * b + 1], v2 = u[4 * b + 2], v3 = u[4 * b + 3];
@@ -714,31 +777,25 @@ __global__ void __launch_bounds__(128, 1) chain_fwd_tc_kernel(Params p, const ui
             }
         }
         fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
+        sync128();
         if (*sh_fail) { ok = false; break; }
-        // MMA2b: D3 = Kd^T U (state update) first, then MMA2a: D1 += [. ; Aqk] U (output)
-        if (tid == 0) {
-            const uint32_t ub = smem_u32(UB), kd = smem_u32(sl + chainlay::SLOT_KD);
-            const uint32_t aq = smem_u32(sl + chainlay::SLOT_AQ) - 16384;
-            for (int kk = 0; kk < 8; ++kk)
-                mma_tf32(tD3, smem_desc(kd + kk * 256, 128, 2048),
-                         smem_desc(ub + kk * 2 * chainlay::UB_LBO, chainlay::UB_LBO, chainlay::UB_SBO), kIdescTF32, kk > 0);
+        if (tid == 0) mbar_arrive(bar_u);   // the MMA warp may read U now
+        // MMA2b: D3 partial w = Kd^T U over t in [16 w, 16 w + 16)
+        if (issuer) {
+            const uint32_t ub = ub_addr(i), kd = smem_u32(sl + chainlay::SLOT_KD);
+            for (int q = 0; q < 2; ++q) {
+                const int kk = 2 * warp + q;
+                mma_tf32(tD3 + 32 * warp, smem_desc(kd + kk * 256, 128, 2048),
+                         smem_desc(ub + kk * 2 * chainlay::UB_LBO, chainlay::UB_LBO, chainlay::UB_SBO), kIdescTF32, q > 0);
+            }
             mma_commit(bar_s);
-            for (int kk = 0; kk < 8; ++kk)
-                mma_tf32(tmem + 32 * (i & 1), smem_desc(aq + kk * 256, 128, 2048),
-                         smem_desc(ub + kk * 2 * chainlay::UB_LBO, chainlay::UB_LBO, chainlay::UB_SBO), kIdescTF32, 1);
-            mma_commit(bar_o);
         }
         fail_wait(bar_s, par);
         tc_fence_after();
         {
             const float gc = reinterpret_cast<const float*>(sl + chainlay::SLOT_GC)[tid];
             float d[32];
-            tmem_ld16(tD3 + lane_base, d);
-            tmem_ld16(tD3 + lane_base + 16, d + 16);
-            tmem_ld_wait();
+            ld_sum4(tD3, d);
 #pragma unroll
             for (int j = 0; j < 32; ++j) S[j] = gc * S[j] + d[j];
 #pragma unroll
@@ -746,57 +803,55 @@ __global__ void __launch_bounds__(128, 1) chain_fwd_tc_kernel(Params p, const ui
                 *reinterpret_cast<uint4*>(SB + mn_bf16(8 * jg, tid, 128, 512)) = pack8_bf16(S + 8 * jg);
         }
         fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
+        sync128();
         if (*sh_fail) { ok = false; break; }
-        if (tid == 0 && i + 1 < nch) {
-            fail_wait(&full[(i + 1) & 1], ((i + 1) >> 1) & 1);
-            tc_fence_after();
-            issue_mma1(i + 1);
-        }
+        if (issuer && i + 1 < nch) issue_mma1(i + 1);
         if (warp >= 2) {
-            // output of chunk i, overlapping the next chunk's MMA1
+            // output of chunk i: rows 64..127 of its MMA1 partials plus the Aqk U accumulator
             fail_wait(bar_o, par);
             tc_fence_after();
-            float d[32];
-            tmem_ld16(tmem + 32 * (i & 1) + lane_base, d);
-            tmem_ld16(tmem + 32 * (i & 1) + lane_base + 16, d + 16);
-            tmem_ld_wait();
+            if (tid == 64) mbar_arrive(&empty[i & 1]);   // every reader of this chunk's slot is done
+            float d[32], e[32];
+            tmem_ld16(tDO + 32 * (i & 1) + lane_base, e);
+            tmem_ld16(tDO + 32 * (i & 1) + lane_base + 16, e + 16);
+            ld_sum4(tD1, d);
             const int t = tid - 64;
             const int tok0 = tb + i * kChunk, len = min(kChunk, te - tok0);
             if (p.out && t < len) {
                 __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)(tok0 + t) * H + h) * V + j0;
                 float sd[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) sd[j] = p.scale * d[j];
+                for (int j = 0; j < 32; ++j) sd[j] = p.scale * (d[j] + e[j]);
 #pragma unroll
                 for (int j = 0; j < 32; j += 8) *reinterpret_cast<uint4*>(o + j) = pack8_bf16(sd + j);
             }
-            // the slot is free once this chunk's MMAs are done: prefetch chunk i + 2 into it
-            if (tid == 64 && i + 2 < nch) chain_load(sl, rec_ptr(i + 2), z, &full[i & 1]);
         }
     }
-    __syncthreads();
+    sync128();
     if (*sh_fail) ok = false;
-    if (!ok) {
-        // Record the timeout; give in-flight copies and MMAs a bounded chance to land before this CTA's
-        // shared and tensor memory are released.
-        if (tid == 0) {
-            record_error(p.status, KDA_ERR_TIMEOUT);
-            for (int b = 0; b < 5; ++b) {
-                mbar_wait(&full[b], 0, 1u << 12);
-                mbar_wait(&full[b], 1, 1u << 12);
-            }
-        }
-    } else if (p.ST) {
+    if (ok && p.ST) {
         float* dst = p.ST + (((size_t)n * H + h) * K + tid) * V + j0;
 #pragma unroll
         for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
+    }
+    __syncthreads();
+    if (*sh_fail && tid == 0) {
+        // Record the timeout; give in-flight copies and MMAs a bounded chance to land before this CTA's
+        // shared and tensor memory are released.
+        record_error(p.status, KDA_ERR_TIMEOUT);
+        for (int b = 0; b < 2; ++b) {
+            mbar_wait(&full[b], 0, 1u << 12);
+            mbar_wait(&full[b], 1, 1u << 12);
+        }
+        for (int b = 4; b < 7; ++b) {
+            mbar_wait(&full[b], 0, 1u << 12);
+            mbar_wait(&full[b], 1, 1u << 12);
+        }
+    }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem, TCOLS);
 }
 
 // ------------------------------------------------------------------ launchers
@@ -860,7 +915,7 @@ cudaError_t launch_chain_fwd_tc(const Params& p, const uint8_t* recs, bool store
                                          (int)chainlay::BYTES);
     if (e != cudaSuccess) return e;
     timing_pre(st, K_CHAIN_FWD_TC);
-    chain_fwd_tc_kernel<<<dim3(p.N, p.H, 4), 128, chainlay::BYTES, st>>>(p, recs, store_states ? 1 : 0);
+    chain_fwd_tc_kernel<<<dim3(p.N, p.H, 4), 192, chainlay::BYTES, st>>>(p, recs, store_states ? 1 : 0);
     timing_post(st);
     return cudaGetLastError();
 }
