@@ -72,15 +72,15 @@ def kernel_work(name: str, w, units: float) -> tuple[float, float]:
     return b * units, f * units
 
 
-# DRAM bytes (read + write) per token-head per launch, from ncu captures of the current kernels on
-# the B=1 T=4096 H=32 K=V=128 case (profiles/grad_tc_B1_T4096_H32_D128.md,
-# profiles/intra_tc_B1_T4096_H32_D128.md).  Per-chunk kernels move the same bytes per chunk-head at
+# DRAM bytes (read + write) per token-head per launch, from ncu captures of the current kernels
+# (profiles/grad_tc_B1_T4096_H32_D128.md, profiles/intra_tc_B1_T4096_H32_D128.md,
+# profiles/intra_tc_fwd_T8192_H32_D128.md).  Per-chunk kernels move the same bytes per chunk-head at
 # any size, so the figure scales with the token-heads of a launch.  An entry is removed when its
 # kernel changes and has not been captured again.
 PROFILED_TRAFFIC = {
-    ("kda_grad_tc", True): 9784.0,
-    ("kda_intra_tc", False): 2408.0,             # forward mode (forward-only workloads)
-    ("kda_intra_tc", True): (2408.0 + 5459.0) / 2,   # forward + backward mode, one launch each per step
+    ("kda_grad_tc", True): 9500.0,
+    ("kda_intra_tc", False): 2608.0,   # forward record only (forward-only workloads)
+    ("kda_intra_tc", True): 7267.0,    # forward that keeps the backward record, once per training step
 }
 
 
