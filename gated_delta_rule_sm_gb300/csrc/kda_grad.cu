@@ -32,28 +32,6 @@ struct Tile {
     __device__ __forceinline__ float at(int r, int c) const { return p[r * rs + c * cs]; }
 };
 
-__device__ __forceinline__ uint32_t tf32(float x) {
-    uint32_t y;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ void mma1688(float* d, const uint32_t* a, const uint32_t* b) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-// Split-precision variant: x = hi + lo with hi = tf32(x), lo = tf32(x - hi); the product keeps
-// hi*hi + hi*lo + lo*hi (relative error ~2^-21).  Used where the result enters sums that cancel
-// (the decayed bilinear forms feeding the log-decay gradient).
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-    hi = tf32(x);
-    lo = tf32(x - __uint_as_float(hi));
-}
-
 // d[b] (16 x 8 blocks at rows m0, cols n0 + 8 b, b < NB) += sum_k A(m, k) B(k, n): one A fragment per
 // k-step serves the whole strip; the k-loop stays rolled to keep the kernel's code small.
 template <int NB>
@@ -169,12 +147,6 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
         f[2 * i] = __uint_as_float(w[i] << 16);
         f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
-}
-
-__device__ __forceinline__ void frag_rc(int lane, int e, int m0, int n0, int& r, int& c) {
-    const int g = lane >> 2, q = lane & 3;
-    r = m0 + g + ((e & 2) ? 8 : 0);
-    c = n0 + 2 * q + (e & 1);
 }
 
 constexpr int P128 = 132, P64 = 68, P32 = 36;   // padded row strides (4 mod 32)

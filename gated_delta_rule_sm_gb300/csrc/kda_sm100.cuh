@@ -224,5 +224,37 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ---------------------------------------------------------------- warp-level tf32 MMA (mma.sync)
+
+// fp32 -> tf32 bit pattern, rounded to nearest (ties away).
+__device__ __forceinline__ uint32_t tf32(float x) {
+    uint32_t y;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
+    return y;
+}
+
+// d (16 x 8, fp32) += A (16 x 8, row-major fragment) B (8 x 8, column fragment), tf32 operands.
+__device__ __forceinline__ void mma1688(float* d, const uint32_t* a, const uint32_t* b) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Split precision: x = hi + lo with hi = tf32(x), lo = tf32(x - hi); the product keeps
+// hi*hi + hi*lo + lo*hi (relative error ~2^-21): about fp32 accuracy from tf32 MMAs.
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+    hi = tf32(x);
+    lo = tf32(x - __uint_as_float(hi));
+}
+
+// Accumulator fragment element e of the 16 x 8 block at (m0, n0): row r, column c.
+__device__ __forceinline__ void frag_rc(int lane, int e, int m0, int n0, int& r, int& c) {
+    const int g = lane >> 2, q = lane & 3;
+    r = m0 + g + ((e & 2) ? 8 : 0);
+    c = n0 + 2 * q + (e & 1);
+}
+
 }  // namespace sm100
 }  // namespace kda

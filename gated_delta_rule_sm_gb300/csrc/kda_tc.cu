@@ -55,7 +55,7 @@ constexpr uint32_t TB_HI = 131072, TB_LO = 139264;  // after the A MMAs (in the 
                                                      // for the next item's tiles
 constexpr uint32_t SL = LA_HI;               // after the A MMAs: fp32 [64][65] Diag(beta) Bkk
 constexpr uint32_t SN = LA_HI + 16640;       // fp32 [64][65] N = (I + L)^-1
-constexpr uint32_t SP = LA_HI + 34816;       // fp32 [3][16][17] scratch of the blocked solve
+constexpr uint32_t SP = LA_HI + 34816;       // fp32 [4][16][24] scratch blocks of the blocked solve
 constexpr uint32_t RB_HI = 131072, RB_LO = 147456;  // B operand (N = s, K = c) 64 x 128, mn_bf16(s, c, 128, 1024), hi / lo
 constexpr uint32_t KVB = 163840;             // A operand [Kg^T; V^T] 256 x 64 (K = s), km_bf16(r, s, 1024, 128)
 constexpr uint32_t KGLO = 196608;            // bf16 lo half of Kg^T (128 x 64), same layout
@@ -63,6 +63,30 @@ constexpr uint32_t SMALL = 212992;           // rq[64] rk[64] beta[64] dtb[128] 
 constexpr uint32_t BAR = SMALL + (64 * 3 + 128 + 1024) * 4;
 constexpr uint32_t BYTES = BAR + 64;
 }  // namespace intralay
+
+// acc (a 16 x 16 block as two 16 x 8 accumulator fragments) += A B for 16 x 16 blocks A, B at row
+// strides sa, sb: warp tf32 MMAs on hi / lo splits of both operands (hi*hi + hi*lo + lo*hi).
+__device__ __forceinline__ void mma16_split(float (&acc)[2][4], const float* a, int sa, const float* b, int sb,
+                                            int lane) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int k0 = 0; k0 < 16; k0 += 8) {
+        uint32_t ah[4], al[4];
+        split_tf32(a[g * sa + k0 + q], ah[0], al[0]);
+        split_tf32(a[(g + 8) * sa + k0 + q], ah[1], al[1]);
+        split_tf32(a[g * sa + k0 + q + 4], ah[2], al[2]);
+        split_tf32(a[(g + 8) * sa + k0 + q + 4], ah[3], al[3]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            uint32_t bh[2], bl[2];
+            split_tf32(b[(k0 + q) * sb + 8 * nt + g], bh[0], bl[0]);
+            split_tf32(b[(k0 + q + 4) * sb + 8 * nt + g], bh[1], bl[1]);
+            mma1688(acc[nt], al, bh);
+            mma1688(acc[nt], ah, bl);
+            mma1688(acc[nt], ah, bh);
+        }
+    }
+}
 
 // MODE 0 writes the chain record (tcrec) of the forward; MODE 1 writes the fp32 per-chunk record
 // (RecLayout) that the backward's operand, chain and gradient kernels read; MODE 2 writes both (a
@@ -179,27 +203,38 @@ __global__ void __launch_bounds__(256, 1)
         const float ea = __expf(p.a_log[h]);
         float kx[2][16], qx[2][16], y[2][16], fj[2][4];
         float lg[BWD ? 2 : 1][16];          // running sum of g inside the sub-block (backward record)
-#pragma unroll
-        for (int ci = 0; ci < 2; ++ci) {
-            const int cc = cp + 64 * ci;
-            const float dtb = sdtb[cc];
-            float a[16];
-            float gs = 0.f;
+        float av[2][16];                    // alpha = exp(g)
+        {
+            // loads and gates of both channels in one pass: independent chains for the scheduler
+            const float dtb[2] = {sdtb[cp], sdtb[cp + 64]};
+            float gs[2] = {0.f, 0.f};
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
                 const int t = t0 + u;
-                const uint32_t o = t * 256 + cc * 2;
-                kx[ci][u] = bf16_at(smem + RAW_K, o) * rk[t];
-                qx[ci][u] = bf16_at(smem + RAW_Q, o) * rq[t];
-                float g = 0.f;
-                if (t < len) g = p.lb * __fdividef(1.f, 1.f + __expf(-ea * (bf16_at(smem + RAW_G, o) + dtb)));
-                a[u] = __expf(g);
-                if (BWD) {
-                    gs += g;
-                    lg[BWD ? ci : 0][u] = gs;
+                const float rkt = rk[t], rqt = rq[t];
+#pragma unroll
+                for (int ci = 0; ci < 2; ++ci) {
+                    const uint32_t o = t * 256 + (cp + 64 * ci) * 2;
+                    kx[ci][u] = bf16_at(smem + RAW_K, o) * rkt;
+                    qx[ci][u] = bf16_at(smem + RAW_Q, o) * rqt;
+                    const float gv = p.lb * __fdividef(1.f, 1.f + __expf(-ea * (bf16_at(smem + RAW_G, o) + dtb[ci])));
+                    const float g = t < len ? gv : 0.f;
+                    av[ci][u] = __expf(g);
+                    if (BWD) {
+                        gs[ci] += g;
+                        lg[BWD ? ci : 0][u] = gs[ci];
+                    }
                 }
             }
-            if (BWD) sgsum[bi * 128 + cc] = gs;
+            if (BWD) {
+                sgsum[bi * 128 + cp] = gs[0];
+                sgsum[bi * 128 + cp + 64] = gs[1];
+            }
+        }
+#pragma unroll
+        for (int ci = 0; ci < 2; ++ci) {
+            const int cc = cp + 64 * ci;
+            const float* a = av[ci];
             float run = 1.f;
 #pragma unroll
             for (int u = 15; u >= 0; --u) {     // y_t = prod_{v > t} alpha_v  (= exp(G_{b+1} - Gamma_t))
@@ -453,24 +488,61 @@ __global__ void __launch_bounds__(256, 1)
             for (int r = 0; r < 16; ++r) SNf[(16 * b + r) * 65 + 16 * b + s2] = col[r];
         }
         __syncthreads();
-        for (int d = 1; d < 4; ++d) {
-            const int r = tid >> 4, s2 = tid & 15;
-            for (int b = 0; b + d < 4; ++b) {
-                const int i = b + d, j = b;
-                float acc = 0.f;
-                for (int m = j; m < i; ++m)
+        // Off-diagonal blocks by two levels of the block lower-triangular inverse, as warp tf32 MMAs on
+        // hi / lo split operands (about fp32 accuracy):
+        //   level 1: N_10 = -N_11 L_10 N_00 and N_32 = -N_33 L_32 N_22;
+        //   level 2: on the 32 x 32 halves, N_BL = -N_BR (L_BL N_TL).
+        {
+            auto blk = [&](float* base, int i, int j) { return base + (16 * i) * 65 + 16 * j; };
+            constexpr int XS = 24;   // scratch row stride: conflict-free as a B operand
+            float acc[2][4];
+            auto zero = [&]() {
 #pragma unroll
-                    for (int qq = 0; qq < 16; ++qq)
-                        acc += SLf[(16 * i + r) * 65 + 16 * m + qq] * SNf[(16 * m + qq) * 65 + 16 * j + s2];
-                SPf[(b * 16 + r) * 17 + s2] = acc;
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+            };
+            auto put = [&](float* d, int sd, float sgn) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        int r, cc;
+                        frag_rc(lane, e, 0, 8 * nt, r, cc);
+                        d[r * sd + cc] = sgn * acc[nt][e];
+                    }
+            };
+            if (warp < 2) {
+                const int i = warp == 0 ? 1 : 3;
+                float* X = SPf + warp * 16 * XS;
+                zero();
+                mma16_split(acc, blk(SLf, i, i - 1), 65, blk(SNf, i - 1, i - 1), 65, lane);
+                put(X, XS, 1.f);
+                __syncwarp();
+                zero();
+                mma16_split(acc, blk(SNf, i, i), 65, X, XS, lane);
+                put(blk(SNf, i, i - 1), 65, -1.f);
             }
             __syncthreads();
-            for (int b = 0; b + d < 4; ++b) {
-                const int i = b + d, j = b;
-                float acc = 0.f;
-#pragma unroll
-                for (int qq = 0; qq < 16; ++qq) acc += SNf[(16 * i + r) * 65 + 16 * i + qq] * SPf[(b * 16 + qq) * 17 + s2];
-                SNf[(16 * i + r) * 65 + 16 * j + s2] = -acc;
+            const int r = 2 + (warp >> 1), cb = warp & 1;   // warps 0..3: block (r, cb) of the bottom-left half
+            if (warp < 4) {
+                // P_{r,cb} = sum_m L_{r,m} (N_TL)_{m,cb}, kept in scratch block 2 (r - 2) + cb
+                zero();
+                if (cb == 0) {
+                    mma16_split(acc, blk(SLf, r, 0), 65, blk(SNf, 0, 0), 65, lane);
+                    mma16_split(acc, blk(SLf, r, 1), 65, blk(SNf, 1, 0), 65, lane);
+                } else {
+                    mma16_split(acc, blk(SLf, r, 1), 65, blk(SNf, 1, 1), 65, lane);
+                }
+                put(SPf + warp * 16 * XS, XS, 1.f);
+            }
+            __syncthreads();
+            if (warp < 4) {
+                // N_{r,cb} = -sum_{m=2}^{r} N_{r,m} P_{m,cb}
+                zero();
+                mma16_split(acc, blk(SNf, r, 2), 65, SPf + cb * 16 * XS, XS, lane);
+                if (r == 3) mma16_split(acc, blk(SNf, 3, 3), 65, SPf + (2 + cb) * 16 * XS, XS, lane);
+                put(blk(SNf, r, cb), 65, -1.f);
             }
             __syncthreads();
         }
