@@ -120,14 +120,16 @@ __global__ void __launch_bounds__(256, 1)
     const RecLayout RL = RecLayout::make(128, 128);
     // Each MMA barrier has at most one pending phase at any time, so parity waits are unambiguous.
     uint64_t* bar_load = reinterpret_cast<uint64_t*>(smem + BAR);
-    uint64_t* bar_a = bar_load + 1;   // A-matrix MMAs reading tile pair A (three issuing warps)
-    uint64_t* bar_b = bar_load + 2;   // A-matrix MMAs reading tile pair B (three issuing warps)
+    uint64_t* bar_a = bar_load + 1;   // A-matrix MMAs reading tile pair A (six issuing warps)
+    uint64_t* bar_b = bar_load + 2;   // A-matrix MMAs reading tile pair B (six issuing warps)
     uint64_t* bar_w = bar_load + 3;   // the final W / U0 MMAs (two issuing warps)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_load + 4);
-    // TMEM columns: A-matrix partial products p = 0, 1, 2 at 64 p + 16 j (sub-block j), W^T at 192,
-    // U0^T at 256.  One thread issues a tcgen05.mma every ~100 cycles, so the three split products
-    // of each sub-block and the two final products go out from different warps in parallel.
-    constexpr uint32_t T_W = 192, T_U0 = 256, TCOLS = 512;
+    // TMEM columns: A-matrix partial products p = 0..5 at 64 p + 16 j (sub-block j), W^T at 384, U0^T
+    // at 448.  One thread issues a tcgen05.mma every ~100 cycles, so each sub-block's three split
+    // products, each halved over K, go out from six warps in parallel, and the two final products
+    // from two.
+    constexpr int NPART = 6;
+    constexpr uint32_t T_W = 384, T_U0 = 448, TCOLS = 512;
     // the raw q, k, g, v tiles of one item (64 tokens x 128 channels each, out-of-range rows zero)
     auto load_raw = [&](int it) {
         int h2, c2, t02;
@@ -141,8 +143,8 @@ __global__ void __launch_bounds__(256, 1)
 
     if (tid == 0) {
         mbar_init(bar_load, 1);
-        mbar_init(bar_a, 3);
-        mbar_init(bar_b, 3);
+        mbar_init(bar_a, NPART);
+        mbar_init(bar_b, NPART);
         mbar_init(bar_w, 2);
         mbar_fence_init();
         load_raw(blockIdx.x);
@@ -154,14 +156,24 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t tmem = *tslot;
     uint32_t par_a = 0, par_b = 0, par_w = 0, par_load = 0;
     bool ok = true;
+    // dt_bias (thread < 128) and the beta logit (thread < 64) of an item, loaded into registers one
+    // item ahead so their latency hides behind the current item
+    float nx_dtb = 0.f, nx_braw = 0.f;
+    auto fetch_small = [&](int it) {
+        int h2, c2, t02;
+        const int len2 = item_tok0(it, h2, c2, t02);
+        if (tid < 128) nx_dtb = p.dt_bias[h2 * 128 + tid];
+        if (tid < 64 && tid < len2) nx_braw = load_act(p.beta_raw, (size_t)(t02 + tid) * H + h2, KDA_BF16);
+    };
+    fetch_small(blockIdx.x);
     // Persistent over items: each item's raw tiles were requested by the previous item (or above).
     for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
     int h, c, tok0;
     const int len = item_tok0(item, h, c, tok0);
     float* frec = BWD ? p.rec + ((size_t)c * H + h) * p.rec_stride : nullptr;
     uint8_t* rec = FWDREC ? recs + ((size_t)c * H + h) * tcrec::BYTES : nullptr;
-    if (tid < 128) sdtb[tid] = p.dt_bias[h * 128 + tid];
-    if (tid < 64) sbeta[tid] = tid < len ? sigmoidf_acc(load_act(p.beta_raw, (size_t)(tok0 + tid) * H + h, KDA_BF16)) : 0.f;
+    if (tid < 128) sdtb[tid] = nx_dtb;
+    if (tid < 64) sbeta[tid] = tid < len ? sigmoidf_acc(nx_braw) : 0.f;
     ok = __syncthreads_and(mbar_wait(bar_load, par_load) ? 1 : 0) != 0;
     par_load ^= 1;
     if (!ok) goto fail;
@@ -361,17 +373,19 @@ __global__ void __launch_bounds__(256, 1)
                 }
             }
         };
-        // A-matrix MMAs of column sub-block j: D_j = L_hi R_hi + L_hi R_lo + L_lo R_hi, one partial
-        // product per issuing warp (warps 0, 1, 2), summed when the accumulators are read
+        // A-matrix MMAs of column sub-block j: D_j = L_hi R_hi + L_hi R_lo + L_lo R_hi.  Issuing warp
+        // w < 6 takes product w / 2 over channel half w % 2 into partial accumulator w; the partials
+        // are summed when the accumulators are read.
         constexpr uint32_t idA = idesc_bf16(128, 16, 1, 1);
         auto issue_A = [&](int j, uint32_t hi_off, uint32_t lo_off, uint64_t* bar) {
-            if (lane != 0 || warp > 2) return;
+            if (lane != 0 || warp >= NPART) return;
+            const int pr = warp >> 1, k0 = 4 * (warp & 1);
             const uint32_t lh = smem_u32(smem + hi_off), ll = smem_u32(smem + lo_off);
             const uint32_t rh = smem_u32(smem + RB_HI) + j * 256, rl = smem_u32(smem + RB_LO) + j * 256;
-            const uint32_t la = warp == 2 ? ll : lh, rb = warp == 1 ? rl : rh;
-            for (int kk = 0; kk < 8; ++kk)
+            const uint32_t la = pr == 2 ? ll : lh, rb = pr == 1 ? rl : rh;
+            for (int kk = k0; kk < k0 + 4; ++kk)
                 mma_bf16(tmem + 64 * warp + 16 * j, smem_desc(la + kk * 4096, 2048, 128),
-                         smem_desc(rb + kk * 2048, 1024, 128), idA, kk > 0);
+                         smem_desc(rb + kk * 2048, 1024, 128), idA, kk > k0);
             mma_commit(bar);
         };
         auto wait_on = [&](uint64_t* bar, uint32_t& par) -> bool {
@@ -411,9 +425,12 @@ __global__ void __launch_bounds__(256, 1)
         if (!wait_on(bar_b, par_b)) goto fail;
         tc_fence_after();
         // the raw / pair-B area is free for the rest of this item: fetch the next item's tiles now
-        if (tid == 0 && item + (int)gridDim.x < nitems) {
-            fence_async_smem();
-            load_raw(item + gridDim.x);
+        if (item + (int)gridDim.x < nitems) {
+            if (tid == 0) {
+                fence_async_smem();
+                load_raw(item + gridDim.x);
+            }
+            fetch_small(item + gridDim.x);
         }
     }
 
@@ -422,51 +439,56 @@ __global__ void __launch_bounds__(256, 1)
         float* SLf = reinterpret_cast<float*>(smem + SL);
         float* SNf = reinterpret_cast<float*>(smem + SN);
         float* SPf = reinterpret_cast<float*>(smem + SP);
-        if (warp < 4) {
-            float d[64];
-            const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+        {
+            // warp w reads lane quarter w % 4 (rows) and columns 32 (w / 4) .. + 32 of the six partials
+            const int qw = warp & 3, c0 = 32 * (warp >> 2);
+            const uint32_t lb = (static_cast<uint32_t>(qw * 32) << 16) + c0;
+            float d[32], e1[32], e2[32];
             tmem_ld16(tmem + lb, d);
             tmem_ld16(tmem + lb + 16, d + 16);
-            tmem_ld16(tmem + lb + 32, d + 32);
-            tmem_ld16(tmem + lb + 48, d + 48);
+            tmem_ld16(tmem + lb + 64, e1);
+            tmem_ld16(tmem + lb + 64 + 16, e1 + 16);
             tmem_ld_wait();
 #pragma unroll
-            for (int pp = 1; pp < 3; ++pp) {   // add the other two partial products
-                float e[16];
+            for (int u = 0; u < 32; ++u) d[u] += e1[u];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    tmem_ld16(tmem + lb + 64 * pp + 16 * q4, e);
-                    tmem_ld_wait();
+            for (int pp = 2; pp < NPART; pp += 2) {
+                tmem_ld16(tmem + lb + 64 * pp, e1);
+                tmem_ld16(tmem + lb + 64 * pp + 16, e1 + 16);
+                tmem_ld16(tmem + lb + 64 * (pp + 1), e2);
+                tmem_ld16(tmem + lb + 64 * (pp + 1) + 16, e2 + 16);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) d[16 * q4 + u] += e[u];
-                }
+                for (int u = 0; u < 32; ++u) d[u] += e1[u] + e2[u];
             }
-            if (warp < 2) {
-                const int t = tid;
+            if (qw < 2) {
+                const int t = 32 * qw + lane;
                 const float bt = sbeta[t];
 #pragma unroll
-                for (int s2 = 0; s2 < 64; ++s2) SLf[t * 65 + s2] = s2 < t ? bt * d[s2] : 0.f;
+                for (int u = 0; u < 32; ++u) SLf[t * 65 + c0 + u] = c0 + u < t ? bt * d[u] : 0.f;
                 if (BWD) {
-                    frec[RL.beta + t] = bt;
-                    frec[RL.rn + t] = rq[t];
-                    frec[RL.rn + 64 + t] = rk[t];
+                    if (c0 == 0) {
+                        frec[RL.beta + t] = bt;
+                        frec[RL.rn + t] = rq[t];
+                        frec[RL.rn + 64 + t] = rk[t];
+                    }
 #pragma unroll
-                    for (int s2 = 0; s2 < 64; ++s2) frec[RL.B + t * 64 + s2] = s2 < t ? d[s2] : 0.f;
+                    for (int u = 0; u < 32; ++u) frec[RL.B + t * 64 + c0 + u] = c0 + u < t ? d[u] : 0.f;
                 }
             } else {
+                const int t = 32 * (qw - 2) + lane;
                 if (BWD) {
-                    const int t = tid - 64;
 #pragma unroll
-                    for (int s2 = 0; s2 < 64; ++s2) frec[RL.A + t * 64 + s2] = s2 <= t ? d[s2] : 0.f;
+                    for (int u = 0; u < 32; ++u) frec[RL.A + t * 64 + c0 + u] = c0 + u <= t ? d[u] : 0.f;
                 }
-                const int t = tid - 64;
 #pragma unroll
-                for (int s4 = 0; s4 < (FWDREC ? 64 : 0); s4 += 4) {
+                for (int u = 0; u < (FWDREC ? 32 : 0); u += 4) {
+                    const int s4 = c0 + u;
                     float4 v4;
-                    v4.x = tf32_rn(s4 <= t ? d[s4] : 0.f);
-                    v4.y = tf32_rn(s4 + 1 <= t ? d[s4 + 1] : 0.f);
-                    v4.z = tf32_rn(s4 + 2 <= t ? d[s4 + 2] : 0.f);
-                    v4.w = tf32_rn(s4 + 3 <= t ? d[s4 + 3] : 0.f);
+                    v4.x = tf32_rn(s4 <= t ? d[u] : 0.f);
+                    v4.y = tf32_rn(s4 + 1 <= t ? d[u + 1] : 0.f);
+                    v4.z = tf32_rn(s4 + 2 <= t ? d[u + 2] : 0.f);
+                    v4.w = tf32_rn(s4 + 3 <= t ? d[u + 3] : 0.f);
                     *reinterpret_cast<float4*>(rec + tcrec::AQ + km_f32(t, s4, 2048, 128)) = v4;
                 }
             }
