@@ -237,6 +237,14 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
                      : "memory");
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(dUg)), "r"(64u * V * 4u)
                      : "memory");
+        // the record fields phase 2 reads row by row from global memory: Qg and Kd (adjacent), Kg,
+        // and Gamma, q_hat, k_hat (adjacent), requested now so they sit in L2 by then
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(rec + L.Qg)),
+                     "r"(2u * 64u * K * 4u) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(rec + L.Kg)),
+                     "r"(64u * K * 4u) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(rec + L.G)),
+                     "r"(3u * 64u * K * 4u) : "memory");
     }
     if (tid >= 64 && tid < 64 + len) {   // one 256-byte row of dout and of v per token
         const size_t row = ((size_t)(tok0 + tid - 64) * H + h) * V;
@@ -667,30 +675,39 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     float* sdq = dQg;     // in place: the owning thread reads then overwrites
     float* sdk = dKg;
     float* sdG = dKdm;
+    // the record rows of block b + 1 are fetched while block b is combined (global loads: L2 latency)
+    float2 G[2][2], Q[2][2], Kk[2][2], QG[2][2], KG[2][2], KD[2][2];
+    auto fetch = [&](int b, int buf) {
+        int r0, c0;
+        frag_rc(lane, 0, wm0, 64 * (warp & 1) + 8 * b, r0, c0);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int gi = (r0 + 8 * hh) * K + c0;
+            G[buf][hh] = *reinterpret_cast<const float2*>(Gm + gi);
+            Q[buf][hh] = *reinterpret_cast<const float2*>(qh + gi);
+            Kk[buf][hh] = *reinterpret_cast<const float2*>(kh + gi);
+            QG[buf][hh] = *reinterpret_cast<const float2*>(rec + L.Qg + gi);
+            KG[buf][hh] = *reinterpret_cast<const float2*>(rec + L.Kg + gi);
+            KD[buf][hh] = *reinterpret_cast<const float2*>(rec + L.Kd + gi);
+        }
+    };
+    fetch(0, 0);
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
+        const int cur = b & 1;
+        if (b + 1 < 8) fetch(b + 1, cur ^ 1);
         const int n0 = 64 * (warp & 1) + 8 * b;
         int r0, c0;
         frag_rc(lane, 0, wm0, n0, r0, c0);   // elements (r0, c0 + e), (r0 + 8, c0 + e), e = 0, 1
         const float2 Gc = *reinterpret_cast<const float2*>(Gm + 63 * K + c0);
-        float2 G[2], Q[2], Kk[2], QG[2], KG[2], KD[2];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {   // every load of the block first
-            const int gi = (r0 + 8 * hh) * K + c0;
-            G[hh] = *reinterpret_cast<const float2*>(Gm + gi);
-            Q[hh] = *reinterpret_cast<const float2*>(qh + gi);
-            Kk[hh] = *reinterpret_cast<const float2*>(kh + gi);
-            QG[hh] = *reinterpret_cast<const float2*>(rec + L.Qg + gi);
-            KG[hh] = *reinterpret_cast<const float2*>(rec + L.Kg + gi);
-            KD[hh] = *reinterpret_cast<const float2*>(rec + L.Kd + gi);
-        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int hh = e >> 1, lo = e & 1;
             const int r = r0 + 8 * hh, cc = c0 + lo;
-            const float g = lo ? G[hh].y : G[hh].x, gc = lo ? Gc.y : Gc.x;
-            const float q = lo ? Q[hh].y : Q[hh].x, k = lo ? Kk[hh].y : Kk[hh].x;
-            const float qg = lo ? QG[hh].y : QG[hh].x, kg = lo ? KG[hh].y : KG[hh].x, kd = lo ? KD[hh].y : KD[hh].x;
+            const float g = lo ? G[cur][hh].y : G[cur][hh].x, gc = lo ? Gc.y : Gc.x;
+            const float q = lo ? Q[cur][hh].y : Q[cur][hh].x, k = lo ? Kk[cur][hh].y : Kk[cur][hh].x;
+            const float qg = lo ? QG[cur][hh].y : QG[cur][hh].x, kg = lo ? KG[cur][hh].y : KG[cur][hh].x;
+            const float kd = lo ? KD[cur][hh].y : KD[cur][hh].x;
             const float eG = __expf(g), eD = __expf(gc - g);
             const float vQg = dQg[r * P128 + cc], vKg = dKg[r * P128 + cc], vKd = dKdm[r * P128 + cc];
             const float dq = fq[b][e] + vQg * eG;
