@@ -61,7 +61,7 @@ def _load():
             lib.oracle_recurrence.restype = ctypes.c_int
             lib.oracle_recurrence.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                               _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_double, _dp, _dp]
-            common = [ctypes.c_int] * 6 + [_ip] + [_dp] * 7 + [ctypes.c_double, ctypes.c_double, _dp]
+            common = [ctypes.c_int] * 7 + [_ip] + [_dp] * 7 + [ctypes.c_double, ctypes.c_double, _dp]
             lib.oracle_kda_fwd.restype = ctypes.c_int
             lib.oracle_kda_fwd.argtypes = common + [_dp, _dp, ctypes.c_int]
             lib.oracle_kda_bwd.restype = ctypes.c_int
@@ -116,20 +116,23 @@ def recurrence(q_hat, k_hat, v, g, beta, scale, S0=None):
 
 def kda_fwd(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale, lower_bound,
             cu_seqlens=None, initial_state=None, output_final_state=True, nthreads=0):
-    """Full forward.  q, k, g_raw: [B, T, H, K]; v: [B, T, H, V]; beta_raw: [B, T, H].
+    """Full forward.  q, k: [B, T, Hk, K]; g_raw: [B, T, H, K]; v: [B, T, H, V]; beta_raw: [B, T, H].
 
-    With ``cu_seqlens`` (B must be 1) every segment is its own recurrence.
+    H counts value heads, Hk key heads (H a multiple of Hk; value head h reads key head
+    h // (H // Hk)).  With ``cu_seqlens`` (B must be 1) every segment is its own recurrence.
     Returns (out [B, T, H, V], final_state [N, H, K, V] or None).
     """
     q, k, v, g_raw, beta_raw, a_log, dt_bias, S0 = map(
         _f64, (q, k, v, g_raw, beta_raw, a_log, dt_bias, initial_state))
-    B, T, H, K = q.shape
-    V = v.shape[-1]
+    B, T, Hk, K = q.shape
+    H, V = v.shape[2], v.shape[-1]
+    if H % Hk:
+        raise ValueError("value heads must be a multiple of key heads")
     cu, cu_p = _cu(cu_seqlens)
     N = (len(cu) - 1) if cu is not None else B
     out = np.zeros((B, T, H, V))
     fs = np.zeros((N, H, K, V)) if output_final_state else None
-    rc = _load().oracle_kda_fwd(B, T, H, K, V, N, cu_p, _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
+    rc = _load().oracle_kda_fwd(B, T, H, Hk, K, V, N, cu_p, _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
                                 _ptr(beta_raw), _ptr(a_log), _ptr(dt_bias), float(scale),
                                 float(lower_bound), _ptr(S0), _ptr(out), _ptr(fs), int(nthreads))
     if rc:
@@ -142,18 +145,20 @@ def kda_bwd(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale, lower_boun
     """Reverse mode of :func:`kda_fwd`.
 
     Returns a dict with dq, dk, dv, dg_raw, dbeta_raw, da_log, ddt_bias,
-    dinitial_state (always computed, [N, H, K, V]).
+    dinitial_state (always computed, [N, H, K, V]).  dq, dk have the key heads' shape.
     """
     q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, S0, dST = map(
         _f64, (q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, initial_state, dfinal_state))
-    B, T, H, K = q.shape
-    V = v.shape[-1]
+    B, T, Hk, K = q.shape
+    H, V = v.shape[2], v.shape[-1]
+    if H % Hk:
+        raise ValueError("value heads must be a multiple of key heads")
     cu, cu_p = _cu(cu_seqlens)
     N = (len(cu) - 1) if cu is not None else B
     res = dict(dq=np.zeros_like(q), dk=np.zeros_like(k), dv=np.zeros_like(v),
                dg_raw=np.zeros_like(g_raw), dbeta_raw=np.zeros_like(beta_raw),
                da_log=np.zeros(H), ddt_bias=np.zeros(H * K), dinitial_state=np.zeros((N, H, K, V)))
-    rc = _load().oracle_kda_bwd(B, T, H, K, V, N, cu_p, _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
+    rc = _load().oracle_kda_bwd(B, T, H, Hk, K, V, N, cu_p, _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
                                 _ptr(beta_raw), _ptr(a_log), _ptr(dt_bias), float(scale),
                                 float(lower_bound), _ptr(S0), _ptr(dout), _ptr(dST),
                                 _ptr(res["dq"]), _ptr(res["dk"]), _ptr(res["dv"]),

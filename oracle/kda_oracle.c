@@ -35,8 +35,15 @@
  * every 64 tokens and recomputed inside each 64-token block.
  *
  * Layouts (token-first, as in `_validate_projected_inputs`):
- *   q, k, g_raw [TT, H, K]; v, out, dout [TT, H, V]; beta_raw [TT, H];
+ *   q, k [TT, Hk, K]; g_raw [TT, H, K]; v, out, dout [TT, H, V]; beta_raw [TT, H];
  *   a_log [H]; dt_bias [H*K]; states [N, H, K, V].   TT = B*T.
+ * H counts value heads and Hk key heads.  The same page's shape checks
+ * (`_validate_projected_inputs`) allow num_v_heads to be a multiple of
+ * num_k_heads, with the gate, beta, a_log and dt_bias per value head; which
+ * key head a value head reads is not printed.  Reading: value head h uses key
+ * head h / (H / Hk), i.e. the key heads repeated in consecutive groups (the
+ * usual grouped-head order).  dq and dk then sum over the value heads of a
+ * group.
  */
 #include <math.h>
 #include <stdint.h>
@@ -64,17 +71,20 @@ double oracle_gate_value(double g_raw, double a_log, double dt_bias, double lowe
     return lower_bound * sigm(z);
 }
 
-/* Prologue for one (segment, head): writes q_hat, k_hat [L,K], g [L,K], beta [L]
- * and the per-token inverse norms rq, rk [L]. */
-static void prologue(int64_t t0, int64_t L, int h, int H, int K,
+/* Prologue for one (segment, value head h): writes q_hat, k_hat [L,K], g [L,K],
+ * beta [L] and the per-token inverse norms rq, rk [L].  q and k come from key
+ * head h / (H / Hk). */
+static void prologue(int64_t t0, int64_t L, int h, int H, int Hk, int K,
                      const double* q, const double* k, const double* g_raw, const double* beta_raw,
                      const double* a_log, const double* dt_bias, double lb,
                      double* qh, double* kh, double* g, double* beta, double* rq, double* rk)
 {
+    const int hk = h / (H / Hk);
     for (int64_t i = 0; i < L; ++i) {
         const int64_t row = (t0 + i) * H + h;
-        const double* qi = q + row * K;
-        const double* ki = k + row * K;
+        const int64_t krow = (t0 + i) * Hk + hk;
+        const double* qi = q + krow * K;
+        const double* ki = k + krow * K;
         double sq = 0.0, sk = 0.0;
         for (int c = 0; c < K; ++c) { sq += qi[c] * qi[c]; sk += ki[c] * ki[c]; }
         rq[i] = 1.0 / sqrt(sq + ORACLE_EPS);
@@ -134,7 +144,7 @@ int oracle_recurrence(int64_t L, int K, int V, const double* qh, const double* k
 
 /* ---- forward ------------------------------------------------------------ */
 
-int oracle_kda_fwd(int B, int T, int H, int K, int V, int num_seqs, const int32_t* cu_seqlens,
+int oracle_kda_fwd(int B, int T, int H, int Hk, int K, int V, int num_seqs, const int32_t* cu_seqlens,
                    const double* q, const double* k, const double* v, const double* g_raw,
                    const double* beta_raw, const double* a_log, const double* dt_bias,
                    double scale, double lower_bound, const double* initial_state,
@@ -164,7 +174,7 @@ int oracle_kda_fwd(int B, int T, int H, int K, int V, int num_seqs, const int32_
         if (!qh || !kh || !g || !beta || !rq || !rk || !S || !w || !vv || !o) {
             err |= 1;
         } else {
-            prologue(t0, L, h, H, K, q, k, g_raw, beta_raw, a_log, dt_bias, lower_bound,
+            prologue(t0, L, h, H, Hk, K, q, k, g_raw, beta_raw, a_log, dt_bias, lower_bound,
                      qh, kh, g, beta, rq, rk);
             if (initial_state)
                 memcpy(S, initial_state + ((size_t)n * H + h) * K * V, sizeof(double) * (size_t)K * V);
@@ -184,7 +194,7 @@ int oracle_kda_fwd(int B, int T, int H, int K, int V, int num_seqs, const int32_
 
 /* ---- backward (reverse mode of the loop above) --------------------------- */
 
-int oracle_kda_bwd(int B, int T, int H, int K, int V, int num_seqs, const int32_t* cu_seqlens,
+int oracle_kda_bwd(int B, int T, int H, int Hk, int K, int V, int num_seqs, const int32_t* cu_seqlens,
                    const double* q, const double* k, const double* v, const double* g_raw,
                    const double* beta_raw, const double* a_log, const double* dt_bias,
                    double scale, double lower_bound, const double* initial_state,
@@ -194,12 +204,21 @@ int oracle_kda_bwd(int B, int T, int H, int K, int V, int num_seqs, const int32_
 {
     const int N = cu_seqlens ? num_seqs : B;
     const int pairs = N * H;
+    const int G = H / Hk;
     const size_t KV = (size_t)K * V;
+    const int64_t TT = cu_seqlens ? (int64_t)cu_seqlens[num_seqs] : (int64_t)B * T;
     /* per-pair partial sums of the parameter gradients, reduced in a fixed order */
     double* pa = (double*)calloc((size_t)pairs, sizeof(double));
     double* pd = (double*)calloc((size_t)pairs * K, sizeof(double));
+    /* with grouped heads, dq and dk per value head first ([TT, H, K]), summed over each group below */
+    double* dqv = G > 1 ? (double*)calloc((size_t)TT * H * K, sizeof(double)) : dq;
+    double* dkv = G > 1 ? (double*)calloc((size_t)TT * H * K, sizeof(double)) : dk;
     int err = 0;
-    if (!pa || !pd) { free(pa); free(pd); return 1; }
+    if (!pa || !pd || !dqv || !dkv) {
+        free(pa); free(pd);
+        if (G > 1) { free(dqv); free(dkv); }
+        return 1;
+    }
     (void)nthreads;
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
@@ -234,7 +253,7 @@ int oracle_kda_bwd(int B, int T, int H, int K, int V, int num_seqs, const int32_
             err |= 1;
             goto done;
         }
-        prologue(t0, L, h, H, K, q, k, g_raw, beta_raw, a_log, dt_bias, lower_bound,
+        prologue(t0, L, h, H, Hk, K, q, k, g_raw, beta_raw, a_log, dt_bias, lower_bound,
                  qh, kh, g, beta, rq, rk);
         if (initial_state) memcpy(S, initial_state + ((size_t)n * H + h) * KV, sizeof(double) * KV);
         /* forward sweep: remember the state entering every 64-token block */
@@ -331,8 +350,8 @@ int oracle_kda_bwd(int B, int T, int H, int K, int V, int num_seqs, const int32_
                 sk += kh[i * K + c] * dkh[i * K + c];
             }
             for (int c = 0; c < K; ++c) {
-                dq[row * K + c] = rq[i] * (dqh[i * K + c] - qh[i * K + c] * sq);
-                dk[row * K + c] = rk[i] * (dkh[i * K + c] - kh[i * K + c] * sk);
+                dqv[row * K + c] = rq[i] * (dqh[i * K + c] - qh[i * K + c] * sq);
+                dkv[row * K + c] = rk[i] * (dkh[i * K + c] - kh[i * K + c] * sk);
             }
             dbeta_raw[row] = dbeta[i] * beta[i] * (1.0 - beta[i]);
             const double ea = exp(a_log[h]);
@@ -357,6 +376,22 @@ int oracle_kda_bwd(int B, int T, int H, int K, int V, int num_seqs, const int32_
             for (int c = 0; c < K; ++c) ddt_bias[h * K + c] += pd[((size_t)n * H + h) * K + c];
         }
         da_log[h] = a;
+    }
+    if (G > 1) {
+        /* key head hk collects the value heads hk*G .. hk*G + G-1, in that order */
+        for (int64_t t = 0; t < TT; ++t)
+            for (int hk = 0; hk < Hk; ++hk)
+                for (int c = 0; c < K; ++c) {
+                    double sq = 0.0, sk = 0.0;
+                    for (int g2 = 0; g2 < G; ++g2) {
+                        const int64_t vr = (t * H + hk * G + g2) * K + c;
+                        sq += dqv[vr];
+                        sk += dkv[vr];
+                    }
+                    dq[(t * Hk + hk) * K + c] = sq;
+                    dk[(t * Hk + hk) * K + c] = sk;
+                }
+        free(dqv); free(dkv);
     }
     free(pa); free(pd);
     return err;

@@ -295,3 +295,66 @@ def test_backward_long_segment_crosses_checkpoints():
             fp = np.sum(oracle.kda_fwd(**dict(d, **{name: xp}), initial_state=S0, **kw)[0] * dout)
             fm = np.sum(oracle.kda_fwd(**dict(d, **{name: xm}), initial_state=S0, **kw)[0] * dout)
             assert abs((fp - fm) / (2 * h) - grads[gname][idx]) < 1e-6 * max(1.0, abs(grads[gname][idx]))
+
+
+# ------------------------------------------------------------------ grouped key heads
+
+def _grouped_inputs(B=1, T=9, H=4, Hk=2, K=3, V=2, seed=0):
+    """Value-head inputs of _full_inputs with q, k on Hk key heads."""
+    d, S0 = _full_inputs(B=B, T=T, H=H, K=K, V=V, seed=seed)
+    r = np.random.default_rng(seed + 100)
+    d["q"] = r.standard_normal((B, T, Hk, K))
+    d["k"] = r.standard_normal((B, T, Hk, K))
+    return d, S0
+
+
+def test_grouped_heads_equal_repeated_keys():
+    """H = 4 value heads on Hk = 2 key heads: value head h reads key head h // 2, so the run equals
+    the ungrouped run on q, k repeated per value head, and dq, dk are the group sums of that run's
+    dq, dk (the chain rule through the repeat)."""
+    d, S0 = _grouped_inputs(seed=21)
+    G = 2
+    rep = dict(d, q=np.repeat(d["q"], G, axis=2), k=np.repeat(d["k"], G, axis=2))
+    kw = dict(scale=0.7, lower_bound=-4.0)
+    out, fs = oracle.kda_fwd(**d, initial_state=S0, **kw)
+    out_r, fs_r = oracle.kda_fwd(**rep, initial_state=S0, **kw)
+    np.testing.assert_array_equal(out, out_r)
+    np.testing.assert_array_equal(fs, fs_r)
+    r = np.random.default_rng(22)
+    dout = r.standard_normal(d["v"].shape)
+    dfs = r.standard_normal(S0.shape)
+    g = oracle.kda_bwd(**d, dout=dout, initial_state=S0, dfinal_state=dfs, **kw)
+    g_r = oracle.kda_bwd(**rep, dout=dout, initial_state=S0, dfinal_state=dfs, **kw)
+    B, T, Hk, K = d["q"].shape
+    for n in ("dq", "dk"):
+        assert g[n].shape == (B, T, Hk, K)
+        np.testing.assert_allclose(g[n], g_r[n].reshape(B, T, Hk, G, K).sum(axis=3), rtol=1e-12, atol=1e-14)
+    for n in ("dv", "dg_raw", "dbeta_raw", "da_log", "ddt_bias", "dinitial_state"):
+        np.testing.assert_array_equal(g[n], g_r[n])
+
+
+def test_grouped_heads_backward_central_differences():
+    d, S0 = _grouped_inputs(B=1, T=6, H=4, Hk=2, K=3, V=2, seed=23)
+    r = np.random.default_rng(24)
+    dout = r.standard_normal(d["v"].shape)
+    kw = dict(scale=0.6, lower_bound=-4.0)
+    grads = oracle.kda_bwd(**d, dout=dout, initial_state=S0, **kw)
+    h = 1e-6
+    for name, gname in (("q", "dq"), ("k", "dk")):
+        x = d[name]
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            fp = np.sum(oracle.kda_fwd(**dict(d, **{name: xp}), initial_state=S0, **kw)[0] * dout)
+            fm = np.sum(oracle.kda_fwd(**dict(d, **{name: xm}), initial_state=S0, **kw)[0] * dout)
+            num[idx] = (fp - fm) / (2 * h)
+        err = np.abs(num - grads[gname]).max() / np.abs(num).max()
+        assert err < 1e-6, (name, err)
+
+
+def test_grouped_heads_reject_uneven_groups():
+    d, S0 = _grouped_inputs(H=3, Hk=2)
+    with pytest.raises(ValueError):
+        oracle.kda_fwd(**d, initial_state=S0, scale=0.5, lower_bound=-5.0)
