@@ -29,7 +29,7 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 
 class KdaDims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int), ("K", ctypes.c_int),
-                ("V", ctypes.c_int), ("dtype", ctypes.c_int), ("num_seqs", ctypes.c_int)]
+                ("V", ctypes.c_int), ("dtype", ctypes.c_int), ("num_seqs", ctypes.c_int), ("Hk", ctypes.c_int)]
 
 
 class KdaError(RuntimeError):
@@ -130,10 +130,24 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 
 def make_dims(q: torch.Tensor, v: torch.Tensor, cu_seqlens: Optional[torch.Tensor]) -> KdaDims:
-    B, T, H, K = q.shape
-    V = v.shape[-1]
+    """Shape of a call: q [B, T, Hk, K] (key heads), v [B, T, H, V] (value heads)."""
+    B, T, Hk, K = q.shape
+    H, V = v.shape[2], v.shape[-1]
     n = int(cu_seqlens.numel() - 1) if cu_seqlens is not None else 0
-    return KdaDims(B, T, H, K, V, _dtype_code(q), n)
+    return KdaDims(B, T, H, K, V, _dtype_code(q), n, Hk)
+
+
+def _check_shapes(q, k, v, g_raw, beta_raw, a_log, dt_bias):
+    B, T, Hk, K = q.shape
+    if k.shape != q.shape or v.dim() != 4 or tuple(v.shape[:2]) != (B, T):
+        raise ValueError("q, k must share [B, T, Hk, K] and v must be [B, T, H, V]")
+    H = v.shape[2]
+    if H % Hk:
+        raise ValueError(f"value heads ({H}) must be a multiple of key heads ({Hk})")
+    if tuple(g_raw.shape) != (B, T, H, K) or tuple(beta_raw.shape) != (B, T, H):
+        raise ValueError("g_raw must be [B, T, H, K] and beta_raw [B, T, H] (value heads)")
+    if a_log.numel() != H or dt_bias.numel() != H * K:
+        raise ValueError("a_log must hold H values and dt_bias H * K (value heads)")
 
 
 class _Workspace:
@@ -179,9 +193,10 @@ def forward(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale: float, lower_bou
     """
     lib = load()
     _contig(q, k, v, g_raw, beta_raw, a_log, dt_bias, cu_seqlens, initial_state)
+    _check_shapes(q, k, v, g_raw, beta_raw, a_log, dt_bias)
     dims = make_dims(q, v, cu_seqlens)
-    B, T, H, K = q.shape
-    V = v.shape[-1]
+    B, T, _, K = q.shape
+    H, V = v.shape[2], v.shape[-1]
     N = dims.num_seqs if cu_seqlens is not None else B
     if out is None:
         out = torch.empty((B, T, H, V), dtype=q.dtype, device=q.device)
@@ -226,14 +241,15 @@ def backward(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale: float, lo
     """
     lib = load()
     _contig(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, cu_seqlens, initial_state, dfinal_state)
+    _check_shapes(q, k, v, g_raw, beta_raw, a_log, dt_bias)
     dims = make_dims(q, v, cu_seqlens)
-    B, T, H, K = q.shape
-    V = v.shape[-1]
+    B, T, Hk, K = q.shape
+    H, V = v.shape[2], v.shape[-1]
     N = dims.num_seqs if cu_seqlens is not None else B
     dev = q.device
     f32 = dict(dtype=torch.float32, device=dev)
     if grads is None:
-        grads = dict(dq=torch.empty((B, T, H, K), **f32), dk=torch.empty((B, T, H, K), **f32),
+        grads = dict(dq=torch.empty((B, T, Hk, K), **f32), dk=torch.empty((B, T, Hk, K), **f32),
                      dv=torch.empty((B, T, H, V), **f32), dg_raw=torch.empty((B, T, H, K), **f32),
                      dbeta_raw=torch.empty((B, T, H), **f32), da_log=torch.empty((H,), **f32),
                      ddt_bias=torch.empty((H * K,), **f32),

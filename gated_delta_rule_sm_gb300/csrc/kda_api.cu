@@ -17,13 +17,15 @@ static constexpr int kGradCtas = 304;  // 2 CTAs per SM on a 152-SM GB300
 static size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Shape {
-    int B, T, H, K, V, N, TT, NCmax, dtype;
+    int B, T, H, Hk, G, K, V, N, TT, NCmax, dtype;
     bool varlen;
 };
 
 static kda_status check_dims(const kda_dims* d, int chunk_size, bool varlen, Shape* s) {
     if (!d) return KDA_ERR_INVALID_ARG;
     if (d->B < 1 || d->T < 1 || d->H < 1 || d->K < 1 || d->V < 1) return KDA_ERR_INVALID_ARG;
+    const int Hk = d->Hk > 0 ? d->Hk : d->H;   // 0: one key head per value head
+    if (d->Hk < 0 || d->H % Hk) return KDA_ERR_INVALID_ARG;
     if (d->dtype != KDA_BF16 && d->dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
     if (chunk_size <= 0) return KDA_ERR_INVALID_ARG;
     if (d->K < 16 || d->V < 16) return KDA_ERR_INVALID_ARG;           // head dims below 16 are rejected
@@ -36,6 +38,7 @@ static kda_status check_dims(const kda_dims* d, int chunk_size, bool varlen, Sha
         if (d->num_seqs > (1 << 24)) return KDA_ERR_UNSUPPORTED;
     }
     s->B = d->B; s->T = d->T; s->H = d->H; s->K = d->K; s->V = d->V;
+    s->Hk = Hk; s->G = d->H / Hk;
     s->dtype = d->dtype;
     s->varlen = varlen;
     s->N = varlen ? d->num_seqs : d->B;
@@ -46,6 +49,7 @@ static kda_status check_dims(const kda_dims* d, int chunk_size, bool varlen, Sha
 
 struct WsPlan {
     size_t off_chunk, off_rec, off_states, off_dstates, off_pdtb, off_palog, off_scratch, total;
+    size_t off_dqv, off_dkv;   // grouped key heads: dq, dk per value head before the group sum
     size_t rec_stride, scratch_stride;
 };
 
@@ -65,6 +69,10 @@ static WsPlan plan_simt(const Shape& s, bool bwd) {
         w.off_palog = o; o = align_up(o + sizeof(float) * (size_t)s.NCmax * s.H);
         w.scratch_stride = GradScratch::make(s.K, s.V).size;
         w.off_scratch = o; o = align_up(o + sizeof(float) * (size_t)kGradCtas * w.scratch_stride);
+        if (s.G > 1) {
+            w.off_dqv = o; o = align_up(o + sizeof(float) * (size_t)s.TT * s.H * s.K);
+            w.off_dkv = o; o = align_up(o + sizeof(float) * (size_t)s.TT * s.H * s.K);
+        }
     }
     w.total = o;
     return w;
@@ -117,6 +125,7 @@ static Params base_params(const Shape& s, const void* q, const void* k, const vo
     Params p;
     memset(&p, 0, sizeof(p));
     p.B = s.B; p.T = s.T; p.H = s.H; p.K = s.K; p.V = s.V; p.N = s.N; p.TT = s.TT;
+    p.Hk = s.Hk; p.G = s.G;
     p.dtype = s.dtype; p.NCmax = s.NCmax;
     p.q = q; p.k = k; p.v = v; p.g_raw = g_raw; p.beta_raw = beta_raw;
     p.a_log = a_log; p.dt_bias = dt_bias; p.scale = scale; p.lb = lb;
@@ -137,6 +146,8 @@ static void carve(Params& p, const WsPlan& w, void* ws) {
         p.scratch = reinterpret_cast<float*>(b + w.off_scratch);
         p.scratch_stride = w.scratch_stride;
         p.grad_ctas = kGradCtas;
+        p.dq_v = w.off_dqv ? reinterpret_cast<float*>(b + w.off_dqv) : p.dq;
+        p.dk_v = w.off_dkv ? reinterpret_cast<float*>(b + w.off_dkv) : p.dk;
     }
 }
 
@@ -215,7 +226,7 @@ static const char* kKernelNames[] = {"kda_plan",          "kda_intra_simt",   "k
                                      "kda_chain_bwd_simt", "kda_grad_simt",    "kda_param_reduce",
                                      "kda_empty_segment", "kda_intra_tc",     "kda_chain_fwd_tc",
                                      "kda_grad_tc",       "kda_bwd_pre",      "kda_chain_bwd_tc",
-                                     "kda_chain_rec_tc"};
+                                     "kda_chain_rec_tc",  "kda_group_sum"};
 
 // saved != NULL: also keep the fp32 backward record there (kda_fwd_save)
 static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cudaStream_t stream,

@@ -15,7 +15,8 @@ constexpr float kNormEps = 1e-6f;
 
 // Everything a kernel of either path needs, passed by value.
 struct Params {
-    int B, T, H, K, V, N;       // N = number of segments
+    int B, T, H, K, V, N;       // N = number of segments; H = value heads
+    int Hk, G;                  // key heads (q, k) and value heads per key head (H = G * Hk)
     int TT;                     // total tokens B*T
     int dtype;                  // KDA_BF16 / KDA_FP32
     int NCmax;                  // upper bound on the number of chunks
@@ -26,6 +27,8 @@ struct Params {
     void* out;
     float* ST;
     float *dq, *dk, *dv, *dg_raw, *dbeta_raw, *da_log, *ddt_bias, *dS0;
+    float *dq_v, *dk_v;         // dq, dk per value head [TT, H, K]: dq / dk when G == 1, else scratch
+                                // that the group sum folds into dq / dk [TT, Hk, K]
     // workspace views
     int32_t* chunk_off;         // [N+1] first chunk of each segment; chunk_off[N] = total chunks
     float* rec;                 // per (chunk, head) intra-chunk records (SIMT path)

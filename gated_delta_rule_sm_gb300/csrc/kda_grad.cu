@@ -767,8 +767,8 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int cc = lane + 32 * u;
-                p.dq[row * K + cc] = rq * (sdq[t * P128 + cc] - qv[w2][u] * sq[w2]);
-                p.dk[row * K + cc] = rk * (sdk[t * P128 + cc] - kv[w2][u] * sk[w2]);
+                p.dq_v[row * K + cc] = rq * (sdq[t * P128 + cc] - qv[w2][u] * sq[w2]);
+                p.dk_v[row * K + cc] = rk * (sdk[t * P128 + cc] - kv[w2][u] * sk[w2]);
             }
             if (lane == 0) {
                 const float b = sbeta[t];

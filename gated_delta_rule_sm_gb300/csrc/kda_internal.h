@@ -62,7 +62,7 @@ struct GradScratch {
 // Kernel ids for kda_kernel_name / kda_timing_end.
 enum KernelId {
     K_PLAN = 0, K_INTRA_SIMT, K_CHAIN_FWD_SIMT, K_CHAIN_BWD_SIMT, K_GRAD_SIMT, K_PARAM_REDUCE, K_EMPTY_SEG,
-    K_INTRA_TC, K_CHAIN_FWD_TC, K_GRAD_TC, K_BWD_PRE, K_CHAIN_BWD_TC, K_CHAIN_REC_TC, K_NUM_KERNELS
+    K_INTRA_TC, K_CHAIN_FWD_TC, K_GRAD_TC, K_BWD_PRE, K_CHAIN_BWD_TC, K_CHAIN_REC_TC, K_GROUP_SUM, K_NUM_KERNELS
 };
 
 // Record of the two tcgen05 state chains of the backward, per (chunk, head), K = V = 128 (bytes).
@@ -102,6 +102,7 @@ cudaError_t launch_chain_fwd_simt(const Params& p, bool store_states, cudaStream
 cudaError_t launch_chain_bwd_simt(const Params& p, cudaStream_t st);
 cudaError_t launch_grad_simt(const Params& p, cudaStream_t st);
 cudaError_t launch_param_reduce(const Params& p, cudaStream_t st);
+cudaError_t launch_group_sum(const Params& p, cudaStream_t st);   // dq_v, dk_v -> dq, dk when G > 1
 cudaError_t launch_grad_tc(const Params& p, cudaStream_t st);
 cudaError_t launch_bwd_pre(const Params& p, uint8_t* bw, cudaStream_t st);
 cudaError_t launch_chain_bwd_tc(const Params& p, const uint8_t* bw, cudaStream_t st);

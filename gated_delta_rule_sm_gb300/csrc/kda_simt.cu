@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(256) intra_simt_kernel(Params p) {
     }
     // L2 norms, one warp per token
     for (int t = warp; t < kChunk; t += 8) {
-        const size_t base = ((size_t)(ch.tok0 + t) * H + h) * K;
+        const size_t base = ((size_t)(ch.tok0 + t) * p.Hk + h / p.G) * K;   // key head of value head h
         float qv[4], kv[4], sq = 0.f, sk = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -458,9 +458,10 @@ __global__ void __launch_bounds__(256) grad_simt_kernel(Params p) {
         const float ea = expf(p.a_log[h]);
         for (int t = warp; t < ch.len; t += 8) {
             const size_t row = (size_t)(ch.tok0 + t) * H + h;
+            const size_t krow = (size_t)(ch.tok0 + t) * p.Hk + h / p.G;   // key head of value head h
             float sq = 0.f, sk = 0.f, nq = 0.f, nk = 0.f;
             for (int cc = lane; cc < K; cc += 32) {
-                const float qr = load_act(p.q, row * K + cc, p.dtype), kr = load_act(p.k, row * K + cc, p.dtype);
+                const float qr = load_act(p.q, krow * K + cc, p.dtype), kr = load_act(p.k, krow * K + cc, p.dtype);
                 nq += qr * qr;
                 nk += kr * kr;
                 sq += qh[t * K + cc] * dq[t * K + cc];
@@ -469,8 +470,8 @@ __global__ void __launch_bounds__(256) grad_simt_kernel(Params p) {
             sq = warp_sum(sq); sk = warp_sum(sk); nq = warp_sum(nq); nk = warp_sum(nk);
             const float rq = 1.0f / sqrtf(nq + kNormEps), rk = 1.0f / sqrtf(nk + kNormEps);
             for (int cc = lane; cc < K; cc += 32) {
-                p.dq[row * K + cc] = rq * (dq[t * K + cc] - qh[t * K + cc] * sq);
-                p.dk[row * K + cc] = rk * (dk[t * K + cc] - kh[t * K + cc] * sk);
+                p.dq_v[row * K + cc] = rq * (dq[t * K + cc] - qh[t * K + cc] * sq);
+                p.dk_v[row * K + cc] = rk * (dk[t * K + cc] - kh[t * K + cc] * sk);
             }
             if (lane == 0) p.dbeta_raw[row] = dbeta[t] * beta[t] * (1.f - beta[t]);
         }
@@ -609,6 +610,40 @@ cudaError_t launch_param_reduce(const Params& p, cudaStream_t st) {
     const int total = p.H * p.K + p.H;
     timing_pre(st, K_PARAM_REDUCE);
     param_reduce_kernel<<<(total + 255) / 256, 256, 0, st>>>(p);
+    timing_post(st);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || p.G == 1) return e;
+    return launch_group_sum(p, st);
+}
+
+// dq[t, hk, c] = sum over the G value heads hk G .. hk G + G-1 of dq_v[t, h, c] (same for dk), in that
+// order: every key head's gradient collects the value heads that read it.
+__global__ void group_sum_kernel(Params p) {
+    const size_t n = (size_t)p.TT * p.Hk * p.K;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int c = (int)(i % p.K);
+        const size_t tk = i / p.K;          // t * Hk + hk
+        const size_t t = tk / p.Hk;
+        const int hk = (int)(tk - t * p.Hk);
+        const size_t v0 = (t * p.H + (size_t)hk * p.G) * p.K + c;
+        float sq = 0.f, sk = 0.f;
+        for (int g = 0; g < p.G; ++g) {
+            sq += p.dq_v[v0 + (size_t)g * p.K];
+            sk += p.dk_v[v0 + (size_t)g * p.K];
+        }
+        p.dq[i] = sq;
+        p.dk[i] = sk;
+    }
+}
+
+cudaError_t launch_group_sum(const Params& p, cudaStream_t st) {
+    const size_t n = (size_t)p.TT * p.Hk * p.K;
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const size_t want = (n + 255) / 256, cap = (size_t)(sms > 0 ? sms : 1) * 8;
+    timing_pre(st, K_GROUP_SUM);
+    group_sum_kernel<<<(unsigned)(want < cap ? want : cap), 256, 0, st>>>(p);
     timing_post(st);
     return cudaGetLastError();
 }

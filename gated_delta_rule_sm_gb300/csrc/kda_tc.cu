@@ -135,8 +135,8 @@ __global__ void __launch_bounds__(256, 1)
         int h2, c2, t02;
         item_tok0(it, h2, c2, t02);
         mbar_expect_tx(bar_load, 4 * 16384);
-        tma_load_3d(smem + RAW_Q, &tm_q, 0, h2, t02, bar_load);
-        tma_load_3d(smem + RAW_K, &tm_k, 0, h2, t02, bar_load);
+        tma_load_3d(smem + RAW_Q, &tm_q, 0, h2 / p.G, t02, bar_load);   // q, k: key head of value head h2
+        tma_load_3d(smem + RAW_K, &tm_k, 0, h2 / p.G, t02, bar_load);
         tma_load_3d(smem + RAW_G, &tm_g, 0, h2, t02, bar_load);
         tma_load_3d(smem + RAW_V, &tm_v, 0, h2, t02, bar_load);
     };
@@ -986,7 +986,7 @@ bool tc_inputs_aligned(const Params& p) {
 
 cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, int mode, cudaStream_t st) {
     CUtensorMap mq, mk, mg, mv;
-    if (!head_tile_map(&mq, p.q, p.H, p.TT) || !head_tile_map(&mk, p.k, p.H, p.TT) ||
+    if (!head_tile_map(&mq, p.q, p.Hk, p.TT) || !head_tile_map(&mk, p.k, p.Hk, p.TT) ||
         !head_tile_map(&mg, p.g_raw, p.H, p.TT) || !head_tile_map(&mv, p.v, p.H, p.TT))
         return cudaErrorInvalidValue;
     auto kern = mode == 0 ? intra_tc_kernel<0> : mode == 1 ? intra_tc_kernel<1> : intra_tc_kernel<2>;

@@ -42,6 +42,7 @@ class Workload:
     lower_bound: float = -5.0
     g_mean: float = 0.0            # mean of g_raw (a "mild gate" variant shifts it negative)
     seed: int = 0
+    Hk: int = 0                    # key heads of q, k (0: Hk = H); H value heads, H a multiple of Hk
 
     @property
     def scale(self) -> float:
@@ -86,7 +87,7 @@ def make_inputs(w: Workload, device: str | torch.device = "cpu",
                 lengths: Optional[list[int]] = None) -> dict:
     """Draw one batch for workload ``w``.
 
-    Returns a dict of torch tensors on ``device``: q, k, g_raw [B, T, H, K];
+    Returns a dict of torch tensors on ``device``: q, k [B, T, Hk, K]; g_raw [B, T, H, K];
     v [B, T, H, V]; beta_raw [B, T, H]; a_log [H] fp32; dt_bias [H*K] fp32;
     cu_seqlens int32 [N+1] or None; initial_state fp32 [N, H, K, V] or None;
     dout [B, T, H, V] or None; plus the scalars scale, lower_bound, chunk_size.
@@ -94,6 +95,7 @@ def make_inputs(w: Workload, device: str | torch.device = "cpu",
     """
     rng = np.random.Generator(np.random.PCG64(w.seed))
     B, T, H, K, V = w.B, w.T, w.H, w.K, w.V
+    Hk = w.Hk or H
     cu = None
     if w.varlen:
         if lengths is None:
@@ -115,8 +117,8 @@ def make_inputs(w: Workload, device: str | torch.device = "cpu",
         return torch.from_numpy(x).to(dt).to(device)
 
     out = {}
-    out["q"] = act(normal((B, T, H, K)))
-    out["k"] = act(normal((B, T, H, K)))
+    out["q"] = act(normal((B, T, Hk, K)))
+    out["k"] = act(normal((B, T, Hk, K)))
     out["v"] = act(normal((B, T, H, V)))
     out["g_raw"] = act(normal((B, T, H, K), mean=w.g_mean))
     out["beta_raw"] = act(normal((B, T, H)))

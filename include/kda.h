@@ -18,14 +18,18 @@
  * printed on the pages and is this library's reading).
  *
  * Layouts follow `_validate_projected_inputs` on the same page (token-first,
- * contiguous, row-major):
- *     q, k, g_raw     [B, T, H, K]        dtype (bf16 or fp32)
+ * contiguous, row-major); H counts value heads and Hk key heads:
+ *     q, k            [B, T, Hk, K]       dtype (bf16 or fp32)
+ *     g_raw           [B, T, H, K]        dtype
  *     v, out, dout    [B, T, H, V]        dtype
  *     beta_raw        [B, T, H]           dtype
  *     a_log           [H]                 fp32
  *     dt_bias         [H * K]             fp32
  *     states          [N, H, K, V]        fp32  (initial, final and their gradients)
  *     gradients       same shape as their input, always fp32
+ * Grouped key heads (the same page's checks let num_v_heads be a multiple of
+ * num_k_heads): value head h reads key head h / (H / Hk); dq and dk sum over
+ * the value heads of each key head.  Hk = H is the ungrouped case.
  * Packed documents (nemo_automodel `kimi_k3.cp`, `segment_cu_seqlens`): with
  * cu_seqlens != NULL, B must be 1 and segment n is tokens
  * [cu_seqlens[n], cu_seqlens[n+1]) of the T tokens; each segment is its own
@@ -70,11 +74,14 @@ typedef enum {
 typedef enum { KDA_BF16 = 0, KDA_FP32 = 1 } kda_dtype;
 
 /* Problem shape.  num_seqs is the number of packed segments N when
- * cu_seqlens is given (then B == 1) and is ignored otherwise (N = B). */
+ * cu_seqlens is given (then B == 1) and is ignored otherwise (N = B).
+ * H = value heads; Hk = key heads (q, k), H a multiple of Hk, 0 meaning Hk = H;
+ * H % Hk != 0 or Hk < 0 is KDA_ERR_INVALID_ARG. */
 typedef struct {
     int B, T, H, K, V;
     kda_dtype dtype;
     int num_seqs;
+    int Hk;
 } kda_dims;
 
 /* Bytes of workspace kda_fwd / kda_bwd need for this shape (0 on invalid input). */

@@ -50,6 +50,7 @@ def tol(dtype):
 def head_slice(x: dict, heads) -> dict:
     """Restrict every per-head input to the listed heads (for sampled oracle runs)."""
     heads = list(heads)
+    assert x["q"].shape[2] == x["v"].shape[2], "head_slice takes ungrouped inputs (one key head per value head)"
     K = x["q"].shape[-1]
     out = dict(x)
     for n in ("q", "k", "v", "g_raw", "dout"):

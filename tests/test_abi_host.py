@@ -142,3 +142,15 @@ def test_saved_context_validation(lib):
     assert _fwd_save(lib, d128, saved=ctypes.c_void_p(4096 + 16), saved_bytes=need) == _lib.KDA_ERR_WORKSPACE
     assert _bwd_saved(lib, d128) == _lib.KDA_ERR_WORKSPACE
     assert _bwd_saved(lib, d128, saved=ctypes.c_void_p(4096), saved_bytes=need - 256) == _lib.KDA_ERR_WORKSPACE
+
+
+def test_grouped_key_heads_validation(lib):
+    """H value heads on Hk key heads: H must be a multiple of Hk; Hk = 0 means Hk = H."""
+    assert _fwd(lib, _dims(H=3, Hk=2)) == _lib.KDA_ERR_INVALID_ARG
+    assert _fwd(lib, _dims(H=4, Hk=-1)) == _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_fwd_workspace_size(ctypes.byref(_dims(H=3, Hk=2)), 64) == 0
+    f = lambda **kw: lib.kda_fwd_workspace_size(ctypes.byref(_dims(**kw)), 64)
+    b = lambda **kw: lib.kda_bwd_workspace_size(ctypes.byref(_dims(**kw)), 64)
+    assert f(H=4, Hk=2) == f(H=4) == f(H=4, Hk=4)           # the forward keeps nothing per key head
+    assert b(H=4, Hk=2) > b(H=4, Hk=4) == b(H=4)             # dq, dk per value head before the group sum
+    assert _fwd(lib, _dims(H=4, Hk=2), ws=None, ws_bytes=0) == _lib.KDA_ERR_WORKSPACE   # valid shape

@@ -226,3 +226,39 @@ def test_saved_pair_matches_plain_calls():
     assert torch.equal(o1, o2) and torch.equal(f1, f2)
     for n in GRADS:
         assert torch.equal(g1[n], g2[n]), n
+
+
+# ------------------------------------------------------------------ grouped key heads
+
+@pytest.mark.parametrize("K,H,Hk", [(128, 4, 2), (128, 4, 1), (64, 4, 2)])
+def test_grouped_heads_fwd_bwd(K, H, Hk):
+    """H value heads on Hk key heads (value head h reads key head h // (H // Hk)); K = 128 takes
+    the tensor-core path, K = 64 the SIMT path; dq, dk are summed over each group."""
+    w = Workload("t", B=2, T=150, H=H, Hk=Hk, K=K, V=K, initial_state=True, backward=True, seed=31 + H + Hk)
+    x = make_inputs(w, device=DEV)
+    assert tuple(x["q"].shape) == (2, 150, Hk, K)
+    _check_fwd(x, "bf16")
+    dfinal = 0.1 * torch.randn((2, H, K, K), generator=torch.Generator().manual_seed(5)).to(DEV)
+    _check_bwd(x, "bf16", dfinal=dfinal)
+
+
+def test_grouped_heads_varlen_and_saved_pair():
+    lens = [5, 70, 130, 1]
+    w = Workload("t", B=1, T=sum(lens), H=4, Hk=2, K=128, V=128, varlen=True, initial_state=True,
+                 backward=True, seed=37)
+    x = make_inputs(w, device=DEV, lengths=lens)
+    _check_fwd(x, "bf16")
+    _check_bwd(x, "bf16")
+    import gated_delta_rule_sm_gb300 as kda
+    names = ("q", "k", "v", "g_raw", "beta_raw", "a_log", "dt_bias")
+    kw = dict(scale=x["scale"], lower_bound=x["lower_bound"], cu_seqlens=x["cu_seqlens"],
+              initial_state=x["initial_state"])
+    buf = torch.empty(kda.saved_size(x["q"], x["v"], x["cu_seqlens"]), dtype=torch.uint8, device=DEV)
+    o1, _ = kda.forward(*[x[n] for n in names], saved=buf, **kw)
+    g1 = kda.backward(*[x[n] for n in names], x["dout"], saved=buf, **kw)
+    o2, _ = kda.forward(*[x[n] for n in names], **kw)
+    g2 = kda.backward(*[x[n] for n in names], x["dout"], **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+    for n in GRADS:
+        assert torch.equal(g1[n], g2[n]), n
