@@ -179,12 +179,23 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
                                  : "memory");
             }
         }
+        // X rows t = 16 warp + lane (lanes 0..15 of each warp carry the M = 64 result).  The Y row is
+        // read from global memory 32 columns ahead of its use: the first block before MMA1 is waited
+        // for, each next block while the current one is combined.
+        const int t = 16 * warp + (lane & 15);
+        const float* yrow = y_ptr(s) + t * V + j0;
+        auto load32 = [](const float* src, float* dst) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(src + j);
+                dst[j] = v.x; dst[j + 1] = v.y; dst[j + 2] = v.z; dst[j + 3] = v.w;
+            }
+        };
+        float ynext[32];
+        load32(yrow, ynext);
         fail_wait(bar1, par);
         tc_fence_after();
         {
-            // X rows t = 16 warp + lane (lanes 0..15 of each warp carry the M = 64 result)
-            const int t = 16 * warp + (lane & 15);
-            const float* yrow = y_ptr(s) + t * V + j0;
 #pragma unroll
             for (int jb = 0; jb < JW; jb += 32) {
                 float d[32];
@@ -192,10 +203,8 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
                 tmem_ld16(tD1 + jb + 16 + lane_base, d + 16);
                 float y[32];
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 v = *reinterpret_cast<const float4*>(yrow + jb + j);
-                    y[j] = v.x; y[j + 1] = v.y; y[j + 2] = v.z; y[j + 3] = v.w;
-                }
+                for (int j = 0; j < 32; ++j) y[j] = ynext[j];
+                if (jb + 32 < JW) load32(yrow + jb + 32, ynext);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) d[j] += y[j];
@@ -225,11 +234,14 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
                  idesc_bf16(128, JW, 1, 1));
             mma_commit(bar2);
         }
+        // the P row likewise, one 32-column block ahead (reverse chain only)
+        const float* prow = REV ? p_ptr(s) + tid * V + j0 : nullptr;
+        float pnext[32];
+        if (REV) load32(prow, pnext);
         fail_wait(bar2, par);
         tc_fence_after();
         {
             const float gc = reinterpret_cast<const float*>(sl + chainrec::GC)[tid];
-            const float* prow = REV ? p_ptr(s) + tid * V + j0 : nullptr;
 #pragma unroll
             for (int jb = 0; jb < JW; jb += 32) {
                 float d[32];
@@ -237,10 +249,8 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
                 tmem_ld16(tD3 + jb + 16 + lane_base, d + 16);
                 float pv[32];
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 v = REV ? *reinterpret_cast<const float4*>(prow + jb + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    pv[j] = v.x; pv[j + 1] = v.y; pv[j + 2] = v.z; pv[j + 3] = v.w;
-                }
+                for (int j = 0; j < 32; ++j) pv[j] = REV ? pnext[j] : 0.f;
+                if (REV && jb + 32 < JW) load32(prow + jb + 32, pnext);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) z[jb + j] = gc * z[jb + j] + d[j] + pv[j];
