@@ -78,9 +78,9 @@ def kernel_work(name: str, w, units: float) -> tuple[float, float]:
 # any size, so the figure scales with the token-heads of a launch.  An entry is removed when its
 # kernel changes and has not been captured again.
 PROFILED_TRAFFIC = {
-    ("kda_grad_tc", True): 9500.0,
-    ("kda_intra_tc", False): 2608.0,   # forward record only (forward-only workloads)
-    ("kda_intra_tc", True): 7267.0,    # forward that keeps the backward record, once per training step
+    ("kda_grad_tc", True): 9814.0,
+    ("kda_intra_tc", False): 2609.0,   # forward record only (forward-only workloads)
+    ("kda_intra_tc", True): 7271.0,    # forward that keeps the backward record, once per training step
 }
 
 
