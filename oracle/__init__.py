@@ -11,7 +11,8 @@ pages it follows).  This module compiles it with the host C compiler and
 marshals numpy float64 arrays through ctypes.
 
 Parity status: the recurrence, the L2 norm, sigmoid(beta), state I/O,
-packed documents and the backward pass are pinned by the tests in
+packed documents, grouped key heads, the backward pass and the short
+convolution + SiLU prologue are pinned by the tests in
 ``tests/test_oracle_pins.py``.  The gate formula
 ``g = lower_bound * sigmoid(exp(a_log) * (g_raw + dt_bias))`` and the
 L2-norm epsilon (1e-6) are readings of pages that print neither:
@@ -66,6 +67,11 @@ def _load():
             lib.oracle_kda_fwd.argtypes = common + [_dp, _dp, ctypes.c_int]
             lib.oracle_kda_bwd.restype = ctypes.c_int
             lib.oracle_kda_bwd.argtypes = common + [_dp, _dp] + [_dp] * 8 + [ctypes.c_int]
+            conv = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _ip, ctypes.c_int, _dp, _dp, _dp]
+            lib.oracle_short_conv_fwd.restype = ctypes.c_int
+            lib.oracle_short_conv_fwd.argtypes = conv + [_dp]
+            lib.oracle_short_conv_bwd.restype = ctypes.c_int
+            lib.oracle_short_conv_bwd.argtypes = conv + [_dp, _dp, _dp, _dp]
             _lib = lib
     return _lib
 
@@ -167,3 +173,32 @@ def kda_bwd(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale, lower_boun
     if rc:
         raise MemoryError("oracle_kda_bwd failed")
     return res
+
+
+def short_conv_fwd(x, weight, bias=None, cu_seqlens=None):
+    """Causal depthwise short convolution + SiLU over tokens (the layer's q/k/v prologue).
+
+    x: [B, T, C]; weight: [C, W]; bias: [C] or None.  With ``cu_seqlens`` (B must be 1) every
+    segment starts from zero history.  Returns y [B, T, C].
+    """
+    x, weight, bias = map(_f64, (x, weight, bias))
+    B, T, C = x.shape
+    W = weight.shape[1]
+    cu, cu_p = _cu(cu_seqlens)
+    y = np.zeros_like(x)
+    _load().oracle_short_conv_fwd(B * T, T, C, W, cu_p, (len(cu) - 1) if cu is not None else 0,
+                                  _ptr(x), _ptr(weight), _ptr(bias), _ptr(y))
+    return y
+
+
+def short_conv_bwd(x, weight, bias, dy, cu_seqlens=None):
+    """Reverse mode of :func:`short_conv_fwd`: dict(dx [B, T, C], dweight [C, W], dbias [C] or None)."""
+    x, weight, bias, dy = map(_f64, (x, weight, bias, dy))
+    B, T, C = x.shape
+    W = weight.shape[1]
+    cu, cu_p = _cu(cu_seqlens)
+    dx, dw = np.zeros_like(x), np.zeros_like(weight)
+    db = np.zeros(C) if bias is not None else None
+    _load().oracle_short_conv_bwd(B * T, T, C, W, cu_p, (len(cu) - 1) if cu is not None else 0,
+                                  _ptr(x), _ptr(weight), _ptr(bias), _ptr(dy), _ptr(dx), _ptr(dw), _ptr(db))
+    return dict(dx=dx, dweight=dw, dbias=db)

@@ -396,3 +396,78 @@ int oracle_kda_bwd(int B, int T, int H, int Hk, int K, int V, int num_seqs, cons
     free(pa); free(pd);
     return err;
 }
+
+/* ---- the layer's q/k/v prologue: causal depthwise short convolution + SiLU ----
+ *
+ * hyper-parallel "KDA context-parallel executors" (`_run_causal_short_conv`,
+ * `_local_short_conv`, `_validate_layer_short_conv`): each of q, k, v passes
+ * through a depthwise Conv1d (groups = channels, stride 1, dilation 1, zero
+ * padding kernel_size - 1 on the left, output cut to the input length) and
+ * SiLU.  With packed documents every segment starts from zero history (the
+ * same convention as the recurrence; the pages hand the conv kernel size to
+ * FLA's per-document context for exactly these boundary tokens).
+ *
+ *   a[t, c] = bias[c] + sum_{i<W} weight[c, i] x[t - (W-1) + i, c]
+ *   y[t, c] = a * sigmoid(a)
+ * x [TT, C], weight [C, W], bias [C] or NULL. */
+static int64_t seg_start_of(const int32_t* cu, int num_seqs, int T, int64_t t)
+{
+    if (!cu) return (t / T) * T;
+    int lo = 0, hi = num_seqs - 1;           /* last n with cu[n] <= t */
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return cu[lo];
+}
+
+static double conv_pre(const double* x, const double* w, const double* b, int C, int W, int64_t s0, int64_t t,
+                       int c)
+{
+    double a = b ? b[c] : 0.0;
+    for (int i = 0; i < W; ++i) {
+        const int64_t tau = t - (W - 1) + i;
+        if (tau >= s0) a += w[c * W + i] * x[tau * C + c];
+    }
+    return a;
+}
+
+int oracle_short_conv_fwd(int64_t TT, int T, int C, int W, const int32_t* cu_seqlens, int num_seqs,
+                          const double* x, const double* weight, const double* bias, double* y)
+{
+    for (int64_t t = 0; t < TT; ++t) {
+        const int64_t s0 = seg_start_of(cu_seqlens, num_seqs, T, t);
+        for (int c = 0; c < C; ++c) {
+            const double a = conv_pre(x, weight, bias, C, W, s0, t, c);
+            y[t * C + c] = a * sigm(a);
+        }
+    }
+    return 0;
+}
+
+/* Reverse mode: da = dy * d silu(a)/da = dy * s (1 + a (1 - s)), s = sigmoid(a); then dx, dweight,
+ * dbias by the chain rule through the sum above. */
+int oracle_short_conv_bwd(int64_t TT, int T, int C, int W, const int32_t* cu_seqlens, int num_seqs,
+                          const double* x, const double* weight, const double* bias, const double* dy,
+                          double* dx, double* dweight, double* dbias)
+{
+    memset(dx, 0, sizeof(double) * (size_t)TT * C);
+    memset(dweight, 0, sizeof(double) * (size_t)C * W);
+    if (dbias) memset(dbias, 0, sizeof(double) * (size_t)C);
+    for (int64_t t = 0; t < TT; ++t) {
+        const int64_t s0 = seg_start_of(cu_seqlens, num_seqs, T, t);
+        for (int c = 0; c < C; ++c) {
+            const double a = conv_pre(x, weight, bias, C, W, s0, t, c);
+            const double s = sigm(a);
+            const double da = dy[t * C + c] * s * (1.0 + a * (1.0 - s));
+            if (dbias) dbias[c] += da;
+            for (int i = 0; i < W; ++i) {
+                const int64_t tau = t - (W - 1) + i;
+                if (tau < s0) continue;
+                dx[tau * C + c] += weight[c * W + i] * da;
+                dweight[c * W + i] += x[tau * C + c] * da;
+            }
+        }
+    }
+    return 0;
+}

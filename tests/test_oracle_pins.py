@@ -358,3 +358,70 @@ def test_grouped_heads_reject_uneven_groups():
     d, S0 = _grouped_inputs(H=3, Hk=2)
     with pytest.raises(ValueError):
         oracle.kda_fwd(**d, initial_state=S0, scale=0.5, lower_bound=-5.0)
+
+
+# ------------------------------------------------------------------ short convolution + SiLU prologue
+
+def _conv_inputs(B=2, T=11, C=5, W=4, seed=0):
+    r = np.random.default_rng(seed)
+    return r.standard_normal((B, T, C)), r.standard_normal((C, W)), r.standard_normal(C)
+
+
+@pytest.mark.parametrize("W", [1, 2, 4])
+def test_short_conv_matches_numpy_convolve(W):
+    """Per row and channel the pre-activation is numpy's full convolution with the reversed taps,
+    cut to the row length (causal, zero history), plus the bias; then SiLU = a * sigmoid(a)."""
+    x, w, b = _conv_inputs(W=W, seed=40 + W)
+    y = oracle.short_conv_fwd(x, w, b)
+    B, T, C = x.shape
+    for bi in range(B):
+        for c in range(C):
+            a = np.convolve(x[bi, :, c], w[c][::-1])[:T] + b[c]
+            np.testing.assert_allclose(y[bi, :, c], a * expit(a), rtol=1e-13, atol=1e-14)
+    y0 = oracle.short_conv_fwd(x, w, None)
+    a0 = np.stack([np.stack([np.convolve(x[bi, :, c], w[c][::-1])[:T] for c in range(C)], -1) for bi in range(B)])
+    np.testing.assert_allclose(y0, a0 * expit(a0), rtol=1e-13, atol=1e-14)
+
+
+def test_short_conv_matches_depthwise_conv1d():
+    """The pages' own formulation: torch conv1d with groups = channels and kernel_size - 1 zero
+    padding, output cut to the input length, then SiLU."""
+    torch = pytest.importorskip("torch")
+    x, w, b = _conv_inputs(B=2, T=9, C=6, W=4, seed=44)
+    y = oracle.short_conv_fwd(x, w, b)
+    xt = torch.from_numpy(x).transpose(1, 2)
+    out = torch.nn.functional.conv1d(xt, torch.from_numpy(w)[:, None, :], torch.from_numpy(b), padding=3, groups=6)
+    ref = torch.nn.functional.silu(out[:, :, :9]).transpose(1, 2).numpy()
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_short_conv_packed_segments_start_from_zero_history():
+    lens = [3, 1, 6]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    x, w, b = _conv_inputs(B=1, T=10, C=3, W=4, seed=45)
+    y = oracle.short_conv_fwd(x, w, b, cu_seqlens=cu)
+    for n in range(3):
+        s, e = cu[n], cu[n + 1]
+        np.testing.assert_array_equal(y[:, s:e], oracle.short_conv_fwd(x[:, s:e], w, b))
+
+
+@pytest.mark.parametrize("packed", [False, True])
+def test_short_conv_backward_central_differences(packed):
+    x, w, b = _conv_inputs(B=1 if packed else 2, T=8, C=3, W=3, seed=46)
+    cu = np.array([0, 3, 8], dtype=np.int32) if packed else None
+    dy = np.random.default_rng(47).standard_normal(x.shape)
+    g = oracle.short_conv_bwd(x, w, b, dy, cu_seqlens=cu)
+    L = lambda xx, ww, bb: float(np.sum(oracle.short_conv_fwd(xx, ww, bb, cu_seqlens=cu) * dy))
+    h = 1e-6
+    for name, arr, gname in (("x", x, "dx"), ("w", w, "dweight"), ("b", b, "dbias")):
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(*arr.shape):
+            ap, am = arr.copy(), arr.copy()
+            ap[idx] += h
+            am[idx] -= h
+            args_p = dict(x=x, w=w, b=b)
+            args_m = dict(x=x, w=w, b=b)
+            args_p[name], args_m[name] = ap, am
+            num[idx] = (L(args_p["x"], args_p["w"], args_p["b"]) - L(args_m["x"], args_m["w"], args_m["b"])) / (2 * h)
+        err = np.abs(num - g[gname]).max() / np.abs(num).max()
+        assert err < 1e-7, (name, err)
