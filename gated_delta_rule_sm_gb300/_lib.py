@@ -23,7 +23,8 @@ KDA_BF16, KDA_FP32 = 0, 1
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_fwd_workspace_size", "kda_bwd_workspace_size", "kda_fwd", "kda_fwd_simt", "kda_bwd",
            "kda_status_string", "kda_device_status", "kda_version", "kda_timing_begin", "kda_timing_end",
-           "kda_kernel_name", "kda_fwd_noalloc", "kda_saved_size", "kda_fwd_save", "kda_bwd_saved")
+           "kda_kernel_name", "kda_fwd_noalloc", "kda_saved_size", "kda_fwd_save", "kda_bwd_saved",
+           "kda_short_conv_fwd", "kda_short_conv_bwd_workspace_size", "kda_short_conv_bwd")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -88,6 +89,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.kda_timing_end.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), ctypes.c_int]
         lib.kda_kernel_name.restype = ctypes.c_char_p
         lib.kda_kernel_name.argtypes = [ctypes.c_int]
+        conv = [ctypes.c_int] * 5 + [_vp] * 4 + [ctypes.c_int]
+        lib.kda_short_conv_fwd.restype = ctypes.c_int
+        lib.kda_short_conv_fwd.argtypes = conv + [_vp, _vp]
+        lib.kda_short_conv_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.kda_short_conv_bwd_workspace_size.argtypes = [ctypes.c_int] * 4
+        lib.kda_short_conv_bwd.restype = ctypes.c_int
+        lib.kda_short_conv_bwd.argtypes = conv + [_vp] * 5 + [ctypes.c_size_t, _vp]
         _lib = lib
         return lib
 
@@ -270,3 +278,44 @@ def backward(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale: float, lo
     code = lib.kda_bwd(*head, *tail)
     _check(code, "kda_bwd")
     return grads
+
+
+def short_conv(x, weight, bias=None, *, cu_seqlens=None, out=None, stream: Optional[torch.cuda.Stream] = None):
+    """Causal depthwise short convolution + SiLU through ``kda_short_conv_fwd``.
+
+    x: [B, T, C] (bf16 or fp32); weight: [C, W] fp32; bias: [C] fp32 or None.  Returns y like x.
+    """
+    lib = load()
+    _contig(x, weight, bias, cu_seqlens)
+    B, T, C = x.shape
+    W = weight.shape[-1]
+    if weight.numel() != C * W or (bias is not None and bias.numel() != C):
+        raise ValueError("weight must be [C, W] and bias [C]")
+    if out is None:
+        out = torch.empty_like(x)
+    st = stream if stream is not None else torch.cuda.current_stream(x.device)
+    n = int(cu_seqlens.numel() - 1) if cu_seqlens is not None else 0
+    code = lib.kda_short_conv_fwd(B, T, C, W, _dtype_code(x), _ptr(x), _ptr(weight), _ptr(bias), _ptr(cu_seqlens),
+                                  n, _ptr(out), ctypes.c_void_p(st.cuda_stream))
+    _check(code, "kda_short_conv_fwd")
+    return out
+
+
+def short_conv_backward(x, weight, bias, dy, *, cu_seqlens=None, stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """Reverse mode of :func:`short_conv`: dict(dx [B, T, C], dweight [C, W], dbias [C] or None), fp32."""
+    lib = load()
+    _contig(x, weight, bias, dy, cu_seqlens)
+    B, T, C = x.shape
+    W = weight.shape[-1]
+    dev = x.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = dict(dx=torch.empty((B, T, C), **f32), dweight=torch.empty((C, W), **f32),
+             dbias=torch.empty((C,), **f32) if bias is not None else None)
+    ws = workspace_cache.get(dev, "conv", int(lib.kda_short_conv_bwd_workspace_size(B, T, C, W)))
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    n = int(cu_seqlens.numel() - 1) if cu_seqlens is not None else 0
+    code = lib.kda_short_conv_bwd(B, T, C, W, _dtype_code(x), _ptr(x), _ptr(weight), _ptr(bias), _ptr(cu_seqlens), n,
+                                  _ptr(dy), _ptr(g["dx"]), _ptr(g["dweight"]), _ptr(g["dbias"]), _ptr(ws),
+                                  ctypes.c_size_t(ws.numel()), ctypes.c_void_p(st.cuda_stream))
+    _check(code, "kda_short_conv_bwd")
+    return g

@@ -226,7 +226,8 @@ static const char* kKernelNames[] = {"kda_plan",          "kda_intra_simt",   "k
                                      "kda_chain_bwd_simt", "kda_grad_simt",    "kda_param_reduce",
                                      "kda_empty_segment", "kda_intra_tc",     "kda_chain_fwd_tc",
                                      "kda_grad_tc",       "kda_bwd_pre",      "kda_chain_bwd_tc",
-                                     "kda_chain_rec_tc",  "kda_group_sum"};
+                                     "kda_chain_rec_tc",  "kda_group_sum",    "kda_short_conv_fwd",
+                                     "kda_short_conv_bwd", "kda_short_conv_reduce"};
 
 // saved != NULL: also keep the fp32 backward record there (kda_fwd_save)
 static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cudaStream_t stream,

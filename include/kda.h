@@ -221,6 +221,39 @@ kda_status kda_timing_begin(int max_launches);
 int kda_timing_end(float* ms, int* kernel_ids, int cap);
 const char* kda_kernel_name(int kernel_id);
 
+/*
+ * The layer's q/k/v prologue: causal depthwise short convolution + SiLU
+ * (hyper-parallel "KDA context-parallel executors", `_run_causal_short_conv`,
+ * `_local_short_conv`, `_validate_layer_short_conv`: a depthwise Conv1d with
+ * groups = channels, stride 1, dilation 1, kernel_size - 1 zero padding on the
+ * left, output cut to the input length, then SiLU):
+ *     a[t, c] = bias[c] + sum_{i < W} weight[c, i] * x[t - (W - 1) + i, c]
+ *     y[t, c] = a * sigmoid(a)
+ * Token-first layout: x, y, dy [B, T, C] in `dtype` (C = heads * head dim of
+ * one projection); weight [C, W] fp32 (a Conv1d weight [C, 1, W]); bias [C]
+ * fp32 or NULL.  With cu_seqlens (device, [num_seqs + 1], B == 1) every
+ * segment starts from zero history, as in kda_fwd.  All pointers are device
+ * pointers owned by the caller; nothing is allocated or retained.
+ * Errors: B, T, C, W < 1, a bad dtype, NULL x / weight / y (dy, dx, dweight,
+ * and dbias when bias != NULL) or cu_seqlens with B != 1 give
+ * KDA_ERR_INVALID_ARG; W > 8, C not a multiple of 8 or a data pointer not
+ * 16-byte aligned give KDA_ERR_UNSUPPORTED; a short or misaligned workspace
+ * gives KDA_ERR_WORKSPACE.
+ */
+kda_status kda_short_conv_fwd(int B, int T, int C, int W, kda_dtype dtype, const void* x, const float* weight,
+                              const float* bias, const int32_t* cu_seqlens, int num_seqs, void* y,
+                              cudaStream_t stream);
+
+/* Bytes of workspace kda_short_conv_bwd needs (per-tile partial sums of the weight / bias gradients). */
+size_t kda_short_conv_bwd_workspace_size(int B, int T, int C, int W);
+
+/* Reverse mode: dx [B, T, C] fp32, dweight [C, W] fp32, dbias [C] fp32 (written when bias != NULL).
+ * dweight and dbias are summed over tokens in a fixed order (deterministic). */
+kda_status kda_short_conv_bwd(int B, int T, int C, int W, kda_dtype dtype, const void* x, const float* weight,
+                              const float* bias, const int32_t* cu_seqlens, int num_seqs, const void* dy,
+                              float* dx, float* dweight, float* dbias, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

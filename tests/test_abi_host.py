@@ -154,3 +154,26 @@ def test_grouped_key_heads_validation(lib):
     assert f(H=4, Hk=2) == f(H=4) == f(H=4, Hk=4)           # the forward keeps nothing per key head
     assert b(H=4, Hk=2) > b(H=4, Hk=4) == b(H=4)             # dq, dk per value head before the group sum
     assert _fwd(lib, _dims(H=4, Hk=2), ws=None, ws_bytes=0) == _lib.KDA_ERR_WORKSPACE   # valid shape
+
+
+def _conv_fwd(lib, B=1, T=64, C=64, W=4, dtype=_lib.KDA_BF16, ptr=16, cu=None, n=0, y=16):
+    p = ctypes.c_void_p(ptr) if ptr else None
+    yp = ctypes.c_void_p(y) if y else None
+    return lib.kda_short_conv_fwd(B, T, C, W, dtype, p, p, None, cu, n, yp, None)
+
+
+def test_short_conv_validation(lib):
+    assert _conv_fwd(lib, B=0) == _lib.KDA_ERR_INVALID_ARG
+    assert _conv_fwd(lib, W=0) == _lib.KDA_ERR_INVALID_ARG
+    assert _conv_fwd(lib, dtype=5) == _lib.KDA_ERR_INVALID_ARG
+    assert _conv_fwd(lib, ptr=0) == _lib.KDA_ERR_INVALID_ARG
+    assert _conv_fwd(lib, y=0) == _lib.KDA_ERR_INVALID_ARG
+    assert _conv_fwd(lib, B=2, cu=ctypes.c_void_p(16), n=2) == _lib.KDA_ERR_INVALID_ARG   # packed needs B == 1
+    assert _conv_fwd(lib, W=9) == _lib.KDA_ERR_UNSUPPORTED        # at most 8 taps
+    assert _conv_fwd(lib, C=12) == _lib.KDA_ERR_UNSUPPORTED       # 8-channel vectors
+    assert _conv_fwd(lib, ptr=24) == _lib.KDA_ERR_UNSUPPORTED     # 16-byte aligned data
+    ws = lambda **kw: lib.kda_short_conv_bwd_workspace_size(kw.get("B", 1), kw.get("T", 64), kw.get("C", 64),
+                                                            kw.get("W", 4))
+    assert ws() > 0 and ws() % 256 == 0
+    assert ws(T=128) == 2 * ws()          # one partial row per 64-token tile
+    assert ws(W=9) == 0 and ws(C=0) == 0

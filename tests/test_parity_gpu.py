@@ -262,3 +262,50 @@ def test_grouped_heads_varlen_and_saved_pair():
     assert torch.equal(o1, o2)
     for n in GRADS:
         assert torch.equal(g1[n], g2[n]), n
+
+
+# ------------------------------------------------------------------ short convolution + SiLU prologue
+
+def _conv_case(B, T, C, W, dtype, bias=True, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    x = torch.randn((B, T, C), generator=g).to(dt)
+    w = (0.5 * torch.randn((C, W), generator=g)).float()
+    b = (0.1 * torch.randn((C,), generator=g)).float() if bias else None
+    dy = torch.randn((B, T, C), generator=g).to(dt)
+    return x, w, b, dy
+
+
+@pytest.mark.parametrize("B,T,C,W,dtype,bias", [(2, 150, 256, 4, "bf16", True), (1, 300, 64, 3, "fp32", False),
+                                                (1, 97, 1024, 1, "bf16", True), (2, 70, 128, 8, "bf16", True),
+                                                (4, 1024, 4096, 4, "bf16", True)])
+def test_short_conv_fwd_bwd(B, T, C, W, dtype, bias):
+    import gated_delta_rule_sm_gb300 as kda
+    import oracle
+    x, w, b, dy = _conv_case(B, T, C, W, dtype, bias, seed=T + C + W)
+    d = lambda t: t.to(DEV) if t is not None else None
+    y = kda.short_conv(d(x), d(w), d(b))
+    g = kda.short_conv_backward(d(x), d(w), d(b), d(dy))
+    torch.cuda.synchronize()
+    ry = oracle.short_conv_fwd(f64(x), f64(w), f64(b) if b is not None else None)
+    rg = oracle.short_conv_bwd(f64(x), f64(w), f64(b) if b is not None else None, f64(dy))
+    assert rel_err(y, ry, "bf16" if dtype == "bf16" else "fp32") <= tol(dtype)
+    # the gradients are fp32 computations on exact inputs: the fp32 bound applies to both dtypes
+    for n in ("dx", "dweight") + (("dbias",) if bias else ()):
+        assert rel_err(g[n], rg[n], "fp32") <= tol("fp32"), n
+
+
+def test_short_conv_packed_documents():
+    import gated_delta_rule_sm_gb300 as kda
+    import oracle
+    lens = [5, 70, 1, 130, 1]
+    x, w, b, dy = _conv_case(1, sum(lens), 256, 4, "bf16", True, seed=7)
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    y = kda.short_conv(x.to(DEV), w.to(DEV), b.to(DEV), cu_seqlens=cu.to(DEV))
+    g = kda.short_conv_backward(x.to(DEV), w.to(DEV), b.to(DEV), dy.to(DEV), cu_seqlens=cu.to(DEV))
+    torch.cuda.synchronize()
+    ry = oracle.short_conv_fwd(f64(x), f64(w), f64(b), cu_seqlens=cu.numpy())
+    rg = oracle.short_conv_bwd(f64(x), f64(w), f64(b), f64(dy), cu_seqlens=cu.numpy())
+    assert rel_err(y, ry, "bf16") <= tol("bf16")
+    for n in ("dx", "dweight", "dbias"):
+        assert rel_err(g[n], rg[n], "fp32") <= tol("fp32"), n
