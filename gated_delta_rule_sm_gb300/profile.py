@@ -30,6 +30,8 @@ def main(argv=None) -> None:
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--fwd-only", action="store_true", help="skip the backward of a fwd+bwd workload")
     ap.add_argument("--saved", action="store_true", help="forward keeps the per-chunk record for the backward")
+    ap.add_argument("--short-conv", type=int, default=0, metavar="W",
+                    help="instead time the W-tap short convolution + SiLU prologue on a q-shaped [B, T, H*K] tensor")
     a = ap.parse_args(argv)
     w = WORKLOADS[a.workload]
     over = {k: v for k, v in (("B", a.B), ("T", a.T), ("H", a.H)) if v is not None}
@@ -38,6 +40,9 @@ def main(argv=None) -> None:
             raise SystemExit("varlen workloads keep their packed length")
         w = dataclasses.replace(w, **over)
     dev = torch.device("cuda:0")
+    if a.short_conv:
+        _time_short_conv(w, a.short_conv, a.iters, dev)
+        return
     x = make_inputs(w, device=dev)
     names = ("q", "k", "v", "g_raw", "beta_raw", "a_log", "dt_bias")
     kw = dict(scale=x["scale"], lower_bound=x["lower_bound"], chunk_size=x["chunk_size"],
@@ -60,6 +65,40 @@ def main(argv=None) -> None:
     torch.cuda.synchronize()
     print(f"workload={w.name} B={w.B} T={w.T} H={w.H} bwd={run_bwd} saved={saved is not None} iters={a.iters} "
           f"ms_per_iter={ev[0].elapsed_time(ev[1]) / max(1, a.iters):.3f}")
+
+
+def _time_short_conv(w, W: int, iters: int, dev) -> None:
+    """Forward and backward of the prologue convolution on a [B, T, H*K] activation of the workload."""
+    from . import short_conv, short_conv_backward
+    g = torch.Generator().manual_seed(w.seed)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    C = w.H * w.K
+    x = torch.randn((w.B, w.T, C), generator=g).to(dt).to(dev)
+    dy = torch.randn((w.B, w.T, C), generator=g).to(dt).to(dev)
+    wt = (0.5 * torch.randn((C, W), generator=g)).to(dev)
+    b = (0.1 * torch.randn((C,), generator=g)).to(dev)
+    y = torch.empty_like(x)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(3):
+        short_conv(x, wt, b, out=y)
+        short_conv_backward(x, wt, b, dy)
+    torch.cuda.synchronize()
+    ev[0].record()
+    for _ in range(iters):
+        short_conv(x, wt, b, out=y)
+    ev[1].record()
+    for _ in range(iters):
+        short_conv_backward(x, wt, b, dy)
+    ev[2].record()
+    torch.cuda.synchronize()
+    e = x.element_size()
+    n = x.numel()
+    f_ms = ev[0].elapsed_time(ev[1]) / iters
+    b_ms = ev[1].elapsed_time(ev[2]) / iters
+    # algorithmic bytes: forward reads x, writes y; backward reads x, dy, writes fp32 dx
+    fb, bb = n * 2 * e, n * (2 * e + 4)
+    print(f"short_conv W={W} B={w.B} T={w.T} C={C} dtype={w.dtype} fwd_ms={f_ms:.4f} fwd_GBs={fb / f_ms / 1e6:.0f} "
+          f"bwd_ms={b_ms:.4f} bwd_GBs={bb / b_ms / 1e6:.0f}")
 
 
 if __name__ == "__main__":
