@@ -1,21 +1,21 @@
 // kda_grad.cu -- per-chunk gradients of the chunkwise KDA recurrence for K = V = 128.
 //
-// Inputs per (chunk, head): the fp32 chunk record (W, Kg, Kd, Qg, U0, Aqk, N, Bkk, Gamma, q_hat,
-// k_hat, beta, exp(Gamma_last)), the chunk-entering state S0 and the gradient dS_end w.r.t. the
-// chunk-leaving state (both from the state chains), dO, v and the raw q, k, g_raw.  The gradient
-// of the chunk equations
+// Inputs per (chunk, head): the fp32 chunk record (Kg, Qg, Kd, N, Bkk, Gamma, q_hat, k_hat, beta,
+// the inverse norms), the chunk-entering state S0 and the gradient dS_end w.r.t. the chunk-leaving
+// state (both from the state chains), U and dU per chunk (written by the two backward chains), dO,
+// v and g_raw.  The gradient of the chunk equations
 //     U = U0 - W S0,   O = scale (Qg S0 + Aqk U),   S_end = Diag(exp(Gamma_last)) S0 + Kd^T U,
 //     T = N Diag(beta), N = (I + Diag(beta) Bkk)^-1, W = T Kg, U0 = T v
 // is formed here and pushed through the decayed bilinear forms, the cumulative log-decay and the
 // prologue (L2 norm, sigmoid beta, lower-bounded gate).
 //
-// The per-chunk contractions are small (64 x 128 x {32, 64, 128}) and interleaved with
-// elementwise work, so they run as warp-level tf32 MMAs (m16n8k8, operands rounded to nearest;
-// the decayed bilinear forms use a hi/lo split because their pair terms cancel in the
-// log-decay gradient)
-// straight from padded shared-memory tiles: no descriptor or accumulator round trips between the
-// many dependent steps.  Row strides = 4 (mod 32) words make every fragment load conflict-free in
-// either orientation.
+// Phase 1 walks the four 32-column slices of V: the slice outer products (dKg, dQg, dKd, dT, dA)
+// accumulate in TMEM from tcgen05 MMAs on bf16 hi / lo operands; the small dependent products in
+// between (v - Kg S0, Diag(beta) N^T dU) and everything in phase 2 run as warp-level tf32 MMAs
+// (m16n8k8, operands rounded to nearest; the decayed bilinear forms use a hi/lo split because
+// their pair terms cancel in the log-decay gradient) straight from padded shared-memory tiles: no
+// descriptor or accumulator round trips between the many dependent steps.  Row strides = 4
+// (mod 32) words make every fragment load conflict-free in either orientation.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_sm100.cuh"

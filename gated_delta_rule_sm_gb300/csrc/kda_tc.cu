@@ -9,7 +9,7 @@
 // fp32.  The state itself stays in fp32 registers.
 //
 // The intra-chunk kernel writes one record per (chunk, head) in exactly the shared-memory layout
-// the chain kernel's MMAs read, so the chain moves it with three bulk copies per chunk.
+// the chain kernel's MMAs read, so the chain's load warp moves it with three bulk copies per chunk.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
@@ -35,7 +35,9 @@ constexpr uint32_t TAIL = BYTES - KD; // KD + AQ + GC, contiguous
 
 // ------------------------------------------------------------------ intra-chunk kernel (tcgen05)
 //
-// One CTA (256 threads) per (chunk, head).  Decay factorisation: inside a chunk, with Gamma_t the
+// Persistent: one CTA (256 threads) per SM loops over (chunk, head) items, fetching the next item's
+// q, k, g, v tiles by TMA once the current item's A-matrix MMAs no longer need the tile area.
+// Decay factorisation: inside a chunk, with Gamma_t the
 // cumulative log-decay and 16-token sub-blocks b (Gamma at the end of sub-block b-1 is G_b),
 //   exp(Gamma_t - Gamma_s) = exp(Gamma_t - G_{j+1}) * exp(G_{j+1} - Gamma_s)   for s in sub-block j.
 // The right factor is <= 1; the left is <= 1 for t past sub-block j and <= exp(16 |lower_bound|)
