@@ -122,15 +122,16 @@ __global__ void __launch_bounds__(256, 1)
     const RecLayout RL = RecLayout::make(128, 128);
     // Each MMA barrier has at most one pending phase at any time, so parity waits are unambiguous.
     uint64_t* bar_load = reinterpret_cast<uint64_t*>(smem + BAR);
-    uint64_t* bar_a = bar_load + 1;   // A-matrix MMAs reading tile pair A (six issuing warps)
-    uint64_t* bar_b = bar_load + 2;   // A-matrix MMAs reading tile pair B (six issuing warps)
+    uint64_t* bar_a = bar_load + 1;   // A-matrix MMAs reading tile pair A (two issuing warps)
+    uint64_t* bar_b = bar_load + 2;   // A-matrix MMAs reading tile pair B (two issuing warps)
     uint64_t* bar_w = bar_load + 3;   // the final W / U0 MMAs (two issuing warps)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_load + 4);
     // TMEM columns: A-matrix partial products p = 0..5 at 64 p + 16 j (sub-block j), W^T at 384, U0^T
-    // at 448.  One thread issues a tcgen05.mma every ~100 cycles, so each sub-block's three split
-    // products, each halved over K, go out from six warps in parallel, and the two final products
-    // from two.
-    constexpr int NPART = 6;
+    // at 448.  One thread issues a tcgen05.mma every ~100 cycles and the tensor pipe takes one about
+    // every 46 at this shape, so two issuing threads keep it busy: warps 0 and 1, whose sub-block
+    // writes no left operand after the first, so the other warps' operand writes for the next
+    // sub-block overlap the MMAs.  The two final products go out from two warps as well.
+    constexpr int NPART = 6, NISSUE = 2;
     constexpr uint32_t T_W = 384, T_U0 = 448, TCOLS = 512;
     // the raw q, k, g, v tiles of one item (64 tokens x 128 channels each, out-of-range rows zero)
     auto load_raw = [&](int it) {
@@ -145,8 +146,8 @@ __global__ void __launch_bounds__(256, 1)
 
     if (tid == 0) {
         mbar_init(bar_load, 1);
-        mbar_init(bar_a, NPART);
-        mbar_init(bar_b, NPART);
+        mbar_init(bar_a, NISSUE);
+        mbar_init(bar_b, NISSUE);
         mbar_init(bar_w, 2);
         mbar_fence_init();
         load_raw(blockIdx.x);
@@ -375,19 +376,21 @@ __global__ void __launch_bounds__(256, 1)
                 }
             }
         };
-        // A-matrix MMAs of column sub-block j: D_j = L_hi R_hi + L_hi R_lo + L_lo R_hi.  Issuing warp
-        // w < 6 takes product w / 2 over channel half w % 2 into partial accumulator w; the partials
-        // are summed when the accumulators are read.
+        // A-matrix MMAs of column sub-block j: D_j = L_hi R_hi + L_hi R_lo + L_lo R_hi, each product
+        // halved over channels: partial p = product p / 2 over channel half p % 2, summed when the
+        // accumulators are read.  Warp w < 2 issues partials w, w + 2, w + 4.
         constexpr uint32_t idA = idesc_bf16(128, 16, 1, 1);
         auto issue_A = [&](int j, uint32_t hi_off, uint32_t lo_off, uint64_t* bar) {
-            if (lane != 0 || warp >= NPART) return;
-            const int pr = warp >> 1, k0 = 4 * (warp & 1);
+            if (lane != 0 || warp >= NISSUE) return;
             const uint32_t lh = smem_u32(smem + hi_off), ll = smem_u32(smem + lo_off);
             const uint32_t rh = smem_u32(smem + RB_HI) + j * 256, rl = smem_u32(smem + RB_LO) + j * 256;
-            const uint32_t la = pr == 2 ? ll : lh, rb = pr == 1 ? rl : rh;
-            for (int kk = k0; kk < k0 + 4; ++kk)
-                mma_bf16(tmem + 64 * warp + 16 * j, smem_desc(la + kk * 4096, 2048, 128),
-                         smem_desc(rb + kk * 2048, 1024, 128), idA, kk > k0);
+            for (int pp = warp; pp < NPART; pp += NISSUE) {
+                const int pr = pp >> 1, k0 = 4 * (pp & 1);
+                const uint32_t la = pr == 2 ? ll : lh, rb = pr == 1 ? rl : rh;
+                for (int kk = k0; kk < k0 + 4; ++kk)
+                    mma_bf16(tmem + 64 * pp + 16 * j, smem_desc(la + kk * 4096, 2048, 128),
+                             smem_desc(rb + kk * 2048, 1024, 128), idA, kk > k0);
+            }
             mma_commit(bar);
         };
         auto wait_on = [&](uint64_t* bar, uint32_t& par) -> bool {
