@@ -29,7 +29,9 @@ static kda_status check_dims(const kda_dims* d, int chunk_size, bool varlen, Sha
     if (d->dtype != KDA_BF16 && d->dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
     if (chunk_size <= 0) return KDA_ERR_INVALID_ARG;
     if (d->K < 16 || d->V < 16) return KDA_ERR_INVALID_ARG;           // head dims below 16 are rejected
-    if (chunk_size != kChunk) return KDA_ERR_UNSUPPORTED;
+    // the chunk size is a blocking choice, not part of the result: 16, 32 and 64 all run the 64-token
+    // kernels (segments still restart at every document start)
+    if (chunk_size != 16 && chunk_size != 32 && chunk_size != kChunk) return KDA_ERR_UNSUPPORTED;
     if (d->K > 128 || d->V > 128 || d->K % 16 || d->V % 16) return KDA_ERR_UNSUPPORTED;
     const long long TT = (long long)d->B * d->T;
     if (TT > (1LL << 30) || TT * d->H * (d->K > d->V ? d->K : d->V) > (1LL << 40)) return KDA_ERR_UNSUPPORTED;

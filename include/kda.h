@@ -92,7 +92,10 @@ size_t kda_bwd_workspace_size(const kda_dims* dims, int chunk_size);
  * Forward.  Writes out [B,T,H,V] (input dtype) and, if final_state != NULL,
  * final_state [N,H,K,V] fp32.  initial_state may be NULL (zero state).
  * scale is applied to the output; lower_bound must be finite and < 0;
- * chunk_size must be 64.
+ * chunk_size must be 16, 32 or 64 (other positive values: KDA_ERR_UNSUPPORTED).
+ * The result does not depend on the chunk size in exact arithmetic; every
+ * accepted value runs the same 64-token blocking, so results agree to
+ * rounding with any chunk size.
  * Requirements: B,T,H >= 1; 16 <= K,V <= 128 and multiples of 16 (the pages
  * reject head dims below 16); N >= 1.  bf16 with K == V == 128, 16-byte
  * aligned q, k, v, g_raw (and dout for kda_bwd) and lower_bound >= -5 runs

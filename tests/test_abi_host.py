@@ -71,7 +71,12 @@ def test_shape_validation(lib, bad, code):
 
 def test_scalar_validation(lib):
     assert _fwd(lib, _dims(), chunk=0) == _lib.KDA_ERR_INVALID_ARG
-    assert _fwd(lib, _dims(), chunk=32) == _lib.KDA_ERR_UNSUPPORTED
+    assert _fwd(lib, _dims(), chunk=48) == _lib.KDA_ERR_UNSUPPORTED
+    assert _fwd(lib, _dims(), chunk=128) == _lib.KDA_ERR_UNSUPPORTED
+    for c in (16, 32, 64):   # accepted: validation passes and stops at the missing workspace
+        assert _fwd(lib, _dims(), chunk=c) == _lib.KDA_ERR_WORKSPACE
+    s = lambda c: lib.kda_fwd_workspace_size(ctypes.byref(_dims()), c)
+    assert s(16) == s(32) == s(64) > 0
     assert _fwd(lib, _dims(), lb=0.0) == _lib.KDA_ERR_INVALID_ARG      # the gate needs a negative bound
     assert _fwd(lib, _dims(), lb=1.0) == _lib.KDA_ERR_INVALID_ARG
     assert _fwd(lib, _dims(), lb=float("nan")) == _lib.KDA_ERR_INVALID_ARG

@@ -309,3 +309,14 @@ def test_short_conv_packed_documents():
     assert rel_err(y, ry, "bf16") <= tol("bf16")
     for n in ("dx", "dweight", "dbias"):
         assert rel_err(g[n], rg[n], "fp32") <= tol("fp32"), n
+
+
+@pytest.mark.parametrize("chunk", [16, 32])
+def test_smaller_chunk_sizes_match_the_oracle(chunk):
+    """The result does not depend on the chunk size; 16 and 32 are accepted and run the same kernels."""
+    w = Workload("t", B=1, T=200, H=2, K=128, V=128, initial_state=True, backward=True, seed=50 + chunk,
+                 chunk_size=chunk)
+    x = make_inputs(w, device=DEV)
+    assert x["chunk_size"] == chunk
+    _check_fwd(x, "bf16")
+    _check_bwd(x, "bf16")
