@@ -197,7 +197,7 @@ def cpu_baseline(w, x_cpu: dict, budget_s: float = 15.0) -> dict:
     heads_total = w.H
     rows = 1
     f64 = lambda t: t.detach().to(dtype=__import__("torch").float64).cpu().numpy()
-    # pairs: row 0, first `nh` heads; grow until the budget is met
+    # pairs: the first `rows` batch rows, first `nh` heads; grow heads, then rows, until the budget is met
     T = w.T
     nh = 1
     sample_desc = ""
@@ -219,11 +219,16 @@ def cpu_baseline(w, x_cpu: dict, budget_s: float = 15.0) -> dict:
             oracle.kda_bwd(*args, f64(x_cpu["dout"][:rows][:, :, heads]), scale=w.scale,
                            lower_bound=w.lower_bound, cu_seqlens=cu, initial_state=S0, nthreads=cores)
         elapsed = time.perf_counter() - t0
-        sample_desc = (f"{'fwd+bwd' if w.backward else 'fwd'} of batch row 0, heads 0..{len(heads) - 1} "
-                       f"({len(heads)} of {heads_total}), all {T} tokens")
-        if elapsed * 2 > budget_s or len(heads) >= heads_total:
+        sample_desc = (f"{'fwd+bwd' if w.backward else 'fwd'} of batch rows 0..{rows - 1} ({rows} of {w.B}), "
+                       f"heads 0..{len(heads) - 1} ({len(heads)} of {heads_total}), all {T} tokens per row")
+        if elapsed * 2 > budget_s:
             break
-        nh = min(heads_total, max(nh * 2, int(nh * budget_s / max(elapsed, 1e-3) * 0.5)))
+        if len(heads) < heads_total:
+            nh = min(heads_total, max(nh * 2, int(nh * budget_s / max(elapsed, 1e-3) * 0.5)))
+        elif rows < w.B and cu is None:
+            rows = min(w.B, max(rows + 1, int(rows * budget_s / max(elapsed, 1e-3) * 0.5)))
+        else:
+            break
     tok_heads = rows * T * len(heads)
     value = tok_heads / heads_total / elapsed          # tokens/s, a token carrying all H heads
     return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample_desc,
