@@ -26,11 +26,13 @@ EXPORTS = ("kda_fwd_workspace_size", "kda_bwd_workspace_size", "kda_fwd", "kda_f
            "kda_kernel_name", "kda_fwd_noalloc", "kda_saved_size", "kda_fwd_save", "kda_bwd_saved",
            "kda_short_conv_fwd", "kda_short_conv_bwd_workspace_size", "kda_short_conv_bwd")
 NOALLOC_SCRATCH_BYTES = 32 << 20
+GATES = {"lower_bounded": 0, "softplus": 1}   # kda_gate
 
 
 class KdaDims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int), ("K", ctypes.c_int),
-                ("V", ctypes.c_int), ("dtype", ctypes.c_int), ("num_seqs", ctypes.c_int), ("Hk", ctypes.c_int)]
+                ("V", ctypes.c_int), ("dtype", ctypes.c_int), ("num_seqs", ctypes.c_int), ("Hk", ctypes.c_int),
+                ("gate", ctypes.c_int)]
 
 
 class KdaError(RuntimeError):
@@ -137,12 +139,19 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported activation dtype {t.dtype} (bf16 or fp32)")
 
 
-def make_dims(q: torch.Tensor, v: torch.Tensor, cu_seqlens: Optional[torch.Tensor]) -> KdaDims:
+def _gate_code(gate: str) -> int:
+    if gate not in GATES:
+        raise ValueError(f"gate must be one of {sorted(GATES)}, got {gate!r}")
+    return GATES[gate]
+
+
+def make_dims(q: torch.Tensor, v: torch.Tensor, cu_seqlens: Optional[torch.Tensor],
+              gate: str = "lower_bounded") -> KdaDims:
     """Shape of a call: q [B, T, Hk, K] (key heads), v [B, T, H, V] (value heads)."""
     B, T, Hk, K = q.shape
     H, V = v.shape[2], v.shape[-1]
     n = int(cu_seqlens.numel() - 1) if cu_seqlens is not None else 0
-    return KdaDims(B, T, H, K, V, _dtype_code(q), n, Hk)
+    return KdaDims(B, T, H, K, V, _dtype_code(q), n, Hk, _gate_code(gate))
 
 
 def _check_shapes(q, k, v, g_raw, beta_raw, a_log, dt_bias):
@@ -191,18 +200,20 @@ def _contig(*ts):
 
 
 def forward(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale: float, lower_bound: float = -5.0,
-            chunk_size: int = 64, cu_seqlens=None, initial_state=None, output_final_state: bool = False,
+            gate: str = "lower_bounded", chunk_size: int = 64, cu_seqlens=None, initial_state=None, output_final_state: bool = False,
             out=None, final_state=None, simt: bool = False, saved: Optional[torch.Tensor] = None,
             stream: Optional[torch.cuda.Stream] = None):
     """KDA forward through ``kda_fwd`` (or ``kda_fwd_simt``).  Returns (out, final_state or None).
 
+    ``gate``: "lower_bounded" (g = lower_bound * sigmoid(exp(a_log) * (g_raw + dt_bias))) or
+    "softplus" (g = -exp(a_log) * softplus(g_raw + dt_bias), unbounded; runs on the SIMT path).
     ``saved``: a device byte buffer of ``saved_size(...)`` bytes; the forward then runs
     ``kda_fwd_save`` and keeps the per-chunk quantities there for ``backward(..., saved=...)``.
     """
     lib = load()
     _contig(q, k, v, g_raw, beta_raw, a_log, dt_bias, cu_seqlens, initial_state)
     _check_shapes(q, k, v, g_raw, beta_raw, a_log, dt_bias)
-    dims = make_dims(q, v, cu_seqlens)
+    dims = make_dims(q, v, cu_seqlens, gate)
     B, T, _, K = q.shape
     H, V = v.shape[2], v.shape[-1]
     N = dims.num_seqs if cu_seqlens is not None else B
@@ -231,15 +242,15 @@ def forward(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale: float, lower_bou
     return out, final_state
 
 
-def saved_size(q, v, cu_seqlens=None, chunk_size: int = 64) -> int:
+def saved_size(q, v, cu_seqlens=None, chunk_size: int = 64, gate: str = "lower_bounded") -> int:
     """Bytes of the buffer ``forward(..., saved=...)`` fills (0: the shape has no saved path)."""
     lib = load()
-    dims = make_dims(q, v, cu_seqlens)
+    dims = make_dims(q, v, cu_seqlens, gate)
     return int(lib.kda_saved_size(ctypes.byref(dims), int(chunk_size)))
 
 
 def backward(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale: float, lower_bound: float = -5.0,
-             chunk_size: int = 64, cu_seqlens=None, initial_state=None, dfinal_state=None,
+             gate: str = "lower_bounded", chunk_size: int = 64, cu_seqlens=None, initial_state=None, dfinal_state=None,
              want_dinitial_state: bool = True, grads: Optional[dict] = None,
              saved: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> dict:
     """KDA backward through ``kda_bwd``.  Returns a dict of fp32 gradients.
@@ -250,7 +261,7 @@ def backward(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale: float, lo
     lib = load()
     _contig(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, cu_seqlens, initial_state, dfinal_state)
     _check_shapes(q, k, v, g_raw, beta_raw, a_log, dt_bias)
-    dims = make_dims(q, v, cu_seqlens)
+    dims = make_dims(q, v, cu_seqlens, gate)
     B, T, Hk, K = q.shape
     H, V = v.shape[2], v.shape[-1]
     N = dims.num_seqs if cu_seqlens is not None else B

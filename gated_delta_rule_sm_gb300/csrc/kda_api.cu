@@ -17,7 +17,7 @@ static constexpr int kGradCtas = 304;  // 2 CTAs per SM on a 152-SM GB300
 static size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Shape {
-    int B, T, H, Hk, G, K, V, N, TT, NCmax, dtype;
+    int B, T, H, Hk, G, K, V, N, TT, NCmax, dtype, gate;
     bool varlen;
 };
 
@@ -27,6 +27,7 @@ static kda_status check_dims(const kda_dims* d, int chunk_size, bool varlen, Sha
     const int Hk = d->Hk > 0 ? d->Hk : d->H;   // 0: one key head per value head
     if (d->Hk < 0 || d->H % Hk) return KDA_ERR_INVALID_ARG;
     if (d->dtype != KDA_BF16 && d->dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
+    if (d->gate != KDA_GATE_LOWER_BOUNDED && d->gate != KDA_GATE_SOFTPLUS) return KDA_ERR_INVALID_ARG;
     if (chunk_size <= 0) return KDA_ERR_INVALID_ARG;
     if (d->K < 16 || d->V < 16) return KDA_ERR_INVALID_ARG;           // head dims below 16 are rejected
     // the chunk size is a blocking choice, not part of the result: 16, 32 and 64 all run the 64-token
@@ -42,6 +43,7 @@ static kda_status check_dims(const kda_dims* d, int chunk_size, bool varlen, Sha
     s->B = d->B; s->T = d->T; s->H = d->H; s->K = d->K; s->V = d->V;
     s->Hk = Hk; s->G = d->H / Hk;
     s->dtype = d->dtype;
+    s->gate = d->gate;
     s->varlen = varlen;
     s->N = varlen ? d->num_seqs : d->B;
     s->TT = (int)TT;
@@ -82,6 +84,10 @@ static WsPlan plan_simt(const Shape& s, bool bwd) {
 
 // Tensor-core path: bf16 activations with K = V = 128.
 static bool tc_eligible(const Shape& s) { return s.dtype == KDA_BF16 && s.K == 128 && s.V == 128; }
+
+// The tensor-core path's 16-token sub-block factorisation of the decay needs the lower-bounded
+// gate with |lower_bound| <= 5 (exp of up to 16 * 5 stays inside fp32 range).
+static bool tc_gate_ok(const Shape& s, float lb) { return s.gate == KDA_GATE_LOWER_BOUNDED && lb >= -5.0f; }
 
 struct TcPlan {
     size_t off_chunk, off_rec, total;
@@ -130,7 +136,7 @@ static Params base_params(const Shape& s, const void* q, const void* k, const vo
     p.Hk = s.Hk; p.G = s.G;
     p.dtype = s.dtype; p.NCmax = s.NCmax;
     p.q = q; p.k = k; p.v = v; p.g_raw = g_raw; p.beta_raw = beta_raw;
-    p.a_log = a_log; p.dt_bias = dt_bias; p.scale = scale; p.lb = lb;
+    p.a_log = a_log; p.dt_bias = dt_bias; p.scale = scale; p.lb = lb; p.gate = s.gate;
     p.cu = cu; p.S0 = S0;
     return p;
 }
@@ -159,7 +165,7 @@ static kda_status common_checks(const kda_dims* dims, int chunk_size, const int3
     kda_status st = check_dims(dims, chunk_size, cu != nullptr, s);
     if (st != KDA_OK) return st;
     if (!q || !k || !v || !g_raw || !beta_raw || !a_log || !dt_bias) return KDA_ERR_INVALID_ARG;
-    if (!(lb < 0.0f) || !isfinite(lb)) return KDA_ERR_INVALID_ARG;   // the gate must be lower-bounded below 0
+    if (!(lb < 0.0f) || !isfinite(lb)) return KDA_ERR_INVALID_ARG;   // lower_bound < 0 under either gate, as the page's executor checks
     if (!isfinite(scale)) return KDA_ERR_INVALID_ARG;
     return KDA_OK;
 }
@@ -280,7 +286,7 @@ static kda_status bwd_tc(const Shape& s, Params p, void* workspace, size_t works
 
 // Bytes of the record kda_fwd_save keeps (0 when the shape does not take the tensor-core path).
 static size_t saved_bytes_for(const Shape& s) {
-    if (!tc_eligible(s)) return 0;
+    if (!tc_eligible(s) || s.gate != KDA_GATE_LOWER_BOUNDED) return 0;
     return sizeof(float) * (size_t)s.NCmax * s.H * RecLayout::make(s.K, s.V).bwd_size;
 }
 
@@ -342,8 +348,8 @@ kda_status kda_fwd(const kda_dims* dims, const void* q, const void* k, const voi
     if (!out) return KDA_ERR_INVALID_ARG;
     Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
                            initial_state);
-    // the tensor-core path needs 16-byte aligned activations and |lower_bound| <= 5
-    if (!tc_eligible(s) || lower_bound < -5.0f || !tc_inputs_aligned(p))
+    // the tensor-core path needs 16-byte aligned activations and a gate it can factorise
+    if (!tc_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p))
         return kda_fwd_simt(dims, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, chunk_size,
                             cu_seqlens, initial_state, out, final_state, workspace, workspace_bytes, stream);
     p.out = out;
@@ -367,7 +373,7 @@ kda_status kda_bwd(const kda_dims* dims, const void* q, const void* k, const voi
     p.dout = dout; p.dST = dfinal_state;
     p.dq = dq; p.dk = dk; p.dv = dv; p.dg_raw = dg_raw; p.dbeta_raw = dbeta_raw;
     p.da_log = da_log; p.ddt_bias = ddt_bias; p.dS0 = dinitial_state;
-    if (tc_eligible(s) && lower_bound >= -5.0f && tc_inputs_aligned(p))
+    if (tc_eligible(s) && tc_gate_ok(s, lower_bound) && tc_inputs_aligned(p))
         return bwd_tc(s, p, workspace, workspace_bytes, stream, nullptr);
     const WsPlan w = plan_simt(s, true);
     st = check_ws(workspace, workspace_bytes, w.total);
@@ -404,7 +410,7 @@ kda_status kda_fwd_save(const kda_dims* dims, const void* q, const void* k, cons
     if (!out) return KDA_ERR_INVALID_ARG;
     Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
                            initial_state);
-    if (!tc_eligible(s) || lower_bound < -5.0f || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
+    if (!tc_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
     const size_t need = saved_bytes_for(s);
     if (!saved || saved_bytes < need || (reinterpret_cast<uintptr_t>(saved) % kAlign)) return KDA_ERR_WORKSPACE;
     p.out = out;
@@ -429,7 +435,7 @@ kda_status kda_bwd_saved(const kda_dims* dims, const void* q, const void* k, con
     p.dout = dout; p.dST = dfinal_state;
     p.dq = dq; p.dk = dk; p.dv = dv; p.dg_raw = dg_raw; p.dbeta_raw = dbeta_raw;
     p.da_log = da_log; p.ddt_bias = ddt_bias; p.dS0 = dinitial_state;
-    if (!tc_eligible(s) || lower_bound < -5.0f || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
+    if (!tc_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
     const size_t need = saved_bytes_for(s);
     if (!saved || saved_bytes < need || (reinterpret_cast<uintptr_t>(saved) % kAlign)) return KDA_ERR_WORKSPACE;
     return bwd_tc(s, p, workspace, workspace_bytes, stream, static_cast<const float*>(saved));

@@ -24,6 +24,7 @@ struct Params {
     const float *a_log, *dt_bias, *S0, *dST;
     const int32_t* cu;          // device cu_seqlens or nullptr
     float scale, lb;
+    int gate;                   // KDA_GATE_LOWER_BOUNDED / KDA_GATE_SOFTPLUS
     void* out;
     float* ST;
     float *dq, *dk, *dv, *dg_raw, *dbeta_raw, *da_log, *ddt_bias, *dS0;
@@ -60,6 +61,14 @@ __device__ __forceinline__ void store_act(void* p, size_t i, float x, int dtype)
 }
 
 __device__ __forceinline__ float sigmoidf_acc(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// log(1 + e^x) without overflow: max(x, 0) + log(1 + e^-|x|)
+__device__ __forceinline__ float softplusf(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
+
+// Log-decay of one gate element (the two gate activations of kda.h).
+__device__ __forceinline__ float gate_value(const Params& p, float ea, float x, float dtb) {
+    return p.gate == KDA_GATE_SOFTPLUS ? -ea * softplusf(x + dtb) : p.lb * sigmoidf_acc(ea * (x + dtb));
+}
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll

@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(256) intra_simt_kernel(Params p) {
         float g = 0.f;
         if (t < ch.len) {
             const float x = load_act(p.g_raw, ((size_t)(ch.tok0 + t) * H + h) * K + cc, p.dtype);
-            g = p.lb * sigmoidf_acc(ea * (x + p.dt_bias[h * K + cc]));
+            g = gate_value(p, ea, x, p.dt_bias[h * K + cc]);
         }
         sG[t * KP + cc] = g;
     }
@@ -424,33 +424,43 @@ __global__ void __launch_bounds__(256) grad_simt_kernel(Params p) {
         for (int i = tid; i < kChunk * K; i += blockDim.x) {
             const int t = i / K, cc = i % K;
             const float gt = G[t * K + cc];
+            // Off-diagonal pairs only: a pair (t, s) carries exp(Gamma_t - Gamma_s), whose derivative
+            // is +x at Gamma_t and -x at Gamma_s.  The diagonal pair's exponent is identically 0, so it
+            // is left out of dGamma (as +x - x its rounding would reach every earlier token through
+            // the cumulative sum, scaled by |g| in d a_log) and added to dq, dk directly.
+            const float dadiag = dA[t * kChunk + t];
             float aq = 0.f, akl = 0.f, akr = 0.f;
-            for (int s = 0; s <= t; ++s) {
+            for (int s = 0; s < t; ++s) {
                 const float e = expf(gt - G[s * K + cc]);
                 aq += dA[t * kChunk + s] * kh[s * K + cc] * e;
-                akl += dL[t * kChunk + s] * kh[s * K + cc] * e;   // dL[t][t] == 0
+                akl += dL[t * kChunk + s] * kh[s * K + cc] * e;
             }
-            for (int t2 = t; t2 < kChunk; ++t2) {
+            for (int t2 = t + 1; t2 < kChunk; ++t2) {
                 const float e = expf(G[t2 * K + cc] - gt);
                 akr += (dA[t2 * kChunk + t] * qh[t2 * K + cc] + dL[t2 * kChunk + t] * kh[t2 * K + cc]) * e;
             }
             const float egt = expf(gt);
             const float egd = expf(G[63 * K + cc] - gt);
             float dgv = qh[i] * aq + kh[i] * akl - kh[i] * akr;
-            dgv += dQg[i] * rec[L.Qg + i] + dKg[i] * rec[L.Kg + i] - dKd[i] * rec[L.Kd + i];
-            dq[i] = aq + dQg[i] * egt;
-            dk[i] = akl + akr + dKg[i] * egt + dKd[i] * egd;
+            dgv += dQg[i] * rec[L.Qg + i] + dKg[i] * rec[L.Kg + i];
+            dq[i] = aq + dadiag * kh[i] + dQg[i] * egt;
+            dk[i] = akl + akr + dadiag * qh[i] + dKg[i] * egt + dKd[i] * egd;
             dG[i] = dgv;
         }
         __syncthreads();
-        // Gamma_last collects dGC and sum_t dKd * Kd; reverse cumsum gives dg
+        // dg_r = sum_{u >= r} dGamma_u (reverse cumulative sum), plus the terms that reach g_r through
+        // Gamma_last: the entering state's decay (dGC, every r) and Kd_t = k_t exp(Gamma_last - Gamma_t),
+        // whose exponent holds g_r for t < r only (an exclusive prefix sum, so no +x - x cancellation)
         for (int cc = tid; cc < K; cc += blockDim.x) {
-            float s = s_dgc[cc];
-            for (int t = 0; t < kChunk; ++t) s += dKd[t * K + cc] * rec[L.Kd + t * K + cc];
-            float run = s;
+            float run = 0.f;
             for (int t = kChunk - 1; t >= 0; --t) {
                 run += dG[t * K + cc];
                 dG[t * K + cc] = run;
+            }
+            float pre = s_dgc[cc];
+            for (int t = 0; t < kChunk; ++t) {
+                dG[t * K + cc] += pre;
+                pre += dKd[t * K + cc] * rec[L.Kd + t * K + cc];
             }
         }
         __syncthreads();
@@ -480,12 +490,22 @@ __global__ void __launch_bounds__(256) grad_simt_kernel(Params p) {
             float dtb = 0.f;
             for (int t = 0; t < ch.len; ++t) {
                 const size_t gi = ((size_t)(ch.tok0 + t) * H + h) * K + cc;
-                const float z = ea * (load_act(p.g_raw, gi, p.dtype) + p.dt_bias[h * K + cc]);
-                const float sg = sigmoidf_acc(z);
-                const float dz = dG[t * K + cc] * p.lb * sg * (1.f - sg);
-                p.dg_raw[gi] = dz * ea;
-                dtb += dz * ea;
-                alog_part += dz * z;
+                const float x = load_act(p.g_raw, gi, p.dtype) + p.dt_bias[h * K + cc];
+                if (p.gate == KDA_GATE_SOFTPLUS) {
+                    // g = -e^a softplus(x): dg/dx = -e^a sigmoid(x), dg/da = g
+                    const float dx = -dG[t * K + cc] * ea * sigmoidf_acc(x);
+                    p.dg_raw[gi] = dx;
+                    dtb += dx;
+                    alog_part -= dG[t * K + cc] * ea * softplusf(x);
+                } else {
+                    // g = lb sigmoid(z), z = e^a x: dg/dx = lb sigma'(z) e^a, dg/da = lb sigma'(z) z
+                    const float z = ea * x;
+                    const float sg = sigmoidf_acc(z);
+                    const float dz = dG[t * K + cc] * p.lb * sg * (1.f - sg);
+                    p.dg_raw[gi] = dz * ea;
+                    dtb += dz * ea;
+                    alog_part += dz * z;
+                }
             }
             p.part_dtb[((size_t)c * H + h) * K + cc] = dtb;
         }

@@ -30,6 +30,8 @@ def main(argv=None) -> None:
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--fwd-only", action="store_true", help="skip the backward of a fwd+bwd workload")
     ap.add_argument("--saved", action="store_true", help="forward keeps the per-chunk record for the backward")
+    ap.add_argument("--gate", default="lower_bounded", choices=("lower_bounded", "softplus"),
+                    help="gate activation (softplus: the unbounded gate, SIMT path)")
     ap.add_argument("--short-conv", type=int, default=0, metavar="W",
                     help="instead time the W-tap short convolution + SiLU prologue on a q-shaped [B, T, H*K] tensor")
     a = ap.parse_args(argv)
@@ -45,12 +47,12 @@ def main(argv=None) -> None:
         return
     x = make_inputs(w, device=dev)
     names = ("q", "k", "v", "g_raw", "beta_raw", "a_log", "dt_bias")
-    kw = dict(scale=x["scale"], lower_bound=x["lower_bound"], chunk_size=x["chunk_size"],
+    kw = dict(scale=x["scale"], lower_bound=x["lower_bound"], gate=a.gate, chunk_size=x["chunk_size"],
               cu_seqlens=x["cu_seqlens"], initial_state=x["initial_state"])
     run_bwd = w.backward and not a.fwd_only
     saved = None
     if run_bwd and a.saved:
-        nb = saved_size(x["q"], x["v"], x["cu_seqlens"], x["chunk_size"])
+        nb = saved_size(x["q"], x["v"], x["cu_seqlens"], x["chunk_size"], a.gate)
         if nb == 0:
             raise SystemExit("this workload has no saved-record path")
         saved = torch.empty(nb, dtype=torch.uint8, device=dev)
@@ -63,7 +65,8 @@ def main(argv=None) -> None:
             backward(*[x[n] for n in names], x["dout"], saved=saved, **kw)
     ev[1].record()
     torch.cuda.synchronize()
-    print(f"workload={w.name} B={w.B} T={w.T} H={w.H} bwd={run_bwd} saved={saved is not None} iters={a.iters} "
+    print(f"workload={w.name} B={w.B} T={w.T} H={w.H} gate={a.gate} bwd={run_bwd} saved={saved is not None} "
+          f"iters={a.iters} "
           f"ms_per_iter={ev[0].elapsed_time(ev[1]) / max(1, a.iters):.3f}")
 
 

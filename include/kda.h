@@ -15,7 +15,11 @@
  *     g     = lower_bound * sigmoid(exp(a_log_h) * (g_raw + dt_bias_{h,c})),  alpha = exp(g)
  * (hyper-parallel "KDA context-parallel executors", `_run_local_kda`: the
  * fused backend requires this lower-bounded gate; the exact formula is not
- * printed on the pages and is this library's reading).
+ * printed on the pages and is this library's reading).  The same page keeps a
+ * second, unbounded gate behind `safe_gate=False` (and the torchtitan note
+ * checks "both gate activations"); selected by kda_dims.gate, it is read as
+ *     g     = -exp(a_log_h) * softplus(g_raw + dt_bias_{h,c})
+ * (again unprinted; the plainest unbounded form over the same ingredients).
  *
  * Layouts follow `_validate_projected_inputs` on the same page (token-first,
  * contiguous, row-major); H counts value heads and Hk key heads:
@@ -73,15 +77,23 @@ typedef enum {
 
 typedef enum { KDA_BF16 = 0, KDA_FP32 = 1 } kda_dtype;
 
+/* Gate activation (the page's `safe_gate` switch).  KDA_GATE_LOWER_BOUNDED, the
+ * default: g = lower_bound * sigmoid(exp(a_log) * (g_raw + dt_bias)), so g lies in
+ * (lower_bound, 0).  KDA_GATE_SOFTPLUS: g = -exp(a_log) * softplus(g_raw + dt_bias),
+ * unbounded below; lower_bound is still validated (< 0, finite) but not used. */
+typedef enum { KDA_GATE_LOWER_BOUNDED = 0, KDA_GATE_SOFTPLUS = 1 } kda_gate;
+
 /* Problem shape.  num_seqs is the number of packed segments N when
  * cu_seqlens is given (then B == 1) and is ignored otherwise (N = B).
  * H = value heads; Hk = key heads (q, k), H a multiple of Hk, 0 meaning Hk = H;
- * H % Hk != 0 or Hk < 0 is KDA_ERR_INVALID_ARG. */
+ * H % Hk != 0 or Hk < 0 is KDA_ERR_INVALID_ARG.  gate: zero-initialised means
+ * the lower-bounded gate; a value outside kda_gate is KDA_ERR_INVALID_ARG. */
 typedef struct {
     int B, T, H, K, V;
     kda_dtype dtype;
     int num_seqs;
     int Hk;
+    kda_gate gate;
 } kda_dims;
 
 /* Bytes of workspace kda_fwd / kda_bwd need for this shape (0 on invalid input). */
@@ -98,10 +110,12 @@ size_t kda_bwd_workspace_size(const kda_dims* dims, int chunk_size);
  * rounding with any chunk size.
  * Requirements: B,T,H >= 1; 16 <= K,V <= 128 and multiples of 16 (the pages
  * reject head dims below 16); N >= 1.  bf16 with K == V == 128, 16-byte
- * aligned q, k, v, g_raw (and dout for kda_bwd) and lower_bound >= -5 runs
- * on the tcgen05 tensor-core path (its 16-token sub-block factorisation of
- * the decay stays inside fp32 range only for |lower_bound| <= 5); every other
- * supported shape (and fp32 inputs) runs on the fp32 SIMT path.
+ * aligned q, k, v, g_raw (and dout for kda_bwd), the lower-bounded gate and
+ * lower_bound >= -5 runs on the tcgen05 tensor-core path (its 16-token
+ * sub-block factorisation of the decay stays inside fp32 range only for
+ * |lower_bound| <= 5); every other supported shape, fp32 inputs and the
+ * unbounded gate run on the fp32 SIMT path, which forms every decay as
+ * exp(Gamma_t - Gamma_s) <= 1 and so holds for any gate.
  */
 kda_status kda_fwd(const kda_dims* dims,
                    const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,

@@ -13,11 +13,12 @@ marshals numpy float64 arrays through ctypes.
 Parity status: the recurrence, the L2 norm, sigmoid(beta), state I/O,
 packed documents, grouped key heads, the backward pass and the short
 convolution + SiLU prologue are pinned by the tests in
-``tests/test_oracle_pins.py``.  The gate formula
-``g = lower_bound * sigmoid(exp(a_log) * (g_raw + dt_bias))`` and the
-L2-norm epsilon (1e-6) are readings of pages that print neither:
-parity unpinned for those two choices (the tests pin only their limits and
-special values).
+``tests/test_oracle_pins.py``.  The gate formulas
+``g = lower_bound * sigmoid(exp(a_log) * (g_raw + dt_bias))`` and, for the
+unbounded gate, ``g = -exp(a_log) * softplus(g_raw + dt_bias)``, and the
+L2-norm epsilon (1e-6) are readings of pages that print none of them:
+parity unpinned for those choices (the tests pin only their limits and
+special values, and the gradients through them by finite differences).
 """
 from __future__ import annotations
 
@@ -58,11 +59,11 @@ def _load():
         if _lib is None:
             lib = ctypes.CDLL(build())
             lib.oracle_gate_value.restype = ctypes.c_double
-            lib.oracle_gate_value.argtypes = [ctypes.c_double] * 4
+            lib.oracle_gate_value.argtypes = [ctypes.c_double] * 4 + [ctypes.c_int]
             lib.oracle_recurrence.restype = ctypes.c_int
             lib.oracle_recurrence.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                               _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_double, _dp, _dp]
-            common = [ctypes.c_int] * 7 + [_ip] + [_dp] * 7 + [ctypes.c_double, ctypes.c_double, _dp]
+            common = [ctypes.c_int] * 7 + [_ip] + [_dp] * 7 + [ctypes.c_double, ctypes.c_double, ctypes.c_int, _dp]
             lib.oracle_kda_fwd.restype = ctypes.c_int
             lib.oracle_kda_fwd.argtypes = common + [_dp, _dp, ctypes.c_int]
             lib.oracle_kda_bwd.restype = ctypes.c_int
@@ -97,9 +98,23 @@ def default_threads() -> int:
     return os.cpu_count() or 1
 
 
-def gate(g_raw, a_log, dt_bias, lower_bound):
-    """Elementwise lower-bounded gate (scalar inputs)."""
-    return _load().oracle_gate_value(float(g_raw), float(a_log), float(dt_bias), float(lower_bound))
+GATES = {"lower_bounded": 0, "softplus": 1}
+
+
+def _gate_kind(gate):
+    if gate not in GATES:
+        raise ValueError(f"gate must be one of {sorted(GATES)}, got {gate!r}")
+    return GATES[gate]
+
+
+def gate(g_raw, a_log, dt_bias, lower_bound, kind="lower_bounded"):
+    """Log-decay g of one gate element (scalar inputs).
+
+    kind "lower_bounded": g = lower_bound * sigmoid(exp(a_log) * (g_raw + dt_bias));
+    kind "softplus": g = -exp(a_log) * softplus(g_raw + dt_bias) (lower_bound unused).
+    """
+    return _load().oracle_gate_value(float(g_raw), float(a_log), float(dt_bias), float(lower_bound),
+                                     _gate_kind(kind))
 
 
 def recurrence(q_hat, k_hat, v, g, beta, scale, S0=None):
@@ -120,12 +135,13 @@ def recurrence(q_hat, k_hat, v, g, beta, scale, S0=None):
     return out, ST
 
 
-def kda_fwd(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale, lower_bound,
+def kda_fwd(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale, lower_bound, gate="lower_bounded",
             cu_seqlens=None, initial_state=None, output_final_state=True, nthreads=0):
     """Full forward.  q, k: [B, T, Hk, K]; g_raw: [B, T, H, K]; v: [B, T, H, V]; beta_raw: [B, T, H].
 
     H counts value heads, Hk key heads (H a multiple of Hk; value head h reads key head
     h // (H // Hk)).  With ``cu_seqlens`` (B must be 1) every segment is its own recurrence.
+    ``gate`` selects the gate activation (see :func:`gate`).
     Returns (out [B, T, H, V], final_state [N, H, K, V] or None).
     """
     q, k, v, g_raw, beta_raw, a_log, dt_bias, S0 = map(
@@ -140,13 +156,13 @@ def kda_fwd(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale, lower_bound,
     fs = np.zeros((N, H, K, V)) if output_final_state else None
     rc = _load().oracle_kda_fwd(B, T, H, Hk, K, V, N, cu_p, _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
                                 _ptr(beta_raw), _ptr(a_log), _ptr(dt_bias), float(scale),
-                                float(lower_bound), _ptr(S0), _ptr(out), _ptr(fs), int(nthreads))
+                                float(lower_bound), _gate_kind(gate), _ptr(S0), _ptr(out), _ptr(fs), int(nthreads))
     if rc:
         raise MemoryError("oracle_kda_fwd failed")
     return out, fs
 
 
-def kda_bwd(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale, lower_bound,
+def kda_bwd(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale, lower_bound, gate="lower_bounded",
             cu_seqlens=None, initial_state=None, dfinal_state=None, nthreads=0):
     """Reverse mode of :func:`kda_fwd`.
 
@@ -166,7 +182,7 @@ def kda_bwd(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale, lower_boun
                da_log=np.zeros(H), ddt_bias=np.zeros(H * K), dinitial_state=np.zeros((N, H, K, V)))
     rc = _load().oracle_kda_bwd(B, T, H, Hk, K, V, N, cu_p, _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
                                 _ptr(beta_raw), _ptr(a_log), _ptr(dt_bias), float(scale),
-                                float(lower_bound), _ptr(S0), _ptr(dout), _ptr(dST),
+                                float(lower_bound), _gate_kind(gate), _ptr(S0), _ptr(dout), _ptr(dST),
                                 _ptr(res["dq"]), _ptr(res["dk"]), _ptr(res["dv"]),
                                 _ptr(res["dg_raw"]), _ptr(res["dbeta_raw"]), _ptr(res["da_log"]),
                                 _ptr(res["ddt_bias"]), _ptr(res["dinitial_state"]), int(nthreads))

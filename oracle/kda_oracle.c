@@ -26,6 +26,12 @@
  *         alpha = exp(g)
  *     The pages name these ingredients but never print the formula; this is
  *     the plainest reading that uses all three and keeps g in (lower_bound, 0).
+ *   - the unbounded gate the same page keeps behind `safe_gate=False` (the
+ *     torchtitan note checks "both gate activations"), gate kind 1:
+ *         g     = -exp(a_log_h) * softplus(g_raw + dt_bias_{h,c})
+ *     Also unprinted: the plainest form over the same ingredients that keeps
+ *     g < 0 without a lower bound (a_log as a log-rate, dt_bias as the bias
+ *     of a softplus step size).  lower_bound is then unused.
  *
  * Packed documents: nemo_automodel `kimi_k3.cp` ("segment_cu_seqlens",
  * "doc_ids_from_cu_seqlens"): every [cu[n], cu[n+1]) segment is its own
@@ -57,6 +63,11 @@
 #define ORACLE_CKPT 64
 
 static double sigm(double x) { return 1.0 / (1.0 + exp(-x)); }
+/* log(1 + e^x), written so that neither branch overflows */
+static double softplus(double x) { return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x)); }
+
+#define ORACLE_GATE_LOWER_BOUNDED 0
+#define ORACLE_GATE_SOFTPLUS 1
 
 /* Segment boundaries: the caller's cu_seqlens, else B rows of T tokens. */
 static int64_t seg_begin(const int32_t* cu, int T, int n) { return cu ? (int64_t)cu[n] : (int64_t)n * T; }
@@ -64,9 +75,10 @@ static int64_t seg_end(const int32_t* cu, int T, int n) { return cu ? (int64_t)c
 
 /* ---- prologue --------------------------------------------------------- */
 
-/* Lower-bounded gate, one element (the reading stated in the header). */
-double oracle_gate_value(double g_raw, double a_log, double dt_bias, double lower_bound)
+/* Gate, one element, of either kind (the readings stated in the header). */
+double oracle_gate_value(double g_raw, double a_log, double dt_bias, double lower_bound, int gate)
 {
+    if (gate == ORACLE_GATE_SOFTPLUS) return -exp(a_log) * softplus(g_raw + dt_bias);
     double z = exp(a_log) * (g_raw + dt_bias);
     return lower_bound * sigm(z);
 }
@@ -76,7 +88,7 @@ double oracle_gate_value(double g_raw, double a_log, double dt_bias, double lowe
  * head h / (H / Hk). */
 static void prologue(int64_t t0, int64_t L, int h, int H, int Hk, int K,
                      const double* q, const double* k, const double* g_raw, const double* beta_raw,
-                     const double* a_log, const double* dt_bias, double lb,
+                     const double* a_log, const double* dt_bias, double lb, int gate,
                      double* qh, double* kh, double* g, double* beta, double* rq, double* rk)
 {
     const int hk = h / (H / Hk);
@@ -92,7 +104,7 @@ static void prologue(int64_t t0, int64_t L, int h, int H, int Hk, int K,
         for (int c = 0; c < K; ++c) {
             qh[i * K + c] = qi[c] * rq[i];
             kh[i * K + c] = ki[c] * rk[i];
-            g[i * K + c] = oracle_gate_value(g_raw[row * K + c], a_log[h], dt_bias[h * K + c], lb);
+            g[i * K + c] = oracle_gate_value(g_raw[row * K + c], a_log[h], dt_bias[h * K + c], lb, gate);
         }
         beta[i] = sigm(beta_raw[row]);
     }
@@ -147,7 +159,7 @@ int oracle_recurrence(int64_t L, int K, int V, const double* qh, const double* k
 int oracle_kda_fwd(int B, int T, int H, int Hk, int K, int V, int num_seqs, const int32_t* cu_seqlens,
                    const double* q, const double* k, const double* v, const double* g_raw,
                    const double* beta_raw, const double* a_log, const double* dt_bias,
-                   double scale, double lower_bound, const double* initial_state,
+                   double scale, double lower_bound, int gate, const double* initial_state,
                    double* out, double* final_state, int nthreads)
 {
     const int N = cu_seqlens ? num_seqs : B;
@@ -174,7 +186,7 @@ int oracle_kda_fwd(int B, int T, int H, int Hk, int K, int V, int num_seqs, cons
         if (!qh || !kh || !g || !beta || !rq || !rk || !S || !w || !vv || !o) {
             err |= 1;
         } else {
-            prologue(t0, L, h, H, Hk, K, q, k, g_raw, beta_raw, a_log, dt_bias, lower_bound,
+            prologue(t0, L, h, H, Hk, K, q, k, g_raw, beta_raw, a_log, dt_bias, lower_bound, gate,
                      qh, kh, g, beta, rq, rk);
             if (initial_state)
                 memcpy(S, initial_state + ((size_t)n * H + h) * K * V, sizeof(double) * (size_t)K * V);
@@ -197,7 +209,7 @@ int oracle_kda_fwd(int B, int T, int H, int Hk, int K, int V, int num_seqs, cons
 int oracle_kda_bwd(int B, int T, int H, int Hk, int K, int V, int num_seqs, const int32_t* cu_seqlens,
                    const double* q, const double* k, const double* v, const double* g_raw,
                    const double* beta_raw, const double* a_log, const double* dt_bias,
-                   double scale, double lower_bound, const double* initial_state,
+                   double scale, double lower_bound, int gate, const double* initial_state,
                    const double* dout, const double* dfinal_state,
                    double* dq, double* dk, double* dv, double* dg_raw, double* dbeta_raw,
                    double* da_log, double* ddt_bias, double* dinitial_state, int nthreads)
@@ -253,7 +265,7 @@ int oracle_kda_bwd(int B, int T, int H, int Hk, int K, int V, int num_seqs, cons
             err |= 1;
             goto done;
         }
-        prologue(t0, L, h, H, Hk, K, q, k, g_raw, beta_raw, a_log, dt_bias, lower_bound,
+        prologue(t0, L, h, H, Hk, K, q, k, g_raw, beta_raw, a_log, dt_bias, lower_bound, gate,
                  qh, kh, g, beta, rq, rk);
         if (initial_state) memcpy(S, initial_state + ((size_t)n * H + h) * KV, sizeof(double) * KV);
         /* forward sweep: remember the state entering every 64-token block */
@@ -356,12 +368,22 @@ int oracle_kda_bwd(int B, int T, int H, int Hk, int K, int V, int num_seqs, cons
             dbeta_raw[row] = dbeta[i] * beta[i] * (1.0 - beta[i]);
             const double ea = exp(a_log[h]);
             for (int c = 0; c < K; ++c) {
-                const double z = ea * (g_raw[row * K + c] + dt_bias[h * K + c]);
-                const double s = sigm(z);
-                const double dz = dg[i * K + c] * lower_bound * s * (1.0 - s);
-                dg_raw[row * K + c] = dz * ea;
-                pd[(size_t)p * K + c] += dz * ea;
-                pa[p] += dz * z;
+                const double x = g_raw[row * K + c] + dt_bias[h * K + c];
+                if (gate == ORACLE_GATE_SOFTPLUS) {
+                    /* g = -e^a softplus(x):  dg/dx = -e^a sigmoid(x),  dg/da = g */
+                    const double dx = -dg[i * K + c] * ea * sigm(x);
+                    dg_raw[row * K + c] = dx;
+                    pd[(size_t)p * K + c] += dx;
+                    pa[p] += dg[i * K + c] * g[i * K + c];
+                } else {
+                    /* g = lb sigmoid(z), z = e^a x:  dg/dz = lb s (1 - s) */
+                    const double z = ea * x;
+                    const double s = sigm(z);
+                    const double dz = dg[i * K + c] * lower_bound * s * (1.0 - s);
+                    dg_raw[row * K + c] = dz * ea;
+                    pd[(size_t)p * K + c] += dz * ea;
+                    pa[p] += dz * z;
+                }
             }
         }
     done:

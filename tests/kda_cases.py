@@ -76,7 +76,7 @@ def oracle_fwd(x: dict, rows=None):
             xs["initial_state"] = xs["initial_state"][rows]
     cu = f64(xs["cu_seqlens"]).astype(np.int64) if xs.get("cu_seqlens") is not None else None
     return oracle.kda_fwd(*[f64(xs[n]) for n in ACT], scale=xs["scale"], lower_bound=xs["lower_bound"],
-                          cu_seqlens=cu, initial_state=f64(xs.get("initial_state")))
+                          gate=xs.get("gate", "lower_bounded"), cu_seqlens=cu, initial_state=f64(xs.get("initial_state")))
 
 
 def oracle_bwd(x: dict, rows=None, dfinal=None):
@@ -92,19 +92,20 @@ def oracle_bwd(x: dict, rows=None, dfinal=None):
             dfinal = dfinal[rows]
     cu = f64(xs["cu_seqlens"]).astype(np.int64) if xs.get("cu_seqlens") is not None else None
     return oracle.kda_bwd(*[f64(xs[n]) for n in ACT], f64(xs["dout"]), scale=xs["scale"],
-                          lower_bound=xs["lower_bound"], cu_seqlens=cu, initial_state=f64(xs.get("initial_state")),
+                          lower_bound=xs["lower_bound"], gate=xs.get("gate", "lower_bounded"), cu_seqlens=cu,
+                          initial_state=f64(xs.get("initial_state")),
                           dfinal_state=f64(dfinal))
 
 
 def gpu_fwd(x: dict, simt=False, final=True):
     import gated_delta_rule_sm_gb300 as kda
     return kda.forward(*[x[n] for n in ACT], scale=x["scale"], lower_bound=x["lower_bound"],
-                       chunk_size=x.get("chunk_size", 64), cu_seqlens=x.get("cu_seqlens"),
+                       gate=x.get("gate", "lower_bounded"), chunk_size=x.get("chunk_size", 64), cu_seqlens=x.get("cu_seqlens"),
                        initial_state=x.get("initial_state"), output_final_state=final, simt=simt)
 
 
 def gpu_bwd(x: dict, dfinal=None):
     import gated_delta_rule_sm_gb300 as kda
     return kda.backward(*[x[n] for n in ACT], x["dout"], scale=x["scale"], lower_bound=x["lower_bound"],
-                        chunk_size=x.get("chunk_size", 64), cu_seqlens=x.get("cu_seqlens"),
+                        gate=x.get("gate", "lower_bounded"), chunk_size=x.get("chunk_size", 64), cu_seqlens=x.get("cu_seqlens"),
                         initial_state=x.get("initial_state"), dfinal_state=dfinal)

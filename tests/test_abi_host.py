@@ -161,6 +161,23 @@ def test_grouped_key_heads_validation(lib):
     assert _fwd(lib, _dims(H=4, Hk=2), ws=None, ws_bytes=0) == _lib.KDA_ERR_WORKSPACE   # valid shape
 
 
+def test_gate_selection_validation(lib):
+    """kda_dims.gate: 0 (lower-bounded, the zero-initialised default) or 1 (softplus); else invalid."""
+    SP = _lib.GATES["softplus"]
+    assert _fwd(lib, _dims(gate=2)) == _lib.KDA_ERR_INVALID_ARG
+    assert _fwd(lib, _dims(gate=-1)) == _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_fwd_workspace_size(ctypes.byref(_dims(gate=2)), 64) == 0
+    assert _fwd(lib, _dims(gate=SP)) == _lib.KDA_ERR_WORKSPACE               # valid: stops at the workspace
+    assert _fwd(lib, _dims(gate=SP), lb=0.0) == _lib.KDA_ERR_INVALID_ARG     # lower_bound checked under either gate
+    f = lambda **kw: lib.kda_fwd_workspace_size(ctypes.byref(_dims(**kw)), 64)
+    assert f(gate=SP) == f() > 0
+    # the unbounded gate has no tensor-core path: no saved context, and the saved pair refuses it
+    d128 = _dims(K=128, V=128, gate=SP)
+    assert lib.kda_saved_size(ctypes.byref(d128), 64) == 0
+    assert _fwd_save(lib, d128) == _lib.KDA_ERR_UNSUPPORTED
+    assert _bwd_saved(lib, d128) == _lib.KDA_ERR_UNSUPPORTED
+
+
 def _conv_fwd(lib, B=1, T=64, C=64, W=4, dtype=_lib.KDA_BF16, ptr=16, cu=None, n=0, y=16):
     p = ctypes.c_void_p(ptr) if ptr else None
     yp = ctypes.c_void_p(y) if y else None

@@ -30,6 +30,10 @@ MUTATIONS = [
     ("beta gradient misses the sigmoid slope", "dbeta_raw[row] = dbeta[i] * beta[i] * (1.0 - beta[i]);",
      "dbeta_raw[row] = dbeta[i] * beta[i];"),
     ("key heads interleaved instead of grouped", "const int hk = h / (H / Hk);", "const int hk = h % Hk;"),
+    ("softplus gate sign", "return -exp(a_log) * softplus(g_raw + dt_bias);",
+     "return exp(a_log) * softplus(g_raw + dt_bias);"),
+    ("softplus gate gradient misses the sigmoid", "const double dx = -dg[i * K + c] * ea * sigm(x);",
+     "const double dx = -dg[i * K + c] * ea;"),
     ("convolution taps reversed", "if (tau >= s0) a += w[c * W + i] * x[tau * C + c];",
      "if (tau >= s0) a += w[c * W + (W - 1 - i)] * x[tau * C + c];"),
 ]
@@ -48,7 +52,10 @@ def _battery():
         pins.test_prologue_invariances,
         pins.test_affine_in_initial_state,
         pins.test_document_isolation,
-        lambda: pins.test_backward_matches_central_differences(False),
+        lambda: pins.backward_central_differences(False),
+        pins.test_softplus_gate_limits_and_special_values,
+        pins.test_softplus_gate_full_path_equals_recurrence,
+        lambda: pins.backward_central_differences(False, "softplus"),
         pins.test_grouped_heads_equal_repeated_keys,
         pins.test_grouped_heads_backward_central_differences,
         lambda: pins.test_short_conv_matches_numpy_convolve(4),

@@ -144,6 +144,44 @@ def test_gate_limits_and_special_values():
     assert abs(oracle.gate(0.5, 2.0, 0.0, lb) - lb / 2) > abs(oracle.gate(0.5, 0.0, 0.0, lb) - lb / 2)
 
 
+def test_softplus_gate_limits_and_special_values():
+    """The unbounded gate g = -exp(a_log) * softplus(g_raw + dt_bias)."""
+    sp = lambda x, a, d: oracle.gate(x, a, d, -5.0, "softplus")
+    for a, d in [(0.0, 0.0), (math.log(16), 0.1), (1.3, -0.2)]:
+        assert sp(-d, a, d) == pytest.approx(-math.exp(a) * math.log(2), rel=1e-15)   # softplus(0) = ln 2
+        assert sp(-800.0, a, d) == 0.0                                               # alpha = 1 exactly
+        assert sp(60.0, a, d) == pytest.approx(-math.exp(a) * (60.0 + d), rel=1e-15)  # linear for large x
+        for x in rng0.standard_normal(20) * 3:
+            assert sp(x, a, d) < 0
+            assert sp(x, a, d) == oracle.gate(x, a, d, -0.1, "softplus")   # lower_bound is not used
+    # unbounded below: far past any lower bound
+    assert sp(100.0, math.log(16), 0.0) == pytest.approx(-1600.0, rel=1e-12)
+    # a_log = 0, dt_bias = 0 reduces to -softplus(g_raw): numpy's log(e^0 + e^x)
+    for x in np.linspace(-30, 30, 61):
+        assert sp(x, 0.0, 0.0) == pytest.approx(-np.logaddexp(0.0, x), rel=1e-14, abs=1e-300)
+    xs = np.linspace(-3, 3, 50)
+    assert np.all(np.diff([sp(x, 1.0, 0.0) for x in xs]) < 0)
+    with pytest.raises(ValueError):
+        oracle.gate(0.0, 0.0, 0.0, -5.0, "relu")
+
+
+def test_softplus_gate_full_path_equals_recurrence():
+    """With gate="softplus" the full path is the bare recurrence on the numpy-computed decay."""
+    d, S0 = _full_inputs(seed=4)
+    out, fs = oracle.kda_fwd(**d, initial_state=S0, scale=0.5, lower_bound=-5.0, gate="softplus")
+    B, T, H, K = d["q"].shape
+    for h in range(H):
+        qh = d["q"][0, :, h] / np.sqrt((d["q"][0, :, h] ** 2).sum(-1, keepdims=True) + 1e-6)
+        kh = d["k"][0, :, h] / np.sqrt((d["k"][0, :, h] ** 2).sum(-1, keepdims=True) + 1e-6)
+        g = -np.exp(d["a_log"][h]) * np.logaddexp(0.0, d["g_raw"][0, :, h] + d["dt_bias"][h * K:(h + 1) * K])
+        o, S = oracle.recurrence(qh, kh, d["v"][0, :, h], g, expit(d["beta_raw"][0, :, h]), 0.5, S0[0, h])
+        np.testing.assert_allclose(out[0, :, h], o, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(fs[0, h], S, rtol=1e-12, atol=1e-13)
+    # and it differs from the lower-bounded gate on the same logits
+    out_lb, _ = oracle.kda_fwd(**d, initial_state=S0, scale=0.5, lower_bound=-5.0)
+    assert np.abs(out - out_lb).max() > 1e-3
+
+
 def _full_inputs(B=1, T=20, H=2, K=4, V=3, seed=0, state=True):
     r = np.random.default_rng(seed)
     d = dict(q=r.standard_normal((B, T, H, K)), k=r.standard_normal((B, T, H, K)),
@@ -232,8 +270,13 @@ def _loss(res_out, res_fs, dout, dfs):
     return float(np.sum(res_out * dout) + np.sum(res_fs * dfs))
 
 
+@pytest.mark.parametrize("gate", ["lower_bounded", "softplus"])
 @pytest.mark.parametrize("varlen", [False, True])
-def test_backward_matches_central_differences(varlen):
+def test_backward_matches_central_differences(varlen, gate):
+    backward_central_differences(varlen, gate)
+
+
+def backward_central_differences(varlen, gate="lower_bounded"):
     if varlen:
         lens = [3, 5, 2]
         cu = np.concatenate([[0], np.cumsum(lens)])
@@ -245,7 +288,7 @@ def test_backward_matches_central_differences(varlen):
     r = np.random.default_rng(15)
     dout = r.standard_normal(d["v"].shape)
     dfs = r.standard_normal(S0.shape)
-    kw = dict(scale=0.6, lower_bound=-4.0, cu_seqlens=cu)
+    kw = dict(scale=0.6, lower_bound=-4.0, gate=gate, cu_seqlens=cu)
     grads = oracle.kda_bwd(**d, dout=dout, initial_state=S0, dfinal_state=dfs, **kw)
 
     def L(dd, S):

@@ -320,3 +320,48 @@ def test_smaller_chunk_sizes_match_the_oracle(chunk):
     assert x["chunk_size"] == chunk
     _check_fwd(x, "bf16")
     _check_bwd(x, "bf16")
+
+
+# ------------------------------------------------------------------ the unbounded (softplus) gate
+
+def _softplus_case(lengths=None, **kw):
+    x = make_inputs(Workload("t", **kw), device=DEV, lengths=lengths)
+    x["gate"] = "softplus"
+    return x
+
+
+def test_softplus_gate_fp32_fwd_bwd():
+    x = _softplus_case(B=2, T=200, H=2, K=64, V=64, dtype="fp32", initial_state=True, backward=True, seed=60)
+    _check_fwd(x, "fp32")
+    _check_bwd(x, "fp32")
+
+
+def test_softplus_gate_bf16_d128_varlen_fwd_bwd():
+    """bf16 K = V = 128 with the unbounded gate runs on the SIMT path (no tensor-core factorisation)."""
+    import gated_delta_rule_sm_gb300 as kda
+    x = _softplus_case(B=1, T=400, H=2, K=128, V=128, varlen=True, initial_state=True, backward=True, seed=61,
+                       lengths=[90, 1, 64, 200, 45])
+    _check_fwd(x, "bf16")
+    _check_bwd(x, "bf16")
+    assert kda.saved_size(x["q"], x["v"], x["cu_seqlens"], gate="softplus") == 0
+    with pytest.raises(kda.KdaError):
+        buf = torch.empty(1 << 20, dtype=torch.uint8, device=DEV)
+        kda.forward(*[x[n] for n in ("q", "k", "v", "g_raw", "beta_raw", "a_log", "dt_bias")], scale=x["scale"],
+                    gate="softplus", cu_seqlens=x["cu_seqlens"], saved=buf)
+
+
+def test_softplus_gate_mild_long_memory():
+    """g_raw ~ N(-6, 1): softplus ~ 2.5e-3, so the state keeps its memory over hundreds of tokens."""
+    x = _softplus_case(B=1, T=700, H=2, K=128, V=128, initial_state=True, backward=True, g_mean=-6.0, seed=62)
+    _check_fwd(x, "bf16")
+    _check_bwd(x, "bf16")
+
+
+def test_softplus_gate_steep_decay_underflows_cleanly():
+    """g_raw ~ N(4, 1) with a_log up to ln 16: g near -64 per token, so exp(Gamma) underflows to 0
+    within a chunk; every decay is formed as exp(Gamma_t - Gamma_s) <= 1 and stays finite."""
+    x = _softplus_case(B=1, T=300, H=2, K=64, V=64, dtype="fp32", initial_state=True, backward=True, g_mean=4.0,
+                       seed=63)
+    out, fs = _check_fwd(x, "fp32")
+    assert torch.isfinite(out).all() and torch.isfinite(fs).all()
+    _check_bwd(x, "fp32")
