@@ -86,11 +86,13 @@ static WsPlan plan_simt(const Shape& s, bool bwd) {
 static bool tc_eligible(const Shape& s) { return s.dtype == KDA_BF16 && s.K == 128 && s.V == 128; }
 
 // The tensor-core path's 16-token sub-block factorisation of the decay needs the lower-bounded
-// gate with |lower_bound| <= 5 (exp of up to 16 * 5 stays inside fp32 range).
+// gate with |lower_bound| <= 5 (exp of up to 16 * 5 stays inside fp32 range).  The forward also
+// takes the unbounded gate: its diagonal sub-blocks then come from diag_tc_kernel instead.
 static bool tc_gate_ok(const Shape& s, float lb) { return s.gate == KDA_GATE_LOWER_BOUNDED && lb >= -5.0f; }
+static bool tc_fwd_gate_ok(const Shape& s, float lb) { return s.gate == KDA_GATE_SOFTPLUS || tc_gate_ok(s, lb); }
 
 struct TcPlan {
-    size_t off_chunk, off_rec, total;
+    size_t off_chunk, off_rec, off_diag, total;
 };
 
 static TcPlan plan_tc_fwd(const Shape& s) {
@@ -98,6 +100,8 @@ static TcPlan plan_tc_fwd(const Shape& s) {
     size_t o = 0;
     w.off_chunk = o; o = align_up(o + sizeof(int32_t) * (size_t)(s.N + 1));
     w.off_rec = o; o = align_up(o + tc_record_bytes(s.NCmax, s.H));
+    w.off_diag = 0;
+    if (s.gate == KDA_GATE_SOFTPLUS) { w.off_diag = o; o = align_up(o + diag_item_bytes() * s.NCmax * s.H); }
     w.total = o;
     return w;
 }
@@ -235,7 +239,7 @@ static const char* kKernelNames[] = {"kda_plan",          "kda_intra_simt",   "k
                                      "kda_empty_segment", "kda_intra_tc",     "kda_chain_fwd_tc",
                                      "kda_grad_tc",       "kda_bwd_pre",      "kda_chain_bwd_tc",
                                      "kda_chain_rec_tc",  "kda_group_sum",    "kda_short_conv_fwd",
-                                     "kda_short_conv_bwd", "kda_short_conv_reduce"};
+                                     "kda_short_conv_bwd", "kda_short_conv_reduce", "kda_diag_tc"};
 
 // saved != NULL: also keep the fp32 backward record there (kda_fwd_save)
 static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cudaStream_t stream,
@@ -252,7 +256,12 @@ static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cu
         p.rec = saved;
         p.rec_stride = RecLayout::make(s.K, s.V).bwd_size;
     }
+    if (s.gate == KDA_GATE_SOFTPLUS) {
+        if (saved) return KDA_ERR_UNSUPPORTED;   // the backward record needs the factorised decay
+        p.diag = reinterpret_cast<float*>(b + w.off_diag);
+    }
     KDA_TRY_CUDA(launch_plan(p, stream));
+    if (p.diag) KDA_TRY_CUDA(launch_diag_tc(p, stream));
     KDA_TRY_CUDA(launch_intra_tc(p, recs, saved ? 2 : 0, stream));
     KDA_TRY_CUDA(launch_chain_fwd_tc(p, recs, false, stream));
     return KDA_OK;
@@ -349,7 +358,7 @@ kda_status kda_fwd(const kda_dims* dims, const void* q, const void* k, const voi
     Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
                            initial_state);
     // the tensor-core path needs 16-byte aligned activations and a gate it can factorise
-    if (!tc_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p))
+    if (!tc_eligible(s) || !tc_fwd_gate_ok(s, lower_bound) || !tc_inputs_aligned(p))
         return kda_fwd_simt(dims, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, chunk_size,
                             cu_seqlens, initial_state, out, final_state, workspace, workspace_bytes, stream);
     p.out = out;

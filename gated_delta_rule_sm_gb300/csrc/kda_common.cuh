@@ -44,6 +44,8 @@ struct Params {
     void* tc;                   // tensor-core path buffers (its own layout)
     float* chunk_u;             // tensor-core backward: U per (chunk, head) [64][V] fp32, from the recompute chain
     float* chunk_du;            // tensor-core backward: dU per (chunk, head) [64][V] fp32, from the reverse chain
+    float* diag;                // tensor-core forward, unbounded gate: diagonal 16 x 16 blocks of Bkk, Aqk per
+                                // (chunk, head), from diag_tc_kernel
     int* status;                // device status word
 };
 

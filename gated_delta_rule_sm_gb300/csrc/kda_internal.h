@@ -63,7 +63,7 @@ struct GradScratch {
 enum KernelId {
     K_PLAN = 0, K_INTRA_SIMT, K_CHAIN_FWD_SIMT, K_CHAIN_BWD_SIMT, K_GRAD_SIMT, K_PARAM_REDUCE, K_EMPTY_SEG,
     K_INTRA_TC, K_CHAIN_FWD_TC, K_GRAD_TC, K_BWD_PRE, K_CHAIN_BWD_TC, K_CHAIN_REC_TC, K_GROUP_SUM,
-    K_CONV_FWD, K_CONV_BWD, K_CONV_REDUCE, K_NUM_KERNELS
+    K_CONV_FWD, K_CONV_BWD, K_CONV_REDUCE, K_DIAG_TC, K_NUM_KERNELS
 };
 
 // Record of the two tcgen05 state chains of the backward, per (chunk, head), K = V = 128 (bytes).
@@ -112,6 +112,10 @@ cudaError_t launch_chain_rec_tc(const Params& p, const uint8_t* bw, cudaStream_t
 // tensor-core path (bf16, K = V = 128)
 size_t tc_record_bytes(int NCmax, int H);
 bool tc_inputs_aligned(const Params& p);
+// Unbounded gate: the diagonal 16 x 16 blocks of Bkk and Aqk per (chunk, head), into p.diag
+// (diag_item_bytes() each), before the intra kernel.
+size_t diag_item_bytes();
+cudaError_t launch_diag_tc(const Params& p, cudaStream_t st);
 // mode 0: forward chain record; 1: fp32 backward record; 2: both
 cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, int mode, cudaStream_t st);
 cudaError_t launch_chain_fwd_tc(const Params& p, const uint8_t* recs, bool store_states, cudaStream_t st);

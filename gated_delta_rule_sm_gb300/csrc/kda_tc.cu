@@ -45,6 +45,16 @@ constexpr uint32_t TAIL = BYTES - KD; // KD + AQ + GC, contiguous
 // sub-block j is one MMA (M = 128: 64 k-rows and 64 q-rows, N = 16, K = 128) with its own left
 // operand L^(j).  The per-token factors are running products of alpha = exp(g) inside each
 // sub-block, so the exponentials per element are exp for the gate sigmoid and exp for alpha.
+// Unbounded gate (g = -exp(a_log) softplus(.)): nothing bounds exp(Gamma_t - G_{j+1}) inside sub-block j,
+// so for that gate the left factor of the diagonal column sub-block (j == b) is zero in the MMAs and
+// diag_tc_kernel supplies those four 16 x 16 blocks of Bkk and Aqk instead.  Off the diagonal both
+// factors stay <= 1 for any gate.  Per item: fp32 [2 (Bkk, Aqk)][64 t][ROW], column u = s - 16 (t / 16).
+namespace diaglay {
+constexpr int ROW = 20;                      // 80-byte rows: float4 reads of 8 consecutive rows hit distinct banks
+constexpr int FLOATS = 2 * 64 * ROW;
+constexpr uint32_t BYTES = FLOATS * 4;       // 10240
+}  // namespace diaglay
+
 namespace intralay {
 constexpr uint32_t RAW_Q = 0, RAW_K = 16384, RAW_G = 32768, RAW_V = 49152;  // TMA tiles [64 t][128 c] bf16
 // Left operands of the A-matrix MMAs, [k rows; q rows] 128 x 128, MN-major mn_bf16(r, c, 128, 2048),
@@ -63,7 +73,8 @@ constexpr uint32_t KVB = 163840;             // A operand [Kg^T; V^T] 256 x 64 (
 constexpr uint32_t KGLO = 196608;            // bf16 lo half of Kg^T (128 x 64), same layout
 constexpr uint32_t SMALL = 212992;           // rq[64] rk[64] beta[64] dtb[128] blk[4][128] gsum[4][128] (fp32)
 constexpr uint32_t BAR = SMALL + (64 * 3 + 128 + 1024) * 4;
-constexpr uint32_t BYTES = BAR + 64;
+constexpr uint32_t DIAG = BAR + 64;          // unbounded gate: the item's diagonal blocks (diaglay), by bulk copy
+constexpr uint32_t BYTES = DIAG + diaglay::BYTES;
 }  // namespace intralay
 
 // acc (a 16 x 16 block as two 16 x 8 accumulator fragments) += A B for 16 x 16 blocks A, B at row
@@ -126,6 +137,12 @@ __global__ void __launch_bounds__(256, 1)
     uint64_t* bar_b = bar_load + 2;   // A-matrix MMAs reading tile pair B (two issuing warps)
     uint64_t* bar_w = bar_load + 3;   // the final W / U0 MMAs (two issuing warps)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_load + 4);
+    uint64_t* bar_diag = bar_load + 5;   // unbounded gate: the diagonal blocks of an item
+    const bool sp = !BWD && p.gate == KDA_GATE_SOFTPLUS;   // the backward modes never see this gate
+    auto load_diag = [&](int it) {
+        mbar_expect_tx(bar_diag, diaglay::BYTES);
+        bulk_g2s(smem + DIAG, p.diag + (size_t)it * diaglay::FLOATS, diaglay::BYTES, bar_diag);
+    };
     // TMEM columns: A-matrix partial products p = 0..5 at 64 p + 16 j (sub-block j), W^T at 384, U0^T
     // at 448.  One thread issues a tcgen05.mma every ~100 cycles and the tensor pipe takes one about
     // every 46 at this shape, so two issuing threads keep it busy: warps 0 and 1, whose sub-block
@@ -149,15 +166,17 @@ __global__ void __launch_bounds__(256, 1)
         mbar_init(bar_a, NISSUE);
         mbar_init(bar_b, NISSUE);
         mbar_init(bar_w, 2);
+        mbar_init(bar_diag, 1);
         mbar_fence_init();
         load_raw(blockIdx.x);
+        if (sp) load_diag(blockIdx.x);
     }
     if (warp == 0) tmem_alloc(tslot, TCOLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    uint32_t par_a = 0, par_b = 0, par_w = 0, par_load = 0;
+    uint32_t par_a = 0, par_b = 0, par_w = 0, par_load = 0, par_diag = 0;
     bool ok = true;
     // dt_bias (thread < 128) and the beta logit (thread < 64) of an item, loaded into registers one
     // item ahead so their latency hides behind the current item
@@ -232,7 +251,10 @@ __global__ void __launch_bounds__(256, 1)
                     const uint32_t o = t * 256 + (cp + 64 * ci) * 2;
                     kx[ci][u] = bf16_at(smem + RAW_K, o) * rkt;
                     qx[ci][u] = bf16_at(smem + RAW_Q, o) * rqt;
-                    const float gv = p.lb * __fdividef(1.f, 1.f + __expf(-ea * (bf16_at(smem + RAW_G, o) + dtb[ci])));
+                    const float z = bf16_at(smem + RAW_G, o) + dtb[ci];
+                    // lower-bounded: lb sigmoid(e^a z); unbounded: -e^a softplus(z) = -e^a (max(z, 0) + log(1 + e^-|z|))
+                    const float gv = sp ? -ea * (fmaxf(z, 0.f) + __logf(1.f + __expf(-fabsf(z))))
+                                        : p.lb * __fdividef(1.f, 1.f + __expf(-ea * z));
                     const float g = t < len ? gv : 0.f;
                     av[ci][u] = __expf(g);
                     if (BWD) {
@@ -298,7 +320,7 @@ __global__ void __launch_bounds__(256, 1)
             const float eG = bi == 0 ? 1.f : bi == 1 ? B0 : bi == 2 ? B0 * B1 : B0 * B1 * B2;      // exp(G_b)
             const float tail = bi == 0 ? B1 * B2 * B3 : bi == 1 ? B2 * B3 : bi == 2 ? B3 : 1.f;   // exp(Gamma_C - G_{b+1})
             const float Bi = bi == 0 ? B0 : bi == 1 ? B1 : bi == 2 ? B2 : B3;
-            const float fd = 1.f / Bi;                                   // j == b
+            const float fd = sp ? 0.f : 1.f / Bi;                        // j == b (from diag_tc_kernel if sp)
             const float fm2 = bi >= 2 ? (bi == 2 ? B1 : B2) : 0.f;       // j == b - 2
             const float fm3 = bi == 3 ? B1 * B2 : 0.f;                   // j == b - 3
             // factor of L^(j) = exp(Gamma_t - G_{j+1}) / x_t for j = 0..3 (zero for j > b)
@@ -444,6 +466,11 @@ __global__ void __launch_bounds__(256, 1)
         float* SLf = reinterpret_cast<float*>(smem + SL);
         float* SNf = reinterpret_cast<float*>(smem + SN);
         float* SPf = reinterpret_cast<float*>(smem + SP);
+        if (sp) {
+            ok = __syncthreads_and(mbar_wait(bar_diag, par_diag) ? 1 : 0) != 0;
+            par_diag ^= 1;
+            if (!ok) goto fail;
+        }
         {
             // warp w reads lane quarter w % 4 (rows) and columns 32 (w / 4) .. + 32 of the six partials
             const int qw = warp & 3, c0 = 32 * (warp >> 2);
@@ -465,6 +492,24 @@ __global__ void __launch_bounds__(256, 1)
                 tmem_ld_wait();
 #pragma unroll
                 for (int u = 0; u < 32; ++u) d[u] += e1[u] + e2[u];
+            }
+            if (sp) {
+                // the row's diagonal sub-block (its MMA rows had a zero left factor), if in these columns
+                const int t = 32 * (qw & 1) + lane, bt = t >> 4;
+                if ((bt >> 1) == (c0 >> 5)) {
+                    const float4* dg = reinterpret_cast<const float4*>(smem + DIAG) + ((qw >> 1) * 64 + t) * (diaglay::ROW / 4);
+                    const bool upper = bt & 1;
+#pragma unroll
+                    for (int u4 = 0; u4 < 4; ++u4) {
+                        const float4 x = dg[u4];
+                        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            d[4 * u4 + e] += upper ? 0.f : xs[e];
+                            d[16 + 4 * u4 + e] += upper ? xs[e] : 0.f;
+                        }
+                    }
+                }
             }
             if (qw < 2) {
                 const int t = 32 * qw + lane;
@@ -499,6 +544,11 @@ __global__ void __launch_bounds__(256, 1)
             }
         }
         __syncthreads();
+        // the diagonal-block area has been read: request the next item's
+        if (sp && tid == 0 && item + (int)gridDim.x < nitems) {
+            fence_async_smem();
+            load_diag(item + gridDim.x);
+        }
         // ---- N = (I + L)^-1, blocked: 16x16 diagonal blocks by forward substitution, then the
         // off-diagonal blocks N_ij = -N_ii sum_{m=j}^{i-1} L_im N_mj by increasing i - j.
         if (warp < 4 && lane < 16) {
@@ -675,10 +725,168 @@ fail:
         mbar_wait(bar_a, par_a, 1u << 16);
         mbar_wait(bar_b, par_b, 1u << 16);
         mbar_wait(bar_w, par_w, 1u << 16);
+        if (sp) mbar_wait(bar_diag, par_diag, 1u << 16);
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, TCOLS);
+}
+
+// ------------------------------------------------------------------ diagonal blocks, unbounded gate
+//
+// For t, s in the same 16-token sub-block b:
+//     Bkk[t,s] = sum_c k_tc k_sc prod_{s<r<=t} alpha_rc   (s < t),
+//     Aqk[t,s] = sum_c q_tc k_sc prod_{s<r<=t} alpha_rc   (s <= t),
+// the decay a running product of alpha = exp(g) <= 1, which cannot overflow for any gate.  One CTA of
+// four warps per (chunk, head); warp b takes sub-block b, a lane channels 2 lane, 2 lane + 1 (pass 0)
+// and 64 + 2 lane, 65 + 2 lane (pass 1).  The lane's partial sums of the 32 lower-triangle entries of
+// columns s and 15 - s go through one warp reduce-scatter (31 shuffles), after which lane l holds one
+// entry; entries above the diagonal stay zero.  Tokens past the segment have q = k = 0 and alpha = 1.
+__global__ void __launch_bounds__(128, 3) diag_tc_kernel(Params p) {
+    // shared: the item's q, k, g tiles [64 t][128 c] bf16 (staged by cp.async in one round trip,
+    // rows past the segment zero), then the output tile
+    extern __shared__ __align__(16) uint8_t dsm[];
+    const __nv_bfloat162* sq2 = reinterpret_cast<const __nv_bfloat162*>(dsm);
+    const __nv_bfloat162* sk2 = reinterpret_cast<const __nv_bfloat162*>(dsm + 16384);
+    const __nv_bfloat162* sg2 = reinterpret_cast<const __nv_bfloat162*>(dsm + 32768);
+    float* tile = reinterpret_cast<float*>(dsm + 49152);
+    __shared__ float srq[64], srk[64];
+    const int H = p.H;
+    const int item = blockIdx.x;
+    if (item >= p.chunk_off[p.N] * H) return;
+    const int c = item / H, h = item - c * H;
+    const int n = chunk_segment(p, c);
+    const int tok0 = seg_begin(p, n) + (c - p.chunk_off[n]) * kChunk;
+    const int len = min(kChunk, seg_end(p, n) - tok0);
+    const int tid = threadIdx.x, lane = tid & 31, b = tid >> 5;
+    {
+        const uint8_t* qg = static_cast<const uint8_t*>(p.q);
+        const uint8_t* kg = static_cast<const uint8_t*>(p.k);
+        const uint8_t* gg = static_cast<const uint8_t*>(p.g_raw);
+        // 3 tensors x 64 rows x 16 pieces of 16 bytes; a row is 256 contiguous bytes
+        for (int i = tid; i < 3 * 64 * 16; i += 128) {
+            const int ten = i >> 10, t = (i >> 4) & 63, piece = i & 15;
+            const int tt = t < len ? t : 0;   // rows past the segment: zero-filled from a valid address
+            const size_t row = ten == 2 ? (size_t)(tok0 + tt) * H + h : (size_t)(tok0 + tt) * p.Hk + h / p.G;
+            const uint8_t* src = (ten == 0 ? qg : ten == 1 ? kg : gg) + row * 256 + piece * 16;
+            cp_async16_zfill(dsm + ten * 16384 + t * 256 + piece * 16, src, t < len ? 16u : 0u);
+        }
+    }
+    for (int i = tid; i < diaglay::FLOATS / 4; i += 128)
+        reinterpret_cast<float4*>(tile)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    cp_async_commit_wait_all();
+    __syncthreads();
+    // inverse L2 norms of the sub-block's tokens
+    {
+        float ss[32];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int t = 16 * b + u;
+            ss[u] = ss[16 + u] = 0.f;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const float2 qv = __bfloat1622float2(sq2[t * 64 + 32 * hf + lane]);
+                const float2 kv = __bfloat1622float2(sk2[t * 64 + 32 * hf + lane]);
+                ss[u] += qv.x * qv.x + qv.y * qv.y;
+                ss[16 + u] += kv.x * kv.x + kv.y * kv.y;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], o);
+        if (lane < 16) {
+            const int t = 16 * b + lane;
+            float sq = ss[0], sk = ss[16];
+#pragma unroll
+            for (int u = 1; u < 16; ++u)
+                if (lane == u) { sq = ss[u]; sk = ss[16 + u]; }
+            srq[t] = t < len ? 1.0f / sqrtf(sq + kNormEps) : 0.f;
+            srk[t] = t < len ? 1.0f / sqrtf(sk + kNormEps) : 0.f;
+        }
+    }
+    __syncwarp();
+    const float ea = __expf(p.a_log[h]);
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+        const int pr = 32 * pass + lane;   // channel pair: channels 2 pr, 2 pr + 1
+        const float dt0 = p.dt_bias[h * 128 + 2 * pr], dt1 = p.dt_bias[h * 128 + 2 * pr + 1];
+        float kh[2][16], qh[2][16], al[2][16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int t = 16 * b + u;
+            if (t < len) {
+                const float2 qv = __bfloat1622float2(sq2[t * 64 + pr]);
+                const float2 kv = __bfloat1622float2(sk2[t * 64 + pr]);
+                const float2 gv = __bfloat1622float2(sg2[t * 64 + pr]);
+                qh[0][u] = qv.x * srq[t]; qh[1][u] = qv.y * srq[t];
+                kh[0][u] = kv.x * srk[t]; kh[1][u] = kv.y * srk[t];
+                // alpha = exp(-e^a softplus(z)), with the fast intrinsics the intra kernel uses for its factors
+                const float z0 = gv.x + dt0, z1 = gv.y + dt1;
+                al[0][u] = __expf(-ea * (fmaxf(z0, 0.f) + __logf(1.f + __expf(-fabsf(z0)))));
+                al[1][u] = __expf(-ea * (fmaxf(z1, 0.f) + __logf(1.f + __expf(-fabsf(z1)))));
+            } else {
+                qh[0][u] = qh[1][u] = kh[0][u] = kh[1][u] = 0.f;
+                al[0][u] = al[1][u] = 1.f;
+            }
+        }
+        // Columns s and 15 - s share one reduce-scatter: column s has 16 - s Aqk and 15 - s Bkk entries
+        // (rows t >= s, resp. t > s), column 15 - s has s + 1 and s, 32 in all.  Slots in that order.
+#pragma unroll
+        for (int sa = 0; sa < 8; ++sa) {
+            const int sb = 15 - sa;
+            float v[32];
+#pragma unroll
+            for (int col = 0; col < 2; ++col) {
+                const int s = col ? sb : sa;
+                const int a0 = col ? 31 - 2 * sa : 0;     // first Aqk slot of this column
+                const int b0 = a0 + 16 - s;               // first Bkk slot
+                float e0 = 1.f, e1 = 1.f;
+#pragma unroll
+                for (int t = s; t < 16; ++t) {
+                    if (t > s) { e0 *= al[0][t]; e1 *= al[1][t]; }
+                    const float w0 = kh[0][s] * e0, w1 = kh[1][s] * e1;
+                    v[a0 + t - s] = qh[0][t] * w0 + qh[1][t] * w1;
+                    if (t > s) v[b0 + t - s - 1] = kh[0][t] * w0 + kh[1][t] * w1;
+                }
+            }
+            // reduce-scatter: each step a lane keeps the half of its values selected by its bit `w`,
+            // ending with the warp's sum of slot `lane`
+#pragma unroll
+            for (int w = 16; w >= 1; w >>= 1) {
+                const bool up = lane & w;
+#pragma unroll
+                for (int i = 0; i < w; ++i) {
+                    const float send = up ? v[i] : v[i + w];
+                    const float keep = up ? v[i + w] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+                }
+            }
+            // slot `lane` -> (column, matrix 0 = Bkk / 1 = Aqk, row)
+            int col_s, m, t;
+            if (lane < 16 - sa) { col_s = sa; m = 1; t = sa + lane; }
+            else if (lane < 31 - 2 * sa) { col_s = sa; m = 0; t = lane - 15 + sa + sa; }
+            else if (lane < 32 - sa) { col_s = sb; m = 1; t = sb + lane - (31 - 2 * sa); }
+            else { col_s = sb; m = 0; t = sb + 1 + lane - (32 - sa); }
+            float* dst = tile + (m * 64 + 16 * b + t) * diaglay::ROW + col_s;
+            *dst = pass ? *dst + v[0] : v[0];
+        }
+    }
+    __syncthreads();
+    float4* dst = reinterpret_cast<float4*>(p.diag + (size_t)item * diaglay::FLOATS);
+    for (int i = tid; i < diaglay::FLOATS / 4; i += 128) dst[i] = reinterpret_cast<const float4*>(tile)[i];
+}
+
+size_t diag_item_bytes() { return diaglay::BYTES; }
+
+cudaError_t launch_diag_tc(const Params& p, cudaStream_t st) {
+    constexpr int kSmem = 49152 + diaglay::BYTES;
+    cudaError_t e = cudaFuncSetAttribute(diag_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    timing_pre(st, K_DIAG_TC);
+    diag_tc_kernel<<<p.NCmax * p.H, 128, kSmem, st>>>(p);
+    timing_post(st);
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ state chain (tcgen05)

@@ -17,7 +17,7 @@ import dataclasses
 
 import torch
 
-from . import backward, forward, saved_size
+from . import _lib, backward, forward, saved_size
 from .inputs import WORKLOADS, make_inputs
 
 
@@ -28,10 +28,12 @@ def main(argv=None) -> None:
     ap.add_argument("--T", type=int)
     ap.add_argument("--H", type=int)
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=0, help="untimed iterations before the timed ones")
+    ap.add_argument("--kernels", action="store_true", help="also print each kernel's mean time (library events)")
     ap.add_argument("--fwd-only", action="store_true", help="skip the backward of a fwd+bwd workload")
     ap.add_argument("--saved", action="store_true", help="forward keeps the per-chunk record for the backward")
     ap.add_argument("--gate", default="lower_bounded", choices=("lower_bounded", "softplus"),
-                    help="gate activation (softplus: the unbounded gate, SIMT path)")
+                    help="gate activation (softplus: the unbounded gate)")
     ap.add_argument("--short-conv", type=int, default=0, metavar="W",
                     help="instead time the W-tap short convolution + SiLU prologue on a q-shaped [B, T, H*K] tensor")
     a = ap.parse_args(argv)
@@ -56,15 +58,27 @@ def main(argv=None) -> None:
         if nb == 0:
             raise SystemExit("this workload has no saved-record path")
         saved = torch.empty(nb, dtype=torch.uint8, device=dev)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    torch.cuda.synchronize()
-    ev[0].record()
-    for _ in range(a.iters):
+    def step():
         forward(*[x[n] for n in names], output_final_state=w.final_state, saved=saved, **kw)
         if run_bwd:
             backward(*[x[n] for n in names], x["dout"], saved=saved, **kw)
+
+    for _ in range(a.warmup):
+        step()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    if a.kernels:
+        _lib.timing_begin(64 * a.iters)
+    ev[0].record()
+    for _ in range(a.iters):
+        step()
     ev[1].record()
     torch.cuda.synchronize()
+    if a.kernels:
+        per: dict = {}
+        for name, ms in _lib.timing_end(64 * a.iters):
+            per[name] = per.get(name, 0.0) + ms
+        print("  ".join(f"{k}={v / max(1, a.iters):.3f}ms" for k, v in per.items()))
     print(f"workload={w.name} B={w.B} T={w.T} H={w.H} gate={a.gate} bwd={run_bwd} saved={saved is not None} "
           f"iters={a.iters} "
           f"ms_per_iter={ev[0].elapsed_time(ev[1]) / max(1, a.iters):.3f}")

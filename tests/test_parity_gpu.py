@@ -365,3 +365,20 @@ def test_softplus_gate_steep_decay_underflows_cleanly():
     out, fs = _check_fwd(x, "fp32")
     assert torch.isfinite(out).all() and torch.isfinite(fs).all()
     _check_bwd(x, "fp32")
+
+
+@pytest.mark.parametrize("g_mean,Hk", [(0.0, 0), (4.0, 0), (-6.0, 0), (0.0, 1)])
+def test_softplus_gate_tensor_core_forward(g_mean, Hk):
+    """bf16 K = V = 128: the forward takes the tcgen05 path with the diagonal sub-blocks from the pre-pass.
+    Typical, steep (g near -64 per token) and mild decays, and grouped key heads; the SIMT forward
+    agrees as well."""
+    x = _softplus_case(B=2, T=300, H=2, K=128, V=128, initial_state=True, g_mean=g_mean, Hk=Hk, seed=64)
+    out, fs = _check_fwd(x, "bf16")
+    assert torch.isfinite(out.float()).all() and torch.isfinite(fs).all()
+    _check_fwd(x, "bf16", simt=True)
+
+
+def test_softplus_gate_tensor_core_forward_packed_documents():
+    x = _softplus_case(B=1, T=333, H=3, K=128, V=128, varlen=True, initial_state=True, seed=65,
+                       lengths=[1, 15, 16, 17, 0, 64, 200, 20])
+    _check_fwd(x, "bf16")
