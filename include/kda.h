@@ -17,7 +17,8 @@
  * fused backend requires this lower-bounded gate; the exact formula is not
  * printed on the pages and is this library's reading).  The same page keeps a
  * second, unbounded gate behind `safe_gate=False` (and the torchtitan note
- * checks "both gate activations"); selected by kda_dims.gate, it is read as
+ * tests the kernel under each of the two gate activations); selected by
+ * kda_dims.gate, it is read as
  *     g     = -exp(a_log_h) * softplus(g_raw + dt_bias_{h,c})
  * (again unprinted; the plainest unbounded form over the same ingredients).
  *

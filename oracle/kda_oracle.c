@@ -27,7 +27,8 @@
  *     The pages name these ingredients but never print the formula; this is
  *     the plainest reading that uses all three and keeps g in (lower_bound, 0).
  *   - the unbounded gate the same page keeps behind `safe_gate=False` (the
- *     torchtitan note checks "both gate activations"), gate kind 1:
+ *     torchtitan note compares kernel and recurrence under each of the two
+ *     gate activations), gate kind 1:
  *         g     = -exp(a_log_h) * softplus(g_raw + dt_bias_{h,c})
  *     Also unprinted: the plainest form over the same ingredients that keeps
  *     g < 0 without a lower bound (a_log as a log-rate, dt_bias as the bias
