@@ -24,7 +24,8 @@ KDA_BF16, KDA_FP32 = 0, 1
 EXPORTS = ("kda_fwd_workspace_size", "kda_bwd_workspace_size", "kda_fwd", "kda_fwd_simt", "kda_bwd",
            "kda_status_string", "kda_device_status", "kda_version", "kda_timing_begin", "kda_timing_end",
            "kda_kernel_name", "kda_fwd_noalloc", "kda_saved_size", "kda_fwd_save", "kda_bwd_saved",
-           "kda_short_conv_fwd", "kda_short_conv_bwd_workspace_size", "kda_short_conv_bwd")
+           "kda_short_conv_fwd", "kda_short_conv_bwd_workspace_size", "kda_short_conv_bwd",
+           "kda_fwd_segmented_workspace_size", "kda_fwd_segmented")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 GATES = {"lower_bounded": 0, "softplus": 1}   # kda_gate
 
@@ -67,6 +68,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             f = getattr(lib, name)
             f.restype = ctypes.c_int
             f.argtypes = fwd_args
+        lib.kda_fwd_segmented_workspace_size.restype = ctypes.c_size_t
+        lib.kda_fwd_segmented_workspace_size.argtypes = [dims_p, ctypes.c_int, ctypes.c_int]
+        lib.kda_fwd_segmented.restype = ctypes.c_int
+        lib.kda_fwd_segmented.argtypes = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int,
+                                                                  ctypes.c_int] + [_vp] * 3 + [_vp, ctypes.c_size_t, _vp]
         lib.kda_fwd_noalloc.restype = ctypes.c_int
         lib.kda_fwd_noalloc.argtypes = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int] + \
             [_vp] * 4 + [_vp]
@@ -200,15 +206,17 @@ def _contig(*ts):
 
 
 def forward(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale: float, lower_bound: float = -5.0,
-            gate: str = "lower_bounded", chunk_size: int = 64, cu_seqlens=None, initial_state=None, output_final_state: bool = False,
-            out=None, final_state=None, simt: bool = False, saved: Optional[torch.Tensor] = None,
-            stream: Optional[torch.cuda.Stream] = None):
+            gate: str = "lower_bounded", chunk_size: int = 64, cu_seqlens=None, initial_state=None,
+            output_final_state: bool = False, out=None, final_state=None, simt: bool = False,
+            saved: Optional[torch.Tensor] = None, segments: int = 0, stream: Optional[torch.cuda.Stream] = None):
     """KDA forward through ``kda_fwd`` (or ``kda_fwd_simt``).  Returns (out, final_state or None).
 
     ``gate``: "lower_bounded" (g = lower_bound * sigmoid(exp(a_log) * (g_raw + dt_bias))) or
-    "softplus" (g = -exp(a_log) * softplus(g_raw + dt_bias), unbounded; runs on the SIMT path).
+    "softplus" (g = -exp(a_log) * softplus(g_raw + dt_bias), unbounded below).
     ``saved``: a device byte buffer of ``saved_size(...)`` bytes; the forward then runs
     ``kda_fwd_save`` and keeps the per-chunk quantities there for ``backward(..., saved=...)``.
+    ``segments`` > 0: run ``kda_fwd_segmented``, the chain cut into that many pieces per row (rows of
+    T tokens only; for long rows with few rows x heads).
     """
     lib = load()
     _contig(q, k, v, g_raw, beta_raw, a_log, dt_bias, cu_seqlens, initial_state)
@@ -223,9 +231,20 @@ def forward(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale: float, lower_bou
         final_state = torch.empty((N, H, K, V), dtype=torch.float32, device=q.device)
     if not output_final_state:
         final_state = None
+    st = stream if stream is not None else torch.cuda.current_stream(q.device)
+    if segments:
+        if cu_seqlens is not None or saved is not None or simt:
+            raise ValueError("segments= takes rows of T tokens, without saved= or simt=")
+        ws_bytes = lib.kda_fwd_segmented_workspace_size(ctypes.byref(dims), int(chunk_size), int(segments))
+        ws = workspace_cache.get(q.device, "fwd", ws_bytes)
+        code = lib.kda_fwd_segmented(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw),
+                                     _ptr(a_log), _ptr(dt_bias), float(scale), float(lower_bound), int(chunk_size),
+                                     int(segments), _ptr(initial_state), _ptr(out), _ptr(final_state), _ptr(ws),
+                                     ctypes.c_size_t(ws.numel()), ctypes.c_void_p(st.cuda_stream))
+        _check(code, "kda_fwd_segmented")
+        return out, final_state
     ws_bytes = lib.kda_fwd_workspace_size(ctypes.byref(dims), chunk_size)
     ws = workspace_cache.get(q.device, "fwd", ws_bytes)
-    st = stream if stream is not None else torch.cuda.current_stream(q.device)
     head = (ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw), _ptr(a_log),
             _ptr(dt_bias), float(scale), float(lower_bound), int(chunk_size), _ptr(cu_seqlens),
             _ptr(initial_state), _ptr(out), _ptr(final_state))

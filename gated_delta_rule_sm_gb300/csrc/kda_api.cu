@@ -239,7 +239,8 @@ static const char* kKernelNames[] = {"kda_plan",          "kda_intra_simt",   "k
                                      "kda_empty_segment", "kda_intra_tc",     "kda_chain_fwd_tc",
                                      "kda_grad_tc",       "kda_bwd_pre",      "kda_chain_bwd_tc",
                                      "kda_chain_rec_tc",  "kda_group_sum",    "kda_short_conv_fwd",
-                                     "kda_short_conv_bwd", "kda_short_conv_reduce", "kda_diag_tc"};
+                                     "kda_short_conv_bwd", "kda_short_conv_reduce", "kda_diag_tc",
+                                     "kda_seg_combine"};
 
 // saved != NULL: also keep the fp32 backward record there (kda_fwd_save)
 static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cudaStream_t stream,
@@ -265,6 +266,34 @@ static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cu
     KDA_TRY_CUDA(launch_intra_tc(p, recs, saved ? 2 : 0, stream));
     KDA_TRY_CUDA(launch_chain_fwd_tc(p, recs, false, stream));
     return KDA_OK;
+}
+
+// Segment-parallel forward: each of the B rows cut into P pieces of L tokens (L a multiple of 64).
+struct SegPlan {
+    Shape ps;            // the pieces as packed segments
+    TcPlan tc;           // chunk table, records (and diagonal blocks) of the piece problem
+    size_t off_cu, off_sloc, off_m, off_sstart, total;
+    int L, P;
+};
+
+static SegPlan plan_seg(const Shape& s, int segments) {
+    SegPlan w;
+    const int nch = (s.T + kChunk - 1) / kChunk;
+    w.L = (nch + segments - 1) / segments * kChunk;
+    w.P = (s.T + w.L - 1) / w.L;
+    w.ps = s;
+    w.ps.varlen = true;
+    w.ps.N = s.B * w.P;
+    w.ps.NCmax = (int)(((long long)s.TT + kChunk - 1) / kChunk + w.ps.N);
+    w.tc = plan_tc_fwd(w.ps);
+    const size_t st = sizeof(float) * (size_t)w.ps.N * s.H * s.K * s.V;
+    size_t o = w.tc.total;
+    w.off_cu = o; o = align_up(o + sizeof(int32_t) * (size_t)(w.ps.N + 1));
+    w.off_sloc = o; o = align_up(o + st);     // end state of each piece from zero
+    w.off_m = o; o = align_up(o + st);        // transfer matrix of each piece (K x K, K == V)
+    w.off_sstart = o; o = align_up(o + st);   // true entering state of each piece
+    w.total = o;
+    return w;
 }
 
 // Tensor-core backward.  saved == NULL: the intra kernel rebuilds the fp32 backward record in the
@@ -395,6 +424,61 @@ kda_status kda_bwd(const kda_dims* dims, const void* q, const void* k, const voi
     KDA_TRY_CUDA(launch_chain_fwd_simt(p, true, stream));
     KDA_TRY_CUDA(launch_chain_bwd_simt(p, stream));
     KDA_TRY_CUDA(launch_grad_simt(p, stream));
+    return KDA_OK;
+}
+
+size_t kda_fwd_segmented_workspace_size(const kda_dims* dims, int chunk_size, int segments) {
+    Shape s;
+    if (!dims || segments < 1 || check_dims(dims, chunk_size, false, &s) != KDA_OK || !tc_eligible(s)) return 0;
+    return plan_seg(s, segments).total;
+}
+
+kda_status kda_fwd_segmented(const kda_dims* dims, const void* q, const void* k, const void* v, const void* g_raw,
+                             const void* beta_raw, const float* a_log, const float* dt_bias, float scale,
+                             float lower_bound, int chunk_size, int segments, const float* initial_state, void* out,
+                             float* final_state, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    Shape s;
+    kda_status st = common_checks(dims, chunk_size, nullptr, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale,
+                                  lower_bound, &s);
+    if (st != KDA_OK) return st;
+    if (!out || segments < 1) return KDA_ERR_INVALID_ARG;
+    Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, nullptr, initial_state);
+    if (!tc_eligible(s) || !tc_fwd_gate_ok(s, lower_bound) || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
+    const SegPlan w = plan_seg(s, segments);
+    st = check_ws(workspace, workspace_bytes, w.total);
+    if (st != KDA_OK) return st;
+    st = status_ptr(&p.status);
+    if (st != KDA_OK) return st;
+    char* b = static_cast<char*>(workspace);
+    // the pieces as packed segments: same chunks as the rows, since pieces start on 64-token boundaries
+    Params pp = p;
+    pp.N = w.ps.N;
+    pp.NCmax = w.ps.NCmax;
+    int32_t* piece_cu = reinterpret_cast<int32_t*>(b + w.off_cu);
+    pp.cu = piece_cu;
+    pp.chunk_off = reinterpret_cast<int32_t*>(b + w.tc.off_chunk);
+    if (s.gate == KDA_GATE_SOFTPLUS) pp.diag = reinterpret_cast<float*>(b + w.tc.off_diag);
+    uint8_t* recs = reinterpret_cast<uint8_t*>(b + w.tc.off_rec);
+    float* sloc = reinterpret_cast<float*>(b + w.off_sloc);
+    float* M = reinterpret_cast<float*>(b + w.off_m);
+    float* sstart = reinterpret_cast<float*>(b + w.off_sstart);
+    KDA_TRY_CUDA(launch_piece_cu(piece_cu, s.B, s.T, w.L, w.P, stream));
+    KDA_TRY_CUDA(launch_plan(pp, stream));
+    if (pp.diag) KDA_TRY_CUDA(launch_diag_tc(pp, stream));
+    KDA_TRY_CUDA(launch_intra_tc(pp, recs, 0, stream));
+    Params pa = pp;   // local end states: from zero, no output
+    pa.S0 = nullptr;
+    pa.out = nullptr;
+    pa.ST = sloc;
+    KDA_TRY_CUDA(launch_chain_fwd_tc(pa, recs, false, stream));
+    pa.ST = M;        // transfer matrices: from the identity with U0 taken as zero
+    KDA_TRY_CUDA(launch_chain_fwd_tc(pa, recs, false, stream, true));
+    KDA_TRY_CUDA(launch_seg_combine(initial_state, final_state, sloc, M, sstart, s.B, s.H, w.P, stream));
+    Params pc = pp;   // the output, from the true entering states
+    pc.S0 = sstart;
+    pc.out = out;
+    pc.ST = nullptr;
+    KDA_TRY_CUDA(launch_chain_fwd_tc(pc, recs, false, stream));
     return KDA_OK;
 }
 

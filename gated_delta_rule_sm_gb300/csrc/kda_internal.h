@@ -63,7 +63,7 @@ struct GradScratch {
 enum KernelId {
     K_PLAN = 0, K_INTRA_SIMT, K_CHAIN_FWD_SIMT, K_CHAIN_BWD_SIMT, K_GRAD_SIMT, K_PARAM_REDUCE, K_EMPTY_SEG,
     K_INTRA_TC, K_CHAIN_FWD_TC, K_GRAD_TC, K_BWD_PRE, K_CHAIN_BWD_TC, K_CHAIN_REC_TC, K_GROUP_SUM,
-    K_CONV_FWD, K_CONV_BWD, K_CONV_REDUCE, K_DIAG_TC, K_NUM_KERNELS
+    K_CONV_FWD, K_CONV_BWD, K_CONV_REDUCE, K_DIAG_TC, K_SEG_COMBINE, K_NUM_KERNELS
 };
 
 // Record of the two tcgen05 state chains of the backward, per (chunk, head), K = V = 128 (bytes).
@@ -118,6 +118,13 @@ size_t diag_item_bytes();
 cudaError_t launch_diag_tc(const Params& p, cudaStream_t st);
 // mode 0: forward chain record; 1: fp32 backward record; 2: both
 cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, int mode, cudaStream_t st);
-cudaError_t launch_chain_fwd_tc(const Params& p, const uint8_t* recs, bool store_states, cudaStream_t st);
+// transfer: start from the identity with U0 taken as zero, so that the final state is the transfer matrix
+cudaError_t launch_chain_fwd_tc(const Params& p, const uint8_t* recs, bool store_states, cudaStream_t st,
+                                bool transfer = false);
+// segment-parallel forward: piece boundaries of B rows of T tokens (P pieces of L tokens), and the
+// serial propagation of piece-entering states S_{k+1} = M_k S_k + S_loc,k (fp32, K = V = 128)
+cudaError_t launch_piece_cu(int32_t* cu, int B, int T, int L, int P, cudaStream_t st);
+cudaError_t launch_seg_combine(const float* S0, float* ST, const float* sloc, const float* M, float* sstart, int B,
+                               int H, int P, cudaStream_t st);
 
 }  // namespace kda

@@ -919,7 +919,12 @@ constexpr uint32_t kIdescTF32 = idesc_tf32(128, 32);
 // plus Aqk U, which the MMA warp issues into its own accumulator as soon as U is staged, off the
 // critical path.  Records stream through two slots; the load warp refills a slot with the chunk two
 // ahead once every reader of its chunk is done (an `empty` mbarrier per slot).
-__global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const uint8_t* recs, int store_states) {
+// flags: kChainStoreStates (write the chunk-entering states), kChainTransfer (start every segment from
+// the identity and take U0 as zero: the final state is then the segment's transfer matrix, the product
+// of Diag(exp(Gamma_last)) - Kd^T W over its chunks; needs K == V).
+constexpr int kChainStoreStates = 1, kChainTransfer = 2;
+__global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const uint8_t* recs, int flags) {
+    const bool store_states = flags & kChainStoreStates, transfer = flags & kChainTransfer;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int n = blockIdx.x, h = blockIdx.y, z = blockIdx.z, j0 = z * 32;
     const int H = p.H, K = 128, V = 128;
@@ -1003,9 +1008,9 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
     } else {
     float S[32];
     {
-        const float* src = p.S0 ? p.S0 + (((size_t)n * H + h) * K + tid) * V + j0 : nullptr;
+        const float* src = p.S0 && !transfer ? p.S0 + (((size_t)n * H + h) * K + tid) * V + j0 : nullptr;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) S[j] = src ? src[j] : 0.f;
+        for (int j = 0; j < 32; ++j) S[j] = src ? src[j] : (transfer && tid == j0 + j ? 1.f : 0.f);
     }
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const bool issuer = lane == 0;
@@ -1066,7 +1071,7 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
             const float* u0 = reinterpret_cast<const float*>(sl + chainlay::SLOT_U0);
             float u[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) u[j] = tf32_rn(u0[j * 64 + tid] - d[j]);
+            for (int j = 0; j < 32; ++j) u[j] = tf32_rn((transfer ? 0.f : u0[j * 64 + tid]) - d[j]);
             const int r = tid & 3;
             const bool top = (r & 2) == 0, even = (r & 1) == 0;
             uint8_t* UB = smem + chainlay::UB + (i & 1) * chainlay::UB_BYTES;
@@ -1217,12 +1222,99 @@ cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, int mode, cudaStream
     return cudaGetLastError();
 }
 
-cudaError_t launch_chain_fwd_tc(const Params& p, const uint8_t* recs, bool store_states, cudaStream_t st) {
+cudaError_t launch_chain_fwd_tc(const Params& p, const uint8_t* recs, bool store_states, cudaStream_t st,
+                                bool transfer) {
     cudaError_t e = cudaFuncSetAttribute(chain_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)chainlay::BYTES);
     if (e != cudaSuccess) return e;
     timing_pre(st, K_CHAIN_FWD_TC);
-    chain_fwd_tc_kernel<<<dim3(p.N, p.H, 4), 192, chainlay::BYTES, st>>>(p, recs, store_states ? 1 : 0);
+    chain_fwd_tc_kernel<<<dim3(p.N, p.H, 4), 192, chainlay::BYTES, st>>>(
+        p, recs, (store_states ? kChainStoreStates : 0) | (transfer ? kChainTransfer : 0));
+    timing_post(st);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ segment-parallel forward
+//
+// The chunk chain of a row is affine in its entering state: S_end = M S_begin + S_loc, with M the
+// product of Diag(exp(Gamma_last)) - Kd^T W over the chunks and S_loc the end state from zero.  The
+// segmented forward cuts each row into pieces, gets (M, S_loc) per piece from two chain passes run
+// in parallel over pieces, propagates the true piece-entering states here, and runs the chain once
+// more from them for the output.
+
+// cu[i] = first token of piece i (P pieces of L tokens per row of T, the last one shorter).
+__global__ void piece_cu_kernel(int32_t* cu, int B, int T, int L, int P) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i <= B * P; i += gridDim.x * blockDim.x) {
+        const int b = i / P, k = i - b * P;
+        cu[i] = b * T + min(k * L, T);
+    }
+}
+
+// One CTA per (row, head, 16-column slice); thread k owns row k of the state slice (fp32).  For each
+// piece in order: record the entering state, then S <- M S + S_loc, with M staged in shared memory by
+// coalesced loads (rows padded to 129 floats: the row-per-thread reads are conflict-free).  The final
+// S is the row's final state.
+constexpr int kCombineSmem = (128 * 129 + 128 * 17) * 4;
+__global__ void __launch_bounds__(128) seg_combine_kernel(const float* S0, float* ST, const float* sloc,
+                                                          const float* M, float* sstart, int H, int P) {
+    extern __shared__ float csm[];
+    float* sM = csm;                 // [128][129]
+    float* sS = csm + 128 * 129;     // [128][17]
+    const int b = blockIdx.x, h = blockIdx.y, j0 = 16 * blockIdx.z, k = threadIdx.x;
+    float S[16];
+    {
+        const float* src = S0 ? S0 + (((size_t)b * H + h) * 128 + k) * 128 + j0 : nullptr;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) S[j] = src ? src[j] : 0.f;
+    }
+    for (int pc = 0; pc < P; ++pc) {
+        const size_t base = ((size_t)(b * P + pc) * H + h) * 128 * 128;
+        float* dst = sstart + base + (size_t)k * 128 + j0;
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) sS[k * 17 + j] = S[j];
+        const float4* m4 = reinterpret_cast<const float4*>(M + base);
+#pragma unroll 8
+        for (int i = k; i < 4096; i += 128) {
+            const float4 m = m4[i];
+            float* row = sM + (i >> 5) * 129 + (i & 31) * 4;
+            row[0] = m.x; row[1] = m.y; row[2] = m.z; row[3] = m.w;
+        }
+        float acc[16];
+        const float* lrow = sloc + base + (size_t)k * 128 + j0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j] = lrow[j];
+        __syncthreads();
+        const float* mrow = sM + k * 129;
+#pragma unroll 4
+        for (int kk = 0; kk < 128; ++kk) {
+            const float m = mrow[kk];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] += m * sS[kk * 17 + j];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) S[j] = acc[j];
+    }
+    if (ST) {
+        float* dst = ST + (((size_t)b * H + h) * 128 + k) * 128 + j0;
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+}
+
+cudaError_t launch_piece_cu(int32_t* cu, int B, int T, int L, int P, cudaStream_t st) {
+    piece_cu_kernel<<<(B * P + 256) / 256, 256, 0, st>>>(cu, B, T, L, P);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_seg_combine(const float* S0, float* ST, const float* sloc, const float* M, float* sstart, int B,
+                               int H, int P, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(seg_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCombineSmem);
+    if (e != cudaSuccess) return e;
+    timing_pre(st, K_SEG_COMBINE);
+    seg_combine_kernel<<<dim3(B, H, 8), 128, kCombineSmem, st>>>(S0, ST, sloc, M, sstart, H, P);
     timing_post(st);
     return cudaGetLastError();
 }

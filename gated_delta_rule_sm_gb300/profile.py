@@ -32,6 +32,8 @@ def main(argv=None) -> None:
     ap.add_argument("--kernels", action="store_true", help="also print each kernel's mean time (library events)")
     ap.add_argument("--fwd-only", action="store_true", help="skip the backward of a fwd+bwd workload")
     ap.add_argument("--saved", action="store_true", help="forward keeps the per-chunk record for the backward")
+    ap.add_argument("--segments", type=int, default=0,
+                    help="forward through kda_fwd_segmented with this many pieces per row (forward only)")
     ap.add_argument("--gate", default="lower_bounded", choices=("lower_bounded", "softplus"),
                     help="gate activation (softplus: the unbounded gate)")
     ap.add_argument("--short-conv", type=int, default=0, metavar="W",
@@ -58,6 +60,11 @@ def main(argv=None) -> None:
         if nb == 0:
             raise SystemExit("this workload has no saved-record path")
         saved = torch.empty(nb, dtype=torch.uint8, device=dev)
+    if a.segments:
+        kw["segments"] = a.segments
+        if run_bwd or w.varlen:
+            raise SystemExit("--segments times the forward of rows of T tokens")
+
     def step():
         forward(*[x[n] for n in names], output_final_state=w.final_state, saved=saved, **kw)
         if run_bwd:
@@ -79,7 +86,8 @@ def main(argv=None) -> None:
         for name, ms in _lib.timing_end(64 * a.iters):
             per[name] = per.get(name, 0.0) + ms
         print("  ".join(f"{k}={v / max(1, a.iters):.3f}ms" for k, v in per.items()))
-    print(f"workload={w.name} B={w.B} T={w.T} H={w.H} gate={a.gate} bwd={run_bwd} saved={saved is not None} "
+    print(f"workload={w.name} B={w.B} T={w.T} H={w.H} gate={a.gate} segments={a.segments} bwd={run_bwd} "
+          f"saved={saved is not None} "
           f"iters={a.iters} "
           f"ms_per_iter={ev[0].elapsed_time(ev[1]) / max(1, a.iters):.3f}")
 

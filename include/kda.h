@@ -221,6 +221,39 @@ kda_status kda_fwd_noalloc(const kda_dims* dims,
                            const int32_t* cu_seqlens, const float* initial_state,
                            void* out, float* final_state, cudaStream_t stream);
 
+/*
+ * Segment-parallel forward for long rows with few rows x heads.  The chunk
+ * chain of kda_fwd is serial per (row, head).  When B * H is small it keeps
+ * only a few SMs busy however long T is.  This entry cuts every row into
+ * `segments` pieces of equal whole-chunk length and works like the state-CP
+ * executor of hyper-parallel "KDA context-parallel executors"
+ * (`_eager_kda_state_p2p`), with pieces in place of ranks, on one GPU:
+ *   1. for every piece in parallel, a summary of its chunks: the end state from
+ *      zero S_loc and the transition M (the K x K product of the per-chunk
+ *      maps S -> Diag(exp(Gamma_last)) S - Kd^T W S);
+ *   2. the entering states, piece after piece: S_{k+1} = M_k S_k + S_loc,k,
+ *      from initial_state (or zero); the last one is final_state;
+ *   3. the output of every piece from its entering state, in parallel.
+ * Same arguments and results as kda_fwd without cu_seqlens: rows of T tokens
+ * only (packed documents are KDA_ERR_UNSUPPORTED here).  It takes only
+ * shapes of the tensor-core forward: bf16, K = V = 128, 16-byte aligned
+ * activations, the softplus gate or lower_bound >= -5; others are
+ * KDA_ERR_UNSUPPORTED.  segments >= 1, else KDA_ERR_INVALID_ARG.  Pieces are
+ * ceil(ceil(T / 64) / segments) chunks long, so fewer pieces than `segments`
+ * can result.  The intra-chunk pass runs once and the chain three times,
+ * each over all pieces at once.  In exact arithmetic the result equals
+ * kda_fwd's; in floating point it agrees to rounding.  The workspace is
+ * kda_fwd_segmented_workspace_size() bytes (0 for invalid or unsupported
+ * shapes); it adds three fp32 states per piece and head to the forward's.
+ */
+size_t kda_fwd_segmented_workspace_size(const kda_dims* dims, int chunk_size, int segments);
+kda_status kda_fwd_segmented(const kda_dims* dims,
+                             const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
+                             const float* a_log, const float* dt_bias, float scale, float lower_bound,
+                             int chunk_size, int segments, const float* initial_state,
+                             void* out, float* final_state,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int kda_version(void);
 

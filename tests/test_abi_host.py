@@ -199,3 +199,26 @@ def test_short_conv_validation(lib):
     assert ws() > 0 and ws() % 256 == 0
     assert ws(T=128) == 2 * ws()          # one partial row per 64-token tile
     assert ws(W=9) == 0 and ws(C=0) == 0
+
+
+def _fwd_seg(lib, dims, segments=4, ws=None, ws_bytes=0, ptr=16):
+    p = ctypes.c_void_p(ptr)
+    return lib.kda_fwd_segmented(ctypes.byref(dims), p, p, p, p, p, p, p, 0.125, -5.0, 64, segments, None, p, None,
+                                 ws, ctypes.c_size_t(ws_bytes), None)
+
+
+def test_segmented_forward_validation(lib):
+    """kda_fwd_segmented: tensor-core shapes only, segments >= 1, its own workspace size."""
+    d128 = _dims(K=128, V=128, T=4096)
+    sz = lambda d, n: lib.kda_fwd_segmented_workspace_size(ctypes.byref(d), 64, n)
+    assert _fwd_seg(lib, d128, segments=0) == _lib.KDA_ERR_INVALID_ARG
+    assert _fwd_seg(lib, _dims(), segments=4) == _lib.KDA_ERR_UNSUPPORTED              # K = V = 64
+    assert _fwd_seg(lib, _dims(K=128, V=128, dtype=_lib.KDA_FP32)) == _lib.KDA_ERR_UNSUPPORTED
+    assert _fwd_seg(lib, d128, ptr=24) == _lib.KDA_ERR_UNSUPPORTED                     # unaligned activations
+    assert _fwd_seg(lib, d128) == _lib.KDA_ERR_WORKSPACE                               # valid: needs its workspace
+    assert sz(_dims(), 4) == 0 and sz(d128, 0) == 0
+    # three fp32 states (64 KiB) per piece and head on top of the tensor-core forward's buffers
+    assert sz(d128, 1) > 3 * 1 * 2 * 65536
+    assert sz(d128, 8) - sz(d128, 4) >= 3 * 4 * 2 * 65536
+    assert sz(d128, 8) > sz(d128, 4) > sz(d128, 1)
+    assert sz(d128, 64) == sz(d128, 1000)            # never more pieces than chunks

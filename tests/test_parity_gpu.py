@@ -382,3 +382,49 @@ def test_softplus_gate_tensor_core_forward_packed_documents():
     x = _softplus_case(B=1, T=333, H=3, K=128, V=128, varlen=True, initial_state=True, seed=65,
                        lengths=[1, 15, 16, 17, 0, 64, 200, 20])
     _check_fwd(x, "bf16")
+
+
+# ------------------------------------------------------------------ segment-parallel forward
+
+def _check_segmented(x, segments, dtype="bf16"):
+    import gated_delta_rule_sm_gb300 as kda
+    names = ("q", "k", "v", "g_raw", "beta_raw", "a_log", "dt_bias")
+    out, fs = kda.forward(*[x[n] for n in names], scale=x["scale"], lower_bound=x["lower_bound"],
+                          gate=x.get("gate", "lower_bounded"), initial_state=x.get("initial_state"),
+                          output_final_state=True, segments=segments)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    r_out, r_fs = oracle_fwd(x)
+    e, e2 = rel_err(out, r_out, dtype), rel_err(fs, r_fs, dtype)
+    assert e <= tol(dtype) and e2 <= tol(dtype), (segments, e, e2)
+    return out, fs
+
+
+@pytest.mark.parametrize("segments", [1, 3, 16, 100])
+def test_segmented_forward_matches_the_oracle(segments):
+    """Mild gates (g_raw ~ N(-4, 1)) so the entering states carry across many pieces; T = 1000 leaves a
+    40-token tail; 100 segments ask for more pieces than the 16 chunks."""
+    w = Workload("t", B=1, T=1000, H=2, K=128, V=128, initial_state=True, g_mean=-4.0, seed=70)
+    _check_segmented(make_inputs(w, device=DEV), segments)
+
+
+def test_segmented_forward_rows_heads_and_plain_agree():
+    w = Workload("t", B=2, T=333, H=3, K=128, V=128, initial_state=True, g_mean=-3.0, seed=71)
+    x = make_inputs(w, device=DEV)
+    out, fs = _check_segmented(x, 4)
+    o2, f2 = gpu_fwd(x)
+    assert rel_err(out, f64(o2), "bf16") <= 2e-2 and rel_err(fs, f64(f2), "bf16") <= 2e-2
+
+
+def test_segmented_forward_softplus_gate():
+    x = _softplus_case(B=1, T=700, H=2, K=128, V=128, initial_state=True, g_mean=-6.0, seed=72)
+    _check_segmented(x, 5)
+
+
+def test_segmented_forward_long_row_few_heads():
+    """The case the schedule is for: one 65536-token row on two heads (the long-context workload's
+    distributions), 16 pieces; and a mild-gate row of 8192 tokens cut into 64-token pieces."""
+    w = Workload("t", B=1, T=65536, H=2, K=128, V=128, initial_state=True, seed=73)
+    _check_segmented(make_inputs(w, device=DEV), 16)
+    w = Workload("t", B=1, T=8192, H=2, K=128, V=128, initial_state=True, g_mean=-4.0, seed=73)
+    _check_segmented(make_inputs(w, device=DEV), 128)
