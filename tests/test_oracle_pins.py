@@ -468,3 +468,28 @@ def test_short_conv_backward_central_differences(packed):
             num[idx] = (L(args_p["x"], args_p["w"], args_p["b"]) - L(args_m["x"], args_m["w"], args_m["b"])) / (2 * h)
         err = np.abs(num - g[gname]).max() / np.abs(num).max()
         assert err < 1e-7, (name, err)
+
+
+def test_state_summary_composes_across_pieces():
+    """[P4] state CP: a shard's effect on the state is affine, S_end = M S_begin + S_loc, with M the
+    end state from the identity with v = 0 and S_loc the end state from zero.  Cutting one row into
+    three pieces and composing the summaries reproduces the whole row's final state and, run from
+    the composed entering states, every piece's output (K = V so that M is the state of a run)."""
+    d, S0 = _full_inputs(B=1, T=37, H=2, K=3, V=3, seed=31)
+    d["g_raw"] -= 3.0            # long memory, so the entering states matter
+    kw = dict(scale=0.8, lower_bound=-5.0)
+    out, fs = oracle.kda_fwd(**d, initial_state=S0, **kw)
+    cuts = [0, 11, 30, 37]
+    piece = lambda dd, a, b: {n: (x[:, a:b] if x.ndim >= 3 else x) for n, x in dd.items()}
+    eye = np.broadcast_to(np.eye(3), (1, 2, 3, 3)).copy()
+    S = S0
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        p = piece(d, a, b)
+        _, S_loc = oracle.kda_fwd(**p, initial_state=None, **kw)
+        _, M = oracle.kda_fwd(**dict(p, v=np.zeros_like(p["v"])), initial_state=eye, **kw)
+        o_p, f_p = oracle.kda_fwd(**p, initial_state=S, **kw)
+        np.testing.assert_allclose(o_p, out[:, a:b], rtol=1e-10, atol=1e-12)
+        S_next = np.einsum("nhkl,nhlv->nhkv", M, S) + S_loc
+        np.testing.assert_allclose(S_next, f_p, rtol=1e-10, atol=1e-12)
+        S = S_next
+    np.testing.assert_allclose(S, fs, rtol=1e-10, atol=1e-12)
