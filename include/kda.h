@@ -197,7 +197,7 @@ const char* kda_status_string(kda_status s);
 kda_status kda_device_status(int reset);
 
 /*
- * Forward without a caller-provided workspace (no counterpart in the paper: an
+ * Forward without a caller-provided workspace (no counterpart on the pages: an
  * integration aid).  Some callers cannot allocate device memory: plugin
  * hosts that own every device allocation and give their plugins no
  * allocator, and latency-critical loops that must not call cudaMalloc
