@@ -110,13 +110,19 @@ size_t kda_bwd_workspace_size(const kda_dims* dims, int chunk_size);
  * accepted value runs the same 64-token blocking, so results agree to
  * rounding with any chunk size.
  * Requirements: B,T,H >= 1; 16 <= K,V <= 128 and multiples of 16 (the pages
- * reject head dims below 16); N >= 1.  bf16 with K == V == 128, 16-byte
- * aligned q, k, v, g_raw (and dout for kda_bwd), the lower-bounded gate and
- * lower_bound >= -5 runs on the tcgen05 tensor-core path (its 16-token
- * sub-block factorisation of the decay stays inside fp32 range only for
- * |lower_bound| <= 5); every other supported shape, fp32 inputs and the
- * unbounded gate run on the fp32 SIMT path, which forms every decay as
- * exp(Gamma_t - Gamma_s) <= 1 and so holds for any gate.
+ * reject head dims below 16); N >= 1.
+ * Paths:
+ *   - bf16 with K == V == 128 and 16-byte aligned q, k, v, g_raw (and dout
+ *     for kda_bwd) runs on the tcgen05 tensor-core path.  Its 16-token
+ *     sub-block factorisation of the decay stays inside fp32 range only for
+ *     |lower_bound| <= 5.  With the lower-bounded gate that is required of
+ *     both directions.
+ *   - Under the unbounded gate the forward takes the tensor-core path too:
+ *     the diagonal sub-blocks, where the factorisation has no bound, are
+ *     formed directly.  The backward runs on the SIMT path.
+ *   - Every other supported shape, and fp32 inputs, run on the fp32 SIMT
+ *     path.  It forms every decay as exp(Gamma_t - Gamma_s) <= 1, which holds
+ *     for any gate.
  */
 kda_status kda_fwd(const kda_dims* dims,
                    const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
