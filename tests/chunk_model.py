@@ -46,6 +46,48 @@ def _chunk_quantities(qh, kh, v, g, beta):
                 W=Tm @ Kg, U0=Tm @ v, gC=np.exp(G[-1]))
 
 
+def decayed_forms_subblocks(qh, kh, g, *, diagonal="factorised", sub=16, dtype=np.float32):
+    """Bkk (strictly lower) and Aqk (lower) of one chunk, formed the way the tensor-core kernels do.
+
+    With Gamma cumulative in ``dtype`` and G_{j+1} its value at the end of column sub-block j,
+        exp(Gamma_t - Gamma_s) = exp(Gamma_t - G_{j+1}) * exp(G_{j+1} - Gamma_s)     (s in sub-block j).
+    The right factor is <= 1; the left is <= 1 for rows past sub-block j.  Rows inside sub-block j take
+    it as exp(Gamma_t - G_j) / exp(G_{j+1} - G_j), which nothing bounds: ``diagonal="factorised"`` keeps
+    that (the lower-bounded gate's path), ``diagonal="direct"`` forms the diagonal blocks from running
+    products of alpha = exp(g) instead (the unbounded gate's path).
+    """
+    qh, kh, g = (np.asarray(x, dtype=dtype) for x in (qh, kh, g))
+    C, K = qh.shape
+    G = np.cumsum(g, axis=0, dtype=dtype)
+    Bkk = np.zeros((C, C), dtype)
+    Aqk = np.zeros((C, C), dtype)
+    with np.errstate(over="ignore", invalid="ignore", under="ignore", divide="ignore"):
+        for s0 in range(0, C, sub):
+            s1 = min(C, s0 + sub)
+            Gj = G[s0 - 1] if s0 > 0 else np.zeros(K, dtype)
+            Gj1 = G[s1 - 1]
+            R = kh[s0:s1] * np.exp(Gj1[None, :] - G[s0:s1])
+            if s1 < C:
+                Lt = np.exp(G[s1:] - Gj1[None, :])
+                Bkk[s1:, s0:s1] = (kh[s1:] * Lt) @ R.T
+                Aqk[s1:, s0:s1] = (qh[s1:] * Lt) @ R.T
+            if diagonal == "factorised":
+                Ld = np.exp(G[s0:s1] - Gj[None, :]) * (dtype(1) / np.exp(Gj1 - Gj))[None, :]
+                Bkk[s0:s1, s0:s1] = (kh[s0:s1] * Ld) @ R.T
+                Aqk[s0:s1, s0:s1] = (qh[s0:s1] * Ld) @ R.T
+            else:
+                alpha = np.exp(g[s0:s1])
+                for s in range(s1 - s0):
+                    e = np.ones(K, dtype)
+                    for t in range(s, s1 - s0):
+                        if t > s:
+                            e = e * alpha[t]
+                        w = kh[s0 + s] * e
+                        Bkk[s0 + t, s0 + s] = kh[s0 + t] @ w
+                        Aqk[s0 + t, s0 + s] = qh[s0 + t] @ w
+    return np.tril(Bkk, -1), np.tril(Aqk)
+
+
 def chunk_forward(qh, kh, v, g, beta, scale, S0=None, C=64):
     """Forward for one segment and one head with the prologue bypassed."""
     L, K = qh.shape
