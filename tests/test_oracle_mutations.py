@@ -34,6 +34,8 @@ MUTATIONS = [
      "return exp(a_log) * softplus(g_raw + dt_bias);"),
     ("softplus gate gradient misses the sigmoid", "const double dx = -dg[i * K + c] * ea * sigm(x);",
      "const double dx = -dg[i * K + c] * ea;"),
+    ("dt_bias read channel-major", "oracle_gate_value(g_raw[row * K + c], a_log[h], dt_bias[h * K + c], lb, gate);",
+     "oracle_gate_value(g_raw[row * K + c], a_log[h], dt_bias[c * H + h], lb, gate);"),
     ("convolution taps reversed", "if (tau >= s0) a += w[c * W + i] * x[tau * C + c];",
      "if (tau >= s0) a += w[c * W + (W - 1 - i)] * x[tau * C + c];"),
 ]
@@ -56,6 +58,7 @@ def _battery():
         pins.test_softplus_gate_limits_and_special_values,
         pins.test_softplus_gate_full_path_equals_recurrence,
         lambda: pins.backward_central_differences(False, "softplus"),
+        pins.test_heads_and_rows_are_equivariant,
         pins.test_grouped_heads_equal_repeated_keys,
         pins.test_grouped_heads_backward_central_differences,
         lambda: pins.test_short_conv_matches_numpy_convolve(4),

@@ -493,3 +493,31 @@ def test_state_summary_composes_across_pieces():
         np.testing.assert_allclose(S_next, f_p, rtol=1e-10, atol=1e-12)
         S = S_next
     np.testing.assert_allclose(S, fs, rtol=1e-10, atol=1e-12)
+
+
+def test_heads_and_rows_are_equivariant():
+    """Heads and batch rows are independent problems: permuting them (with their a_log, dt_bias rows
+    and states) permutes every output and gradient the same way.  Catches head / row index mix-ups in
+    the per-head parameters (a_log [H], dt_bias [H*K]) and the [N, H, K, V] states."""
+    d, S0 = _full_inputs(B=2, T=9, H=3, K=4, V=2, seed=51)
+    r = np.random.default_rng(52)
+    dout = r.standard_normal(d["v"].shape)
+    dfs = r.standard_normal(S0.shape)
+    kw = dict(scale=0.6, lower_bound=-4.0)
+    ph, pb = [2, 0, 1], [1, 0]
+    K = d["q"].shape[-1]
+    perm = {n: d[n][pb][:, :, ph] for n in ("q", "k", "v", "g_raw", "beta_raw")}
+    perm["a_log"] = d["a_log"][ph]
+    perm["dt_bias"] = d["dt_bias"].reshape(-1, K)[ph].reshape(-1)
+    S0p = S0[pb][:, ph]
+    out, fs = oracle.kda_fwd(**d, initial_state=S0, **kw)
+    out_p, fs_p = oracle.kda_fwd(**perm, initial_state=S0p, **kw)
+    np.testing.assert_array_equal(out_p, out[pb][:, :, ph])
+    np.testing.assert_array_equal(fs_p, fs[pb][:, ph])
+    g = oracle.kda_bwd(**d, dout=dout, initial_state=S0, dfinal_state=dfs, **kw)
+    g_p = oracle.kda_bwd(**perm, dout=dout[pb][:, :, ph], initial_state=S0p, dfinal_state=dfs[pb][:, ph], **kw)
+    for n in ("dq", "dk", "dv", "dg_raw", "dbeta_raw"):
+        np.testing.assert_array_equal(g_p[n], g[n][pb][:, :, ph])
+    np.testing.assert_allclose(g_p["da_log"], g["da_log"][ph], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(g_p["ddt_bias"], g["ddt_bias"].reshape(-1, K)[ph].reshape(-1), rtol=1e-13, atol=1e-15)
+    np.testing.assert_array_equal(g_p["dinitial_state"], g["dinitial_state"][pb][:, ph])
