@@ -36,6 +36,10 @@ MUTATIONS = [
      "const double dx = -dg[i * K + c] * ea;"),
     ("dt_bias read channel-major", "oracle_gate_value(g_raw[row * K + c], a_log[h], dt_bias[h * K + c], lb, gate);",
      "oracle_gate_value(g_raw[row * K + c], a_log[h], dt_bias[c * H + h], lb, gate);"),
+    ("grouped dq keeps only the last value head", "sq += dqv[vr];", "sq = dqv[vr];"),
+    ("SiLU derivative misses the a (1 - s) term", "const double da = dy[t * C + c] * s * (1.0 + a * (1.0 - s));",
+     "const double da = dy[t * C + c] * s;"),
+    ("convolution gradient crosses document starts", "if (tau < s0) continue;", "if (tau < 0) continue;"),
     ("convolution taps reversed", "if (tau >= s0) a += w[c * W + i] * x[tau * C + c];",
      "if (tau >= s0) a += w[c * W + (W - 1 - i)] * x[tau * C + c];"),
 ]
@@ -63,6 +67,7 @@ def _battery():
         pins.test_grouped_heads_backward_central_differences,
         lambda: pins.test_short_conv_matches_numpy_convolve(4),
         lambda: pins.test_short_conv_backward_central_differences(False),
+        lambda: pins.test_short_conv_backward_central_differences(True),
     ]
 
 
