@@ -25,7 +25,7 @@ EXPORTS = ("kda_fwd_workspace_size", "kda_bwd_workspace_size", "kda_fwd", "kda_f
            "kda_status_string", "kda_device_status", "kda_version", "kda_timing_begin", "kda_timing_end",
            "kda_kernel_name", "kda_fwd_noalloc", "kda_saved_size", "kda_fwd_save", "kda_bwd_saved",
            "kda_short_conv_fwd", "kda_short_conv_bwd_workspace_size", "kda_short_conv_bwd",
-           "kda_fwd_segmented_workspace_size", "kda_fwd_segmented")
+           "kda_fwd_segmented_workspace_size", "kda_fwd_segmented", "kda_selftest_wait_timeout")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 GATES = {"lower_bounded": 0, "softplus": 1}   # kda_gate
 
@@ -73,6 +73,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.kda_fwd_segmented.restype = ctypes.c_int
         lib.kda_fwd_segmented.argtypes = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int,
                                                                   ctypes.c_int] + [_vp] * 3 + [_vp, ctypes.c_size_t, _vp]
+        lib.kda_selftest_wait_timeout.restype = ctypes.c_int
+        lib.kda_selftest_wait_timeout.argtypes = [_vp]
         lib.kda_fwd_noalloc.restype = ctypes.c_int
         lib.kda_fwd_noalloc.argtypes = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int] + \
             [_vp] * 4 + [_vp]

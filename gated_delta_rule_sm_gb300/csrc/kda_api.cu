@@ -557,6 +557,14 @@ kda_status kda_device_status(int reset) {
     return static_cast<kda_status>(v);
 }
 
+kda_status kda_selftest_wait_timeout(cudaStream_t stream) {
+    int* status = nullptr;
+    kda_status st = status_ptr(&status);
+    if (st != KDA_OK) return st;
+    KDA_TRY_CUDA(launch_selftest_wait(status, stream));
+    return KDA_OK;
+}
+
 int kda_version(void) { return 100; }
 
 kda_status kda_timing_begin(int max_launches) {

@@ -124,6 +124,8 @@ cudaError_t launch_chain_fwd_tc(const Params& p, const uint8_t* recs, bool store
 // segment-parallel forward: piece boundaries of B rows of T tokens (P pieces of L tokens), and the
 // serial propagation of piece-entering states S_{k+1} = M_k S_k + S_loc,k (fp32, K = V = 128)
 cudaError_t launch_piece_cu(int32_t* cu, int B, int T, int L, int P, cudaStream_t st);
+// failure-detection self-test: a bounded wait that cannot complete records KDA_ERR_TIMEOUT
+cudaError_t launch_selftest_wait(int* status, cudaStream_t st);
 cudaError_t launch_seg_combine(const float* S0, float* ST, const float* sloc, const float* M, float* sstart, int B,
                                int H, int P, cudaStream_t st);
 

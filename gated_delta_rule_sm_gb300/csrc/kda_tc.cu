@@ -1234,6 +1234,26 @@ cudaError_t launch_chain_fwd_tc(const Params& p, const uint8_t* recs, bool store
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ failure-detection self-test
+//
+// One CTA waits on an mbarrier that nothing arrives on, with the bounded wait every kernel here uses
+// (a fixed number of polls), gives up and records KDA_ERR_TIMEOUT in the device status word, as the
+// kernels' own fail paths do.  It shows the timeout path end to end without hanging or faulting.
+__global__ void selftest_wait_kernel(int* status, uint32_t polls) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0, polls)) record_error(status, KDA_ERR_TIMEOUT);
+}
+
+cudaError_t launch_selftest_wait(int* status, cudaStream_t st) {
+    selftest_wait_kernel<<<1, 32, 0, st>>>(status, 1u << 8);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ segment-parallel forward
 //
 // The chunk chain of a row is affine in its entering state: S_end = M S_begin + S_loc, with M the

@@ -260,6 +260,18 @@ kda_status kda_fwd_segmented(const kda_dims* dims,
                              void* out, float* final_state,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Failure-detection self-test.  Every device-side wait in this library is
+ * bounded; a wait that gives up records KDA_ERR_TIMEOUT in the device status
+ * word (kda_device_status) and its kernel returns, so the context stays
+ * usable.  This call launches one CTA whose mbarrier wait can never complete
+ * (nothing arrives on it).  The same bounded wait gives up after 256 polls,
+ * milliseconds at most, and records KDA_ERR_TIMEOUT.  It neither hangs nor
+ * faults.  Returns KDA_OK once launched on `stream`; read the word with
+ * kda_device_status afterwards.
+ */
+kda_status kda_selftest_wait_timeout(cudaStream_t stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int kda_version(void);
 
