@@ -16,7 +16,8 @@ convolution + SiLU prologue are pinned by the tests in
 ``tests/test_oracle_pins.py``.  The gate formulas
 ``g = lower_bound * sigmoid(exp(a_log) * (g_raw + dt_bias))`` and, for the
 unbounded gate, ``g = -exp(a_log) * softplus(g_raw + dt_bias)``, and the
-L2-norm epsilon (1e-6) are readings of pages that print none of them:
+L2-norm epsilon (1e-6) are readings of pages that print none of them, and so is the
+gated output norm's formula (``gated_norm_fwd``: RMS norm with a weight, gated by a sigmoid):
 parity unpinned for those choices (the tests pin only their limits and
 special values, and the gradients through them by finite differences).
 """
@@ -73,6 +74,11 @@ def _load():
             lib.oracle_short_conv_fwd.argtypes = conv + [_dp]
             lib.oracle_short_conv_bwd.restype = ctypes.c_int
             lib.oracle_short_conv_bwd.argtypes = conv + [_dp, _dp, _dp, _dp]
+            gn = [ctypes.c_int64, ctypes.c_int, _dp, _dp, _dp, ctypes.c_double]
+            lib.oracle_gated_norm_fwd.restype = ctypes.c_int
+            lib.oracle_gated_norm_fwd.argtypes = gn + [_dp]
+            lib.oracle_gated_norm_bwd.restype = ctypes.c_int
+            lib.oracle_gated_norm_bwd.argtypes = gn + [_dp, _dp, _dp, _dp]
             _lib = lib
     return _lib
 
@@ -218,3 +224,25 @@ def short_conv_bwd(x, weight, bias, dy, cu_seqlens=None):
     _load().oracle_short_conv_bwd(B * T, T, C, W, cu_p, (len(cu) - 1) if cu is not None else 0,
                                   _ptr(x), _ptr(weight), _ptr(bias), _ptr(dy), _ptr(dx), _ptr(dw), _ptr(db))
     return dict(dx=dx, dweight=dw, dbias=db)
+
+
+def gated_norm_fwd(o, gate, weight, eps):
+    """The output epilogue: y = o / sqrt(mean(o^2) + eps) * weight * sigmoid(gate) over the last axis.
+
+    o, gate: [..., V]; weight: [V].  Returns y like o.
+    """
+    o, gate, weight = map(_f64, (o, gate, weight))
+    V = o.shape[-1]
+    y = np.zeros_like(o)
+    _load().oracle_gated_norm_fwd(o.size // V, V, _ptr(o), _ptr(gate), _ptr(weight), float(eps), _ptr(y))
+    return y
+
+
+def gated_norm_bwd(o, gate, weight, eps, dy):
+    """Reverse mode of :func:`gated_norm_fwd`: dict(do, dgate like o, dweight [V])."""
+    o, gate, weight, dy = map(_f64, (o, gate, weight, dy))
+    V = o.shape[-1]
+    d_o, dg, dw = np.zeros_like(o), np.zeros_like(o), np.zeros(V)
+    _load().oracle_gated_norm_bwd(o.size // V, V, _ptr(o), _ptr(gate), _ptr(weight), float(eps), _ptr(dy),
+                                  _ptr(d_o), _ptr(dg), _ptr(dw))
+    return dict(do=d_o, dgate=dg, dweight=dw)

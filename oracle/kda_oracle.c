@@ -494,3 +494,53 @@ int oracle_short_conv_bwd(int64_t TT, int T, int C, int W, const int32_t* cu_seq
     }
     return 0;
 }
+
+/* ---- the layer's output epilogue: gated RMS norm over each head's value vector ----
+ *
+ * hyper-parallel "KDA context-parallel executors" (`KimiDeltaAttentionUlyssesCP` forward, the
+ * full-layer adapter) applies `o_norm(output, output_gate)` to the attention output before the
+ * output projection, with `output_gate` from the layer's `g_proj` (or `g_b_proj(g_a_proj(.))`); the
+ * torchtitan review describes the model's RMS norm as one reduced in fp32 with its own epsilon.
+ * The pages print neither the norm's formula nor the gate's activation.  Reading: an RMS norm of
+ * each head's V values with a per-channel weight, gated by the sigmoid of the output gate,
+ *     y_v = o_v / sqrt(mean_u o_u^2 + eps) * w_v * sigmoid(gate_v),
+ * eps given by the caller.  rows = B*T*H rows of V values each. */
+int oracle_gated_norm_fwd(int64_t rows, int V, const double* o, const double* gate, const double* w, double eps,
+                          double* y)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const double* orow = o + r * V;
+        double ss = 0.0;
+        for (int v = 0; v < V; ++v) ss += orow[v] * orow[v];
+        const double rn = 1.0 / sqrt(ss / V + eps);
+        for (int v = 0; v < V; ++v) y[r * V + v] = orow[v] * rn * w[v] * sigm(gate[r * V + v]);
+    }
+    return 0;
+}
+
+/* Reverse mode.  With n = o rn and s = sigmoid(gate):  dgate = dy n w s (1 - s),
+ * dw = sum_rows dy n s,  dn = dy w s,  do = rn (dn - n mean_u(dn_u n_u)). */
+int oracle_gated_norm_bwd(int64_t rows, int V, const double* o, const double* gate, const double* w, double eps,
+                          const double* dy, double* d_o, double* dgate, double* dw)
+{
+    for (int v = 0; v < V; ++v) dw[v] = 0.0;
+    for (int64_t r = 0; r < rows; ++r) {
+        const double* orow = o + r * V;
+        double ss = 0.0;
+        for (int v = 0; v < V; ++v) ss += orow[v] * orow[v];
+        const double rn = 1.0 / sqrt(ss / V + eps);
+        double dot = 0.0;
+        for (int v = 0; v < V; ++v) {
+            const double n = orow[v] * rn, s = sigm(gate[r * V + v]), g = dy[r * V + v];
+            dot += g * w[v] * s * n;
+        }
+        for (int v = 0; v < V; ++v) {
+            const double n = orow[v] * rn, s = sigm(gate[r * V + v]), g = dy[r * V + v];
+            const double dn = g * w[v] * s;
+            d_o[r * V + v] = rn * (dn - n * dot / V);
+            dgate[r * V + v] = g * n * w[v] * s * (1.0 - s);
+            dw[v] += g * n * s;
+        }
+    }
+    return 0;
+}

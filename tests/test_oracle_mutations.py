@@ -40,6 +40,9 @@ MUTATIONS = [
     ("SiLU derivative misses the a (1 - s) term", "const double da = dy[t * C + c] * s * (1.0 + a * (1.0 - s));",
      "const double da = dy[t * C + c] * s;"),
     ("convolution gradient crosses document starts", "if (tau < s0) continue;", "if (tau < 0) continue;"),
+    ("output gate applied as SiLU", "y[r * V + v] = orow[v] * rn * w[v] * sigm(gate[r * V + v]);",
+     "y[r * V + v] = orow[v] * rn * w[v] * gate[r * V + v] * sigm(gate[r * V + v]);"),
+    ("norm backward misses the mean term", "d_o[r * V + v] = rn * (dn - n * dot / V);", "d_o[r * V + v] = rn * dn;"),
     ("convolution taps reversed", "if (tau >= s0) a += w[c * W + i] * x[tau * C + c];",
      "if (tau >= s0) a += w[c * W + (W - 1 - i)] * x[tau * C + c];"),
 ]
@@ -66,6 +69,9 @@ def _battery():
         pins.test_grouped_heads_equal_repeated_keys,
         pins.test_grouped_heads_backward_central_differences,
         lambda: pins.test_short_conv_matches_numpy_convolve(4),
+        pins.test_gated_norm_ungated_limit_is_torch_rms_norm,
+        pins.test_gated_norm_gate_and_scale,
+        pins.test_gated_norm_backward_central_differences,
         lambda: pins.test_short_conv_backward_central_differences(False),
         lambda: pins.test_short_conv_backward_central_differences(True),
     ]

@@ -521,3 +521,53 @@ def test_heads_and_rows_are_equivariant():
     np.testing.assert_allclose(g_p["da_log"], g["da_log"][ph], rtol=1e-13, atol=1e-15)
     np.testing.assert_allclose(g_p["ddt_bias"], g["ddt_bias"].reshape(-1, K)[ph].reshape(-1), rtol=1e-13, atol=1e-15)
     np.testing.assert_array_equal(g_p["dinitial_state"], g["dinitial_state"][pb][:, ph])
+
+
+# ------------------------------------------------------------------ gated output norm
+
+def _gn_case(rows=7, V=16, seed=60):
+    r = np.random.default_rng(seed)
+    return r.standard_normal((rows, V)), r.standard_normal((rows, V)), r.uniform(0.5, 1.5, V)
+
+
+def test_gated_norm_ungated_limit_is_torch_rms_norm():
+    """With the gate saturated (sigmoid = 1) the epilogue is an RMS norm with a weight: torch's
+    rms_norm in float64 on the CPU."""
+    torch = pytest.importorskip("torch")
+    o, _, w = _gn_case()
+    y = oracle.gated_norm_fwd(o, np.full_like(o, 800.0), w, 1e-6)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(o), (o.shape[-1],), torch.from_numpy(w), eps=1e-6).numpy()
+    np.testing.assert_allclose(y, ref, rtol=1e-13, atol=1e-14)
+
+
+def test_gated_norm_gate_and_scale():
+    """The gate multiplies each element by sigmoid(gate) exactly; with eps = 0 a positive rescaling of a
+    row leaves it unchanged; every normalised row has mean square 1 before weight and gate."""
+    o, g, w = _gn_case(seed=61)
+    y = oracle.gated_norm_fwd(o, g, w, 0.0)
+    y1 = oracle.gated_norm_fwd(o, np.full_like(o, 800.0), w, 0.0)
+    np.testing.assert_allclose(y, y1 * expit(g), rtol=1e-14, atol=0)
+    np.testing.assert_allclose(oracle.gated_norm_fwd(3.7 * o, g, w, 0.0), y, rtol=1e-13, atol=1e-15)
+    n = oracle.gated_norm_fwd(o, np.full_like(o, 800.0), np.ones_like(w), 0.0)
+    np.testing.assert_allclose((n * n).mean(-1), 1.0, rtol=1e-13)
+
+
+def test_gated_norm_backward_central_differences():
+    o, g, w = _gn_case(rows=3, V=8, seed=62)
+    dy = np.random.default_rng(63).standard_normal(o.shape)
+    grads = oracle.gated_norm_bwd(o, g, w, 1e-3, dy)
+    L = lambda oo, gg, ww: np.sum(oracle.gated_norm_fwd(oo, gg, ww, 1e-3) * dy)
+    h = 1e-6
+    for name, x, key in (("o", o, "do"), ("gate", g, "dgate"), ("weight", w, "dweight")):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = dict(oo=o, gg=g, ww=w)
+            args_m = dict(oo=o, gg=g, ww=w)
+            k = {"o": "oo", "gate": "gg", "weight": "ww"}[name]
+            args_p[k], args_m[k] = xp, xm
+            num[idx] = (L(**args_p) - L(**args_m)) / (2 * h)
+        err = np.abs(num - grads[key]).max() / np.abs(num).max()
+        assert err < 1e-7, (name, err)
