@@ -2,13 +2,14 @@
 
 The computation lives in the CUDA library ``libkda_gb300.so`` behind the C
 ABI in ``include/kda.h``; this package only marshals torch tensors to it
-(``forward`` / ``backward``, and the layer's short-convolution prologue
-``short_conv`` / ``short_conv_backward``) and draws seeded synthetic inputs
+(``forward`` / ``backward``, the layer's short-convolution prologue
+``short_conv`` / ``short_conv_backward`` and its gated output norm ``gated_norm`` /
+``gated_norm_backward``) and draws seeded synthetic inputs
 (``inputs``).  Importing the package does not load the library; the first
 call does, and raises if it has not been built.
 """
-from ._lib import (KdaError, backward, device_status, forward, load, saved_size, short_conv,  # noqa: F401
-                   short_conv_backward)
+from ._lib import (KdaError, backward, device_status, forward, gated_norm, gated_norm_backward, load,  # noqa: F401
+                   saved_size, short_conv, short_conv_backward)
 
-__all__ = ["forward", "backward", "saved_size", "short_conv", "short_conv_backward", "load", "device_status",
-           "KdaError"]
+__all__ = ["forward", "backward", "saved_size", "short_conv", "short_conv_backward", "gated_norm",
+           "gated_norm_backward", "load", "device_status", "KdaError"]

@@ -25,7 +25,8 @@ EXPORTS = ("kda_fwd_workspace_size", "kda_bwd_workspace_size", "kda_fwd", "kda_f
            "kda_status_string", "kda_device_status", "kda_version", "kda_timing_begin", "kda_timing_end",
            "kda_kernel_name", "kda_fwd_noalloc", "kda_saved_size", "kda_fwd_save", "kda_bwd_saved",
            "kda_short_conv_fwd", "kda_short_conv_bwd_workspace_size", "kda_short_conv_bwd",
-           "kda_fwd_segmented_workspace_size", "kda_fwd_segmented", "kda_selftest_wait_timeout")
+           "kda_fwd_segmented_workspace_size", "kda_fwd_segmented", "kda_selftest_wait_timeout",
+           "kda_gated_norm_fwd", "kda_gated_norm_bwd_workspace_size", "kda_gated_norm_bwd")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 GATES = {"lower_bounded": 0, "softplus": 1}   # kda_gate
 
@@ -73,6 +74,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.kda_fwd_segmented.restype = ctypes.c_int
         lib.kda_fwd_segmented.argtypes = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int,
                                                                   ctypes.c_int] + [_vp] * 3 + [_vp, ctypes.c_size_t, _vp]
+        gn = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, ctypes.c_float]
+        lib.kda_gated_norm_fwd.restype = ctypes.c_int
+        lib.kda_gated_norm_fwd.argtypes = gn + [_vp, _vp]
+        lib.kda_gated_norm_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.kda_gated_norm_bwd_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int]
+        lib.kda_gated_norm_bwd.restype = ctypes.c_int
+        lib.kda_gated_norm_bwd.argtypes = gn + [_vp] * 4 + [_vp, ctypes.c_size_t, _vp]
         lib.kda_selftest_wait_timeout.restype = ctypes.c_int
         lib.kda_selftest_wait_timeout.argtypes = [_vp]
         lib.kda_fwd_noalloc.restype = ctypes.c_int
@@ -350,4 +358,39 @@ def short_conv_backward(x, weight, bias, dy, *, cu_seqlens=None, stream: Optiona
                                   _ptr(dy), _ptr(g["dx"]), _ptr(g["dweight"]), _ptr(g["dbias"]), _ptr(ws),
                                   ctypes.c_size_t(ws.numel()), ctypes.c_void_p(st.cuda_stream))
     _check(code, "kda_short_conv_bwd")
+    return g
+
+
+def gated_norm(o, gate, weight, *, eps: float = 1e-6, out=None, stream: Optional[torch.cuda.Stream] = None):
+    """The output epilogue through ``kda_gated_norm_fwd``: o / sqrt(mean(o^2) + eps) * weight * sigmoid(gate)
+    over the last axis.  o, gate: [..., V] (bf16 or fp32, same dtype); weight: [V] fp32.  Returns y like o."""
+    lib = load()
+    _contig(o, gate, weight)
+    if gate.shape != o.shape or gate.dtype != o.dtype or weight.numel() != o.shape[-1]:
+        raise ValueError("gate must match o, and weight must hold o.shape[-1] values")
+    V = o.shape[-1]
+    if out is None:
+        out = torch.empty_like(o)
+    st = stream if stream is not None else torch.cuda.current_stream(o.device)
+    _check(lib.kda_gated_norm_fwd(o.numel() // V, V, _dtype_code(o), _ptr(o), _ptr(gate), _ptr(weight), float(eps),
+                                  _ptr(out), ctypes.c_void_p(st.cuda_stream)), "kda_gated_norm_fwd")
+    return out
+
+
+def gated_norm_backward(o, gate, weight, dy, *, eps: float = 1e-6, stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """Reverse mode through ``kda_gated_norm_bwd``: dict(do, dgate [..., V], dweight [V]), all fp32."""
+    lib = load()
+    _contig(o, gate, weight, dy)
+    if gate.shape != o.shape or dy.shape != o.shape or weight.numel() != o.shape[-1]:
+        raise ValueError("gate and dy must match o, and weight must hold o.shape[-1] values")
+    V = o.shape[-1]
+    rows = o.numel() // V
+    f32 = dict(dtype=torch.float32, device=o.device)
+    g = dict(do=torch.empty(o.shape, **f32), dgate=torch.empty(o.shape, **f32), dweight=torch.empty((V,), **f32))
+    nb = lib.kda_gated_norm_bwd_workspace_size(rows, V)
+    ws = workspace_cache.get(o.device, "norm", nb)
+    st = stream if stream is not None else torch.cuda.current_stream(o.device)
+    _check(lib.kda_gated_norm_bwd(rows, V, _dtype_code(o), _ptr(o), _ptr(gate), _ptr(weight), float(eps), _ptr(dy),
+                                  _ptr(g["do"]), _ptr(g["dgate"]), _ptr(g["dweight"]), _ptr(ws),
+                                  ctypes.c_size_t(ws.numel()), ctypes.c_void_p(st.cuda_stream)), "kda_gated_norm_bwd")
     return g

@@ -240,7 +240,8 @@ static const char* kKernelNames[] = {"kda_plan",          "kda_intra_simt",   "k
                                      "kda_grad_tc",       "kda_bwd_pre",      "kda_chain_bwd_tc",
                                      "kda_chain_rec_tc",  "kda_group_sum",    "kda_short_conv_fwd",
                                      "kda_short_conv_bwd", "kda_short_conv_reduce", "kda_diag_tc",
-                                     "kda_seg_combine"};
+                                     "kda_seg_combine",   "kda_gated_norm_fwd", "kda_gated_norm_bwd",
+                                     "kda_gated_norm_reduce"};
 
 // saved != NULL: also keep the fp32 backward record there (kda_fwd_save)
 static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cudaStream_t stream,

@@ -63,7 +63,8 @@ struct GradScratch {
 enum KernelId {
     K_PLAN = 0, K_INTRA_SIMT, K_CHAIN_FWD_SIMT, K_CHAIN_BWD_SIMT, K_GRAD_SIMT, K_PARAM_REDUCE, K_EMPTY_SEG,
     K_INTRA_TC, K_CHAIN_FWD_TC, K_GRAD_TC, K_BWD_PRE, K_CHAIN_BWD_TC, K_CHAIN_REC_TC, K_GROUP_SUM,
-    K_CONV_FWD, K_CONV_BWD, K_CONV_REDUCE, K_DIAG_TC, K_SEG_COMBINE, K_NUM_KERNELS
+    K_CONV_FWD, K_CONV_BWD, K_CONV_REDUCE, K_DIAG_TC, K_SEG_COMBINE, K_NORM_FWD, K_NORM_BWD, K_NORM_REDUCE,
+    K_NUM_KERNELS
 };
 
 // Record of the two tcgen05 state chains of the backward, per (chunk, head), K = V = 128 (bytes).

@@ -1,0 +1,211 @@
+// kda_norm.cu -- the layer's output epilogue: gated RMS norm of each head's value vector.
+//
+// hyper-parallel "KDA context-parallel executors" (the full-layer adapter's forward) applies
+// `o_norm(output, output_gate)` between the attention core and the output projection, and the
+// torchtitan review describes the model's RMS norm as one reduced in fp32.  Neither prints the
+// formula; the reading (the oracle's too) is, per row of V values (one token of one head),
+//     y_v = o_v / sqrt(mean_u o_u^2 + eps) * w_v * sigmoid(gate_v),
+// with the sum of squares in fp32.
+//
+// Memory-bound: one read of o and gate, one write of y (forward); reads of o, gate, dy and fp32
+// writes of do, dgate (backward).  One warp per row, grid-stride over rows; a lane owns the values
+// lane, lane + 32, ... (V <= 256, at most 8 per lane), so every access is a contiguous 32-element
+// segment of the row.  The backward keeps per-CTA partial sums of dweight, which a second kernel adds
+// in CTA order (deterministic).
+#include <math.h>
+#include <string.h>
+
+#include "kda.h"
+#include "kda_common.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+
+namespace {
+
+constexpr int kNormMaxV = 256;
+constexpr int kNormPer = kNormMaxV / 32;   // values per lane
+constexpr int kNormThreads = 256;          // eight rows in flight per CTA
+constexpr int kNormBwdCtas = 304;          // two per SM: rows of the dweight partials
+
+struct NormArgs {
+    long long rows;
+    int V, dtype;
+    const void* o;
+    const void* gate;
+    const float* w;
+    float eps;
+    void* y;            // forward output (dtype)
+    const void* dy;     // backward input (dtype)
+    float* d_o;         // [rows, V]
+    float* dgate;       // [rows, V]
+    float* part;        // [ctas, V] per-CTA partial sums of dweight
+    float* dw;          // [V]
+};
+
+__global__ void __launch_bounds__(kNormThreads) gated_norm_fwd_kernel(NormArgs a) {
+    const int lane = threadIdx.x & 31;
+    const long long nw = (long long)gridDim.x * (kNormThreads / 32);
+    float wv[kNormPer];
+#pragma unroll
+    for (int i = 0; i < kNormPer; ++i) {
+        const int v = lane + 32 * i;
+        wv[i] = v < a.V ? a.w[v] : 0.f;
+    }
+    for (long long r = (long long)blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5); r < a.rows; r += nw) {
+        const size_t base = (size_t)r * a.V;
+        float ov[kNormPer], gv[kNormPer];
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < kNormPer; ++i) {
+            const int v = lane + 32 * i;
+            ov[i] = v < a.V ? load_act(a.o, base + v, a.dtype) : 0.f;
+            gv[i] = v < a.V ? load_act(a.gate, base + v, a.dtype) : 0.f;
+            ss += ov[i] * ov[i];
+        }
+        ss = warp_sum(ss);
+        const float rn = 1.0f / sqrtf(ss / a.V + a.eps);
+#pragma unroll
+        for (int i = 0; i < kNormPer; ++i) {
+            const int v = lane + 32 * i;
+            if (v < a.V) store_act(a.y, base + v, ov[i] * rn * wv[i] * sigmoidf_acc(gv[i]), a.dtype);
+        }
+    }
+}
+
+// With n = o rn and s = sigmoid(gate):  dgate = dy n w s (1 - s),  dw += dy n s,  dn = dy w s,
+// do = rn (dn - n mean(dn n)).
+__global__ void __launch_bounds__(kNormThreads) gated_norm_bwd_kernel(NormArgs a) {
+    __shared__ float sdw[kNormThreads / 32][kNormMaxV];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long nw = (long long)gridDim.x * (kNormThreads / 32);
+    float wv[kNormPer], acc[kNormPer];
+#pragma unroll
+    for (int i = 0; i < kNormPer; ++i) {
+        const int v = lane + 32 * i;
+        wv[i] = v < a.V ? a.w[v] : 0.f;
+        acc[i] = 0.f;
+    }
+    for (long long r = (long long)blockIdx.x * (kNormThreads / 32) + warp; r < a.rows; r += nw) {
+        const size_t base = (size_t)r * a.V;
+        float ov[kNormPer], sv[kNormPer], dyv[kNormPer];
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < kNormPer; ++i) {
+            const int v = lane + 32 * i;
+            const bool in = v < a.V;
+            ov[i] = in ? load_act(a.o, base + v, a.dtype) : 0.f;
+            sv[i] = in ? sigmoidf_acc(load_act(a.gate, base + v, a.dtype)) : 0.f;
+            dyv[i] = in ? load_act(a.dy, base + v, a.dtype) : 0.f;
+            ss += ov[i] * ov[i];
+        }
+        ss = warp_sum(ss);
+        const float rn = 1.0f / sqrtf(ss / a.V + a.eps);
+        float dot = 0.f;
+#pragma unroll
+        for (int i = 0; i < kNormPer; ++i) dot += dyv[i] * wv[i] * sv[i] * (ov[i] * rn);
+        dot = warp_sum(dot) / a.V;
+#pragma unroll
+        for (int i = 0; i < kNormPer; ++i) {
+            const int v = lane + 32 * i;
+            if (v < a.V) {
+                const float n = ov[i] * rn, dn = dyv[i] * wv[i] * sv[i];
+                a.d_o[base + v] = rn * (dn - n * dot);
+                a.dgate[base + v] = dyv[i] * n * wv[i] * sv[i] * (1.f - sv[i]);
+                acc[i] += dyv[i] * n * sv[i];
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kNormPer; ++i) {
+        const int v = lane + 32 * i;
+        if (v < a.V) sdw[warp][v] = acc[i];
+    }
+    __syncthreads();
+    for (int v = threadIdx.x; v < a.V; v += kNormThreads) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNormThreads / 32; ++w) t += sdw[w][v];
+        a.part[(size_t)blockIdx.x * a.V + v] = t;
+    }
+}
+
+__global__ void gated_norm_reduce_kernel(NormArgs a, int ctas) {
+    const int v = blockIdx.x * blockDim.x + threadIdx.x;
+    if (v >= a.V) return;
+    float t = 0.f;
+    for (int c = 0; c < ctas; ++c) t += a.part[(size_t)c * a.V + v];
+    a.dw[v] = t;
+}
+
+kda_status norm_check(int64_t rows, int V, int dtype, const void* o, const void* gate, const float* w, float eps) {
+    if (rows < 1 || V < 1) return KDA_ERR_INVALID_ARG;
+    if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
+    if (!o || !gate || !w) return KDA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !isfinite(eps)) return KDA_ERR_INVALID_ARG;
+    if (V > kNormMaxV) return KDA_ERR_UNSUPPORTED;
+    if (rows > (1LL << 40) / V) return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+NormArgs norm_args(int64_t rows, int V, int dtype, const void* o, const void* gate, const float* w, float eps) {
+    NormArgs a;
+    memset(&a, 0, sizeof(a));
+    a.rows = rows; a.V = V; a.dtype = dtype; a.o = o; a.gate = gate; a.w = w; a.eps = eps;
+    return a;
+}
+
+int norm_ctas(int64_t rows, int cap) {
+    const int64_t need = (rows + kNormThreads / 32 - 1) / (kNormThreads / 32);
+    return (int)(need < cap ? need : cap);
+}
+
+}  // namespace
+
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" {
+
+kda_status kda_gated_norm_fwd(int64_t rows, int V, kda_dtype dtype, const void* o, const void* gate,
+                              const float* weight, float eps, void* y, cudaStream_t stream) {
+    kda_status st = norm_check(rows, V, dtype, o, gate, weight, eps);
+    if (st != KDA_OK) return st;
+    if (!y) return KDA_ERR_INVALID_ARG;
+    NormArgs a = norm_args(rows, V, dtype, o, gate, weight, eps);
+    a.y = y;
+    timing_pre(stream, K_NORM_FWD);
+    gated_norm_fwd_kernel<<<norm_ctas(rows, 8 * 152), kNormThreads, 0, stream>>>(a);
+    timing_post(stream);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+size_t kda_gated_norm_bwd_workspace_size(int64_t rows, int V) {
+    if (rows < 1 || V < 1 || V > kNormMaxV) return 0;
+    return ((size_t)kNormBwdCtas * V * sizeof(float) + 255) / 256 * 256;
+}
+
+kda_status kda_gated_norm_bwd(int64_t rows, int V, kda_dtype dtype, const void* o, const void* gate,
+                              const float* weight, float eps, const void* dy, float* d_o, float* dgate,
+                              float* dweight, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    kda_status st = norm_check(rows, V, dtype, o, gate, weight, eps);
+    if (st != KDA_OK) return st;
+    if (!dy || !d_o || !dgate || !dweight) return KDA_ERR_INVALID_ARG;
+    const size_t need = kda_gated_norm_bwd_workspace_size(rows, V);
+    if (workspace_bytes < need || !workspace || reinterpret_cast<uintptr_t>(workspace) % 256) return KDA_ERR_WORKSPACE;
+    NormArgs a = norm_args(rows, V, dtype, o, gate, weight, eps);
+    a.dy = dy; a.d_o = d_o; a.dgate = dgate; a.dw = dweight;
+    a.part = static_cast<float*>(workspace);
+    const int ctas = norm_ctas(rows, kNormBwdCtas);
+    timing_pre(stream, K_NORM_BWD);
+    gated_norm_bwd_kernel<<<ctas, kNormThreads, 0, stream>>>(a);
+    timing_post(stream);
+    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+    timing_pre(stream, K_NORM_REDUCE);
+    gated_norm_reduce_kernel<<<(V + 255) / 256, 256, 0, stream>>>(a, ctas);
+    timing_post(stream);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -261,6 +261,35 @@ kda_status kda_fwd_segmented(const kda_dims* dims,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * The layer's output epilogue: a gated RMS norm of each head's value vector.
+ * hyper-parallel "KDA context-parallel executors" applies
+ * `o_norm(output, output_gate)` between the attention core and the output
+ * projection.  The torchtitan review describes the model's RMS norm as one
+ * reduced in fp32.  Neither prints the formula.  This library's reading, per
+ * row of V values (one token of one head, rows = B * T * H):
+ *     y_v = o_v / sqrt(mean_u o_u^2 + eps) * weight_v * sigmoid(gate_v)
+ * Layouts:
+ *   o, gate, y, dy   [rows, V] in `dtype` (bf16 or fp32);
+ *   weight [V], dweight [V], do, dgate [rows, V]   fp32.
+ * The sum of squares and every gradient are computed in fp32.  dweight sums
+ * over all rows in a fixed order, so results are deterministic.
+ * Errors:
+ *   - KDA_ERR_INVALID_ARG: rows < 1, V < 1, a bad dtype, a NULL pointer, or
+ *     eps < 0 or not finite;
+ *   - KDA_ERR_UNSUPPORTED: V > 256;
+ *   - KDA_ERR_WORKSPACE: the backward's workspace is too small or not
+ *     256-byte aligned; it needs kda_gated_norm_bwd_workspace_size() bytes.
+ * Every pointer is a device pointer the caller owns; nothing is kept after the
+ * call, and the work is enqueued on `stream`.
+ */
+kda_status kda_gated_norm_fwd(int64_t rows, int V, kda_dtype dtype, const void* o, const void* gate,
+                              const float* weight, float eps, void* y, cudaStream_t stream);
+size_t kda_gated_norm_bwd_workspace_size(int64_t rows, int V);
+kda_status kda_gated_norm_bwd(int64_t rows, int V, kda_dtype dtype, const void* o, const void* gate,
+                              const float* weight, float eps, const void* dy, float* d_o, float* dgate,
+                              float* dweight, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Failure-detection self-test.  Every device-side wait in this library is
  * bounded; a wait that gives up records KDA_ERR_TIMEOUT in the device status
  * word (kda_device_status) and its kernel returns, so the context stays

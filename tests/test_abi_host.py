@@ -222,3 +222,24 @@ def test_segmented_forward_validation(lib):
     assert sz(d128, 8) - sz(d128, 4) >= 3 * 4 * 2 * 65536
     assert sz(d128, 8) > sz(d128, 4) > sz(d128, 1)
     assert sz(d128, 64) == sz(d128, 1000)            # never more pieces than chunks
+
+
+def test_gated_norm_validation(lib):
+    p = ctypes.c_void_p(16)
+    fwd = lambda rows=10, V=128, dtype=_lib.KDA_BF16, eps=1e-6, o=p, y=p: lib.kda_gated_norm_fwd(
+        rows, V, dtype, o, p, p, eps, y, None)
+    assert fwd(rows=0) == _lib.KDA_ERR_INVALID_ARG
+    assert fwd(V=0) == _lib.KDA_ERR_INVALID_ARG
+    assert fwd(dtype=3) == _lib.KDA_ERR_INVALID_ARG
+    assert fwd(eps=-1.0) == _lib.KDA_ERR_INVALID_ARG
+    assert fwd(eps=float("nan")) == _lib.KDA_ERR_INVALID_ARG
+    assert fwd(o=None) == _lib.KDA_ERR_INVALID_ARG
+    assert fwd(y=None) == _lib.KDA_ERR_INVALID_ARG
+    assert fwd(V=257) == _lib.KDA_ERR_UNSUPPORTED
+    ws = lambda rows, V: lib.kda_gated_norm_bwd_workspace_size(rows, V)
+    assert ws(10, 128) > 0 and ws(10, 128) % 256 == 0 and ws(10, 128) == ws(10 ** 6, 128)   # per-CTA partials
+    assert ws(0, 128) == 0 and ws(10, 257) == 0
+    bwd = lambda w=None, nbytes=0: lib.kda_gated_norm_bwd(10, 128, _lib.KDA_BF16, p, p, p, 1e-6, p, p, p, p, w,
+                                                          ctypes.c_size_t(nbytes), None)
+    assert bwd() == _lib.KDA_ERR_WORKSPACE
+    assert bwd(ctypes.c_void_p(4096 + 16), ws(10, 128)) == _lib.KDA_ERR_WORKSPACE       # misaligned
