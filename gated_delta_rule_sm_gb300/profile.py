@@ -36,6 +36,8 @@ def main(argv=None) -> None:
                     help="forward through kda_fwd_segmented with this many pieces per row (forward only)")
     ap.add_argument("--gate", default="lower_bounded", choices=("lower_bounded", "softplus"),
                     help="gate activation (softplus: the unbounded gate)")
+    ap.add_argument("--gated-norm", action="store_true",
+                    help="instead time the gated output norm (forward and backward) on the workload's [B, T, H, V] output")
     ap.add_argument("--short-conv", type=int, default=0, metavar="W",
                     help="instead time the W-tap short convolution + SiLU prologue on a q-shaped [B, T, H*K] tensor")
     a = ap.parse_args(argv)
@@ -48,6 +50,9 @@ def main(argv=None) -> None:
     dev = torch.device("cuda:0")
     if a.short_conv:
         _time_short_conv(w, a.short_conv, a.iters, dev)
+        return
+    if a.gated_norm:
+        _time_gated_norm(w, a.iters, dev)
         return
     x = make_inputs(w, device=dev)
     names = ("q", "k", "v", "g_raw", "beta_raw", "a_log", "dt_bias")
@@ -90,6 +95,37 @@ def main(argv=None) -> None:
           f"saved={saved is not None} "
           f"iters={a.iters} "
           f"ms_per_iter={ev[0].elapsed_time(ev[1]) / max(1, a.iters):.3f}")
+
+
+def _time_gated_norm(w, iters: int, dev) -> None:
+    """Forward and backward of the output epilogue on a [B, T, H, V] tensor of the workload's dtype."""
+    from . import gated_norm, gated_norm_backward
+    g = torch.Generator().manual_seed(w.seed)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    shape = (w.B, w.T, w.H, w.V)
+    o, gate, dy = (torch.randn(shape, generator=g).to(dt).to(dev) for _ in range(3))
+    wt = (torch.rand((w.V,), generator=g) + 0.5).to(dev)
+    y = torch.empty_like(o)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for _ in range(3):
+        gated_norm(o, gate, wt, out=y)
+        gated_norm_backward(o, gate, wt, dy)
+    torch.cuda.synchronize()
+    ev[0].record()
+    for _ in range(iters):
+        gated_norm(o, gate, wt, out=y)
+    ev[1].record()
+    for _ in range(iters):
+        gated_norm_backward(o, gate, wt, dy)
+    ev[2].record()
+    torch.cuda.synchronize()
+    e, n = o.element_size(), o.numel()
+    f_ms = ev[0].elapsed_time(ev[1]) / iters
+    b_ms = ev[1].elapsed_time(ev[2]) / iters
+    # algorithmic bytes: forward reads o, gate and writes y; backward reads o, gate, dy and writes fp32 do, dgate
+    fb, bb = n * 3 * e, n * (3 * e + 8)
+    print(f"gated_norm B={w.B} T={w.T} H={w.H} V={w.V} dtype={w.dtype} fwd_ms={f_ms:.4f} fwd_GBs={fb / f_ms / 1e6:.0f} "
+          f"bwd_ms={b_ms:.4f} bwd_GBs={bb / b_ms / 1e6:.0f}")
 
 
 def _time_short_conv(w, W: int, iters: int, dev) -> None:
