@@ -29,6 +29,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "fwdbwd_bf16_B4_T4096_H32_D128"
+# the five quoted workloads, in order; the default one is the headline, the others go in per_config
+WORKLOAD_NAMES = ("fwd_fp32_T256_H2_D64", "fwd_bf16_B2_T2048_H16_D128", "varlen_fwd_bf16_T16384_H32_D128",
+                  "long_fwd_bf16_T65536_H32_D128", "fwdbwd_bf16_B4_T4096_H32_D128")
 METRIC = "KDA fwd(+bwd) tokens/sec on 1 GB300"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -72,11 +75,11 @@ def kernel_work(name: str, w, units: float) -> tuple[float, float]:
     return b * units, f * units
 
 
-# DRAM bytes (read + write) per token-head per launch, from ncu captures of the current kernels
-# (profiles/grad_tc_B1_T4096_H32_D128.md, profiles/intra_tc_B1_T4096_H32_D128.md,
-# profiles/intra_tc_fwd_T8192_H32_D128.md).  Per-chunk kernels move the same bytes per chunk-head at
-# any size, so the figure scales with the token-heads of a launch.  An entry is removed when its
-# kernel changes and has not been captured again.
+# DRAM bytes (read + write) per token-head per launch, from one-kernel ncu captures of the current
+# kernels on shortened shapes of the same workloads (B=1 T=4096 H=32 for the training step, T=8192
+# H=32 for the long forward).  Per-chunk kernels move the same bytes per chunk-head at any size, so
+# the figure scales with the token-heads of a launch.  An entry is removed when its kernel changes and
+# has not been captured again.
 PROFILED_TRAFFIC = {
     ("kda_grad_tc", True): 9814.0,
     ("kda_intra_tc", False): 2609.0,   # forward record only (forward-only workloads)
@@ -235,6 +238,81 @@ def cpu_baseline(w, x_cpu: dict, budget_s: float = 15.0) -> dict:
             "seconds": elapsed}
 
 
+# ------------------------------------------------------------------ the other workloads, same process
+
+def step_roofline_of(w, ms_step: float, peaks: dict) -> dict:
+    a = algorithmic(w.K, w.V, act_bytes=2 if w.dtype == "bf16" else 4)
+    step_bytes = w.tokens * w.H * (a["fwd_bytes"] + (a["bwd_bytes"] if w.backward else 0))
+    state_bytes = 4 * w.H * w.K * w.V * (w.B if not w.varlen else 0) * (int(w.initial_state) + int(w.final_state))
+    step_bytes += state_bytes
+    step_flops = w.tokens * w.H * (a["fwd_flops"] + (a["bwd_flops"] if w.backward else 0))
+    roof_s = max(step_bytes / (peaks["hbm_gbs"] * 1e9), step_flops / (peaks["bf16_tflops"] * 1e12))
+    return {"roofline_ms": roof_s * 1e3, "frac": roof_s / (ms_step / 1e3), "bytes": step_bytes,
+            "flops": step_flops, "peak_source": peaks["source"]}
+
+
+def time_workload(name: str, dev, steps: int, warmup: int, peaks: dict) -> dict:
+    """Device time of one workload's step (forward, or forward + backward), timed step by step with CUDA
+    events on the launching stream and L2 flushed (a 256 MiB write) before every step, since the smaller
+    workloads' inputs fit in L2.  Returns ms per step, tokens/s, the step roofline fraction, the
+    dominant kernel and the clocks seen while timing."""
+    import torch
+
+    import gated_delta_rule_sm_gb300 as kda
+    from gated_delta_rule_sm_gb300 import _lib
+    from gated_delta_rule_sm_gb300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS[name]
+    x = {k: (v.to(dev) if hasattr(v, "to") else v) for k, v in make_inputs(w, device="cpu").items()}
+    names = ("q", "k", "v", "g_raw", "beta_raw", "a_log", "dt_bias")
+    kw = dict(scale=x["scale"], lower_bound=x["lower_bound"], chunk_size=x["chunk_size"],
+              cu_seqlens=x["cu_seqlens"], initial_state=x["initial_state"])
+    outs = {}
+    nsaved = kda.saved_size(x["q"], x["v"], x["cu_seqlens"]) if w.backward else 0
+    saved = torch.empty(nsaved, dtype=torch.uint8, device=dev) if nsaved > 0 else None
+
+    def step():
+        o, fs = kda.forward(*[x[n] for n in names], output_final_state=w.final_state, out=outs.get("out"),
+                            final_state=outs.get("fs"), saved=saved, **kw)
+        outs["out"], outs["fs"] = o, fs
+        if w.backward:
+            outs["grads"] = kda.backward(*[x[n] for n in names], x["dout"], grads=outs.get("grads"), saved=saved,
+                                         **kw)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0, f"device status word set during warm-up of {name}"
+    stream = torch.cuda.current_stream(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    _lib.timing_begin(64 * steps)
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    launches = _lib.timing_end(64 * steps)
+    clk = clocks.stop()
+    assert kda.device_status() == 0
+    ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+    per = {}
+    for kname, kms in launches:
+        per[kname] = per.get(kname, 0.0) + kms
+    tot = sum(per.values())
+    dom = max(per.items(), key=lambda kv: kv[1])[0] if per else None
+    del x, outs, saved, flush
+    torch.cuda.empty_cache()
+    return {"workload": name, "ms": ms, "tokens_per_s": w.tokens / (ms / 1e3),
+            "step_roofline": step_roofline_of(w, ms, peaks), "backward": w.backward,
+            "dominant_kernel": dom, "dominant_share": (per[dom] / tot) if dom else None,
+            "kernels_ms_per_step": {k: v / steps for k, v in sorted(per.items(), key=lambda kv: -kv[1])},
+            "l2": "flushed before every step", "clocks": clk}
+
+
 # ------------------------------------------------------------------ our implementation
 
 def run_ours(args, w):
@@ -277,7 +355,11 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     assert kda.device_status() == 0, "device status word set during warm-up"
 
-    # ---- device-resident timed region (inputs > L2, so no flush between steps)
+    # ---- device-resident timed region.  Inputs larger than L2 need no flush between steps; a workload
+    # that fits in L2 is timed step by step with a 256 MiB write (L2 flush) before every step.
+    peaks = read_peaks()
+    fits_l2 = step_roofline_of(w, 1.0, peaks)["bytes"] < 2 * 129e6
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if fits_l2 else None
     clocks = ClockSampler(local)
     clocks.start()
     barrier(world, dev)
@@ -285,16 +367,25 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     _lib.timing_begin(64 * args.steps)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step(x)
-    ev1.record(stream)
+    if fits_l2:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            step(x)
+            e1.record(stream)
+    else:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step(x)
+        ev1.record(stream)
     torch.cuda.synchronize()
     launches = _lib.timing_end(64 * args.steps)
     barrier(world, dev)
     clk = clocks.stop()
-    ms_total = ev0.elapsed_time(ev1)
+    ms_total = sum(e0.elapsed_time(e1) for e0, e1 in evs) if fits_l2 else ev0.elapsed_time(ev1)
     ms_step = max_over_ranks(ms_total / args.steps, world, dev)
+    del flush
     assert kda.device_status() == 0
 
     # ---- end to end: pinned host inputs -> device, the C-ABI calls, results -> pinned host.
@@ -375,7 +466,6 @@ def run_ours(args, w):
 
     tokens = w.tokens
     value = world * tokens / (ms_step / 1e3)
-    peaks = read_peaks()
 
     # ---- dominant kernel roofline
     per = {}
@@ -405,12 +495,8 @@ def run_ours(args, w):
         roofline["kernel"] = dom
         roofline["peak_source"] = peaks["source"]
         roofline["avg_launch_ms"] = tot_ms / n_launch
-    a = algorithmic(w.K, w.V, act_bytes=2 if w.dtype == "bf16" else 4)
-    step_bytes = w.tokens * w.H * (a["fwd_bytes"] + (a["bwd_bytes"] if w.backward else 0))
-    step_flops = w.tokens * w.H * (a["fwd_flops"] + (a["bwd_flops"] if w.backward else 0))
-    roof_s = max(step_bytes / (peaks["hbm_gbs"] * 1e9), step_flops / (peaks["bf16_tflops"] * 1e12))
-    step_roofline = {"roofline_ms": roof_s * 1e3, "frac": roof_s / (ms_step / 1e3),
-                     "bytes": step_bytes, "flops": step_flops, "peak_source": peaks["source"]}
+    step_roofline = step_roofline_of(w, ms_step, peaks)
+    step_bytes = step_roofline["bytes"]
     kernels = {k: {"launches": v[0], "ms_total": v[1]} for k, v in sorted(per.items(), key=lambda kv: -kv[1][1])}
 
     result = {
@@ -421,7 +507,7 @@ def run_ours(args, w):
                    "chunk_size": w.chunk_size, "backward": w.backward, "tokens_per_step": w.tokens,
                    "global_batch": w.B * world, "seq_len": w.T,
                    "parallelism": f"replicas x{world} (independent shards, no collective)",
-                   "l2": "inputs larger than L2 (no flush)" if step_bytes > 129e6 else "L2-resident inputs"},
+                   "l2": "L2 flushed before every timed step" if fits_l2 else "inputs larger than L2 (no flush)"},
         "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": len(launches),
@@ -430,6 +516,12 @@ def run_ours(args, w):
         "kernels": kernels,
         "clocks": clk,
     }
+    if world == 1 and not args.no_per_config:
+        # every other workload, timed in this process (forward-only workloads time the forward)
+        del host_in, dev_in, outs_b, host_out, outs, saved, x
+        torch.cuda.empty_cache()
+        result["per_config"] = [time_workload(n, dev, args.config_steps, args.warmup, peaks)
+                                for n in WORKLOAD_NAMES if n != w.name]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, x_cpu, budget_s=args.cpu_budget)
     if rank == 0:
@@ -478,6 +570,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip timing the other workloads")
+    ap.add_argument("--config-steps", type=int, default=10, help="timed steps per workload in per_config")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds of oracle work per reference step")
     args = ap.parse_args(argv)

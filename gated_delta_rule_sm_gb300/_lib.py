@@ -63,7 +63,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.kda_fwd_workspace_size.argtypes = [dims_p, ctypes.c_int]
         lib.kda_bwd_workspace_size.restype = ctypes.c_size_t
         lib.kda_bwd_workspace_size.argtypes = [dims_p, ctypes.c_int]
-        fwd_args = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int] + [_vp] * 4 + \
+        # ... chunk_size, cu_seqlens, cu_seqlens_host, initial_state, out, final_state, workspace, bytes, stream
+        fwd_args = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int] + [_vp] * 5 + \
             [_vp, ctypes.c_size_t, _vp]
         for name in ("kda_fwd", "kda_fwd_simt"):
             f = getattr(lib, name)
@@ -85,10 +86,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.kda_selftest_wait_timeout.argtypes = [_vp]
         lib.kda_fwd_noalloc.restype = ctypes.c_int
         lib.kda_fwd_noalloc.argtypes = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int] + \
-            [_vp] * 4 + [_vp]
+            [_vp] * 5 + [_vp]
         lib.kda_bwd.restype = ctypes.c_int
         lib.kda_bwd.argtypes = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int] + \
-            [_vp] * 2 + [_vp] * 2 + [_vp] * 8 + [_vp, ctypes.c_size_t, _vp]
+            [_vp] * 3 + [_vp] * 2 + [_vp] * 8 + [_vp, ctypes.c_size_t, _vp]
         lib.kda_saved_size.restype = ctypes.c_size_t
         lib.kda_saved_size.argtypes = [dims_p, ctypes.c_int]
         lib.kda_fwd_save.restype = ctypes.c_int
@@ -145,6 +146,25 @@ def timing_end(cap: int = 1 << 16) -> list[tuple[str, float]]:
 
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def host_offsets(cu_seqlens_host, n_expected: Optional[int] = None):
+    """A host copy of packed-document offsets as a ctypes int32 array (None stays None).
+
+    Accepts a CPU tensor or any sequence of ints.  ``n_expected``: the entry count the call needs
+    (num_seqs + 1); a copy of another length is refused here, since the library reads exactly that
+    many entries."""
+    if cu_seqlens_host is None:
+        return None
+    if isinstance(cu_seqlens_host, torch.Tensor):
+        if cu_seqlens_host.is_cuda:
+            raise ValueError("cu_seqlens_host must live in host memory")
+        vals = [int(x) for x in cu_seqlens_host.reshape(-1).tolist()]
+    else:
+        vals = [int(x) for x in cu_seqlens_host]
+    if n_expected is not None and len(vals) != n_expected:
+        raise ValueError(f"cu_seqlens_host has {len(vals)} entries, the call needs {n_expected}")
+    return (ctypes.c_int32 * len(vals))(*vals)
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -216,8 +236,8 @@ def _contig(*ts):
 
 
 def forward(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale: float, lower_bound: float = -5.0,
-            gate: str = "lower_bounded", chunk_size: int = 64, cu_seqlens=None, initial_state=None,
-            output_final_state: bool = False, out=None, final_state=None, simt: bool = False,
+            gate: str = "lower_bounded", chunk_size: int = 64, cu_seqlens=None, cu_seqlens_host=None,
+            initial_state=None, output_final_state: bool = False, out=None, final_state=None, simt: bool = False,
             saved: Optional[torch.Tensor] = None, segments: int = 0, stream: Optional[torch.cuda.Stream] = None):
     """KDA forward through ``kda_fwd`` (or ``kda_fwd_simt``).  Returns (out, final_state or None).
 
@@ -227,6 +247,8 @@ def forward(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale: float, lower_bou
     ``kda_fwd_save`` and keeps the per-chunk quantities there for ``backward(..., saved=...)``.
     ``segments`` > 0: run ``kda_fwd_segmented``, the chain cut into that many pieces per row (rows of
     T tokens only; for long rows with few rows x heads).
+    ``cu_seqlens_host``: optional host copy of ``cu_seqlens`` (CPU tensor or sequence); the library then
+    checks the offsets before it launches anything and a bad one raises ``KdaError`` (invalid argument).
     """
     lib = load()
     _contig(q, k, v, g_raw, beta_raw, a_log, dt_bias, cu_seqlens, initial_state)
@@ -255,8 +277,9 @@ def forward(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale: float, lower_bou
         return out, final_state
     ws_bytes = lib.kda_fwd_workspace_size(ctypes.byref(dims), chunk_size)
     ws = workspace_cache.get(q.device, "fwd", ws_bytes)
+    cu_h = host_offsets(cu_seqlens_host, N + 1 if cu_seqlens is not None else None)
     head = (ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw), _ptr(a_log),
-            _ptr(dt_bias), float(scale), float(lower_bound), int(chunk_size), _ptr(cu_seqlens),
+            _ptr(dt_bias), float(scale), float(lower_bound), int(chunk_size), _ptr(cu_seqlens), cu_h,
             _ptr(initial_state), _ptr(out), _ptr(final_state))
     tail = (_ptr(ws), ctypes.c_size_t(ws.numel()), ctypes.c_void_p(st.cuda_stream))
     if saved is not None:
@@ -279,7 +302,8 @@ def saved_size(q, v, cu_seqlens=None, chunk_size: int = 64, gate: str = "lower_b
 
 
 def backward(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale: float, lower_bound: float = -5.0,
-             gate: str = "lower_bounded", chunk_size: int = 64, cu_seqlens=None, initial_state=None, dfinal_state=None,
+             gate: str = "lower_bounded", chunk_size: int = 64, cu_seqlens=None, cu_seqlens_host=None,
+             initial_state=None, dfinal_state=None,
              want_dinitial_state: bool = True, grads: Optional[dict] = None,
              saved: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> dict:
     """KDA backward through ``kda_bwd``.  Returns a dict of fp32 gradients.
@@ -305,8 +329,9 @@ def backward(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale: float, lo
     ws_bytes = lib.kda_bwd_workspace_size(ctypes.byref(dims), chunk_size)
     ws = workspace_cache.get(dev, "bwd", ws_bytes)
     st = stream if stream is not None else torch.cuda.current_stream(dev)
+    cu_h = host_offsets(cu_seqlens_host, N + 1 if cu_seqlens is not None else None)
     head = (ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw), _ptr(a_log),
-            _ptr(dt_bias), float(scale), float(lower_bound), int(chunk_size), _ptr(cu_seqlens),
+            _ptr(dt_bias), float(scale), float(lower_bound), int(chunk_size), _ptr(cu_seqlens), cu_h,
             _ptr(initial_state), _ptr(dout), _ptr(dfinal_state), _ptr(grads["dq"]), _ptr(grads["dk"]),
             _ptr(grads["dv"]), _ptr(grads["dg_raw"]), _ptr(grads["dbeta_raw"]), _ptr(grads["da_log"]),
             _ptr(grads["ddt_bias"]), _ptr(grads.get("dinitial_state")))
@@ -361,13 +386,28 @@ def short_conv_backward(x, weight, bias, dy, *, cu_seqlens=None, stream: Optiona
     return g
 
 
+def _norm_types(o, *others):
+    """The norm kernels read every activation with o's element size and the weight as fp32: refuse
+    anything else before it reaches them (a bf16 weight, or a bf16 gate beside fp32 o, would be read
+    past its end).  ``others``: gate, weight[, dy]."""
+    gate, weight = others[0], others[1]
+    acts = [gate] + list(others[2:])
+    if any(t.dtype != o.dtype for t in acts):
+        raise ValueError(f"gate and dy must have o's dtype ({o.dtype})")
+    if weight.dtype != torch.float32:
+        raise ValueError(f"weight must be float32, got {weight.dtype}")
+    if any(t.device != o.device for t in others):
+        raise ValueError("o, gate, weight and dy must be on one device")
+
+
 def gated_norm(o, gate, weight, *, eps: float = 1e-6, out=None, stream: Optional[torch.cuda.Stream] = None):
     """The output epilogue through ``kda_gated_norm_fwd``: o / sqrt(mean(o^2) + eps) * weight * sigmoid(gate)
     over the last axis.  o, gate: [..., V] (bf16 or fp32, same dtype); weight: [V] fp32.  Returns y like o."""
     lib = load()
     _contig(o, gate, weight)
-    if gate.shape != o.shape or gate.dtype != o.dtype or weight.numel() != o.shape[-1]:
+    if gate.shape != o.shape or weight.numel() != o.shape[-1]:
         raise ValueError("gate must match o, and weight must hold o.shape[-1] values")
+    _norm_types(o, gate, weight)
     V = o.shape[-1]
     if out is None:
         out = torch.empty_like(o)
@@ -383,6 +423,7 @@ def gated_norm_backward(o, gate, weight, dy, *, eps: float = 1e-6, stream: Optio
     _contig(o, gate, weight, dy)
     if gate.shape != o.shape or dy.shape != o.shape or weight.numel() != o.shape[-1]:
         raise ValueError("gate and dy must match o, and weight must hold o.shape[-1] values")
+    _norm_types(o, gate, weight, dy)
     V = o.shape[-1]
     rows = o.numel() // V
     f32 = dict(dtype=torch.float32, device=o.device)

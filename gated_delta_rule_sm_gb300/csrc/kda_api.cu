@@ -163,10 +163,26 @@ static void carve(Params& p, const WsPlan& w, void* ws) {
     }
 }
 
-static kda_status common_checks(const kda_dims* dims, int chunk_size, const int32_t* cu, const void* q,
-                                const void* k, const void* v, const void* g_raw, const void* beta_raw,
-                                const float* a_log, const float* dt_bias, float scale, float lb, Shape* s) {
+// The packed-document offsets' contract (nemo_automodel `kimi_k3.cp`, `segment_cu_seqlens` and
+// `doc_ids_from_cu_seqlens`): N + 1 entries, starting at 0, never decreasing, ending at the token
+// count.  Checked here when the caller hands over a host copy; plan_kernel checks the device array
+// otherwise.
+static kda_status check_cu_host(const Shape& s, const int32_t* cu, const int32_t* cu_host) {
+    if (!cu_host) return KDA_OK;
+    if (!cu) return KDA_ERR_INVALID_ARG;   // a host copy of offsets the call does not use
+    if (cu_host[0] != 0 || cu_host[s.N] != s.TT) return KDA_ERR_INVALID_ARG;
+    for (int n = 0; n < s.N; ++n)
+        if (cu_host[n + 1] < cu_host[n]) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
+static kda_status common_checks(const kda_dims* dims, int chunk_size, const int32_t* cu, const int32_t* cu_host,
+                                const void* q, const void* k, const void* v, const void* g_raw,
+                                const void* beta_raw, const float* a_log, const float* dt_bias, float scale, float lb,
+                                Shape* s) {
     kda_status st = check_dims(dims, chunk_size, cu != nullptr, s);
+    if (st != KDA_OK) return st;
+    st = check_cu_host(*s, cu, cu_host);
     if (st != KDA_OK) return st;
     if (!q || !k || !v || !g_raw || !beta_raw || !a_log || !dt_bias) return KDA_ERR_INVALID_ARG;
     if (!(lb < 0.0f) || !isfinite(lb)) return KDA_ERR_INVALID_ARG;   // lower_bound < 0 under either gate, as the page's executor checks
@@ -361,12 +377,12 @@ size_t kda_bwd_workspace_size(const kda_dims* dims, int chunk_size) {
 
 kda_status kda_fwd_simt(const kda_dims* dims, const void* q, const void* k, const void* v, const void* g_raw,
                         const void* beta_raw, const float* a_log, const float* dt_bias, float scale,
-                        float lower_bound, int chunk_size, const int32_t* cu_seqlens, const float* initial_state,
-                        void* out, float* final_state, void* workspace, size_t workspace_bytes,
-                        cudaStream_t stream) {
+                        float lower_bound, int chunk_size, const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                        const float* initial_state, void* out, float* final_state, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
     Shape s;
-    kda_status st = common_checks(dims, chunk_size, cu_seqlens, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale,
-                                  lower_bound, &s);
+    kda_status st = common_checks(dims, chunk_size, cu_seqlens, cu_seqlens_host, q, k, v, g_raw, beta_raw, a_log,
+                                  dt_bias, scale, lower_bound, &s);
     if (st != KDA_OK) return st;
     if (!out) return KDA_ERR_INVALID_ARG;
     Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
@@ -378,11 +394,12 @@ kda_status kda_fwd_simt(const kda_dims* dims, const void* q, const void* k, cons
 
 kda_status kda_fwd(const kda_dims* dims, const void* q, const void* k, const void* v, const void* g_raw,
                    const void* beta_raw, const float* a_log, const float* dt_bias, float scale, float lower_bound,
-                   int chunk_size, const int32_t* cu_seqlens, const float* initial_state, void* out,
-                   float* final_state, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                   int chunk_size, const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                   const float* initial_state, void* out, float* final_state, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream) {
     Shape s;
-    kda_status st = common_checks(dims, chunk_size, cu_seqlens, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale,
-                                  lower_bound, &s);
+    kda_status st = common_checks(dims, chunk_size, cu_seqlens, cu_seqlens_host, q, k, v, g_raw, beta_raw, a_log,
+                                  dt_bias, scale, lower_bound, &s);
     if (st != KDA_OK) return st;
     if (!out) return KDA_ERR_INVALID_ARG;
     Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
@@ -390,7 +407,8 @@ kda_status kda_fwd(const kda_dims* dims, const void* q, const void* k, const voi
     // the tensor-core path needs 16-byte aligned activations and a gate it can factorise
     if (!tc_eligible(s) || !tc_fwd_gate_ok(s, lower_bound) || !tc_inputs_aligned(p))
         return kda_fwd_simt(dims, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, chunk_size,
-                            cu_seqlens, initial_state, out, final_state, workspace, workspace_bytes, stream);
+                            cu_seqlens, cu_seqlens_host, initial_state, out, final_state, workspace, workspace_bytes,
+                            stream);
     p.out = out;
     p.ST = final_state;
     return fwd_tc(s, p, workspace, workspace_bytes, stream);
@@ -398,13 +416,13 @@ kda_status kda_fwd(const kda_dims* dims, const void* q, const void* k, const voi
 
 kda_status kda_bwd(const kda_dims* dims, const void* q, const void* k, const void* v, const void* g_raw,
                    const void* beta_raw, const float* a_log, const float* dt_bias, float scale, float lower_bound,
-                   int chunk_size, const int32_t* cu_seqlens, const float* initial_state, const void* dout,
-                   const float* dfinal_state, float* dq, float* dk, float* dv, float* dg_raw, float* dbeta_raw,
-                   float* da_log, float* ddt_bias, float* dinitial_state, void* workspace, size_t workspace_bytes,
-                   cudaStream_t stream) {
+                   int chunk_size, const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                   const float* initial_state, const void* dout, const float* dfinal_state, float* dq, float* dk,
+                   float* dv, float* dg_raw, float* dbeta_raw, float* da_log, float* ddt_bias, float* dinitial_state,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     Shape s;
-    kda_status st = common_checks(dims, chunk_size, cu_seqlens, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale,
-                                  lower_bound, &s);
+    kda_status st = common_checks(dims, chunk_size, cu_seqlens, cu_seqlens_host, q, k, v, g_raw, beta_raw, a_log,
+                                  dt_bias, scale, lower_bound, &s);
     if (st != KDA_OK) return st;
     if (!dout || !dq || !dk || !dv || !dg_raw || !dbeta_raw || !da_log || !ddt_bias) return KDA_ERR_INVALID_ARG;
     Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
@@ -439,8 +457,8 @@ kda_status kda_fwd_segmented(const kda_dims* dims, const void* q, const void* k,
                              float lower_bound, int chunk_size, int segments, const float* initial_state, void* out,
                              float* final_state, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     Shape s;
-    kda_status st = common_checks(dims, chunk_size, nullptr, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale,
-                                  lower_bound, &s);
+    kda_status st = common_checks(dims, chunk_size, nullptr, nullptr, q, k, v, g_raw, beta_raw, a_log, dt_bias,
+                                  scale, lower_bound, &s);
     if (st != KDA_OK) return st;
     if (!out || segments < 1) return KDA_ERR_INVALID_ARG;
     Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, nullptr, initial_state);
@@ -494,12 +512,13 @@ size_t kda_saved_size(const kda_dims* dims, int chunk_size) {
 
 kda_status kda_fwd_save(const kda_dims* dims, const void* q, const void* k, const void* v, const void* g_raw,
                         const void* beta_raw, const float* a_log, const float* dt_bias, float scale,
-                        float lower_bound, int chunk_size, const int32_t* cu_seqlens, const float* initial_state,
-                        void* out, float* final_state, void* saved, size_t saved_bytes, void* workspace,
+                        float lower_bound, int chunk_size, const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                        const float* initial_state, void* out, float* final_state, void* saved, size_t saved_bytes,
+                        void* workspace,
                         size_t workspace_bytes, cudaStream_t stream) {
     Shape s;
-    kda_status st = common_checks(dims, chunk_size, cu_seqlens, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale,
-                                  lower_bound, &s);
+    kda_status st = common_checks(dims, chunk_size, cu_seqlens, cu_seqlens_host, q, k, v, g_raw, beta_raw, a_log,
+                                  dt_bias, scale, lower_bound, &s);
     if (st != KDA_OK) return st;
     if (!out) return KDA_ERR_INVALID_ARG;
     Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
@@ -514,14 +533,15 @@ kda_status kda_fwd_save(const kda_dims* dims, const void* q, const void* k, cons
 
 kda_status kda_bwd_saved(const kda_dims* dims, const void* q, const void* k, const void* v, const void* g_raw,
                          const void* beta_raw, const float* a_log, const float* dt_bias, float scale,
-                         float lower_bound, int chunk_size, const int32_t* cu_seqlens, const float* initial_state,
-                         const void* dout, const float* dfinal_state, float* dq, float* dk, float* dv,
+                         float lower_bound, int chunk_size, const int32_t* cu_seqlens,
+                         const int32_t* cu_seqlens_host, const float* initial_state, const void* dout,
+                         const float* dfinal_state, float* dq, float* dk, float* dv,
                          float* dg_raw, float* dbeta_raw, float* da_log, float* ddt_bias, float* dinitial_state,
                          const void* saved, size_t saved_bytes, void* workspace, size_t workspace_bytes,
                          cudaStream_t stream) {
     Shape s;
-    kda_status st = common_checks(dims, chunk_size, cu_seqlens, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale,
-                                  lower_bound, &s);
+    kda_status st = common_checks(dims, chunk_size, cu_seqlens, cu_seqlens_host, q, k, v, g_raw, beta_raw, a_log,
+                                  dt_bias, scale, lower_bound, &s);
     if (st != KDA_OK) return st;
     if (!dout || !dq || !dk || !dv || !dg_raw || !dbeta_raw || !da_log || !ddt_bias) return KDA_ERR_INVALID_ARG;
     Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,

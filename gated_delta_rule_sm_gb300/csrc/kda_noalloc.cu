@@ -35,19 +35,20 @@ kda_status scratch_address(void** out) {
 extern "C" kda_status kda_fwd_noalloc(const kda_dims* dims, const void* q, const void* k, const void* v,
                                       const void* g_raw, const void* beta_raw, const float* a_log,
                                       const float* dt_bias, float scale, float lower_bound, int chunk_size,
-                                      const int32_t* cu_seqlens, const float* initial_state, void* out,
-                                      float* final_state, cudaStream_t stream) {
+                                      const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                                      const float* initial_state, void* out, float* final_state,
+                                      cudaStream_t stream) {
     if (!dims) return KDA_ERR_INVALID_ARG;
     const size_t need = kda_fwd_workspace_size(dims, chunk_size);
     if (need == 0) {
         // invalid shape: let the ordinary entry point report the precise error
         return kda_fwd(dims, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, chunk_size, cu_seqlens,
-                       initial_state, out, final_state, nullptr, 0, stream);
+                       cu_seqlens_host, initial_state, out, final_state, nullptr, 0, stream);
     }
     if (need > KDA_NOALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
     void* ws = nullptr;
     const kda_status st = scratch_address(&ws);
     if (st != KDA_OK) return st;
     return kda_fwd(dims, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, chunk_size, cu_seqlens,
-                   initial_state, out, final_state, ws, KDA_NOALLOC_SCRATCH_BYTES, stream);
+                   cu_seqlens_host, initial_state, out, final_state, ws, KDA_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -142,7 +142,8 @@ kda_status norm_check(int64_t rows, int V, int dtype, const void* o, const void*
     if (rows < 1 || V < 1) return KDA_ERR_INVALID_ARG;
     if (dtype != KDA_BF16 && dtype != KDA_FP32) return KDA_ERR_INVALID_ARG;
     if (!o || !gate || !w) return KDA_ERR_INVALID_ARG;
-    if (!(eps >= 0.f) || !isfinite(eps)) return KDA_ERR_INVALID_ARG;
+    // eps > 0: with eps = 0 an all-zero row would give 0 * inf = NaN in y, do and dgate
+    if (!(eps > 0.f) || !isfinite(eps)) return KDA_ERR_INVALID_ARG;
     if (V > kNormMaxV) return KDA_ERR_UNSUPPORTED;
     if (rows > (1LL << 40) / V) return KDA_ERR_UNSUPPORTED;
     return KDA_OK;

@@ -39,10 +39,28 @@
  * cu_seqlens != NULL, B must be 1 and segment n is tokens
  * [cu_seqlens[n], cu_seqlens[n+1]) of the T tokens; each segment is its own
  * recurrence starting from initial_state[n] (or zero).  Without cu_seqlens
- * the N = B rows are the segments.
+ * the N = B rows are the segments.  The same page's contract for the offsets
+ * (`segment_cu_seqlens`, `doc_ids_from_cu_seqlens`): N + 1 entries, the
+ * first 0, never decreasing, the last equal to T (empty segments are
+ * allowed and pass their state through).
+ *   - cu_seqlens_host (optional, HOST memory, N + 1 int32, read during the
+ *     call only): a host copy of the same offsets.  When given, the contract
+ *     is checked on the host and a violation returns KDA_ERR_INVALID_ARG
+ *     before anything is enqueued; it is also KDA_ERR_INVALID_ARG without
+ *     cu_seqlens.  The library trusts the caller that both copies agree.
+ *   - Without the host copy the device array is checked on the device by the
+ *     first kernel of the call.  A violation then cannot change the return
+ *     code (the call has already returned KDA_OK): the kernel records
+ *     KDA_ERR_INVALID_ARG in the device status word (kda_device_status) and
+ *     empties the call's chunk table, so every later kernel of the call
+ *     finds no chunk to process and touches no token of any segment: out
+ *     and the per-token gradients are not written, while final_state,
+ *     dinitial_state and the parameter gradients get what an all-empty
+ *     problem gives (the entering state, the final-state gradient, zeros).
+ *     Read the status word before using the results.
  *
- * Ownership: every pointer is a DEVICE pointer owned by the caller (cu_seqlens
- * too).  The library allocates no memory, keeps no pointer after a call
+ * Ownership: every pointer except cu_seqlens_host is a DEVICE pointer owned
+ * by the caller (cu_seqlens too).  The library allocates no memory, keeps no pointer after a call
  * returns, and enqueues all work on `stream` asynchronously; outputs are
  * fully overwritten.  Scratch memory comes from the caller's `workspace`
  * (device, 256-byte aligned, at least the size the *_workspace_size query
@@ -127,7 +145,7 @@ size_t kda_bwd_workspace_size(const kda_dims* dims, int chunk_size);
 kda_status kda_fwd(const kda_dims* dims,
                    const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
                    const float* a_log, const float* dt_bias, float scale, float lower_bound, int chunk_size,
-                   const int32_t* cu_seqlens, const float* initial_state,
+                   const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, const float* initial_state,
                    void* out, float* final_state,
                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
@@ -135,7 +153,7 @@ kda_status kda_fwd(const kda_dims* dims,
 kda_status kda_fwd_simt(const kda_dims* dims,
                         const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
                         const float* a_log, const float* dt_bias, float scale, float lower_bound, int chunk_size,
-                        const int32_t* cu_seqlens, const float* initial_state,
+                        const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, const float* initial_state,
                         void* out, float* final_state,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
@@ -150,7 +168,7 @@ kda_status kda_fwd_simt(const kda_dims* dims,
 kda_status kda_bwd(const kda_dims* dims,
                    const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
                    const float* a_log, const float* dt_bias, float scale, float lower_bound, int chunk_size,
-                   const int32_t* cu_seqlens, const float* initial_state,
+                   const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, const float* initial_state,
                    const void* dout, const float* dfinal_state,
                    float* dq, float* dk, float* dv, float* dg_raw, float* dbeta_raw,
                    float* da_log, float* ddt_bias, float* dinitial_state,
@@ -182,13 +200,13 @@ size_t kda_saved_size(const kda_dims* dims, int chunk_size);
 kda_status kda_fwd_save(const kda_dims* dims,
                         const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
                         const float* a_log, const float* dt_bias, float scale, float lower_bound, int chunk_size,
-                        const int32_t* cu_seqlens, const float* initial_state,
+                        const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, const float* initial_state,
                         void* out, float* final_state, void* saved, size_t saved_bytes,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
 kda_status kda_bwd_saved(const kda_dims* dims,
                          const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
                          const float* a_log, const float* dt_bias, float scale, float lower_bound, int chunk_size,
-                         const int32_t* cu_seqlens, const float* initial_state,
+                         const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, const float* initial_state,
                          const void* dout, const float* dfinal_state,
                          float* dq, float* dk, float* dv, float* dg_raw, float* dbeta_raw,
                          float* da_log, float* ddt_bias, float* dinitial_state,
@@ -215,7 +233,10 @@ kda_status kda_device_status(int reset);
  * call).  Shapes whose workspace (kda_fwd_workspace_size) exceeds that size
  * return KDA_ERR_WORKSPACE.  The first call on a device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  All calls share the one
+ * make that first call before any stream capture.  The address is kept for
+ * the life of the process: after cudaDeviceReset on a device the kept
+ * address no longer names the array in the new context, so do not call this
+ * entry on a device that has been reset.  All calls share the one
  * array: calls that overlap on the GPU (different streams, or several host
  * threads) race and must be serialised by the caller.  No scratch content
  * needs to start at zero (every call rewrites what it reads).
@@ -224,7 +245,7 @@ kda_status kda_device_status(int reset);
 kda_status kda_fwd_noalloc(const kda_dims* dims,
                            const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
                            const float* a_log, const float* dt_bias, float scale, float lower_bound, int chunk_size,
-                           const int32_t* cu_seqlens, const float* initial_state,
+                           const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, const float* initial_state,
                            void* out, float* final_state, cudaStream_t stream);
 
 /*
@@ -268,14 +289,15 @@ kda_status kda_fwd_segmented(const kda_dims* dims,
  * reduced in fp32.  Neither prints the formula.  This library's reading, per
  * row of V values (one token of one head, rows = B * T * H):
  *     y_v = o_v / sqrt(mean_u o_u^2 + eps) * weight_v * sigmoid(gate_v)
- * Layouts:
+ * Layouts (every activation in the one `dtype`; the kernels read each of
+ * them with that element size, so a buffer of another type is misread):
  *   o, gate, y, dy   [rows, V] in `dtype` (bf16 or fp32);
- *   weight [V], dweight [V], do, dgate [rows, V]   fp32.
+ *   weight [V] fp32 (also when dtype is bf16), dweight [V], do, dgate [rows, V]   fp32.
  * The sum of squares and every gradient are computed in fp32.  dweight sums
  * over all rows in a fixed order, so results are deterministic.
  * Errors:
  *   - KDA_ERR_INVALID_ARG: rows < 1, V < 1, a bad dtype, a NULL pointer, or
- *     eps < 0 or not finite;
+ *     eps <= 0 or not finite (eps = 0 would turn an all-zero row into NaN);
  *   - KDA_ERR_UNSUPPORTED: V > 256;
  *   - KDA_ERR_WORKSPACE: the backward's workspace is too small or not
  *     256-byte aligned; it needs kda_gated_norm_bwd_workspace_size() bytes.

@@ -50,9 +50,9 @@ def _dims(**kw):
     return _lib.KdaDims(**d)
 
 
-def _fwd(lib, dims, chunk=64, lb=-5.0, scale=0.125, ptr=1, ws=None, ws_bytes=0, cu=None):
+def _fwd(lib, dims, chunk=64, lb=-5.0, scale=0.125, ptr=1, ws=None, ws_bytes=0, cu=None, cu_host=None):
     p = ctypes.c_void_p(ptr) if ptr else None
-    return lib.kda_fwd(ctypes.byref(dims), p, p, p, p, p, p, p, scale, lb, chunk, cu, None, p, None, ws,
+    return lib.kda_fwd(ctypes.byref(dims), p, p, p, p, p, p, p, scale, lb, chunk, cu, cu_host, None, p, None, ws,
                        ctypes.c_size_t(ws_bytes), None)
 
 
@@ -90,6 +90,52 @@ def test_varlen_validation(lib):
     assert _fwd(lib, _dims(num_seqs=0), cu=cu) == _lib.KDA_ERR_INVALID_ARG
 
 
+def _bwd(lib, dims, cu=None, cu_host=None, ptr=16):
+    p = ctypes.c_void_p(ptr)
+    return lib.kda_bwd(ctypes.byref(dims), p, p, p, p, p, p, p, 0.125, -5.0, 64, cu, cu_host, None, p, None,
+                       p, p, p, p, p, p, p, None, None, ctypes.c_size_t(0), None)
+
+
+@pytest.mark.parametrize("offsets,ok", [
+    ([0, 100, 256], True),
+    ([0, 0, 100, 100, 256], True),      # empty segments pass their state through
+    ([0, 256], True),
+    ([1, 100, 256], False),             # does not start at 0
+    ([0, 100, 255], False),             # does not end at T
+    ([0, 100, 300], False),             # ends past T
+    ([0, 150, 100, 256], False),        # decreasing
+    ([0, -4, 256], False),
+])
+def test_host_offsets_validation(lib, offsets, ok):
+    """A host copy of cu_seqlens is checked before anything is enqueued (packed-document contract:
+    N + 1 entries from 0, never decreasing, ending at T).  Valid copies get past validation and stop at
+    the missing workspace; the device pointer is never dereferenced here."""
+    n = len(offsets) - 1
+    host = _lib.host_offsets(offsets, n + 1)
+    cu = ctypes.c_void_p(4096)          # stands for the device copy; not read on the host
+    want = _lib.KDA_ERR_WORKSPACE if ok else _lib.KDA_ERR_INVALID_ARG
+    d = _dims(num_seqs=n)
+    assert _fwd(lib, d, cu=cu, cu_host=host, ptr=16) == want
+    assert _bwd(lib, d, cu=cu, cu_host=host) == want
+    p = ctypes.c_void_p(16)
+    assert lib.kda_fwd_simt(ctypes.byref(d), p, p, p, p, p, p, p, 0.125, -5.0, 64, cu, host, None, p, None, None,
+                            ctypes.c_size_t(0), None) == want
+    d128 = _dims(num_seqs=n, K=128, V=128)
+    want_save = _lib.KDA_ERR_WORKSPACE if ok else _lib.KDA_ERR_INVALID_ARG   # saved buffer missing
+    assert lib.kda_fwd_save(ctypes.byref(d128), p, p, p, p, p, p, p, 0.125, -5.0, 64, cu, host, None, p, None,
+                            None, ctypes.c_size_t(0), None, ctypes.c_size_t(0), None) == want_save
+    assert lib.kda_bwd_saved(ctypes.byref(d128), p, p, p, p, p, p, p, 0.125, -5.0, 64, cu, host, None, p, None,
+                             p, p, p, p, p, p, p, None, None, ctypes.c_size_t(0), None, ctypes.c_size_t(0),
+                             None) == want_save
+
+
+def test_host_offsets_without_device_offsets(lib):
+    host = _lib.host_offsets([0, 256], 2)
+    assert _fwd(lib, _dims(), cu=None, cu_host=host, ptr=16) == _lib.KDA_ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        _lib.host_offsets([0, 100, 256], 2)        # wrong entry count for the call
+
+
 def test_workspace_validation(lib):
     d = _dims()
     need = lib.kda_fwd_workspace_size(ctypes.byref(d), 64)
@@ -111,13 +157,13 @@ def test_workspace_sizes_grow_with_problem(lib):
 
 def _fwd_save(lib, dims, saved=None, saved_bytes=0, ptr=16, lb=-5.0):
     p = ctypes.c_void_p(ptr)
-    return lib.kda_fwd_save(ctypes.byref(dims), p, p, p, p, p, p, p, 0.125, lb, 64, None, None, p, None,
+    return lib.kda_fwd_save(ctypes.byref(dims), p, p, p, p, p, p, p, 0.125, lb, 64, None, None, None, p, None,
                             saved, ctypes.c_size_t(saved_bytes), None, ctypes.c_size_t(0), None)
 
 
 def _bwd_saved(lib, dims, saved=None, saved_bytes=0, ptr=16):
     p = ctypes.c_void_p(ptr)
-    return lib.kda_bwd_saved(ctypes.byref(dims), p, p, p, p, p, p, p, 0.125, -5.0, 64, None, None, p, None,
+    return lib.kda_bwd_saved(ctypes.byref(dims), p, p, p, p, p, p, p, 0.125, -5.0, 64, None, None, None, p, None,
                              p, p, p, p, p, p, p, None, saved, ctypes.c_size_t(saved_bytes), None,
                              ctypes.c_size_t(0), None)
 
@@ -232,6 +278,7 @@ def test_gated_norm_validation(lib):
     assert fwd(V=0) == _lib.KDA_ERR_INVALID_ARG
     assert fwd(dtype=3) == _lib.KDA_ERR_INVALID_ARG
     assert fwd(eps=-1.0) == _lib.KDA_ERR_INVALID_ARG
+    assert fwd(eps=0.0) == _lib.KDA_ERR_INVALID_ARG      # an all-zero row would turn into NaN
     assert fwd(eps=float("nan")) == _lib.KDA_ERR_INVALID_ARG
     assert fwd(o=None) == _lib.KDA_ERR_INVALID_ARG
     assert fwd(y=None) == _lib.KDA_ERR_INVALID_ARG
@@ -243,3 +290,19 @@ def test_gated_norm_validation(lib):
                                                           ctypes.c_size_t(nbytes), None)
     assert bwd() == _lib.KDA_ERR_WORKSPACE
     assert bwd(ctypes.c_void_p(4096 + 16), ws(10, 128)) == _lib.KDA_ERR_WORKSPACE       # misaligned
+
+
+def test_gated_norm_binding_refuses_mixed_types():
+    """The norm kernels read every activation with o's element size and the weight as fp32; the
+    binding refuses other combinations before anything reaches the library."""
+    import torch
+    o = torch.zeros(4, 128, dtype=torch.bfloat16)
+    w = torch.ones(128)
+    _lib._norm_types(o, o.clone(), w)                                    # accepted
+    _lib._norm_types(o, o.clone(), w, o.clone())
+    with pytest.raises(ValueError):
+        _lib._norm_types(o, o.clone(), w.to(torch.bfloat16))             # bf16 weight
+    with pytest.raises(ValueError):
+        _lib._norm_types(o, o.float(), w)                                # fp32 gate beside bf16 o
+    with pytest.raises(ValueError):
+        _lib._norm_types(o.float(), o.float(), w, o)                     # bf16 dy beside fp32 o

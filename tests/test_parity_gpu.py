@@ -85,6 +85,69 @@ def test_fwd_varlen_with_empty_and_tiny_documents():
     _check_fwd(x, "bf16")
 
 
+def test_fwd_varlen_with_host_offsets():
+    """The host copy of cu_seqlens: a valid copy changes nothing; a bad one is refused before launch."""
+    import gated_delta_rule_sm_gb300 as kda
+    from gated_delta_rule_sm_gb300 import KdaError
+    lens = [5, 0, 64, 130, 1, 63, 65]
+    w = Workload("t", B=1, T=sum(lens), H=2, K=128, V=128, varlen=True, initial_state=True, seed=7)
+    x = make_inputs(w, device=DEV, lengths=lens)
+    ref, ref_fs = gpu_fwd(x)
+    host = x["cu_seqlens"].cpu()
+    args = [x[n] for n in ("q", "k", "v", "g_raw", "beta_raw", "a_log", "dt_bias")]
+    kw = dict(scale=x["scale"], lower_bound=x["lower_bound"], cu_seqlens=x["cu_seqlens"],
+              initial_state=x["initial_state"], output_final_state=True)
+    out, fs = kda.forward(*args, cu_seqlens_host=host, **kw)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    assert torch.equal(out, ref) and torch.equal(fs, ref_fs)
+    bad = host.clone()
+    bad[2], bad[3] = bad[3], bad[2]                      # decreasing
+    with pytest.raises(KdaError) as ei:
+        kda.forward(*args, cu_seqlens_host=bad, **kw)
+    assert ei.value.code == 1                            # KDA_ERR_INVALID_ARG, nothing enqueued
+
+
+@pytest.mark.parametrize("bad", [[0, 150, 100, 256], [8, 100, 256], [0, 100, 200]],
+                         ids=["decreasing", "nonzero_start", "short_end"])
+@pytest.mark.parametrize("path", ["tc", "simt", "bwd"])
+def test_bad_device_offsets_reported_in_status_word(bad, path):
+    """Device-only cu_seqlens that break the packed-document contract (every value inside [0, T]): the
+    call returns OK, the first kernel records KDA_ERR_INVALID_ARG in the status word and empties the
+    chunk table, so no later kernel touches a token (out and dv keep their NaN fill) and the context
+    stays usable for the next call."""
+    import gated_delta_rule_sm_gb300 as kda
+    D = 64 if path == "simt" else 128
+    w = Workload("t", B=1, T=256, H=2, K=D, V=D, varlen=True, initial_state=True, backward=(path == "bwd"), seed=40)
+    x = make_inputs(w, device=DEV, lengths=[100, 156])
+    x["cu_seqlens"] = torch.tensor(bad, dtype=torch.int32, device=DEV)
+    args = [x[n] for n in ("q", "k", "v", "g_raw", "beta_raw", "a_log", "dt_bias")]
+    kw = dict(scale=x["scale"], lower_bound=x["lower_bound"], cu_seqlens=x["cu_seqlens"])
+    device_status()                                       # start from a clear word
+    if path == "bwd":
+        N = len(bad) - 1
+        f32 = dict(dtype=torch.float32, device=DEV)
+        K = x["q"].shape[-1]
+        grads = dict(dq=torch.full((1, 256, 2, K), float("nan"), **f32), dk=torch.full((1, 256, 2, K), float("nan"), **f32),
+                     dv=torch.full((1, 256, 2, K), float("nan"), **f32), dg_raw=torch.full((1, 256, 2, K), float("nan"), **f32),
+                     dbeta_raw=torch.full((1, 256, 2), float("nan"), **f32), da_log=torch.empty(2, **f32),
+                     ddt_bias=torch.empty(2 * K, **f32), dinitial_state=torch.empty((N, 2, K, K), **f32))
+        kw["initial_state"] = torch.zeros((N, 2, K, K), **f32)
+        kda.backward(*args, x["dout"], grads=grads, **kw)
+        assert kda.device_status() == 1                  # KDA_ERR_INVALID_ARG
+        assert torch.isnan(grads["dv"]).all() and torch.isnan(grads["dg_raw"]).all()
+    else:
+        N = len(bad) - 1
+        kw["initial_state"] = torch.zeros((N, 2, D, D), dtype=torch.float32, device=DEV)
+        out = torch.full_like(x["v"], float("nan"))
+        kda.forward(*args, out=out, simt=(path == "simt"), **kw)
+        assert kda.device_status() == 1
+        assert torch.isnan(out.float()).all()
+    # the context is still usable: a valid call right after runs clean and matches the oracle
+    y = make_inputs(Workload("t", B=1, T=130, H=2, K=D, V=D, seed=41), device=DEV)
+    _check_fwd(y, "bf16", simt=(path == "simt"))
+
+
 def test_fwd_no_final_state_and_simt_agree():
     w = Workload("t", B=1, T=257, H=2, K=128, V=128, seed=8)
     x = make_inputs(w, device=DEV)

@@ -4,8 +4,9 @@ Plugin hosts that own every device allocation, or latency-critical loops that mu
 cudaMalloc (it can synchronise the device), cannot hand the library a workspace.  The entry point
 under test takes its scratch from a fixed-size array built into the library instead.  Here it is
 called through the C ABI twice in a row and compared with kda_fwd (which takes a caller-provided
-workspace) within the parity tolerance; a shape too large for the built-in scratch must be
-rejected with KDA_ERR_WORKSPACE.  This file is collected last so that a failure here leaves every
+workspace): the same kernels run on the same inputs with only the scratch address changed, so the
+results must be bit-identical; a shape too large for the built-in scratch must be rejected with
+KDA_ERR_WORKSPACE.  This file is collected last so that a failure here leaves every
 other test already run.
 """
 from __future__ import annotations
@@ -22,7 +23,7 @@ if not torch.cuda.is_available():
 
 from gated_delta_rule_sm_gb300 import _lib  # noqa: E402
 from gated_delta_rule_sm_gb300.inputs import Workload, make_inputs  # noqa: E402
-from kda_cases import ACT, gpu_fwd, rel_err, tol  # noqa: E402
+from kda_cases import ACT, gpu_fwd  # noqa: E402
 
 DEV = "cuda:0"
 
@@ -32,7 +33,7 @@ def _noalloc(x, out, fs):
     dims = _lib.make_dims(x["q"], x["v"], x.get("cu_seqlens"))
     ptr = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
     return lib.kda_fwd_noalloc(ctypes.byref(dims), *[ptr(x[n]) for n in ACT], float(x["scale"]),
-                               float(x["lower_bound"]), 64, ptr(x.get("cu_seqlens")), ptr(x.get("initial_state")),
+                               float(x["lower_bound"]), 64, ptr(x.get("cu_seqlens")), None, ptr(x.get("initial_state")),
                                ptr(out), ptr(fs), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
@@ -49,8 +50,8 @@ def test_noalloc_matches_kda_fwd_twice(w):
         assert _noalloc(x, out, fs) == _lib.KDA_OK
         torch.cuda.synchronize()
         assert _lib.device_status() == 0
-        assert rel_err(out, ref_out.double().cpu().numpy(), w.dtype) <= tol(w.dtype)
-        assert rel_err(fs, ref_fs.double().cpu().numpy(), w.dtype) <= tol(w.dtype)
+        assert torch.equal(out, ref_out)
+        assert torch.equal(fs, ref_fs)
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
@@ -60,6 +61,6 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     assert lib.kda_fwd_workspace_size(ctypes.byref(dims), 64) > _lib.NOALLOC_SCRATCH_BYTES
     dummy = torch.zeros(16, device=DEV)
     p = ctypes.c_void_p(dummy.data_ptr())
-    rc = lib.kda_fwd_noalloc(ctypes.byref(dims), p, p, p, p, p, p, p, 0.1, -5.0, 64, None, None, p, None,
+    rc = lib.kda_fwd_noalloc(ctypes.byref(dims), p, p, p, p, p, p, p, 0.1, -5.0, 64, None, None, None, p, None,
                              ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == _lib.KDA_ERR_WORKSPACE

@@ -43,9 +43,11 @@ def test_gated_norm_fwd_bwd(shape, dtype):
     rg = oracle.gated_norm_bwd(f64(o), f64(gate), f64(w), 1e-6, f64(dy))
     assert y.dtype == o.dtype and y.shape == o.shape
     assert rel_err(y, ry, dtype) <= tol(dtype)
+    # the gradients are fp32 results computed from the exact (bf16 or fp32) inputs: fp32 bound whatever
+    # the activation dtype
     for n in ("do", "dgate", "dweight"):
-        e = rel_err(g[n], rg[n], dtype)
-        assert e <= tol(dtype), (n, e)
+        e = rel_err(g[n], rg[n], "fp32")
+        assert e <= tol("fp32"), (n, e)
 
 
 def test_gated_norm_at_the_training_shape():
@@ -64,4 +66,5 @@ def test_gated_norm_at_the_training_shape():
     rg = oracle.gated_norm_bwd(f64(o), f64(gate), f64(w), 1e-6, f64(dy))
     assert rel_err(y, ry, "bf16") <= tol("bf16")
     for n in ("do", "dgate", "dweight"):
-        assert rel_err(g1[n], rg[n], "bf16") <= tol("bf16"), n
+        e = rel_err(g1[n], rg[n], "fp32")
+        assert e <= tol("fp32"), (n, e)
