@@ -27,6 +27,9 @@ def main(argv=None) -> None:
     ap.add_argument("--B", type=int)
     ap.add_argument("--T", type=int)
     ap.add_argument("--H", type=int)
+    ap.add_argument("--dtype", choices=("bf16", "fp32"), help="activation dtype (fp32 runs the SIMT path)")
+    ap.add_argument("--Hk", type=int, help="key heads (H a multiple of it; grouped heads)")
+    ap.add_argument("--final-state", action="store_true", help="also write the final state")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=0, help="untimed iterations before the timed ones")
     ap.add_argument("--kernels", action="store_true", help="also print each kernel's mean time (library events)")
@@ -42,7 +45,9 @@ def main(argv=None) -> None:
                     help="instead time the W-tap short convolution + SiLU prologue on a q-shaped [B, T, H*K] tensor")
     a = ap.parse_args(argv)
     w = WORKLOADS[a.workload]
-    over = {k: v for k, v in (("B", a.B), ("T", a.T), ("H", a.H)) if v is not None}
+    over = {k: v for k, v in (("B", a.B), ("T", a.T), ("H", a.H), ("dtype", a.dtype), ("Hk", a.Hk)) if v is not None}
+    if a.final_state:
+        over["final_state"] = True
     if over:
         if w.varlen and ("B" in over or "T" in over):
             raise SystemExit("varlen workloads keep their packed length")

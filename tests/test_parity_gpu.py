@@ -101,8 +101,9 @@ def test_fwd_varlen_with_host_offsets():
     torch.cuda.synchronize()
     assert device_status() == 0
     assert torch.equal(out, ref) and torch.equal(fs, ref_fs)
-    bad = host.clone()
-    bad[2], bad[3] = bad[3], bad[2]                      # decreasing
+    bad = [int(v) for v in host.tolist()]
+    bad[2], bad[3] = bad[3], bad[2]                      # decreasing (5, 69, 5, ...)
+    assert bad[3] < bad[2]
     with pytest.raises(KdaError) as ei:
         kda.forward(*args, cu_seqlens_host=bad, **kw)
     assert ei.value.code == 1                            # KDA_ERR_INVALID_ARG, nothing enqueued
