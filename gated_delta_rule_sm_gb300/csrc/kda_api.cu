@@ -280,7 +280,8 @@ static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cu
     }
     KDA_TRY_CUDA(launch_plan(p, stream));
     if (p.diag) KDA_TRY_CUDA(launch_diag_tc(p, stream));
-    KDA_TRY_CUDA(launch_intra_tc(p, recs, saved ? 2 : 0, stream));
+    if (!saved && !p.diag) KDA_TRY_CUDA(launch_intra2(p, recs, stream));
+    else KDA_TRY_CUDA(launch_intra_tc(p, recs, saved ? 2 : 0, stream));
     KDA_TRY_CUDA(launch_chain_fwd_tc(p, recs, false, stream));
     return KDA_OK;
 }

@@ -119,6 +119,8 @@ size_t diag_item_bytes();
 cudaError_t launch_diag_tc(const Params& p, cudaStream_t st);
 // mode 0: forward chain record; 1: fp32 backward record; 2: both
 cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, int mode, cudaStream_t st);
+// the forward chain record under the lower-bounded gate, two CTAs per SM (kda_intra2.cu)
+cudaError_t launch_intra2(const Params& p, uint8_t* recs, cudaStream_t st);
 // transfer: start from the identity with U0 taken as zero, so that the final state is the transfer matrix
 cudaError_t launch_chain_fwd_tc(const Params& p, const uint8_t* recs, bool store_states, cudaStream_t st,
                                 bool transfer = false);

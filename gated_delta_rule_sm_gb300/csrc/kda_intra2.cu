@@ -1,0 +1,570 @@
+// kda_intra2.cu -- intra-chunk pass of the tensor-core forward (bf16, K = V = 128, lower-bounded gate):
+// the chain record of every (chunk, head) from q, k, v, g_raw, beta_raw, two CTAs per SM.
+//
+// The record is the one kda_tc.cu's chain kernel reads (tcrec layout): [W; Qg] bf16, U0 fp32, Kd^T and
+// Aqk tf32, exp(Gamma_last).  What differs from the persistent intra kernel is how the decayed forms
+//     Bkk[t,s] = sum_c k_tc k_sc exp(Gamma_tc - Gamma_sc) (s < t),   Aqk[t,s] = sum_c q_tc k_sc exp(...) (s <= t)
+// are formed.  With 16-token row blocks i and G_i the cumulative log-decay just before block i, every
+// pair (t in block i, s <= t) factorises against the one reference G_i:
+//     exp(Gamma_t - Gamma_s) = exp(Gamma_t - G_i) * exp(G_i - Gamma_s),
+// the left factor in [exp(16 lb), 1] and the right one <= 1 for s before block i and <= exp(-16 lb) inside
+// it, so both stay inside fp32 range for lower_bound >= -5.  Row block i therefore needs one s-side operand
+// R^(i) = k * exp(G_i - Gamma) over s < 16 (i + 1) and one t-side operand P_i = [k; q] * exp(Gamma - G_i) of
+// its 32 rows.  Two tf32 MMAs (M = 128, N = 64) cover the four blocks: A = [R^(2) ; R^(0)] against
+// B = [P_2 ; P_0], and A = [R^(3) ; R^(1)] against B = [P_3 ; P_1] (the off-diagonal quadrants of each
+// product are not read).  tf32 operands rounded to nearest give the output error of split-bf16 products
+// here (a NumPy emulation of the whole forward: 0.0071 of the output RMS either way under the workloads'
+// gates).  The operands are built a quarter of the channels at a time (8 K-steps of each product per
+// quarter), which keeps the CTA near 100 KB of shared memory so that two CTAs share an SM and hide each
+// other's barrier and MMA waits.
+//
+// Per item (256 threads; thread = sub-block b, 16-channel group, token half of the sub-block):
+//   1. q, k, g, v tiles by TMA; inverse L2 norms of q and k per token;
+//   2. the gate, alpha = exp(g) and, per channel, running products of alpha inside each 16-token
+//      sub-block (x_t = exp(Gamma_t - G_b), y_t = exp(G_{b+1} - Gamma_t)) and the block totals;
+//      v copied into the U0 product's operand;
+//   3. four channel quarters: P, R^(i) (tf32), Kg^T (bf16, for W), Qg and Kd straight into the record;
+//      the two decayed-form MMAs of the quarter;
+//   4. read back Bkk, Aqk; (I + Diag(beta) Bkk)^-1 by 16 x 16 forward substitution and two levels of the
+//      block lower-triangular inverse (split-tf32 warp MMAs, about fp32 accuracy); T = N Diag(beta) split
+//      into bf16 hi + lo;
+//   5. W^T = Kg^T T^T and U0^T = V^T T^T (bf16 MMAs, M = 128, N = 64), read back into the record.
+#include "kda_common.cuh"
+#include "kda_internal.h"
+#include "kda_sm100.cuh"
+
+#include <cudaTypedefs.h>
+
+namespace kda {
+
+using namespace sm100;
+
+namespace intra2 {
+// record fields (bytes; the chain kernel's tcrec layout)
+constexpr uint32_t REC_WQ = 0, REC_U0 = 32768, REC_KD = 65536, REC_AQ = 98304, REC_GC = 114688, REC_BYTES = 115712;
+
+// Shared memory.  [0, 64K) holds the TMA tiles, then (once the element pass has read them) the operand
+// quarter, then the solve's buffers.
+constexpr uint32_t RAW_Q = 0, RAW_K = 16384, RAW_G = 32768, RAW_V = 49152;
+// Operand quarter: 32 channels, tf32 K-major; 8 K-chunks of 16 B per row, K-chunks 144 B apart and
+// 8-row groups 1216 B apart, so that a warp's 4-byte stores (16 channels x 2 token halves) hit 32 banks.
+constexpr uint32_t QLBO = 144, QSBO = 1216;
+constexpr uint32_t RT = 0;                 // R tile: 26 row groups
+constexpr int RG2 = 0, RG0 = 8, RG3 = 10, RG1 = 18;   // first row group of R^(2), R^(0), R^(3), R^(1)
+constexpr uint32_t PT = 31744;             // P tile: 16 row groups (rows 0-63: product X, 64-127: product Y)
+// after the decayed-form MMAs
+constexpr uint32_t SL = 0;                 // fp32 [64][65] Diag(beta) Bkk
+constexpr uint32_t SN = 16640;             // fp32 [64][65] N = (I + L)^-1
+constexpr uint32_t SP = 33280;             // fp32 [4][16][24] scratch of the blocked solve
+constexpr uint32_t SAQ = 39424;            // fp32 [64][65] Aqk (until written to the record)
+constexpr uint32_t TB_HI = 39424, TB_LO = 47616;   // then: T split in bf16, km_bf16(t, s, 1024, 128)
+constexpr uint32_t VB = 65536;             // V^T bf16 K-major km_bf16(v, t, 1024, 128)
+constexpr uint32_t KG = 81920;             // Kg^T bf16 K-major km_bf16(c, t, 1024, 128)
+constexpr uint32_t SMALL = 98304;          // rq[64] rk[64] beta[64] dtb[128] blk[4][128] other[4][256] (fp32)
+constexpr uint32_t BAR = SMALL + (64 * 3 + 128 + 512 + 1024) * 4;
+constexpr uint32_t BYTES = BAR + 64;
+// TMEM columns
+constexpr uint32_t T_Y = 0, T_X = 64, T_W = 128, T_U0 = 192, TCOLS = 256;
+}  // namespace intra2
+
+// Byte offset of (row, channel) in an operand-quarter tile (channel 0..31 within the quarter).
+__device__ __forceinline__ uint32_t q_off(int row, int c) {
+    return (uint32_t)((row >> 3) * intra2::QSBO + (c >> 2) * intra2::QLBO + (row & 7) * 16 + (c & 3) * 4);
+}
+
+// acc (a 16 x 16 block as two 16 x 8 accumulator fragments) += A B for 16 x 16 blocks A, B at row
+// strides sa, sb: warp tf32 MMAs on hi / lo splits of both operands (hi*hi + hi*lo + lo*hi).
+__device__ __forceinline__ void mma16_split2(float (&acc)[2][4], const float* a, int sa, const float* b, int sb,
+                                             int lane) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int k0 = 0; k0 < 16; k0 += 8) {
+        uint32_t ah[4], al[4];
+        split_tf32(a[g * sa + k0 + q], ah[0], al[0]);
+        split_tf32(a[(g + 8) * sa + k0 + q], ah[1], al[1]);
+        split_tf32(a[g * sa + k0 + q + 4], ah[2], al[2]);
+        split_tf32(a[(g + 8) * sa + k0 + q + 4], ah[3], al[3]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            uint32_t bh[2], bl[2];
+            split_tf32(b[(k0 + q) * sb + 8 * nt + g], bh[0], bl[0]);
+            split_tf32(b[(k0 + q + 4) * sb + 8 * nt + g], bh[1], bl[1]);
+            mma1688(acc[nt], al, bh);
+            mma1688(acc[nt], ah, bl);
+            mma1688(acc[nt], ah, bh);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256, 2)
+    intra2_kernel(Params p, uint8_t* recs, const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_g,
+                  const __grid_constant__ CUtensorMap tm_v) {
+    using namespace intra2;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int H = p.H;
+    const int nitems = p.chunk_off[p.N] * H;   // (chunk, head) items, head fastest
+    if ((int)blockIdx.x >= nitems) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // element-pass roles: sub-block b, channel group cw (16 channels of each quarter), token half th
+    const int eb = tid >> 6, cw = (tid >> 5) & 1, th = (tid >> 4) & 1, cl = tid & 15;
+    const int ec = 16 * cw + cl;              // channel within a quarter
+    const int et0 = 16 * eb + 8 * th;         // first of this thread's 8 tokens
+    auto item_tok0 = [&](int it, int& h, int& c, int& tok0) {
+        c = it / H;
+        h = it - c * H;
+        const int n = chunk_segment(p, c);
+        tok0 = seg_begin(p, n) + (c - p.chunk_off[n]) * kChunk;
+        return min(kChunk, seg_end(p, n) - tok0);
+    };
+    float* rq = reinterpret_cast<float*>(smem + SMALL);
+    float* rk = rq + 64;
+    float* sbeta = rk + 64;
+    float* sdtb = sbeta + 64;
+    float* sblk = sdtb + 128;                 // [4 sub-blocks][128 channels] block totals exp(G_{b+1} - G_b)
+    float* soth = sblk + 512;                 // [4 quarters][256 threads] product of alpha over the other token half
+    uint64_t* bar_load = reinterpret_cast<uint64_t*>(smem + BAR);
+    uint64_t* bar_a = bar_load + 1;           // decayed-form MMAs of a quarter
+    uint64_t* bar_w = bar_load + 2;           // W / U0 MMAs
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_load + 3);
+    auto load_raw = [&](int it) {
+        int h2, c2, t02;
+        item_tok0(it, h2, c2, t02);
+        mbar_expect_tx(bar_load, 4 * 16384);
+        tma_load_3d(smem + RAW_Q, &tm_q, 0, h2 / p.G, t02, bar_load);   // q, k: key head of value head h2
+        tma_load_3d(smem + RAW_K, &tm_k, 0, h2 / p.G, t02, bar_load);
+        tma_load_3d(smem + RAW_G, &tm_g, 0, h2, t02, bar_load);
+        tma_load_3d(smem + RAW_V, &tm_v, 0, h2, t02, bar_load);
+    };
+    if (tid == 0) {
+        mbar_init(bar_load, 1);
+        mbar_init(bar_a, 1);
+        mbar_init(bar_w, 1);
+        mbar_fence_init();
+        load_raw(blockIdx.x);
+    }
+    if (warp == 0) tmem_alloc(tslot, TCOLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    uint32_t par_a = 0, par_w = 0, par_load = 0;
+    bool ok = true;
+    float nx_dtb = 0.f, nx_braw = 0.f;
+    auto fetch_small = [&](int it) {
+        int h2, c2, t02;
+        const int len2 = item_tok0(it, h2, c2, t02);
+        if (tid < 128) nx_dtb = p.dt_bias[h2 * 128 + tid];
+        if (tid < 64 && tid < len2) nx_braw = load_act(p.beta_raw, (size_t)(t02 + tid) * H + h2, KDA_BF16);
+    };
+    fetch_small(blockIdx.x);
+    auto wait_all = [&](uint64_t* bar, uint32_t& par) -> bool {
+        const bool r = __syncthreads_and(mbar_wait(bar, par) ? 1 : 0) != 0;
+        par ^= 1;
+        return r;
+    };
+
+    for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+        int h, c, tok0;
+        const int len = item_tok0(item, h, c, tok0);
+        uint8_t* rec = recs + ((size_t)c * H + h) * REC_BYTES;
+        if (tid < 128) sdtb[tid] = nx_dtb;
+        if (tid < 64) sbeta[tid] = tid < len ? sigmoidf_acc(nx_braw) : 0.f;
+        if (!wait_all(bar_load, par_load)) { ok = false; break; }
+
+        // ---- 1. inverse L2 norms (warp w: tokens 8w .. 8w + 7)
+        {
+            float ss[16];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = warp * 8 + u;
+                const uint2 qv = *reinterpret_cast<const uint2*>(smem + RAW_Q + t * 256 + lane * 8);
+                const uint2 kv = *reinterpret_cast<const uint2*>(smem + RAW_K + t * 256 + lane * 8);
+                const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv.x));
+                const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv.y));
+                const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.x));
+                const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.y));
+                ss[u] = q0.x * q0.x + q0.y * q0.y + q1.x * q1.x + q1.y * q1.y;
+                ss[8 + u] = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], o);
+            if (lane < 8) {
+                const int t = warp * 8 + lane;
+                float sq = ss[0], sk = ss[8];
+#pragma unroll
+                for (int u = 1; u < 8; ++u)
+                    if (lane == u) { sq = ss[u]; sk = ss[8 + u]; }
+                rq[t] = t < len ? 1.0f / sqrtf(sq + kNormEps) : 0.f;
+                rk[t] = t < len ? 1.0f / sqrtf(sk + kNormEps) : 0.f;
+            }
+        }
+        __syncthreads();
+
+        // ---- 2. element pass: this thread's 8 tokens of channel 32 r + ec, r = 0..3.  The raw (q, k)
+        // pairs and alpha of each quarter wait in TMEM columns that the W / U0 products only use later
+        // (16 per quarter; warps 0-3 and 4-7 share lane quarters, so they take different columns).
+        const float ea = __expf(p.a_log[h]);
+        const uint32_t stash = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (warp < 4 ? T_W : T_U0);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int cc = 32 * r + ec;
+            const float dtb = sdtb[cc];
+            float prod = 1.f;
+            uint32_t st[16];     // (q, k) bf16 pairs, then alpha
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = et0 + u;
+                const uint32_t o = t * 256 + cc * 2;
+                const __nv_bfloat16 qb = *reinterpret_cast<const __nv_bfloat16*>(smem + RAW_Q + o);
+                const __nv_bfloat16 kb = *reinterpret_cast<const __nv_bfloat16*>(smem + RAW_K + o);
+                __nv_bfloat162 pr;
+                pr.x = qb;
+                pr.y = kb;
+                st[u] = *reinterpret_cast<uint32_t*>(&pr);
+                const float z = bf16_at(smem + RAW_G, o) + dtb;
+                const float gv = p.lb * __fdividef(1.f, 1.f + __expf(-ea * z));
+                const float a = t < len ? __expf(gv) : 1.f;
+                st[8 + u] = __float_as_uint(a);
+                prod *= a;
+            }
+            tmem_st16(stash + 16 * r, st);
+            // token halves of a sub-block sit in lanes l and l ^ 16
+            const float other = __shfl_xor_sync(0xffffffffu, prod, 16);
+            soth[r * 256 + tid] = other;
+            if (th == 0) sblk[eb * 128 + cc] = prod * other;   // exp(G_{b+1} - G_b)
+            // V^T rows of the U0 product: 8 tokens of value column cc (zero past the segment)
+            float vv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) vv[u] = et0 + u < len ? bf16_at(smem + RAW_V, (et0 + u) * 256 + cc * 2) : 0.f;
+            *reinterpret_cast<uint4*>(smem + VB + km_bf16(cc, et0, 1024, 128)) = pack8_bf16(vv);
+        }
+        tmem_st_wait();
+        __syncthreads();   // block totals visible; the raw tiles are dead from here on
+
+        // ---- 3. four channel quarters: operands, record fields, decayed-form MMAs
+#pragma unroll 1
+        for (int r = 0; r < 4; ++r) {
+            const int cc = 32 * r + ec;
+            const float B0 = sblk[cc], B1 = sblk[128 + cc], B2 = sblk[256 + cc], B3 = sblk[384 + cc];
+            const float Bb = eb == 0 ? B0 : eb == 1 ? B1 : eb == 2 ? B2 : B3;
+            const float eG = eb == 0 ? 1.f : eb == 1 ? B0 : eb == 2 ? B0 * B1 : B0 * B1 * B2;       // exp(G_b)
+            const float tail = eb == 0 ? B1 * B2 * B3 : eb == 1 ? B2 * B3 : eb == 2 ? B3 : 1.f;    // exp(G_C - G_{b+1})
+            float kh[8], x[8], y[8];
+            uint32_t st[16];
+            tmem_ld16u(stash + 16 * r, st);
+            const float other = soth[r * 256 + tid];
+            tmem_ld_wait();
+            {
+                float run = th ? other : 1.f;   // alpha over the earlier token half
+#pragma unroll
+                for (int u = 0; u < 8; ++u) { run *= __uint_as_float(st[8 + u]); x[u] = run; }   // exp(Gamma_t - G_b)
+                run = th ? 1.f : other;         // alpha over the later token half
+#pragma unroll
+                for (int u = 7; u >= 0; --u) { y[u] = run; run *= __uint_as_float(st[8 + u]); }  // exp(G_{b+1} - Gamma_t)
+            }
+            if (r > 0 && !wait_all(bar_a, par_a)) { ok = false; break; }   // the previous quarter's MMAs are done
+            float qx[8], kg[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = et0 + u;
+                const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&st[u]);
+                const float qv = __bfloat162float(pr.x) * rq[t];
+                kh[u] = __bfloat162float(pr.y) * rk[t];
+                qx[u] = qv * x[u];
+                const float kx = kh[u] * x[u];
+                // P rows: k x and q x of block eb (product X: blocks 3, 1; product Y: blocks 2, 0)
+                const int tr = 8 * th + u;
+                const int prow = (eb == 3 ? 0 : eb == 1 ? 32 : eb == 2 ? 64 : 96) + tr;
+                *reinterpret_cast<float*>(smem + PT + q_off(prow, ec)) = tf32_rn(kx);
+                *reinterpret_cast<float*>(smem + PT + q_off(prow + 16, ec)) = tf32_rn(qx[u]);
+                kg[u] = kx * eG;
+                qx[u] *= eG;
+            }
+            // R^(i) rows of this sub-block for every row block i >= eb:
+            //   k y exp(G_i - G_{b+1}) = k y * (1 / B_b if i == b, else prod_{b < m < i} B_m)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (i < eb) continue;
+                float f;
+                if (i == eb) f = 1.f / Bb;
+                else {
+                    f = 1.f;
+                    if (eb < 1 && 1 < i) f *= B1;
+                    if (eb < 2 && 2 < i) f *= B2;
+                }
+                const int g0 = i == 0 ? RG0 : i == 1 ? RG1 : i == 2 ? RG2 : RG3;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int s = et0 + u;
+                    *reinterpret_cast<float*>(smem + RT + q_off(8 * g0 + s, ec)) = tf32_rn(kh[u] * y[u] * f);
+                }
+            }
+            // record: Qg (bf16, MN-major rows 64 + t), Kd^T (tf32, K-major); W's operand Kg^T (bf16)
+            *reinterpret_cast<uint4*>(rec + REC_WQ + mn_bf16(64 + et0, cc, 128, 2048)) = pack8_bf16(qx);
+#pragma unroll
+            for (int qd = 0; qd < 2; ++qd) {
+                const int u = 4 * qd;
+                const float4 v4 = make_float4(tf32_rn(kh[u] * y[u] * tail), tf32_rn(kh[u + 1] * y[u + 1] * tail),
+                                              tf32_rn(kh[u + 2] * y[u + 2] * tail), tf32_rn(kh[u + 3] * y[u + 3] * tail));
+                *reinterpret_cast<float4*>(rec + REC_KD + km_f32(cc, et0 + u, 2048, 128)) = v4;
+            }
+            *reinterpret_cast<uint4*>(smem + KG + km_bf16(cc, et0, 1024, 128)) = pack8_bf16(kg);
+            if (eb == 0 && th == 0) reinterpret_cast<float*>(rec + REC_GC)[cc] = B0 * B1 * B2 * B3;
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (tid == 0) {
+                constexpr uint32_t idA = idesc_tf32(128, 64);
+                const uint32_t rt = smem_u32(smem + RT), pt = smem_u32(smem + PT);
+                // product Y: A = R groups 0..15 ([R^(2); R^(0)]), B = P rows 64..127 ([P_2; P_0])
+                // product X: A = R groups 10..25 ([R^(3); R^(1)]), B = P rows 0..63 ([P_3; P_1])
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_tf32(tmem + T_Y, smem_desc(rt + kk * 2 * QLBO, QLBO, QSBO),
+                             smem_desc(pt + 8 * QSBO + kk * 2 * QLBO, QLBO, QSBO), idA, (r > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_tf32(tmem + T_X, smem_desc(rt + RG3 * QSBO + kk * 2 * QLBO, QLBO, QSBO),
+                             smem_desc(pt + kk * 2 * QLBO, QLBO, QSBO), idA, (r > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar_a);
+            }
+        }
+        if (!ok) break;
+        if (!wait_all(bar_a, par_a)) { ok = false; break; }
+        tc_fence_after();
+
+        // ---- 4. read back Bkk, Aqk (lane = s; column = row t of one block); solve
+        float* SLf = reinterpret_cast<float*>(smem + SL);
+        float* SNf = reinterpret_cast<float*>(smem + SN);
+        float* SPf = reinterpret_cast<float*>(smem + SP);
+        float* SAf = reinterpret_cast<float*>(smem + SAQ);
+        for (int i = tid; i < 64 * 65; i += 256) {
+            SLf[i] = 0.f;
+            SAf[i] = 0.f;
+        }
+        __syncthreads();
+        {
+            // warp w < 4: product Y of lane quarter w, w >= 4: product X of lane quarter w - 4
+            const int qw = warp & 3;
+            const bool isX = warp >= 4;
+            // lane quarters 0, 1 hold R^(2) / R^(3) (columns 0..31, blocks 2 / 3); quarter 2 R^(0) / R^(1)
+            // (columns 32..63, blocks 0 / 1); quarter 3 nothing
+            const int s = (qw & 1) * 32 + lane;            // s of quarters 0, 1; quarter 2: s = lane
+            const bool use = qw < 2 ? (isX || s < 48) : qw == 2 ? (isX ? lane < 32 : lane < 16) : false;
+            if (qw < 3) {
+                const uint32_t col = (isX ? T_X : T_Y) + (qw == 2 ? 32 : 0);
+                const uint32_t ta = tmem + ((uint32_t)(qw * 32) << 16) + col;
+                float d[32];
+                tmem_ld16(ta, d);
+                tmem_ld16(ta + 16, d + 16);
+                tmem_ld_wait();
+                if (use) {
+                    const int ss = qw == 2 ? lane : s;
+                    const int blk = qw < 2 ? (isX ? 3 : 2) : (isX ? 1 : 0);
+#pragma unroll
+                    for (int n = 0; n < 16; ++n) {
+                        const int t = 16 * blk + n;
+                        if (ss < t) SLf[t * 65 + ss] = sbeta[t] * d[n];
+                        if (ss <= t) SAf[t * 65 + ss] = d[16 + n];
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        // Aqk to the record (tf32, K-major): thread -> (row t, 16 columns)
+        {
+            const int t = tid >> 2, s0 = (tid & 3) * 16;
+#pragma unroll
+            for (int u = 0; u < 16; u += 4) {
+                const float* srow = SAf + t * 65 + s0 + u;
+                const float4 v4 = make_float4(tf32_rn(srow[0]), tf32_rn(srow[1]), tf32_rn(srow[2]), tf32_rn(srow[3]));
+                *reinterpret_cast<float4*>(rec + REC_AQ + km_f32(t, s0 + u, 2048, 128)) = v4;
+            }
+        }
+        // N = (I + L)^-1: 16 x 16 diagonal blocks by forward substitution
+        if (warp < 4 && lane < 16) {
+            const int b = warp, s2 = lane;
+            float col[16];
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m < rr; ++m) acc += SLf[(16 * b + rr) * 65 + 16 * b + m] * col[m];
+                col[rr] = rr == s2 ? 1.f : (rr > s2 ? -acc : 0.f);
+            }
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) SNf[(16 * b + rr) * 65 + 16 * b + s2] = col[rr];
+        }
+        __syncthreads();
+        // off-diagonal blocks: level 1 N_10, N_32; level 2 N_BL = -N_BR (L_BL N_TL) on the 32 x 32 halves
+        {
+            auto blk = [&](float* base, int i, int j) { return base + (16 * i) * 65 + 16 * j; };
+            constexpr int XS = 24;
+            float acc[2][4];
+            auto zero = [&]() {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+            };
+            auto put = [&](float* d, int sd, float sgn) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        int rr, c2;
+                        frag_rc(lane, e, 0, 8 * nt, rr, c2);
+                        d[rr * sd + c2] = sgn * acc[nt][e];
+                    }
+            };
+            if (warp < 2) {
+                const int i = warp == 0 ? 1 : 3;
+                float* X = SPf + warp * 16 * XS;
+                zero();
+                mma16_split2(acc, blk(SLf, i, i - 1), 65, blk(SNf, i - 1, i - 1), 65, lane);
+                put(X, XS, 1.f);
+                __syncwarp();
+                zero();
+                mma16_split2(acc, blk(SNf, i, i), 65, X, XS, lane);
+                put(blk(SNf, i, i - 1), 65, -1.f);
+            }
+            __syncthreads();
+            const int rr = 2 + (warp >> 1), cb = warp & 1;
+            if (warp < 4) {
+                zero();
+                if (cb == 0) {
+                    mma16_split2(acc, blk(SLf, rr, 0), 65, blk(SNf, 0, 0), 65, lane);
+                    mma16_split2(acc, blk(SLf, rr, 1), 65, blk(SNf, 1, 0), 65, lane);
+                } else {
+                    mma16_split2(acc, blk(SLf, rr, 1), 65, blk(SNf, 1, 1), 65, lane);
+                }
+                put(SPf + warp * 16 * XS, XS, 1.f);
+            }
+            __syncthreads();
+            if (warp < 4) {
+                zero();
+                mma16_split2(acc, blk(SNf, rr, 2), 65, SPf + cb * 16 * XS, XS, lane);
+                if (rr == 3) mma16_split2(acc, blk(SNf, 3, 3), 65, SPf + (2 + cb) * 16 * XS, XS, lane);
+                put(blk(SNf, rr, cb), 65, -1.f);
+            }
+            __syncthreads();
+        }
+        // T = N Diag(beta), split into bf16 hi + lo, as the B operand (N = t, K = s)
+        {
+            const int t = tid >> 2, sq = (tid & 3) * 16;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float hi[8], lo[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int s2 = sq + 8 * hh + e;
+                    const float tv = s2 <= t ? SNf[t * 65 + s2] * sbeta[s2] : 0.f;
+                    hi[e] = __bfloat162float(__float2bfloat16_rn(tv));
+                    lo[e] = tv - hi[e];
+                }
+                *reinterpret_cast<uint4*>(smem + TB_HI + km_bf16(t, sq + 8 * hh, 1024, 128)) = pack8_bf16(hi);
+                *reinterpret_cast<uint4*>(smem + TB_LO + km_bf16(t, sq + 8 * hh, 1024, 128)) = pack8_bf16(lo);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // ---- 5. W^T = Kg^T (T_hi + T_lo)^T and U0^T = V^T (T_hi + T_lo)^T (M = 128, N = 64, K = 64)
+        if (tid == 0) {
+            constexpr uint32_t idW = idesc_bf16(128, 64, 0, 0);
+            const uint32_t kg = smem_u32(smem + KG), vb = smem_u32(smem + VB);
+            const uint32_t thi = smem_u32(smem + TB_HI), tlo = smem_u32(smem + TB_LO);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tmem + T_W, smem_desc(kg + kk * 256, 128, 1024), smem_desc(thi + kk * 256, 128, 1024), idW, kk > 0);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tmem + T_W, smem_desc(kg + kk * 256, 128, 1024), smem_desc(tlo + kk * 256, 128, 1024), idW, 1);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tmem + T_U0, smem_desc(vb + kk * 256, 128, 1024), smem_desc(thi + kk * 256, 128, 1024), idW, kk > 0);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tmem + T_U0, smem_desc(vb + kk * 256, 128, 1024), smem_desc(tlo + kk * 256, 128, 1024), idW, 1);
+            mma_commit(bar_w);
+        }
+        if (!wait_all(bar_w, par_w)) { ok = false; break; }
+        tc_fence_after();
+        // every shared operand of this item is consumed: fetch the next item's tiles
+        if (item + (int)gridDim.x < nitems) {
+            if (tid == 0) {
+                fence_async_smem();
+                load_raw(item + gridDim.x);
+            }
+            fetch_small(item + gridDim.x);
+        }
+        // record W (MN-major bf16, thread = channel) and U0 (column-major fp32, thread = value column)
+        {
+            const uint32_t lb = static_cast<uint32_t>((warp & 3) * 32) << 16;
+            const uint32_t col = warp < 4 ? T_W : T_U0;
+            const int row = (warp & 3) * 32 + lane;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float d[32];
+                tmem_ld16(tmem + lb + col + 32 * half, d);
+                tmem_ld16(tmem + lb + col + 32 * half + 16, d + 16);
+                tmem_ld_wait();
+                if (warp < 4) {
+#pragma unroll
+                    for (int tb = 0; tb < 32; tb += 8)
+                        *reinterpret_cast<uint4*>(rec + REC_WQ + mn_bf16(32 * half + tb, row, 128, 2048)) =
+                            pack8_bf16(d + tb);
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(rec + REC_U0 + row * 256 + half * 128);
+#pragma unroll
+                    for (int t4 = 0; t4 < 8; ++t4)
+                        dst[t4] = make_float4(d[4 * t4], d[4 * t4 + 1], d[4 * t4 + 2], d[4 * t4 + 3]);
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();   // TMEM read back before the next item's MMAs
+        tc_fence_after();
+    }
+    if (!ok) {
+        // A wait gave up: record it, give outstanding copies / MMAs a bounded chance to land, release TMEM.
+        if (tid == 0) {
+            record_error(p.status, KDA_ERR_TIMEOUT);
+            mbar_wait(bar_load, par_load, 1u << 16);
+            mbar_wait(bar_a, par_a, 1u << 16);
+            mbar_wait(bar_w, par_w, 1u << 16);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, TCOLS);
+}
+
+static_assert(intra2::PT + 16 * intra2::QSBO <= 65536, "operand quarter inside the tile area");
+static_assert(intra2::RT + 26 * intra2::QSBO <= intra2::PT, "R tile before the P tile");
+static_assert(intra2::TB_LO + 8192 <= 65536, "T split inside the tile area");
+static_assert(intra2::BYTES <= 113 * 1024, "two CTAs per SM");
+
+// [TT tokens][H heads][128 channels] bf16 -> boxes of 64 tokens x 1 head x 128 channels (row-major in smem).
+bool head_tile_map2(CUtensorMap* m, const void* base, int H, int TT);
+
+cudaError_t launch_intra2(const Params& p, uint8_t* recs, cudaStream_t st) {
+    CUtensorMap mq, mk, mg, mv;
+    if (!head_tile_map2(&mq, p.q, p.Hk, p.TT) || !head_tile_map2(&mk, p.k, p.Hk, p.TT) ||
+        !head_tile_map2(&mg, p.g_raw, p.H, p.TT) || !head_tile_map2(&mv, p.v, p.H, p.TT))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(intra2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)intra2::BYTES);
+    if (e != cudaSuccess) return e;
+    timing_pre(st, K_INTRA_TC);
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long items = (long)p.NCmax * p.H;
+    const long cap = 2L * sms;   // two CTAs per SM, each looping over (chunk, head) items
+    const int grid = (int)(items < cap ? items : cap);
+    intra2_kernel<<<grid, 256, intra2::BYTES, st>>>(p, recs, mq, mk, mg, mv);
+    timing_post(st);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -1197,6 +1197,8 @@ static bool head_tile_map(CUtensorMap* m, const void* base, int H, int TT) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool head_tile_map2(CUtensorMap* m, const void* base, int H, int TT) { return head_tile_map(m, base, H, TT); }
+
 bool tc_inputs_aligned(const Params& p) {
     auto al = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
     return al(p.q) && al(p.k) && al(p.g_raw) && al(p.v) && (p.dout == nullptr || al(p.dout));

@@ -183,7 +183,10 @@ kda_status kda_bwd(const kda_dims* dims,
  * runs the forward and also writes those quantities (fp32, per chunk and
  * head, an internal layout) to the caller's `saved` buffer; kda_bwd_saved
  * takes the same arguments as kda_bwd plus that buffer and skips the
- * rebuild.  Results are identical to kda_fwd / kda_bwd.
+ * rebuild.  The gradients are bit-identical to kda_bwd's.  The forward
+ * output agrees with kda_fwd's to rounding, not bit for bit: kda_fwd alone
+ * forms the intra-chunk decayed products with tf32 operands, the saving
+ * pass with split-bf16 ones.
  *
  * kda_saved_size returns the bytes `saved` must hold for these dims (0 when
  * the shape does not take the tensor-core path; then use kda_fwd / kda_bwd).

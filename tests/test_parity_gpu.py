@@ -287,7 +287,11 @@ def test_saved_pair_matches_plain_calls():
     g2 = kda.backward(*[x[n] for n in names], x["dout"], dfinal_state=dfinal, saved=saved, **kw)
     torch.cuda.synchronize()
     assert device_status() == 0
-    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+    # the forward-only pass forms the intra-chunk products its own way (tf32 decayed forms): both forwards
+    # must meet the bound against the oracle; the backward is the same computation either way
+    r_out, r_fs = oracle_fwd(x)
+    for o, f in ((o1, f1), (o2, f2)):
+        assert rel_err(o, r_out, "bf16") <= tol("bf16") and rel_err(f, r_fs, "bf16") <= tol("bf16")
     for n in GRADS:
         assert torch.equal(g1[n], g2[n]), n
 
@@ -323,7 +327,8 @@ def test_grouped_heads_varlen_and_saved_pair():
     o2, _ = kda.forward(*[x[n] for n in names], **kw)
     g2 = kda.backward(*[x[n] for n in names], x["dout"], **kw)
     torch.cuda.synchronize()
-    assert torch.equal(o1, o2)
+    r_out, _ = oracle_fwd(x)
+    assert rel_err(o1, r_out, "bf16") <= tol("bf16") and rel_err(o2, r_out, "bf16") <= tol("bf16")
     for n in GRADS:
         assert torch.equal(g1[n], g2[n]), n
 
