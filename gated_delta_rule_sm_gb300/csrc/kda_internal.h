@@ -67,6 +67,21 @@ enum KernelId {
     K_NUM_KERNELS
 };
 
+// Chain record of the tensor-core forward, one per (chunk, head), written by the intra-chunk kernels in
+// exactly the shared-memory layouts the forward chain's MMAs read (bytes).  The chain's operands are fp16:
+// its values stay far inside fp16's range (|W|, |Qg|, |S|, |U|, |Kd|, |Aqk| of order 1 to 10), where the
+// 11-bit significand gives every product tf32-like accuracy in one kind::f16 MMA.
+namespace tcrec {
+constexpr uint32_t WQ = 0;            // [W; Qg]  fp16, 128 rows x 128 K (c), MN-major: mn_bf16(r, c, 128, 2048)
+constexpr uint32_t U0 = 32768;        // U0       fp32, column-major [128 j][64 t]; slice z = j in [32z, 32z+32)
+constexpr uint32_t KD = 65536;        // Kd^T     fp16, 128 rows (c) x 64 K (t), K-major: km_bf16(c, t, 1024, 128)
+constexpr uint32_t AQ = 81920;        // Aqk      fp16, 64 rows (t) x 64 K (s), K-major: km_bf16(t, s, 1024, 128)
+constexpr uint32_t GC = 90112;        // exp(Gamma_last) fp32 [128]
+constexpr uint32_t BYTES = 91136;     // record stride (1 KB aligned)
+constexpr uint32_t U0_SLICE = 8192;   // one 32-column slice of U0
+constexpr uint32_t TAIL = BYTES - KD; // KD + AQ + GC (+ padding), contiguous
+}  // namespace tcrec
+
 // Record of the two tcgen05 state chains of the backward, per (chunk, head), K = V = 128 (bytes).
 // Both chains run  X = Y + A1 Z,  Z' = Diag(exp(Gamma_last)) Z + A2 X (+ P)  with every product in
 // split precision: operand = hi + lo, both bf16 (hi = bf16(x), lo = bf16(x - hi)), and the products

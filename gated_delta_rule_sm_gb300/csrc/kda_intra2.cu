@@ -1,8 +1,8 @@
 // kda_intra2.cu -- intra-chunk pass of the tensor-core forward (bf16, K = V = 128, lower-bounded gate):
 // the chain record of every (chunk, head) from q, k, v, g_raw, beta_raw, two CTAs per SM.
 //
-// The record is the one kda_tc.cu's chain kernel reads (tcrec layout): [W; Qg] bf16, U0 fp32, Kd^T and
-// Aqk tf32, exp(Gamma_last).  What differs from the persistent intra kernel is how the decayed forms
+// The record is the one kda_tc.cu's chain kernel reads (tcrec layout): [W; Qg], Kd^T and Aqk in fp16, U0
+// fp32, exp(Gamma_last).  What differs from the persistent intra kernel is how the decayed forms
 //     Bkk[t,s] = sum_c k_tc k_sc exp(Gamma_tc - Gamma_sc) (s < t),   Aqk[t,s] = sum_c q_tc k_sc exp(...) (s <= t)
 // are formed.  With 16-token row blocks i and G_i the cumulative log-decay just before block i, every
 // pair (t in block i, s <= t) factorises against the one reference G_i:
@@ -41,7 +41,8 @@ using namespace sm100;
 
 namespace intra2 {
 // record fields (bytes; the chain kernel's tcrec layout)
-constexpr uint32_t REC_WQ = 0, REC_U0 = 32768, REC_KD = 65536, REC_AQ = 98304, REC_GC = 114688, REC_BYTES = 115712;
+constexpr uint32_t REC_WQ = tcrec::WQ, REC_U0 = tcrec::U0, REC_KD = tcrec::KD, REC_AQ = tcrec::AQ,
+                   REC_GC = tcrec::GC, REC_BYTES = tcrec::BYTES;
 
 // Shared memory.  [0, 64K) holds the TMA tiles, then (once the element pass has read them) the operand
 // quarter, then the solve's buffers.
@@ -303,13 +304,12 @@ __global__ void __launch_bounds__(256, 2)
                 }
             }
             // record: Qg (bf16, MN-major rows 64 + t), Kd^T (tf32, K-major); W's operand Kg^T (bf16)
-            *reinterpret_cast<uint4*>(rec + REC_WQ + mn_bf16(64 + et0, cc, 128, 2048)) = pack8_bf16(qx);
+            *reinterpret_cast<uint4*>(rec + REC_WQ + mn_bf16(64 + et0, cc, 128, 2048)) = pack8_f16(qx);
+            {
+                float kd[8];
 #pragma unroll
-            for (int qd = 0; qd < 2; ++qd) {
-                const int u = 4 * qd;
-                const float4 v4 = make_float4(tf32_rn(kh[u] * y[u] * tail), tf32_rn(kh[u + 1] * y[u + 1] * tail),
-                                              tf32_rn(kh[u + 2] * y[u + 2] * tail), tf32_rn(kh[u + 3] * y[u + 3] * tail));
-                *reinterpret_cast<float4*>(rec + REC_KD + km_f32(cc, et0 + u, 2048, 128)) = v4;
+                for (int u = 0; u < 8; ++u) kd[u] = kh[u] * y[u] * tail;
+                *reinterpret_cast<uint4*>(rec + REC_KD + km_bf16(cc, et0, 1024, 128)) = pack8_f16(kd);
             }
             *reinterpret_cast<uint4*>(smem + KG + km_bf16(cc, et0, 1024, 128)) = pack8_bf16(kg);
             if (eb == 0 && th == 0) reinterpret_cast<float*>(rec + REC_GC)[cc] = B0 * B1 * B2 * B3;
@@ -373,14 +373,16 @@ __global__ void __launch_bounds__(256, 2)
             }
         }
         __syncthreads();
-        // Aqk to the record (tf32, K-major): thread -> (row t, 16 columns)
+        // Aqk to the record (fp16, K-major): thread -> (row t, 16 columns)
         {
             const int t = tid >> 2, s0 = (tid & 3) * 16;
 #pragma unroll
-            for (int u = 0; u < 16; u += 4) {
+            for (int u = 0; u < 16; u += 8) {
                 const float* srow = SAf + t * 65 + s0 + u;
-                const float4 v4 = make_float4(tf32_rn(srow[0]), tf32_rn(srow[1]), tf32_rn(srow[2]), tf32_rn(srow[3]));
-                *reinterpret_cast<float4*>(rec + REC_AQ + km_f32(t, s0 + u, 2048, 128)) = v4;
+                float a8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a8[e] = srow[e];
+                *reinterpret_cast<uint4*>(rec + REC_AQ + km_bf16(t, s0 + u, 1024, 128)) = pack8_f16(a8);
             }
         }
         // N = (I + L)^-1: 16 x 16 diagonal blocks by forward substitution
@@ -513,7 +515,7 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
                     for (int tb = 0; tb < 32; tb += 8)
                         *reinterpret_cast<uint4*>(rec + REC_WQ + mn_bf16(32 * half + tb, row, 128, 2048)) =
-                            pack8_bf16(d + tb);
+                            pack8_f16(d + tb);
                 } else {
                     float4* dst = reinterpret_cast<float4*>(rec + REC_U0 + row * 256 + half * 128);
 #pragma unroll

@@ -20,18 +20,6 @@ namespace kda {
 
 using namespace sm100;
 
-// ------------------------------------------------------------------ record layout (bytes)
-namespace tcrec {
-// One record per (chunk, head), stored in the shared-memory layouts the chain kernel's MMAs read.
-constexpr uint32_t WQ = 0;            // [W; Qg]  bf16, 128 rows x 128 K (c), MN-major: mn_bf16(r, c, 128, 2048)
-constexpr uint32_t U0 = 32768;        // U0       fp32, column-major [128 j][64 t]; slice z = j in [32z, 32z+32)
-constexpr uint32_t KD = 65536;        // Kd^T     tf32, 128 rows (c) x 64 K (t), K-major: km_f32(c, t, 2048, 128)
-constexpr uint32_t AQ = 98304;        // Aqk      tf32, 64 rows (t) x 64 K (s), K-major: km_f32(t, s, 2048, 128)
-constexpr uint32_t GC = 114688;       // exp(Gamma_last) fp32 [128]
-constexpr uint32_t BYTES = 115712;    // record stride (1 KB aligned)
-constexpr uint32_t U0_SLICE = 8192;   // one 32-column slice of U0
-constexpr uint32_t TAIL = BYTES - KD; // KD + AQ + GC, contiguous
-}  // namespace tcrec
 
 // ------------------------------------------------------------------ intra-chunk kernel (tcgen05)
 //
@@ -358,18 +346,18 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 *reinterpret_cast<uint4*>(smem + KVB + km_bf16(cc, tb, 1024, 128)) = pack8_bf16(vk);
                 *reinterpret_cast<uint4*>(smem + KGLO + km_bf16(cc, tb, 1024, 128)) = pack8_bf16(vkl);
-                if (FWDREC) *reinterpret_cast<uint4*>(rec + tcrec::WQ + mn_bf16(64 + tb, cc, 128, 2048)) = pack8_bf16(vq);
+                if (FWDREC) *reinterpret_cast<uint4*>(rec + tcrec::WQ + mn_bf16(64 + tb, cc, 128, 2048)) = pack8_f16(vq);
             }
-            // Kd^T (tf32): k * exp(Gamma_C - Gamma_t), four tokens per 16 B (forward record only)
+            // Kd^T (fp16): k * exp(Gamma_C - Gamma_t), eight tokens per 16 B (forward record only)
 #pragma unroll
-            for (int qd = 0; qd < (FWDREC ? 4 : 0); ++qd) {
-                const int u = 4 * qd;
-                float kb[4];
+            for (int hh = 0; hh < (FWDREC ? 2 : 0); ++hh) {
+                float kd[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) kb[e] = bf16_at(smem + RAW_K, (t0 + u + e) * 256 + cc * 2) * rk[t0 + u + e];
-                const float4 v4 = make_float4(tf32_rn(kb[0] * y[ci][u] * tail), tf32_rn(kb[1] * y[ci][u + 1] * tail),
-                                              tf32_rn(kb[2] * y[ci][u + 2] * tail), tf32_rn(kb[3] * y[ci][u + 3] * tail));
-                *reinterpret_cast<float4*>(rec + tcrec::KD + km_f32(cc, t0 + u, 2048, 128)) = v4;
+                for (int e = 0; e < 8; ++e) {
+                    const int u = 8 * hh + e;
+                    kd[e] = bf16_at(smem + RAW_K, (t0 + u) * 256 + cc * 2) * rk[t0 + u] * y[ci][u] * tail;
+                }
+                *reinterpret_cast<uint4*>(rec + tcrec::KD + km_bf16(cc, t0 + 8 * hh, 1024, 128)) = pack8_f16(kd);
             }
         }
         // L^(j) rows of this thread's sub-block (k rows t, q rows 64 + t), split into bf16 hi + lo
@@ -532,14 +520,11 @@ __global__ void __launch_bounds__(256, 1)
                     for (int u = 0; u < 32; ++u) frec[RL.A + t * 64 + c0 + u] = c0 + u <= t ? d[u] : 0.f;
                 }
 #pragma unroll
-                for (int u = 0; u < (FWDREC ? 32 : 0); u += 4) {
-                    const int s4 = c0 + u;
-                    float4 v4;
-                    v4.x = tf32_rn(s4 <= t ? d[u] : 0.f);
-                    v4.y = tf32_rn(s4 + 1 <= t ? d[u + 1] : 0.f);
-                    v4.z = tf32_rn(s4 + 2 <= t ? d[u + 2] : 0.f);
-                    v4.w = tf32_rn(s4 + 3 <= t ? d[u + 3] : 0.f);
-                    *reinterpret_cast<float4*>(rec + tcrec::AQ + km_f32(t, s4, 2048, 128)) = v4;
+                for (int u = 0; u < (FWDREC ? 32 : 0); u += 8) {
+                    float a8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) a8[e] = c0 + u + e <= t ? d[u + e] : 0.f;
+                    *reinterpret_cast<uint4*>(rec + tcrec::AQ + km_bf16(t, c0 + u, 1024, 128)) = pack8_f16(a8);
                 }
             }
         }
@@ -692,7 +677,7 @@ __global__ void __launch_bounds__(256, 1)
                 if (FWDREC)
 #pragma unroll
                     for (int tb = 0; tb < 64; tb += 8)
-                        *reinterpret_cast<uint4*>(rec + tcrec::WQ + mn_bf16(tb, cc, 128, 2048)) = pack8_bf16(d + tb);
+                        *reinterpret_cast<uint4*>(rec + tcrec::WQ + mn_bf16(tb, cc, 128, 2048)) = pack8_f16(d + tb);
                 if (BWD)
 #pragma unroll
                     for (int t = 0; t < 64; ++t) frec[RL.W + t * 128 + cc] = d[t];
@@ -892,25 +877,28 @@ cudaError_t launch_diag_tc(const Params& p, cudaStream_t st) {
 // ------------------------------------------------------------------ state chain (tcgen05)
 
 namespace chainlay {
+constexpr int NSLOT = 3;                  // record slots: a chunk's copy is requested two chunks ahead
 constexpr uint32_t SLOT_WQ = 0;
 constexpr uint32_t SLOT_U0 = 32768;
 constexpr uint32_t SLOT_KD = 40960;       // KD, AQ, GC follow contiguously (tcrec::TAIL bytes)
 constexpr uint32_t SLOT_AQ = SLOT_KD + (tcrec::AQ - tcrec::KD);
 constexpr uint32_t SLOT_GC = SLOT_KD + (tcrec::GC - tcrec::KD);
 constexpr uint32_t SLOT_BYTES = (SLOT_KD + tcrec::TAIL + 1023) / 1024 * 1024;
-constexpr uint32_t SB = 2 * SLOT_BYTES;   // S as bf16 B operand (N = j, K = c), MN-major: mn_bf16(j, c, 128, 512)
-constexpr uint32_t UB = SB + 8192;        // U as tf32 B operand (N = j, K = t), K-major, padded: km_f32(j, t, 2304, 144)
-constexpr uint32_t UB_LBO = 144, UB_SBO = 2304;   // two buffers (chunk parity), UB_BYTES apart
-constexpr uint32_t UB_BYTES = 4 * UB_SBO;
-constexpr uint32_t BAR = UB + 2 * UB_BYTES; // mbarriers: full[2], empty[2], ws, s, o, u
-constexpr uint32_t TSLOT = BAR + 64;
+constexpr uint32_t SB = NSLOT * SLOT_BYTES;   // S as fp16 B operand (N = j, K = c), MN-major: mn_bf16(j, c, 128, 512)
+constexpr uint32_t UB = SB + 8192;        // U as fp16 B operand (N = j, K = t), MN-major: mn_bf16(j, t, 128, 512)
+constexpr uint32_t UB_BYTES = 4096;       // two buffers (chunk parity), UB_BYTES apart
+constexpr uint32_t BAR = UB + 2 * UB_BYTES; // mbarriers: full[3], empty[3], ws, s, o, u
+constexpr uint32_t TSLOT = BAR + 128;
 constexpr uint32_t BYTES = TSLOT + 64;
 }  // namespace chainlay
+static_assert(chainlay::BYTES <= 232448, "shared memory per CTA");
 
-constexpr uint32_t kIdescWS = idesc_bf16(128, 32, 1, 1);   // [W; Qg] and S both MN-major
-constexpr uint32_t kIdescTF32 = idesc_tf32(128, 32);
+constexpr uint32_t kIdescWS = idesc_f16(128, 32, 1, 1);   // [W; Qg] and S both MN-major
+constexpr uint32_t kIdescKU = idesc_f16(128, 32, 0, 1);   // Kd^T / Aqk K-major, U MN-major
 
 // One CTA per (segment, head, 32-column slice of V): four compute warps, an MMA warp and a load warp.
+// Every operand is fp16 (one kind::f16 MMA per product, tf32-like accuracy at these magnitudes); the
+// state itself stays fp32 in registers.
 // Compute thread c keeps row c of the state slice (32 fp32) in registers.  Per chunk the critical path
 // is
 //   MMA1 (W S) -> U = U0 - W S -> MMA2b (Kd^T U) -> S <- Diag(gC) S + Kd^T U -> next MMA1.
@@ -929,12 +917,13 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
     const int n = blockIdx.x, h = blockIdx.y, z = blockIdx.z, j0 = z * 32;
     const int H = p.H, K = 128, V = 128;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + chainlay::BAR);   // [2] record slots landed
-    uint64_t* empty = full + 2;     // [2] record slots released
-    uint64_t* bar_ws = full + 4;    // MMA1 (4 issuers)
-    uint64_t* bar_s = full + 5;     // MMA2b, state update (4 issuers)
-    uint64_t* bar_o = full + 6;     // MMA2a, output (MMA warp)
-    uint64_t* bar_u = full + 7;     // U of this chunk is in shared memory
+    constexpr int NS = chainlay::NSLOT;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + chainlay::BAR);   // [NS] record slots landed
+    uint64_t* empty = full + NS;    // [NS] record slots released
+    uint64_t* bar_ws = full + 2 * NS;       // MMA1 (4 issuers)
+    uint64_t* bar_s = bar_ws + 1;   // MMA2b, state update (4 issuers)
+    uint64_t* bar_o = bar_ws + 2;   // MMA2a, output (MMA warp)
+    uint64_t* bar_u = bar_ws + 3;   // U of this chunk is in shared memory
     volatile int* sh_fail = reinterpret_cast<volatile int*>(smem + chainlay::TSLOT + 4);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + chainlay::TSLOT);
     uint8_t* SB = smem + chainlay::SB;
@@ -944,7 +933,7 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
     constexpr uint32_t TCOLS = 512;
 
     if (tid == 0) {
-        for (int b = 0; b < 4; ++b) mbar_init(&full[b], 1);   // full[2], empty[2]
+        for (int b = 0; b < 2 * NS; ++b) mbar_init(&full[b], 1);   // full[NS], empty[NS]
         mbar_init(bar_ws, 4);
         mbar_init(bar_s, 4);
         mbar_init(bar_o, 1);
@@ -953,7 +942,7 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(tslot, TCOLS);
-    auto slot_ptr = [&](int i) { return smem + (i & 1) * chainlay::SLOT_BYTES; };
+    auto slot_ptr = [&](int i) { return smem + (i % NS) * chainlay::SLOT_BYTES; };
     auto rec_ptr = [&](int i) { return recs + ((size_t)(cb + i) * H + h) * tcrec::BYTES; };
     auto ub_addr = [&](int i) { return smem_u32(smem + chainlay::UB + (i & 1) * chainlay::UB_BYTES); };
     auto fail_wait = [&](uint64_t* bar, uint32_t parity) {
@@ -968,14 +957,14 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
 
     bool ok = true;
     if (warp == 5) {
-        // load warp: chunk k into slot k & 1 once chunk k - 2 has released it
+        // load warp: chunk k into slot k % NS once chunk k - NS has released it
         if (lane == 0) {
             for (int k = 0; k < nch; ++k) {
-                const int sl = k & 1;
-                if (k >= 2) {
+                const int sl = k % NS;
+                if (k >= NS) {
                     bool got = false;
                     for (int tries = 0; tries < 64 && !got && *sh_fail == 0; ++tries)
-                        got = mbar_wait(&empty[sl], ((k >> 1) - 1) & 1, 1u << 16);
+                        got = mbar_wait(&empty[sl], ((k / NS) - 1) & 1, 1u << 16);
                     if (!got) { atomicExch((int*)sh_fail, 1); break; }
                 }
                 uint8_t* slot = slot_ptr(k);
@@ -996,11 +985,11 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
                 if (!got) { atomicExch((int*)sh_fail, 1); break; }
                 tc_fence_after();
                 const uint32_t ub = ub_addr(i);
-                const uint32_t aq = smem_u32(slot_ptr(i) + chainlay::SLOT_AQ) - 16384;
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_tf32(tDO + 32 * (i & 1), smem_desc(aq + kk * 256, 128, 2048),
-                             smem_desc(ub + kk * 2 * chainlay::UB_LBO, chainlay::UB_LBO, chainlay::UB_SBO), kIdescTF32,
-                             kk > 0);
+                // an M = 128 window whose rows 64..127 are Aqk (rows 0..63: the tail of Kd^T, not read back)
+                const uint32_t aq = smem_u32(slot_ptr(i) + chainlay::SLOT_AQ) - 8192;
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tDO + 32 * (i & 1), smem_desc(aq + kk * 256, 128, 1024), smem_desc(ub + kk * 1024, 512, 128),
+                             kIdescKU, kk > 0);
                 mma_commit(bar_o);
             }
         }
@@ -1035,7 +1024,7 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
     };
     // MMA1 partial `warp`: K rows 32 warp .. 32 warp + 31 of [W; Qg] S
     auto issue_mma1 = [&](int i) {
-        fail_wait(&full[i & 1], (i >> 1) & 1);
+        fail_wait(&full[i % NS], (i / NS) & 1);
         tc_fence_after();
         const uint32_t wq = smem_u32(slot_ptr(i) + chainlay::SLOT_WQ), sb = smem_u32(SB);
         for (int q = 0; q < 2; ++q) {
@@ -1046,7 +1035,7 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
         mma_commit(bar_ws);
     };
 #pragma unroll
-    for (int jg = 0; jg < 4; ++jg) *reinterpret_cast<uint4*>(SB + mn_bf16(8 * jg, tid, 128, 512)) = pack8_bf16(S + 8 * jg);
+    for (int jg = 0; jg < 4; ++jg) *reinterpret_cast<uint4*>(SB + mn_bf16(8 * jg, tid, 128, 512)) = pack8_f16(S + 8 * jg);
     fence_async_smem();
     sync128();
     if (issuer && nch > 0) issue_mma1(0);
@@ -1061,45 +1050,32 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
 #pragma unroll
             for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
         }
-        fail_wait(&full[i & 1], (i >> 1) & 1);   // record visible to this thread
+        fail_wait(&full[i % NS], (i / NS) & 1);   // record visible to this thread
         if (warp < 2) {
-            // U[t][j] = U0[t][j] - (W S)[t][j], t = tid; rounded to tf32 and transposed in lane quads
+            // U[t][j] = U0[t][j] - (W S)[t][j], t = tid, as fp16: eight j per 16-byte row of a core matrix
             fail_wait(bar_ws, par);
             tc_fence_after();
             float d[32];
             ld_sum4(tD1, d);
             const float* u0 = reinterpret_cast<const float*>(sl + chainlay::SLOT_U0);
-            float u[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) u[j] = tf32_rn((transfer ? 0.f : u0[j * 64 + tid]) - d[j]);
-            const int r = tid & 3;
-            const bool top = (r & 2) == 0, even = (r & 1) == 0;
             uint8_t* UB = smem + chainlay::UB + (i & 1) * chainlay::UB_BYTES;
 #pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                float v0 = u[4 * b], v1 = u[4 * b + 1], v2 = u[4 * b + 2], v3 = u[4 * b + 3];
-                const float s0 = top ? v2 : v0, s1 = top ? v3 : v1;
-                const float g0 = __shfl_xor_sync(0xffffffffu, s0, 2), g1 = __shfl_xor_sync(0xffffffffu, s1, 2);
-                if (top) { v2 = g0; v3 = g1; } else { v0 = g0; v1 = g1; }
-                const float e0 = even ? v1 : v0, e1 = even ? v3 : v2;
-                const float h0 = __shfl_xor_sync(0xffffffffu, e0, 1), h1 = __shfl_xor_sync(0xffffffffu, e1, 1);
-                if (even) { v1 = h0; v3 = h1; } else { v0 = h0; v2 = h1; }
-                *reinterpret_cast<float4*>(UB + km_f32(4 * b + r, tid - r, chainlay::UB_SBO, chainlay::UB_LBO)) =
-                    make_float4(v0, v1, v2, v3);
+            for (int jg = 0; jg < 32; jg += 8) {
+                float u[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) u[e] = (transfer ? 0.f : u0[(jg + e) * 64 + tid]) - d[jg + e];
+                *reinterpret_cast<uint4*>(UB + mn_bf16(jg, tid, 128, 512)) = pack8_f16(u);
             }
         }
         fence_async_smem();
         sync128();
         if (*sh_fail) { ok = false; break; }
         if (tid == 0) mbar_arrive(bar_u);   // the MMA warp may read U now
-        // MMA2b: D3 partial w = Kd^T U over t in [16 w, 16 w + 16)
+        // MMA2b: D3 partial w = Kd^T U over t in [16 w, 16 w + 16) (one K step)
         if (issuer) {
             const uint32_t ub = ub_addr(i), kd = smem_u32(sl + chainlay::SLOT_KD);
-            for (int q = 0; q < 2; ++q) {
-                const int kk = 2 * warp + q;
-                mma_tf32(tD3 + 32 * warp, smem_desc(kd + kk * 256, 128, 2048),
-                         smem_desc(ub + kk * 2 * chainlay::UB_LBO, chainlay::UB_LBO, chainlay::UB_SBO), kIdescTF32, q > 0);
-            }
+            mma_bf16(tD3 + 32 * warp, smem_desc(kd + warp * 256, 128, 1024), smem_desc(ub + warp * 1024, 512, 128),
+                     kIdescKU, 0);
             mma_commit(bar_s);
         }
         fail_wait(bar_s, par);
@@ -1112,7 +1088,7 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
             for (int j = 0; j < 32; ++j) S[j] = gc * S[j] + d[j];
 #pragma unroll
             for (int jg = 0; jg < 4; ++jg)
-                *reinterpret_cast<uint4*>(SB + mn_bf16(8 * jg, tid, 128, 512)) = pack8_bf16(S + 8 * jg);
+                *reinterpret_cast<uint4*>(SB + mn_bf16(8 * jg, tid, 128, 512)) = pack8_f16(S + 8 * jg);
         }
         fence_async_smem();
         sync128();
@@ -1122,7 +1098,7 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
             // output of chunk i: rows 64..127 of its MMA1 partials plus the Aqk U accumulator
             fail_wait(bar_o, par);
             tc_fence_after();
-            if (tid == 64) mbar_arrive(&empty[i & 1]);   // every reader of this chunk's slot is done
+            if (tid == 64) mbar_arrive(&empty[i % NS]);   // every reader of this chunk's slot is done
             float d[32], e[32];
             tmem_ld16(tDO + 32 * (i & 1) + lane_base, e);
             tmem_ld16(tDO + 32 * (i & 1) + lane_base + 16, e + 16);
@@ -1152,11 +1128,11 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
         // Record the timeout; give in-flight copies and MMAs a bounded chance to land before this CTA's
         // shared and tensor memory are released.
         record_error(p.status, KDA_ERR_TIMEOUT);
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NS; ++b) {
             mbar_wait(&full[b], 0, 1u << 12);
             mbar_wait(&full[b], 1, 1u << 12);
         }
-        for (int b = 4; b < 7; ++b) {
+        for (int b = 2 * NS; b < 2 * NS + 3; ++b) {
             mbar_wait(&full[b], 0, 1u << 12);
             mbar_wait(&full[b], 1, 1u << 12);
         }
