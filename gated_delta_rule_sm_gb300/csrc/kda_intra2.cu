@@ -139,8 +139,8 @@ __global__ void __launch_bounds__(256, 2)
     };
     if (tid == 0) {
         mbar_init(bar_load, 1);
-        mbar_init(bar_a, 1);
-        mbar_init(bar_w, 1);
+        mbar_init(bar_a, 2);   // the two decayed-form products, issued by warps 0 and 1
+        mbar_init(bar_w, 4);   // the four W / U0 partial products, issued by warps 0-3
         mbar_fence_init();
         load_raw(blockIdx.x);
     }
@@ -317,17 +317,22 @@ __global__ void __launch_bounds__(256, 2)
             tc_fence_before();
             __syncthreads();
             tc_fence_after();
-            if (tid == 0) {
+            // Issuing a tcgen05.mma occupies its thread for a few hundred cycles, so the two products go
+            // out from two warps.
+            if (lane == 0 && warp < 2) {
                 constexpr uint32_t idA = idesc_tf32(128, 64);
                 const uint32_t rt = smem_u32(smem + RT), pt = smem_u32(smem + PT);
-                // product Y: A = R groups 0..15 ([R^(2); R^(0)]), B = P rows 64..127 ([P_2; P_0])
-                // product X: A = R groups 10..25 ([R^(3); R^(1)]), B = P rows 0..63 ([P_3; P_1])
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_tf32(tmem + T_Y, smem_desc(rt + kk * 2 * QLBO, QLBO, QSBO),
-                             smem_desc(pt + 8 * QSBO + kk * 2 * QLBO, QLBO, QSBO), idA, (r > 0 || kk > 0) ? 1u : 0u);
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_tf32(tmem + T_X, smem_desc(rt + RG3 * QSBO + kk * 2 * QLBO, QLBO, QSBO),
-                             smem_desc(pt + kk * 2 * QLBO, QLBO, QSBO), idA, (r > 0 || kk > 0) ? 1u : 0u);
+                if (warp == 0) {
+                    // product Y: A = R groups 0..15 ([R^(2); R^(0)]), B = P rows 64..127 ([P_2; P_0])
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_tf32(tmem + T_Y, smem_desc(rt + kk * 2 * QLBO, QLBO, QSBO),
+                                 smem_desc(pt + 8 * QSBO + kk * 2 * QLBO, QLBO, QSBO), idA, (r > 0 || kk > 0) ? 1u : 0u);
+                } else {
+                    // product X: A = R groups 10..25 ([R^(3); R^(1)]), B = P rows 0..63 ([P_3; P_1])
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_tf32(tmem + T_X, smem_desc(rt + RG3 * QSBO + kk * 2 * QLBO, QLBO, QSBO),
+                                 smem_desc(pt + kk * 2 * QLBO, QLBO, QSBO), idA, (r > 0 || kk > 0) ? 1u : 0u);
+                }
                 mma_commit(bar_a);
             }
         }
@@ -476,18 +481,15 @@ __global__ void __launch_bounds__(256, 2)
         tc_fence_after();
 
         // ---- 5. W^T = Kg^T (T_hi + T_lo)^T and U0^T = V^T (T_hi + T_lo)^T (M = 128, N = 64, K = 64)
-        if (tid == 0) {
+        // four partial products, one per issuing warp, each in its own 64 TMEM columns (the decayed-form
+        // accumulators are read): Kg^T T_hi^T, Kg^T T_lo^T, V^T T_hi^T, V^T T_lo^T
+        if (lane == 0 && warp < 4) {
             constexpr uint32_t idW = idesc_bf16(128, 64, 0, 0);
-            const uint32_t kg = smem_u32(smem + KG), vb = smem_u32(smem + VB);
-            const uint32_t thi = smem_u32(smem + TB_HI), tlo = smem_u32(smem + TB_LO);
+            const uint32_t a = smem_u32(smem + (warp < 2 ? KG : VB));
+            const uint32_t b = smem_u32(smem + ((warp & 1) ? TB_LO : TB_HI));
             for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + T_W, smem_desc(kg + kk * 256, 128, 1024), smem_desc(thi + kk * 256, 128, 1024), idW, kk > 0);
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + T_W, smem_desc(kg + kk * 256, 128, 1024), smem_desc(tlo + kk * 256, 128, 1024), idW, 1);
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + T_U0, smem_desc(vb + kk * 256, 128, 1024), smem_desc(thi + kk * 256, 128, 1024), idW, kk > 0);
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + T_U0, smem_desc(vb + kk * 256, 128, 1024), smem_desc(tlo + kk * 256, 128, 1024), idW, 1);
+                mma_bf16(tmem + 64 * warp, smem_desc(a + kk * 256, 128, 1024), smem_desc(b + kk * 256, 128, 1024), idW,
+                         kk > 0);
             mma_commit(bar_w);
         }
         if (!wait_all(bar_w, par_w)) { ok = false; break; }
@@ -500,17 +502,22 @@ __global__ void __launch_bounds__(256, 2)
             }
             fetch_small(item + gridDim.x);
         }
-        // record W (MN-major bf16, thread = channel) and U0 (column-major fp32, thread = value column)
+        // record W (MN-major fp16, thread = channel) and U0 (column-major fp32, thread = value column), each
+        // the sum of its hi and lo partial
         {
             const uint32_t lb = static_cast<uint32_t>((warp & 3) * 32) << 16;
-            const uint32_t col = warp < 4 ? T_W : T_U0;
+            const uint32_t col = warp < 4 ? 0 : 128;
             const int row = (warp & 3) * 32 + lane;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                float d[32];
+                float d[32], e[32];
                 tmem_ld16(tmem + lb + col + 32 * half, d);
                 tmem_ld16(tmem + lb + col + 32 * half + 16, d + 16);
+                tmem_ld16(tmem + lb + col + 64 + 32 * half, e);
+                tmem_ld16(tmem + lb + col + 64 + 32 * half + 16, e + 16);
                 tmem_ld_wait();
+#pragma unroll
+                for (int u = 0; u < 32; ++u) d[u] += e[u];
                 if (warp < 4) {
 #pragma unroll
                     for (int tb = 0; tb < 32; tb += 8)
