@@ -82,7 +82,7 @@ def kernel_work(name: str, w, units: float) -> tuple[float, float]:
 # has not been captured again.
 PROFILED_TRAFFIC = {
     ("kda_grad_tc", True): 9814.0,
-    ("kda_intra_tc", False): 2609.0,   # forward record only (forward-only workloads)
+    ("kda_intra_tc", False): 2225.0,   # forward record only (forward-only workloads; intra2_kernel)
     ("kda_intra_tc", True): 7271.0,    # forward that keeps the backward record, once per training step
 }
 
