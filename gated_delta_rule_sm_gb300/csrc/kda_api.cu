@@ -86,10 +86,12 @@ static WsPlan plan_simt(const Shape& s, bool bwd) {
 static bool tc_eligible(const Shape& s) { return s.dtype == KDA_BF16 && s.K == 128 && s.V == 128; }
 
 // The tensor-core path's 16-token sub-block factorisation of the decay needs the lower-bounded
-// gate with |lower_bound| <= 5 (exp of up to 16 * 5 stays inside fp32 range).  The forward also
-// takes the unbounded gate: its diagonal sub-blocks then come from diag_tc_kernel instead.
-static bool tc_gate_ok(const Shape& s, float lb) { return s.gate == KDA_GATE_LOWER_BOUNDED && lb >= -5.0f; }
-static bool tc_fwd_gate_ok(const Shape& s, float lb) { return s.gate == KDA_GATE_SOFTPLUS || tc_gate_ok(s, lb); }
+// gate with |lower_bound| <= 5 (exp of up to 16 * 5 stays inside fp32 range).  It also takes the
+// unbounded gate: the diagonal sub-blocks of the intra-chunk forms then come from diag_tc_kernel,
+// and the gradient kernel sums its diagonal sub-blocks pair by pair.
+static bool tc_gate_ok(const Shape& s, float lb) {
+    return s.gate == KDA_GATE_SOFTPLUS || (s.gate == KDA_GATE_LOWER_BOUNDED && lb >= -5.0f);
+}
 
 struct TcPlan {
     size_t off_chunk, off_rec, off_diag, total;
@@ -110,6 +112,7 @@ struct TcBwdPlan {
     WsPlan simt;        // chunk table, fp32 backward records, states, partials, scratch
     size_t off_bwrec;   // reverse-chain records
     size_t off_u, off_du;   // U and dU per (chunk, head), written by the two chains
+    size_t off_diag;    // unbounded gate: diagonal sub-blocks for the record pass (0 otherwise)
     size_t total;
 };
 
@@ -120,6 +123,8 @@ static TcBwdPlan plan_tc_bwd(const Shape& s) {
     w.off_bwrec = o; o = align_up(o + (size_t)s.NCmax * s.H * bwrec::BYTES);
     w.off_u = o; o = align_up(o + sizeof(float) * (size_t)s.NCmax * s.H * 64 * s.V);
     w.off_du = o; o = align_up(o + sizeof(float) * (size_t)s.NCmax * s.H * 64 * s.V);
+    w.off_diag = 0;
+    if (s.gate == KDA_GATE_SOFTPLUS) { w.off_diag = o; o = align_up(o + diag_item_bytes() * s.NCmax * s.H); }
     w.total = o;
     return w;
 }
@@ -274,10 +279,7 @@ static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cu
         p.rec = saved;
         p.rec_stride = RecLayout::make(s.K, s.V).bwd_size;
     }
-    if (s.gate == KDA_GATE_SOFTPLUS) {
-        if (saved) return KDA_ERR_UNSUPPORTED;   // the backward record needs the factorised decay
-        p.diag = reinterpret_cast<float*>(b + w.off_diag);
-    }
+    if (s.gate == KDA_GATE_SOFTPLUS) p.diag = reinterpret_cast<float*>(b + w.off_diag);
     KDA_TRY_CUDA(launch_plan(p, stream));
     if (p.diag) KDA_TRY_CUDA(launch_diag_tc(p, stream));
     if (!saved && !p.diag) KDA_TRY_CUDA(launch_intra2(p, recs, stream));
@@ -332,7 +334,13 @@ static kda_status bwd_tc(const Shape& s, Params p, void* workspace, size_t works
     pf.out = nullptr;
     pf.ST = nullptr;
     KDA_TRY_CUDA(launch_plan(p, stream));
-    if (!saved) KDA_TRY_CUDA(launch_intra_tc(p, nullptr, 1, stream));
+    if (!saved) {
+        if (s.gate == KDA_GATE_SOFTPLUS) {
+            p.diag = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.off_diag);
+            KDA_TRY_CUDA(launch_diag_tc(p, stream));
+        }
+        KDA_TRY_CUDA(launch_intra_tc(p, nullptr, 1, stream));
+    }
     KDA_TRY_CUDA(launch_bwd_pre(p, bw, stream));
     KDA_TRY_CUDA(launch_chain_rec_tc(pf, bw, stream));
     KDA_TRY_CUDA(launch_chain_bwd_tc(p, bw, stream));
@@ -342,7 +350,7 @@ static kda_status bwd_tc(const Shape& s, Params p, void* workspace, size_t works
 
 // Bytes of the record kda_fwd_save keeps (0 when the shape does not take the tensor-core path).
 static size_t saved_bytes_for(const Shape& s) {
-    if (!tc_eligible(s) || s.gate != KDA_GATE_LOWER_BOUNDED) return 0;
+    if (!tc_eligible(s)) return 0;
     return sizeof(float) * (size_t)s.NCmax * s.H * RecLayout::make(s.K, s.V).bwd_size;
 }
 
@@ -406,7 +414,7 @@ kda_status kda_fwd(const kda_dims* dims, const void* q, const void* k, const voi
     Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
                            initial_state);
     // the tensor-core path needs 16-byte aligned activations and a gate it can factorise
-    if (!tc_eligible(s) || !tc_fwd_gate_ok(s, lower_bound) || !tc_inputs_aligned(p))
+    if (!tc_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p))
         return kda_fwd_simt(dims, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, chunk_size,
                             cu_seqlens, cu_seqlens_host, initial_state, out, final_state, workspace, workspace_bytes,
                             stream);
@@ -463,7 +471,7 @@ kda_status kda_fwd_segmented(const kda_dims* dims, const void* q, const void* k,
     if (st != KDA_OK) return st;
     if (!out || segments < 1) return KDA_ERR_INVALID_ARG;
     Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, nullptr, initial_state);
-    if (!tc_eligible(s) || !tc_fwd_gate_ok(s, lower_bound) || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
+    if (!tc_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
     const SegPlan w = plan_seg(s, segments);
     st = check_ws(workspace, workspace_bytes, w.total);
     if (st != KDA_OK) return st;

@@ -7,7 +7,7 @@
 //     U = U0 - W S0,   O = scale (Qg S0 + Aqk U),   S_end = Diag(exp(Gamma_last)) S0 + Kd^T U,
 //     T = N Diag(beta), N = (I + Diag(beta) Bkk)^-1, W = T Kg, U0 = T v
 // is formed here and pushed through the decayed bilinear forms, the cumulative log-decay and the
-// prologue (L2 norm, sigmoid beta, lower-bounded gate).
+// prologue (L2 norm, sigmoid beta, the gate under either activation).
 //
 // Phase 1 walks the four 32-column slices of V: the slice outer products (dKg, dQg, dKd, dT, dA)
 // accumulate in TMEM from tcgen05 MMAs on bf16 hi / lo operands; the small dependent products in
@@ -185,6 +185,8 @@ constexpr uint32_t T_KG = 0, T_QG = 128, T_KD = 256, T_T = 384, T_A = 448;
 
 }  // namespace
 
+// SP: the unbounded (softplus) gate, whose diagonal sub-blocks are summed pair by pair.
+template <bool SP>
 __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     extern __shared__ float sm[];
     const int c = blockIdx.x, h = blockIdx.y;
@@ -589,13 +591,17 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     //   dk_L[t]  = sum_j l_j(t) (dB[:, J] R[J, :])[t]
     //   dk_R[s]  = r(s) sum_t (dA[t][s] q[t] + dB[t][s] k[t]) l_j(t),   s in J
     // Each warp owns the same 8 blocks (rows wm0, cols 64 (w % 2) + 8 b) of all three results.
+    // Under the unbounded gate nothing bounds l_j(t) inside sub-block j itself, so there the
+    // factorised forms cover only the pairs across sub-blocks and the diagonal sub-block is summed
+    // directly below.
+    constexpr bool sp = SP;
     float fq[8][4], fkl[8][4], fkr[8][4];
 #pragma unroll
     for (int b = 0; b < 8; ++b)
 #pragma unroll
         for (int e = 0; e < 4; ++e) fq[b][e] = fkl[b][e] = fkr[b][e] = 0.f;
     const int bt = warp >> 1;   // sub-block of this warp's rows
-    for (int j = 0; j <= bt; ++j) {
+    for (int j = 0; j <= (sp ? bt - 1 : bt); ++j) {
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
             const int n0 = 64 * (warp & 1) + 32 * hb;
@@ -631,7 +637,7 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
             for (int e = 0; e < 4; ++e) fkr[b][e] = 0.f;
         }
 #pragma unroll 1
-        for (int k0 = 16 * j; k0 < 64; k0 += 8) {
+        for (int k0 = sp ? 16 * j + 16 : 16 * j; k0 < 64; k0 += 8) {
             uint32_t aAh[4], aAl[4], aBh[4], aBl[4];
             // A(m = s, k = t) = dA[t][s] (transposed access), rows s = wm0 + ...
             split_tf32(dA[(k0 + qd) * P64 + wm0 + g], aAh[0], aAl[0]);
@@ -719,6 +725,43 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         }
     }
     __syncthreads();
+    if (sp) {
+        // Unbounded gate: the pairs inside each diagonal sub-block, which the factorised forms left out,
+        // directly.  Thread = (channel, two sub-blocks); the 16 tokens of a sub-block sit in registers and
+        // every pair s <= t takes one exponential exp(Gamma_t - Gamma_s) <= 1 that serves all three sums
+        // (dq_A and dk_L of row t, dk_R of row s); dA, dB are read as warp-wide broadcasts.
+        const int cc = tid & 127;
+#pragma unroll 1
+        for (int bb = 0; bb < 2; ++bb) {
+            const int t0 = 16 * (2 * (tid >> 7) + bb);
+            float gg[16], kk[16], qq[16], Dq[16], Dl[16], Dr[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                gg[u] = Gm[(t0 + u) * K + cc];
+                kk[u] = kh[(t0 + u) * K + cc];
+                qq[u] = qh[(t0 + u) * K + cc];
+                Dq[u] = Dl[u] = Dr[u] = 0.f;
+            }
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+#pragma unroll
+                for (int u = 0; u <= t; ++u) {
+                    const float E = __expf(gg[t] - gg[u]);
+                    const float a = dA[(t0 + t) * P64 + t0 + u], b = dB[(t0 + t) * P64 + t0 + u];
+                    Dq[t] += a * kk[u] * E;
+                    Dl[t] += b * kk[u] * E;
+                    Dr[u] += (a * qq[t] + b * kk[t]) * E;
+                }
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                const int r = (t0 + t) * P128 + cc;
+                sdq[r] += Dq[t];
+                sdk[r] += Dl[t] + Dr[t];
+                sdG[r] += qq[t] * Dq[t] + kk[t] * (Dl[t] - Dr[t]);
+            }
+        }
+        __syncthreads();
+    }
     // reverse cumulative sum over t (plus the Gamma_last term) gives dg
     if (tid < K) {
         float run = sgl[tid];
@@ -728,7 +771,7 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         }
     }
     __syncthreads();
-    // ---- prologue backward: L2 norms, sigmoid(beta), lower-bounded gate
+    // ---- prologue backward: L2 norms, sigmoid(beta), the gate
     for (int t0 = warp; t0 < len; t0 += 16) {   // rows t0 and t0 + 8 of this warp, interleaved
         float qv[2][4], kv[2][4], sq[2] = {0.f, 0.f}, sk[2] = {0.f, 0.f};
 #pragma unroll
@@ -795,7 +838,15 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
             const int t = hf + 2 * u;
-            if (t < len) {
+            if (t < len && sp) {
+                // g = -e^a softplus(x): dg/dx = -e^a sigmoid(x), dg/da = g
+                const float x = gv[u] + dtbv;
+                const float sg = __fdividef(1.f, 1.f + __expf(-x));
+                const float dx = -sdG[t * P128 + cc] * ea * sg;
+                dgr[((size_t)(tok0 + t) * H + h) * K + cc] = dx;
+                dtb += dx;
+                alog_part -= sdG[t * P128 + cc] * ea * (fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x))));
+            } else if (t < len) {
                 const float z = ea * (gv[u] + dtbv);
                 const float sg = __fdividef(1.f, 1.f + __expf(-z));   // ~2^-21 relative: ample for dg_raw
                 const float dz = sdG[t * P128 + cc] * p.lb * sg * (1.f - sg);
@@ -952,10 +1003,11 @@ cudaError_t launch_bwd_pre(const Params& p, uint8_t* bw, cudaStream_t st) {
 
 cudaError_t launch_grad_tc(const Params& p, cudaStream_t st) {
     const size_t smem = (size_t)SMEM_FLOATS * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = p.gate == KDA_GATE_SOFTPLUS ? grad_tc_kernel<true> : grad_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     timing_pre(st, K_GRAD_TC);
-    grad_tc_kernel<<<dim3(p.NCmax, p.H), 256, smem, st>>>(p);
+    kern<<<dim3(p.NCmax, p.H), 256, smem, st>>>(p);
     timing_post(st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -92,7 +92,9 @@ __device__ __forceinline__ void mma16_split(float (&acc)[2][4], const float* a, 
 // MODE 0 writes the chain record (tcrec) of the forward; MODE 1 writes the fp32 per-chunk record
 // (RecLayout) that the backward's operand, chain and gradient kernels read; MODE 2 writes both (a
 // forward that keeps the backward record, so the backward skips this pass).
-template <int MODE>
+// GATE_RT: the gate is read from Params at run time (either activation); otherwise the lower-bounded gate
+// is compiled in and the unbounded gate's diagonal-block steps are left out.
+template <int MODE, bool GATE_RT>
 __global__ void __launch_bounds__(256, 1)
     intra_tc_kernel(Params p, uint8_t* recs, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_g,
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(256, 1)
     uint64_t* bar_w = bar_load + 3;   // the final W / U0 MMAs (two issuing warps)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_load + 4);
     uint64_t* bar_diag = bar_load + 5;   // unbounded gate: the diagonal blocks of an item
-    const bool sp = !BWD && p.gate == KDA_GATE_SOFTPLUS;   // the backward modes never see this gate
+    const bool sp = GATE_RT && p.gate == KDA_GATE_SOFTPLUS;   // diagonal sub-blocks from diag_tc_kernel
     auto load_diag = [&](int it) {
         mbar_expect_tx(bar_diag, diaglay::BYTES);
         bulk_g2s(smem + DIAG, p.diag + (size_t)it * diaglay::FLOATS, diaglay::BYTES, bar_diag);
@@ -1185,7 +1187,10 @@ cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, int mode, cudaStream
     if (!head_tile_map(&mq, p.q, p.Hk, p.TT) || !head_tile_map(&mk, p.k, p.Hk, p.TT) ||
         !head_tile_map(&mg, p.g_raw, p.H, p.TT) || !head_tile_map(&mv, p.v, p.H, p.TT))
         return cudaErrorInvalidValue;
-    auto kern = mode == 0 ? intra_tc_kernel<0> : mode == 1 ? intra_tc_kernel<1> : intra_tc_kernel<2>;
+    const bool sp = p.gate == KDA_GATE_SOFTPLUS;
+    auto kern = mode == 0 ? (sp ? intra_tc_kernel<0, true> : intra_tc_kernel<0, false>)
+              : mode == 1 ? (sp ? intra_tc_kernel<1, true> : intra_tc_kernel<1, false>)
+                          : (sp ? intra_tc_kernel<2, true> : intra_tc_kernel<2, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)intralay::BYTES);
     if (e != cudaSuccess) return e;
     timing_pre(st, K_INTRA_TC);

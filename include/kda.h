@@ -135,9 +135,10 @@ size_t kda_bwd_workspace_size(const kda_dims* dims, int chunk_size);
  *     sub-block factorisation of the decay stays inside fp32 range only for
  *     |lower_bound| <= 5.  With the lower-bounded gate that is required of
  *     both directions.
- *   - Under the unbounded gate the forward takes the tensor-core path too:
- *     the diagonal sub-blocks, where the factorisation has no bound, are
- *     formed directly.  The backward runs on the SIMT path.
+ *   - Under the unbounded gate both directions take the tensor-core path
+ *     too: the diagonal sub-blocks, where the factorisation has no bound,
+ *     are formed directly (in the forward's intra-chunk forms and in the
+ *     backward's decayed bilinear forms).
  *   - Every other supported shape, and fp32 inputs, run on the fp32 SIMT
  *     path.  It forms every decay as exp(Gamma_t - Gamma_s) <= 1, which holds
  *     for any gate.
@@ -195,7 +196,7 @@ kda_status kda_bwd(const kda_dims* dims,
  * them (same q, k, v, g_raw, beta_raw, a_log, dt_bias, lower_bound,
  * cu_seqlens), until the caller reuses the buffer.  Both calls return
  * KDA_ERR_UNSUPPORTED when the tensor-core path does not apply (dtype, K, V,
- * lower_bound < -5 or unaligned activations) and KDA_ERR_WORKSPACE for a
+ * the lower-bounded gate with lower_bound < -5, or unaligned activations) and KDA_ERR_WORKSPACE for a
  * missing, small or misaligned `saved`.  The workspace of kda_fwd_save is
  * kda_fwd_workspace_size's, of kda_bwd_saved kda_bwd_workspace_size's.
  */

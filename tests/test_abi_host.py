@@ -217,11 +217,16 @@ def test_gate_selection_validation(lib):
     assert _fwd(lib, _dims(gate=SP), lb=0.0) == _lib.KDA_ERR_INVALID_ARG     # lower_bound checked under either gate
     f = lambda **kw: lib.kda_fwd_workspace_size(ctypes.byref(_dims(**kw)), 64)
     assert f(gate=SP) == f() > 0
-    # the unbounded gate has no tensor-core path: no saved context, and the saved pair refuses it
-    d128 = _dims(K=128, V=128, gate=SP)
-    assert lib.kda_saved_size(ctypes.byref(d128), 64) == 0
-    assert _fwd_save(lib, d128) == _lib.KDA_ERR_UNSUPPORTED
-    assert _bwd_saved(lib, d128) == _lib.KDA_ERR_UNSUPPORTED
+    # the unbounded gate takes the tensor-core path in both directions: the same saved context as the
+    # lower-bounded gate, and the saved pair stops at the missing buffer; its backward workspace adds
+    # the diagonal sub-blocks of the record pass
+    d128, b128 = _dims(K=128, V=128, gate=SP), _dims(K=128, V=128)
+    assert lib.kda_saved_size(ctypes.byref(d128), 64) == lib.kda_saved_size(ctypes.byref(b128), 64) > 0
+    assert _fwd_save(lib, d128) == _lib.KDA_ERR_WORKSPACE
+    assert _bwd_saved(lib, d128) == _lib.KDA_ERR_WORKSPACE
+    assert _fwd_save(lib, d128, lb=-50.0) == _lib.KDA_ERR_WORKSPACE           # lower_bound not used by this gate
+    bw = lambda d: lib.kda_bwd_workspace_size(ctypes.byref(d), 64)
+    assert bw(d128) > bw(b128) > 0
 
 
 def _conv_fwd(lib, B=1, T=64, C=64, W=4, dtype=_lib.KDA_BF16, ptr=16, cu=None, n=0, y=16):

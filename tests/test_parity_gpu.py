@@ -405,18 +405,55 @@ def test_softplus_gate_fp32_fwd_bwd():
     _check_bwd(x, "fp32")
 
 
+def _launched(fn):
+    """Names of the library kernels fn() launches."""
+    from gated_delta_rule_sm_gb300 import _lib
+    _lib.timing_begin(4096)
+    try:
+        fn()
+        torch.cuda.synchronize()
+    finally:
+        names = {n for n, _ in _lib.timing_end()}
+    return names
+
+
 def test_softplus_gate_bf16_d128_varlen_fwd_bwd():
-    """bf16 K = V = 128 with the unbounded gate runs on the SIMT path (no tensor-core factorisation)."""
+    """bf16 K = V = 128 with the unbounded gate: both directions on the tensor-core path (the diagonal
+    sub-blocks from the pre-pass in the record pass, summed pair by pair in the gradient kernel), and the
+    training pair keeps the record for it too."""
     import gated_delta_rule_sm_gb300 as kda
     x = _softplus_case(B=1, T=400, H=2, K=128, V=128, varlen=True, initial_state=True, backward=True, seed=61,
                        lengths=[90, 1, 64, 200, 45])
     _check_fwd(x, "bf16")
-    _check_bwd(x, "bf16")
-    assert kda.saved_size(x["q"], x["v"], x["cu_seqlens"], gate="softplus") == 0
-    with pytest.raises(kda.KdaError):
-        buf = torch.empty(1 << 20, dtype=torch.uint8, device=DEV)
-        kda.forward(*[x[n] for n in ("q", "k", "v", "g_raw", "beta_raw", "a_log", "dt_bias")], scale=x["scale"],
-                    gate="softplus", cu_seqlens=x["cu_seqlens"], saved=buf)
+    names = _launched(lambda: _check_bwd(x, "bf16"))
+    assert {"kda_diag_tc", "kda_intra_tc", "kda_grad_tc", "kda_chain_bwd_tc"} <= names, names
+    assert "kda_grad_simt" not in names, names
+    args = [x[n] for n in ("q", "k", "v", "g_raw", "beta_raw", "a_log", "dt_bias")]
+    kw = dict(scale=x["scale"], lower_bound=x["lower_bound"], gate="softplus", cu_seqlens=x["cu_seqlens"],
+              initial_state=x["initial_state"])
+    nbytes = kda.saved_size(x["q"], x["v"], x["cu_seqlens"], gate="softplus")
+    assert nbytes > 0
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    o1, _ = kda.forward(*args, saved=buf, **kw)
+    g1 = kda.backward(*args, x["dout"], saved=buf, **kw)
+    g2 = kda.backward(*args, x["dout"], **kw)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    r_out, _ = oracle_fwd(x)
+    assert rel_err(o1, r_out, "bf16") <= tol("bf16")
+    for n in GRADS:
+        assert torch.equal(g1[n], g2[n]), n
+
+
+@pytest.mark.parametrize("g_mean,Hk", [(0.0, 0), (4.0, 0), (-6.0, 0), (0.0, 1)])
+def test_softplus_gate_tensor_core_backward(g_mean, Hk):
+    """The tcgen05 backward under the unbounded gate: typical, steep (g near -64 per token: exp(Gamma)
+    underflows inside a chunk) and mild decays, and grouped key heads, with a final-state gradient."""
+    x = _softplus_case(B=2, T=300, H=2, K=128, V=128, initial_state=True, backward=True, g_mean=g_mean, Hk=Hk,
+                       seed=66)
+    dfinal = 0.1 * torch.randn((2, 2, 128, 128), generator=torch.Generator().manual_seed(7)).to(DEV)
+    names = _launched(lambda: _check_bwd(x, "bf16", dfinal=dfinal))
+    assert "kda_grad_tc" in names and "kda_grad_simt" not in names, names
 
 
 def test_softplus_gate_mild_long_memory():
