@@ -167,6 +167,7 @@ constexpr int O_DY = O_DU + 64 * P32;       // [64][P32]   dY slice
 constexpr int O_BETA = O_DY + 64 * P32;     // [64]
 constexpr int O_GRAW = O_DO + 64 * P64;    // bf16 [64][128] g_raw tile, phase 2 (after dB: tmp is dead)
 static_assert(O_GRAW >= O_DS + 64 * P128 && O_GRAW + 64 * 128 / 2 <= O_BETA, "g_raw tile inside the free tail");
+static_assert(2 * 16 * 256 <= 64 * P128 && 16 * 256 <= 64 * P64, "diagonal-pass scratch inside the R and N tiles");
 constexpr int O_RED = O_BETA + 64;          // [64] dbeta, [128] Gamma_last gradient, [8] block sums, [256] dt_bias parts
 constexpr int O_MBAR = O_RED + 64 + 128 + 8 + 256;   // 8-byte mbarrier + TMEM slot (4 floats)
 constexpr int SMEM_FLOATS = O_MBAR + 4;
@@ -184,6 +185,54 @@ static_assert(B_DS + 16384 <= (uint32_t)O_KG * 4 && B_DO + 4096 <= (uint32_t)O_N
 constexpr uint32_t T_KG = 0, T_QG = 128, T_KD = 256, T_T = 384, T_A = 448;
 
 }  // namespace
+
+// Unbounded gate: the pairs inside each diagonal sub-block, which the factorised forms left out,
+// directly.  Thread = (channel, two sub-blocks).  For every pair s <= t of a sub-block one decay
+// exp(Gamma_t - Gamma_s) <= 1 (it can only underflow) serves all three sums (dq_A and dk_L of row t,
+// dk_R of row s); the row-t terms go straight into the thread's own column of dq, dk and dGamma in
+// shared memory, and dA, dB are warp-wide broadcasts.  The sub-block's Gamma, k and q of the thread's
+// channel are first copied into shared scratch ([16][256], the thread's own column, so no barrier), where
+// rolled loops index them cheaply: the gradient kernel is large enough that unrolled code here costs
+// more in instruction fetch than it saves, and rolled loops over global rows wait on L2 every pair.
+__device__ __noinline__ void diag_pairs(const float* __restrict__ Gm, const float* __restrict__ kh,
+                                        const float* __restrict__ qh, const float* dA, const float* dB, float* sdq,
+                                        float* sdk, float* sdG, float* sg, float* sk, float* sq, int tid) {
+    constexpr int K = 128;
+    const int cc = tid & 127;
+#pragma unroll 1
+    for (int bb = 0; bb < 2; ++bb) {
+        const int t0 = 16 * (2 * (tid >> 7) + bb);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int gi = (t0 + u) * K + cc;
+            sg[u * 256 + tid] = Gm[gi];
+            sk[u * 256 + tid] = kh[gi];
+            sq[u * 256 + tid] = qh[gi];
+        }
+#pragma unroll 1
+        for (int s = 0; s < 16; ++s) {
+            const float ks = sk[s * 256 + tid], gs = sg[s * 256 + tid];
+            const float* ca = dA + t0 * P64 + t0 + s;   // column s of the sub-block: ca[t * P64]
+            const float* cb = dB + t0 * P64 + t0 + s;
+            float dr = 0.f;
+#pragma unroll 2
+            for (int t = s; t < 16; ++t) {
+                const float E = __expf(sg[t * 256 + tid] - gs);
+                const float a = ca[t * P64], b = cb[t * P64];
+                const float qt = sq[t * 256 + tid], kt = sk[t * 256 + tid];
+                const float x = a * ks * E, y = b * ks * E;
+                const int r = (t0 + t) * P128 + cc;
+                sdq[r] += x;
+                sdk[r] += y;
+                sdG[r] += qt * x + kt * y;
+                dr += (a * qt + b * kt) * E;
+            }
+            const int r = (t0 + s) * P128 + cc;
+            sdk[r] += dr;
+            sdG[r] -= ks * dr;
+        }
+    }
+}
 
 // SP: the unbounded (softplus) gate, whose diagonal sub-blocks are summed pair by pair.
 template <bool SP>
@@ -726,40 +775,8 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     }
     __syncthreads();
     if (sp) {
-        // Unbounded gate: the pairs inside each diagonal sub-block, which the factorised forms left out,
-        // directly.  Thread = (channel, two sub-blocks); the 16 tokens of a sub-block sit in registers and
-        // every pair s <= t takes one exponential exp(Gamma_t - Gamma_s) <= 1 that serves all three sums
-        // (dq_A and dk_L of row t, dk_R of row s); dA, dB are read as warp-wide broadcasts.
-        const int cc = tid & 127;
-#pragma unroll 1
-        for (int bb = 0; bb < 2; ++bb) {
-            const int t0 = 16 * (2 * (tid >> 7) + bb);
-            float gg[16], kk[16], qq[16], Dq[16], Dl[16], Dr[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                gg[u] = Gm[(t0 + u) * K + cc];
-                kk[u] = kh[(t0 + u) * K + cc];
-                qq[u] = qh[(t0 + u) * K + cc];
-                Dq[u] = Dl[u] = Dr[u] = 0.f;
-            }
-#pragma unroll
-            for (int t = 0; t < 16; ++t)
-#pragma unroll
-                for (int u = 0; u <= t; ++u) {
-                    const float E = __expf(gg[t] - gg[u]);
-                    const float a = dA[(t0 + t) * P64 + t0 + u], b = dB[(t0 + t) * P64 + t0 + u];
-                    Dq[t] += a * kk[u] * E;
-                    Dl[t] += b * kk[u] * E;
-                    Dr[u] += (a * qq[t] + b * kk[t]) * E;
-                }
-#pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                const int r = (t0 + t) * P128 + cc;
-                sdq[r] += Dq[t];
-                sdk[r] += Dl[t] + Dr[t];
-                sdG[r] += qq[t] * Dq[t] + kk[t] * (Dl[t] - Dr[t]);
-            }
-        }
+        // scratch: the R tile's area (dead since the bilinear forms) and N's (dead since dL)
+        diag_pairs(Gm, kh, qh, dA, dB, sdq, sdk, sdG, R, R + 16 * 256, sN, tid);
         __syncthreads();
     }
     // reverse cumulative sum over t (plus the Gamma_last term) gives dg
@@ -845,7 +862,7 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
                 const float dx = -sdG[t * P128 + cc] * ea * sg;
                 dgr[((size_t)(tok0 + t) * H + h) * K + cc] = dx;
                 dtb += dx;
-                alog_part -= sdG[t * P128 + cc] * ea * (fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x))));
+                alog_part -= sdG[t * P128 + cc] * ea * (fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x))));
             } else if (t < len) {
                 const float z = ea * (gv[u] + dtbv);
                 const float sg = __fdividef(1.f, 1.f + __expf(-z));   // ~2^-21 relative: ample for dg_raw
