@@ -898,22 +898,26 @@ static_assert(chainlay::BYTES <= 232448, "shared memory per CTA");
 constexpr uint32_t kIdescWS = idesc_f16(128, 32, 1, 1);   // [W; Qg] and S both MN-major
 constexpr uint32_t kIdescKU = idesc_f16(128, 32, 0, 1);   // Kd^T / Aqk K-major, U MN-major
 
-// One CTA per (segment, head, 32-column slice of V): four compute warps, an MMA warp and a load warp.
-// Every operand is fp16 (one kind::f16 MMA per product, tf32-like accuracy at these magnitudes); the
-// state itself stays fp32 in registers.
+// One CTA per (segment, head, 32-column slice of V): four compute warps (0-3), two U helper warps
+// (4, 5), an MMA warp (6) and a load warp (7).  Every operand is fp16 (one kind::f16 MMA per product,
+// tf32-like accuracy at these magnitudes); the state itself stays fp32 in registers.
 // Compute thread c keeps row c of the state slice (32 fp32) in registers.  Per chunk the critical path
 // is
 //   MMA1 (W S) -> U = U0 - W S -> MMA2b (Kd^T U) -> S <- Diag(gC) S + Kd^T U -> next MMA1.
 // MMA1 and MMA2b are split over K into four partial accumulators, one per compute warp (lane 0
-// issues), and the epilogues add the partials.  The output is Qg S (rows 64..127 of the MMA1 partials)
-// plus Aqk U, which the MMA warp issues into its own accumulator as soon as U is staged, off the
-// critical path.  Records stream through two slots; the load warp refills a slot with the chunk two
-// ahead once every reader of its chunk is done (an `empty` mbarrier per slot).
+// issues), and the epilogues add the partials.  The U step reads TMEM lanes 0..63, which only warps
+// whose index is 0 or 1 modulo 4 can reach: warps 0, 1 take columns 0..15 and warps 4, 5 columns
+// 16..31, which halves that step's latency.  A compute warp issues its MMA1 partial of the next chunk
+// as soon as its own 32 rows of S are written (the partial contracts over exactly those rows).  The
+// output is Qg S (rows 64..127 of the MMA1 partials) plus Aqk U, which the MMA warp issues into its own
+// accumulator as soon as U is staged, off the critical path.  Records stream through three slots; the
+// load warp refills a slot with the chunk three ahead once every reader of its chunk is done (an
+// `empty` mbarrier per slot).
 // flags: kChainStoreStates (write the chunk-entering states), kChainTransfer (start every segment from
 // the identity and take U0 as zero: the final state is then the segment's transfer matrix, the product
 // of Diag(exp(Gamma_last)) - Kd^T W over its chunks; needs K == V).
 constexpr int kChainStoreStates = 1, kChainTransfer = 2;
-__global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const uint8_t* recs, int flags) {
+__global__ void __launch_bounds__(256, 1) chain_fwd_tc_kernel(Params p, const uint8_t* recs, int flags) {
     const bool store_states = flags & kChainStoreStates, transfer = flags & kChainTransfer;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int n = blockIdx.x, h = blockIdx.y, z = blockIdx.z, j0 = z * 32;
@@ -935,7 +939,10 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
     constexpr uint32_t TCOLS = 512;
 
     if (tid == 0) {
-        for (int b = 0; b < 2 * NS; ++b) mbar_init(&full[b], 1);   // full[NS], empty[NS]
+        for (int b = 0; b < NS; ++b) mbar_init(&full[b], 1);
+        // a slot is free once the four compute warps have read its exp(Gamma_last) (S step) and warp 2
+        // has seen the chunk's last MMA complete (output step)
+        for (int b = 0; b < NS; ++b) mbar_init(&empty[b], 5);
         mbar_init(bar_ws, 4);
         mbar_init(bar_s, 4);
         mbar_init(bar_o, 1);
@@ -956,9 +963,32 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
     const uint32_t tmem = *tslot;
     // D1[b] partial w at tmem + 128 b + 32 w; D3 partial w at tmem + 256 + 32 w; Aqk U of D1[b] at 384 + 32 b
     const uint32_t tD3 = tmem + 256, tDO = tmem + 384;
+    // U[t][j] = U0[t][j] - (W S)[t][j] for the 16 columns j0h .. j0h + 15 of row t (lane t % 32 of this
+    // warp's lane quarter), summed over the four MMA1 partials, as fp16 into the chunk's U buffer
+    auto u_half = [&](int i, int t, uint32_t lane_base, int j0h) {
+        const uint32_t tD1 = tmem + 128 * (i & 1) + lane_base + j0h;
+        float d[16], e[3][16];
+        tmem_ld16(tD1, d);
+#pragma unroll
+        for (int w = 0; w < 3; ++w) tmem_ld16(tD1 + 32 * (w + 1), e[w]);
+        tmem_ld_wait();
+        const float* u0 = reinterpret_cast<const float*>(slot_ptr(i) + chainlay::SLOT_U0);
+        uint8_t* UB = smem + chainlay::UB + (i & 1) * chainlay::UB_BYTES;
+#pragma unroll
+        for (int jg = 0; jg < 16; jg += 8) {
+            float u[8];
+#pragma unroll
+            for (int e8 = 0; e8 < 8; ++e8) {
+                const int j = jg + e8;
+                const float ws = d[j] + (e[0][j] + e[1][j]) + e[2][j];
+                u[e8] = (transfer ? 0.f : u0[(j0h + j) * 64 + t]) - ws;
+            }
+            *reinterpret_cast<uint4*>(UB + mn_bf16(j0h + jg, t, 128, 512)) = pack8_f16(u);
+        }
+    };
 
     bool ok = true;
-    if (warp == 5) {
+    if (warp == 7) {
         // load warp: chunk k into slot k % NS once chunk k - NS has released it
         if (lane == 0) {
             for (int k = 0; k < nch; ++k) {
@@ -978,7 +1008,7 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
             }
         }
         __syncwarp();
-    } else if (warp == 4) {
+    } else if (warp == 6) {
         // MMA warp: Aqk U of chunk i once its U is staged (rows 0..63 of this accumulator are unused)
         if (lane == 0) {
             for (int i = 0; i < nch; ++i) {
@@ -996,6 +1026,22 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
             }
         }
         __syncwarp();
+    } else if (warp >= 4) {
+        // U helpers: columns 16..31 of the U rows in lane quarter warp - 4 (t = tid - 128); warps 0 and 1
+        // take columns 0..15 of the same rows, so each thread of the U step handles half a row
+        const int t = tid - 128;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        for (int i = 0; i < nch; ++i) {
+            fail_wait(&full[i % NS], (i / NS) & 1);
+            fail_wait(bar_ws, i & 1);
+            tc_fence_after();
+            u_half(i, t, lane_base, 16);
+            fence_async_smem();
+            tc_fence_before();
+            const bool failed = named_sync_or(2, 192, *sh_fail != 0);
+            tc_fence_after();
+            if (failed) { ok = false; break; }
+        }
     } else {
     float S[32];
     {
@@ -1054,24 +1100,18 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
         }
         fail_wait(&full[i % NS], (i / NS) & 1);   // record visible to this thread
         if (warp < 2) {
-            // U[t][j] = U0[t][j] - (W S)[t][j], t = tid, as fp16: eight j per 16-byte row of a core matrix
+            // columns 0..15 of U rows t = tid (the helper warps take 16..31)
             fail_wait(bar_ws, par);
             tc_fence_after();
-            float d[32];
-            ld_sum4(tD1, d);
-            const float* u0 = reinterpret_cast<const float*>(sl + chainlay::SLOT_U0);
-            uint8_t* UB = smem + chainlay::UB + (i & 1) * chainlay::UB_BYTES;
-#pragma unroll
-            for (int jg = 0; jg < 32; jg += 8) {
-                float u[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) u[e] = (transfer ? 0.f : u0[(jg + e) * 64 + tid]) - d[jg + e];
-                *reinterpret_cast<uint4*>(UB + mn_bf16(jg, tid, 128, 512)) = pack8_f16(u);
-            }
+            u_half(i, tid, lane_base, 0);
         }
         fence_async_smem();
-        sync128();
-        if (*sh_fail) { ok = false; break; }
+        // U staged by warps 0, 1 and the helpers.  This is the loop's one exit point: a wait that gave up
+        // anywhere in the previous step is seen here by every thread of warps 0..5 at once.
+        tc_fence_before();
+        const bool failed = named_sync_or(2, 192, *sh_fail != 0);
+        tc_fence_after();
+        if (failed) { ok = false; break; }
         if (tid == 0) mbar_arrive(bar_u);   // the MMA warp may read U now
         // MMA2b: D3 partial w = Kd^T U over t in [16 w, 16 w + 16) (one K step)
         if (issuer) {
@@ -1092,10 +1132,12 @@ __global__ void __launch_bounds__(192, 1) chain_fwd_tc_kernel(Params p, const ui
             for (int jg = 0; jg < 4; ++jg)
                 *reinterpret_cast<uint4*>(SB + mn_bf16(8 * jg, tid, 128, 512)) = pack8_f16(S + 8 * jg);
         }
+        // MMA1 partial `warp` of the next chunk reads only this warp's 32 rows of S
         fence_async_smem();
-        sync128();
-        if (*sh_fail) { ok = false; break; }
+        __syncwarp();
+        if (issuer) mbar_arrive(&empty[i % NS]);   // this warp is done with the slot's exp(Gamma_last)
         if (issuer && i + 1 < nch) issue_mma1(i + 1);
+        __syncwarp();
         if (warp >= 2) {
             // output of chunk i: rows 64..127 of its MMA1 partials plus the Aqk U accumulator
             fail_wait(bar_o, par);
@@ -1211,7 +1253,7 @@ cudaError_t launch_chain_fwd_tc(const Params& p, const uint8_t* recs, bool store
                                          (int)chainlay::BYTES);
     if (e != cudaSuccess) return e;
     timing_pre(st, K_CHAIN_FWD_TC);
-    chain_fwd_tc_kernel<<<dim3(p.N, p.H, 4), 192, chainlay::BYTES, st>>>(
+    chain_fwd_tc_kernel<<<dim3(p.N, p.H, 4), 256, chainlay::BYTES, st>>>(
         p, recs, (store_states ? kChainStoreStates : 0) | (transfer ? kChainTransfer : 0));
     timing_post(st);
     return cudaGetLastError();
