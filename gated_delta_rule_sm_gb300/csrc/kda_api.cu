@@ -413,7 +413,9 @@ kda_status kda_fwd(const kda_dims* dims, const void* q, const void* k, const voi
     if (!out) return KDA_ERR_INVALID_ARG;
     Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
                            initial_state);
-    // the tensor-core path needs 16-byte aligned activations and a gate it can factorise
+    p.out = out;
+    p.ST = final_state;
+    // the tensor-core path needs 16-byte aligned activations and outputs and a gate it can factorise
     if (!tc_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p))
         return kda_fwd_simt(dims, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, chunk_size,
                             cu_seqlens, cu_seqlens_host, initial_state, out, final_state, workspace, workspace_bytes,
@@ -471,6 +473,8 @@ kda_status kda_fwd_segmented(const kda_dims* dims, const void* q, const void* k,
     if (st != KDA_OK) return st;
     if (!out || segments < 1) return KDA_ERR_INVALID_ARG;
     Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, nullptr, initial_state);
+    p.out = out;
+    p.ST = final_state;
     if (!tc_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
     const SegPlan w = plan_seg(s, segments);
     st = check_ws(workspace, workspace_bytes, w.total);
@@ -532,6 +536,8 @@ kda_status kda_fwd_save(const kda_dims* dims, const void* q, const void* k, cons
     if (!out) return KDA_ERR_INVALID_ARG;
     Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
                            initial_state);
+    p.out = out;
+    p.ST = final_state;
     if (!tc_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
     const size_t need = saved_bytes_for(s);
     if (!saved || saved_bytes < need || (reinterpret_cast<uintptr_t>(saved) % kAlign)) return KDA_ERR_WORKSPACE;

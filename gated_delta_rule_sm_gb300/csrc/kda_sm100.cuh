@@ -140,11 +140,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* mbar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* mbar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(mbar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait: false after `limit` polls (each poll may suspend the thread for a short while).
 __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, uint32_t limit = (1u << 22)) {
     for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(mbar, parity)) return true;
     return false;
+}
+
+// The same, tried first with one non-blocking test: for a phase that has usually completed already (a
+// blocking try_wait costs a couple of hundred cycles even then).  Where the phase is usually still
+// running, the plain wait is the better choice.
+__device__ __forceinline__ bool mbar_wait_done(uint64_t* mbar, uint32_t parity, uint32_t limit = (1u << 22)) {
+    if (mbar_test_wait(mbar, parity)) return true;
+    return mbar_wait(mbar, parity, limit);
 }
 
 // ---------------------------------------------------------------- named barriers

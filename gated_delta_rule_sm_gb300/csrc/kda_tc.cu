@@ -955,7 +955,7 @@ __global__ void __launch_bounds__(256, 1) chain_fwd_tc_kernel(Params p, const ui
     auto rec_ptr = [&](int i) { return recs + ((size_t)(cb + i) * H + h) * tcrec::BYTES; };
     auto ub_addr = [&](int i) { return smem_u32(smem + chainlay::UB + (i & 1) * chainlay::UB_BYTES); };
     auto fail_wait = [&](uint64_t* bar, uint32_t parity) {
-        if (!mbar_wait(bar, parity)) atomicExch((int*)sh_fail, 1);
+        if (!mbar_wait_done(bar, parity)) atomicExch((int*)sh_fail, 1);
     };
     tc_fence_before();
     __syncthreads();
@@ -1221,7 +1221,9 @@ bool head_tile_map2(CUtensorMap* m, const void* base, int H, int TT) { return he
 
 bool tc_inputs_aligned(const Params& p) {
     auto al = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
-    return al(p.q) && al(p.k) && al(p.g_raw) && al(p.v) && (p.dout == nullptr || al(p.dout));
+    // the forward chain stores the output and the final state 16 bytes at a time
+    return al(p.q) && al(p.k) && al(p.g_raw) && al(p.v) && (p.dout == nullptr || al(p.dout)) && al(p.out) &&
+           al(p.ST);
 }
 
 cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, int mode, cudaStream_t st) {
