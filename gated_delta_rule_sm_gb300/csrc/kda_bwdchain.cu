@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
     auto y_ptr = [&](int s) { return src.ybase + ((size_t)chunk_of(s) * H + h) * src.ystride; };
     auto p_ptr = [&](int s) { return src.pbase + ((size_t)chunk_of(s) * H + h) * src.pstride; };
     auto fail_wait = [&](uint64_t* bar, uint32_t parity) {
-        if (!mbar_wait(bar, parity)) atomicExch(sh_fail, 1);
+        if (!mbar_wait_done(bar, parity)) atomicExch(sh_fail, 1);
     };
     if (tid == 0)
         for (int s = 0; s < 2 && s < nch; ++s) {
