@@ -84,6 +84,12 @@ static WsPlan plan_simt(const Shape& s, bool bwd) {
 
 // Tensor-core path: bf16 activations with K = V = 128.
 static bool tc_eligible(const Shape& s) { return s.dtype == KDA_BF16 && s.K == 128 && s.V == 128; }
+// The plain forward also takes K = V = 64 heads under the lower-bounded gate: the intra pass loads them
+// as 128-channel tiles whose upper half the TMA fills with zeros, and the chain runs the two value
+// slices that exist over a state whose rows 64..127 stay zero.
+static bool tc_fwd_eligible(const Shape& s) {
+    return tc_eligible(s) || (s.dtype == KDA_BF16 && s.K == 64 && s.V == 64 && s.gate == KDA_GATE_LOWER_BOUNDED);
+}
 
 // The tensor-core path's 16-token sub-block factorisation of the decay needs the lower-bounded
 // gate with |lower_bound| <= 5 (exp of up to 16 * 5 stays inside fp32 range).  It also takes the
@@ -369,7 +375,7 @@ size_t kda_fwd_workspace_size(const kda_dims* dims, int chunk_size) {
     // size for the varlen bound when num_seqs is given, which also covers the fixed-length layout;
     // the larger of the two paths, so either entry point can use it
     const size_t a = plan_simt(s, false).total;
-    const size_t b = tc_eligible(s) ? plan_tc_fwd(s).total : 0;
+    const size_t b = tc_fwd_eligible(s) ? plan_tc_fwd(s).total : 0;
     return a > b ? a : b;
 }
 
@@ -416,7 +422,7 @@ kda_status kda_fwd(const kda_dims* dims, const void* q, const void* k, const voi
     p.out = out;
     p.ST = final_state;
     // the tensor-core path needs 16-byte aligned activations and outputs and a gate it can factorise
-    if (!tc_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p))
+    if (!tc_fwd_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p))
         return kda_fwd_simt(dims, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, chunk_size,
                             cu_seqlens, cu_seqlens_host, initial_state, out, final_state, workspace, workspace_bytes,
                             stream);

@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(256, 2)
     auto fetch_small = [&](int it) {
         int h2, c2, t02;
         const int len2 = item_tok0(it, h2, c2, t02);
-        if (tid < 128) nx_dtb = p.dt_bias[h2 * 128 + tid];
+        if (tid < 128) nx_dtb = tid < p.K ? p.dt_bias[h2 * p.K + tid] : 0.f;   // K = 64: channels 64.. padded
         if (tid < 64 && tid < len2) nx_braw = load_act(p.beta_raw, (size_t)(t02 + tid) * H + h2, KDA_BF16);
     };
     fetch_small(blockIdx.x);
@@ -555,12 +555,12 @@ static_assert(intra2::TB_LO + 8192 <= 65536, "T split inside the tile area");
 static_assert(intra2::BYTES <= 113 * 1024, "two CTAs per SM");
 
 // [TT tokens][H heads][128 channels] bf16 -> boxes of 64 tokens x 1 head x 128 channels (row-major in smem).
-bool head_tile_map2(CUtensorMap* m, const void* base, int H, int TT);
+bool head_tile_map2(CUtensorMap* m, const void* base, int H, int TT, int C);
 
 cudaError_t launch_intra2(const Params& p, uint8_t* recs, cudaStream_t st) {
     CUtensorMap mq, mk, mg, mv;
-    if (!head_tile_map2(&mq, p.q, p.Hk, p.TT) || !head_tile_map2(&mk, p.k, p.Hk, p.TT) ||
-        !head_tile_map2(&mg, p.g_raw, p.H, p.TT) || !head_tile_map2(&mv, p.v, p.H, p.TT))
+    if (!head_tile_map2(&mq, p.q, p.Hk, p.TT, p.K) || !head_tile_map2(&mk, p.k, p.Hk, p.TT, p.K) ||
+        !head_tile_map2(&mg, p.g_raw, p.H, p.TT, p.K) || !head_tile_map2(&mv, p.v, p.H, p.TT, p.V))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(intra2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)intra2::BYTES);
     if (e != cudaSuccess) return e;

@@ -921,7 +921,9 @@ __global__ void __launch_bounds__(256, 1) chain_fwd_tc_kernel(Params p, const ui
     const bool store_states = flags & kChainStoreStates, transfer = flags & kChainTransfer;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int n = blockIdx.x, h = blockIdx.y, z = blockIdx.z, j0 = z * 32;
-    const int H = p.H, K = 128, V = 128;
+    // the state slice has 128 rows in TMEM and registers; heads with K = V = 64 leave rows and columns
+    // 64..127 zero (their record rows are zero) and read / write only the real ones
+    const int H = p.H, K = p.K, V = p.V;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int NS = chainlay::NSLOT;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + chainlay::BAR);   // [NS] record slots landed
@@ -1045,7 +1047,7 @@ __global__ void __launch_bounds__(256, 1) chain_fwd_tc_kernel(Params p, const ui
     } else {
     float S[32];
     {
-        const float* src = p.S0 && !transfer ? p.S0 + (((size_t)n * H + h) * K + tid) * V + j0 : nullptr;
+        const float* src = p.S0 && !transfer && tid < K ? p.S0 + (((size_t)n * H + h) * K + tid) * V + j0 : nullptr;
 #pragma unroll
         for (int j = 0; j < 32; ++j) S[j] = src ? src[j] : (transfer && tid == j0 + j ? 1.f : 0.f);
     }
@@ -1093,7 +1095,7 @@ __global__ void __launch_bounds__(256, 1) chain_fwd_tc_kernel(Params p, const ui
         uint8_t* sl = slot_ptr(i);
         const uint32_t par = i & 1;
         const uint32_t tD1 = tmem + 128 * (i & 1);
-        if (store_states) {
+        if (store_states && tid < K) {
             float* dst = p.states + (((size_t)c * H + h) * K + tid) * V + j0;
 #pragma unroll
             for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
@@ -1161,7 +1163,7 @@ __global__ void __launch_bounds__(256, 1) chain_fwd_tc_kernel(Params p, const ui
     }
     sync128();
     if (*sh_fail) ok = false;
-    if (ok && p.ST) {
+    if (ok && p.ST && tid < K) {
         float* dst = p.ST + (((size_t)n * H + h) * K + tid) * V + j0;
 #pragma unroll
         for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
@@ -1205,11 +1207,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // [TT tokens][H heads][128 channels] bf16 -> boxes of 64 tokens x 1 head x 128 channels (row-major in smem).
-static bool head_tile_map(CUtensorMap* m, const void* base, int H, int TT) {
+// [TT tokens][H heads][C channels] bf16 -> boxes of 64 tokens x 1 head x 128 channels, row-major in shared
+// memory; with C = 64 the upper 64 channels of every row, like tokens past the end, are filled with zeros.
+static bool head_tile_map(CUtensorMap* m, const void* base, int H, int TT, int C = 128) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
-    cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)TT};
-    cuuint64_t strides[2] = {128 * 2, (cuuint64_t)H * 128 * 2};
+    cuuint64_t dims[3] = {(cuuint64_t)C, (cuuint64_t)H, (cuuint64_t)TT};
+    cuuint64_t strides[2] = {(cuuint64_t)C * 2, (cuuint64_t)H * C * 2};
     cuuint32_t box[3] = {128, 1, 64};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
@@ -1217,7 +1221,7 @@ static bool head_tile_map(CUtensorMap* m, const void* base, int H, int TT) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool head_tile_map2(CUtensorMap* m, const void* base, int H, int TT) { return head_tile_map(m, base, H, TT); }
+bool head_tile_map2(CUtensorMap* m, const void* base, int H, int TT, int C) { return head_tile_map(m, base, H, TT, C); }
 
 bool tc_inputs_aligned(const Params& p) {
     auto al = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
@@ -1255,7 +1259,7 @@ cudaError_t launch_chain_fwd_tc(const Params& p, const uint8_t* recs, bool store
                                          (int)chainlay::BYTES);
     if (e != cudaSuccess) return e;
     timing_pre(st, K_CHAIN_FWD_TC);
-    chain_fwd_tc_kernel<<<dim3(p.N, p.H, 4), 256, chainlay::BYTES, st>>>(
+    chain_fwd_tc_kernel<<<dim3(p.N, p.H, p.V / 32), 256, chainlay::BYTES, st>>>(
         p, recs, (store_states ? kChainStoreStates : 0) | (transfer ? kChainTransfer : 0));
     timing_post(st);
     return cudaGetLastError();

@@ -445,6 +445,21 @@ def test_softplus_gate_bf16_d128_varlen_fwd_bwd():
         assert torch.equal(g1[n], g2[n]), n
 
 
+@pytest.mark.parametrize("case", ["rows", "packed", "grouped"])
+def test_fwd_bf16_k64_tensor_core(case):
+    """bf16 K = V = 64 heads take the tensor-core forward: the intra pass loads 128-channel tiles whose
+    upper half the TMA fills with zeros, and the chain runs the two value slices that exist."""
+    if case == "packed":
+        lens = [1, 63, 64, 65, 130, 0, 17]
+        x = make_inputs(Workload("t", B=1, T=sum(lens), H=3, K=64, V=64, varlen=True, initial_state=True, seed=71),
+                        device=DEV, lengths=lens)
+    else:
+        x = make_inputs(Workload("t", B=2, T=300, H=4, Hk=2 if case == "grouped" else 0, K=64, V=64,
+                                 initial_state=True, seed=70), device=DEV)
+    names = _launched(lambda: _check_fwd(x, "bf16"))
+    assert {"kda_intra_tc", "kda_chain_fwd_tc"} <= names and "kda_intra_simt" not in names, names
+
+
 @pytest.mark.parametrize("g_mean,Hk", [(0.0, 0), (4.0, 0), (-6.0, 0), (0.0, 1)])
 def test_softplus_gate_tensor_core_backward(g_mean, Hk):
     """The tcgen05 backward under the unbounded gate: typical, steep (g near -64 per token: exp(Gamma)
