@@ -952,17 +952,27 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) 
         *reinterpret_cast<uint4*>(base + o) = pack8_bf16(hv);
         *reinterpret_cast<uint4*>(base + o + lo_off) = pack8_bf16(lv);
     };
-    for (int i = tid; i < 64 * K / 8; i += 256) {
-        const int t = i >> 4, c8 = (i & 15) * 8;
-        float kd[8], w[8];
-        *reinterpret_cast<float4*>(kd) = *reinterpret_cast<const float4*>(rec + L.Kd + t * K + c8);
-        *reinterpret_cast<float4*>(kd + 4) = *reinterpret_cast<const float4*>(rec + L.Kd + t * K + c8 + 4);
-        *reinterpret_cast<float4*>(w) = *reinterpret_cast<const float4*>(rec + L.W + t * K + c8);
-        *reinterpret_cast<float4*>(w + 4) = *reinterpret_cast<const float4*>(rec + L.W + t * K + c8 + 4);
-        const uint32_t o = km_bf16(t, c8, 2048, 128);
-        put_split8(out, chainrec::KD + o, chainrec::KD_LO - chainrec::KD, kd, 1.f);
-        put_split8(out, chainrec::WN + o, chainrec::WN_LO - chainrec::WN, w, -1.f);
+    {
+        // every load of the four rows a thread converts is issued before the first store (the stores
+        // could alias the loads as far as the compiler knows, which would otherwise serialise them)
+        float kd[4][8], w[4][8];
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int i = tid + 256 * it, t = i >> 4, c8 = (i & 15) * 8;
+            *reinterpret_cast<float4*>(kd[it]) = *reinterpret_cast<const float4*>(rec + L.Kd + t * K + c8);
+            *reinterpret_cast<float4*>(kd[it] + 4) = *reinterpret_cast<const float4*>(rec + L.Kd + t * K + c8 + 4);
+            *reinterpret_cast<float4*>(w[it]) = *reinterpret_cast<const float4*>(rec + L.W + t * K + c8);
+            *reinterpret_cast<float4*>(w[it] + 4) = *reinterpret_cast<const float4*>(rec + L.W + t * K + c8 + 4);
+        }
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int i = tid + 256 * it, t = i >> 4, c8 = (i & 15) * 8;
+            const uint32_t o = km_bf16(t, c8, 2048, 128);
+            put_split8(out, chainrec::KD + o, chainrec::KD_LO - chainrec::KD, kd[it], 1.f);
+            put_split8(out, chainrec::WN + o, chainrec::WN_LO - chainrec::WN, w[it], -1.f);
+        }
     }
+    static_assert(64 * 128 / 8 == 4 * 256, "four rows of eight channels per thread");
     if (tid < K) reinterpret_cast<float*>(out + chainrec::GC)[tid] = rec[L.gC + tid];
     cp_async_wait_all();
     __syncthreads();
