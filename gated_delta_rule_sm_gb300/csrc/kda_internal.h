@@ -73,13 +73,20 @@ enum KernelId {
 // 11-bit significand gives every product tf32-like accuracy in one kind::f16 MMA.
 namespace tcrec {
 constexpr uint32_t WQ = 0;            // [W; Qg]  fp16, 128 rows x 128 K (c), MN-major: mn_bf16(r, c, 128, 2048)
-constexpr uint32_t U0 = 32768;        // U0       fp32, column-major [128 j][64 t]; slice z = j in [32z, 32z+32)
+constexpr uint32_t U0 = 32768;        // U0       fp32, per 32-column slice z (j in [32z, 32z+32)): [64 t][32 j] at
+                                      // U0 + z U0_SLICE, 16-byte chunks of a row swizzled (u0_off)
 constexpr uint32_t KD = 65536;        // Kd^T     fp16, 128 rows (c) x 64 K (t), K-major: km_bf16(c, t, 1024, 128)
 constexpr uint32_t AQ = 81920;        // Aqk      fp16, 64 rows (t) x 64 K (s), K-major: km_bf16(t, s, 1024, 128)
 constexpr uint32_t GC = 90112;        // exp(Gamma_last) fp32 [128]
 constexpr uint32_t BYTES = 91136;     // record stride (1 KB aligned)
 constexpr uint32_t U0_SLICE = 8192;   // one 32-column slice of U0
 constexpr uint32_t TAIL = BYTES - KD; // KD + AQ + GC (+ padding), contiguous
+// Byte offset of U0[t][j] inside its slice (j < 32 the column within the slice): row t holds 32 floats,
+// its 16-byte chunk c at position c ^ (t % 8).  The writer (thread = column j) stores a whole 128-byte row
+// per warp instruction; the reader (thread = row t) loads 16-byte chunks with no bank conflict.
+__host__ __device__ constexpr uint32_t u0_off(int t, int j) {
+    return 4u * static_cast<uint32_t>(t * 32 + ((((j >> 2) ^ (t & 7))) << 2) + (j & 3));
+}
 }  // namespace tcrec
 
 // Record of the two tcgen05 state chains of the backward, per (chunk, head), K = V = 128 (bytes).

@@ -502,8 +502,8 @@ __global__ void __launch_bounds__(256, 2)
             }
             fetch_small(item + gridDim.x);
         }
-        // record W (MN-major fp16, thread = channel) and U0 (column-major fp32, thread = value column), each
-        // the sum of its hi and lo partial
+        // record W (MN-major fp16, thread = channel) and U0 (fp32, thread = value column), each the sum of
+        // its hi and lo partial
         {
             const uint32_t lb = static_cast<uint32_t>((warp & 3) * 32) << 16;
             const uint32_t col = warp < 4 ? 0 : 128;
@@ -524,10 +524,11 @@ __global__ void __launch_bounds__(256, 2)
                         *reinterpret_cast<uint4*>(rec + REC_WQ + mn_bf16(32 * half + tb, row, 128, 2048)) =
                             pack8_f16(d + tb);
                 } else {
-                    float4* dst = reinterpret_cast<float4*>(rec + REC_U0 + row * 256 + half * 128);
+                    // U0 column `row`: one float per token, a warp writing whole 128-byte rows
+                    uint8_t* dst = rec + REC_U0 + (row >> 5) * tcrec::U0_SLICE;
 #pragma unroll
-                    for (int t4 = 0; t4 < 8; ++t4)
-                        dst[t4] = make_float4(d[4 * t4], d[4 * t4 + 1], d[4 * t4 + 2], d[4 * t4 + 3]);
+                    for (int u = 0; u < 32; ++u)
+                        *reinterpret_cast<float*>(dst + tcrec::u0_off(32 * half + u, row & 31)) = d[u];
                 }
             }
         }

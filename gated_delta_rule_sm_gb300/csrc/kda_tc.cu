@@ -685,11 +685,10 @@ __global__ void __launch_bounds__(256, 1)
                     for (int t = 0; t < 64; ++t) frec[RL.W + t * 128 + cc] = d[t];
             } else {
                 const int j = tid - 128;
-                float4* dst = reinterpret_cast<float4*>(rec + tcrec::U0 + j * 256);
+                uint8_t* dst = FWDREC ? rec + tcrec::U0 + (j >> 5) * tcrec::U0_SLICE : nullptr;
                 if (FWDREC)
 #pragma unroll
-                    for (int t4 = 0; t4 < 16; ++t4)
-                        dst[t4] = make_float4(d[4 * t4], d[4 * t4 + 1], d[4 * t4 + 2], d[4 * t4 + 3]);
+                    for (int t = 0; t < 64; ++t) *reinterpret_cast<float*>(dst + tcrec::u0_off(t, j & 31)) = d[t];
                 if (BWD)
 #pragma unroll
                     for (int t = 0; t < 64; ++t) frec[RL.U0 + t * 128 + j] = d[t];
@@ -974,16 +973,22 @@ __global__ void __launch_bounds__(256, 1) chain_fwd_tc_kernel(Params p, const ui
 #pragma unroll
         for (int w = 0; w < 3; ++w) tmem_ld16(tD1 + 32 * (w + 1), e[w]);
         tmem_ld_wait();
-        const float* u0 = reinterpret_cast<const float*>(slot_ptr(i) + chainlay::SLOT_U0);
+        const uint8_t* u0 = slot_ptr(i) + chainlay::SLOT_U0;
         uint8_t* UB = smem + chainlay::UB + (i & 1) * chainlay::UB_BYTES;
 #pragma unroll
         for (int jg = 0; jg < 16; jg += 8) {
             float u[8];
 #pragma unroll
-            for (int e8 = 0; e8 < 8; ++e8) {
-                const int j = jg + e8;
-                const float ws = d[j] + (e[0][j] + e[1][j]) + e[2][j];
-                u[e8] = (transfer ? 0.f : u0[(j0h + j) * 64 + t]) - ws;
+            for (int h4 = 0; h4 < 8; h4 += 4) {
+                // columns j0h + jg + h4 .. + 3 of row t: one 16-byte chunk of the swizzled U0 slice
+                const float4 c4 = transfer ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                           : *reinterpret_cast<const float4*>(u0 + tcrec::u0_off(t, j0h + jg + h4));
+                const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                for (int e4 = 0; e4 < 4; ++e4) {
+                    const int j = jg + h4 + e4;
+                    u[h4 + e4] = cv[e4] - (d[j] + (e[0][j] + e[1][j]) + e[2][j]);
+                }
             }
             *reinterpret_cast<uint4*>(UB + mn_bf16(j0h + jg, t, 128, 512)) = pack8_f16(u);
         }
