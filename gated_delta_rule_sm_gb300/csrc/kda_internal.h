@@ -32,6 +32,8 @@ struct RecLayout {
         r.beta = o; o += 64;
         r.rn = o; o += 128;
         r.bwd_size = (o + 63) / 64 * 64;
+        // (every field starts on a multiple of 4 floats: the tensor-core record pass writes rows of B and A
+        // with 16-byte stores)
         return r;
     }
 };

@@ -512,14 +512,21 @@ __global__ void __launch_bounds__(256, 1)
                         frec[RL.rn + t] = rq[t];
                         frec[RL.rn + 64 + t] = rk[t];
                     }
+                    // a lane writes its own row: 16-byte stores (a warp store touches 32 rows)
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) frec[RL.B + t * 64 + c0 + u] = c0 + u < t ? d[u] : 0.f;
+                    for (int u = 0; u < 32; u += 4)
+                        *reinterpret_cast<float4*>(frec + RL.B + t * 64 + c0 + u) =
+                            make_float4(c0 + u < t ? d[u] : 0.f, c0 + u + 1 < t ? d[u + 1] : 0.f,
+                                        c0 + u + 2 < t ? d[u + 2] : 0.f, c0 + u + 3 < t ? d[u + 3] : 0.f);
                 }
             } else {
                 const int t = 32 * (qw - 2) + lane;
                 if (BWD) {
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) frec[RL.A + t * 64 + c0 + u] = c0 + u <= t ? d[u] : 0.f;
+                    for (int u = 0; u < 32; u += 4)
+                        *reinterpret_cast<float4*>(frec + RL.A + t * 64 + c0 + u) =
+                            make_float4(c0 + u <= t ? d[u] : 0.f, c0 + u + 1 <= t ? d[u + 1] : 0.f,
+                                        c0 + u + 2 <= t ? d[u + 2] : 0.f, c0 + u + 3 <= t ? d[u + 3] : 0.f);
                 }
 #pragma unroll
                 for (int u = 0; u < (FWDREC ? 32 : 0); u += 8) {
