@@ -397,12 +397,18 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
                 for (int e = 0; e < 4; ++e) {
                     int r, cc;
                     frag_rc(lane, e, m0, n0 + 8 * b, r, cc);
-                    const float y = sbeta[r] * d[b][e];
-                    sdY[r * P32 + cc] = y;
-                    if (r < len) p.dv[((size_t)(tok0 + r) * H + h) * V + j0 + cc] = y;
+                    sdY[r * P32 + cc] = sbeta[r] * d[b][e];
                 }
         }
         __syncthreads();
+        {   // dv = dY for this slice, from the tile: 32 columns = one 128-byte row segment per 4 threads
+            const int r = tid >> 2, c8 = (tid & 3) * 8;
+            if (r < len) {
+                float* dst = p.dv + ((size_t)(tok0 + r) * H + h) * V + j0 + c8;
+                *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(sdY + r * P32 + c8);
+                *reinterpret_cast<float4*>(dst + 4) = *reinterpret_cast<const float4*>(sdY + r * P32 + c8 + 4);
+            }
+        }
         // slice contributions on the tensor cores: the previous slice's MMAs must be done with the
         // operand tiles before they are rewritten
         if (z > 0 && !mbar_wait(mbar, (z - 1) & 1)) mma_ok = false;

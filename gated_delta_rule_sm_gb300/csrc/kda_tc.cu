@@ -1237,9 +1237,9 @@ bool head_tile_map2(CUtensorMap* m, const void* base, int H, int TT, int C) { re
 
 bool tc_inputs_aligned(const Params& p) {
     auto al = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
-    // the forward chain stores the output and the final state 16 bytes at a time
+    // the forward chain stores the output and the final state 16 bytes at a time, the gradient kernel dv
     return al(p.q) && al(p.k) && al(p.g_raw) && al(p.v) && (p.dout == nullptr || al(p.dout)) && al(p.out) &&
-           al(p.ST);
+           al(p.ST) && al(p.dv);
 }
 
 cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, int mode, cudaStream_t st) {
