@@ -19,7 +19,8 @@
 // are independent.  Thread r owns row r of Z.  Per chunk: MMA1 (M = 64, N = JW, K = 128) into TMEM,
 // X = D1 + Y split into bf16 hi + lo (MN-major, one 16-byte store per 8 columns), MMA2 (M = 128,
 // N = JW, K = 64), then Z' = gC Z + D3 (+ P).  Record slots (A1, A2 hi/lo, gC) are double buffered
-// by bulk copies.  X (U, or dU) is also written out per chunk for the gradient kernel.
+// by bulk copies.  X (U, or dU) and the chunk's Z are also written out per chunk for the gradient
+// kernel, in x4 order (x4_off) so that every warp store covers whole 128-byte lines.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
@@ -29,7 +30,9 @@ namespace kda {
 using namespace sm100;
 
 // Where a chain finds its per-chunk inputs: slot (chainrec) of chunk c at slots + (c H + h) *
-// slot_stride bytes; Y rows at ybase + (c H + h) * ystride floats (row t, 128 columns); P likewise.
+// slot_stride bytes; the Y tile (64 rows t, 128 columns) at ybase + (c H + h) * ystride floats: in x4
+// order for the reverse chain (bwd_pre's Y), row-major for the recompute (U0 of the forward record);
+// the P tile (128 rows, x4 order) likewise.
 struct ChainSrc {
     const uint8_t* slots;
     size_t slot_stride;
@@ -156,12 +159,6 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
         const int c = chunk_of(s);
         uint8_t* sl = slot_ptr(s);
         const uint32_t par = s & 1;
-        {   // reverse: gradient w.r.t. the state leaving chunk c; forward: the state entering chunk c
-            float* dst = (REV ? p.dstates : p.states) + (((size_t)c * H + h) * K + tid) * V + j0;
-#pragma unroll
-            for (int j = 0; j < JW; j += 4)
-                *reinterpret_cast<float4*>(dst + j) = make_float4(z[j], z[j + 1], z[j + 2], z[j + 3]);
-        }
         fail_wait(&full[s & 1], (s >> 1) & 1);
         tc_fence_after();
         if (tid == 0) {   // D1 = A1 Z  (M = 64, N = JW, K = 128)
@@ -179,20 +176,29 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
                                  : "memory");
             }
         }
+        {   // reverse: gradient w.r.t. the state leaving chunk c; forward: the state entering chunk c
+            // (x4 order: the warp's 32 rows make 512 contiguous bytes per 16-byte store)
+            float* dst = (REV ? p.dstates : p.states) + ((size_t)c * H + h) * K * V;
+#pragma unroll
+            for (int j = 0; j < JW; j += 4)
+                *reinterpret_cast<float4*>(dst + x4_off(tid, j0 + j, K)) = make_float4(z[j], z[j + 1], z[j + 2], z[j + 3]);
+        }
         // X rows t = 16 warp + lane (lanes 0..15 of each warp carry the M = 64 result).  The Y row is
         // read from global memory 32 columns ahead of its use: the first block before MMA1 is waited
         // for, each next block while the current one is combined.
         const int t = 16 * warp + (lane & 15);
-        const float* yrow = y_ptr(s) + t * V + j0;
-        auto load32 = [](const float* src, float* dst) {
+        // 32 columns from col of row `row` of a tile with `rows` rows, x4-ordered or row-major
+        auto load32 = [](const float* tile, int row, int col, int rows, bool x4, float* dst) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
-                const float4 v = *reinterpret_cast<const float4*>(src + j);
+                const float4 v = *reinterpret_cast<const float4*>(tile + (x4 ? x4_off(row, col + j, rows)
+                                                                              : (size_t)row * V + col + j));
                 dst[j] = v.x; dst[j + 1] = v.y; dst[j + 2] = v.z; dst[j + 3] = v.w;
             }
         };
+        const float* ytile = y_ptr(s);
         float ynext[32];
-        load32(yrow, ynext);
+        load32(ytile, t, j0, 64, REV, ynext);
         fail_wait(bar1, par);
         tc_fence_after();
         {
@@ -204,14 +210,16 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
                 float y[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) y[j] = ynext[j];
-                if (jb + 32 < JW) load32(yrow + jb + 32, ynext);
+                if (jb + 32 < JW) load32(ytile, t, j0 + jb + 32, 64, REV, ynext);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) d[j] += y[j];
-                if (lane < 16) {   // X row t (U or dU) for the gradient kernel
-                    float* xo = (REV ? p.chunk_du : p.chunk_u) + (((size_t)c * H + h) * 64 + t) * V + j0 + jb;
+                if (lane < 16) {   // X row t (U or dU) for the gradient kernel, x4 order
+                    float* xo = (REV ? p.chunk_du : p.chunk_u) + ((size_t)c * H + h) * 64 * V;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(xo + j) = make_float4(d[j], d[j + 1], d[j + 2], d[j + 3]);
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(xo + x4_off(t, j0 + jb + j, 64)) =
+                            make_float4(d[j], d[j + 1], d[j + 2], d[j + 3]);
                 }
                 if (lane < 16)
 #pragma unroll
@@ -235,9 +243,9 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
             mma_commit(bar2);
         }
         // the P row likewise, one 32-column block ahead (reverse chain only)
-        const float* prow = REV ? p_ptr(s) + tid * V + j0 : nullptr;
+        const float* ptile = REV ? p_ptr(s) : nullptr;
         float pnext[32];
-        if (REV) load32(prow, pnext);
+        if (REV) load32(ptile, tid, j0, K, true, pnext);
         fail_wait(bar2, par);
         tc_fence_after();
         {
@@ -250,7 +258,7 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
                 float pv[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) pv[j] = REV ? pnext[j] : 0.f;
-                if (REV && jb + 32 < JW) load32(prow + jb + 32, pnext);
+                if (REV && jb + 32 < JW) load32(ptile, tid, j0 + jb + 32, K, true, pnext);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) z[jb + j] = gc * z[jb + j] + d[j] + pv[j];

@@ -248,6 +248,7 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     const int len = min(kChunk, seg_end(p, n) - tok0);
     const RecLayout L = RecLayout::make(K, V);
     const float* rec = p.rec + ((size_t)c * H + h) * p.rec_stride;
+    // the chains' per-chunk tiles, each in x4 order
     const float* S0g = p.states + ((size_t)c * H + h) * K * V;
     const float* dSg = p.dstates + ((size_t)c * H + h) * K * V;
     const float* Ug = p.chunk_u + ((size_t)c * H + h) * 64 * V;     // U = U0 - W S0 (recompute chain)
@@ -334,34 +335,50 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     for (int z = 0; z < 4; ++z) {
         const int j0 = 32 * z;
         __syncthreads();   // previous slice's readers are done
-        for (int i = tid; i < K * 8; i += 256) {
-            const int cc = i >> 3, j4 = (i & 7) * 4;
-            cp_async16(sS0 + cc * P32 + j4, S0g + cc * V + j0 + j4);
-            cp_async16(sdS + cc * P32 + j4, dSg + cc * V + j0 + j4);
-        }
-        for (int i = tid; i < 64 * 8; i += 256) {
-            const int t = i >> 3, j4 = (i & 7) * 4;
-            cp_async16(sU + t * P32 + j4, Ug + t * V + j0 + j4);
-            cp_async16(sdU + t * P32 + j4, dUg + t * V + j0 + j4);
-        }
-        {   // dO and v slices (bf16, 8 per 16-byte load): one row-quarter per thread
+        {   // x4-ordered tiles: consecutive threads read consecutive rows' 16-byte chunks (all loads
+            // issued before the first shared store)
+            float4 a[4], b[4], u[2], du[2];
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int i = tid + 256 * it, cc = i & (K - 1), j4 = (i / K) * 4;
+                a[it] = *reinterpret_cast<const float4*>(S0g + x4_off(cc, j0 + j4, K));
+                b[it] = *reinterpret_cast<const float4*>(dSg + x4_off(cc, j0 + j4, K));
+            }
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+                const int i = tid + 256 * it, r = i & 63, j4 = (i >> 6) * 4;
+                u[it] = *reinterpret_cast<const float4*>(Ug + x4_off(r, j0 + j4, 64));
+                du[it] = *reinterpret_cast<const float4*>(dUg + x4_off(r, j0 + j4, 64));
+            }
+            // dO and v slices (bf16, 8 per 16-byte load): one row-quarter per thread
             const int t = tid >> 2, j8 = (tid & 3) * 8;
-            float fo[8], fv[8];
+            uint4 ro = make_uint4(0u, 0u, 0u, 0u), rv = ro;
             if (t < len) {
                 const size_t gi = ((size_t)(tok0 + t) * H + h) * V + j0 + j8;
-                bf16x8_to_f32(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + gi), fo);
-                bf16x8_to_f32(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.v) + gi), fv);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) fo[e] = fv[e] = 0.f;
+                ro = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + gi);
+                rv = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.v) + gi);
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                sdO[t * P32 + j8 + e] = fo[e];
-                sVt[t * P32 + j8 + e] = fv[e];
+            for (int it = 0; it < 4; ++it) {
+                const int i = tid + 256 * it, cc = i & (K - 1), j4 = (i / K) * 4;
+                *reinterpret_cast<float4*>(sS0 + cc * P32 + j4) = a[it];
+                *reinterpret_cast<float4*>(sdS + cc * P32 + j4) = b[it];
             }
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+                const int i = tid + 256 * it, r = i & 63, j4 = (i >> 6) * 4;
+                *reinterpret_cast<float4*>(sU + r * P32 + j4) = u[it];
+                *reinterpret_cast<float4*>(sdU + r * P32 + j4) = du[it];
+            }
+            float fo[8], fv[8];
+            bf16x8_to_f32(ro, fo);
+            bf16x8_to_f32(rv, fv);
+            *reinterpret_cast<float4*>(sdO + t * P32 + j8) = make_float4(fo[0], fo[1], fo[2], fo[3]);
+            *reinterpret_cast<float4*>(sdO + t * P32 + j8 + 4) = make_float4(fo[4], fo[5], fo[6], fo[7]);
+            *reinterpret_cast<float4*>(sVt + t * P32 + j8) = make_float4(fv[0], fv[1], fv[2], fv[3]);
+            *reinterpret_cast<float4*>(sVt + t * P32 + j8 + 4) = make_float4(fv[4], fv[5], fv[6], fv[7]);
         }
-        cp_async_wait_all();
+        if (z == 0) cp_async_wait_all();   // the record tiles requested before the loop
         __syncthreads();
         // Vt = v - Kg S0 (64 x 32): warp w takes rows 16 (w % 4), columns 16 (w / 4) .. + 16
         {
@@ -997,8 +1014,8 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) 
         for (int b = 0; b < 8; ++b) {
             int r, cc;
             frag_rc(lane, 0, m0, n0 + 8 * b, r, cc);
-            *reinterpret_cast<float2*>(Yg + r * V + cc) = make_float2(scale * d[b][0], scale * d[b][1]);
-            *reinterpret_cast<float2*>(Yg + (r + 8) * V + cc) = make_float2(scale * d[b][2], scale * d[b][3]);
+            *reinterpret_cast<float2*>(Yg + x4_off(r, cc, 64)) = make_float2(scale * d[b][0], scale * d[b][1]);
+            *reinterpret_cast<float2*>(Yg + x4_off(r + 8, cc, 64)) = make_float2(scale * d[b][2], scale * d[b][3]);
         }
     }
     // P = scale Qg^T dO (128 x 128): warp w owns rows 16 w, all columns in two strips of 64
@@ -1017,8 +1034,8 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) 
             for (int b = 0; b < 8; ++b) {
                 int r, cc;
                 frag_rc(lane, 0, m0, 64 * half + 8 * b, r, cc);
-                *reinterpret_cast<float2*>(Pg + r * V + cc) = make_float2(scale * a1[b][0], scale * a1[b][1]);
-                *reinterpret_cast<float2*>(Pg + (r + 8) * V + cc) = make_float2(scale * a1[b][2], scale * a1[b][3]);
+                *reinterpret_cast<float2*>(Pg + x4_off(r, cc, K)) = make_float2(scale * a1[b][0], scale * a1[b][1]);
+                *reinterpret_cast<float2*>(Pg + x4_off(r + 8, cc, K)) = make_float2(scale * a1[b][2], scale * a1[b][3]);
             }
         }
     }

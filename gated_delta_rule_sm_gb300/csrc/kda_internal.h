@@ -113,10 +113,20 @@ constexpr uint32_t SLOT = 66048;
 }  // namespace chainrec
 
 namespace bwrec {
-constexpr uint32_t Y = chainrec::SLOT;          // fp32 [64 t][128 j]: scale Aqk^T dO
-constexpr uint32_t P = Y + 32768;               // fp32 [128 c][128 j]: scale Qg^T dO
+constexpr uint32_t Y = chainrec::SLOT;          // fp32 [64 t][128 j] in x4 order: scale Aqk^T dO
+constexpr uint32_t P = Y + 32768;               // fp32 [128 c][128 j] in x4 order: scale Qg^T dO
 constexpr uint32_t BYTES = P + 65536;           // record stride (256-byte multiple)
 }  // namespace bwrec
+
+// "x4 order" of an fp32 tile of `rows` rows and 128 value columns: element (row, j) at
+// x4_off(row, j, rows) = (j / 4, row, j % 4) row-major.  Four adjacent columns of one row form a
+// 16-byte chunk and the chunks of consecutive rows are adjacent, so a warp whose lanes own
+// consecutive rows moves whole 128-byte lines with 16-byte accesses.  The tiles passed between the
+// backward's tensor-core kernels use it: Y and P above, and the per-chunk states, state gradients,
+// U and dU that the two chains write for the gradient kernel.
+__host__ __device__ constexpr size_t x4_off(int row, int j, int rows) {
+    return ((size_t)(j >> 2) * rows + row) * 4 + (j & 3);
+}
 
 // Launch bracketing for kda_timing_*: no-ops unless timing is active.
 void timing_pre(cudaStream_t st, int kernel_id);
