@@ -332,52 +332,61 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     float dgc = 0.f;   // thread tid < 128: sum_j dS_end[c][j] S0[c][j] for channel c = tid
     const int wm0 = 16 * (warp >> 1);
 
+    // Slice z's tiles pass through registers: x4-ordered tiles with consecutive threads on
+    // consecutive rows' 16-byte chunks, dO and v one row-quarter per thread.  The next slice's loads
+    // are issued as soon as the current slice is in shared memory, so they fly during its products.
+    float4 ra[4], rb[4], ru[2], rdu[2];
+    uint4 ro, rv;
+    const int tq = tid >> 2, j8q = (tid & 3) * 8;   // dO / v: row and first column of this thread
+    auto fetch_slice = [&](int z) {
+        const int j0 = 32 * z;
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int i = tid + 256 * it, cc = i & (K - 1), j4 = (i / K) * 4;
+            ra[it] = *reinterpret_cast<const float4*>(S0g + x4_off(cc, j0 + j4, K));
+            rb[it] = *reinterpret_cast<const float4*>(dSg + x4_off(cc, j0 + j4, K));
+        }
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int i = tid + 256 * it, r = i & 63, j4 = (i >> 6) * 4;
+            ru[it] = *reinterpret_cast<const float4*>(Ug + x4_off(r, j0 + j4, 64));
+            rdu[it] = *reinterpret_cast<const float4*>(dUg + x4_off(r, j0 + j4, 64));
+        }
+        ro = rv = make_uint4(0u, 0u, 0u, 0u);
+        if (tq < len) {
+            const size_t gi = ((size_t)(tok0 + tq) * H + h) * V + j0 + j8q;
+            ro = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + gi);
+            rv = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.v) + gi);
+        }
+    };
+    auto stage = [&]() {
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int i = tid + 256 * it, cc = i & (K - 1), j4 = (i / K) * 4;
+            *reinterpret_cast<float4*>(sS0 + cc * P32 + j4) = ra[it];
+            *reinterpret_cast<float4*>(sdS + cc * P32 + j4) = rb[it];
+        }
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int i = tid + 256 * it, r = i & 63, j4 = (i >> 6) * 4;
+            *reinterpret_cast<float4*>(sU + r * P32 + j4) = ru[it];
+            *reinterpret_cast<float4*>(sdU + r * P32 + j4) = rdu[it];
+        }
+        float fo[8], fv[8];
+        bf16x8_to_f32(ro, fo);
+        bf16x8_to_f32(rv, fv);
+        *reinterpret_cast<float4*>(sdO + tq * P32 + j8q) = make_float4(fo[0], fo[1], fo[2], fo[3]);
+        *reinterpret_cast<float4*>(sdO + tq * P32 + j8q + 4) = make_float4(fo[4], fo[5], fo[6], fo[7]);
+        *reinterpret_cast<float4*>(sVt + tq * P32 + j8q) = make_float4(fv[0], fv[1], fv[2], fv[3]);
+        *reinterpret_cast<float4*>(sVt + tq * P32 + j8q + 4) = make_float4(fv[4], fv[5], fv[6], fv[7]);
+    };
+    fetch_slice(0);
+
     for (int z = 0; z < 4; ++z) {
         const int j0 = 32 * z;
         __syncthreads();   // previous slice's readers are done
-        {   // x4-ordered tiles: consecutive threads read consecutive rows' 16-byte chunks (all loads
-            // issued before the first shared store)
-            float4 a[4], b[4], u[2], du[2];
-#pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int i = tid + 256 * it, cc = i & (K - 1), j4 = (i / K) * 4;
-                a[it] = *reinterpret_cast<const float4*>(S0g + x4_off(cc, j0 + j4, K));
-                b[it] = *reinterpret_cast<const float4*>(dSg + x4_off(cc, j0 + j4, K));
-            }
-#pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int i = tid + 256 * it, r = i & 63, j4 = (i >> 6) * 4;
-                u[it] = *reinterpret_cast<const float4*>(Ug + x4_off(r, j0 + j4, 64));
-                du[it] = *reinterpret_cast<const float4*>(dUg + x4_off(r, j0 + j4, 64));
-            }
-            // dO and v slices (bf16, 8 per 16-byte load): one row-quarter per thread
-            const int t = tid >> 2, j8 = (tid & 3) * 8;
-            uint4 ro = make_uint4(0u, 0u, 0u, 0u), rv = ro;
-            if (t < len) {
-                const size_t gi = ((size_t)(tok0 + t) * H + h) * V + j0 + j8;
-                ro = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + gi);
-                rv = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.v) + gi);
-            }
-#pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int i = tid + 256 * it, cc = i & (K - 1), j4 = (i / K) * 4;
-                *reinterpret_cast<float4*>(sS0 + cc * P32 + j4) = a[it];
-                *reinterpret_cast<float4*>(sdS + cc * P32 + j4) = b[it];
-            }
-#pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int i = tid + 256 * it, r = i & 63, j4 = (i >> 6) * 4;
-                *reinterpret_cast<float4*>(sU + r * P32 + j4) = u[it];
-                *reinterpret_cast<float4*>(sdU + r * P32 + j4) = du[it];
-            }
-            float fo[8], fv[8];
-            bf16x8_to_f32(ro, fo);
-            bf16x8_to_f32(rv, fv);
-            *reinterpret_cast<float4*>(sdO + t * P32 + j8) = make_float4(fo[0], fo[1], fo[2], fo[3]);
-            *reinterpret_cast<float4*>(sdO + t * P32 + j8 + 4) = make_float4(fo[4], fo[5], fo[6], fo[7]);
-            *reinterpret_cast<float4*>(sVt + t * P32 + j8) = make_float4(fv[0], fv[1], fv[2], fv[3]);
-            *reinterpret_cast<float4*>(sVt + t * P32 + j8 + 4) = make_float4(fv[4], fv[5], fv[6], fv[7]);
-        }
+        stage();
+        if (z + 1 < 4) fetch_slice(z + 1);
         if (z == 0) cp_async_wait_all();   // the record tiles requested before the loop
         __syncthreads();
         // Vt = v - Kg S0 (64 x 32): warp w takes rows 16 (w % 4), columns 16 (w / 4) .. + 16
