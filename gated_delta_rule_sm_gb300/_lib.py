@@ -25,7 +25,8 @@ EXPORTS = ("kda_fwd_workspace_size", "kda_bwd_workspace_size", "kda_fwd", "kda_f
            "kda_status_string", "kda_device_status", "kda_version", "kda_timing_begin", "kda_timing_end",
            "kda_kernel_name", "kda_fwd_noalloc", "kda_saved_size", "kda_fwd_save", "kda_bwd_saved",
            "kda_short_conv_fwd", "kda_short_conv_bwd_workspace_size", "kda_short_conv_bwd",
-           "kda_fwd_segmented_workspace_size", "kda_fwd_segmented", "kda_selftest_wait_timeout",
+           "kda_fwd_segmented_workspace_size", "kda_fwd_segmented", "kda_bwd_segmented_workspace_size",
+           "kda_bwd_segmented", "kda_selftest_wait_timeout",
            "kda_gated_norm_fwd", "kda_gated_norm_bwd_workspace_size", "kda_gated_norm_bwd")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 GATES = {"lower_bounded": 0, "softplus": 1}   # kda_gate
@@ -73,8 +74,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.kda_fwd_segmented_workspace_size.restype = ctypes.c_size_t
         lib.kda_fwd_segmented_workspace_size.argtypes = [dims_p, ctypes.c_int, ctypes.c_int]
         lib.kda_fwd_segmented.restype = ctypes.c_int
+        # ... chunk_size, segments, cu_seqlens, cu_seqlens_host, initial_state, out, final_state, ws, bytes, stream
         lib.kda_fwd_segmented.argtypes = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int,
-                                                                  ctypes.c_int] + [_vp] * 3 + [_vp, ctypes.c_size_t, _vp]
+                                                                  ctypes.c_int] + [_vp] * 5 + [_vp, ctypes.c_size_t, _vp]
         gn = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, ctypes.c_float]
         lib.kda_gated_norm_fwd.restype = ctypes.c_int
         lib.kda_gated_norm_fwd.argtypes = gn + [_vp, _vp]
@@ -90,6 +92,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.kda_bwd.restype = ctypes.c_int
         lib.kda_bwd.argtypes = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int] + \
             [_vp] * 3 + [_vp] * 2 + [_vp] * 8 + [_vp, ctypes.c_size_t, _vp]
+        lib.kda_bwd_segmented_workspace_size.restype = ctypes.c_size_t
+        lib.kda_bwd_segmented_workspace_size.argtypes = [dims_p, ctypes.c_int, ctypes.c_int]
+        lib.kda_bwd_segmented.restype = ctypes.c_int
+        lib.kda_bwd_segmented.argtypes = [dims_p] + [_vp] * 7 + [ctypes.c_float, ctypes.c_float, ctypes.c_int,
+                                                                  ctypes.c_int] + [_vp] * 3 + [_vp] * 2 + [_vp] * 8 + \
+            [_vp, ctypes.c_size_t, _vp]
         lib.kda_saved_size.restype = ctypes.c_size_t
         lib.kda_saved_size.argtypes = [dims_p, ctypes.c_int]
         lib.kda_fwd_save.restype = ctypes.c_int
@@ -245,8 +253,8 @@ def forward(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale: float, lower_bou
     "softplus" (g = -exp(a_log) * softplus(g_raw + dt_bias), unbounded below).
     ``saved``: a device byte buffer of ``saved_size(...)`` bytes; the forward then runs
     ``kda_fwd_save`` and keeps the per-chunk quantities there for ``backward(..., saved=...)``.
-    ``segments`` > 0: run ``kda_fwd_segmented``, the chain cut into that many pieces per row (rows of
-    T tokens only; for long rows with few rows x heads).
+    ``segments`` > 0: run ``kda_fwd_segmented``, the chain cut into pieces of about 1 / segments of a
+    row (of the longest possible document with ``cu_seqlens``); for long rows with few rows x heads.
     ``cu_seqlens_host``: optional host copy of ``cu_seqlens`` (CPU tensor or sequence); the library then
     checks the offsets before it launches anything and a bad one raises ``KdaError`` (invalid argument).
     """
@@ -264,20 +272,21 @@ def forward(q, k, v, g_raw, beta_raw, a_log, dt_bias, *, scale: float, lower_bou
     if not output_final_state:
         final_state = None
     st = stream if stream is not None else torch.cuda.current_stream(q.device)
+    cu_h = host_offsets(cu_seqlens_host, N + 1 if cu_seqlens is not None else None)
     if segments:
-        if cu_seqlens is not None or saved is not None or simt:
-            raise ValueError("segments= takes rows of T tokens, without saved= or simt=")
+        if saved is not None or simt:
+            raise ValueError("segments= runs without saved= or simt=")
         ws_bytes = lib.kda_fwd_segmented_workspace_size(ctypes.byref(dims), int(chunk_size), int(segments))
         ws = workspace_cache.get(q.device, "fwd", ws_bytes)
         code = lib.kda_fwd_segmented(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw),
                                      _ptr(a_log), _ptr(dt_bias), float(scale), float(lower_bound), int(chunk_size),
-                                     int(segments), _ptr(initial_state), _ptr(out), _ptr(final_state), _ptr(ws),
-                                     ctypes.c_size_t(ws.numel()), ctypes.c_void_p(st.cuda_stream))
+                                     int(segments), _ptr(cu_seqlens), cu_h, _ptr(initial_state), _ptr(out),
+                                     _ptr(final_state), _ptr(ws), ctypes.c_size_t(ws.numel()),
+                                     ctypes.c_void_p(st.cuda_stream))
         _check(code, "kda_fwd_segmented")
         return out, final_state
     ws_bytes = lib.kda_fwd_workspace_size(ctypes.byref(dims), chunk_size)
     ws = workspace_cache.get(q.device, "fwd", ws_bytes)
-    cu_h = host_offsets(cu_seqlens_host, N + 1 if cu_seqlens is not None else None)
     head = (ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw), _ptr(a_log),
             _ptr(dt_bias), float(scale), float(lower_bound), int(chunk_size), _ptr(cu_seqlens), cu_h,
             _ptr(initial_state), _ptr(out), _ptr(final_state))
@@ -305,11 +314,14 @@ def backward(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale: float, lo
              gate: str = "lower_bounded", chunk_size: int = 64, cu_seqlens=None, cu_seqlens_host=None,
              initial_state=None, dfinal_state=None,
              want_dinitial_state: bool = True, grads: Optional[dict] = None,
-             saved: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> dict:
+             saved: Optional[torch.Tensor] = None, segments: int = 0,
+             stream: Optional[torch.cuda.Stream] = None) -> dict:
     """KDA backward through ``kda_bwd``.  Returns a dict of fp32 gradients.
 
     ``saved``: the buffer a ``forward(..., saved=...)`` on the same inputs filled; the backward then
     runs ``kda_bwd_saved`` and skips rebuilding the per-chunk quantities.
+    ``segments`` > 0: run ``kda_bwd_segmented``, both state chains cut into the pieces of
+    ``forward(..., segments=...)``.
     """
     lib = load()
     _contig(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, cu_seqlens, initial_state, dfinal_state)
@@ -326,7 +338,10 @@ def backward(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale: float, lo
                      dbeta_raw=torch.empty((B, T, H), **f32), da_log=torch.empty((H,), **f32),
                      ddt_bias=torch.empty((H * K,), **f32),
                      dinitial_state=torch.empty((N, H, K, V), **f32) if want_dinitial_state else None)
-    ws_bytes = lib.kda_bwd_workspace_size(ctypes.byref(dims), chunk_size)
+    if segments and saved is not None:
+        raise ValueError("segments= runs without saved=")
+    ws_bytes = (lib.kda_bwd_segmented_workspace_size(ctypes.byref(dims), int(chunk_size), int(segments))
+                if segments else lib.kda_bwd_workspace_size(ctypes.byref(dims), chunk_size))
     ws = workspace_cache.get(dev, "bwd", ws_bytes)
     st = stream if stream is not None else torch.cuda.current_stream(dev)
     cu_h = host_offsets(cu_seqlens_host, N + 1 if cu_seqlens is not None else None)
@@ -339,6 +354,11 @@ def backward(q, k, v, g_raw, beta_raw, a_log, dt_bias, dout, *, scale: float, lo
     if saved is not None:
         code = lib.kda_bwd_saved(*head, _ptr(saved), ctypes.c_size_t(saved.numel() * saved.element_size()), *tail)
         _check(code, "kda_bwd_saved")
+        return grads
+    if segments:
+        # kda_bwd_segmented takes `segments` right after chunk_size
+        code = lib.kda_bwd_segmented(*head[:11], int(segments), *head[11:], *tail)
+        _check(code, "kda_bwd_segmented")
         return grads
     code = lib.kda_bwd(*head, *tail)
     _check(code, "kda_bwd")

@@ -294,32 +294,63 @@ static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cu
     return KDA_OK;
 }
 
-// Segment-parallel forward: each of the B rows cut into P pieces of L tokens (L a multiple of 64).
+// Segment-parallel schedule: every row (a document of cu_seqlens, or one of B rows of T tokens) cut
+// into pieces of at most L tokens, L a multiple of 64 so that the pieces' chunks are the rows'.  The
+// pieces run as packed segments; Pmax bounds their number (unused ones are empty).
 struct SegPlan {
-    Shape ps;            // the pieces as packed segments
-    TcPlan tc;           // chunk table, records (and diagonal blocks) of the piece problem
-    size_t off_cu, off_sloc, off_m, off_sstart, total;
-    int L, P;
+    Shape ps;          // the pieces as packed segments
+    int L, Pmax, rows;
+    size_t off_piece_cu, off_row_piece, off_sloc, off_m, off_sstart;
 };
 
-static SegPlan plan_seg(const Shape& s, int segments) {
+static SegPlan plan_seg_shape(const Shape& s, int segments) {
     SegPlan w;
-    const int nch = (s.T + kChunk - 1) / kChunk;
+    w.rows = s.N;
+    const int span = s.varlen ? s.TT : s.T;   // the longest row can be
+    const int nch = (span + kChunk - 1) / kChunk;
     w.L = (nch + segments - 1) / segments * kChunk;
-    w.P = (s.T + w.L - 1) / w.L;
+    // each row gives ceil(len / L) <= len / L + 1 pieces
+    w.Pmax = s.varlen ? s.N + (s.TT + w.L - 1) / w.L : s.B * ((s.T + w.L - 1) / w.L);
     w.ps = s;
     w.ps.varlen = true;
-    w.ps.N = s.B * w.P;
-    w.ps.NCmax = (int)(((long long)s.TT + kChunk - 1) / kChunk + w.ps.N);
-    w.tc = plan_tc_fwd(w.ps);
-    const size_t st = sizeof(float) * (size_t)w.ps.N * s.H * s.K * s.V;
-    size_t o = w.tc.total;
-    w.off_cu = o; o = align_up(o + sizeof(int32_t) * (size_t)(w.ps.N + 1));
-    w.off_sloc = o; o = align_up(o + st);     // end state of each piece from zero
-    w.off_m = o; o = align_up(o + st);        // transfer matrix of each piece (K x K, K == V)
-    w.off_sstart = o; o = align_up(o + st);   // true entering state of each piece
-    w.total = o;
+    w.ps.N = w.Pmax;
+    w.ps.NCmax = (int)(((long long)s.TT + kChunk - 1) / kChunk + w.Pmax);
     return w;
+}
+
+// The piece tables and the three fp32 states per piece and head (end state from zero, transfer
+// matrix, true starting state), after `base` bytes of the piece problem's own workspace.
+static size_t plan_seg_tail(SegPlan& w, size_t base) {
+    const size_t st = sizeof(float) * (size_t)w.Pmax * w.ps.H * w.ps.K * w.ps.V;
+    size_t o = base;
+    w.off_piece_cu = o; o = align_up(o + sizeof(int32_t) * (size_t)(w.Pmax + 1));
+    w.off_row_piece = o; o = align_up(o + sizeof(int32_t) * (size_t)(w.rows + 1));
+    w.off_sloc = o; o = align_up(o + st);
+    w.off_m = o; o = align_up(o + st);
+    w.off_sstart = o; o = align_up(o + st);
+    return o;
+}
+
+struct SegFwdPlan {
+    SegPlan seg;
+    TcPlan tc;
+    size_t total;
+};
+static SegFwdPlan plan_seg_fwd(const Shape& s, int segments) {
+    SegFwdPlan w;
+    w.seg = plan_seg_shape(s, segments);
+    w.tc = plan_tc_fwd(w.seg.ps);
+    w.total = plan_seg_tail(w.seg, w.tc.total);
+    return w;
+}
+
+// Params of the piece problem: the pieces as packed segments of the same chunks.
+static Params piece_params(const Params& p, const SegPlan& w, char* ws) {
+    Params pp = p;
+    pp.N = w.ps.N;
+    pp.NCmax = w.ps.NCmax;
+    pp.cu = reinterpret_cast<int32_t*>(ws + w.off_piece_cu);
+    return pp;
 }
 
 // Tensor-core backward.  saved == NULL: the intra kernel rebuilds the fp32 backward record in the
@@ -463,44 +494,52 @@ kda_status kda_bwd(const kda_dims* dims, const void* q, const void* k, const voi
     return KDA_OK;
 }
 
+// Dims as the entry points read them: packed documents when num_seqs is given with B == 1 (this
+// bound also covers B = 1 rows), rows otherwise.
+static bool seg_shape(const kda_dims* dims, int chunk_size, int segments, Shape* s) {
+    if (!dims || segments < 1) return false;
+    if (check_dims(dims, chunk_size, dims->num_seqs > 0 && dims->B == 1, s) != KDA_OK &&
+        check_dims(dims, chunk_size, false, s) != KDA_OK)
+        return false;
+    return tc_eligible(*s);
+}
+
 size_t kda_fwd_segmented_workspace_size(const kda_dims* dims, int chunk_size, int segments) {
     Shape s;
-    if (!dims || segments < 1 || check_dims(dims, chunk_size, false, &s) != KDA_OK || !tc_eligible(s)) return 0;
-    return plan_seg(s, segments).total;
+    return seg_shape(dims, chunk_size, segments, &s) ? plan_seg_fwd(s, segments).total : 0;
 }
 
 kda_status kda_fwd_segmented(const kda_dims* dims, const void* q, const void* k, const void* v, const void* g_raw,
                              const void* beta_raw, const float* a_log, const float* dt_bias, float scale,
-                             float lower_bound, int chunk_size, int segments, const float* initial_state, void* out,
+                             float lower_bound, int chunk_size, int segments, const int32_t* cu_seqlens,
+                             const int32_t* cu_seqlens_host, const float* initial_state, void* out,
                              float* final_state, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     Shape s;
-    kda_status st = common_checks(dims, chunk_size, nullptr, nullptr, q, k, v, g_raw, beta_raw, a_log, dt_bias,
-                                  scale, lower_bound, &s);
+    kda_status st = common_checks(dims, chunk_size, cu_seqlens, cu_seqlens_host, q, k, v, g_raw, beta_raw, a_log,
+                                  dt_bias, scale, lower_bound, &s);
     if (st != KDA_OK) return st;
     if (!out || segments < 1) return KDA_ERR_INVALID_ARG;
-    Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, nullptr, initial_state);
+    Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
+                           initial_state);
     p.out = out;
     p.ST = final_state;
     if (!tc_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
-    const SegPlan w = plan_seg(s, segments);
+    const SegFwdPlan w = plan_seg_fwd(s, segments);
     st = check_ws(workspace, workspace_bytes, w.total);
     if (st != KDA_OK) return st;
     st = status_ptr(&p.status);
     if (st != KDA_OK) return st;
     char* b = static_cast<char*>(workspace);
-    // the pieces as packed segments: same chunks as the rows, since pieces start on 64-token boundaries
-    Params pp = p;
-    pp.N = w.ps.N;
-    pp.NCmax = w.ps.NCmax;
-    int32_t* piece_cu = reinterpret_cast<int32_t*>(b + w.off_cu);
-    pp.cu = piece_cu;
+    Params pp = piece_params(p, w.seg, b);
     pp.chunk_off = reinterpret_cast<int32_t*>(b + w.tc.off_chunk);
     if (s.gate == KDA_GATE_SOFTPLUS) pp.diag = reinterpret_cast<float*>(b + w.tc.off_diag);
     uint8_t* recs = reinterpret_cast<uint8_t*>(b + w.tc.off_rec);
-    float* sloc = reinterpret_cast<float*>(b + w.off_sloc);
-    float* M = reinterpret_cast<float*>(b + w.off_m);
-    float* sstart = reinterpret_cast<float*>(b + w.off_sstart);
-    KDA_TRY_CUDA(launch_piece_cu(piece_cu, s.B, s.T, w.L, w.P, stream));
+    int32_t* row_piece = reinterpret_cast<int32_t*>(b + w.seg.off_row_piece);
+    float* sloc = reinterpret_cast<float*>(b + w.seg.off_sloc);
+    float* M = reinterpret_cast<float*>(b + w.seg.off_m);
+    float* sstart = reinterpret_cast<float*>(b + w.seg.off_sstart);
+    KDA_TRY_CUDA(launch_piece_plan(cu_seqlens, s.N, s.T, s.TT, w.seg.L, w.seg.Pmax, const_cast<int32_t*>(pp.cu),
+                                   row_piece, p.status, stream));
     KDA_TRY_CUDA(launch_plan(pp, stream));
     if (pp.diag) KDA_TRY_CUDA(launch_diag_tc(pp, stream));
     KDA_TRY_CUDA(launch_intra_tc(pp, recs, 0, stream));
@@ -511,12 +550,99 @@ kda_status kda_fwd_segmented(const kda_dims* dims, const void* q, const void* k,
     KDA_TRY_CUDA(launch_chain_fwd_tc(pa, recs, false, stream));
     pa.ST = M;        // transfer matrices: from the identity with U0 taken as zero
     KDA_TRY_CUDA(launch_chain_fwd_tc(pa, recs, false, stream, true));
-    KDA_TRY_CUDA(launch_seg_combine(initial_state, final_state, sloc, M, sstart, s.B, s.H, w.P, stream));
+    KDA_TRY_CUDA(launch_seg_combine(initial_state, final_state, sloc, M, sstart, s.N, s.H, row_piece, false, stream));
     Params pc = pp;   // the output, from the true entering states
     pc.S0 = sstart;
     pc.out = out;
     pc.ST = nullptr;
     KDA_TRY_CUDA(launch_chain_fwd_tc(pc, recs, false, stream));
+    return KDA_OK;
+}
+
+struct SegBwdPlan {
+    SegPlan seg;
+    TcBwdPlan tc;
+    size_t total;
+};
+static SegBwdPlan plan_seg_bwd(const Shape& s, int segments) {
+    SegBwdPlan w;
+    w.seg = plan_seg_shape(s, segments);
+    w.tc = plan_tc_bwd(w.seg.ps);
+    w.total = plan_seg_tail(w.seg, w.tc.total);
+    return w;
+}
+
+size_t kda_bwd_segmented_workspace_size(const kda_dims* dims, int chunk_size, int segments) {
+    Shape s;
+    return seg_shape(dims, chunk_size, segments, &s) ? plan_seg_bwd(s, segments).total : 0;
+}
+
+kda_status kda_bwd_segmented(const kda_dims* dims, const void* q, const void* k, const void* v, const void* g_raw,
+                             const void* beta_raw, const float* a_log, const float* dt_bias, float scale,
+                             float lower_bound, int chunk_size, int segments, const int32_t* cu_seqlens,
+                             const int32_t* cu_seqlens_host, const float* initial_state, const void* dout,
+                             const float* dfinal_state, float* dq, float* dk, float* dv, float* dg_raw,
+                             float* dbeta_raw, float* da_log, float* ddt_bias, float* dinitial_state, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+    Shape s;
+    kda_status st = common_checks(dims, chunk_size, cu_seqlens, cu_seqlens_host, q, k, v, g_raw, beta_raw, a_log,
+                                  dt_bias, scale, lower_bound, &s);
+    if (st != KDA_OK) return st;
+    if (!dout || !dq || !dk || !dv || !dg_raw || !dbeta_raw || !da_log || !ddt_bias || segments < 1)
+        return KDA_ERR_INVALID_ARG;
+    Params p = base_params(s, q, k, v, g_raw, beta_raw, a_log, dt_bias, scale, lower_bound, cu_seqlens,
+                           initial_state);
+    p.dout = dout; p.dST = dfinal_state;
+    p.dq = dq; p.dk = dk; p.dv = dv; p.dg_raw = dg_raw; p.dbeta_raw = dbeta_raw;
+    p.da_log = da_log; p.ddt_bias = ddt_bias; p.dS0 = dinitial_state;
+    if (!tc_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
+    const SegBwdPlan w = plan_seg_bwd(s, segments);
+    st = check_ws(workspace, workspace_bytes, w.total);
+    if (st != KDA_OK) return st;
+    st = status_ptr(&p.status);
+    if (st != KDA_OK) return st;
+    char* b = static_cast<char*>(workspace);
+    Params pp = piece_params(p, w.seg, b);
+    carve(pp, w.tc.simt, workspace);
+    uint8_t* bw = reinterpret_cast<uint8_t*>(b + w.tc.off_bwrec);
+    pp.chunk_u = reinterpret_cast<float*>(b + w.tc.off_u);
+    pp.chunk_du = reinterpret_cast<float*>(b + w.tc.off_du);
+    int32_t* row_piece = reinterpret_cast<int32_t*>(b + w.seg.off_row_piece);
+    float* sloc = reinterpret_cast<float*>(b + w.seg.off_sloc);
+    float* M = reinterpret_cast<float*>(b + w.seg.off_m);
+    float* sstart = reinterpret_cast<float*>(b + w.seg.off_sstart);
+    KDA_TRY_CUDA(launch_piece_plan(cu_seqlens, s.N, s.T, s.TT, w.seg.L, w.seg.Pmax, const_cast<int32_t*>(pp.cu),
+                                   row_piece, p.status, stream));
+    KDA_TRY_CUDA(launch_plan(pp, stream));
+    if (s.gate == KDA_GATE_SOFTPLUS) {
+        pp.diag = reinterpret_cast<float*>(b + w.tc.off_diag);
+        KDA_TRY_CUDA(launch_diag_tc(pp, stream));
+    }
+    KDA_TRY_CUDA(launch_intra_tc(pp, nullptr, 1, stream));
+    KDA_TRY_CUDA(launch_bwd_pre(pp, bw, stream));
+    // the states entering every chunk: local end states and transfer matrices of the pieces, the
+    // pieces' true entering states along each row, then the recompute chain from those
+    Params pf = pp;
+    pf.out = nullptr;
+    pf.ST = sloc;
+    KDA_TRY_CUDA(launch_chain_rec_tc(pf, bw, stream, kBwdChainLocal));
+    pf.ST = M;
+    KDA_TRY_CUDA(launch_chain_rec_tc(pf, bw, stream, kBwdChainTransfer));
+    KDA_TRY_CUDA(launch_seg_combine(initial_state, nullptr, sloc, M, sstart, s.N, s.H, row_piece, false, stream));
+    pf.S0 = sstart;
+    pf.ST = nullptr;
+    KDA_TRY_CUDA(launch_chain_rec_tc(pf, bw, stream, kBwdChainFull));
+    // the reverse chain likewise, last piece to first: dS leaving each piece, and the row's dS_0
+    Params pr = pp;
+    pr.dS0 = sloc;
+    KDA_TRY_CUDA(launch_chain_bwd_tc(pr, bw, stream, kBwdChainLocal));
+    pr.dS0 = M;
+    KDA_TRY_CUDA(launch_chain_bwd_tc(pr, bw, stream, kBwdChainTransfer));
+    KDA_TRY_CUDA(launch_seg_combine(dfinal_state, dinitial_state, sloc, M, sstart, s.N, s.H, row_piece, true, stream));
+    pr.dST = sstart;
+    pr.dS0 = nullptr;
+    KDA_TRY_CUDA(launch_chain_bwd_tc(pr, bw, stream, kBwdChainFull));
+    KDA_TRY_CUDA(launch_grad_tc(pp, stream));
     return KDA_OK;
 }
 

@@ -40,6 +40,7 @@ struct ChainSrc {
     size_t ystride;
     const float* pbase;   // reverse chain only
     size_t pstride;
+    int mode;             // BwdChainMode
 };
 
 namespace bwchain {
@@ -70,7 +71,7 @@ __device__ __forceinline__ void split8_bf16(const float* x, uint4& hi, uint4& lo
     lo = pack8_bf16(l);
 }
 
-template <int JW, bool REV>
+template <int JW, bool REV, int MODE>
 __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc src) {
     using L = bwchain::Lay<JW>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -96,15 +97,20 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(tslot, L::TCOLS);
+    // local and transfer passes write only the end state; the transfer pass takes Y and P as zero
+    constexpr bool full_pass = MODE == kBwdChainFull, zero_y = MODE == kBwdChainTransfer;
     float z[JW];   // row tid of Z (dS for the reverse chain, S for the recompute)
     {
-        const float* z0 = REV ? p.dST : p.S0;
+        const float* z0 = full_pass ? (REV ? p.dST : p.S0) : nullptr;
         const float* zs = z0 ? z0 + (((size_t)n * H + h) * K + tid) * V + j0 : nullptr;
 #pragma unroll
         for (int j = 0; j < JW; j += 4) {
             const float4 v = zs ? *reinterpret_cast<const float4*>(zs + j) : make_float4(0.f, 0.f, 0.f, 0.f);
             z[j] = v.x; z[j + 1] = v.y; z[j + 2] = v.z; z[j + 3] = v.w;
         }
+        if (zero_y)   // the identity (K = V): row tid has its one in column tid
+#pragma unroll
+            for (int j = 0; j < JW; ++j) z[j] = (j0 + j == tid) ? 1.f : 0.f;
     }
     auto write_z_operand = [&]() {   // thread = K index c: eight j per 16-byte row of a core matrix
 #pragma unroll
@@ -165,7 +171,7 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
             mma3(tD1, smem_u32(sl + A1), smem_u32(sl + A1L), smem_u32(ZB), smem_u32(ZL), 8, 256, 128, 2048, L::ZK,
                  idesc_bf16(64, JW, 0, 1));
             mma_commit(bar1);
-            if (s + 1 < nch) {   // warm L2 with the next chunk's Y (and P)
+            if (s + 1 < nch && !zero_y) {   // warm L2 with the next chunk's Y (and P)
                 asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(y_ptr(s + 1))),
                              "r"(64u * V * 4u)
                              : "memory");
@@ -176,8 +182,8 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
                                  : "memory");
             }
         }
-        {   // reverse: gradient w.r.t. the state leaving chunk c; forward: the state entering chunk c
-            // (x4 order: the warp's 32 rows make 512 contiguous bytes per 16-byte store)
+        if (full_pass) {   // reverse: gradient w.r.t. the state leaving chunk c; forward: the state entering
+            // chunk c (x4 order: the warp's 32 rows make 512 contiguous bytes per 16-byte store)
             float* dst = (REV ? p.dstates : p.states) + ((size_t)c * H + h) * K * V;
 #pragma unroll
             for (int j = 0; j < JW; j += 4)
@@ -189,6 +195,11 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
         const int t = 16 * warp + (lane & 15);
         // 32 columns from col of row `row` of a tile with `rows` rows, x4-ordered or row-major
         auto load32 = [](const float* tile, int row, int col, int rows, bool x4, float* dst) {
+            if (zero_y) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) dst[j] = 0.f;
+                return;
+            }
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
                 const float4 v = *reinterpret_cast<const float4*>(tile + (x4 ? x4_off(row, col + j, rows)
@@ -214,7 +225,7 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) d[j] += y[j];
-                if (lane < 16) {   // X row t (U or dU) for the gradient kernel, x4 order
+                if (full_pass && lane < 16) {   // X row t (U or dU) for the gradient kernel, x4 order
                     float* xo = (REV ? p.chunk_du : p.chunk_u) + ((size_t)c * H + h) * 64 * V;
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
@@ -303,11 +314,13 @@ template <int JW, bool REV>
 static cudaError_t launch_chain_jw(const Params& p, const ChainSrc& src, cudaStream_t st) {
     using L = bwchain::Lay<JW>;
     static_assert(L::BYTES <= 232448, "shared memory per CTA");
-    cudaError_t e = cudaFuncSetAttribute(chain_split_kernel<JW, REV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)L::BYTES);
+    auto kern = src.mode == kBwdChainLocal      ? chain_split_kernel<JW, REV, kBwdChainLocal>
+                : src.mode == kBwdChainTransfer ? chain_split_kernel<JW, REV, kBwdChainTransfer>
+                                                : chain_split_kernel<JW, REV, kBwdChainFull>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
     if (e != cudaSuccess) return e;
     timing_pre(st, REV ? K_CHAIN_BWD_TC : K_CHAIN_REC_TC);
-    chain_split_kernel<JW, REV><<<dim3(p.N, p.H, 128 / JW), 128, L::BYTES, st>>>(p, src);
+    kern<<<dim3(p.N, p.H, 128 / JW), 128, L::BYTES, st>>>(p, src);
     timing_post(st);
     return cudaGetLastError();
 }
@@ -325,16 +338,16 @@ static cudaError_t launch_chain(const Params& p, const ChainSrc& src, cudaStream
     return launch_chain_jw<32, REV>(p, src, st);
 }
 
-cudaError_t launch_chain_bwd_tc(const Params& p, const uint8_t* bw, cudaStream_t st) {
+cudaError_t launch_chain_bwd_tc(const Params& p, const uint8_t* bw, cudaStream_t st, int mode) {
     ChainSrc src{bw, bwrec::BYTES, reinterpret_cast<const float*>(bw + bwrec::Y), bwrec::BYTES / 4,
-                 reinterpret_cast<const float*>(bw + bwrec::P), bwrec::BYTES / 4};
+                 reinterpret_cast<const float*>(bw + bwrec::P), bwrec::BYTES / 4, mode};
     static_assert(bwrec::BYTES % 256 == 0, "record stride");
     return launch_chain<true>(p, src, st);
 }
 
-cudaError_t launch_chain_rec_tc(const Params& p, const uint8_t* bw, cudaStream_t st) {
+cudaError_t launch_chain_rec_tc(const Params& p, const uint8_t* bw, cudaStream_t st, int mode) {
     const RecLayout L = RecLayout::make(128, 128);
-    ChainSrc src{bw, bwrec::BYTES, p.rec + L.U0, p.rec_stride, nullptr, 0};
+    ChainSrc src{bw, bwrec::BYTES, p.rec + L.U0, p.rec_stride, nullptr, 0, mode};
     return launch_chain<false>(p, src, st);
 }
 

@@ -141,8 +141,13 @@ cudaError_t launch_param_reduce(const Params& p, cudaStream_t st);
 cudaError_t launch_group_sum(const Params& p, cudaStream_t st);   // dq_v, dk_v -> dq, dk when G > 1
 cudaError_t launch_grad_tc(const Params& p, cudaStream_t st);
 cudaError_t launch_bwd_pre(const Params& p, uint8_t* bw, cudaStream_t st);
-cudaError_t launch_chain_bwd_tc(const Params& p, const uint8_t* bw, cudaStream_t st);
-cudaError_t launch_chain_rec_tc(const Params& p, const uint8_t* bw, cudaStream_t st);
+// The two state chains of the backward.  kBwdChainFull: from p.S0 / p.dST, writing the per-chunk
+// tiles the gradient kernel reads (and p.ST / p.dS0 at the end if set); kBwdChainLocal: from zero,
+// only the end state (into p.ST / p.dS0); kBwdChainTransfer: from the identity with Y and P taken as
+// zero, only the end state, which is then the segment's transfer matrix.
+enum BwdChainMode { kBwdChainFull = 0, kBwdChainLocal = 1, kBwdChainTransfer = 2 };
+cudaError_t launch_chain_bwd_tc(const Params& p, const uint8_t* bw, cudaStream_t st, int mode = kBwdChainFull);
+cudaError_t launch_chain_rec_tc(const Params& p, const uint8_t* bw, cudaStream_t st, int mode = kBwdChainFull);
 
 // tensor-core path (bf16, K = V = 128)
 size_t tc_record_bytes(int NCmax, int H);
@@ -158,12 +163,15 @@ cudaError_t launch_intra2(const Params& p, uint8_t* recs, cudaStream_t st);
 // transfer: start from the identity with U0 taken as zero, so that the final state is the transfer matrix
 cudaError_t launch_chain_fwd_tc(const Params& p, const uint8_t* recs, bool store_states, cudaStream_t st,
                                 bool transfer = false);
-// segment-parallel forward: piece boundaries of B rows of T tokens (P pieces of L tokens), and the
-// serial propagation of piece-entering states S_{k+1} = M_k S_k + S_loc,k (fp32, K = V = 128)
-cudaError_t launch_piece_cu(int32_t* cu, int B, int T, int L, int P, cudaStream_t st);
+// segment-parallel schedule: the pieces of the rows (documents of cu, or B rows of T tokens when cu
+// is null) at most L tokens long, at most Pmax of them, and the serial propagation of the pieces'
+// starting states S_{k+1} = M_k S_k + S_loc,k along each row (fp32, K = V = 128), first to last, or
+// last to first for the reverse chain of the backward
+cudaError_t launch_piece_plan(const int32_t* cu, int rows, int T, int TT, int L, int Pmax, int32_t* piece_cu,
+                              int32_t* row_piece, int* status, cudaStream_t st);
+cudaError_t launch_seg_combine(const float* S0, float* ST, const float* sloc, const float* M, float* sstart, int rows,
+                               int H, const int32_t* row_piece, bool reverse, cudaStream_t st);
 // failure-detection self-test: a bounded wait that cannot complete records KDA_ERR_TIMEOUT
 cudaError_t launch_selftest_wait(int* status, cudaStream_t st);
-cudaError_t launch_seg_combine(const float* S0, float* ST, const float* sloc, const float* M, float* sstart, int B,
-                               int H, int P, cudaStream_t st);
 
 }  // namespace kda

@@ -1305,21 +1305,40 @@ cudaError_t launch_selftest_wait(int* status, cudaStream_t st) {
 // in parallel over pieces, propagates the true piece-entering states here, and runs the chain once
 // more from them for the output.
 
-// cu[i] = first token of piece i (P pieces of L tokens per row of T, the last one shorter).
-__global__ void piece_cu_kernel(int32_t* cu, int B, int T, int L, int P) {
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i <= B * P; i += gridDim.x * blockDim.x) {
-        const int b = i / P, k = i - b * P;
-        cu[i] = b * T + min(k * L, T);
+// Pieces of the rows: row n (a document of cu_seqlens, or row n of B rows of T tokens when cu is
+// null) is cut into ceil(len / L) pieces of L tokens (the last one shorter; none for an empty row).
+// piece_cu[i] = first token of piece i, rows' pieces in order, row_piece[n] = first piece of row n;
+// the Pmax - used unused pieces at the end are empty (piece_cu = TT).  One thread: the rows are few.
+// A cu that does not start at 0, decreases or does not end at TT is reported in the status word and
+// yields no pieces, so every later kernel finds nothing to do.
+__global__ void piece_plan_kernel(const int32_t* cu, int rows, int T, int TT, int L, int Pmax, int32_t* piece_cu,
+                                  int32_t* row_piece, int* status) {
+    if (blockIdx.x != 0 || threadIdx.x != 0) return;
+    bool ok = !cu || (cu[0] == 0 && cu[rows] == TT);
+    for (int n = 0; ok && cu && n < rows; ++n) ok = cu[n + 1] >= cu[n];
+    int np = 0;
+    if (ok)
+        for (int n = 0; n < rows; ++n) {
+            row_piece[n] = np;
+            const int b0 = cu ? cu[n] : n * T, e0 = cu ? cu[n + 1] : (n + 1) * T;
+            for (int t = b0; t < e0 && np < Pmax; t += L) piece_cu[np++] = t;
+        }
+    else {
+        record_error(status, KDA_ERR_INVALID_ARG);
+        for (int n = 0; n < rows; ++n) row_piece[n] = 0;
     }
+    row_piece[rows] = np;
+    for (int i = np; i <= Pmax; ++i) piece_cu[i] = TT;
 }
-
 // One CTA per (row, head, 16-column slice); thread k owns row k of the state slice (fp32).  For each
-// piece in order: record the entering state, then S <- M S + S_loc, with M staged in shared memory by
-// coalesced loads (rows padded to 129 floats: the row-per-thread reads are conflict-free).  The final
-// S is the row's final state.
+// piece of the row in order (last to first when `reverse`): record the piece's starting state, then
+// S <- M S + S_loc, with M staged in shared memory by coalesced loads (rows padded to 129 floats: the
+// row-per-thread reads are conflict-free).  The final S is the row's result: its final state, or for
+// the reverse chain of the backward the gradient w.r.t. its initial state.
 constexpr int kCombineSmem = (128 * 129 + 128 * 17) * 4;
 __global__ void __launch_bounds__(128) seg_combine_kernel(const float* S0, float* ST, const float* sloc,
-                                                          const float* M, float* sstart, int H, int P) {
+                                                          const float* M, float* sstart, int H,
+                                                          const int32_t* row_piece, int reverse) {
     extern __shared__ float csm[];
     float* sM = csm;                 // [128][129]
     float* sS = csm + 128 * 129;     // [128][17]
@@ -1330,8 +1349,10 @@ __global__ void __launch_bounds__(128) seg_combine_kernel(const float* S0, float
 #pragma unroll
         for (int j = 0; j < 16; ++j) S[j] = src ? src[j] : 0.f;
     }
-    for (int pc = 0; pc < P; ++pc) {
-        const size_t base = ((size_t)(b * P + pc) * H + h) * 128 * 128;
+    const int p0 = row_piece[b], np = row_piece[b + 1] - p0;
+    for (int i = 0; i < np; ++i) {
+        const int pc = reverse ? p0 + np - 1 - i : p0 + i;
+        const size_t base = ((size_t)pc * H + h) * 128 * 128;
         float* dst = sstart + base + (size_t)k * 128 + j0;
 #pragma unroll
         for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
@@ -1367,17 +1388,18 @@ __global__ void __launch_bounds__(128) seg_combine_kernel(const float* S0, float
     }
 }
 
-cudaError_t launch_piece_cu(int32_t* cu, int B, int T, int L, int P, cudaStream_t st) {
-    piece_cu_kernel<<<(B * P + 256) / 256, 256, 0, st>>>(cu, B, T, L, P);
+cudaError_t launch_piece_plan(const int32_t* cu, int rows, int T, int TT, int L, int Pmax, int32_t* piece_cu,
+                              int32_t* row_piece, int* status, cudaStream_t st) {
+    piece_plan_kernel<<<1, 32, 0, st>>>(cu, rows, T, TT, L, Pmax, piece_cu, row_piece, status);
     return cudaGetLastError();
 }
-
-cudaError_t launch_seg_combine(const float* S0, float* ST, const float* sloc, const float* M, float* sstart, int B,
-                               int H, int P, cudaStream_t st) {
+cudaError_t launch_seg_combine(const float* S0, float* ST, const float* sloc, const float* M, float* sstart, int rows,
+                               int H, const int32_t* row_piece, bool reverse, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(seg_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCombineSmem);
     if (e != cudaSuccess) return e;
     timing_pre(st, K_SEG_COMBINE);
-    seg_combine_kernel<<<dim3(B, H, 8), 128, kCombineSmem, st>>>(S0, ST, sloc, M, sstart, H, P);
+    seg_combine_kernel<<<dim3(rows, H, 8), 128, kCombineSmem, st>>>(S0, ST, sloc, M, sstart, H, row_piece,
+                                                                     reverse ? 1 : 0);
     timing_post(st);
     return cudaGetLastError();
 }

@@ -36,7 +36,8 @@ def main(argv=None) -> None:
     ap.add_argument("--fwd-only", action="store_true", help="skip the backward of a fwd+bwd workload")
     ap.add_argument("--saved", action="store_true", help="forward keeps the per-chunk record for the backward")
     ap.add_argument("--segments", type=int, default=0,
-                    help="forward through kda_fwd_segmented with this many pieces per row (forward only)")
+                    help="forward and backward through kda_fwd_segmented / kda_bwd_segmented, rows cut into "
+                         "pieces of 1 / segments of a row")
     ap.add_argument("--gate", default="lower_bounded", choices=("lower_bounded", "softplus"),
                     help="gate activation (softplus: the unbounded gate)")
     ap.add_argument("--gated-norm", action="store_true",
@@ -72,8 +73,8 @@ def main(argv=None) -> None:
         saved = torch.empty(nb, dtype=torch.uint8, device=dev)
     if a.segments:
         kw["segments"] = a.segments
-        if run_bwd or w.varlen:
-            raise SystemExit("--segments times the forward of rows of T tokens")
+        if saved is not None:
+            raise SystemExit("--segments runs without --saved")
 
     def step():
         forward(*[x[n] for n in names], output_final_state=w.final_state, saved=saved, **kw)

@@ -259,33 +259,73 @@ kda_status kda_fwd_noalloc(const kda_dims* dims,
  * Segment-parallel forward for long rows with few rows x heads.  The chunk
  * chain of kda_fwd is serial per (row, head).  When B * H is small it keeps
  * only a few SMs busy however long T is.  This entry cuts every row into
- * `segments` pieces of equal whole-chunk length and works like the state-CP
- * executor of hyper-parallel "KDA context-parallel executors"
- * (`_eager_kda_state_p2p`), with pieces in place of ranks, on one GPU:
+ * pieces of whole chunks and works like the state-CP executor of
+ * hyper-parallel "KDA context-parallel executors" (`_eager_kda_state_p2p`),
+ * with pieces in place of ranks, on one GPU:
  *   1. for every piece in parallel, a summary of its chunks: the end state from
  *      zero S_loc and the transition M (the K x K product of the per-chunk
  *      maps S -> Diag(exp(Gamma_last)) S - Kd^T W S);
- *   2. the entering states, piece after piece: S_{k+1} = M_k S_k + S_loc,k,
- *      from initial_state (or zero); the last one is final_state;
+ *   2. the entering states, piece after piece along each row:
+ *      S_{k+1} = M_k S_k + S_loc,k, from the row's initial_state (or zero);
+ *      the last one is the row's final_state;
  *   3. the output of every piece from its entering state, in parallel.
- * Same arguments and results as kda_fwd without cu_seqlens: rows of T tokens
- * only (packed documents are KDA_ERR_UNSUPPORTED here).  It takes only
- * shapes of the tensor-core forward: bf16, K = V = 128, 16-byte aligned
- * activations, the softplus gate or lower_bound >= -5; others are
- * KDA_ERR_UNSUPPORTED.  segments >= 1, else KDA_ERR_INVALID_ARG.  Pieces are
- * ceil(ceil(T / 64) / segments) chunks long, so fewer pieces than `segments`
- * can result.  The intra-chunk pass runs once and the chain three times,
- * each over all pieces at once.  In exact arithmetic the result equals
- * kda_fwd's; in floating point it agrees to rounding.  The workspace is
+ * Same arguments and results as kda_fwd plus `segments`.  A row is one of
+ * the B rows of T tokens, or with cu_seqlens one packed document (the
+ * documents of nemo_automodel `kimi_k3.cp`, `segment_cu_seqlens`, each
+ * starting from its own initial state); cu_seqlens and cu_seqlens_host as
+ * for kda_fwd.  Pieces are L = ceil(ceil(span / 64) / segments) chunks of 64
+ * tokens long, span = T for rows and the total token count for documents;
+ * a row of len tokens gets ceil(len / L) pieces, its last one shorter.  It
+ * takes only shapes of the tensor-core forward: bf16, K = V = 128, 16-byte
+ * aligned activations, the softplus gate or lower_bound >= -5; others are
+ * KDA_ERR_UNSUPPORTED.  segments >= 1, else KDA_ERR_INVALID_ARG.  The
+ * intra-chunk pass runs once and the chain three times, each over all
+ * pieces at once.  In exact arithmetic the result equals kda_fwd's; in
+ * floating point it agrees to rounding.  The workspace is
  * kda_fwd_segmented_workspace_size() bytes (0 for invalid or unsupported
  * shapes); it adds three fp32 states per piece and head to the forward's.
+ * A device-only cu_seqlens with bad contents is reported, as for kda_fwd,
+ * through kda_device_status, and no piece is run.
  */
 size_t kda_fwd_segmented_workspace_size(const kda_dims* dims, int chunk_size, int segments);
 kda_status kda_fwd_segmented(const kda_dims* dims,
                              const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
                              const float* a_log, const float* dt_bias, float scale, float lower_bound,
-                             int chunk_size, int segments, const float* initial_state,
+                             int chunk_size, int segments, const int32_t* cu_seqlens,
+                             const int32_t* cu_seqlens_host, const float* initial_state,
                              void* out, float* final_state,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Segment-parallel backward: kda_bwd with both state chains of the
+ * backward cut into the pieces of kda_fwd_segmented.  The forward state
+ * recompute runs steps 1-3 above (end states from zero and transitions per
+ * piece, entering states along each row, then every piece from its entering
+ * state).  The reverse chain is affine in the same way, from the end of a
+ * piece to its start: dS_begin = M'_k dS_end + dS_loc,k, with M'_k the
+ * piece's K x K transition of dS and dS_loc,k its start value from a zero
+ * end value.  Its pieces' end values follow along each row from the last
+ * piece, dS_end of the last piece = dfinal_state (or zero), dS_end,k-1 =
+ * M'_k dS_end,k + dS_loc,k; the first piece's dS_begin is the row's
+ * dinitial_state.  This is the gradient the state-CP executor of
+ * hyper-parallel "KDA context-parallel executors" (`_eager_kda_state_p2p`)
+ * sends back from rank to rank.  Both chains run in the split bf16
+ * precision of kda_bwd's tensor-core chains, the combines in fp32.  Same
+ * arguments and results as kda_bwd plus `segments`; the same shapes as
+ * kda_fwd_segmented, else KDA_ERR_UNSUPPORTED.  The gradients agree with
+ * kda_bwd's to rounding.  The workspace is
+ * kda_bwd_segmented_workspace_size() bytes (0 for invalid or unsupported
+ * shapes).
+ */
+size_t kda_bwd_segmented_workspace_size(const kda_dims* dims, int chunk_size, int segments);
+kda_status kda_bwd_segmented(const kda_dims* dims,
+                             const void* q, const void* k, const void* v, const void* g_raw, const void* beta_raw,
+                             const float* a_log, const float* dt_bias, float scale, float lower_bound,
+                             int chunk_size, int segments, const int32_t* cu_seqlens,
+                             const int32_t* cu_seqlens_host, const float* initial_state,
+                             const void* dout, const float* dfinal_state,
+                             float* dq, float* dk, float* dv, float* dg_raw, float* dbeta_raw,
+                             float* da_log, float* ddt_bias, float* dinitial_state,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*

@@ -97,15 +97,15 @@ def oracle_bwd(x: dict, rows=None, dfinal=None):
                           dfinal_state=f64(dfinal))
 
 
-def gpu_fwd(x: dict, simt=False, final=True):
+def gpu_fwd(x: dict, simt=False, final=True, segments=0):
     import gated_delta_rule_sm_gb300 as kda
     return kda.forward(*[x[n] for n in ACT], scale=x["scale"], lower_bound=x["lower_bound"],
                        gate=x.get("gate", "lower_bounded"), chunk_size=x.get("chunk_size", 64), cu_seqlens=x.get("cu_seqlens"),
-                       initial_state=x.get("initial_state"), output_final_state=final, simt=simt)
+                       initial_state=x.get("initial_state"), output_final_state=final, simt=simt, segments=segments)
 
 
-def gpu_bwd(x: dict, dfinal=None):
+def gpu_bwd(x: dict, dfinal=None, segments=0):
     import gated_delta_rule_sm_gb300 as kda
     return kda.backward(*[x[n] for n in ACT], x["dout"], scale=x["scale"], lower_bound=x["lower_bound"],
                         gate=x.get("gate", "lower_bounded"), chunk_size=x.get("chunk_size", 64), cu_seqlens=x.get("cu_seqlens"),
-                        initial_state=x.get("initial_state"), dfinal_state=dfinal)
+                        initial_state=x.get("initial_state"), dfinal_state=dfinal, segments=segments)

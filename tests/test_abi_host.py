@@ -254,10 +254,16 @@ def test_short_conv_validation(lib):
     assert ws(W=9) == 0 and ws(C=0) == 0
 
 
-def _fwd_seg(lib, dims, segments=4, ws=None, ws_bytes=0, ptr=16):
+def _fwd_seg(lib, dims, segments=4, ws=None, ws_bytes=0, ptr=16, cu=None, cu_host=None):
     p = ctypes.c_void_p(ptr)
-    return lib.kda_fwd_segmented(ctypes.byref(dims), p, p, p, p, p, p, p, 0.125, -5.0, 64, segments, None, p, None,
-                                 ws, ctypes.c_size_t(ws_bytes), None)
+    return lib.kda_fwd_segmented(ctypes.byref(dims), p, p, p, p, p, p, p, 0.125, -5.0, 64, segments, cu, cu_host,
+                                 None, p, None, ws, ctypes.c_size_t(ws_bytes), None)
+
+
+def _bwd_seg(lib, dims, segments=4, ws=None, ws_bytes=0, ptr=16, cu=None, cu_host=None):
+    p = ctypes.c_void_p(ptr)
+    return lib.kda_bwd_segmented(ctypes.byref(dims), p, p, p, p, p, p, p, 0.125, -5.0, 64, segments, cu, cu_host,
+                                 None, p, None, p, p, p, p, p, p, p, None, ws, ctypes.c_size_t(ws_bytes), None)
 
 
 def test_segmented_forward_validation(lib):
@@ -275,6 +281,39 @@ def test_segmented_forward_validation(lib):
     assert sz(d128, 8) - sz(d128, 4) >= 3 * 4 * 2 * 65536
     assert sz(d128, 8) > sz(d128, 4) > sz(d128, 1)
     assert sz(d128, 64) == sz(d128, 1000)            # never more pieces than chunks
+
+
+def test_segmented_backward_validation(lib):
+    """kda_bwd_segmented: the forward's shape rules, segments >= 1, a workspace of its own that holds
+    the backward's buffers for the pieces plus three states per piece and head."""
+    d128 = _dims(K=128, V=128, T=4096)
+    sz = lambda d, n: lib.kda_bwd_segmented_workspace_size(ctypes.byref(d), 64, n)
+    assert _bwd_seg(lib, d128, segments=0) == _lib.KDA_ERR_INVALID_ARG
+    assert _bwd_seg(lib, _dims(), segments=4) == _lib.KDA_ERR_UNSUPPORTED              # K = V = 64
+    assert _bwd_seg(lib, _dims(K=128, V=128, dtype=_lib.KDA_FP32)) == _lib.KDA_ERR_UNSUPPORTED
+    assert _bwd_seg(lib, d128, ptr=24) == _lib.KDA_ERR_UNSUPPORTED                     # unaligned activations
+    assert _bwd_seg(lib, d128) == _lib.KDA_ERR_WORKSPACE
+    assert sz(_dims(), 4) == 0 and sz(d128, 0) == 0
+    plain = lib.kda_bwd_workspace_size(ctypes.byref(d128), 64)
+    assert sz(d128, 1) > plain + 3 * 1 * 2 * 65536
+    assert sz(d128, 8) - sz(d128, 4) >= 3 * 4 * 2 * 65536
+    assert sz(d128, 64) == sz(d128, 1000)
+
+
+def test_segmented_packed_documents_host_checks(lib):
+    """With packed documents both segmented entries check a host copy of the offsets before any
+    launch, and size their workspace for one piece more per document."""
+    lens = [100, 0, 300, 5]
+    cu = (ctypes.c_int32 * 5)(0, 100, 100, 400, 405)
+    bad = (ctypes.c_int32 * 5)(0, 100, 90, 400, 405)      # decreasing
+    dev = ctypes.c_void_p(64)                              # device copy (never read on the host)
+    d = _dims(K=128, V=128, B=1, T=sum(lens), num_seqs=len(lens))
+    for f in (_fwd_seg, _bwd_seg):
+        assert f(lib, d, cu=dev, cu_host=bad) == _lib.KDA_ERR_INVALID_ARG
+        assert f(lib, d, cu=dev, cu_host=cu) == _lib.KDA_ERR_WORKSPACE
+    rows = _dims(K=128, V=128, B=1, T=sum(lens))
+    for f in (lib.kda_fwd_segmented_workspace_size, lib.kda_bwd_segmented_workspace_size):
+        assert f(ctypes.byref(d), 64, 4) > f(ctypes.byref(rows), 64, 4) > 0
 
 
 def test_gated_norm_validation(lib):

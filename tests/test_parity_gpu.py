@@ -34,14 +34,15 @@ def _check_fwd(x, dtype, simt=False, final=True):
 GRADS = ("dq", "dk", "dv", "dg_raw", "dbeta_raw", "da_log", "ddt_bias", "dinitial_state")
 
 
-def _check_bwd(x, dtype, dfinal=None):
-    g = gpu_bwd(x, dfinal=dfinal)
+def _check_bwd(x, dtype, dfinal=None, segments=0):
+    g = gpu_bwd(x, dfinal=dfinal, segments=segments)
     torch.cuda.synchronize()
     assert device_status() == 0
     r = oracle_bwd(x, dfinal=dfinal)
     errs = {n: rel_err(g[n], r[n], dtype) for n in GRADS}
     bad = {n: e for n, e in errs.items() if not e <= tol(dtype)}
     assert not bad, bad
+    return g
 
 
 # ------------------------------------------------------------------ the fp32 workload, exact config
@@ -512,7 +513,7 @@ def _check_segmented(x, segments, dtype="bf16"):
     names = ("q", "k", "v", "g_raw", "beta_raw", "a_log", "dt_bias")
     out, fs = kda.forward(*[x[n] for n in names], scale=x["scale"], lower_bound=x["lower_bound"],
                           gate=x.get("gate", "lower_bounded"), initial_state=x.get("initial_state"),
-                          output_final_state=True, segments=segments)
+                          cu_seqlens=x.get("cu_seqlens"), output_final_state=True, segments=segments)
     torch.cuda.synchronize()
     assert device_status() == 0
     r_out, r_fs = oracle_fwd(x)
@@ -542,6 +543,17 @@ def test_segmented_forward_softplus_gate():
     _check_segmented(x, 5)
 
 
+def test_segmented_forward_packed_documents():
+    """Documents of 0 to 700 tokens, each with its own initial state: a document gets as many pieces
+    as its length needs (none when empty), and states never cross a document boundary."""
+    lens = [700, 0, 1, 64, 65, 300, 17]
+    w = Workload("t", B=1, T=sum(lens), H=2, K=128, V=128, varlen=True, initial_state=True, g_mean=-4.0,
+                 seed=74)
+    x = make_inputs(w, device=DEV, lengths=lens)
+    for segments in (2, 5, 100):
+        _check_segmented(x, segments)
+
+
 def test_segmented_forward_long_row_few_heads():
     """The case the schedule is for: one 65536-token row on two heads (the long-context workload's
     distributions), 16 pieces; and a mild-gate row of 8192 tokens cut into 64-token pieces."""
@@ -549,3 +561,59 @@ def test_segmented_forward_long_row_few_heads():
     _check_segmented(make_inputs(w, device=DEV), 16)
     w = Workload("t", B=1, T=8192, H=2, K=128, V=128, initial_state=True, g_mean=-4.0, seed=73)
     _check_segmented(make_inputs(w, device=DEV), 128)
+
+
+# ------------------------------------------------------------------ segment-parallel backward
+
+@pytest.mark.parametrize("segments", [1, 3, 16])
+def test_segmented_backward_matches_the_oracle(segments):
+    """Both state chains of the backward cut into pieces: mild gates so that the states and their
+    gradients carry across pieces, an initial state and a final-state gradient, a 60-token tail."""
+    w = Workload("t", B=1, T=700, H=2, K=128, V=128, initial_state=True, backward=True, g_mean=-4.0, seed=80)
+    x = make_inputs(w, device=DEV)
+    dfinal = 0.05 * torch.randn((1, 2, 128, 128), generator=torch.Generator().manual_seed(80)).to(DEV)
+    _check_bwd(x, "bf16", dfinal=dfinal, segments=segments)
+
+
+def test_segmented_backward_rows_and_plain_agree():
+    """Two rows, three heads: every gradient agrees with the oracle and with kda_bwd."""
+    w = Workload("t", B=2, T=333, H=3, K=128, V=128, initial_state=True, backward=True, g_mean=-3.0, seed=81)
+    x = make_inputs(w, device=DEV)
+    dfinal = 0.05 * torch.randn((2, 3, 128, 128), generator=torch.Generator().manual_seed(81)).to(DEV)
+    g = _check_bwd(x, "bf16", dfinal=dfinal, segments=4)
+    g0 = gpu_bwd(x, dfinal=dfinal)
+    torch.cuda.synchronize()
+    for n in GRADS:
+        assert rel_err(g[n], f64(g0[n]), "bf16") <= 2e-2, n
+
+
+def test_segmented_backward_packed_documents():
+    lens = [300, 0, 1, 64, 200, 17]
+    w = Workload("t", B=1, T=sum(lens), H=2, K=128, V=128, varlen=True, initial_state=True, backward=True,
+                 g_mean=-4.0, seed=82)
+    x = make_inputs(w, device=DEV, lengths=lens)
+    dfinal = 0.05 * torch.randn((len(lens), 2, 128, 128), generator=torch.Generator().manual_seed(82)).to(DEV)
+    for segments in (3, 40):
+        _check_bwd(x, "bf16", dfinal=dfinal, segments=segments)
+
+
+def test_segmented_backward_softplus_gate():
+    x = _softplus_case(B=1, T=500, H=2, K=128, V=128, initial_state=True, g_mean=-6.0, seed=83, backward=True)
+    _check_bwd(x, "bf16", segments=4)
+
+
+def test_segmented_backward_long_row_few_heads():
+    """One 8192-token row on two heads cut into 16 pieces (the backward workload's distributions),
+    against the oracle on one head."""
+    w = Workload("t", B=1, T=8192, H=2, K=128, V=128, initial_state=True, backward=True, seed=84)
+    x = make_inputs(w, device=DEV)
+    dfinal = 0.05 * torch.randn((1, 2, 128, 128), generator=torch.Generator().manual_seed(84)).to(DEV)
+    g = gpu_bwd(x, dfinal=dfinal, segments=16)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    heads = [1]
+    r = oracle_bwd(head_slice(x, heads), dfinal=dfinal[:, heads])
+    for n in ("dq", "dk", "dv", "dg_raw", "dbeta_raw"):
+        assert rel_err(g[n][:, :, heads], r[n], "bf16") <= 2e-2, n
+    assert rel_err(g["dinitial_state"][:, heads], r["dinitial_state"], "bf16") <= 2e-2
+    assert rel_err(g["da_log"][heads], r["da_log"], "bf16") <= 2e-2
