@@ -1237,9 +1237,11 @@ bool head_tile_map2(CUtensorMap* m, const void* base, int H, int TT, int C) { re
 
 bool tc_inputs_aligned(const Params& p) {
     auto al = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
-    // the forward chain stores the output and the final state 16 bytes at a time, the gradient kernel dv
+    // the forward chain stores the output and the final state 16 bytes at a time, the gradient kernel dv;
+    // the backward chains read the initial state and the final-state gradient and store the
+    // initial-state gradient likewise (a null pointer counts as aligned)
     return al(p.q) && al(p.k) && al(p.g_raw) && al(p.v) && (p.dout == nullptr || al(p.dout)) && al(p.out) &&
-           al(p.ST) && al(p.dv);
+           al(p.ST) && al(p.dv) && al(p.S0) && al(p.dST) && al(p.dS0);
 }
 
 cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, int mode, cudaStream_t st) {
@@ -1330,62 +1332,79 @@ __global__ void piece_plan_kernel(const int32_t* cu, int rows, int T, int TT, in
     row_piece[rows] = np;
     for (int i = np; i <= Pmax; ++i) piece_cu[i] = TT;
 }
-// One CTA per (row, head, 16-column slice); thread k owns row k of the state slice (fp32).  For each
-// piece of the row in order (last to first when `reverse`): record the piece's starting state, then
-// S <- M S + S_loc, with M staged in shared memory by coalesced loads (rows padded to 129 floats: the
-// row-per-thread reads are conflict-free).  The final S is the row's result: its final state, or for
-// the reverse chain of the backward the gradient w.r.t. its initial state.
-constexpr int kCombineSmem = (128 * 129 + 128 * 17) * 4;
+// One CTA per (row, head, slice of kCombineCols state columns); thread k owns row k of the slice
+// (fp32).  For each piece of the row in order (last to first when `reverse`): record the piece's
+// starting state, then S <- M S + S_loc.  M (64 KB) moves into shared memory by 16-byte cp.async
+// copies, double buffered: the next piece's M is requested before this piece's product, so the
+// serial walk along the row waits on the copy only when the product is shorter than the copy.  Rows
+// of M are padded to 132 floats (16-byte aligned; a quarter warp's 16-byte row reads hit distinct
+// banks).  The final S is the row's result: its final state, or for the reverse chain of the
+// backward the gradient w.r.t. its initial state.
+constexpr int kCombineCols = 4, kCombinePad = 132;
+constexpr int kCombineSmem = (2 * 128 * kCombinePad + 128 * kCombineCols) * 4;
 __global__ void __launch_bounds__(128) seg_combine_kernel(const float* S0, float* ST, const float* sloc,
                                                           const float* M, float* sstart, int H,
                                                           const int32_t* row_piece, int reverse) {
-    extern __shared__ float csm[];
-    float* sM = csm;                 // [128][129]
-    float* sS = csm + 128 * 129;     // [128][17]
-    const int b = blockIdx.x, h = blockIdx.y, j0 = 16 * blockIdx.z, k = threadIdx.x;
-    float S[16];
+    extern __shared__ __align__(16) float csm[];
+    float* sS = csm + 2 * 128 * kCombinePad;   // [128][kCombineCols]
+    const int b = blockIdx.x, h = blockIdx.y, j0 = kCombineCols * blockIdx.z, k = threadIdx.x;
+    float S[kCombineCols];
     {
+        // the caller's state (4-byte alignment only): plain loads
         const float* src = S0 ? S0 + (((size_t)b * H + h) * 128 + k) * 128 + j0 : nullptr;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) S[j] = src ? src[j] : 0.f;
+        for (int j = 0; j < kCombineCols; ++j) S[j] = src ? src[j] : 0.f;
     }
     const int p0 = row_piece[b], np = row_piece[b + 1] - p0;
+    auto piece = [&](int i) { return reverse ? p0 + np - 1 - i : p0 + i; };
+    auto fetch_m = [&](int i) {   // M of the i-th piece into buffer i & 1: 4096 chunks of 16 bytes
+        const float* src = M + ((size_t)piece(i) * H + h) * 128 * 128;
+        float* dst = csm + (i & 1) * 128 * kCombinePad;
+        for (int c = k; c < 4096; c += 128) {
+            const int r = c >> 5, c4 = (c & 31) * 4;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(
+                             __cvta_generic_to_shared(dst + r * kCombinePad + c4))),
+                         "l"(src + r * 128 + c4)
+                         : "memory");
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    if (np > 0) fetch_m(0);
     for (int i = 0; i < np; ++i) {
-        const int pc = reverse ? p0 + np - 1 - i : p0 + i;
+        const int pc = piece(i);
         const size_t base = ((size_t)pc * H + h) * 128 * 128;
-        float* dst = sstart + base + (size_t)k * 128 + j0;
-#pragma unroll
-        for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) sS[k * 17 + j] = S[j];
-        const float4* m4 = reinterpret_cast<const float4*>(M + base);
-#pragma unroll 8
-        for (int i = k; i < 4096; i += 128) {
-            const float4 m = m4[i];
-            float* row = sM + (i >> 5) * 129 + (i & 31) * 4;
-            row[0] = m.x; row[1] = m.y; row[2] = m.z; row[3] = m.w;
+        *reinterpret_cast<float4*>(sstart + base + (size_t)k * 128 + j0) = make_float4(S[0], S[1], S[2], S[3]);
+        *reinterpret_cast<float4*>(sS + k * kCombineCols) = make_float4(S[0], S[1], S[2], S[3]);
+        const float4 l = *reinterpret_cast<const float4*>(sloc + base + (size_t)k * 128 + j0);
+        float acc[kCombineCols] = {l.x, l.y, l.z, l.w};
+        if (i + 1 < np) {
+            fetch_m(i + 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
         }
-        float acc[16];
-        const float* lrow = sloc + base + (size_t)k * 128 + j0;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] = lrow[j];
-        __syncthreads();
-        const float* mrow = sM + k * 129;
+        __syncthreads();   // M of this piece and the slice of S are in shared memory
+        const float* mrow = csm + (i & 1) * 128 * kCombinePad + k * kCombinePad;
 #pragma unroll 4
-        for (int kk = 0; kk < 128; ++kk) {
-            const float m = mrow[kk];
+        for (int kk = 0; kk < 128; kk += 4) {
+            const float4 m = *reinterpret_cast<const float4*>(mrow + kk);
+            const float mv[4] = {m.x, m.y, m.z, m.w};
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] += m * sS[kk * 17 + j];
+            for (int u = 0; u < 4; ++u) {
+                const float4 sv = *reinterpret_cast<const float4*>(sS + (kk + u) * kCombineCols);
+                acc[0] += mv[u] * sv.x;
+                acc[1] += mv[u] * sv.y;
+                acc[2] += mv[u] * sv.z;
+                acc[3] += mv[u] * sv.w;
+            }
         }
-        __syncthreads();
+        __syncthreads();   // every reader of this M buffer and of sS is done
 #pragma unroll
-        for (int j = 0; j < 16; ++j) S[j] = acc[j];
+        for (int j = 0; j < kCombineCols; ++j) S[j] = acc[j];
     }
-    if (ST) {
-        float* dst = ST + (((size_t)b * H + h) * 128 + k) * 128 + j0;
+    if (ST)
 #pragma unroll
-        for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-    }
+        for (int j = 0; j < kCombineCols; ++j) ST[(((size_t)b * H + h) * 128 + k) * 128 + j0 + j] = S[j];
 }
 
 cudaError_t launch_piece_plan(const int32_t* cu, int rows, int T, int TT, int L, int Pmax, int32_t* piece_cu,
@@ -1398,8 +1417,9 @@ cudaError_t launch_seg_combine(const float* S0, float* ST, const float* sloc, co
     cudaError_t e = cudaFuncSetAttribute(seg_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCombineSmem);
     if (e != cudaSuccess) return e;
     timing_pre(st, K_SEG_COMBINE);
-    seg_combine_kernel<<<dim3(rows, H, 8), 128, kCombineSmem, st>>>(S0, ST, sloc, M, sstart, H, row_piece,
-                                                                     reverse ? 1 : 0);
+    static_assert(kCombineCols == 4, "one float4 of state columns per thread");
+    seg_combine_kernel<<<dim3(rows, H, 128 / kCombineCols), 128, kCombineSmem, st>>>(S0, ST, sloc, M, sstart, H,
+                                                                                    row_piece, reverse ? 1 : 0);
     timing_post(st);
     return cudaGetLastError();
 }

@@ -130,8 +130,9 @@ size_t kda_bwd_workspace_size(const kda_dims* dims, int chunk_size);
  * Requirements: B,T,H >= 1; 16 <= K,V <= 128 and multiples of 16 (the pages
  * reject head dims below 16); N >= 1.
  * Paths:
- *   - bf16 with K == V == 128 and 16-byte aligned q, k, v, g_raw, out and
- *     final_state (and dout, dv for kda_bwd) runs on the tcgen05 tensor-core path.  Its 16-token
+ *   - bf16 with K == V == 128 and 16-byte aligned q, k, v, g_raw, out,
+ *     initial_state and final_state (and dout, dv, dfinal_state and
+ *     dinitial_state for kda_bwd) runs on the tcgen05 tensor-core path.  Its 16-token
  *     sub-block factorisation of the decay stays inside fp32 range only for
  *     |lower_bound| <= 5.  With the lower-bounded gate that is required of
  *     both directions.

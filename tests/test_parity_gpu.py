@@ -617,3 +617,24 @@ def test_segmented_backward_long_row_few_heads():
         assert rel_err(g[n][:, :, heads], r[n], "bf16") <= 2e-2, n
     assert rel_err(g["dinitial_state"][:, heads], r["dinitial_state"], "bf16") <= 2e-2
     assert rel_err(g["da_log"][heads], r["da_log"], "bf16") <= 2e-2
+
+
+def test_unaligned_state_buffers_take_the_simt_path():
+    """fp32 states at an address that is not a multiple of 16 bytes: the tensor-core path moves states
+    16 bytes at a time, so kda_fwd / kda_bwd run such calls on the SIMT path, still against the
+    oracle, and the segmented entry refuses them."""
+    import gated_delta_rule_sm_gb300 as kda
+    from gated_delta_rule_sm_gb300._lib import KdaError
+    w = Workload("t", B=1, T=150, H=2, K=128, V=128, initial_state=True, backward=True, seed=85)
+    x = make_inputs(w, device=DEV)
+    n = x["initial_state"].numel()
+    buf = torch.empty(n + 1, dtype=torch.float32, device=DEV)
+    buf[1:].copy_(x["initial_state"].reshape(-1))
+    x["initial_state"] = buf[1:].view_as(x["initial_state"])      # 4 bytes past a 16-byte boundary
+    assert x["initial_state"].data_ptr() % 16 == 4
+    names = _launched(lambda: _check_fwd(x, "bf16"))
+    assert "kda_intra_tc" not in names and "kda_chain_fwd_simt" in names, names
+    names = _launched(lambda: _check_bwd(x, "bf16"))
+    assert "kda_grad_tc" not in names and "kda_grad_simt" in names, names
+    with pytest.raises(KdaError):
+        gpu_fwd(x, segments=2)
