@@ -289,12 +289,8 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
                      : "memory");
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(dUg)), "r"(64u * V * 4u)
                      : "memory");
-        // the record fields phase 2 reads row by row from global memory: Qg and Kd (adjacent), Kg,
-        // and Gamma, q_hat, k_hat (adjacent), requested now so they sit in L2 by then
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(rec + L.Qg)),
-                     "r"(2u * 64u * K * 4u) : "memory");
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(rec + L.Kg)),
-                     "r"(64u * K * 4u) : "memory");
+        // the record fields phase 2 reads row by row from global memory, Gamma, q_hat, k_hat (adjacent),
+        // requested now so they sit in L2 by then (Qg, Kg and Kd are formed from them where needed)
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(rec + L.G)),
                      "r"(3u * 64u * K * 4u) : "memory");
     }
@@ -554,11 +550,17 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
-    // Gamma_last gathers exp(Gamma_last) rowsum(dS_end * S0) and sum_t dKd Kd
+    // Gamma_last gathers exp(Gamma_last) rowsum(dS_end * S0) and sum_t dKd Kd, with
+    // Kd = k_hat exp(Gamma_last - Gamma) formed exactly as the combine below forms it (the two
+    // terms cancel in dGamma, so both take the same rounded Kd)
     float* sgl = sred + 64;
     if (tid < K) {
+        const float* Gr = rec + L.G;
+        const float* khr = rec + L.kh;
+        const float gl = Gr[63 * K + tid];
         float acc = rec[L.gC + tid] * dgc;
-        for (int t = 0; t < 64; ++t) acc += dKdm[t * P128 + tid] * rec[L.Kd + t * K + tid];
+#pragma unroll 8
+        for (int t = 0; t < 64; ++t) acc += dKdm[t * P128 + tid] * (khr[t * K + tid] * __expf(gl - Gr[t * K + tid]));
         sgl[tid] = acc;
     }
     // dbeta_s = sum_t N[t][s] dT[t][s];  dN = dT Diag(beta)
@@ -762,8 +764,9 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     float* sdq = dQg;     // in place: the owning thread reads then overwrites
     float* sdk = dKg;
     float* sdG = dKdm;
-    // the record rows of block b + 1 are fetched while block b is combined (global loads: L2 latency)
-    float2 G[2][2], Q[2][2], Kk[2][2], QG[2][2], KG[2][2], KD[2][2];
+    // the record rows of block b + 1 are fetched while block b is combined (global loads: L2 latency);
+    // Qg = q_hat e^Gamma, Kg = k_hat e^Gamma and Kd = k_hat e^(Gamma_last - Gamma) are formed here
+    float2 G[2][2], Q[2][2], Kk[2][2];
     auto fetch = [&](int b, int buf) {
         int r0, c0;
         frag_rc(lane, 0, wm0, 64 * (warp & 1) + 8 * b, r0, c0);
@@ -773,9 +776,6 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
             G[buf][hh] = *reinterpret_cast<const float2*>(Gm + gi);
             Q[buf][hh] = *reinterpret_cast<const float2*>(qh + gi);
             Kk[buf][hh] = *reinterpret_cast<const float2*>(kh + gi);
-            QG[buf][hh] = *reinterpret_cast<const float2*>(rec + L.Qg + gi);
-            KG[buf][hh] = *reinterpret_cast<const float2*>(rec + L.Kg + gi);
-            KD[buf][hh] = *reinterpret_cast<const float2*>(rec + L.Kd + gi);
         }
     };
     fetch(0, 0);
@@ -793,9 +793,8 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
             const int r = r0 + 8 * hh, cc = c0 + lo;
             const float g = lo ? G[cur][hh].y : G[cur][hh].x, gc = lo ? Gc.y : Gc.x;
             const float q = lo ? Q[cur][hh].y : Q[cur][hh].x, k = lo ? Kk[cur][hh].y : Kk[cur][hh].x;
-            const float qg = lo ? QG[cur][hh].y : QG[cur][hh].x, kg = lo ? KG[cur][hh].y : KG[cur][hh].x;
-            const float kd = lo ? KD[cur][hh].y : KD[cur][hh].x;
             const float eG = __expf(g), eD = __expf(gc - g);
+            const float qg = q * eG, kg = k * eG, kd = k * eD;
             const float vQg = dQg[r * P128 + cc], vKg = dKg[r * P128 + cc], vKd = dKdm[r * P128 + cc];
             const float dq = fq[b][e] + vQg * eG;
             const float dk = fkl[b][e] + fkr[b][e] + vKg * eG + vKd * eD;
