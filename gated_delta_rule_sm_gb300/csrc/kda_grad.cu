@@ -684,27 +684,47 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) fq[b][e] = fkl[b][e] = fkr[b][e] = 0.f;
     const int bt = warp >> 1;   // sub-block of this warp's rows
-    for (int j = 0; j <= (sp ? bt - 1 : bt); ++j) {
+    {
+        // Gamma at this thread's fragment elements (the same for every j), loaded once; Gamma at the
+        // end of sub-block j for its columns, loaded before the sub-block's products so the L2
+        // latency hides behind them
+        float grow[8][4];
 #pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-            const int n0 = 64 * (warp & 1) + 32 * hb;
-            float dq[4][4], dk[4][4];
+        for (int b = 0; b < 8; ++b) {
+            int r0, c0;
+            frag_rc(lane, 0, wm0, 64 * (warp & 1) + 8 * b, r0, c0);   // (r0, c0 + e), (r0 + 8, c0 + e)
+            const float2 x0 = *reinterpret_cast<const float2*>(Gm + r0 * K + c0);
+            const float2 x1 = *reinterpret_cast<const float2*>(Gm + (r0 + 8) * K + c0);
+            grow[b][0] = x0.x; grow[b][1] = x0.y; grow[b][2] = x1.x; grow[b][3] = x1.y;
+        }
+        for (int j = 0; j <= (sp ? bt - 1 : bt); ++j) {
+            float2 gend[8];
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
+            for (int b = 0; b < 8; ++b) {
+                int r0, c0;
+                frag_rc(lane, 0, wm0, 64 * (warp & 1) + 8 * b, r0, c0);
+                gend[b] = *reinterpret_cast<const float2*>(Gm + (16 * j + 15) * K + c0);
+            }
 #pragma unroll
-                for (int e = 0; e < 4; ++e) dq[b][e] = dk[b][e] = 0.f;
-            mma_strip3_pair<4>(dq, dk, Tile{dA, P64, 1}, Tile{dB, P64, 1}, Tile{R, P128, 1}, wm0, n0, 16 * j,
-                               16 * j + 16, lane);
+            for (int hb = 0; hb < 2; ++hb) {
+                const int n0 = 64 * (warp & 1) + 32 * hb;
+                float dq[4][4], dk[4][4];
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
+                for (int b = 0; b < 4; ++b)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    int r, cc;
-                    frag_rc(lane, e, wm0, n0 + 8 * b, r, cc);
-                    const float l = __expf(Gm[r * K + cc] - Gm[(16 * j + 15) * K + cc]);
-                    fq[4 * hb + b][e] += l * dq[b][e];
-                    fkl[4 * hb + b][e] += l * dk[b][e];
-                }
+                    for (int e = 0; e < 4; ++e) dq[b][e] = dk[b][e] = 0.f;
+                mma_strip3_pair<4>(dq, dk, Tile{dA, P64, 1}, Tile{dB, P64, 1}, Tile{R, P128, 1}, wm0, n0, 16 * j,
+                                   16 * j + 16, lane);
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int bb = 4 * hb + b;
+                        const float l = __expf(grow[bb][e] - ((e & 1) ? gend[bb].y : gend[bb].x));
+                        fq[bb][e] += l * dq[b][e];
+                        fkl[bb][e] += l * dk[b][e];
+                    }
+            }
         }
     }
     // dk_R: rows s of this warp's sub-block bt; sum over t >= 16 bt.  One k-step loads and splits the
@@ -719,8 +739,36 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) fkr[b][e] = 0.f;
         }
+        // the record values of the next k-step (Gamma, q_hat, k_hat at rows t1, t2 and this thread's
+        // eight columns) are loaded while the current step runs its products
+        float ng[2][8], nq[2][8], nk[2][8];
+        auto fetch_step = [&](int k0) {
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                const int cn = 64 * (warp & 1) + 8 * b + g;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int t = k0 + qd + 4 * i;
+                    ng[i][b] = Gm[t * K + cn];
+                    nq[i][b] = qh[t * K + cn];
+                    nk[i][b] = kh[t * K + cn];
+                }
+            }
+        };
+        const int kfirst = sp ? 16 * j + 16 : 16 * j;
+        if (kfirst < 64) fetch_step(kfirst);
 #pragma unroll 1
-        for (int k0 = sp ? 16 * j + 16 : 16 * j; k0 < 64; k0 += 8) {
+        for (int k0 = kfirst; k0 < 64; k0 += 8) {
+            float cg[2][8], cq[2][8], ck[2][8];
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    cg[i][b] = ng[i][b];
+                    cq[i][b] = nq[i][b];
+                    ck[i][b] = nk[i][b];
+                }
+            if (k0 + 8 < 64) fetch_step(k0 + 8);
             uint32_t aAh[4], aAl[4], aBh[4], aBl[4];
             // A(m = s, k = t) = dA[t][s] (transposed access), rows s = wm0 + ...
             split_tf32(dA[(k0 + qd) * P64 + wm0 + g], aAh[0], aAl[0]);
@@ -731,16 +779,14 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
             split_tf32(dB[(k0 + qd) * P64 + wm0 + g + 8], aBh[1], aBl[1]);
             split_tf32(dB[(k0 + qd + 4) * P64 + wm0 + g], aBh[2], aBl[2]);
             split_tf32(dB[(k0 + qd + 4) * P64 + wm0 + g + 8], aBh[3], aBl[3]);
-            const int t1 = k0 + qd, t2 = k0 + qd + 4;
 #pragma unroll
             for (int b = 0; b < 8; ++b) {
-                const int cn = 64 * (warp & 1) + 8 * b + g;
                 uint32_t bqh[2], bql[2], bkh[2], bkl[2];
-                const float l1 = __expf(Gm[t1 * K + cn] - gref[b]), l2 = __expf(Gm[t2 * K + cn] - gref[b]);
-                split_tf32(qh[t1 * K + cn] * l1, bqh[0], bql[0]);
-                split_tf32(qh[t2 * K + cn] * l2, bqh[1], bql[1]);
-                split_tf32(kh[t1 * K + cn] * l1, bkh[0], bkl[0]);
-                split_tf32(kh[t2 * K + cn] * l2, bkh[1], bkl[1]);
+                const float l1 = __expf(cg[0][b] - gref[b]), l2 = __expf(cg[1][b] - gref[b]);
+                split_tf32(cq[0][b] * l1, bqh[0], bql[0]);
+                split_tf32(cq[1][b] * l2, bqh[1], bql[1]);
+                split_tf32(ck[0][b] * l1, bkh[0], bkl[0]);
+                split_tf32(ck[1][b] * l2, bkh[1], bkl[1]);
                 mma1688(fkr[b], aAl, bqh);
                 mma1688(fkr[b], aAh, bql);
                 mma1688(fkr[b], aAh, bqh);
