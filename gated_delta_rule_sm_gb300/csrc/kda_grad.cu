@@ -167,6 +167,8 @@ constexpr int O_DY = O_DU + 64 * P32;       // [64][P32]   dY slice
 constexpr int O_BETA = O_DY + 64 * P32;     // [64]
 constexpr int O_GRAW = O_DO + 64 * P64;    // bf16 [64][128] g_raw tile, phase 2 (after dB: tmp is dead)
 static_assert(O_GRAW >= O_DS + 64 * P128 && O_GRAW + 64 * 128 / 2 <= O_BETA, "g_raw tile inside the free tail");
+constexpr int O_GPART = O_GRAW + 64 * 128 / 2;   // [4][128] column partials of sum_t dKd Kd, phase 2
+static_assert(O_GPART + 4 * 128 <= O_BETA, "partials inside the free tail");
 static_assert(2 * 16 * 256 <= 64 * P128 && 16 * 256 <= 64 * P64, "diagonal-pass scratch inside the R and N tiles");
 constexpr int O_RED = O_BETA + 64;          // [64] dbeta, [128] Gamma_last gradient, [8] block sums, [256] dt_bias parts
 constexpr int O_MBAR = O_RED + 64 + 128 + 8 + 256;   // 8-byte mbarrier + TMEM slot (4 floats)
@@ -550,19 +552,10 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
-    // Gamma_last gathers exp(Gamma_last) rowsum(dS_end * S0) and sum_t dKd Kd, with
-    // Kd = k_hat exp(Gamma_last - Gamma) formed exactly as the combine below forms it (the two
-    // terms cancel in dGamma, so both take the same rounded Kd)
+    // Gamma_last gathers exp(Gamma_last) rowsum(dS_end * S0) and sum_t dKd Kd; the combine below
+    // forms the second sum (partials per 16-row block in sgpart) with the Kd it uses itself
     float* sgl = sred + 64;
-    if (tid < K) {
-        const float* Gr = rec + L.G;
-        const float* khr = rec + L.kh;
-        const float gl = Gr[63 * K + tid];
-        float acc = rec[L.gC + tid] * dgc;
-#pragma unroll 8
-        for (int t = 0; t < 64; ++t) acc += dKdm[t * P128 + tid] * (khr[t * K + tid] * __expf(gl - Gr[t * K + tid]));
-        sgl[tid] = acc;
-    }
+    float* sgpart = sm + O_GPART;   // [4][128]
     // dbeta_s = sum_t N[t][s] dT[t][s];  dN = dT Diag(beta)
     float* sdbeta = sred;
     if (tid < 64) {
@@ -825,6 +818,16 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         }
     };
     fetch(0, 0);
+    float2 Gcs[8];   // Gamma_last at this thread's columns
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        int r0, c0;
+        frag_rc(lane, 0, wm0, 64 * (warp & 1) + 8 * b, r0, c0);
+        Gcs[b] = *reinterpret_cast<const float2*>(Gm + 63 * K + c0);
+    }
+    // the Gamma_last gradient's sum_t dKd Kd, per column over this warp's 16 rows (the same rounded Kd
+    // as the per-token term of dGamma, with which it cancels)
+    float csum[8][2];
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
         const int cur = b & 1;
@@ -832,7 +835,8 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         const int n0 = 64 * (warp & 1) + 8 * b;
         int r0, c0;
         frag_rc(lane, 0, wm0, n0, r0, c0);   // elements (r0, c0 + e), (r0 + 8, c0 + e), e = 0, 1
-        const float2 Gc = *reinterpret_cast<const float2*>(Gm + 63 * K + c0);
+        const float2 Gc = Gcs[b];
+        csum[b][0] = csum[b][1] = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int hh = e >> 1, lo = e & 1;
@@ -848,9 +852,24 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
             sdq[r * P128 + cc] = dq;
             sdk[r * P128 + cc] = dk;
             sdG[r * P128 + cc] = dG;
+            csum[b][lo] += vKd * kd;
         }
     }
+    // column sums over the warp's rows (lanes of equal lane % 4 share columns), one partial per
+    // row block of 16 and column
+#pragma unroll
+    for (int b = 0; b < 8; ++b)
+#pragma unroll
+        for (int lo = 0; lo < 2; ++lo) {
+            float v = csum[b][lo];
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            if (lane < 4) sgpart[(warp >> 1) * K + 64 * (warp & 1) + 8 * b + 2 * lane + lo] = v;
+        }
     __syncthreads();
+    if (tid < K)
+        sgl[tid] = rec[L.gC + tid] * dgc + sgpart[tid] + sgpart[K + tid] + sgpart[2 * K + tid] + sgpart[3 * K + tid];
     if (sp) {
         // scratch: the R tile's area (dead since the bilinear forms) and N's (dead since dL)
         diag_pairs(Gm, kh, qh, dA, dB, sdq, sdk, sdG, R, R + 16 * 256, sN, tid);
