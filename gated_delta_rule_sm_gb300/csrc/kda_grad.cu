@@ -32,6 +32,13 @@ struct Tile {
     __device__ __forceinline__ float at(int r, int c) const { return p[r * rs + c * cs]; }
 };
 
+// A bf16 tile read as fp32 (exact; tf32 holds every bf16 value).
+struct TileH {
+    const __nv_bfloat16* p;
+    int rs, cs;
+    __device__ __forceinline__ float at(int r, int c) const { return __bfloat162float(p[r * rs + c * cs]); }
+};
+
 // d[b] (16 x 8 blocks at rows m0, cols n0 + 8 b, b < NB) += sum_k A(m, k) B(k, n): one A fragment per
 // k-step serves the whole strip; the k-loop stays rolled to keep the kernel's code small.
 template <int NB>
@@ -80,8 +87,8 @@ __device__ __forceinline__ void mma_strip3(float (&d)[NB][4], const Tile& A, con
 }
 
 // Strip with the left operand split (d += A_lo B + A_hi B): for a right operand that is exact in tf32.
-template <int NB>
-__device__ __forceinline__ void mma_strip_splitA(float (&d)[NB][4], const Tile& A, const Tile& B, int m0, int n0,
+template <int NB, class TB>
+__device__ __forceinline__ void mma_strip_splitA(float (&d)[NB][4], const Tile& A, const TB& B, int m0, int n0,
                                                  int k_lo, int k_hi, int lane) {
     const int g = lane >> 2, q = lane & 3;
 #pragma unroll 1
@@ -993,11 +1000,12 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
 namespace {
 constexpr int PB_A = 0;                  // [64][P64]   Aqk
 constexpr int PB_Q = PB_A + 64 * P64;    // [64][P128]  Qg
-constexpr int PB_D = PB_Q + 64 * P128;   // [64][P128]  dO
-constexpr int PB_FLOATS = PB_D + 64 * P128;
+constexpr int PB_D = PB_Q + 64 * P128;   // bf16 [64][PD16]  dO (exact, as loaded)
+constexpr int PD16 = 136;                // bf16 row stride: 272 bytes, 16-byte aligned, rows 4 banks apart
+constexpr int PB_FLOATS = PB_D + 64 * PD16 / 2;
 }  // namespace
 
-__global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) {
+__global__ void __launch_bounds__(256, 3) bwd_pre_kernel(Params p, uint8_t* bw) {
     extern __shared__ float sm[];
     const int c = blockIdx.x, h = blockIdx.y;
     if (c >= p.chunk_off[p.N]) return;
@@ -1012,7 +1020,7 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) 
     uint8_t* out = bw + ((size_t)c * H + h) * bwrec::BYTES;
     float* sA = sm + PB_A;
     float* sQ = sm + PB_Q;
-    float* sD = sm + PB_D;
+    __nv_bfloat16* sD = reinterpret_cast<__nv_bfloat16*>(sm + PB_D);
     const float scale = p.scale;
 
     for (int i = tid; i < 64 * K / 4; i += 256) {
@@ -1023,18 +1031,14 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) 
         const int t = i >> 4, s4 = (i & 15) * 4;
         cp_async16(sA + t * P64 + s4, rec + L.A + t * 64 + s4);
     }
-    for (int i = tid; i < 64 * V / 8; i += 256) {
+    for (int i = tid; i < 64 * V / 8; i += 256) {   // dO rows as they are (bf16), zero past the segment
         const int t = i >> 4, j8 = (i & 15) * 8;
-        float f[8];
-        if (t < len) {
-            const size_t gi = ((size_t)(tok0 + t) * H + h) * V + j8;
-            bf16x8_to_f32(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + gi), f);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sD[t * P128 + j8 + e] = f[e];
+        if (t < len)
+            cp_async16(reinterpret_cast<float*>(sD + t * PD16 + j8),
+                       reinterpret_cast<const float*>(static_cast<const __nv_bfloat16*>(p.dout) +
+                                                      ((size_t)(tok0 + t) * H + h) * V + j8));
+        else
+            *reinterpret_cast<uint4*>(sD + t * PD16 + j8) = make_uint4(0u, 0u, 0u, 0u);
     }
     // Chain operands: Kd and -W as bf16 hi + lo [64 t][128 c] K-major tiles (one slot for both chains)
     auto put_split8 = [](uint8_t* base, uint32_t o, uint32_t lo_off, const float* v, float sg) {
@@ -1082,7 +1086,7 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) 
         for (int b = 0; b < 8; ++b)
 #pragma unroll
             for (int e = 0; e < 4; ++e) d[b][e] = 0.f;
-        mma_strip_splitA<8>(d, Tile{sA, 1, P64}, Tile{sD, P128, 1}, m0, n0, m0, 64, lane);
+        mma_strip_splitA<8>(d, Tile{sA, 1, P64}, TileH{sD, PD16, 1}, m0, n0, m0, 64, lane);
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
             int r, cc;
@@ -1102,7 +1106,7 @@ __global__ void __launch_bounds__(256, 2) bwd_pre_kernel(Params p, uint8_t* bw) 
             for (int b = 0; b < 8; ++b)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) a1[b][e] = 0.f;
-            mma_strip_splitA<8>(a1, Tile{sQ, 1, P128}, Tile{sD, P128, 1}, m0, 64 * half, 0, 64, lane);
+            mma_strip_splitA<8>(a1, Tile{sQ, 1, P128}, TileH{sD, PD16, 1}, m0, 64 * half, 0, 64, lane);
 #pragma unroll
             for (int b = 0; b < 8; ++b) {
                 int r, cc;
