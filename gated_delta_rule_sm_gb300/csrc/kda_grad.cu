@@ -109,6 +109,60 @@ __device__ __forceinline__ void mma_strip_splitA(float (&d)[NB][4], const Tile& 
     }
 }
 
+// bf16 warp MMA, 16 x 8 x 16, fp32 accumulate.  Fragments (g = lane / 4, q = lane % 4): A words
+// (row g, k 2q..2q+1), (row g + 8, k 2q..), (row g, k 2q + 8..), (row g + 8, k 2q + 8..); B words
+// (k 2q..2q+1, col g), (k 2q + 8.., col g); the first element of a pair in the low half.  C as for
+// the tf32 shape.
+__device__ __forceinline__ void mma16816(float* d, const uint32_t* a, const uint32_t* b) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// (x0, x1) as bf16 pairs hi = bf16(x), lo = bf16(x - hi): hi + lo carries 16 significant bits.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// mma_strip3_pair on bf16 halves: K = 16 per instruction, products hi*hi + hi*lo + lo*hi (relative
+// error ~1e-5, as the backward chains' split products).  k_hi - k_lo a multiple of 16.
+template <int NB>
+__device__ __forceinline__ void mma_strip3_pair_bf16(float (&d1)[NB][4], float (&d2)[NB][4], const Tile& A1,
+                                                     const Tile& A2, const Tile& B, int m0, int n0, int k_lo,
+                                                     int k_hi, int lane) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll 1
+    for (int k0 = k_lo; k0 < k_hi; k0 += 16) {
+        uint32_t h1[4], l1[4], h2[4], l2[4];
+        const int rr[4] = {m0 + g, m0 + g + 8, m0 + g, m0 + g + 8};
+        const int kk[4] = {k0 + 2 * q, k0 + 2 * q, k0 + 2 * q + 8, k0 + 2 * q + 8};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            split_bf16x2(A1.at(rr[i], kk[i]), A1.at(rr[i], kk[i] + 1), h1[i], l1[i]);
+            split_bf16x2(A2.at(rr[i], kk[i]), A2.at(rr[i], kk[i] + 1), h2[i], l2[i]);
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const int n = n0 + 8 * b + g;
+            uint32_t bh[2], bl[2];
+            split_bf16x2(B.at(k0 + 2 * q, n), B.at(k0 + 2 * q + 1, n), bh[0], bl[0]);
+            split_bf16x2(B.at(k0 + 2 * q + 8, n), B.at(k0 + 2 * q + 9, n), bh[1], bl[1]);
+            mma16816(d1[b], l1, bh);
+            mma16816(d1[b], h1, bl);
+            mma16816(d1[b], h1, bh);
+            mma16816(d2[b], l2, bh);
+            mma16816(d2[b], h2, bl);
+            mma16816(d2[b], h2, bh);
+        }
+    }
+}
+
 // Split-precision strip for two left operands sharing the right one: d1 += A1 B, d2 += A2 B with
 // hi*hi + hi*lo + lo*hi products.
 template <int NB>
@@ -713,7 +767,7 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
                 for (int b = 0; b < 4; ++b)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) dq[b][e] = dk[b][e] = 0.f;
-                mma_strip3_pair<4>(dq, dk, Tile{dA, P64, 1}, Tile{dB, P64, 1}, Tile{R, P128, 1}, wm0, n0, 16 * j,
+                mma_strip3_pair_bf16<4>(dq, dk, Tile{dA, P64, 1}, Tile{dB, P64, 1}, Tile{R, P128, 1}, wm0, n0, 16 * j,
                                    16 * j + 16, lane);
 #pragma unroll
                 for (int b = 0; b < 4; ++b)
