@@ -32,11 +32,10 @@ struct Tile {
     __device__ __forceinline__ float at(int r, int c) const { return p[r * rs + c * cs]; }
 };
 
-// A bf16 tile read as fp32 (exact; tf32 holds every bf16 value).
+// A bf16 tile: element (r, c) at p[r * rs + c * cs].
 struct TileH {
     const __nv_bfloat16* p;
     int rs, cs;
-    __device__ __forceinline__ float at(int r, int c) const { return __bfloat162float(p[r * rs + c * cs]); }
 };
 
 // d[b] (16 x 8 blocks at rows m0, cols n0 + 8 b, b < NB) += sum_k A(m, k) B(k, n): one A fragment per
@@ -87,8 +86,8 @@ __device__ __forceinline__ void mma_strip3(float (&d)[NB][4], const Tile& A, con
 }
 
 // Strip with the left operand split (d += A_lo B + A_hi B): for a right operand that is exact in tf32.
-template <int NB, class TB>
-__device__ __forceinline__ void mma_strip_splitA(float (&d)[NB][4], const Tile& A, const TB& B, int m0, int n0,
+template <int NB>
+__device__ __forceinline__ void mma_strip_splitA(float (&d)[NB][4], const Tile& A, const Tile& B, int m0, int n0,
                                                  int k_lo, int k_hi, int lane) {
     const int g = lane >> 2, q = lane & 3;
 #pragma unroll 1
@@ -159,6 +158,39 @@ __device__ __forceinline__ void mma_strip3_pair_bf16(float (&d1)[NB][4], float (
             mma16816(d2[b], l2, bh);
             mma16816(d2[b], h2, bl);
             mma16816(d2[b], h2, bh);
+        }
+    }
+}
+
+// mma_strip_splitA on bf16 halves for a bf16 right operand (exact): d += A_lo B + A_hi B with K = 16
+// per instruction; A's hi + lo carries 16 significant bits (relative error ~1e-5).  k_hi - k_lo a
+// multiple of 16.
+template <int NB>
+__device__ __forceinline__ void mma_strip_splitA_bf16(float (&d)[NB][4], const Tile& A, const TileH& B, int m0,
+                                                      int n0, int k_lo, int k_hi, int lane) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll 1
+    for (int k0 = k_lo; k0 < k_hi; k0 += 16) {
+        uint32_t ah[4], al[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = m0 + g + 8 * (i & 1), k = k0 + 2 * q + 8 * (i >> 1);
+            split_bf16x2(A.at(r, k), A.at(r, k + 1), ah[i], al[i]);
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const int n = n0 + 8 * b + g;
+            const __nv_bfloat16* col = B.p + n * B.cs;
+            uint32_t bb[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int k = k0 + 2 * q + 8 * i;
+                const uint32_t lo16 = __bfloat16_as_ushort(col[k * B.rs]);
+                const uint32_t hi16 = __bfloat16_as_ushort(col[(k + 1) * B.rs]);
+                bb[i] = lo16 | (hi16 << 16);
+            }
+            mma16816(d[b], al, bb);
+            mma16816(d[b], ah, bb);
         }
     }
 }
@@ -1140,7 +1172,7 @@ __global__ void __launch_bounds__(256, 3) bwd_pre_kernel(Params p, uint8_t* bw) 
         for (int b = 0; b < 8; ++b)
 #pragma unroll
             for (int e = 0; e < 4; ++e) d[b][e] = 0.f;
-        mma_strip_splitA<8>(d, Tile{sA, 1, P64}, TileH{sD, PD16, 1}, m0, n0, m0, 64, lane);
+        mma_strip_splitA_bf16<8>(d, Tile{sA, 1, P64}, TileH{sD, PD16, 1}, m0, n0, m0, 64, lane);
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
             int r, cc;
@@ -1160,7 +1192,7 @@ __global__ void __launch_bounds__(256, 3) bwd_pre_kernel(Params p, uint8_t* bw) 
             for (int b = 0; b < 8; ++b)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) a1[b][e] = 0.f;
-            mma_strip_splitA<8>(a1, Tile{sQ, 1, P128}, TileH{sD, PD16, 1}, m0, 64 * half, 0, 64, lane);
+            mma_strip_splitA_bf16<8>(a1, Tile{sQ, 1, P128}, TileH{sD, PD16, 1}, m0, 64 * half, 0, 64, lane);
 #pragma unroll
             for (int b = 0; b < 8; ++b) {
                 int r, cc;
