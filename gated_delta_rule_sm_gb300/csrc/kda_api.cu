@@ -119,18 +119,30 @@ struct TcBwdPlan {
     size_t off_bwrec;   // reverse-chain records
     size_t off_u, off_du;   // U and dU per (chunk, head), written by the two chains
     size_t off_diag;    // unbounded gate: diagonal sub-blocks for the record pass (0 otherwise)
+    size_t off_pad;     // K = V = 64 heads: three zero-padded 128 x 128 states per (row, head) (0 otherwise)
     size_t total;
 };
 
+// The tensor-core backward also takes bf16 K = V = 64 heads under the lower-bounded gate: every
+// per-chunk record and tile is laid out for 128 channels, the record pass loads the heads as
+// 128-channel tiles whose upper half is zero, and the chains run on zero-padded 128 x 128 states.
+static bool tc_bwd_eligible(const Shape& s) {
+    return tc_eligible(s) || (s.dtype == KDA_BF16 && s.K == 64 && s.V == 64 && s.gate == KDA_GATE_LOWER_BOUNDED);
+}
+
 static TcBwdPlan plan_tc_bwd(const Shape& s) {
     TcBwdPlan w;
-    w.simt = plan_simt(s, true);
+    Shape s128 = s;   // the kernels' internal layouts are those of 128-channel heads
+    s128.K = s128.V = 128;
+    w.simt = plan_simt(s128, true);
     size_t o = w.simt.total;
     w.off_bwrec = o; o = align_up(o + (size_t)s.NCmax * s.H * bwrec::BYTES);
-    w.off_u = o; o = align_up(o + sizeof(float) * (size_t)s.NCmax * s.H * 64 * s.V);
-    w.off_du = o; o = align_up(o + sizeof(float) * (size_t)s.NCmax * s.H * 64 * s.V);
+    w.off_u = o; o = align_up(o + sizeof(float) * (size_t)s.NCmax * s.H * 64 * s128.V);
+    w.off_du = o; o = align_up(o + sizeof(float) * (size_t)s.NCmax * s.H * 64 * s128.V);
     w.off_diag = 0;
     if (s.gate == KDA_GATE_SOFTPLUS) { w.off_diag = o; o = align_up(o + diag_item_bytes() * s.NCmax * s.H); }
+    w.off_pad = 0;
+    if (s.K != 128) { w.off_pad = o; o = align_up(o + 3 * sizeof(float) * (size_t)s.N * s.H * 128 * 128); }
     w.total = o;
     return w;
 }
@@ -379,8 +391,24 @@ static kda_status bwd_tc(const Shape& s, Params p, void* workspace, size_t works
         KDA_TRY_CUDA(launch_intra_tc(p, nullptr, 1, stream));
     }
     KDA_TRY_CUDA(launch_bwd_pre(p, bw, stream));
+    float* user_dS0 = p.dS0;
+    if (w.off_pad) {   // K = V = 64: the chains take and give zero-padded 128 x 128 states
+        float* pad = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.off_pad);
+        const size_t one = (size_t)s.N * s.H * 128 * 128;
+        const int NH = s.N * s.H;
+        if (p.S0) {
+            KDA_TRY_CUDA(launch_state_pad(p.S0, pad, s.K, s.V, NH, stream));
+            pf.S0 = pad;
+        }
+        if (p.dST) {
+            KDA_TRY_CUDA(launch_state_pad(p.dST, pad + one, s.K, s.V, NH, stream));
+            p.dST = pad + one;
+        }
+        if (p.dS0) p.dS0 = pad + 2 * one;
+    }
     KDA_TRY_CUDA(launch_chain_rec_tc(pf, bw, stream));
     KDA_TRY_CUDA(launch_chain_bwd_tc(p, bw, stream));
+    if (w.off_pad && user_dS0) KDA_TRY_CUDA(launch_state_unpad(p.dS0, user_dS0, s.K, s.V, s.N * s.H, stream));
     KDA_TRY_CUDA(launch_grad_tc(p, stream));
     return KDA_OK;
 }
@@ -417,7 +445,7 @@ size_t kda_bwd_workspace_size(const kda_dims* dims, int chunk_size) {
         check_dims(dims, chunk_size, false, &s) != KDA_OK)
         return 0;
     const size_t a = plan_simt(s, true).total;
-    const size_t b = tc_eligible(s) ? plan_tc_bwd(s).total : 0;
+    const size_t b = tc_bwd_eligible(s) ? plan_tc_bwd(s).total : 0;
     return a > b ? a : b;
 }
 
@@ -478,7 +506,7 @@ kda_status kda_bwd(const kda_dims* dims, const void* q, const void* k, const voi
     p.dout = dout; p.dST = dfinal_state;
     p.dq = dq; p.dk = dk; p.dv = dv; p.dg_raw = dg_raw; p.dbeta_raw = dbeta_raw;
     p.da_log = da_log; p.ddt_bias = ddt_bias; p.dS0 = dinitial_state;
-    if (tc_eligible(s) && tc_gate_ok(s, lower_bound) && tc_inputs_aligned(p))
+    if (tc_bwd_eligible(s) && tc_gate_ok(s, lower_bound) && tc_inputs_aligned(p))
         return bwd_tc(s, p, workspace, workspace_bytes, stream, nullptr);
     const WsPlan w = plan_simt(s, true);
     st = check_ws(workspace, workspace_bytes, w.total);

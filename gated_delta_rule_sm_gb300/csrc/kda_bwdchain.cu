@@ -352,3 +352,44 @@ cudaError_t launch_chain_rec_tc(const Params& p, const uint8_t* bw, cudaStream_t
 }
 
 }  // namespace kda
+
+namespace kda {
+
+// K = V = 64 heads on the tensor-core backward: the chains carry a 128 x 128 state whose upper-left
+// 64 x 64 quarter is the head's state.  The caller's [N, H, K, V] states are copied into zeroed
+// 128 x 128 ones before the chains (pad) and the initial-state gradient copied back after (unpad).
+__global__ void state_pad_kernel(const float* __restrict__ src, float* __restrict__ dst, int K, int V, int NH) {
+    const size_t total = (size_t)NH * 128 * 128;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const int c = (int)(i & 127), r = (int)((i >> 7) & 127);
+        const size_t nh = i >> 14;
+        dst[i] = (src && r < K && c < V) ? src[(nh * K + r) * V + c] : 0.f;
+    }
+}
+
+__global__ void state_unpad_kernel(const float* __restrict__ src, float* __restrict__ dst, int K, int V, int NH) {
+    const size_t total = (size_t)NH * K * V;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const int c = (int)(i % V);
+        const size_t rr = i / V;
+        const int r = (int)(rr % K);
+        const size_t nh = rr / K;
+        dst[i] = src[(nh * 128 + r) * 128 + c];
+    }
+}
+
+cudaError_t launch_state_pad(const float* src, float* dst, int K, int V, int NH, cudaStream_t st) {
+    const size_t total = (size_t)NH * 128 * 128;
+    const int grid = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+    state_pad_kernel<<<grid, 256, 0, st>>>(src, dst, K, V, NH);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_state_unpad(const float* src, float* dst, int K, int V, int NH, cudaStream_t st) {
+    const size_t total = (size_t)NH * K * V;
+    const int grid = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+    state_unpad_kernel<<<grid, 256, 0, st>>>(src, dst, K, V, NH);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

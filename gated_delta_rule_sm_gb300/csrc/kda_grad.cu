@@ -129,6 +129,33 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
     lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+// mma_strip on bf16 halves of both operands (hi*hi + hi*lo + lo*hi, relative error ~1e-5 instead of
+// a single tf32 product's ~5e-4).  k_lo and k_hi - k_lo multiples of 16.
+template <int NB>
+__device__ __forceinline__ void mma_strip3_bf16(float (&d)[NB][4], const Tile& A, const Tile& B, int m0, int n0,
+                                                int k_lo, int k_hi, int lane) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll 1
+    for (int k0 = k_lo; k0 < k_hi; k0 += 16) {
+        uint32_t ah[4], al[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = m0 + g + 8 * (i & 1), k = k0 + 2 * q + 8 * (i >> 1);
+            split_bf16x2(A.at(r, k), A.at(r, k + 1), ah[i], al[i]);
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const int n = n0 + 8 * b + g;
+            uint32_t bh[2], bl[2];
+            split_bf16x2(B.at(k0 + 2 * q, n), B.at(k0 + 2 * q + 1, n), bh[0], bl[0]);
+            split_bf16x2(B.at(k0 + 2 * q + 8, n), B.at(k0 + 2 * q + 9, n), bh[1], bl[1]);
+            mma16816(d[b], al, bh);
+            mma16816(d[b], ah, bl);
+            mma16816(d[b], ah, bh);
+        }
+    }
+}
+
 // mma_strip3_pair on bf16 halves: K = 16 per instruction, products hi*hi + hi*lo + lo*hi (relative
 // error ~1e-5, as the backward chains' split products).  k_hi - k_lo a multiple of 16.
 template <int NB>
@@ -389,14 +416,16 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(rec + L.G)),
                      "r"(3u * 64u * K * 4u) : "memory");
     }
-    if (tid >= 64 && tid < 64 + len) {   // one 256-byte row of dout and of v per token
-        const size_t row = ((size_t)(tok0 + tid - 64) * H + h) * V;
+    if (tid >= 64 && tid < 64 + len) {   // one row of dout and of v per token (256 bytes, or 128 at V = 64)
+        const size_t row = ((size_t)(tok0 + tid - 64) * H + h) * p.V;
         const char* po = reinterpret_cast<const char*>(static_cast<const __nv_bfloat16*>(p.dout) + row);
         const char* pv = reinterpret_cast<const char*>(static_cast<const __nv_bfloat16*>(p.v) + row);
         asm volatile("prefetch.global.L2 [%0];" ::"l"(po));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(po + 128));
         asm volatile("prefetch.global.L2 [%0];" ::"l"(pv));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(pv + 128));
+        if (p.V > 64) {
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(po + 128));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(pv + 128));
+        }
     }
 
     // accumulators over the four 32-column slices of V (register fragments)
@@ -444,8 +473,8 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
             rdu[it] = *reinterpret_cast<const float4*>(dUg + x4_off(r, j0 + j4, 64));
         }
         ro = rv = make_uint4(0u, 0u, 0u, 0u);
-        if (tq < len) {
-            const size_t gi = ((size_t)(tok0 + tq) * H + h) * V + j0 + j8q;
+        if (tq < len && j0 + j8q < p.V) {   // (V = 64 heads: the upper value columns stay zero)
+            const size_t gi = ((size_t)(tok0 + tq) * H + h) * p.V + j0 + j8q;
             ro = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + gi);
             rv = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.v) + gi);
         }
@@ -488,7 +517,7 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
             for (int b = 0; b < 2; ++b)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) d[b][e] = 0.f;
-            mma_strip<2>(d, Tile{sKg, P128, 1}, Tile{sS0, P32, 1}, m0, n0, 0, K, lane);
+            mma_strip3_bf16<2>(d, Tile{sKg, P128, 1}, Tile{sS0, P32, 1}, m0, n0, 0, K, lane);
 #pragma unroll
             for (int b = 0; b < 2; ++b)
 #pragma unroll
@@ -507,7 +536,7 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
             for (int b = 0; b < 2; ++b)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) d[b][e] = 0.f;
-            mma_strip<2>(d, Tile{sN, 1, P64}, Tile{sdU, P32, 1}, m0, n0, m0, 64, lane);
+            mma_strip3_bf16<2>(d, Tile{sN, 1, P64}, Tile{sdU, P32, 1}, m0, n0, m0, 64, lane);
 #pragma unroll
             for (int b = 0; b < 2; ++b)
 #pragma unroll
@@ -520,8 +549,8 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         __syncthreads();
         {   // dv = dY for this slice, from the tile: 32 columns = one 128-byte row segment per 4 threads
             const int r = tid >> 2, c8 = (tid & 3) * 8;
-            if (r < len) {
-                float* dst = p.dv + ((size_t)(tok0 + r) * H + h) * V + j0 + c8;
+            if (r < len && j0 + c8 < p.V) {
+                float* dst = p.dv + ((size_t)(tok0 + r) * H + h) * p.V + j0 + c8;
                 *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(sdY + r * P32 + c8);
                 *reinterpret_cast<float4*>(dst + 4) = *reinterpret_cast<const float4*>(sdY + r * P32 + c8 + 4);
             }
@@ -670,7 +699,7 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         for (int b = 0; b < 4; ++b)
 #pragma unroll
             for (int e = 0; e < 4; ++e) d[b][e] = 0.f;
-        mma_strip<4>(d, Tile{sN, 1, P64}, Tile{dT, P64, 1}, wm0, 32 * (warp & 1), wm0, 64, lane);   // N[t][s], t >= s
+        mma_strip3_bf16<4>(d, Tile{sN, 1, P64}, Tile{dT, P64, 1}, wm0, 32 * (warp & 1), wm0, 64, lane);   // N[t][s], t >= s
 #pragma unroll
         for (int b = 0; b < 4; ++b)
 #pragma unroll
@@ -688,7 +717,7 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         for (int b = 0; b < 4; ++b)
 #pragma unroll
             for (int e = 0; e < 4; ++e) d[b][e] = 0.f;
-        mma_strip<4>(d, Tile{tmp, P64, 1}, Tile{sN, 1, P64}, wm0, 32 * (warp & 1), 0, 64, lane);
+        mma_strip3_bf16<4>(d, Tile{tmp, P64, 1}, Tile{sN, 1, P64}, wm0, 32 * (warp & 1), 0, 64, lane);
         __syncwarp();
 #pragma unroll
         for (int b = 0; b < 4; ++b)
@@ -730,10 +759,10 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     __nv_bfloat16* sgraw = reinterpret_cast<__nv_bfloat16*>(sm + O_GRAW);
     for (int i = tid; i < 64 * 16; i += 256) {
         const int t = i >> 4, c8 = (i & 15) * 8;
-        if (t < len)
+        if (t < len && c8 < p.K)
             cp_async16(reinterpret_cast<float*>(sgraw + t * 128 + c8),
                        reinterpret_cast<const float*>(static_cast<const __nv_bfloat16*>(p.g_raw) +
-                                                      ((size_t)(tok0 + t) * H + h) * K + c8));
+                                                      ((size_t)(tok0 + t) * H + h) * p.K + c8));
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
     // R[s][c] = k_hat[s][c] exp(G_{b(s)+1,c} - Gamma[s][c]) (<= 1), with G_{b+1} = Gamma at the end of
@@ -1016,8 +1045,10 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int cc = lane + 32 * u;
-                p.dq_v[row * K + cc] = rq * (sdq[t * P128 + cc] - qv[w2][u] * sq[w2]);
-                p.dk_v[row * K + cc] = rk * (sdk[t * P128 + cc] - kv[w2][u] * sk[w2]);
+                if (cc < p.K) {   // K = 64 heads: the padded channels are not written
+                    p.dq_v[row * p.K + cc] = rq * (sdq[t * P128 + cc] - qv[w2][u] * sq[w2]);
+                    p.dk_v[row * p.K + cc] = rk * (sdk[t * P128 + cc] - kv[w2][u] * sk[w2]);
+                }
             }
             if (lane == 0) {
                 const float b = sbeta[t];
@@ -1029,8 +1060,9 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
     float alog_part = 0.f;
     {
         const int cc = tid & 127, hf = tid >> 7;
+        const bool ch = cc < p.K;   // a real channel (K = 64 heads are padded to 128)
         const float ea = expf(p.a_log[h]);
-        const float dtbv = p.dt_bias[h * K + cc];
+        const float dtbv = ch ? p.dt_bias[h * p.K + cc] : 0.f;
         float* __restrict__ dgr = p.dg_raw;
         asm volatile("cp.async.wait_group 0;" ::: "memory");
         __syncthreads();
@@ -1038,25 +1070,25 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
             const int t = hf + 2 * u;
-            gv[u] = t < len ? __bfloat162float(sgraw[t * 128 + cc]) : 0.f;
+            gv[u] = t < len && ch ? __bfloat162float(sgraw[t * 128 + cc]) : 0.f;
         }
         float dtb = 0.f;
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
             const int t = hf + 2 * u;
-            if (t < len && sp) {
+            if (t < len && ch && sp) {
                 // g = -e^a softplus(x): dg/dx = -e^a sigmoid(x), dg/da = g
                 const float x = gv[u] + dtbv;
                 const float sg = __fdividef(1.f, 1.f + __expf(-x));
                 const float dx = -sdG[t * P128 + cc] * ea * sg;
-                dgr[((size_t)(tok0 + t) * H + h) * K + cc] = dx;
+                dgr[((size_t)(tok0 + t) * H + h) * p.K + cc] = dx;
                 dtb += dx;
                 alog_part -= sdG[t * P128 + cc] * ea * (fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x))));
-            } else if (t < len) {
+            } else if (t < len && ch) {
                 const float z = ea * (gv[u] + dtbv);
                 const float sg = __fdividef(1.f, 1.f + __expf(-z));   // ~2^-21 relative: ample for dg_raw
                 const float dz = sdG[t * P128 + cc] * p.lb * sg * (1.f - sg);
-                dgr[((size_t)(tok0 + t) * H + h) * K + cc] = dz * ea;
+                dgr[((size_t)(tok0 + t) * H + h) * p.K + cc] = dz * ea;
                 dtb += dz * ea;
                 alog_part += dz * z;
             }
@@ -1064,7 +1096,7 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
         float* sdtb = sred + 64 + 128 + 8;   // [256]
         sdtb[tid] = dtb;
         __syncthreads();
-        if (tid < K) p.part_dtb[((size_t)c * H + h) * K + tid] = sdtb[tid] + sdtb[tid + 128];
+        if (tid < p.K) p.part_dtb[((size_t)c * H + h) * p.K + tid] = sdtb[tid] + sdtb[tid + 128];
     }
     alog_part = warp_sum(alog_part);
     float* sblk = sred + 64 + 128;
@@ -1117,12 +1149,13 @@ __global__ void __launch_bounds__(256, 3) bwd_pre_kernel(Params p, uint8_t* bw) 
         const int t = i >> 4, s4 = (i & 15) * 4;
         cp_async16(sA + t * P64 + s4, rec + L.A + t * 64 + s4);
     }
-    for (int i = tid; i < 64 * V / 8; i += 256) {   // dO rows as they are (bf16), zero past the segment
+    // dO rows as they are (bf16); zero past the segment and, for V = 64 heads, past the value columns
+    for (int i = tid; i < 64 * V / 8; i += 256) {
         const int t = i >> 4, j8 = (i & 15) * 8;
-        if (t < len)
+        if (t < len && j8 < p.V)
             cp_async16(reinterpret_cast<float*>(sD + t * PD16 + j8),
                        reinterpret_cast<const float*>(static_cast<const __nv_bfloat16*>(p.dout) +
-                                                      ((size_t)(tok0 + t) * H + h) * V + j8));
+                                                      ((size_t)(tok0 + t) * H + h) * p.V + j8));
         else
             *reinterpret_cast<uint4*>(sD + t * PD16 + j8) = make_uint4(0u, 0u, 0u, 0u);
     }

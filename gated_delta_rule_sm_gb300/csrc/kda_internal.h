@@ -147,6 +147,10 @@ cudaError_t launch_bwd_pre(const Params& p, uint8_t* bw, cudaStream_t st);
 // zero, only the end state, which is then the segment's transfer matrix.
 enum BwdChainMode { kBwdChainFull = 0, kBwdChainLocal = 1, kBwdChainTransfer = 2 };
 cudaError_t launch_chain_bwd_tc(const Params& p, const uint8_t* bw, cudaStream_t st, int mode = kBwdChainFull);
+// K = V = 64 heads on the tensor-core backward: caller states [NH, K, V] <-> zero-padded [NH, 128, 128]
+// (src == null pads zeros)
+cudaError_t launch_state_pad(const float* src, float* dst, int K, int V, int NH, cudaStream_t st);
+cudaError_t launch_state_unpad(const float* src, float* dst, int K, int V, int NH, cudaStream_t st);
 cudaError_t launch_chain_rec_tc(const Params& p, const uint8_t* bw, cudaStream_t st, int mode = kBwdChainFull);
 
 // tensor-core path (bf16, K = V = 128)

@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(256, 1)
     auto fetch_small = [&](int it) {
         int h2, c2, t02;
         const int len2 = item_tok0(it, h2, c2, t02);
-        if (tid < 128) nx_dtb = p.dt_bias[h2 * 128 + tid];
+        if (tid < 128) nx_dtb = tid < p.K ? p.dt_bias[h2 * p.K + tid] : 0.f;   // K = 64: channels padded
         if (tid < 64 && tid < len2) nx_braw = load_act(p.beta_raw, (size_t)(t02 + tid) * H + h2, KDA_BF16);
     };
     fetch_small(blockIdx.x);
@@ -1246,8 +1246,9 @@ bool tc_inputs_aligned(const Params& p) {
 
 cudaError_t launch_intra_tc(const Params& p, uint8_t* recs, int mode, cudaStream_t st) {
     CUtensorMap mq, mk, mg, mv;
-    if (!head_tile_map(&mq, p.q, p.Hk, p.TT) || !head_tile_map(&mk, p.k, p.Hk, p.TT) ||
-        !head_tile_map(&mg, p.g_raw, p.H, p.TT) || !head_tile_map(&mv, p.v, p.H, p.TT))
+    // K = V = 64 heads load as 128-channel tiles whose upper half the copy fills with zeros
+    if (!head_tile_map(&mq, p.q, p.Hk, p.TT, p.K) || !head_tile_map(&mk, p.k, p.Hk, p.TT, p.K) ||
+        !head_tile_map(&mg, p.g_raw, p.H, p.TT, p.K) || !head_tile_map(&mv, p.v, p.H, p.TT, p.V))
         return cudaErrorInvalidValue;
     const bool sp = p.gate == KDA_GATE_SOFTPLUS;
     auto kern = mode == 0 ? (sp ? intra_tc_kernel<0, true> : intra_tc_kernel<0, false>)

@@ -301,14 +301,16 @@ def test_saved_pair_matches_plain_calls():
 
 @pytest.mark.parametrize("K,H,Hk", [(128, 4, 2), (128, 4, 1), (64, 4, 2)])
 def test_grouped_heads_fwd_bwd(K, H, Hk):
-    """H value heads on Hk key heads (value head h reads key head h // (H // Hk)); K = 128 takes
-    the tensor-core path, K = 64 the SIMT path; dq, dk are summed over each group."""
+    """H value heads on Hk key heads (value head h reads key head h // (H // Hk)); both head sizes
+    take the tensor-core path (K = 64 zero-padded to 128 channels inside the kernels); dq, dk are
+    summed over each group."""
     w = Workload("t", B=2, T=150, H=H, Hk=Hk, K=K, V=K, initial_state=True, backward=True, seed=31 + H + Hk)
     x = make_inputs(w, device=DEV)
     assert tuple(x["q"].shape) == (2, 150, Hk, K)
     _check_fwd(x, "bf16")
     dfinal = 0.1 * torch.randn((2, H, K, K), generator=torch.Generator().manual_seed(5)).to(DEV)
-    _check_bwd(x, "bf16", dfinal=dfinal)
+    names = _launched(lambda: _check_bwd(x, "bf16", dfinal=dfinal))
+    assert {"kda_grad_tc", "kda_chain_bwd_tc", "kda_intra_tc"} <= names and "kda_grad_simt" not in names, names
 
 
 def test_grouped_heads_varlen_and_saved_pair():
@@ -459,6 +461,27 @@ def test_fwd_bf16_k64_tensor_core(case):
                                  initial_state=True, seed=70), device=DEV)
     names = _launched(lambda: _check_fwd(x, "bf16"))
     assert {"kda_intra_tc", "kda_chain_fwd_tc"} <= names and "kda_intra_simt" not in names, names
+
+
+@pytest.mark.parametrize("case", ["rows", "packed", "mild"])
+def test_bwd_bf16_k64_tensor_core(case):
+    """bf16 K = V = 64 heads take the tensor-core backward: the record pass loads 128-channel tiles
+    whose upper half is zero, the chains carry 128 x 128 states padded from the caller's 64 x 64 ones
+    (initial state and final-state gradient in, initial-state gradient out), and the gradient kernel
+    writes only the real channels."""
+    if case == "packed":
+        lens = [1, 63, 64, 65, 130, 0, 17]
+        x = make_inputs(Workload("t", B=1, T=sum(lens), H=3, K=64, V=64, varlen=True, initial_state=True,
+                                 backward=True, seed=86), device=DEV, lengths=lens)
+        n = len(lens)
+    else:
+        x = make_inputs(Workload("t", B=2, T=300, H=3, K=64, V=64, initial_state=True, backward=True,
+                                 g_mean=-4.0 if case == "mild" else 0.0, seed=87), device=DEV)
+        n = 2
+    dfinal = 0.1 * torch.randn((n, 3, 64, 64), generator=torch.Generator().manual_seed(9)).to(DEV)
+    names = _launched(lambda: _check_bwd(x, "bf16", dfinal=dfinal))
+    assert {"kda_intra_tc", "kda_bwd_pre", "kda_chain_rec_tc", "kda_chain_bwd_tc", "kda_grad_tc"} <= names, names
+    assert "kda_grad_simt" not in names and "kda_intra_simt" not in names, names
 
 
 @pytest.mark.parametrize("g_mean,Hk", [(0.0, 0), (4.0, 0), (-6.0, 0), (0.0, 1)])
