@@ -192,10 +192,15 @@ __device__ __forceinline__ void mma_strip3_pair_bf16(float (&d1)[NB][4], float (
 // mma_strip_splitA on bf16 halves for a bf16 right operand (exact): d += A_lo B + A_hi B with K = 16
 // per instruction; A's hi + lo carries 16 significant bits (relative error ~1e-5).  k_hi - k_lo a
 // multiple of 16.
+// B is a row-major [k][n] bf16 tile (B.cs == 1, row stride B.rs elements, a multiple of 8, rows 16-byte
+// aligned): each k-step moves two n-blocks' fragments with one ldmatrix.x4.trans (lanes 8 i .. 8 i + 7
+// address rows k0 + 8 (i % 2) .. + 7 of n-block b + i / 2).  NB even, n0 a multiple of 8.
 template <int NB>
 __device__ __forceinline__ void mma_strip_splitA_bf16(float (&d)[NB][4], const Tile& A, const TileH& B, int m0,
                                                       int n0, int k_lo, int k_hi, int lane) {
+    static_assert(NB % 2 == 0, "n-blocks in pairs");
     const int g = lane >> 2, q = lane & 3;
+    const int mi = lane >> 3, ri = lane & 7;
 #pragma unroll 1
     for (int k0 = k_lo; k0 < k_hi; k0 += 16) {
         uint32_t ah[4], al[4];
@@ -205,19 +210,17 @@ __device__ __forceinline__ void mma_strip_splitA_bf16(float (&d)[NB][4], const T
             split_bf16x2(A.at(r, k), A.at(r, k + 1), ah[i], al[i]);
         }
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            const int n = n0 + 8 * b + g;
-            const __nv_bfloat16* col = B.p + n * B.cs;
-            uint32_t bb[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int k = k0 + 2 * q + 8 * i;
-                const uint32_t lo16 = __bfloat16_as_ushort(col[k * B.rs]);
-                const uint32_t hi16 = __bfloat16_as_ushort(col[(k + 1) * B.rs]);
-                bb[i] = lo16 | (hi16 << 16);
-            }
+        for (int b = 0; b < NB; b += 2) {
+            const __nv_bfloat16* row = B.p + (k0 + 8 * (mi & 1) + ri) * B.rs + n0 + 8 * (b + (mi >> 1));
+            uint32_t bb[4];
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(bb[0]), "=r"(bb[1]), "=r"(bb[2]), "=r"(bb[3])
+                         : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(row)))
+                         : "memory");
             mma16816(d[b], al, bb);
             mma16816(d[b], ah, bb);
+            mma16816(d[b + 1], al, bb + 2);
+            mma16816(d[b + 1], ah, bb + 2);
         }
     }
 }
