@@ -27,6 +27,7 @@ def main(argv=None) -> None:
     ap.add_argument("--B", type=int)
     ap.add_argument("--T", type=int)
     ap.add_argument("--H", type=int)
+    ap.add_argument("--D", type=int, help="head size K = V (64 or 128)")
     ap.add_argument("--dtype", choices=("bf16", "fp32"), help="activation dtype (fp32 runs the SIMT path)")
     ap.add_argument("--Hk", type=int, help="key heads (H a multiple of it; grouped heads)")
     ap.add_argument("--final-state", action="store_true", help="also write the final state")
@@ -46,7 +47,8 @@ def main(argv=None) -> None:
                     help="instead time the W-tap short convolution + SiLU prologue on a q-shaped [B, T, H*K] tensor")
     a = ap.parse_args(argv)
     w = WORKLOADS[a.workload]
-    over = {k: v for k, v in (("B", a.B), ("T", a.T), ("H", a.H), ("dtype", a.dtype), ("Hk", a.Hk)) if v is not None}
+    over = {k: v for k, v in (("B", a.B), ("T", a.T), ("H", a.H), ("dtype", a.dtype), ("Hk", a.Hk), ("K", a.D),
+                              ("V", a.D)) if v is not None}
     if a.final_state:
         over["final_state"] = True
     if over:
