@@ -293,9 +293,9 @@ static kda_status fwd_tc(const Shape& s, Params p, void* ws, size_t ws_bytes, cu
     char* b = static_cast<char*>(ws);
     p.chunk_off = reinterpret_cast<int32_t*>(b + w.off_chunk);
     uint8_t* recs = reinterpret_cast<uint8_t*>(b + w.off_rec);
-    if (saved) {
+    if (saved) {   // the backward record, in the 128-channel layout (K = V = 64 heads padded)
         p.rec = saved;
-        p.rec_stride = RecLayout::make(s.K, s.V).bwd_size;
+        p.rec_stride = RecLayout::make(128, 128).bwd_size;
     }
     if (s.gate == KDA_GATE_SOFTPLUS) p.diag = reinterpret_cast<float*>(b + w.off_diag);
     KDA_TRY_CUDA(launch_plan(p, stream));
@@ -415,8 +415,8 @@ static kda_status bwd_tc(const Shape& s, Params p, void* workspace, size_t works
 
 // Bytes of the record kda_fwd_save keeps (0 when the shape does not take the tensor-core path).
 static size_t saved_bytes_for(const Shape& s) {
-    if (!tc_eligible(s)) return 0;
-    return sizeof(float) * (size_t)s.NCmax * s.H * RecLayout::make(s.K, s.V).bwd_size;
+    if (!tc_bwd_eligible(s)) return 0;
+    return sizeof(float) * (size_t)s.NCmax * s.H * RecLayout::make(128, 128).bwd_size;   // 128-channel layout
 }
 
 }  // namespace kda
@@ -698,7 +698,7 @@ kda_status kda_fwd_save(const kda_dims* dims, const void* q, const void* k, cons
                            initial_state);
     p.out = out;
     p.ST = final_state;
-    if (!tc_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
+    if (!tc_bwd_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
     const size_t need = saved_bytes_for(s);
     if (!saved || saved_bytes < need || (reinterpret_cast<uintptr_t>(saved) % kAlign)) return KDA_ERR_WORKSPACE;
     p.out = out;
@@ -724,7 +724,7 @@ kda_status kda_bwd_saved(const kda_dims* dims, const void* q, const void* k, con
     p.dout = dout; p.dST = dfinal_state;
     p.dq = dq; p.dk = dk; p.dv = dv; p.dg_raw = dg_raw; p.dbeta_raw = dbeta_raw;
     p.da_log = da_log; p.ddt_bias = ddt_bias; p.dS0 = dinitial_state;
-    if (!tc_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
+    if (!tc_bwd_eligible(s) || !tc_gate_ok(s, lower_bound) || !tc_inputs_aligned(p)) return KDA_ERR_UNSUPPORTED;
     const size_t need = saved_bytes_for(s);
     if (!saved || saved_bytes < need || (reinterpret_cast<uintptr_t>(saved) % kAlign)) return KDA_ERR_WORKSPACE;
     return bwd_tc(s, p, workspace, workspace_bytes, stream, static_cast<const float*>(saved));

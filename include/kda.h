@@ -136,10 +136,12 @@ size_t kda_bwd_workspace_size(const kda_dims* dims, int chunk_size);
  *     sub-block factorisation of the decay stays inside fp32 range only for
  *     |lower_bound| <= 5.  With the lower-bounded gate that is required of
  *     both directions.
- *   - kda_fwd and kda_bwd also take bf16 K == V == 64 heads under the
- *     lower-bounded gate on the tensor-core path (channels padded to 128 inside
- *     the kernels; kda_bwd pads the states it reads and unpads dinitial_state in
- *     its workspace); the other entry points run them on the SIMT path.
+ *   - kda_fwd, kda_bwd and the training pair (kda_fwd_save / kda_bwd_saved)
+ *     also take bf16 K == V == 64 heads under the lower-bounded gate on the
+ *     tensor-core path (channels padded to 128 inside the kernels, so the saved
+ *     record has the 128-channel size; the backward pads the states it reads
+ *     and unpads dinitial_state in its workspace).  The segmented entries
+ *     refuse them.
  *   - Under the unbounded gate both directions take the tensor-core path
  *     too: the diagonal sub-blocks, where the factorisation has no bound,
  *     are formed directly (in the forward's intra-chunk forms and in the

@@ -170,9 +170,10 @@ def _bwd_saved(lib, dims, saved=None, saved_bytes=0, ptr=16):
 
 def test_saved_context_sizes(lib):
     sz = lambda **kw: lib.kda_saved_size(ctypes.byref(_dims(**kw)), 64)
-    assert sz() == 0                                        # K = V = 64: no tensor-core path, nothing to keep
-    assert sz(K=128, V=128, dtype=_lib.KDA_FP32) == 0
+    assert sz(K=128, V=128, dtype=_lib.KDA_FP32) == 0       # fp32: no tensor-core path, nothing to keep
+    assert sz(K=64, V=128) == 0 and sz(K=64, V=64, gate=_lib.GATES["softplus"]) == 0
     one = sz(K=128, V=128)
+    assert sz() == one                                      # K = V = 64 heads keep the padded 128-channel record
     assert one > 0 and one % 256 == 0
     assert sz(K=128, V=128, T=512) == 2 * one               # one record per (chunk, head)
     assert sz(K=128, V=128, H=4) == 2 * one
@@ -180,11 +181,12 @@ def test_saved_context_sizes(lib):
 
 
 def test_saved_context_validation(lib):
-    d64, d128 = _dims(), _dims(K=128, V=128)
+    d64, d128 = _dims(K=64, V=128), _dims(K=128, V=128)
     need = lib.kda_saved_size(ctypes.byref(d128), 64)
     # shapes off the tensor-core path are refused, not silently recomputed
     assert _fwd_save(lib, d64) == _lib.KDA_ERR_UNSUPPORTED
     assert _bwd_saved(lib, d64) == _lib.KDA_ERR_UNSUPPORTED
+    assert _fwd_save(lib, _dims(dtype=_lib.KDA_FP32)) == _lib.KDA_ERR_UNSUPPORTED
     assert _fwd_save(lib, d128, lb=-6.0) == _lib.KDA_ERR_UNSUPPORTED
     assert _fwd_save(lib, d128, ptr=24) == _lib.KDA_ERR_UNSUPPORTED          # unaligned activations
     # the saved buffer: missing, too small, misaligned

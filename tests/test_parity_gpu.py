@@ -484,6 +484,31 @@ def test_bwd_bf16_k64_tensor_core(case):
     assert "kda_grad_simt" not in names and "kda_intra_simt" not in names, names
 
 
+def test_k64_saved_pair_matches_plain_calls():
+    """The training pair takes K = V = 64 heads too (the record in its 128-channel layout): the
+    gradients equal kda_bwd's bit for bit, and the forward stays within the bound of the oracle."""
+    import gated_delta_rule_sm_gb300 as kda
+    lens = [70, 0, 129, 1, 64]
+    x = make_inputs(Workload("t", B=1, T=sum(lens), H=2, K=64, V=64, varlen=True, initial_state=True,
+                             backward=True, seed=88), device=DEV, lengths=lens)
+    names = ("q", "k", "v", "g_raw", "beta_raw", "a_log", "dt_bias")
+    kw = dict(scale=x["scale"], lower_bound=x["lower_bound"], chunk_size=64, cu_seqlens=x["cu_seqlens"],
+              initial_state=x["initial_state"])
+    nbytes = kda.saved_size(x["q"], x["v"], x["cu_seqlens"])
+    assert nbytes > 0
+    saved = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    o2, f2 = kda.forward(*[x[n] for n in names], output_final_state=True, saved=saved, **kw)
+    dfinal = 0.05 * torch.randn((len(lens), 2, 64, 64), generator=torch.Generator().manual_seed(4)).to(DEV)
+    g1 = kda.backward(*[x[n] for n in names], x["dout"], dfinal_state=dfinal, **kw)
+    g2 = kda.backward(*[x[n] for n in names], x["dout"], dfinal_state=dfinal, saved=saved, **kw)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    r_out, r_fs = oracle_fwd(x)
+    assert rel_err(o2, r_out, "bf16") <= 2e-2 and rel_err(f2, r_fs, "bf16") <= 2e-2
+    for n in GRADS:
+        assert torch.equal(g1[n], g2[n]), n
+
+
 @pytest.mark.parametrize("g_mean,Hk", [(0.0, 0), (4.0, 0), (-6.0, 0), (0.0, 1)])
 def test_softplus_gate_tensor_core_backward(g_mean, Hk):
     """The tcgen05 backward under the unbounded gate: typical, steep (g near -64 per token: exp(Gamma)
