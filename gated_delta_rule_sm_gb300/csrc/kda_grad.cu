@@ -38,80 +38,10 @@ struct TileH {
     int rs, cs;
 };
 
-// d[b] (16 x 8 blocks at rows m0, cols n0 + 8 b, b < NB) += sum_k A(m, k) B(k, n): one A fragment per
-// k-step serves the whole strip; the k-loop stays rolled to keep the kernel's code small.
-template <int NB>
-__device__ __forceinline__ void mma_strip(float (&d)[NB][4], const Tile& A, const Tile& B, int m0, int n0, int k_lo,
-                                          int k_hi, int lane) {
-    const int g = lane >> 2, q = lane & 3;
-#pragma unroll 1
-    for (int k0 = k_lo; k0 < k_hi; k0 += 8) {
-        uint32_t a[4];
-        a[0] = tf32(A.at(m0 + g, k0 + q));
-        a[1] = tf32(A.at(m0 + g + 8, k0 + q));
-        a[2] = tf32(A.at(m0 + g, k0 + q + 4));
-        a[3] = tf32(A.at(m0 + g + 8, k0 + q + 4));
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            uint32_t bb[2];
-            bb[0] = tf32(B.at(k0 + q, n0 + 8 * b + g));
-            bb[1] = tf32(B.at(k0 + q + 4, n0 + 8 * b + g));
-            mma1688(d[b], a, bb);
-        }
-    }
-}
-
-// Split-precision strip: d += A B with hi*hi + hi*lo + lo*hi products.
-template <int NB>
-__device__ __forceinline__ void mma_strip3(float (&d)[NB][4], const Tile& A, const Tile& B, int m0, int n0, int k_lo,
-                                           int k_hi, int lane) {
-    const int g = lane >> 2, q = lane & 3;
-#pragma unroll 1
-    for (int k0 = k_lo; k0 < k_hi; k0 += 8) {
-        uint32_t ah[4], al[4];
-        split_tf32(A.at(m0 + g, k0 + q), ah[0], al[0]);
-        split_tf32(A.at(m0 + g + 8, k0 + q), ah[1], al[1]);
-        split_tf32(A.at(m0 + g, k0 + q + 4), ah[2], al[2]);
-        split_tf32(A.at(m0 + g + 8, k0 + q + 4), ah[3], al[3]);
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            uint32_t bh[2], bl[2];
-            split_tf32(B.at(k0 + q, n0 + 8 * b + g), bh[0], bl[0]);
-            split_tf32(B.at(k0 + q + 4, n0 + 8 * b + g), bh[1], bl[1]);
-            mma1688(d[b], al, bh);
-            mma1688(d[b], ah, bl);
-            mma1688(d[b], ah, bh);
-        }
-    }
-}
-
-// Strip with the left operand split (d += A_lo B + A_hi B): for a right operand that is exact in tf32.
-template <int NB>
-__device__ __forceinline__ void mma_strip_splitA(float (&d)[NB][4], const Tile& A, const Tile& B, int m0, int n0,
-                                                 int k_lo, int k_hi, int lane) {
-    const int g = lane >> 2, q = lane & 3;
-#pragma unroll 1
-    for (int k0 = k_lo; k0 < k_hi; k0 += 8) {
-        uint32_t ah[4], al[4];
-        split_tf32(A.at(m0 + g, k0 + q), ah[0], al[0]);
-        split_tf32(A.at(m0 + g + 8, k0 + q), ah[1], al[1]);
-        split_tf32(A.at(m0 + g, k0 + q + 4), ah[2], al[2]);
-        split_tf32(A.at(m0 + g + 8, k0 + q + 4), ah[3], al[3]);
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            uint32_t bb[2];
-            bb[0] = tf32(B.at(k0 + q, n0 + 8 * b + g));
-            bb[1] = tf32(B.at(k0 + q + 4, n0 + 8 * b + g));
-            mma1688(d[b], al, bb);
-            mma1688(d[b], ah, bb);
-        }
-    }
-}
-
 // bf16 warp MMA, 16 x 8 x 16, fp32 accumulate.  Fragments (g = lane / 4, q = lane % 4): A words
 // (row g, k 2q..2q+1), (row g + 8, k 2q..), (row g, k 2q + 8..), (row g + 8, k 2q + 8..); B words
-// (k 2q..2q+1, col g), (k 2q + 8.., col g); the first element of a pair in the low half.  C as for
-// the tf32 shape.
+// (k 2q..2q+1, col g), (k 2q + 8.., col g); the first element of a pair in the low half.  C words
+// (row g, col 2q), (row g, col 2q + 1), (row g + 8, col 2q), (row g + 8, col 2q + 1), as frag_rc gives.
 __device__ __forceinline__ void mma16816(float* d, const uint32_t* a, const uint32_t* b) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -129,8 +59,10 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
     lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// mma_strip on bf16 halves of both operands (hi*hi + hi*lo + lo*hi, relative error ~1e-5 instead of
-// a single tf32 product's ~5e-4).  k_lo and k_hi - k_lo multiples of 16.
+// d[b] (16 x 8 blocks at rows m0, cols n0 + 8 b, b < NB) += sum_k A(m, k) B(k, n) over k in [k_lo, k_hi),
+// both operands split into bf16 halves (hi*hi + hi*lo + lo*hi, relative error ~1e-5 where one tf32
+// product gives ~5e-4); one A fragment per k-step serves the whole strip, the k-loop stays rolled to
+// keep the kernel's code small.  k_lo and k_hi - k_lo multiples of 16.
 template <int NB>
 __device__ __forceinline__ void mma_strip3_bf16(float (&d)[NB][4], const Tile& A, const Tile& B, int m0, int n0,
                                                 int k_lo, int k_hi, int lane) {
@@ -156,8 +88,8 @@ __device__ __forceinline__ void mma_strip3_bf16(float (&d)[NB][4], const Tile& A
     }
 }
 
-// mma_strip3_pair on bf16 halves: K = 16 per instruction, products hi*hi + hi*lo + lo*hi (relative
-// error ~1e-5, as the backward chains' split products).  k_hi - k_lo a multiple of 16.
+// Two left operands sharing the right one, d1 += A1 B and d2 += A2 B, in the same split bf16 products
+// (relative error ~1e-5, as the backward chains' split products).  k_hi - k_lo a multiple of 16.
 template <int NB>
 __device__ __forceinline__ void mma_strip3_pair_bf16(float (&d1)[NB][4], float (&d2)[NB][4], const Tile& A1,
                                                      const Tile& A2, const Tile& B, int m0, int n0, int k_lo,
@@ -189,9 +121,8 @@ __device__ __forceinline__ void mma_strip3_pair_bf16(float (&d1)[NB][4], float (
     }
 }
 
-// mma_strip_splitA on bf16 halves for a bf16 right operand (exact): d += A_lo B + A_hi B with K = 16
-// per instruction; A's hi + lo carries 16 significant bits (relative error ~1e-5).  k_hi - k_lo a
-// multiple of 16.
+// For a bf16 right operand (exact): d += A_lo B + A_hi B with K = 16 per instruction; A's hi + lo
+// carries 16 significant bits (relative error ~1e-5).  k_hi - k_lo a multiple of 16.
 // B is a row-major [k][n] bf16 tile (B.cs == 1, row stride B.rs elements, a multiple of 8, rows 16-byte
 // aligned): each k-step moves two n-blocks' fragments with one ldmatrix.x4.trans (lanes 8 i .. 8 i + 7
 // address rows k0 + 8 (i % 2) .. + 7 of n-block b + i / 2).  NB even, n0 a multiple of 8.
@@ -221,37 +152,6 @@ __device__ __forceinline__ void mma_strip_splitA_bf16(float (&d)[NB][4], const T
             mma16816(d[b], ah, bb);
             mma16816(d[b + 1], al, bb + 2);
             mma16816(d[b + 1], ah, bb + 2);
-        }
-    }
-}
-
-// Split-precision strip for two left operands sharing the right one: d1 += A1 B, d2 += A2 B with
-// hi*hi + hi*lo + lo*hi products.
-template <int NB>
-__device__ __forceinline__ void mma_strip3_pair(float (&d1)[NB][4], float (&d2)[NB][4], const Tile& A1, const Tile& A2,
-                                                const Tile& B, int m0, int n0, int k_lo, int k_hi, int lane) {
-    const int g = lane >> 2, q = lane & 3;
-#pragma unroll 1
-    for (int k0 = k_lo; k0 < k_hi; k0 += 8) {
-        uint32_t h1[4], l1[4], h2[4], l2[4];
-        const int rr[4] = {m0 + g, m0 + g + 8, m0 + g, m0 + g + 8};
-        const int kk[4] = {k0 + q, k0 + q, k0 + q + 4, k0 + q + 4};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            split_tf32(A1.at(rr[i], kk[i]), h1[i], l1[i]);
-            split_tf32(A2.at(rr[i], kk[i]), h2[i], l2[i]);
-        }
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            uint32_t bh[2], bl[2];
-            split_tf32(B.at(k0 + q, n0 + 8 * b + g), bh[0], bl[0]);
-            split_tf32(B.at(k0 + q + 4, n0 + 8 * b + g), bh[1], bl[1]);
-            mma1688(d1[b], l1, bh);
-            mma1688(d1[b], h1, bl);
-            mma1688(d1[b], h1, bh);
-            mma1688(d2[b], l2, bh);
-            mma1688(d2[b], h2, bl);
-            mma1688(d2[b], h2, bh);
         }
     }
 }
