@@ -686,3 +686,22 @@ def test_unaligned_state_buffers_take_the_simt_path():
     assert "kda_grad_tc" not in names and "kda_grad_simt" in names, names
     with pytest.raises(KdaError):
         gpu_fwd(x, segments=2)
+
+
+@pytest.mark.parametrize("case", ["k64", "segmented"])
+def test_backward_without_states(case):
+    """No initial state, no final-state gradient and no initial-state gradient requested: the K = 64
+    tensor-core backward pads nothing, and the segmented backward's combines start from zero and
+    write no row result."""
+    import gated_delta_rule_sm_gb300 as kda
+    D = 64 if case == "k64" else 128
+    x = make_inputs(Workload("t", B=2, T=260, H=2, K=D, V=D, backward=True, seed=89), device=DEV)
+    names = ("q", "k", "v", "g_raw", "beta_raw", "a_log", "dt_bias")
+    g = kda.backward(*[x[n] for n in names], x["dout"], scale=x["scale"], lower_bound=x["lower_bound"],
+                     want_dinitial_state=False, segments=3 if case == "segmented" else 0)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    assert g["dinitial_state"] is None
+    r = oracle_bwd(x)
+    for n in ("dq", "dk", "dv", "dg_raw", "dbeta_raw", "da_log", "ddt_bias"):
+        assert rel_err(g[n], r[n], "bf16") <= tol("bf16"), n
