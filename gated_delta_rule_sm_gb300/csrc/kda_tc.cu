@@ -954,7 +954,7 @@ __global__ void __launch_bounds__(256, 1) chain_fwd_tc_kernel(Params p, const ui
         mbar_init(bar_ws, 4);
         mbar_init(bar_s, 4);
         mbar_init(bar_o, 1);
-        mbar_init(bar_u, 1);
+        mbar_init(bar_u, 4);   // the four MMA2b issuers, each after its product is queued
         *sh_fail = 0;
         mbar_fence_init();
     }
@@ -1126,13 +1126,15 @@ __global__ void __launch_bounds__(256, 1) chain_fwd_tc_kernel(Params p, const ui
         const bool failed = named_sync_or(2, 192, *sh_fail != 0);
         tc_fence_after();
         if (failed) { ok = false; break; }
-        if (tid == 0) mbar_arrive(bar_u);   // the MMA warp may read U now
-        // MMA2b: D3 partial w = Kd^T U over t in [16 w, 16 w + 16) (one K step)
+        // MMA2b: D3 partial w = Kd^T U over t in [16 w, 16 w + 16) (one K step).  The MMA warp's output
+        // product (Aqk U) is released only after these four are queued, so the state's product, on the
+        // chain's critical path, does not wait behind it in the tensor pipe.
         if (issuer) {
             const uint32_t ub = ub_addr(i), kd = smem_u32(sl + chainlay::SLOT_KD);
             mma_bf16(tD3 + 32 * warp, smem_desc(kd + warp * 256, 128, 1024), smem_desc(ub + warp * 1024, 512, 128),
                      kIdescKU, 0);
             mma_commit(bar_s);
+            mbar_arrive(bar_u);   // the MMA warp may read U now
         }
         fail_wait(bar_s, par);
         tc_fence_after();
