@@ -63,7 +63,7 @@ static WsPlan plan_simt(const Shape& s, bool bwd) {
     const RecLayout L = RecLayout::make(s.K, s.V);
     w.rec_stride = bwd ? L.bwd_size : L.fwd_size;
     size_t o = 0;
-    w.off_chunk = o; o = align_up(o + sizeof(int32_t) * (size_t)(s.N + 1));
+    w.off_chunk = o; o = align_up(o + sizeof(int32_t) * (size_t)(2 * s.N + 1));   // chunk table, segment order
     w.off_rec = o; o = align_up(o + sizeof(float) * (size_t)s.NCmax * s.H * w.rec_stride);
     if (bwd) {
         const size_t kv = (size_t)s.K * s.V;
@@ -106,7 +106,7 @@ struct TcPlan {
 static TcPlan plan_tc_fwd(const Shape& s) {
     TcPlan w;
     size_t o = 0;
-    w.off_chunk = o; o = align_up(o + sizeof(int32_t) * (size_t)(s.N + 1));
+    w.off_chunk = o; o = align_up(o + sizeof(int32_t) * (size_t)(2 * s.N + 1));   // chunk table, segment order
     w.off_rec = o; o = align_up(o + tc_record_bytes(s.NCmax, s.H));
     w.off_diag = 0;
     if (s.gate == KDA_GATE_SOFTPLUS) { w.off_diag = o; o = align_up(o + diag_item_bytes() * s.NCmax * s.H); }

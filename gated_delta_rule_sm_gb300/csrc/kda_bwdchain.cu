@@ -41,6 +41,7 @@ struct ChainSrc {
     const float* pbase;   // reverse chain only
     size_t pstride;
     int mode;             // BwdChainMode
+    int rank_major;       // blockIdx.x = (head, slice), blockIdx.y = rank in seg_order (longest first)
 };
 
 namespace bwchain {
@@ -75,7 +76,17 @@ template <int JW, bool REV, int MODE>
 __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc src) {
     using L = bwchain::Lay<JW>;
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int n = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * JW;
+    int n, h, j0;
+    if (src.rank_major) {
+        constexpr int NZ = 128 / JW;
+        h = blockIdx.x / NZ;
+        j0 = (blockIdx.x - h * NZ) * JW;
+        n = seg_order(p)[blockIdx.y];
+    } else {
+        n = blockIdx.x;
+        h = blockIdx.y;
+        j0 = blockIdx.z * JW;
+    }
     const int H = p.H;
     constexpr int K = 128, V = 128;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -320,7 +331,12 @@ static cudaError_t launch_chain_jw(const Params& p, const ChainSrc& src, cudaStr
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
     if (e != cudaSuccess) return e;
     timing_pre(st, REV ? K_CHAIN_BWD_TC : K_CHAIN_REC_TC);
-    kern<<<dim3(p.N, p.H, 128 / JW), 128, L::BYTES, st>>>(p, src);
+    ChainSrc s2 = src;
+    s2.rank_major = p.N <= 65535;   // segments in launch order, longest first (grid y holds at most 65535)
+    if (s2.rank_major)
+        kern<<<dim3(p.H * (128 / JW), p.N), 128, L::BYTES, st>>>(p, s2);
+    else
+        kern<<<dim3(p.N, p.H, 128 / JW), 128, L::BYTES, st>>>(p, s2);
     timing_post(st);
     return cudaGetLastError();
 }
@@ -340,14 +356,14 @@ static cudaError_t launch_chain(const Params& p, const ChainSrc& src, cudaStream
 
 cudaError_t launch_chain_bwd_tc(const Params& p, const uint8_t* bw, cudaStream_t st, int mode) {
     ChainSrc src{bw, bwrec::BYTES, reinterpret_cast<const float*>(bw + bwrec::Y), bwrec::BYTES / 4,
-                 reinterpret_cast<const float*>(bw + bwrec::P), bwrec::BYTES / 4, mode};
+                 reinterpret_cast<const float*>(bw + bwrec::P), bwrec::BYTES / 4, mode, 0};
     static_assert(bwrec::BYTES % 256 == 0, "record stride");
     return launch_chain<true>(p, src, st);
 }
 
 cudaError_t launch_chain_rec_tc(const Params& p, const uint8_t* bw, cudaStream_t st, int mode) {
     const RecLayout L = RecLayout::make(128, 128);
-    ChainSrc src{bw, bwrec::BYTES, p.rec + L.U0, p.rec_stride, nullptr, 0, mode};
+    ChainSrc src{bw, bwrec::BYTES, p.rec + L.U0, p.rec_stride, nullptr, 0, mode, 0};
     return launch_chain<false>(p, src, st);
 }
 

@@ -31,7 +31,8 @@ struct Params {
     float *dq_v, *dk_v;         // dq, dk per value head [TT, H, K]: dq / dk when G == 1, else scratch
                                 // that the group sum folds into dq / dk [TT, Hk, K]
     // workspace views
-    int32_t* chunk_off;         // [N+1] first chunk of each segment; chunk_off[N] = total chunks
+    int32_t* chunk_off;         // [N+1] first chunk of each segment; chunk_off[N] = total chunks; then
+                                // [N] the segments in launch order (seg_order)
     float* rec;                 // per (chunk, head) intra-chunk records (SIMT path)
     size_t rec_stride;          // floats per record
     float* states;              // [NCmax, H, K, V] chunk-entering states (backward)
@@ -48,6 +49,10 @@ struct Params {
                                 // (chunk, head), from diag_tc_kernel
     int* status;                // device status word
 };
+
+// The segments in the order the chain kernels take them (longest first for packed documents), written by
+// the planner right after the chunk table.
+__host__ __device__ __forceinline__ int32_t* seg_order(const Params& p) { return p.chunk_off + p.N + 1; }
 
 // Device status word (first error wins); `status` points at the library's word on this device.
 __device__ __forceinline__ void record_error(int* status, int code) { atomicCAS(status, 0, code); }

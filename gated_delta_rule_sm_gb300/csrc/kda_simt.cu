@@ -35,8 +35,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params p) {
         if (tid == 0 && (p.cu[0] != 0 || p.cu[p.N] != p.TT)) bad_s = 1;
     }
     __syncthreads();
+    int32_t* order = seg_order(p);
     if (bad_s) {
         for (int n = tid; n <= p.N; n += blockDim.x) p.chunk_off[n] = 0;
+        for (int n = tid; n < p.N; n += blockDim.x) order[n] = n;
         if (tid == 0) record_error(p.status, KDA_ERR_INVALID_ARG);
         return;
     }
@@ -72,6 +74,24 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params p) {
         __syncthreads();
     }
     if (tid == 0) p.chunk_off[p.N] = carry_s;
+    __syncthreads();
+    // Segments by decreasing chunk count (ties by index): the chain kernels take their segments in this
+    // order, so the longest documents start first and the last wave holds the short ones.  Rows of equal
+    // length, and more than kOrderMax documents (the rank count is quadratic), keep the given order.
+    constexpr int kOrderMax = 2048;
+    if (!p.cu || p.N > kOrderMax) {
+        for (int n = tid; n < p.N; n += blockDim.x) order[n] = n;
+        return;
+    }
+    for (int n = tid; n < p.N; n += blockDim.x) {
+        const int cn = p.chunk_off[n + 1] - p.chunk_off[n];
+        int rank = 0;
+        for (int m = 0; m < p.N; ++m) {
+            const int cm = p.chunk_off[m + 1] - p.chunk_off[m];
+            rank += (cm > cn) || (cm == cn && m < n);
+        }
+        order[rank] = n;
+    }
 }
 
 // ------------------------------------------------------------------ intra-chunk

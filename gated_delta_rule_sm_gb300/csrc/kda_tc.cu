@@ -922,11 +922,24 @@ constexpr uint32_t kIdescKU = idesc_f16(128, 32, 0, 1);   // Kd^T / Aqk K-major,
 // flags: kChainStoreStates (write the chunk-entering states), kChainTransfer (start every segment from
 // the identity and take U0 as zero: the final state is then the segment's transfer matrix, the product
 // of Diag(exp(Gamma_last)) - Kd^T W over its chunks; needs K == V).
-constexpr int kChainStoreStates = 1, kChainTransfer = 2;
+constexpr int kChainStoreStates = 1, kChainTransfer = 2, kChainRankMajor = 4;
 __global__ void __launch_bounds__(256, 1) chain_fwd_tc_kernel(Params p, const uint8_t* recs, int flags) {
     const bool store_states = flags & kChainStoreStates, transfer = flags & kChainTransfer;
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int n = blockIdx.x, h = blockIdx.y, z = blockIdx.z, j0 = z * 32;
+    // kChainRankMajor: blockIdx.x = (head, slice), blockIdx.y = the segment's rank in seg_order (longest
+    // first), so every head and slice of the longest segments start in the first wave
+    int n, h, z;
+    if (flags & kChainRankMajor) {
+        const int nz = p.V / 32;
+        h = blockIdx.x / nz;
+        z = blockIdx.x - h * nz;
+        n = seg_order(p)[blockIdx.y];
+    } else {
+        n = blockIdx.x;
+        h = blockIdx.y;
+        z = blockIdx.z;
+    }
+    const int j0 = z * 32;
     // the state slice has 128 rows in TMEM and registers; heads with K = V = 64 leave rows and columns
     // 64..127 zero (their record rows are zero) and read / write only the real ones
     const int H = p.H, K = p.K, V = p.V;
@@ -1276,8 +1289,12 @@ cudaError_t launch_chain_fwd_tc(const Params& p, const uint8_t* recs, bool store
                                          (int)chainlay::BYTES);
     if (e != cudaSuccess) return e;
     timing_pre(st, K_CHAIN_FWD_TC);
-    chain_fwd_tc_kernel<<<dim3(p.N, p.H, p.V / 32), 256, chainlay::BYTES, st>>>(
-        p, recs, (store_states ? kChainStoreStates : 0) | (transfer ? kChainTransfer : 0));
+    const int flags = (store_states ? kChainStoreStates : 0) | (transfer ? kChainTransfer : 0);
+    if (p.N <= 65535)   // segments in launch order, longest first (grid y holds at most 65535)
+        chain_fwd_tc_kernel<<<dim3(p.H * (p.V / 32), p.N), 256, chainlay::BYTES, st>>>(p, recs,
+                                                                                   flags | kChainRankMajor);
+    else
+        chain_fwd_tc_kernel<<<dim3(p.N, p.H, p.V / 32), 256, chainlay::BYTES, st>>>(p, recs, flags);
     timing_post(st);
     return cudaGetLastError();
 }
