@@ -21,6 +21,12 @@
 // N = JW, K = 64), then Z' = gC Z + D3 (+ P).  Record slots (A1, A2 hi/lo, gC) are double buffered
 // by bulk copies.  X (U, or dU) and the chunk's Z are also written out per chunk for the gradient
 // kernel, in x4 order (x4_off) so that every warp store covers whole 128-byte lines.
+//
+// Three modes (template MODE): the full pass above; for the segment-parallel backward a local pass
+// (Z from zero, only the end Z written) and a transfer pass (Z from the identity, Y and P taken as
+// zero, only the end Z written: the segment's transition, since K = V).  The blocks take segments
+// longest first (seg_order).  K = V = 64 heads run on zero-padded 128 x 128 states that the host side
+// pads and unpads with the two small kernels at the end of this file.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
