@@ -1,7 +1,9 @@
-// kda_grad.cu -- per-chunk gradients of the chunkwise KDA recurrence for K = V = 128.
+// kda_grad.cu -- per-chunk gradients of the chunkwise KDA recurrence for K = V = 128 (K = V = 64
+// heads zero-padded to 128 channels, only the real channels written out).
 //
-// Inputs per (chunk, head): the fp32 chunk record (Kg, Qg, Kd, N, Bkk, Gamma, q_hat, k_hat, beta,
-// the inverse norms), the chunk-entering state S0 and the gradient dS_end w.r.t. the chunk-leaving
+// Inputs per (chunk, head): the fp32 chunk record (Kg, N, Bkk, Gamma, q_hat, k_hat, beta, the inverse
+// norms; Qg and Kd are formed from Gamma, q_hat, k_hat), the chunk-entering state S0 and the gradient
+// dS_end w.r.t. the chunk-leaving
 // state (both from the state chains), U and dU per chunk (written by the two backward chains), dO,
 // v and g_raw.  The gradient of the chunk equations
 //     U = U0 - W S0,   O = scale (Qg S0 + Aqk U),   S_end = Diag(exp(Gamma_last)) S0 + Kd^T U,
@@ -11,11 +13,12 @@
 //
 // Phase 1 walks the four 32-column slices of V: the slice outer products (dKg, dQg, dKd, dT, dA)
 // accumulate in TMEM from tcgen05 MMAs on bf16 hi / lo operands; the small dependent products in
-// between (v - Kg S0, Diag(beta) N^T dU) and everything in phase 2 run as warp-level tf32 MMAs
-// (m16n8k8, operands rounded to nearest; the decayed bilinear forms use a hi/lo split because
-// their pair terms cancel in the log-decay gradient) straight from padded shared-memory tiles: no
-// descriptor or accumulator round trips between the many dependent steps.  Row strides = 4
-// (mod 32) words make every fragment load conflict-free in either orientation.
+// between (v - Kg S0, Diag(beta) N^T dU) and those of phase 2 run as warp-level MMAs straight from
+// padded shared-memory tiles, no descriptor or accumulator round trips between the many dependent
+// steps.  Every one of them splits its operands (hi + lo, three products): bf16 m16n8k16 for most,
+// tf32 m16n8k8 for dk_R, whose record loads run a k-step ahead; the log-decay gradient's pair terms
+// cancel, so single-product rounding (~5e-4) showed up there at ~1e-2 of its RMS under mild gates.
+// Row strides = 4 (mod 32) words make the fragment loads conflict-free.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_sm100.cuh"

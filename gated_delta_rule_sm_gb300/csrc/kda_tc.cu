@@ -1,15 +1,18 @@
-// kda_tc.cu -- tensor-core (tcgen05 / TMEM) path for bf16 inputs with K = V = 128.
+// kda_tc.cu -- tensor-core (tcgen05 / TMEM) path for bf16 inputs with K = V = 128 (and K = V = 64
+// heads, loaded as 128-channel tiles whose upper half is zero).
 //
 // Same chunkwise algebra as the SIMT path (the gated delta rule of "[kimi k3] add eager reference
 // model with FSDP2", 64 tokens per chunk):
 //     U = U0 - W S,   O = scale (Qg S + Aqk U),   S' = Diag(exp(Gamma_last)) S + Kd^T U.
-// Precision plan (bf16 inputs, fp32 state): the products whose rounding reaches the outputs least
-// run with bf16 operands (W S, Qg S: kind::f16); the ones that feed the state or the output
-// directly (Aqk U, Kd^T U) run with tf32 operands rounded to nearest (kind::tf32); U0 is added in
-// fp32.  The state itself stays in fp32 registers.
+// Precision plan (bf16 inputs, fp32 state): the chain's products run with fp16 operands (kind::f16):
+// W, Qg, Kd, Aqk, S and U stay far inside fp16's range, where its 11-bit significand gives each
+// product tf32-like accuracy in one MMA; U0 is added in fp32 and the state stays in fp32 registers.
 //
-// The intra-chunk kernel writes one record per (chunk, head) in exactly the shared-memory layout
-// the chain kernel's MMAs read, so the chain's load warp moves it with three bulk copies per chunk.
+// The intra-chunk kernels write one record per (chunk, head) in exactly the shared-memory layout the
+// chain kernel's MMAs read, so the chain's load warp moves it with three bulk copies per chunk.  The
+// chain's blocks take segments longest first (seg_order), the saving intra pass here also writes
+// the fp32 backward record, and the segment-parallel schedule's piece table and state combine close
+// the file.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
