@@ -14,6 +14,7 @@
 // decay difference is taken directly (no factorisation), in fp32.
 #include "kda_common.cuh"
 #include "kda_internal.h"
+#include "kda_sm100.cuh"
 
 namespace kda {
 
@@ -109,7 +110,10 @@ __device__ __forceinline__ ChunkRef locate_chunk(const Params& p, int c) {
 }
 
 // One CTA per (chunk, head).  Computes the prologue and every intra-chunk
-// quantity and writes the chunk record (layout: RecLayout).
+// quantity and writes the chunk record (layout: RecLayout).  The decayed bilinear forms take one
+// (t, s <= t) pair per thread at a time over the 2080 pairs of the triangle; the unit lower
+// triangular inverse runs in 16 x 16 blocks (the four diagonal blocks by forward substitution on
+// four warps at once, then the off-diagonal blocks level by level); v is staged in shared memory.
 template <bool BWD>
 __global__ void __launch_bounds__(256) intra_simt_kernel(Params p) {
     const int c = blockIdx.x, h = blockIdx.y;
@@ -126,47 +130,87 @@ __global__ void __launch_bounds__(256) intra_simt_kernel(Params p) {
     float* sB = sA + 64 * 65;        // [64][65] Bkk (strict lower)
     float* sN = sB + 64 * 65;        // [64][65] N = (I + Diag(beta) Bkk)^-1
     float* sb = sN + 64 * 65;        // [64] beta
+    float* sV = sb + 64;             // [64][V] v (zero past the segment)
+    float* sX = sV + 64 * V;         // [3][16][16] scratch of the blocked inverse
 
     if (tid < kChunk) {
         float b = 0.f;
         if (tid < ch.len) b = sigmoidf_acc(load_act(p.beta_raw, (size_t)(ch.tok0 + tid) * H + h, p.dtype));
         sb[tid] = b;
     }
-    // L2 norms, one warp per token
-    for (int t = warp; t < kChunk; t += 8) {
-        const size_t base = ((size_t)(ch.tok0 + t) * p.Hk + h / p.G) * K;   // key head of value head h
-        float qv[4], kv[4], sq = 0.f, sk = 0.f;
+    // L2 norms, one warp per token; each warp loads four tokens' q and k before reducing them
+    for (int t0 = warp; t0 < kChunk; t0 += 32) {
+        float qv[4][4], kv[4][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int cc = lane + 32 * i;
-            const bool ok = t < ch.len && cc < K;
-            qv[i] = ok ? load_act(p.q, base + cc, p.dtype) : 0.f;
-            kv[i] = ok ? load_act(p.k, base + cc, p.dtype) : 0.f;
-            sq += qv[i] * qv[i];
-            sk += kv[i] * kv[i];
+        for (int u = 0; u < 4; ++u) {
+            const int t = t0 + 8 * u;
+            const size_t base = ((size_t)(ch.tok0 + t) * p.Hk + h / p.G) * K;   // key head of value head h
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int cc = lane + 32 * i;
+                const bool ok = t < ch.len && cc < K;
+                qv[u][i] = ok ? load_act(p.q, base + cc, p.dtype) : 0.f;
+                kv[u][i] = ok ? load_act(p.k, base + cc, p.dtype) : 0.f;
+            }
         }
-        sq = warp_sum(sq);
-        sk = warp_sum(sk);
-        const float rq = 1.0f / sqrtf(sq + kNormEps), rk = 1.0f / sqrtf(sk + kNormEps);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int cc = lane + 32 * i;
-            if (cc < K) {
-                sQ[t * KP + cc] = qv[i] * rq;
-                sK[t * KP + cc] = kv[i] * rk;
+        for (int u = 0; u < 4; ++u) {
+            const int t = t0 + 8 * u;
+            float sq = 0.f, sk = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                sq += qv[u][i] * qv[u][i];
+                sk += kv[u][i] * kv[u][i];
+            }
+            sq = warp_sum(sq);
+            sk = warp_sum(sk);
+            const float rq = 1.0f / sqrtf(sq + kNormEps), rk = 1.0f / sqrtf(sk + kNormEps);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int cc = lane + 32 * i;
+                if (cc < K) {
+                    sQ[t * KP + cc] = qv[u][i] * rq;
+                    sK[t * KP + cc] = kv[u][i] * rk;
+                }
             }
         }
     }
-    // gate
+    // gate and v, eight elements per thread loaded before any is used
     const float ea = expf(p.a_log[h]);
-    for (int i = tid; i < kChunk * K; i += blockDim.x) {
-        const int t = i / K, cc = i % K;
-        float g = 0.f;
-        if (t < ch.len) {
-            const float x = load_act(p.g_raw, ((size_t)(ch.tok0 + t) * H + h) * K + cc, p.dtype);
-            g = gate_value(p, ea, x, p.dt_bias[h * K + cc]);
+    for (int i0 = tid; i0 < kChunk * K; i0 += 8 * blockDim.x) {
+        float x[8], db[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * blockDim.x, t = i / K, cc = i % K;
+            const bool ok = i < kChunk * K && t < ch.len;
+            x[u] = ok ? load_act(p.g_raw, ((size_t)(ch.tok0 + t) * H + h) * K + cc, p.dtype) : 0.f;
+            db[u] = ok ? p.dt_bias[h * K + cc] : 0.f;
         }
-        sG[t * KP + cc] = g;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * blockDim.x, t = i / K, cc = i % K;
+            if (i < kChunk * K) sG[t * KP + cc] = t < ch.len ? gate_value(p, ea, x[u], db[u]) : 0.f;
+        }
+    }
+    for (int i0 = tid; i0 < kChunk * V; i0 += 8 * blockDim.x) {
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * blockDim.x, t = i / V, j = i % V;
+            x[u] = (i < kChunk * V && t < ch.len) ? load_act(p.v, ((size_t)(ch.tok0 + t) * H + h) * V + j, p.dtype) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (i0 + u * blockDim.x < kChunk * V) sV[i0 + u * blockDim.x] = x[u];
+    }
+    for (int i = tid; i < kChunk * kChunk; i += blockDim.x) {
+        const int t = i >> 6, s = i & 63;
+        if (s > t) {
+            sA[t * 65 + s] = 0.f;
+            sB[t * 65 + s] = 0.f;
+        }
+        if (s == t) sB[t * 65 + s] = 0.f;
+        sN[t * 65 + s] = (s == t) ? 1.f : 0.f;
     }
     __syncthreads();
     for (int cc = tid; cc < K; cc += blockDim.x) {
@@ -178,29 +222,63 @@ __global__ void __launch_bounds__(256) intra_simt_kernel(Params p) {
         }
     }
     __syncthreads();
-    // decayed bilinear forms
-    for (int i = tid; i < kChunk * kChunk; i += blockDim.x) {
-        const int t = i >> 6, s = i & 63;
-        float aq = 0.f, ak = 0.f;
-        if (s <= t) {
-            for (int cc = 0; cc < K; ++cc) {
-                const float e = expf(sG[t * KP + cc] - sG[s * KP + cc]);
-                const float ks = sK[s * KP + cc] * e;
-                aq += sQ[t * KP + cc] * ks;
-                ak += sK[t * KP + cc] * ks;
+    // decayed bilinear forms over the pairs s <= t (pair index i = t (t + 1) / 2 + s)
+    for (int i = tid; i < kChunk * (kChunk + 1) / 2; i += blockDim.x) {
+        int t = (int)((sqrtf(8.f * (float)i + 1.f) - 1.f) * 0.5f);
+        while (t * (t + 1) / 2 > i) --t;
+        while ((t + 1) * (t + 2) / 2 <= i) ++t;
+        const int s = i - t * (t + 1) / 2;
+        const float* gt = sG + t * KP;
+        const float* gs = sG + s * KP;
+        const float* qt = sQ + t * KP;
+        const float* kt = sK + t * KP;
+        const float* ks = sK + s * KP;
+        float aq[4] = {0.f, 0.f, 0.f, 0.f}, ak[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int c0 = 0; c0 < K; c0 += 4) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float e = ks[c0 + u] * expf(gt[c0 + u] - gs[c0 + u]);
+                aq[u] += qt[c0 + u] * e;
+                ak[u] += kt[c0 + u] * e;
             }
         }
-        sA[t * 65 + s] = aq;
-        sB[t * 65 + s] = (s < t) ? ak : 0.f;
-        sN[t * 65 + s] = (s == t) ? 1.f : 0.f;
+        sA[t * 65 + s] = (aq[0] + aq[1]) + (aq[2] + aq[3]);
+        if (s < t) sB[t * 65 + s] = (ak[0] + ak[1]) + (ak[2] + ak[3]);
     }
     __syncthreads();
-    // forward substitution: N[t][s] = -sum_{r=s}^{t-1} beta_t B[t][r] N[r][s]
-    for (int t = 1; t < kChunk; ++t) {
-        if (tid < t) {
+    // N = (I + L)^-1, L = Diag(beta) Bkk.  Diagonal 16 x 16 blocks: warp b < 4 substitutes block b,
+    // lane = column:  N[t][s] = -beta_t sum_{r=s}^{t-1} Bkk[t][r] N[r][s].
+    if (warp < 4 && lane < 16) {
+        const int o = 16 * warp, sc = o + lane;
+        for (int tl = 1; tl < 16; ++tl) {
+            const int t = o + tl;
+            if (lane < tl) {
+                float acc = 0.f;
+                for (int r = sc; r < t; ++r) acc += sB[t * 65 + r] * sN[r * 65 + sc];
+                sN[t * 65 + sc] = -sb[t] * acc;
+            }
+            __syncwarp(0x0000ffffu);
+        }
+    }
+    __syncthreads();
+    // Off-diagonal blocks (i, j), i - j = d = 1, 2, 3:  N_ij = -N_ii X,  X = sum_{k=j}^{i-1} L_ik N_kj.
+    for (int d = 1; d < 4; ++d) {
+        const int nel = (4 - d) * 256;
+        for (int e = tid; e < nel; e += blockDim.x) {
+            const int i = d + (e >> 8), r = (e >> 4) & 15, col = e & 15;
+            const int t = 16 * i + r, sc = 16 * (i - d) + col;
             float acc = 0.f;
-            for (int r = tid; r < t; ++r) acc += sB[t * 65 + r] * sN[r * 65 + tid];
-            sN[t * 65 + tid] = -sb[t] * acc;
+            for (int m = 16 * (i - d); m < 16 * i; ++m) acc += sB[t * 65 + m] * sN[m * 65 + sc];
+            sX[e] = sb[t] * acc;
+        }
+        __syncthreads();
+        for (int e = tid; e < nel; e += blockDim.x) {
+            const int i = d + (e >> 8), r = (e >> 4) & 15, col = e & 15;
+            const int t = 16 * i + r, sc = 16 * (i - d) + col;
+            const float* x = sX + (e & ~255);
+            float acc = 0.f;
+            for (int m = 0; m <= r; ++m) acc += sN[t * 65 + 16 * i + m] * x[m * 16 + col];
+            sN[t * 65 + sc] = -acc;
         }
         __syncthreads();
     }
@@ -209,9 +287,14 @@ __global__ void __launch_bounds__(256) intra_simt_kernel(Params p) {
     // W = N Diag(beta) (k * exp(Gamma));  Qg;  Kd
     for (int i = tid; i < kChunk * K; i += blockDim.x) {
         const int t = i / K, cc = i % K;
-        float acc = 0.f;
-        for (int s = 0; s <= t; ++s) acc += sN[t * 65 + s] * sb[s] * sK[s * KP + cc] * sE[s * KP + cc];
-        rec[L.W + i] = acc;
+        float acc[2] = {0.f, 0.f};
+        int s = 0;
+        for (; s + 1 <= t; s += 2) {
+            acc[0] += sN[t * 65 + s] * sb[s] * sK[s * KP + cc] * sE[s * KP + cc];
+            acc[1] += sN[t * 65 + s + 1] * sb[s + 1] * sK[(s + 1) * KP + cc] * sE[(s + 1) * KP + cc];
+        }
+        if (s == t) acc[0] += sN[t * 65 + s] * sb[s] * sK[s * KP + cc] * sE[s * KP + cc];
+        rec[L.W + i] = acc[0] + acc[1];
         rec[L.Qg + i] = sQ[t * KP + cc] * sE[t * KP + cc];
         rec[L.Kd + i] = sK[t * KP + cc] * expf(sG[63 * KP + cc] - sG[t * KP + cc]);
         if (BWD) {
@@ -224,10 +307,14 @@ __global__ void __launch_bounds__(256) intra_simt_kernel(Params p) {
     // U0 = N Diag(beta) v
     for (int i = tid; i < kChunk * V; i += blockDim.x) {
         const int t = i / V, j = i % V;
-        float acc = 0.f;
-        for (int s = 0; s <= t && s < ch.len; ++s)
-            acc += sN[t * 65 + s] * sb[s] * load_act(p.v, ((size_t)(ch.tok0 + s) * H + h) * V + j, p.dtype);
-        rec[L.U0 + i] = acc;
+        float acc[2] = {0.f, 0.f};
+        int s = 0;
+        for (; s + 1 <= t; s += 2) {
+            acc[0] += sN[t * 65 + s] * sb[s] * sV[s * V + j];
+            acc[1] += sN[t * 65 + s + 1] * sb[s + 1] * sV[(s + 1) * V + j];
+        }
+        if (s == t) acc[0] += sN[t * 65 + s] * sb[s] * sV[s * V + j];
+        rec[L.U0 + i] = acc[0] + acc[1];
     }
     for (int i = tid; i < kChunk * kChunk; i += blockDim.x) {
         const int t = i >> 6, s = i & 63;
@@ -243,53 +330,198 @@ __global__ void __launch_bounds__(256) intra_simt_kernel(Params p) {
 
 // ------------------------------------------------------------------ forward chain
 
-// One CTA per (segment, head, 32-wide slice of V): S_slice [K][32] in shared memory.
-__global__ void __launch_bounds__(256) chain_fwd_simt_kernel(Params p, int store_states) {
+// One CTA of 16 warps per (segment, head, 32-wide slice of V): S_slice [K][32] in shared memory.  The
+// record fields of a chunk are staged into shared memory by 16-byte asynchronous copies in three
+// groups, each issued as soon as the previous chunk is done with its buffer: W and the U0 slice after
+// the U phase, Qg and Aqk after the output, Kd and exp(Gamma_last) after the state update.  Lane = column
+// j; warp w owns the rows t = w + 16 i of U and O and the state rows c = 4 w + 64 m + e (e < 4), so that
+// one 16-byte load of a Kd row serves four of its accumulators.
+constexpr int kChainSimtWarps = 16;
+
+__global__ void __launch_bounds__(kChainSimtWarps * 32) chain_fwd_simt_kernel(Params p, int store_states) {
+    constexpr int NW = kChainSimtWarps, NT = NW * 32;
     const int n = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * 32;
     const int K = p.K, V = p.V, H = p.H;
     const int tid = threadIdx.x, j = tid & 31, grp = tid >> 5;
     const bool jv = (j0 + j) < V;
-    extern __shared__ float sm[];
-    float* sS = sm;              // [K][32]
-    float* sU = sS + K * 32;     // [64][32]
+    const bool want_out = p.out != nullptr;   // the backward's recompute needs no output
+    extern __shared__ __align__(16) float sm[];
+    float* sS = sm;                  // [K][32] state slice
+    float* sU = sS + K * 32;         // [64][32]
+    float* sW = sU + 64 * 32;        // [64][K]
+    float* sQg = sW + 64 * K;        // [64][K]
+    float* sKd = sQg + 64 * K;       // [64][K]
+    float* sA = sKd + 64 * K;        // [64][64] Aqk (zero above the diagonal: the record stores it causal)
+    float* sU0 = sA + 64 * 64;       // [64][32] U0 columns j0 .. j0 + 31
+    float* sgC = sU0 + 64 * 32;      // [K] exp(Gamma_last)
     const RecLayout L = RecLayout::make(K, V);
-    for (int cc = grp; cc < K; cc += 8)
-        sS[cc * 32 + j] = (p.S0 && jv) ? p.S0[(((size_t)n * H + h) * K + cc) * V + j0 + j] : 0.f;
-    __syncthreads();
+    const int KQ = K / 4;            // float4 per row of a [64][K] field
+    auto rec_of = [&](int c) { return p.rec + ((size_t)c * H + h) * p.rec_stride; };
+    auto stage_rows = [&](float* dst, const float* src, int nq) {   // nq float4 of a contiguous field
+        for (int i = tid; i < nq; i += NT) sm100::cp_async16_zfill(dst + 4 * i, src + 4 * i, 16);
+    };
+    auto stage_wu = [&](int c) {
+        const float* rec = rec_of(c);
+        stage_rows(sW, rec + L.W, 64 * KQ);
+        for (int i = tid; i < 64 * 8; i += NT) {
+            const int t = i >> 3, q = i & 7;
+            const bool ok = j0 + 4 * q < V;   // V is a multiple of 16: a float4 is all in or all out
+            sm100::cp_async16_zfill(sU0 + t * 32 + 4 * q, rec + L.U0 + (size_t)t * V + (ok ? j0 + 4 * q : 0), ok ? 16 : 0);
+        }
+    };
+    auto stage_qa = [&](int c) {
+        if (!want_out) return;
+        const float* rec = rec_of(c);
+        stage_rows(sQg, rec + L.Qg, 64 * KQ);
+        stage_rows(sA, rec + L.A, 64 * 16);
+    };
+    auto stage_kd = [&](int c) {
+        const float* rec = rec_of(c);
+        stage_rows(sKd, rec + L.Kd, 64 * KQ);
+        stage_rows(sgC, rec + L.gC, KQ);
+    };
+    auto commit = [] { asm volatile("cp.async.commit_group;" ::: "memory"); };
+    auto wait_older = [] { asm volatile("cp.async.wait_group 2;" ::: "memory"); };   // all but the 2 newest groups
+    auto state_row = [&](int m, int e) { return 4 * grp + 64 * m + e; };   // K <= 128: m < 2
+
+    {
+        float s0[2][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int cc = state_row(m, e);
+                s0[m][e] = (cc < K && p.S0 && jv) ? p.S0[(((size_t)n * H + h) * K + cc) * V + j0 + j] : 0.f;
+            }
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (state_row(m, e) < K) sS[state_row(m, e) * 32 + j] = s0[m][e];
+    }
     const int cb = p.chunk_off[n], ce = p.chunk_off[n + 1];
     const int tb = seg_begin(p, n), te = seg_end(p, n);
-    for (int c = cb; c < ce; ++c) {
-        const float* rec = p.rec + ((size_t)c * H + h) * p.rec_stride;
-        const int tok0 = tb + (c - cb) * kChunk, len = min(kChunk, te - tok0);
-        if (store_states && jv)
-            for (int cc = grp; cc < K; cc += 8)
-                p.states[(((size_t)c * H + h) * K + cc) * V + j0 + j] = sS[cc * 32 + j];
-        for (int t = grp; t < kChunk; t += 8) {
-            float acc = jv ? rec[L.U0 + t * V + j0 + j] : 0.f;
-            const float* w = rec + L.W + t * K;
-            for (int cc = 0; cc < K; ++cc) acc -= w[cc] * sS[cc * 32 + j];
-            sU[t * 32 + j] = acc;
-        }
-        __syncthreads();
-        for (int t = grp; p.out && t < len; t += 8) {   // the backward's recompute needs no output
-            float acc = 0.f;
-            const float* qg = rec + L.Qg + t * K;
-            for (int cc = 0; cc < K; ++cc) acc += qg[cc] * sS[cc * 32 + j];
-            const float* a = rec + L.A + t * kChunk;
-            for (int s = 0; s <= t; ++s) acc += a[s] * sU[s * 32 + j];
-            if (jv) store_act(p.out, ((size_t)(tok0 + t) * H + h) * V + j0 + j, p.scale * acc, p.dtype);
-        }
-        __syncthreads();
-        for (int cc = grp; cc < K; cc += 8) {
-            float acc = rec[L.gC + cc] * sS[cc * 32 + j];
-            const float* kd = rec + L.Kd + cc;
-            for (int t = 0; t < kChunk; ++t) acc += kd[t * K] * sU[t * 32 + j];
-            sS[cc * 32 + j] = acc;
-        }
-        __syncthreads();
+    if (cb < ce) {
+        stage_wu(cb);
+        commit();
+        stage_qa(cb);
+        commit();
+        stage_kd(cb);
+        commit();
     }
+    for (int c = cb; c < ce; ++c) {
+        const int tok0 = tb + (c - cb) * kChunk, len = min(kChunk, te - tok0);
+        const bool more = c + 1 < ce;
+        wait_older();                // W, U0 of chunk c landed (this thread's copies) ...
+        __syncthreads();             // ... and every thread's; the state update of c - 1 is done
+        if (store_states && jv)
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int cc = state_row(m, e);
+                    if (cc < K) p.states[(((size_t)c * H + h) * K + cc) * V + j0 + j] = sS[cc * 32 + j];
+                }
+        // U = U0 - W S
+        {
+            float acc[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] = sU0[(grp + NW * i) * 32 + j];
+#pragma unroll 2
+            for (int c4 = 0; c4 < KQ; ++c4) {
+                const float s0 = sS[(4 * c4) * 32 + j], s1 = sS[(4 * c4 + 1) * 32 + j];
+                const float s2 = sS[(4 * c4 + 2) * 32 + j], s3 = sS[(4 * c4 + 3) * 32 + j];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 w = *reinterpret_cast<const float4*>(sW + (grp + NW * i) * K + 4 * c4);
+                    acc[i] -= w.x * s0 + w.y * s1 + w.z * s2 + w.w * s3;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sU[(grp + NW * i) * 32 + j] = acc[i];
+        }
+        __syncthreads();             // U visible; W and U0 are free
+        if (more) stage_wu(c + 1);
+        commit();
+        wait_older();                // Qg, Aqk of chunk c
+        __syncthreads();
+        // O = scale (Qg S + Aqk U)
+        if (want_out) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+            for (int c4 = 0; c4 < KQ; ++c4) {
+                const float s0 = sS[(4 * c4) * 32 + j], s1 = sS[(4 * c4 + 1) * 32 + j];
+                const float s2 = sS[(4 * c4 + 2) * 32 + j], s3 = sS[(4 * c4 + 3) * 32 + j];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 q = *reinterpret_cast<const float4*>(sQg + (grp + NW * i) * K + 4 * c4);
+                    acc[i] += q.x * s0 + q.y * s1 + q.z * s2 + q.w * s3;
+                }
+            }
+#pragma unroll 2
+            for (int s4 = 0; s4 < 16; ++s4) {
+                const float u0 = sU[(4 * s4) * 32 + j], u1 = sU[(4 * s4 + 1) * 32 + j];
+                const float u2 = sU[(4 * s4 + 2) * 32 + j], u3 = sU[(4 * s4 + 3) * 32 + j];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 a = *reinterpret_cast<const float4*>(sA + (grp + NW * i) * 64 + 4 * s4);
+                    acc[i] += a.x * u0 + a.y * u1 + a.z * u2 + a.w * u3;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = grp + NW * i;
+                if (jv && t < len) store_act(p.out, ((size_t)(tok0 + t) * H + h) * V + j0 + j, p.scale * acc[i], p.dtype);
+            }
+        }
+        __syncthreads();             // Qg and Aqk are free
+        if (more) stage_qa(c + 1);
+        commit();
+        wait_older();                // Kd, exp(Gamma_last) of chunk c
+        __syncthreads();
+        // S <- Diag(exp(Gamma_last)) S + Kd^T U  (rows owned by this thread: read, then overwritten)
+        {
+            float acc[2][4];
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int cc = state_row(m, e);
+                    acc[m][e] = cc < K ? sgC[cc] * sS[cc * 32 + j] : 0.f;
+                }
+            const bool hi = state_row(1, 0) < K;
+#pragma unroll 4
+            for (int t = 0; t < kChunk; ++t) {
+                const float u = sU[t * 32 + j];
+                if (state_row(0, 0) < K) {
+                    const float4 k0 = *reinterpret_cast<const float4*>(sKd + t * K + state_row(0, 0));
+                    acc[0][0] += k0.x * u; acc[0][1] += k0.y * u; acc[0][2] += k0.z * u; acc[0][3] += k0.w * u;
+                }
+                if (hi) {
+                    const float4 k1 = *reinterpret_cast<const float4*>(sKd + t * K + state_row(1, 0));
+                    acc[1][0] += k1.x * u; acc[1][1] += k1.y * u; acc[1][2] += k1.z * u; acc[1][3] += k1.w * u;
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (state_row(m, e) < K) sS[state_row(m, e) * 32 + j] = acc[m][e];
+        }
+        __syncthreads();             // Kd and exp(Gamma_last) are free
+        if (more) stage_kd(c + 1);
+        commit();
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
     if (p.ST && jv)
-        for (int cc = grp; cc < K; cc += 8) p.ST[(((size_t)n * H + h) * K + cc) * V + j0 + j] = sS[cc * 32 + j];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int cc = state_row(m, e);
+                if (cc < K) p.ST[(((size_t)n * H + h) * K + cc) * V + j0 + j] = sS[cc * 32 + j];
+            }
 }
 
 // ------------------------------------------------------------------ backward chain
@@ -577,7 +809,10 @@ __global__ void empty_segment_kernel(Params p, int fwd) {
 
 // ------------------------------------------------------------------ host launchers
 
-static size_t intra_smem(int K) { return (size_t)(4 * 64 * (K + 1) + 3 * 64 * 65 + 64) * sizeof(float); }
+// q_hat, k_hat, Gamma, exp(Gamma) [64][K+1]; Aqk, Bkk, N [64][65]; beta; v [64][V]; the inverse's scratch
+static size_t intra_smem(int K, int V) {
+    return (size_t)(4 * 64 * (K + 1) + 3 * 64 * 65 + 64 + 64 * V + 3 * 256) * sizeof(float);
+}
 
 cudaError_t launch_plan(const Params& p, cudaStream_t st) {
     timing_pre(st, K_PLAN);
@@ -587,7 +822,7 @@ cudaError_t launch_plan(const Params& p, cudaStream_t st) {
 }
 
 cudaError_t launch_intra_simt(const Params& p, bool bwd, cudaStream_t st) {
-    const size_t smem = intra_smem(p.K);
+    const size_t smem = intra_smem(p.K, p.V);
     cudaError_t e;
     if (bwd) {
         e = cudaFuncSetAttribute(intra_simt_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -605,10 +840,17 @@ cudaError_t launch_intra_simt(const Params& p, bool bwd, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+// S, U, the W / Qg / Kd / Aqk / U0 / exp(Gamma_last) fields of one chunk (floats)
+static size_t chain_fwd_simt_smem(int K) {
+    return (size_t)(K * 32 + 64 * 32 + 3 * 64 * K + 64 * 64 + 64 * 32 + K) * sizeof(float);
+}
+
 cudaError_t launch_chain_fwd_simt(const Params& p, bool store_states, cudaStream_t st) {
-    const size_t smem = (size_t)(p.K * 32 + 64 * 32) * sizeof(float);
+    const size_t smem = chain_fwd_simt_smem(p.K);
+    cudaError_t e0 = cudaFuncSetAttribute(chain_fwd_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e0 != cudaSuccess) return e0;
     timing_pre(st, K_CHAIN_FWD_SIMT);
-    chain_fwd_simt_kernel<<<dim3(p.N, p.H, (p.V + 31) / 32), 256, smem, st>>>(p, store_states ? 1 : 0);
+    chain_fwd_simt_kernel<<<dim3(p.N, p.H, (p.V + 31) / 32), kChainSimtWarps * 32, smem, st>>>(p, store_states ? 1 : 0);
     timing_post(st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
