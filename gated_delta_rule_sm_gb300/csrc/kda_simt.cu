@@ -138,12 +138,12 @@ __global__ void __launch_bounds__(256) intra_simt_kernel(Params p) {
         if (tid < ch.len) b = sigmoidf_acc(load_act(p.beta_raw, (size_t)(ch.tok0 + tid) * H + h, p.dtype));
         sb[tid] = b;
     }
-    // L2 norms, one warp per token; each warp loads four tokens' q and k before reducing them
-    for (int t0 = warp; t0 < kChunk; t0 += 32) {
-        float qv[4][4], kv[4][4];
+    // L2 norms, one warp per token; each warp loads its eight tokens' q and k before reducing them
+    {
+        float qv[8][4], kv[8][4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int t = t0 + 8 * u;
+        for (int u = 0; u < 8; ++u) {
+            const int t = warp + 8 * u;
             const size_t base = ((size_t)(ch.tok0 + t) * p.Hk + h / p.G) * K;   // key head of value head h
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -154,8 +154,8 @@ __global__ void __launch_bounds__(256) intra_simt_kernel(Params p) {
             }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int t = t0 + 8 * u;
+        for (int u = 0; u < 8; ++u) {
+            const int t = warp + 8 * u;
             float sq = 0.f, sk = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -175,33 +175,25 @@ __global__ void __launch_bounds__(256) intra_simt_kernel(Params p) {
             }
         }
     }
-    // gate and v, eight elements per thread loaded before any is used
+    // gate and v: eight elements of each per thread, all loaded before any is used
     const float ea = expf(p.a_log[h]);
-    for (int i0 = tid; i0 < kChunk * K; i0 += 8 * blockDim.x) {
-        float x[8], db[8];
+    for (int i0 = tid; i0 < kChunk * max(K, V); i0 += 8 * blockDim.x) {
+        float x[8], db[8], vv[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * blockDim.x, t = i / K, cc = i % K;
+            const int i = i0 + u * blockDim.x;
+            const int t = i / K, cc = i % K, tv = i / V, j = i % V;
             const bool ok = i < kChunk * K && t < ch.len;
             x[u] = ok ? load_act(p.g_raw, ((size_t)(ch.tok0 + t) * H + h) * K + cc, p.dtype) : 0.f;
             db[u] = ok ? p.dt_bias[h * K + cc] : 0.f;
+            vv[u] = (i < kChunk * V && tv < ch.len) ? load_act(p.v, ((size_t)(ch.tok0 + tv) * H + h) * V + j, p.dtype) : 0.f;
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int i = i0 + u * blockDim.x, t = i / K, cc = i % K;
             if (i < kChunk * K) sG[t * KP + cc] = t < ch.len ? gate_value(p, ea, x[u], db[u]) : 0.f;
+            if (i < kChunk * V) sV[i] = vv[u];
         }
-    }
-    for (int i0 = tid; i0 < kChunk * V; i0 += 8 * blockDim.x) {
-        float x[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * blockDim.x, t = i / V, j = i % V;
-            x[u] = (i < kChunk * V && t < ch.len) ? load_act(p.v, ((size_t)(ch.tok0 + t) * H + h) * V + j, p.dtype) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-            if (i0 + u * blockDim.x < kChunk * V) sV[i0 + u * blockDim.x] = x[u];
     }
     for (int i = tid; i < kChunk * kChunk; i += blockDim.x) {
         const int t = i >> 6, s = i & 63;
@@ -284,37 +276,53 @@ __global__ void __launch_bounds__(256) intra_simt_kernel(Params p) {
     }
     float* rec = p.rec + ((size_t)c * H + h) * p.rec_stride;
     const RecLayout L = RecLayout::make(K, V);
-    // W = N Diag(beta) (k * exp(Gamma));  Qg;  Kd
+    // elementwise record fields (Qg, Kd; Kg, Gamma, q_hat, k_hat for the backward; exp(Gamma_last)),
+    // then exp(Gamma) becomes Diag(beta) (k * exp(Gamma)) and v becomes Diag(beta) v in place
     for (int i = tid; i < kChunk * K; i += blockDim.x) {
         const int t = i / K, cc = i % K;
-        float acc[2] = {0.f, 0.f};
-        int s = 0;
-        for (; s + 1 <= t; s += 2) {
-            acc[0] += sN[t * 65 + s] * sb[s] * sK[s * KP + cc] * sE[s * KP + cc];
-            acc[1] += sN[t * 65 + s + 1] * sb[s + 1] * sK[(s + 1) * KP + cc] * sE[(s + 1) * KP + cc];
-        }
-        if (s == t) acc[0] += sN[t * 65 + s] * sb[s] * sK[s * KP + cc] * sE[s * KP + cc];
-        rec[L.W + i] = acc[0] + acc[1];
-        rec[L.Qg + i] = sQ[t * KP + cc] * sE[t * KP + cc];
-        rec[L.Kd + i] = sK[t * KP + cc] * expf(sG[63 * KP + cc] - sG[t * KP + cc]);
+        const float e = sE[t * KP + cc], kk = sK[t * KP + cc];
+        rec[L.Qg + i] = sQ[t * KP + cc] * e;
+        rec[L.Kd + i] = kk * expf(sG[63 * KP + cc] - sG[t * KP + cc]);
         if (BWD) {
-            rec[L.Kg + i] = sK[t * KP + cc] * sE[t * KP + cc];
+            rec[L.Kg + i] = kk * e;
             rec[L.G + i] = sG[t * KP + cc];
             rec[L.qh + i] = sQ[t * KP + cc];
-            rec[L.kh + i] = sK[t * KP + cc];
+            rec[L.kh + i] = kk;
         }
+        if (t == kChunk - 1) rec[L.gC + cc] = e;
+        sE[t * KP + cc] = sb[t] * kk * e;
     }
-    // U0 = N Diag(beta) v
-    for (int i = tid; i < kChunk * V; i += blockDim.x) {
-        const int t = i / V, j = i % V;
-        float acc[2] = {0.f, 0.f};
-        int s = 0;
-        for (; s + 1 <= t; s += 2) {
-            acc[0] += sN[t * 65 + s] * sb[s] * sV[s * V + j];
-            acc[1] += sN[t * 65 + s + 1] * sb[s + 1] * sV[(s + 1) * V + j];
-        }
-        if (s == t) acc[0] += sN[t * 65 + s] * sb[s] * sV[s * V + j];
-        rec[L.U0 + i] = acc[0] + acc[1];
+    for (int i = tid; i < kChunk * V; i += blockDim.x) sV[i] *= sb[i / V];
+    __syncthreads();
+    // W = N Kb and U0 = N (beta v): thread (ty, tx) takes rows 4 ty .. 4 ty + 3 and columns tx + 16 j;
+    // N is lower triangular, so the sum stops at s = 4 ty + 3
+    {
+        const int ty = tid >> 4, tx = tid & 15;
+        auto tile = [&](const float* src, int ld, int ncol, float* dst) {
+            float acc[4][8];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[r][q] = 0.f;
+            for (int s = 0; s <= 4 * ty + 3; ++s) {
+                float nv[4], x[8];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) nv[r] = sN[(4 * ty + r) * 65 + s];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) x[q] = tx + 16 * q < ncol ? src[s * ld + tx + 16 * q] : 0.f;
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc[r][q] += nv[r] * x[q];
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (tx + 16 * q < ncol) dst[(4 * ty + r) * ncol + tx + 16 * q] = acc[r][q];
+        };
+        tile(sE, KP, K, rec + L.W);
+        tile(sV, V, V, rec + L.U0);
     }
     for (int i = tid; i < kChunk * kChunk; i += blockDim.x) {
         const int t = i >> 6, s = i & 63;
@@ -324,7 +332,6 @@ __global__ void __launch_bounds__(256) intra_simt_kernel(Params p) {
             rec[L.B + i] = sB[t * 65 + s];
         }
     }
-    for (int cc = tid; cc < K; cc += blockDim.x) rec[L.gC + cc] = sE[63 * KP + cc];
     if (BWD && tid < kChunk) rec[L.beta + tid] = sb[tid];
 }
 
