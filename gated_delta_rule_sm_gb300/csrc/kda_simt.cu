@@ -535,51 +535,165 @@ __global__ void __launch_bounds__(kChainSimtWarps * 32) chain_fwd_simt_kernel(Pa
 
 // Reverse chain of the state gradient:  dU = scale Aqk^T dO + Kd dS_end,
 // dS_begin = Diag(exp(Gamma_last)) dS_end + scale Qg^T dO - W^T dU.
-// Stores dS_end of every chunk for the per-chunk gradient kernel.
-__global__ void __launch_bounds__(256) chain_bwd_simt_kernel(Params p) {
+// Stores dS_end of every chunk for the per-chunk gradient kernel.  Same schedule as the forward
+// chain, walking the chunks backwards: 16 warps, lane = column j; Kd and Aqk of a chunk staged by
+// asynchronous copies during the previous chunk's state update, Qg, W and exp(Gamma_last) during
+// this chunk's dU phase; the next chunk's dO rows are loaded into registers a step ahead.
+__global__ void __launch_bounds__(kChainSimtWarps * 32) chain_bwd_simt_kernel(Params p) {
+    constexpr int NW = kChainSimtWarps, NT = NW * 32;
     const int n = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * 32;
     const int K = p.K, V = p.V, H = p.H;
     const int tid = threadIdx.x, j = tid & 31, grp = tid >> 5;
     const bool jv = (j0 + j) < V;
-    extern __shared__ float sm[];
-    float* sS = sm;              // [K][32]  dS
-    float* sU = sS + K * 32;     // [64][32] dU
-    float* sD = sU + 64 * 32;    // [64][32] dO
+    extern __shared__ __align__(16) float sm[];
+    float* sS = sm;                  // [K][32]  dS
+    float* sU = sS + K * 32;         // [64][32] dU
+    float* sD = sU + 64 * 32;        // [64][32] dO
+    float* sKd = sD + 64 * 32;       // [64][K]
+    float* sA = sKd + 64 * K;        // [64][64] Aqk (zero above the diagonal)
+    float* sQg = sA + 64 * 64;       // [64][K]
+    float* sW = sQg + 64 * K;        // [64][K]
+    float* sgC = sW + 64 * K;        // [K]
     const RecLayout L = RecLayout::make(K, V);
-    for (int cc = grp; cc < K; cc += 8)
-        sS[cc * 32 + j] = (p.dST && jv) ? p.dST[(((size_t)n * H + h) * K + cc) * V + j0 + j] : 0.f;
+    const int KQ = K / 4;
+    auto rec_of = [&](int c) { return p.rec + ((size_t)c * H + h) * p.rec_stride; };
+    auto stage_rows = [&](float* dst, const float* src, int nq) {
+        for (int i = tid; i < nq; i += NT) sm100::cp_async16_zfill(dst + 4 * i, src + 4 * i, 16);
+    };
+    auto stage_ka = [&](int c) {
+        const float* rec = rec_of(c);
+        stage_rows(sKd, rec + L.Kd, 64 * KQ);
+        stage_rows(sA, rec + L.A, 64 * 16);
+    };
+    auto stage_qw = [&](int c) {
+        const float* rec = rec_of(c);
+        stage_rows(sQg, rec + L.Qg, 64 * KQ);
+        stage_rows(sW, rec + L.W, 64 * KQ);
+        stage_rows(sgC, rec + L.gC, KQ);
+    };
+    auto commit = [] { asm volatile("cp.async.commit_group;" ::: "memory"); };
+    auto wait_older = [] { asm volatile("cp.async.wait_group 1;" ::: "memory"); };   // all but the newest group
+    auto state_row = [&](int m, int e) { return 4 * grp + 64 * m + e; };
     const int cb = p.chunk_off[n], ce = p.chunk_off[n + 1];
     const int tb = seg_begin(p, n), te = seg_end(p, n);
-    __syncthreads();
-    for (int c = ce - 1; c >= cb; --c) {
-        const float* rec = p.rec + ((size_t)c * H + h) * p.rec_stride;
+    float dnext[4];                  // dO rows grp + 16 i of the next chunk (going backwards)
+    auto fetch_do = [&](int c) {
         const int tok0 = tb + (c - cb) * kChunk, len = min(kChunk, te - tok0);
-        if (jv)
-            for (int cc = grp; cc < K; cc += 8)
-                p.dstates[(((size_t)c * H + h) * K + cc) * V + j0 + j] = sS[cc * 32 + j];
-        for (int t = grp; t < kChunk; t += 8)
-            sD[t * 32 + j] = (t < len && jv) ? load_act(p.dout, ((size_t)(tok0 + t) * H + h) * V + j0 + j, p.dtype) : 0.f;
-        __syncthreads();
-        for (int t = grp; t < kChunk; t += 8) {
-            float acc = 0.f;
-            const float* kd = rec + L.Kd + t * K;
-            for (int cc = 0; cc < K; ++cc) acc += kd[cc] * sS[cc * 32 + j];
-            float a2 = 0.f;
-            for (int t2 = t; t2 < kChunk; ++t2) a2 += rec[L.A + t2 * kChunk + t] * sD[t2 * 32 + j];
-            sU[t * 32 + j] = acc + p.scale * a2;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = grp + NW * i;
+            dnext[i] = (t < len && jv) ? load_act(p.dout, ((size_t)(tok0 + t) * H + h) * V + j0 + j, p.dtype) : 0.f;
         }
-        __syncthreads();
-        for (int cc = grp; cc < K; cc += 8) {
-            float acc = rec[L.gC + cc] * sS[cc * 32 + j];
-            const float* qg = rec + L.Qg + cc;
-            const float* w = rec + L.W + cc;
-            for (int t = 0; t < kChunk; ++t) acc += p.scale * qg[t * K] * sD[t * 32 + j] - w[t * K] * sU[t * 32 + j];
-            sS[cc * 32 + j] = acc;
-        }
-        __syncthreads();
+    };
+    {
+        float s0[2][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int cc = state_row(m, e);
+                s0[m][e] = (cc < K && p.dST && jv) ? p.dST[(((size_t)n * H + h) * K + cc) * V + j0 + j] : 0.f;
+            }
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (state_row(m, e) < K) sS[state_row(m, e) * 32 + j] = s0[m][e];
     }
+    if (cb < ce) {
+        stage_ka(ce - 1);
+        commit();
+        stage_qw(ce - 1);
+        commit();
+        fetch_do(ce - 1);
+    }
+    for (int c = ce - 1; c >= cb; --c) {
+        const bool more = c > cb;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sD[(grp + NW * i) * 32 + j] = dnext[i];
+        wait_older();                // Kd, Aqk of chunk c (this thread's copies) ...
+        __syncthreads();             // ... every thread's; dO rows written; dS of chunk c final
+        if (more) fetch_do(c - 1);
+        if (jv)
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int cc = state_row(m, e);
+                    if (cc < K) p.dstates[(((size_t)c * H + h) * K + cc) * V + j0 + j] = sS[cc * 32 + j];
+                }
+        // dU = Kd dS + scale Aqk^T dO
+        {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+            for (int c4 = 0; c4 < KQ; ++c4) {
+                const float s0 = sS[(4 * c4) * 32 + j], s1 = sS[(4 * c4 + 1) * 32 + j];
+                const float s2 = sS[(4 * c4 + 2) * 32 + j], s3 = sS[(4 * c4 + 3) * 32 + j];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 k = *reinterpret_cast<const float4*>(sKd + (grp + NW * i) * K + 4 * c4);
+                    acc[i] += k.x * s0 + k.y * s1 + k.z * s2 + k.w * s3;
+                }
+            }
+#pragma unroll 4
+            for (int t2 = 0; t2 < kChunk; ++t2) {
+                const float d = sD[t2 * 32 + j];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) a2[i] += sA[t2 * 64 + grp + NW * i] * d;   // zero for t2 < t
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sU[(grp + NW * i) * 32 + j] = acc[i] + p.scale * a2[i];
+        }
+        __syncthreads();             // dU visible; Kd and Aqk are free
+        if (more) stage_ka(c - 1);
+        commit();
+        wait_older();                // Qg, W, exp(Gamma_last) of chunk c
+        __syncthreads();
+        // dS <- Diag(exp(Gamma_last)) dS + scale Qg^T dO - W^T dU  (rows owned by this thread)
+        {
+            float acc[2][4];
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int cc = state_row(m, e);
+                    acc[m][e] = cc < K ? sgC[cc] * sS[cc * 32 + j] : 0.f;
+                }
+#pragma unroll 2
+            for (int t = 0; t < kChunk; ++t) {
+                const float d = p.scale * sD[t * 32 + j], u = sU[t * 32 + j];
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    if (state_row(m, 0) < K) {
+                        const float4 q = *reinterpret_cast<const float4*>(sQg + t * K + state_row(m, 0));
+                        const float4 w = *reinterpret_cast<const float4*>(sW + t * K + state_row(m, 0));
+                        acc[m][0] += q.x * d - w.x * u;
+                        acc[m][1] += q.y * d - w.y * u;
+                        acc[m][2] += q.z * d - w.z * u;
+                        acc[m][3] += q.w * d - w.w * u;
+                    }
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (state_row(m, e) < K) sS[state_row(m, e) * 32 + j] = acc[m][e];
+        }
+        __syncthreads();             // Qg, W, exp(Gamma_last) and dO are free
+        if (more) stage_qw(c - 1);
+        commit();
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
     if (p.dS0 && jv)
-        for (int cc = grp; cc < K; cc += 8) p.dS0[(((size_t)n * H + h) * K + cc) * V + j0 + j] = sS[cc * 32 + j];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int cc = state_row(m, e);
+                if (cc < K) p.dS0[(((size_t)n * H + h) * K + cc) * V + j0 + j] = sS[cc * 32 + j];
+            }
 }
 
 // ------------------------------------------------------------------ per-chunk gradients
@@ -871,9 +985,12 @@ cudaError_t launch_chain_fwd_simt(const Params& p, bool store_states, cudaStream
 }
 
 cudaError_t launch_chain_bwd_simt(const Params& p, cudaStream_t st) {
-    const size_t smem = (size_t)(p.K * 32 + 2 * 64 * 32) * sizeof(float);
+    // dS, dU, dO; the Kd / Aqk / Qg / W / exp(Gamma_last) fields of one chunk (floats)
+    const size_t smem = (size_t)(p.K * 32 + 2 * 64 * 32 + 3 * 64 * p.K + 64 * 64 + p.K) * sizeof(float);
+    cudaError_t e0 = cudaFuncSetAttribute(chain_bwd_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e0 != cudaSuccess) return e0;
     timing_pre(st, K_CHAIN_BWD_SIMT);
-    chain_bwd_simt_kernel<<<dim3(p.N, p.H, (p.V + 31) / 32), 256, smem, st>>>(p);
+    chain_bwd_simt_kernel<<<dim3(p.N, p.H, (p.V + 31) / 32), kChainSimtWarps * 32, smem, st>>>(p);
     timing_post(st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
