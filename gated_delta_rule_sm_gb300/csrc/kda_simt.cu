@@ -699,16 +699,44 @@ __global__ void __launch_bounds__(kChainSimtWarps * 32) chain_bwd_simt_kernel(Pa
 // ------------------------------------------------------------------ per-chunk gradients
 
 // C[i][j] = alpha * sum_k A(i,k) B(k,j) (+ C[i][j] if acc); element strides given.
-// mask: 0 all, 1 keep j <= i, 2 keep j < i.
+// mask: 0 all, 1 keep j <= i, 2 keep j < i.  M and N are multiples of 4: each thread takes 4 x 4 output
+// tiles and sums over k in order (16 independent accumulators per tile, 8 operand loads per k step);
+// tiles that the mask clears entirely skip the sum.
 __device__ void block_gemm(int M, int N, int Kd, const float* A, int ars, int acs, const float* B, int brs,
                            int bcs, float* C, int crs, float alpha, bool acc, int mask) {
-    for (int idx = threadIdx.x; idx < M * N; idx += blockDim.x) {
-        const int i = idx / N, jj = idx % N;
-        float s = 0.f;
-        const bool keep = mask == 0 || (mask == 1 && jj <= i) || (mask == 2 && jj < i);
-        if (keep)
-            for (int k = 0; k < Kd; ++k) s += A[(size_t)i * ars + (size_t)k * acs] * B[(size_t)k * brs + (size_t)jj * bcs];
-        C[(size_t)i * crs + jj] = alpha * s + (acc ? C[(size_t)i * crs + jj] : 0.f);
+    const int tn = N >> 2, tiles = (M >> 2) * tn;
+    for (int tix = threadIdx.x; tix < tiles; tix += blockDim.x) {
+        const int i0 = (tix / tn) * 4, j0 = (tix % tn) * 4;
+        float s[4][4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) s[r][q] = 0.f;
+        if (mask == 0 || j0 <= i0 + 3) {
+            const float* a0 = A + (size_t)i0 * ars;
+            const float* b0 = B + (size_t)j0 * bcs;
+#pragma unroll 2
+            for (int k = 0; k < Kd; ++k) {
+                float a[4], b[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) a[r] = a0[(size_t)r * ars + (size_t)k * acs];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) b[q] = b0[(size_t)k * brs + (size_t)q * bcs];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) s[r][q] += a[r] * b[q];
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int i = i0 + r, jj = j0 + q;
+                const bool keep = mask == 0 || (mask == 1 && jj <= i) || (mask == 2 && jj < i);
+                float* cp = C + (size_t)i * crs + jj;
+                *cp = (keep ? alpha * s[r][q] : 0.f) + (acc ? *cp : 0.f);
+            }
     }
 }
 
@@ -861,23 +889,34 @@ __global__ void __launch_bounds__(256) grad_simt_kernel(Params p) {
         float alog_part = 0.f;
         for (int cc = tid; cc < K; cc += blockDim.x) {
             float dtb = 0.f;
-            for (int t = 0; t < ch.len; ++t) {
-                const size_t gi = ((size_t)(ch.tok0 + t) * H + h) * K + cc;
-                const float x = load_act(p.g_raw, gi, p.dtype) + p.dt_bias[h * K + cc];
-                if (p.gate == KDA_GATE_SOFTPLUS) {
-                    // g = -e^a softplus(x): dg/dx = -e^a sigmoid(x), dg/da = g
-                    const float dx = -dG[t * K + cc] * ea * sigmoidf_acc(x);
-                    p.dg_raw[gi] = dx;
-                    dtb += dx;
-                    alog_part -= dG[t * K + cc] * ea * softplusf(x);
-                } else {
-                    // g = lb sigmoid(z), z = e^a x: dg/dx = lb sigma'(z) e^a, dg/da = lb sigma'(z) z
-                    const float z = ea * x;
-                    const float sg = sigmoidf_acc(z);
-                    const float dz = dG[t * K + cc] * p.lb * sg * (1.f - sg);
-                    p.dg_raw[gi] = dz * ea;
-                    dtb += dz * ea;
-                    alog_part += dz * z;
+            const float dtbias = p.dt_bias[h * K + cc];
+#pragma unroll 1
+            for (int t0 = 0; t0 < ch.len; t0 += 8) {
+                float xr[8];   // eight tokens' raw gate, loaded before they are used
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    xr[u] = t0 + u < ch.len ? load_act(p.g_raw, ((size_t)(ch.tok0 + t0 + u) * H + h) * K + cc, p.dtype) : 0.f;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int t = t0 + u;
+                    if (t >= ch.len) break;
+                    const size_t gi = ((size_t)(ch.tok0 + t) * H + h) * K + cc;
+                    const float x = xr[u] + dtbias;
+                    if (p.gate == KDA_GATE_SOFTPLUS) {
+                        // g = -e^a softplus(x): dg/dx = -e^a sigmoid(x), dg/da = g
+                        const float dx = -dG[t * K + cc] * ea * sigmoidf_acc(x);
+                        p.dg_raw[gi] = dx;
+                        dtb += dx;
+                        alog_part -= dG[t * K + cc] * ea * softplusf(x);
+                    } else {
+                        // g = lb sigmoid(z), z = e^a x: dg/dx = lb sigma'(z) e^a, dg/da = lb sigma'(z) z
+                        const float z = ea * x;
+                        const float sg = sigmoidf_acc(z);
+                        const float dz = dG[t * K + cc] * p.lb * sg * (1.f - sg);
+                        p.dg_raw[gi] = dz * ea;
+                        dtb += dz * ea;
+                        alog_part += dz * z;
+                    }
                 }
             }
             p.part_dtb[((size_t)c * H + h) * K + cc] = dtb;
