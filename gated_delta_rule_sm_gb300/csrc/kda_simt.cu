@@ -698,50 +698,97 @@ __global__ void __launch_bounds__(kChainSimtWarps * 32) chain_bwd_simt_kernel(Pa
 
 // ------------------------------------------------------------------ per-chunk gradients
 
-// C[i][j] = alpha * sum_k A(i,k) B(k,j) (+ C[i][j] if acc); element strides given.
-// mask: 0 all, 1 keep j <= i, 2 keep j < i.  M and N are multiples of 4: each thread takes 4 x 4 output
-// tiles and sums over k in order (16 independent accumulators per tile, 8 operand loads per k step);
-// tiles that the mask clears entirely skip the sum.
+// C[i][j] = alpha * sum_k A(i,k) B(k,j) (+ C[i][j] if acc); element strides given; M = 64, N <= 128,
+// Kd a multiple of 16.  mask: 0 all, 1 keep j <= i, 2 keep j < i.  Called by the whole CTA: slabs of 16
+// k-steps of A and B are copied into shared memory with coalesced loads (along whichever of the two
+// strides is 1), then each thread accumulates its 4 x 4 output tiles (at most two) from there, summing
+// over k in order.  Tiles that the mask clears entirely skip the sums.
 __device__ void block_gemm(int M, int N, int Kd, const float* A, int ars, int acs, const float* B, int brs,
                            int bcs, float* C, int crs, float alpha, bool acc, int mask) {
+    __shared__ __align__(16) float sa[16][64];    // A slab, k-major
+    __shared__ __align__(16) float sb[16][128];   // B slab, k-major
+    const int tid = threadIdx.x, nthr = blockDim.x;
     const int tn = N >> 2, tiles = (M >> 2) * tn;
-    for (int tix = threadIdx.x; tix < tiles; tix += blockDim.x) {
-        const int i0 = (tix / tn) * 4, j0 = (tix % tn) * 4;
-        float s[4][4];
+    int i0[2], j0[2];
+    bool live[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int tix = tid + u * nthr;
+        i0[u] = tix < tiles ? (tix / tn) * 4 : 0;
+        j0[u] = tix < tiles ? (tix % tn) * 4 : 0;
+        live[u] = tix < tiles && (mask == 0 || j0[u] <= i0[u] + 3);
+    }
+    float s[2][4][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) s[r][q] = 0.f;
-        if (mask == 0 || j0 <= i0 + 3) {
-            const float* a0 = A + (size_t)i0 * ars;
-            const float* b0 = B + (size_t)j0 * bcs;
-#pragma unroll 2
-            for (int k = 0; k < Kd; ++k) {
-                float a[4], b[4];
+            for (int q = 0; q < 4; ++q) s[u][r][q] = 0.f;
+    const bool a_krow = acs == 1;   // A(i, k..k+15) contiguous
+    const bool b_kcol = bcs == 1;   // B(k, j..) contiguous
+    for (int k0 = 0; k0 < Kd; k0 += 16) {
+        __syncthreads();            // the previous slab (or call) is done with the buffers
+        {
+            float va[4], vb[8];
 #pragma unroll
-                for (int r = 0; r < 4; ++r) a[r] = a0[(size_t)r * ars + (size_t)k * acs];
+            for (int e = 0; e < 4; ++e) {   // 64 x 16 elements of A, 4 per thread
+                const int x = tid + e * nthr;
+                const int i = a_krow ? x >> 4 : x & 63, k = a_krow ? x & 15 : x >> 6;
+                va[e] = x < M * 16 ? A[(size_t)i * ars + (size_t)(k0 + k) * acs] : 0.f;
+            }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) b[q] = b0[(size_t)k * brs + (size_t)q * bcs];
+            for (int e = 0; e < 8; ++e) {   // 16 x N elements of B, up to 8 per thread
+                const int x = tid + e * nthr;
+                const int j = b_kcol ? x % N : x >> 4, k = b_kcol ? x / N : x & 15;
+                vb[e] = x < N * 16 ? B[(size_t)(k0 + k) * brs + (size_t)j * bcs] : 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int x = tid + e * nthr;
+                const int i = a_krow ? x >> 4 : x & 63, k = a_krow ? x & 15 : x >> 6;
+                if (x < M * 16) sa[k][i] = va[e];
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int x = tid + e * nthr;
+                const int j = b_kcol ? x % N : x >> 4, k = b_kcol ? x / N : x & 15;
+                if (x < N * 16) sb[k][j] = vb[e];
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (!live[u]) continue;
+#pragma unroll 4
+            for (int k = 0; k < 16; ++k) {
+                const float4 a = *reinterpret_cast<const float4*>(&sa[k][i0[u]]);
+                const float4 b = *reinterpret_cast<const float4*>(&sb[k][j0[u]]);
+                const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) s[r][q] += a[r] * b[q];
+                    for (int q = 0; q < 4; ++q) s[u][r][q] += av[r] * bv[q];
             }
         }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        if (tid + u * nthr >= tiles) continue;
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const int i = i0 + r, jj = j0 + q;
+                const int i = i0[u] + r, jj = j0[u] + q;
                 const bool keep = mask == 0 || (mask == 1 && jj <= i) || (mask == 2 && jj < i);
                 float* cp = C + (size_t)i * crs + jj;
-                *cp = (keep ? alpha * s[r][q] : 0.f) + (acc ? *cp : 0.f);
+                *cp = (keep ? alpha * s[u][r][q] : 0.f) + (acc ? *cp : 0.f);
             }
     }
 }
 
 // One (chunk, head) item per loop trip; per-CTA scratch in global memory.
-__global__ void __launch_bounds__(256) grad_simt_kernel(Params p) {
+__global__ void __launch_bounds__(256, 2) grad_simt_kernel(Params p) {
     const int K = p.K, V = p.V, H = p.H;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int NC = p.chunk_off[p.N];
@@ -795,11 +842,13 @@ __global__ void __launch_bounds__(256) grad_simt_kernel(Params p) {
         for (int i = tid; i < kChunk * kChunk; i += blockDim.x) dN[i] = dT[i] * beta[i & 63];
         if (tid < kChunk) {
             float s = 0.f;
+#pragma unroll 8
             for (int t = 0; t < kChunk; ++t) s += rec[L.N + t * kChunk + tid] * dT[t * kChunk + tid];
             dbeta[tid] = s;
         }
         for (int cc = tid; cc < K; cc += blockDim.x) {
             float s = 0.f;
+#pragma unroll 8
             for (int jj = 0; jj < V; ++jj) s += dSC[cc * V + jj] * S0[cc * V + jj];
             s_dgc[cc] = rec[L.gC + cc] * s;
         }
@@ -812,6 +861,7 @@ __global__ void __launch_bounds__(256) grad_simt_kernel(Params p) {
         // dbeta_t += sum_s dL[t][s] B[t][s] ; dB = beta_t dL (kept in dL)
         if (tid < kChunk) {
             float s = 0.f;
+#pragma unroll 8
             for (int ss = 0; ss < tid; ++ss) s += dL[tid * kChunk + ss] * rec[L.B + tid * kChunk + ss];
             dbeta[tid] += s;
         }
@@ -831,11 +881,13 @@ __global__ void __launch_bounds__(256) grad_simt_kernel(Params p) {
             // the cumulative sum, scaled by |g| in d a_log) and added to dq, dk directly.
             const float dadiag = dA[t * kChunk + t];
             float aq = 0.f, akl = 0.f, akr = 0.f;
+#pragma unroll 8
             for (int s = 0; s < t; ++s) {
                 const float e = expf(gt - G[s * K + cc]);
                 aq += dA[t * kChunk + s] * kh[s * K + cc] * e;
                 akl += dL[t * kChunk + s] * kh[s * K + cc] * e;
             }
+#pragma unroll 8
             for (int t2 = t + 1; t2 < kChunk; ++t2) {
                 const float e = expf(G[t2 * K + cc] - gt);
                 akr += (dA[t2 * kChunk + t] * qh[t2 * K + cc] + dL[t2 * kChunk + t] * kh[t2 * K + cc]) * e;
@@ -854,11 +906,13 @@ __global__ void __launch_bounds__(256) grad_simt_kernel(Params p) {
         // whose exponent holds g_r for t < r only (an exclusive prefix sum, so no +x - x cancellation)
         for (int cc = tid; cc < K; cc += blockDim.x) {
             float run = 0.f;
+#pragma unroll 8
             for (int t = kChunk - 1; t >= 0; --t) {
                 run += dG[t * K + cc];
                 dG[t * K + cc] = run;
             }
             float pre = s_dgc[cc];
+#pragma unroll 8
             for (int t = 0; t < kChunk; ++t) {
                 dG[t * K + cc] += pre;
                 pre += dKd[t * K + cc] * rec[L.Kd + t * K + cc];
