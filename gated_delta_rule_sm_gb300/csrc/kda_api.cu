@@ -570,7 +570,8 @@ kda_status kda_fwd_segmented(const kda_dims* dims, const void* q, const void* k,
                                    row_piece, p.status, stream));
     KDA_TRY_CUDA(launch_plan(pp, stream));
     if (pp.diag) KDA_TRY_CUDA(launch_diag_tc(pp, stream));
-    KDA_TRY_CUDA(launch_intra_tc(pp, recs, 0, stream));
+    if (!pp.diag) KDA_TRY_CUDA(launch_intra2(pp, recs, stream));   // the chain record, as in kda_fwd
+    else KDA_TRY_CUDA(launch_intra_tc(pp, recs, 0, stream));
     Params pa = pp;   // local end states: from zero, no output
     pa.S0 = nullptr;
     pa.out = nullptr;
