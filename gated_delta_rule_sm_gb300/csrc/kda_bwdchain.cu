@@ -15,8 +15,9 @@
 // dS, NumPy emulation and GPU measurement agree) put it outside the bf16 tolerance under slowly
 // decaying gates.
 //
-// One CTA of 128 threads per (segment, head, column slice of JW value columns); the columns of Z
-// are independent.  Thread r owns row r of Z.  Per chunk: MMA1 (M = 64, N = JW, K = 128) into TMEM,
+// One CTA per (segment, head, column slice of JW value columns); the columns of Z are independent.
+// Thread r owns row r of Z (128 threads), or for JW >= 64 threads r and r + 128 own its two column
+// halves (256 threads: the TMEM read-backs, splits and stores of a step spread over twice the warps).  Per chunk: MMA1 (M = 64, N = JW, K = 128) into TMEM,
 // X = D1 + Y split into bf16 hi + lo (MN-major, one 16-byte store per 8 columns), MMA2 (M = 128,
 // N = JW, K = 64), then Z' = gC Z + D3 (+ P).  Record slots (A1, A2 hi/lo, gC) are double buffered
 // by bulk copies.  X (U, or dU) and the chunk's Z are also written out per chunk for the gradient
@@ -51,6 +52,9 @@ struct ChainSrc {
 };
 
 namespace bwchain {
+// Threads per CTA: 128 (one per row of Z), or 256 for JW >= 64 (two per row, half the columns each).
+__host__ __device__ constexpr int threads(int jw) { return jw >= 64 ? 256 : 128; }
+
 template <int JW>
 struct Lay {
     static constexpr uint32_t SLOT = chainrec::SLOT;       // two record slots at 0 and SLOT
@@ -79,7 +83,7 @@ __device__ __forceinline__ void split8_bf16(const float* x, uint4& hi, uint4& lo
 }
 
 template <int JW, bool REV, int MODE>
-__global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc src) {
+__global__ void __launch_bounds__(bwchain::threads(JW), 1) chain_split_kernel(Params p, ChainSrc src) {
     using L = bwchain::Lay<JW>;
     extern __shared__ __align__(1024) uint8_t smem[];
     int n, h, j0;
@@ -96,6 +100,10 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
     const int H = p.H;
     constexpr int K = 128, V = 128;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // JW >= 64: two threads per row of Z, each with JH of the slice's columns (warps 4-7 read the same
+    // TMEM lane quarters as warps 0-3, at column offset JH)
+    constexpr int JH = JW / (bwchain::threads(JW) / 128);
+    const int row = tid & 127, jo = (tid >> 7) * JH, quarter = warp & 3;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR);
     uint64_t* bar1 = full + 2;
     uint64_t* bar2 = full + 3;
@@ -116,25 +124,25 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
     if (warp == 0) tmem_alloc(tslot, L::TCOLS);
     // local and transfer passes write only the end state; the transfer pass takes Y and P as zero
     constexpr bool full_pass = MODE == kBwdChainFull, zero_y = MODE == kBwdChainTransfer;
-    float z[JW];   // row tid of Z (dS for the reverse chain, S for the recompute)
+    float z[JH];   // columns jo .. jo + JH - 1 of row `row` of Z (dS for the reverse chain, S for the recompute)
     {
         const float* z0 = full_pass ? (REV ? p.dST : p.S0) : nullptr;
-        const float* zs = z0 ? z0 + (((size_t)n * H + h) * K + tid) * V + j0 : nullptr;
+        const float* zs = z0 ? z0 + (((size_t)n * H + h) * K + row) * V + j0 + jo : nullptr;
 #pragma unroll
-        for (int j = 0; j < JW; j += 4) {
+        for (int j = 0; j < JH; j += 4) {
             const float4 v = zs ? *reinterpret_cast<const float4*>(zs + j) : make_float4(0.f, 0.f, 0.f, 0.f);
             z[j] = v.x; z[j + 1] = v.y; z[j + 2] = v.z; z[j + 3] = v.w;
         }
-        if (zero_y)   // the identity (K = V): row tid has its one in column tid
+        if (zero_y)   // the identity (K = V): row r has its one in column r
 #pragma unroll
-            for (int j = 0; j < JW; ++j) z[j] = (j0 + j == tid) ? 1.f : 0.f;
+            for (int j = 0; j < JH; ++j) z[j] = (j0 + jo + j == row) ? 1.f : 0.f;
     }
     auto write_z_operand = [&]() {   // thread = K index c: eight j per 16-byte row of a core matrix
 #pragma unroll
-        for (int jg = 0; jg < JW / 8; ++jg) {
+        for (int jg = 0; jg < JH / 8; ++jg) {
             uint4 hi, lo;
             split8_bf16(z + 8 * jg, hi, lo);
-            const uint32_t o = mn_bf16(8 * jg, tid, 128, L::ZK);
+            const uint32_t o = mn_bf16(jo + 8 * jg, row, 128, L::ZK);
             *reinterpret_cast<uint4*>(ZB + o) = hi;
             *reinterpret_cast<uint4*>(ZL + o) = lo;
         }
@@ -146,7 +154,7 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tD1 = tmem, tD3 = tmem + JW;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     auto slot_ptr = [&](int s) { return smem + (s & 1) * L::SLOT; };
     // step s handles chunk cb + nch - 1 - s (reverse) or cb + s (forward)
     auto chunk_of = [&](int s) { return REV ? cb + nch - 1 - s : cb + s; };
@@ -203,13 +211,13 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
             // chunk c (x4 order: the warp's 32 rows make 512 contiguous bytes per 16-byte store)
             float* dst = (REV ? p.dstates : p.states) + ((size_t)c * H + h) * K * V;
 #pragma unroll
-            for (int j = 0; j < JW; j += 4)
-                *reinterpret_cast<float4*>(dst + x4_off(tid, j0 + j, K)) = make_float4(z[j], z[j + 1], z[j + 2], z[j + 3]);
+            for (int j = 0; j < JH; j += 4)
+                *reinterpret_cast<float4*>(dst + x4_off(row, j0 + jo + j, K)) = make_float4(z[j], z[j + 1], z[j + 2], z[j + 3]);
         }
         // X rows t = 16 warp + lane (lanes 0..15 of each warp carry the M = 64 result).  The Y row is
         // read from global memory 32 columns ahead of its use: the first block before MMA1 is waited
         // for, each next block while the current one is combined.
-        const int t = 16 * warp + (lane & 15);
+        const int t = 16 * quarter + (lane & 15);
         // 32 columns from col of row `row` of a tile with `rows` rows, x4-ordered or row-major
         auto load32 = [](const float* tile, int row, int col, int rows, bool x4, float* dst) {
             if (zero_y) {
@@ -226,19 +234,19 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
         };
         const float* ytile = y_ptr(s);
         float ynext[32];
-        load32(ytile, t, j0, 64, REV, ynext);
+        load32(ytile, t, j0 + jo, 64, REV, ynext);
         fail_wait(bar1, par);
         tc_fence_after();
         {
 #pragma unroll
-            for (int jb = 0; jb < JW; jb += 32) {
+            for (int jb = 0; jb < JH; jb += 32) {
                 float d[32];
-                tmem_ld16(tD1 + jb + lane_base, d);
-                tmem_ld16(tD1 + jb + 16 + lane_base, d + 16);
+                tmem_ld16(tD1 + jo + jb + lane_base, d);
+                tmem_ld16(tD1 + jo + jb + 16 + lane_base, d + 16);
                 float y[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) y[j] = ynext[j];
-                if (jb + 32 < JW) load32(ytile, t, j0 + jb + 32, 64, REV, ynext);
+                if (jb + 32 < JH) load32(ytile, t, j0 + jo + jb + 32, 64, REV, ynext);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) d[j] += y[j];
@@ -246,7 +254,7 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
                     float* xo = (REV ? p.chunk_du : p.chunk_u) + ((size_t)c * H + h) * 64 * V;
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4*>(xo + x4_off(t, j0 + jb + j, 64)) =
+                        *reinterpret_cast<float4*>(xo + x4_off(t, j0 + jo + jb + j, 64)) =
                             make_float4(d[j], d[j + 1], d[j + 2], d[j + 3]);
                 }
                 if (lane < 16)
@@ -254,7 +262,7 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
                     for (int g8 = 0; g8 < 4; ++g8) {
                         uint4 hi, lo;
                         split8_bf16(d + 8 * g8, hi, lo);
-                        const uint32_t o = mn_bf16(jb + 8 * g8, t, 128, L::XK);
+                        const uint32_t o = mn_bf16(jo + jb + 8 * g8, t, 128, L::XK);
                         *reinterpret_cast<uint4*>(XB + o) = hi;
                         *reinterpret_cast<uint4*>(XL + o) = lo;
                     }
@@ -273,20 +281,20 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
         // the P row likewise, one 32-column block ahead (reverse chain only)
         const float* ptile = REV ? p_ptr(s) : nullptr;
         float pnext[32];
-        if (REV) load32(ptile, tid, j0, K, true, pnext);
+        if (REV) load32(ptile, row, j0 + jo, K, true, pnext);
         fail_wait(bar2, par);
         tc_fence_after();
         {
-            const float gc = reinterpret_cast<const float*>(sl + chainrec::GC)[tid];
+            const float gc = reinterpret_cast<const float*>(sl + chainrec::GC)[row];
 #pragma unroll
-            for (int jb = 0; jb < JW; jb += 32) {
+            for (int jb = 0; jb < JH; jb += 32) {
                 float d[32];
-                tmem_ld16(tD3 + jb + lane_base, d);
-                tmem_ld16(tD3 + jb + 16 + lane_base, d + 16);
+                tmem_ld16(tD3 + jo + jb + lane_base, d);
+                tmem_ld16(tD3 + jo + jb + 16 + lane_base, d + 16);
                 float pv[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) pv[j] = REV ? pnext[j] : 0.f;
-                if (REV && jb + 32 < JW) load32(ptile, tid, j0 + jb + 32, K, true, pnext);
+                if (REV && jb + 32 < JH) load32(ptile, row, j0 + jo + jb + 32, K, true, pnext);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) z[jb + j] = gc * z[jb + j] + d[j] + pv[j];
@@ -317,9 +325,9 @@ __global__ void __launch_bounds__(128, 1) chain_split_kernel(Params p, ChainSrc 
             }
         }
     } else if (REV ? p.dS0 != nullptr : p.ST != nullptr) {
-        float* dst = (REV ? p.dS0 : p.ST) + (((size_t)n * H + h) * K + tid) * V + j0;
+        float* dst = (REV ? p.dS0 : p.ST) + (((size_t)n * H + h) * K + row) * V + j0 + jo;
 #pragma unroll
-        for (int j = 0; j < JW; j += 4)
+        for (int j = 0; j < JH; j += 4)
             *reinterpret_cast<float4*>(dst + j) = make_float4(z[j], z[j + 1], z[j + 2], z[j + 3]);
     }
     tc_fence_before();
@@ -340,9 +348,9 @@ static cudaError_t launch_chain_jw(const Params& p, const ChainSrc& src, cudaStr
     ChainSrc s2 = src;
     s2.rank_major = p.N <= 65535;   // segments in launch order, longest first (grid y holds at most 65535)
     if (s2.rank_major)
-        kern<<<dim3(p.H * (128 / JW), p.N), 128, L::BYTES, st>>>(p, s2);
+        kern<<<dim3(p.H * (128 / JW), p.N), bwchain::threads(JW), L::BYTES, st>>>(p, s2);
     else
-        kern<<<dim3(p.N, p.H, 128 / JW), 128, L::BYTES, st>>>(p, s2);
+        kern<<<dim3(p.N, p.H, 128 / JW), bwchain::threads(JW), L::BYTES, st>>>(p, s2);
     timing_post(st);
     return cudaGetLastError();
 }
