@@ -53,7 +53,7 @@ struct ChainSrc {
 
 namespace bwchain {
 // Threads per CTA: 128 (one per row of Z), or 256 for JW >= 64 (two per row, half the columns each).
-__host__ __device__ constexpr int threads(int jw) { return jw >= 64 ? 256 : 128; }
+__host__ __device__ constexpr int threads(int jw) { return jw >= 128 ? 512 : jw >= 64 ? 256 : 128; }
 
 template <int JW>
 struct Lay {
