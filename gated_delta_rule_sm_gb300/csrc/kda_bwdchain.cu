@@ -52,8 +52,9 @@ struct ChainSrc {
 };
 
 namespace bwchain {
-// Threads per CTA: 128 (one per row of Z), or 256 for JW >= 64 (two per row, half the columns each).
-__host__ __device__ constexpr int threads(int jw) { return jw >= 128 ? 512 : jw >= 64 ? 256 : 128; }
+// Threads per CTA: 256 (two per row of Z, half the slice's columns each), or 512 for JW = 128 (four per
+// row, 32 columns each).
+__host__ __device__ constexpr int threads(int jw) { return jw >= 128 ? 512 : 256; }
 
 template <int JW>
 struct Lay {
@@ -103,6 +104,7 @@ __global__ void __launch_bounds__(bwchain::threads(JW), 1) chain_split_kernel(Pa
     // JW >= 64: two threads per row of Z, each with JH of the slice's columns (warps 4-7 read the same
     // TMEM lane quarters as warps 0-3, at column offset JH)
     constexpr int JH = JW / (bwchain::threads(JW) / 128);
+    constexpr int BLK = JH < 32 ? JH : 32;   // columns per TMEM read-back block
     const int row = tid & 127, jo = (tid >> 7) * JH, quarter = warp & 3;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR);
     uint64_t* bar1 = full + 2;
@@ -219,47 +221,47 @@ __global__ void __launch_bounds__(bwchain::threads(JW), 1) chain_split_kernel(Pa
         // for, each next block while the current one is combined.
         const int t = 16 * quarter + (lane & 15);
         // 32 columns from col of row `row` of a tile with `rows` rows, x4-ordered or row-major
-        auto load32 = [](const float* tile, int row, int col, int rows, bool x4, float* dst) {
+        auto load32 = [](const float* tile, int row, int col, int rows, bool x4, float* dst) {   // BLK columns
             if (zero_y) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) dst[j] = 0.f;
+                for (int j = 0; j < BLK; ++j) dst[j] = 0.f;
                 return;
             }
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
+            for (int j = 0; j < BLK; j += 4) {
                 const float4 v = *reinterpret_cast<const float4*>(tile + (x4 ? x4_off(row, col + j, rows)
                                                                               : (size_t)row * V + col + j));
                 dst[j] = v.x; dst[j + 1] = v.y; dst[j + 2] = v.z; dst[j + 3] = v.w;
             }
         };
         const float* ytile = y_ptr(s);
-        float ynext[32];
+        float ynext[BLK];
         load32(ytile, t, j0 + jo, 64, REV, ynext);
         fail_wait(bar1, par);
         tc_fence_after();
         {
 #pragma unroll
-            for (int jb = 0; jb < JH; jb += 32) {
-                float d[32];
+            for (int jb = 0; jb < JH; jb += BLK) {
+                float d[BLK];
                 tmem_ld16(tD1 + jo + jb + lane_base, d);
-                tmem_ld16(tD1 + jo + jb + 16 + lane_base, d + 16);
-                float y[32];
+                if (BLK == 32) tmem_ld16(tD1 + jo + jb + 16 + lane_base, d + 16);
+                float y[BLK];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) y[j] = ynext[j];
-                if (jb + 32 < JH) load32(ytile, t, j0 + jo + jb + 32, 64, REV, ynext);
+                for (int j = 0; j < BLK; ++j) y[j] = ynext[j];
+                if (jb + BLK < JH) load32(ytile, t, j0 + jo + jb + BLK, 64, REV, ynext);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) d[j] += y[j];
+                for (int j = 0; j < BLK; ++j) d[j] += y[j];
                 if (full_pass && lane < 16) {   // X row t (U or dU) for the gradient kernel, x4 order
                     float* xo = (REV ? p.chunk_du : p.chunk_u) + ((size_t)c * H + h) * 64 * V;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
+                    for (int j = 0; j < BLK; j += 4)
                         *reinterpret_cast<float4*>(xo + x4_off(t, j0 + jo + jb + j, 64)) =
                             make_float4(d[j], d[j + 1], d[j + 2], d[j + 3]);
                 }
                 if (lane < 16)
 #pragma unroll
-                    for (int g8 = 0; g8 < 4; ++g8) {
+                    for (int g8 = 0; g8 < BLK / 8; ++g8) {
                         uint4 hi, lo;
                         split8_bf16(d + 8 * g8, hi, lo);
                         const uint32_t o = mn_bf16(jo + jb + 8 * g8, t, 128, L::XK);
@@ -280,24 +282,24 @@ __global__ void __launch_bounds__(bwchain::threads(JW), 1) chain_split_kernel(Pa
         }
         // the P row likewise, one 32-column block ahead (reverse chain only)
         const float* ptile = REV ? p_ptr(s) : nullptr;
-        float pnext[32];
+        float pnext[BLK];
         if (REV) load32(ptile, row, j0 + jo, K, true, pnext);
         fail_wait(bar2, par);
         tc_fence_after();
         {
             const float gc = reinterpret_cast<const float*>(sl + chainrec::GC)[row];
 #pragma unroll
-            for (int jb = 0; jb < JH; jb += 32) {
-                float d[32];
+            for (int jb = 0; jb < JH; jb += BLK) {
+                float d[BLK];
                 tmem_ld16(tD3 + jo + jb + lane_base, d);
-                tmem_ld16(tD3 + jo + jb + 16 + lane_base, d + 16);
-                float pv[32];
+                if (BLK == 32) tmem_ld16(tD3 + jo + jb + 16 + lane_base, d + 16);
+                float pv[BLK];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) pv[j] = REV ? pnext[j] : 0.f;
-                if (REV && jb + 32 < JH) load32(ptile, row, j0 + jo + jb + 32, K, true, pnext);
+                for (int j = 0; j < BLK; ++j) pv[j] = REV ? pnext[j] : 0.f;
+                if (REV && jb + BLK < JH) load32(ptile, row, j0 + jo + jb + BLK, K, true, pnext);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) z[jb + j] = gc * z[jb + j] + d[j] + pv[j];
+                for (int j = 0; j < BLK; ++j) z[jb + j] = gc * z[jb + j] + d[j] + pv[j];
             }
             write_z_operand();
         }
