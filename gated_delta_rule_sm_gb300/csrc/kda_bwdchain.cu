@@ -16,8 +16,9 @@
 // decaying gates.
 //
 // One CTA per (segment, head, column slice of JW value columns); the columns of Z are independent.
-// Thread r owns row r of Z (128 threads), or for JW >= 64 threads r and r + 128 own its two column
-// halves (256 threads: the TMEM read-backs, splits and stores of a step spread over twice the warps).  Per chunk: MMA1 (M = 64, N = JW, K = 128) into TMEM,
+// Row r of Z belongs to threads r + 128 i, each with JH consecutive columns of the slice (bwchain::
+// threads: 256 threads of JW / 2 columns for JW = 32 or 64, 512 threads of 32 columns for JW = 128), so
+// the TMEM read-backs, hi / lo splits and stores of a step spread over 8 or 16 warps.  Per chunk: MMA1 (M = 64, N = JW, K = 128) into TMEM,
 // X = D1 + Y split into bf16 hi + lo (MN-major, one 16-byte store per 8 columns), MMA2 (M = 128,
 // N = JW, K = 64), then Z' = gC Z + D3 (+ P).  Record slots (A1, A2 hi/lo, gC) are double buffered
 // by bulk copies.  X (U, or dU) and the chunk's Z are also written out per chunk for the gradient
