@@ -31,6 +31,7 @@ def main(argv=None) -> None:
     ap.add_argument("--dtype", choices=("bf16", "fp32"), help="activation dtype (fp32 runs the SIMT path)")
     ap.add_argument("--Hk", type=int, help="key heads (H a multiple of it; grouped heads)")
     ap.add_argument("--final-state", action="store_true", help="also write the final state")
+    ap.add_argument("--initial-state", action="store_true", help="also read an initial state")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=0, help="untimed iterations before the timed ones")
     ap.add_argument("--kernels", action="store_true", help="also print each kernel's mean time (library events)")
@@ -51,6 +52,8 @@ def main(argv=None) -> None:
                               ("V", a.D)) if v is not None}
     if a.final_state:
         over["final_state"] = True
+    if a.initial_state:
+        over["initial_state"] = True
     if over:
         if w.varlen and ("B" in over or "T" in over):
             raise SystemExit("varlen workloads keep their packed length")
