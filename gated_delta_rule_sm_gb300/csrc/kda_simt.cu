@@ -993,20 +993,29 @@ __global__ void __launch_bounds__(256, 2) grad_simt_kernel(Params p) {
 }
 
 // Deterministic reduction of the per-chunk parameter partials.
-__global__ void param_reduce_kernel(Params p) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+__global__ void __launch_bounds__(256) param_reduce_kernel(Params p) {
+    // Block b < nb: 32 consecutive entries i of d dt_bias (i = h K + c); the blocks after: 32 heads of
+    // d a_log.  Warp w sums the chunks c = w, w + 8, ... (lane = entry; one 128-byte row per step) and
+    // the eight warp sums are added in warp order: a fixed order, so the result is deterministic.
+    __shared__ float part[8][32];
     const int NC = p.chunk_off[p.N];
-    const int HK = p.H * p.K;
-    if (i < HK) {
-        const int h = i / p.K, cc = i % p.K;
-        float s = 0.f;
-        for (int c = 0; c < NC; ++c) s += p.part_dtb[((size_t)c * p.H + h) * p.K + cc];
-        p.ddt_bias[i] = s;
-    } else if (i < HK + p.H) {
-        const int h = i - HK;
-        float s = 0.f;
-        for (int c = 0; c < NC; ++c) s += p.part_alog[(size_t)c * p.H + h];
-        p.da_log[h] = s;
+    const int HK = p.H * p.K, nb = (HK + 31) / 32;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const bool dtb = (int)blockIdx.x < nb;
+    const int i = (dtb ? (int)blockIdx.x : (int)blockIdx.x - nb) * 32 + lane;
+    const int n = dtb ? HK : p.H;
+    const float* src = dtb ? p.part_dtb : p.part_alog;
+    float s = 0.f;
+    if (i < n)
+#pragma unroll 4
+        for (int c = w; c < NC; c += 8) s += src[(size_t)c * n + i];
+    part[w][lane] = s;
+    __syncthreads();
+    if (w == 0 && i < n) {
+        float t = 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) t += part[u][lane];
+        (dtb ? p.ddt_bias : p.da_log)[i] = t;
     }
 }
 
@@ -1106,9 +1115,9 @@ cudaError_t launch_grad_simt(const Params& p, cudaStream_t st) {
 }
 
 cudaError_t launch_param_reduce(const Params& p, cudaStream_t st) {
-    const int total = p.H * p.K + p.H;
+    const int blocks = (p.H * p.K + 31) / 32 + (p.H + 31) / 32;
     timing_pre(st, K_PARAM_REDUCE);
-    param_reduce_kernel<<<(total + 255) / 256, 256, 0, st>>>(p);
+    param_reduce_kernel<<<blocks, 256, 0, st>>>(p);
     timing_post(st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.G == 1) return e;
