@@ -172,8 +172,9 @@ __global__ void __launch_bounds__(bwchain::threads(JW), 1) chain_split_kernel(Pa
             mbar_expect_tx(&full[s], L::SLOT);
             bulk_g2s(slot_ptr(s), rec_ptr(s), L::SLOT, &full[s]);
         }
-    // D += hi*hi + hi*lo + lo*hi, the small products first.  A: start advance per K = 16 step, LBO, SBO
-    // (K-major: 256, 128, 2048; the same tile as MN-major transpose: 4096, 2048, 128); B: MN-major.
+    // D += hi*hi + hi*lo + lo*hi, the small products first.  A: start advance per K = 16 step, LBO, SBO.
+    // The slot tiles are [128 c][64 t] K-major: A2 (M = c, K = t) reads them K-major (256, 128, 1024), A1
+    // (M = t, K = c) as their MN-major transpose (2048, 1024, 128); B: MN-major.
     auto mma3 = [](uint32_t d, uint32_t ah, uint32_t al, uint32_t bh, uint32_t bl, int nk, uint32_t a_step,
                    uint32_t a_lbo, uint32_t a_sbo, uint32_t b_lbo, uint32_t idesc) {
         for (int kk = 0; kk < nk; ++kk)
@@ -196,8 +197,8 @@ __global__ void __launch_bounds__(bwchain::threads(JW), 1) chain_split_kernel(Pa
         fail_wait(&full[s & 1], (s >> 1) & 1);
         tc_fence_after();
         if (tid == 0) {   // D1 = A1 Z  (M = 64, N = JW, K = 128)
-            mma3(tD1, smem_u32(sl + A1), smem_u32(sl + A1L), smem_u32(ZB), smem_u32(ZL), 8, 256, 128, 2048, L::ZK,
-                 idesc_bf16(64, JW, 0, 1));
+            mma3(tD1, smem_u32(sl + A1), smem_u32(sl + A1L), smem_u32(ZB), smem_u32(ZL), 8, 2048, 1024, 128, L::ZK,
+                 idesc_bf16(64, JW, 1, 1));
             mma_commit(bar1);
             if (s + 1 < nch && !zero_y) {   // warm L2 with the next chunk's Y (and P)
                 asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(y_ptr(s + 1))),
@@ -277,8 +278,8 @@ __global__ void __launch_bounds__(bwchain::threads(JW), 1) chain_split_kernel(Pa
         tc_fence_after();
         if (*sh_fail) { ok = false; break; }
         if (tid == 0) {   // D3 = A2 X  (M = 128, N = JW, K = 64)
-            mma3(tD3, smem_u32(sl + A2), smem_u32(sl + A2L), smem_u32(XB), smem_u32(XL), 4, 4096, 2048, 128, L::XK,
-                 idesc_bf16(128, JW, 1, 1));
+            mma3(tD3, smem_u32(sl + A2), smem_u32(sl + A2L), smem_u32(XB), smem_u32(XL), 4, 256, 128, 1024, L::XK,
+                 idesc_bf16(128, JW, 0, 1));
             mma_commit(bar2);
         }
         // the P row likewise, one 32-column block ahead (reverse chain only)
@@ -372,7 +373,9 @@ static cudaError_t launch_chain(const Params& p, const ChainSrc& src, cudaStream
 }
 
 cudaError_t launch_chain_bwd_tc(const Params& p, const uint8_t* bw, cudaStream_t st, int mode) {
-    ChainSrc src{bw, bwrec::BYTES, reinterpret_cast<const float*>(bw + bwrec::Y), bwrec::BYTES / 4,
+    const RecLayout L = RecLayout::make(128, 128);   // the slot leads each chunk's record (W, Kd, gC)
+    ChainSrc src{reinterpret_cast<const uint8_t*>(p.rec + L.W), p.rec_stride * sizeof(float),
+                 reinterpret_cast<const float*>(bw + bwrec::Y), bwrec::BYTES / 4,
                  reinterpret_cast<const float*>(bw + bwrec::P), bwrec::BYTES / 4, mode, 0};
     static_assert(bwrec::BYTES % 256 == 0, "record stride");
     return launch_chain<true>(p, src, st);
@@ -380,7 +383,8 @@ cudaError_t launch_chain_bwd_tc(const Params& p, const uint8_t* bw, cudaStream_t
 
 cudaError_t launch_chain_rec_tc(const Params& p, const uint8_t* bw, cudaStream_t st, int mode) {
     const RecLayout L = RecLayout::make(128, 128);
-    ChainSrc src{bw, bwrec::BYTES, p.rec + L.U0, p.rec_stride, nullptr, 0, mode, 0};
+    ChainSrc src{reinterpret_cast<const uint8_t*>(p.rec + L.W), p.rec_stride * sizeof(float), p.rec + L.U0,
+                 p.rec_stride, nullptr, 0, mode, 0};
     return launch_chain<false>(p, src, st);
 }
 

@@ -1018,9 +1018,9 @@ __global__ void __launch_bounds__(256, 1) grad_tc_kernel(Params p) {
 // ------------------------------------------------------------------ reverse-chain operands
 //
 // Per (chunk, head): the dS-independent terms of the reverse recursion, Y = scale Aqk^T dO and
-// P = scale Qg^T dO (warp tf32 MMAs with the left operand split into hi + lo; dO is bf16 and exact
-// in tf32), plus the split bf16 operand slot of the two tcgen05 chains of the backward (Kd and -W,
-// record layout chainrec / bwrec).
+// P = scale Qg^T dO (bf16 warp MMAs with the left operand split into hi + lo; dO is bf16 and exact),
+// into the backward workspace record (bwrec).  The chains' split bf16 operand slot (Kd and -W,
+// chainrec) is written by the intra pass itself, at the head of each chunk's record.
 namespace {
 constexpr int PB_A = 0;                  // [64][P64]   Aqk
 constexpr int PB_Q = PB_A + 64 * P64;    // [64][P128]  Qg
@@ -1065,40 +1065,6 @@ __global__ void __launch_bounds__(256, 3) bwd_pre_kernel(Params p, uint8_t* bw) 
         else
             *reinterpret_cast<uint4*>(sD + t * PD16 + j8) = make_uint4(0u, 0u, 0u, 0u);
     }
-    // Chain operands: Kd and -W as bf16 hi + lo [64 t][128 c] K-major tiles (one slot for both chains)
-    auto put_split8 = [](uint8_t* base, uint32_t o, uint32_t lo_off, const float* v, float sg) {
-        float hv[8], lv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float x = sg * v[e];
-            hv[e] = __bfloat162float(__float2bfloat16_rn(x));
-            lv[e] = x - hv[e];
-        }
-        *reinterpret_cast<uint4*>(base + o) = pack8_bf16(hv);
-        *reinterpret_cast<uint4*>(base + o + lo_off) = pack8_bf16(lv);
-    };
-    {
-        // every load of the four rows a thread converts is issued before the first store (the stores
-        // could alias the loads as far as the compiler knows, which would otherwise serialise them)
-        float kd[4][8], w[4][8];
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int i = tid + 256 * it, t = i >> 4, c8 = (i & 15) * 8;
-            *reinterpret_cast<float4*>(kd[it]) = *reinterpret_cast<const float4*>(rec + L.Kd + t * K + c8);
-            *reinterpret_cast<float4*>(kd[it] + 4) = *reinterpret_cast<const float4*>(rec + L.Kd + t * K + c8 + 4);
-            *reinterpret_cast<float4*>(w[it]) = *reinterpret_cast<const float4*>(rec + L.W + t * K + c8);
-            *reinterpret_cast<float4*>(w[it] + 4) = *reinterpret_cast<const float4*>(rec + L.W + t * K + c8 + 4);
-        }
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int i = tid + 256 * it, t = i >> 4, c8 = (i & 15) * 8;
-            const uint32_t o = km_bf16(t, c8, 2048, 128);
-            put_split8(out, chainrec::KD + o, chainrec::KD_LO - chainrec::KD, kd[it], 1.f);
-            put_split8(out, chainrec::WN + o, chainrec::WN_LO - chainrec::WN, w[it], -1.f);
-        }
-    }
-    static_assert(64 * 128 / 8 == 4 * 256, "four rows of eight channels per thread");
-    if (tid < K) reinterpret_cast<float*>(out + chainrec::GC)[tid] = rec[L.gC + tid];
     cp_async_wait_all();
     __syncthreads();
     // Y = scale Aqk^T dO (64 x 128): warp w owns rows 16 (w / 2) and columns 64 (w % 2) .. + 64.

@@ -16,12 +16,14 @@ struct RecLayout {
     __host__ __device__ static RecLayout make(int K, int V) {
         RecLayout r;
         size_t o = 0;
+        // W, Kd and gC first and adjacent: in the tensor-core record (K = V = 128) their 66048 bytes hold
+        // the backward chains' operand slot instead (chainrec: Kd and -W as bf16 hi / lo, then gC)
         r.W = o; o += 64 * (size_t)K;
-        r.Qg = o; o += 64 * (size_t)K;
         r.Kd = o; o += 64 * (size_t)K;
+        r.gC = o; o += (size_t)K;
+        r.Qg = o; o += 64 * (size_t)K;
         r.U0 = o; o += 64 * (size_t)V;
         r.A = o; o += 64 * 64;
-        r.gC = o; o += (size_t)K;
         r.fwd_size = (o + 63) / 64 * 64;
         r.Kg = o; o += 64 * (size_t)K;
         r.N = o; o += 64 * 64;
@@ -100,9 +102,10 @@ __host__ __device__ constexpr uint32_t u0_off(int t, int j) {
 //   forward state recompute (Z = S entering chunk c):  A1 = -W,  A2 = Kd^T,  Y = U0, no P;
 //   reverse chain (Z = dS leaving chunk c):            A1 = Kd,  A2 = -W^T,  Y = scale Aqk^T dO,
 //                                                      P = scale Qg^T dO.
-// One slot serves both: Kd and -W are stored once as [64 t][128 c] bf16 K-major tiles
-// (km_bf16(t, c, 2048, 128)); read with swapped strides the same bytes are the MN-major layout of
-// Kd^T and -W^T (M = c, K = t).  The first SLOT bytes move into shared memory by one bulk copy:
+// One slot serves both: Kd and -W are stored once as [128 c][64 t] bf16 K-major tiles
+// (km_bf16(c, t, 1024, 128)), the layout in which the intra pass produces them (a thread per channel);
+// read with swapped strides the same bytes are the MN-major layout of Kd and -W (M = t, K = c).  The
+// slot leads each chunk's tensor-core record and moves into shared memory by one bulk copy:
 namespace chainrec {
 constexpr uint32_t KD = 0;           // Kd  hi
 constexpr uint32_t KD_LO = 16384;    // Kd  lo
@@ -113,7 +116,7 @@ constexpr uint32_t SLOT = 66048;
 }  // namespace chainrec
 
 namespace bwrec {
-constexpr uint32_t Y = chainrec::SLOT;          // fp32 [64 t][128 j] in x4 order: scale Aqk^T dO
+constexpr uint32_t Y = 0;                       // fp32 [64 t][128 j] in x4 order: scale Aqk^T dO
 constexpr uint32_t P = Y + 32768;               // fp32 [128 c][128 j] in x4 order: scale Qg^T dO
 constexpr uint32_t BYTES = P + 65536;           // record stride (256-byte multiple)
 }  // namespace bwrec

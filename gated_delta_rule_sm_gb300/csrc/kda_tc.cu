@@ -97,6 +97,21 @@ __device__ __forceinline__ void mma16_split(float (&acc)[2][4], const float* a, 
 // forward that keeps the backward record, so the backward skips this pass).
 // GATE_RT: the gate is read from Params at run time (either activation); otherwise the lower-bounded gate
 // is compiled in and the unbounded gate's diagonal-block steps are left out.
+// Eight consecutive t of one channel c of a chain-slot tile (chainrec: [128 c][64 t] bf16 K-major, hi,
+// then lo `lo_off` bytes later), times sg: hi = bf16(x), lo = bf16(x - hi), the split the backward
+// chains' products take.  One 16-byte store each.
+__device__ __forceinline__ void put_slot_split8(uint8_t* slot, uint32_t off, uint32_t lo_off, const float* v, float sg) {
+    float hv[8], lv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float x = sg * v[e];
+        hv[e] = __bfloat162float(__float2bfloat16_rn(x));
+        lv[e] = x - hv[e];
+    }
+    *reinterpret_cast<uint4*>(slot + off) = pack8_bf16(hv);
+    *reinterpret_cast<uint4*>(slot + off + lo_off) = pack8_bf16(lv);
+}
+
 template <int MODE, bool GATE_RT>
 __global__ void __launch_bounds__(256, 1)
     intra_tc_kernel(Params p, uint8_t* recs, const __grid_constant__ CUtensorMap tm_q,
@@ -186,6 +201,8 @@ __global__ void __launch_bounds__(256, 1)
     int h, c, tok0;
     const int len = item_tok0(item, h, c, tok0);
     float* frec = BWD ? p.rec + ((size_t)c * H + h) * p.rec_stride : nullptr;
+    // the backward chains' operand slot, in place of the fp32 W and Kd fields (W, Kd, gC lead the record)
+    uint8_t* slot = BWD ? reinterpret_cast<uint8_t*>(frec + RL.W) : nullptr;
     uint8_t* rec = FWDREC ? recs + ((size_t)c * H + h) * tcrec::BYTES : nullptr;
     if (tid < 128) sdtb[tid] = nx_dtb;
     if (tid < 64) sbeta[tid] = tid < len ? sigmoidf_acc(nx_braw) : 0.f;
@@ -326,6 +343,7 @@ __global__ void __launch_bounds__(256, 1)
                 float gpre = 0.f;
                 for (int m = 0; m < bi; ++m) gpre += sgsum[m * 128 + cc];
                 if (bi == 0) frec[RL.gC + cc] = B0 * B1 * B2 * B3;
+                float kdv[16];
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int t = t0 + u;
@@ -333,11 +351,13 @@ __global__ void __launch_bounds__(256, 1)
                     const float qh = bf16_at(smem + RAW_Q, t * 256 + cc * 2) * rq[t];
                     frec[RL.Kg + t * 128 + cc] = kx[ci][u] * eG;
                     frec[RL.Qg + t * 128 + cc] = qx[ci][u] * eG;
-                    frec[RL.Kd + t * 128 + cc] = kh * y[ci][u] * tail;
+                    kdv[u] = kh * y[ci][u] * tail;
                     frec[RL.G + t * 128 + cc] = gpre + lg[BWD ? ci : 0][u];
                     frec[RL.qh + t * 128 + cc] = qh;
                     frec[RL.kh + t * 128 + cc] = kh;
                 }
+                put_slot_split8(slot, chainrec::KD + km_bf16(cc, t0, 1024, 128), chainrec::KD_LO - chainrec::KD, kdv, 1.f);
+                put_slot_split8(slot, chainrec::KD + km_bf16(cc, t0 + 8, 1024, 128), chainrec::KD_LO - chainrec::KD, kdv + 8, 1.f);
             }
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -692,7 +712,8 @@ __global__ void __launch_bounds__(256, 1)
                         *reinterpret_cast<uint4*>(rec + tcrec::WQ + mn_bf16(tb, cc, 128, 2048)) = pack8_f16(d + tb);
                 if (BWD)
 #pragma unroll
-                    for (int t = 0; t < 64; ++t) frec[RL.W + t * 128 + cc] = d[t];
+                    for (int tb = 0; tb < 64; tb += 8)   // -W, as the chains take it
+                        put_slot_split8(slot, chainrec::WN + km_bf16(cc, tb, 1024, 128), chainrec::WN_LO - chainrec::WN, d + tb, -1.f);
             } else {
                 const int j = tid - 128;
                 uint8_t* dst = FWDREC ? rec + tcrec::U0 + (j >> 5) * tcrec::U0_SLICE : nullptr;
