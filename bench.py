@@ -81,9 +81,9 @@ def kernel_work(name: str, w, units: float) -> tuple[float, float]:
 # the figure scales with the token-heads of a launch.  An entry is removed when its kernel changes and
 # has not been captured again.
 PROFILED_TRAFFIC = {
-    ("kda_grad_tc", True): 8387.0,
+    ("kda_grad_tc", True): 8353.0,
     ("kda_intra_tc", False): 2222.0,   # forward record only (forward-only workloads; intra2_kernel)
-    ("kda_intra_tc", True): 6854.0,    # forward that keeps the backward record, once per training step
+    ("kda_intra_tc", True): 6859.0,    # forward that keeps the backward record, once per training step
 }
 
 
