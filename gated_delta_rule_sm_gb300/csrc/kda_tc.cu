@@ -11,8 +11,8 @@
 // The intra-chunk kernels write one record per (chunk, head) in exactly the shared-memory layout the
 // chain kernel's MMAs read, so the chain's load warp moves it with three bulk copies per chunk.  The
 // chain's blocks take segments longest first (seg_order), the saving intra pass here also writes
-// the fp32 backward record, and the segment-parallel schedule's piece table and state combine close
-// the file.
+// the backward record (led by the backward chains' split-bf16 Kd / -W slot, then fp32 fields), and the
+// segment-parallel schedule's piece table and state combine close the file.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
